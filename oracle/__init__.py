@@ -1,0 +1,270 @@
+"""CPU oracle for the W4A4 NVFP4 quantised projection -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product library never does, and this
+package never imports the product library.  The arithmetic is in ``oracle.c``
+(plain C, fp64 accumulation, fixed-order fp32 transforms); this file only
+compiles it with gcc and marshals numpy arrays through ctypes.
+
+Every function states the passage it follows in ``oracle.c``'s header.
+Parity pins live in ``tests/test_oracle_pins.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from dataclasses import dataclass
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+CFLAGS = ["-O2", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fno-fast-math",
+          "-fPIC", "-shared"]
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so (gcc, no FMA contraction, no fast-math)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", *CFLAGS, _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            L = ctypes.CDLL(_LIB)
+            P = ctypes.c_void_p
+            i64, i32, f32 = ctypes.c_long, ctypes.c_int, ctypes.c_float
+            L.orc_e2m1_encode.argtypes = [f32]; L.orc_e2m1_encode.restype = ctypes.c_uint8
+            L.orc_e2m1_decode.argtypes = [ctypes.c_uint8]; L.orc_e2m1_decode.restype = ctypes.c_double
+            L.orc_e4m3_encode.argtypes = [f32]; L.orc_e4m3_encode.restype = ctypes.c_uint8
+            L.orc_e4m3_decode.argtypes = [ctypes.c_uint8]; L.orc_e4m3_decode.restype = ctypes.c_double
+            L.orc_bf16_from_f64.argtypes = [ctypes.c_double]; L.orc_bf16_from_f64.restype = ctypes.c_uint16
+            L.orc_fwht64_f32.argtypes = [P]; L.orc_fwht64_f32.restype = None
+            L.orc_fwht64_f64.argtypes = [P, i64]; L.orc_fwht64_f64.restype = None
+            L.orc_nvfp4_quantize.argtypes = [P, i64, f32, P, P]; L.orc_nvfp4_quantize.restype = None
+            L.orc_quantize_act.argtypes = [P, i64, i64, P, i32, P, i32, i32, P, P, P, P, P, i32]
+            L.orc_quantize_act.restype = i32
+            L.orc_fold_weights.argtypes = [P, i64, i64, P, P, P, i32, P, i32, i32, P, P, P, P, P, i32]
+            L.orc_fold_weights.restype = i32
+            L.orc_quantize_weights.argtypes = [P, i64, i64, P, P, P]; L.orc_quantize_weights.restype = i32
+            L.orc_lowrank_act.argtypes = [P, i64, i64, P, i32, P]; L.orc_lowrank_act.restype = None
+            L.orc_linear_forward.argtypes = [P, P, P, i32, i64, P, P, f32, i64, i64, P, P, i32,
+                                             P, P, i32, P, P, i32]
+            L.orc_linear_forward.restype = i32
+            L.orc_forward_noquant.argtypes = [P, P, i64, i64, i64, P, P, i32, P, P, P, i32, P, P]
+            L.orc_forward_noquant.restype = i32
+            _lib = L
+    return _lib
+
+
+def _p(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return None if a is None else np.ascontiguousarray(a, dtype=dtype)
+
+
+# ------------------------------------------------------------------ scalar formats
+def e2m1_encode(v: float) -> int:
+    return int(lib().orc_e2m1_encode(float(v)))
+
+
+def e2m1_decode(c: int) -> float:
+    return float(lib().orc_e2m1_decode(int(c)))
+
+
+def e4m3_encode(v: float) -> int:
+    return int(lib().orc_e4m3_encode(float(v)))
+
+
+def e4m3_decode(c: int) -> float:
+    return float(lib().orc_e4m3_decode(int(c)))
+
+
+def fwht64_f32(v: np.ndarray) -> np.ndarray:
+    """FoldQuantVLA Key Contribution 2: block Hadamard by FWHT, beta = 64 (fp32)."""
+    out = np.array(v, dtype=np.float32, copy=True)
+    assert out.shape == (64,)
+    lib().orc_fwht64_f32(_p(out))
+    return out
+
+
+def fwht64_f64(v: np.ndarray) -> np.ndarray:
+    out = np.array(v, dtype=np.float64, copy=True)
+    assert out.shape == (64,)
+    lib().orc_fwht64_f64(_p(out), 1)
+    return out
+
+
+def nvfp4_quantize(v: np.ndarray, g: float):
+    """NVFP4 two-level quantisation of a vector with a given fp32 tensor scale g."""
+    v = _c(v, np.float32)
+    n = v.size
+    codes = np.zeros(n // 2, np.uint8)
+    scales = np.zeros(n // 16, np.uint8)
+    lib().orc_nvfp4_quantize(_p(v), n, np.float32(g), _p(codes), _p(scales))
+    return codes, scales
+
+
+def inv_smoothing(s: Optional[np.ndarray]) -> Optional[np.ndarray]:
+    """inv_s = 1/s, one IEEE fp32 division per channel."""
+    if s is None:
+        return None
+    s = np.asarray(s, np.float32)
+    return (np.float32(1.0) / s).astype(np.float32)
+
+
+# ------------------------------------------------------------------ activations
+@dataclass
+class ActQuant:
+    codes: np.ndarray        # uint8 [M, K/2], element 2i in the low nibble
+    scales: np.ndarray       # uint8 [M, K/16] (e4m3)
+    g: np.ndarray            # fp32 [M] (per row) or [1] (per tensor)
+    x_omega: np.ndarray      # fp16 bits [M, n_omega]
+    xt: Optional[np.ndarray] = None   # fp32 [M, K] transformed rows, outliers zeroed
+
+
+def quantize_act(x_bits: np.ndarray, s: Optional[np.ndarray], rotate: bool,
+                 omega: Optional[np.ndarray] = None, per_tensor: bool = False,
+                 keep_xt: bool = False, n_threads: int = 0) -> ActQuant:
+    """Smoothing -> block FWHT -> outlier split -> NVFP4 (FoldQuantVLA contribution 2;
+    QuantWAMs sec. 3.1 Eq. (1))."""
+    x_bits = _c(x_bits, np.uint16)
+    M, K = x_bits.shape
+    inv_s = inv_smoothing(s)
+    omega = np.zeros(0, np.int32) if omega is None else _c(omega, np.int32)
+    no = int(omega.size)
+    codes = np.zeros((M, K // 2), np.uint8)
+    scales = np.zeros((M, K // 16), np.uint8)
+    g = np.zeros(1 if per_tensor else M, np.float32)
+    xo = np.zeros((M, no), np.uint16)
+    xt = np.zeros((M, K), np.float32) if keep_xt else None
+    rc = lib().orc_quantize_act(_p(x_bits), M, K, _p(inv_s), int(rotate), _p(omega), no,
+                                int(per_tensor), _p(codes), _p(scales), _p(g), _p(xo), _p(xt),
+                                int(n_threads))
+    if rc:
+        raise ValueError(f"orc_quantize_act failed: {rc}")
+    return ActQuant(codes, scales, g, xo, xt)
+
+
+# ------------------------------------------------------------------ weights
+@dataclass
+class WeightQuant:
+    codes: np.ndarray        # uint8 [N, K/2]
+    scales: np.ndarray       # uint8 [N, K/16]
+    gW: float
+    W_omega: np.ndarray      # fp16 bits [n_omega, N]
+    P: np.ndarray            # bf16 bits [K, r]
+    Q: np.ndarray            # bf16 bits [r, N]
+    Rp: np.ndarray           # fp32 [K, N] folded weight (outlier rows zeroed)
+    W_omega_f32: np.ndarray  # fp32 [n_omega, N]
+
+
+def prepare_weights(W: np.ndarray, s: Optional[np.ndarray], L1: Optional[np.ndarray],
+                    L2: Optional[np.ndarray], omega: Optional[np.ndarray], rotate: bool,
+                    n_threads: int = 0) -> WeightQuant:
+    """Consistent folding (FoldQuantVLA Prop. 1) of smoothing + rotation into W, the
+    16-bit low-rank complement (Q-WAM ASP), the fp16 outlier rows (QuantWAMs sec. 3.1),
+    then per-tensor NVFP4 of the folded weight."""
+    W = _c(W, np.float32)
+    K, N = W.shape
+    r = 0 if L1 is None else L1.shape[1]
+    s = _c(s, np.float32)
+    L1 = _c(L1, np.float32)
+    L2 = _c(L2, np.float32)
+    omega = np.zeros(0, np.int32) if omega is None else _c(omega, np.int32)
+    no = int(omega.size)
+    Rp = np.zeros((K, N), np.float32)
+    Wo = np.zeros((no, N), np.uint16)
+    Wo32 = np.zeros((no, N), np.float32)
+    P = np.zeros((K, r), np.uint16)
+    Q = np.zeros((r, N), np.uint16)
+    rc = lib().orc_fold_weights(_p(W), K, N, _p(s), _p(L1), _p(L2), r, _p(omega), no,
+                                int(rotate), _p(Rp), _p(Wo), _p(Wo32), _p(P), _p(Q), int(n_threads))
+    if rc:
+        raise ValueError(f"orc_fold_weights failed: {rc}")
+    codes = np.zeros((N, K // 2), np.uint8)
+    scales = np.zeros((N, K // 16), np.uint8)
+    gW = np.zeros(1, np.float32)
+    rc = lib().orc_quantize_weights(_p(Rp), K, N, _p(codes), _p(scales), _p(gW))
+    if rc:
+        raise ValueError(f"orc_quantize_weights failed: {rc}")
+    return WeightQuant(codes, scales, float(gW[0]), Wo, P, Q, Rp, Wo32)
+
+
+def lowrank_act(x_bits: np.ndarray, P: np.ndarray) -> np.ndarray:
+    """U = bf16(x P), the 16-bit low-rank down-projection (Q-WAM ASP)."""
+    x_bits = _c(x_bits, np.uint16)
+    P = _c(P, np.uint16)
+    M, K = x_bits.shape
+    r = P.shape[1]
+    U = np.zeros((M, r), np.uint16)
+    if r:
+        lib().orc_lowrank_act(_p(x_bits), M, K, _p(P), r, _p(U))
+    return U
+
+
+def linear_forward(aq: ActQuant, wq: WeightQuant, U: Optional[np.ndarray],
+                   bias: Optional[np.ndarray], per_tensor_act: bool = False,
+                   n_threads: int = 0) -> np.ndarray:
+    """y = gA gW (A4 . W4) + U Q + x_omega W_omega + b, accumulated in fp64."""
+    M, K2 = aq.codes.shape
+    K = 2 * K2
+    N = wq.codes.shape[0]
+    r = wq.P.shape[1]
+    no = wq.W_omega.shape[0]
+    y = np.zeros((M, N), np.float64)
+    U = np.zeros((M, 0), np.uint16) if U is None else _c(U, np.uint16)
+    bias = _c(bias, np.float32)
+    rc = lib().orc_linear_forward(_p(aq.codes), _p(aq.scales), _p(aq.g), int(per_tensor_act), M,
+                                  _p(wq.codes), _p(wq.scales), np.float32(wq.gW), N, K,
+                                  _p(U), _p(wq.Q), r, _p(aq.x_omega), _p(wq.W_omega), no,
+                                  _p(bias), _p(y), int(n_threads))
+    if rc:
+        raise ValueError(f"orc_linear_forward failed: {rc}")
+    return y
+
+
+def forward_noquant(x_bits, s, rotate, omega, wq: WeightQuant, bias) -> np.ndarray:
+    """The folded pipeline with quantisation disabled (FoldQuantVLA Proposition 1)."""
+    x_bits = _c(x_bits, np.uint16)
+    M, K = x_bits.shape
+    N = wq.codes.shape[0]
+    r = wq.P.shape[1]
+    omega = np.zeros(0, np.int32) if omega is None else _c(omega, np.int32)
+    no = omega.size
+    aq = quantize_act(x_bits, s, rotate, omega, keep_xt=True)
+    # unrounded transformed outlier values: recompute the rows without the split
+    full = quantize_act(x_bits, s, rotate, None, keep_xt=True).xt
+    xo = np.ascontiguousarray(full[:, omega]) if no else np.zeros((M, 0), np.float32)
+    y = np.zeros((M, N), np.float64)
+    bias = _c(bias, np.float32)
+    lib().orc_forward_noquant(_p(aq.xt), _p(xo), M, K, N, _p(wq.Rp), _p(wq.W_omega_f32), no,
+                              _p(x_bits), _p(wq.P), _p(wq.Q), r, _p(bias), _p(y))
+    return y
+
+
+def reference_forward(layer, n_threads: int = 0, rows: Optional[np.ndarray] = None):
+    """Full oracle pass for one ``workloads`` layer: returns (y fp64, ActQuant, WeightQuant, U).
+    ``rows`` restricts the activation side to a subset of rows (sampled parity)."""
+    x_bits = layer.x_bits if rows is None else layer.x_bits[rows]
+    rotate = layer.rotate
+    wq = prepare_weights(layer.W, layer.s, layer.L1, layer.L2, layer.omega, rotate, n_threads)
+    aq = quantize_act(x_bits, layer.s, rotate, layer.omega, n_threads=n_threads)
+    U = lowrank_act(x_bits, wq.P) if wq.P.shape[1] else None
+    y = linear_forward(aq, wq, U, layer.bias, n_threads=n_threads)
+    return y, aq, wq, U

@@ -1,0 +1,296 @@
+"""Pins of the CPU oracle to facts that do not come from the oracle itself.
+
+Each test checks one oracle function against mathematics the pages (or the NVFP4
+format definition they name) fix: a dense matrix definition, a closed form, an
+invariant, an exhaustive independent restatement, or a library routine.
+"""
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+import pytest
+import torch
+from scipy.linalg import hadamard
+
+import oracle
+import workloads as wlmod
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def _golden_formats():
+    tab = {"e2m1": {}, "e4m3": {}}
+    with open(os.path.join(HERE, "golden", "nvfp4_formats.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            fmt, code, val = line.split()
+            tab[fmt][int(code)] = float(val)
+    return tab
+
+
+GOLD = _golden_formats()
+
+
+# ------------------------------------------------------------------ FWHT
+# FoldQuantVLA, Key Contribution 2: block Hadamard rotation applied via the FWHT, beta = 64.
+def test_fwht_equals_dense_sylvester_matrix():
+    H = hadamard(64).astype(np.float64) / 8.0
+    rng = np.random.default_rng(11)
+    for _ in range(20):
+        v = rng.standard_normal(64).astype(np.float32)
+        got = oracle.fwht64_f32(v).astype(np.float64)
+        ref = H @ v.astype(np.float64)
+        assert np.max(np.abs(got - ref)) <= 1e-6 * np.max(np.abs(ref))
+        got64 = oracle.fwht64_f64(v.astype(np.float64))
+        assert np.max(np.abs(got64 - ref)) <= 1e-13 * np.max(np.abs(ref))
+
+
+def test_fwht_basis_vectors_give_hadamard_rows_exactly():
+    H = hadamard(64).astype(np.float32) / np.float32(8.0)
+    for i in range(64):
+        e = np.zeros(64, np.float32)
+        e[i] = 1.0
+        assert np.array_equal(oracle.fwht64_f32(e), H[:, i])
+
+
+def test_fwht_self_inverse_and_orthonormal():
+    rng = np.random.default_rng(12)
+    for _ in range(50):
+        v = (rng.standard_normal(64) * 10 ** rng.uniform(-3, 3)).astype(np.float32)
+        w = oracle.fwht64_f32(v)
+        np.testing.assert_allclose(np.linalg.norm(w.astype(np.float64)),
+                                   np.linalg.norm(v.astype(np.float64)), rtol=1e-6)
+        back = oracle.fwht64_f32(w)
+        ulp = np.spacing(np.max(np.abs(v)))
+        assert np.max(np.abs(back - v)) <= 4 * ulp
+
+
+# ------------------------------------------------------------------ formats
+def test_e2m1_grid_literal():
+    for code, val in GOLD["e2m1"].items():
+        d = oracle.e2m1_decode(code)
+        assert d == val and np.signbit(d) == np.signbit(val), (code, d, val)
+        assert oracle.e2m1_encode(val) == code
+
+
+def test_e4m3_points_literal():
+    for code, val in GOLD["e4m3"].items():
+        assert oracle.e4m3_decode(code) == val
+        assert oracle.e4m3_encode(val) == code
+
+
+def test_e2m1_ties_round_to_even_code():
+    # midpoints of the grid -> the neighbour with the even magnitude code
+    cases = {0.25: 0, 0.75: 2, 1.25: 2, 1.75: 4, 2.5: 4, 3.5: 6, 5.0: 6, 6.0: 7, 7.0: 7, 1e30: 7,
+             -0.1: 8, -0.25: 8, -0.75: 10, -5.0: 14, -100.0: 15}
+    for v, c in cases.items():
+        assert oracle.e2m1_encode(v) == c, (v, oracle.e2m1_encode(v), c)
+
+
+@pytest.fixture(scope="module")
+def pinlib():
+    src = os.path.join(HERE, "pins", "rounding_pin.c")
+    out = os.path.join(HERE, "pins", "librounding_pin.so")
+    if not os.path.exists(out) or os.path.getmtime(out) < os.path.getmtime(src):
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared",
+                               src, "-o", out, "-lm"])
+    L = ctypes.CDLL(out)
+    L.pin_e2m1_all.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32)]
+    L.pin_e2m1_all.restype = ctypes.c_long
+    L.pin_e4m3_all.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32)]
+    L.pin_e4m3_all.restype = ctypes.c_long
+    return L
+
+
+def test_e2m1_encoder_exhaustive_against_ieee_rounding(pinlib):
+    first = ctypes.c_uint32(0)
+    fn = ctypes.cast(oracle.lib().orc_e2m1_encode, ctypes.c_void_p)
+    bad = pinlib.pin_e2m1_all(fn, ctypes.byref(first))
+    assert bad == 0, f"{bad} mismatches, first fp32 bits {first.value:#010x}"
+
+
+def test_e4m3_encoder_exhaustive_against_ieee_rounding(pinlib):
+    first = ctypes.c_uint32(0)
+    fn = ctypes.cast(oracle.lib().orc_e4m3_encode, ctypes.c_void_p)
+    bad = pinlib.pin_e4m3_all(fn, ctypes.byref(first))
+    assert bad == 0, f"{bad} mismatches, first fp32 bits {first.value:#010x}"
+
+
+def test_e4m3_encoder_matches_torch_float8_in_range():
+    # torch's fp32 -> float8_e4m3fn is round-to-nearest-even; compare where it is finite
+    rng = np.random.default_rng(5)
+    v = np.concatenate([rng.uniform(0, 448, 200000), 2.0 ** rng.uniform(-12, 8.8, 200000)]).astype(np.float32)
+    v = v[v <= 448]
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_encode(float(a)) for a in v[:40000]], np.uint8)
+    assert np.array_equal(got, ref[:40000])
+
+
+def test_bf16_from_f64_matches_torch_on_fp32_values():
+    rng = np.random.default_rng(6)
+    v = (rng.standard_normal(20000) * 10 ** rng.uniform(-30, 30, 20000)).astype(np.float32)
+    ref = torch.from_numpy(v).to(torch.bfloat16).view(torch.uint16).numpy()
+    L = oracle.lib()
+    got = np.array([L.orc_bf16_from_f64(float(a)) for a in v], np.uint16)
+    assert np.array_equal(got, ref)
+
+
+# ------------------------------------------------------------------ the quantiser
+def _dec_table():
+    e2 = np.array([GOLD["e2m1"][c] for c in range(16)], np.float64)
+    return e2
+
+
+def _dequant(codes, scales, K):
+    """Test-side dequantisation from the golden grid (independent of the oracle)."""
+    e2 = _dec_table()
+    lo = codes & 15
+    hi = codes >> 4
+    el = np.empty(codes.shape[:-1] + (K,), np.float64)
+    el[..., 0::2] = e2[lo]
+    el[..., 1::2] = e2[hi]
+    sc = np.array([oracle.e4m3_decode(c) for c in range(256)], np.float64)
+    return el * np.repeat(sc[scales], 16, axis=-1)
+
+
+def test_representable_blocks_round_trip_exactly():
+    """A block built from representable code x scale values (with g = 1) quantises
+    back to exactly those codes and that scale."""
+    rng = np.random.default_rng(7)
+    e2 = _dec_table()
+    for sc in [1, 8, 9, 40, 56, 57, 90, 119, 125]:
+        dsc = oracle.e4m3_decode(sc)
+        for _ in range(20):
+            codes = rng.integers(0, 16, 16)
+            codes[rng.integers(0, 16)] = 7 | (8 * rng.integers(0, 2))   # block max = 6 * scale
+            v = (e2[codes] * dsc).astype(np.float32)
+            c, s = oracle.nvfp4_quantize(v, 1.0)
+            assert s[0] == sc
+            got = np.empty(16, np.int64)
+            got[0::2] = c & 15
+            got[1::2] = c >> 4
+            want = codes.copy()
+            want[(e2[codes] == 0)] = want[(e2[codes] == 0)] & 8       # +-0 keep their sign
+            assert np.array_equal(got, want), (sc, got, want)
+
+
+def test_constant_row_closed_form():
+    """A row of equal values c: after the block FWHT only element 0 of each 64-block
+    is non-zero (= 8c); it takes the largest code and scale, all others are zero."""
+    for c in [0.5, 1.0, -3.0, 1.5]:
+        K = 256
+        x = np.full((1, K), c, np.float32)
+        aq = oracle.quantize_act(wlmod.bf16_bits(x), None, True)
+        deq = _dequant(aq.codes, aq.scales, K)[0]
+        # element 0 of each block: code +-6 with scale 448 (largest e4m3)
+        assert np.array_equal(deq[0::64], np.full(K // 64, np.copysign(6.0 * 448.0, c)))
+        assert not np.delete(deq, np.arange(0, K, 64)).any()
+        # g = fp32(8|c| / 2688), so the dequantised value is 8c to within one fp32 rounding
+        val = deq[0] * np.float64(aq.g[0])
+        assert abs(val - 8 * c) <= 2.0 ** -24 * 8 * abs(c)
+
+
+def test_zero_row_gives_zero_scale_and_codes():
+    x = np.zeros((2, 128), np.uint16)
+    aq = oracle.quantize_act(x, None, True)
+    assert aq.g.tolist() == [0.0, 0.0]
+    assert not aq.codes.any() and not aq.scales.any()
+
+
+def test_quantiser_brute_force_tiny():
+    """Brute force on one 16-block: every code is the nearest point of the scaled grid
+    (tie -> even code), and the scale is the nearest e4m3 to bmax/6/g."""
+    rng = np.random.default_rng(8)
+    e2 = _dec_table()[:8]
+    for _ in range(300):
+        v = (rng.standard_normal(16) * 10 ** rng.uniform(-2, 2)).astype(np.float32)
+        g = np.float32(10 ** rng.uniform(-3, 0))
+        c, s = oracle.nvfp4_quantize(v, g)
+        t = np.float32(np.float32(np.max(np.abs(v))) / np.float32(6.0)) / g
+        sv = np.array([oracle.e4m3_decode(k) for k in range(127)])
+        dist = np.abs(sv - np.float64(np.float32(t)))
+        best = np.flatnonzero(dist == dist.min())
+        exp_sc = 126 if t >= 448 else (best[0] if len(best) == 1 else best[best % 2 == 0][0])
+        assert s[0] == exp_sc
+        d = np.float32(np.float32(sv[exp_sc]) * g)
+        for i in range(16):
+            code = (c[i // 2] >> (4 * (i % 2))) & 15
+            if d == 0:
+                assert code == 0
+                continue
+            q = np.float64(np.float32(v[i] / d))
+            a = min(abs(q), 6.0)
+            dd = np.abs(e2 - a)
+            cand = np.flatnonzero(dd == dd.min())
+            mag = cand[0] if len(cand) == 1 else cand[cand % 2 == 0][0]
+            assert code == (mag | (8 if np.signbit(q) else 0)), (v[i], d, code, mag)
+
+
+# ------------------------------------------------------------------ Proposition 1
+@pytest.mark.parametrize("r,n_om", [(0, 0), (16, 0), (0, 16), (16, 16)])
+def test_folding_invariance_prop1(r, n_om):
+    """FoldQuantVLA Proposition 1: with quantisation disabled, the folded graph
+    (x diag(s)^-1 H)(H^T diag(s) W) (+ low-rank + outlier branches) computes x W + b."""
+    L = wlmod.make_layer_inputs("tiny", M=8, K=256, N=96, rank=r, n_omega=n_om)
+    wq = oracle.prepare_weights(L.W, L.s, L.L1, L.L2, L.omega, True)
+    y = oracle.forward_noquant(L.x_bits, L.s, True, L.omega, wq, L.bias)
+    ref = L.x_f32.astype(np.float64) @ L.W.astype(np.float64)
+    if L.bias is not None:
+        ref += L.bias
+    rel = np.max(np.abs(y - ref)) / np.max(np.abs(ref))
+    assert rel <= 1e-5, rel
+
+
+def test_folding_invariance_detects_unfolded_rotation():
+    """Sanity of the pin itself: rotating only one side breaks the identity."""
+    L = wlmod.make_layer_inputs("tiny", M=8, K=256, N=96, rank=0, n_omega=0)
+    wq = oracle.prepare_weights(L.W, L.s, None, None, None, False)       # weight not rotated
+    y = oracle.forward_noquant(L.x_bits, L.s, True, None, wq, None)      # activation rotated
+    ref = L.x_f32.astype(np.float64) @ L.W.astype(np.float64)
+    assert np.max(np.abs(y - ref)) / np.max(np.abs(ref)) > 1e-2
+
+
+# ------------------------------------------------------------------ reduction to a matmul
+def test_plain_case_reduces_to_dequantised_matmul():
+    """s = 1, no rotation, r = 0, Omega empty: the oracle forward equals
+    (deq(A) gA) @ (deq(W) gW)^T + b computed by numpy from the codes."""
+    L = wlmod.make_layer_inputs("expert", M=12, K=256, N=80, rank=0, n_omega=0, smooth=False,
+                                rotate=False)
+    y, aq, wq, _ = oracle.reference_forward(L)
+    A = _dequant(aq.codes, aq.scales, 256) * aq.g.astype(np.float64)[:, None]
+    B = _dequant(wq.codes, wq.scales, 256) * np.float64(wq.gW)
+    ref = A @ B.T + L.bias.astype(np.float64)
+    np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-12 * np.max(np.abs(ref)))
+
+
+def test_lowrank_and_outlier_terms_enter_with_the_right_sign():
+    """y(with branches) - y(main only) equals U Q + x_Omega W_Omega computed by numpy."""
+    L = wlmod.make_layer_inputs("video_dit", M=16, K=256, N=64, rank=16, n_omega=16)
+    y, aq, wq, U = oracle.reference_forward(L)
+    y0 = oracle.linear_forward(aq, oracle.WeightQuant(wq.codes, wq.scales, wq.gW,
+                                                      np.zeros((0, 64), np.uint16),
+                                                      np.zeros((256, 0), np.uint16),
+                                                      np.zeros((0, 64), np.uint16), wq.Rp,
+                                                      wq.W_omega_f32[:0]),
+                               None, None)
+    side = (wlmod.bf16_from_bits(U).astype(np.float64) @ wlmod.bf16_from_bits(wq.Q).astype(np.float64)
+            + aq.x_omega.view(np.float16).astype(np.float64) @ wq.W_omega.view(np.float16).astype(np.float64)
+            + L.bias.astype(np.float64))
+    np.testing.assert_allclose(y - y0, side, rtol=1e-9, atol=1e-9 * np.max(np.abs(side)))
+
+
+# ------------------------------------------------------------------ error sanity (monotone)
+def test_branches_reduce_quantisation_error_on_outlier_heavy_input():
+    """QuantWAMs Fig. 1 / Q-WAM: keeping outlier channels in 16-bit and adding a 16-bit
+    low-rank branch lowers the W4A4 error against the unquantised product."""
+    errs = []
+    for r, n_om in [(0, 0), (0, 32), (32, 32)]:
+        L = wlmod.make_layer_inputs("video_dit", M=64, K=512, N=256, rank=r, n_omega=n_om)
+        y, *_ = oracle.reference_forward(L)
+        ref = L.x_f32.astype(np.float64) @ L.W.astype(np.float64) + L.bias
+        errs.append(np.linalg.norm(y - ref) / np.linalg.norm(ref))
+    assert errs[0] > errs[1] > errs[2], errs
+    assert errs[2] < 0.2
