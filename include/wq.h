@@ -1,0 +1,170 @@
+/*
+ * wq.h -- C ABI of libwq, the W4A4 NVFP4 quantised projection for NVIDIA B300
+ * (sm_103a).
+ *
+ * The operation (citations are page title + section):
+ *   y = x W + b  computed as
+ *   y = gA gW (Q4(xt_~O) . Q4(R'_~O)) + U Q + x_O W_O + b
+ * where
+ *   xt  = (x * inv_s) H             per-channel smoothing, then block-64 Walsh-Hadamard
+ *                                   rotation (FoldQuantVLA, Key Contribution 2; QuantWAMs
+ *                                   sec. 3.1 Eq. (1), Fig. 1(b));
+ *   R'  = H diag(s) (W - P Q)       the inverse transform folded into the weight
+ *                                   (FoldQuantVLA, Key Contribution 1, Proposition 1;
+ *                                   QuantWAMs sec. 3.2: the Hadamard is fused into the weights);
+ *   P Q                             the 16-bit low-rank protection branch (Q-WAM abstract,
+ *                                   Action-Subspace Protection); P = bf16(L1 * inv_s),
+ *                                   Q = bf16(L2), U = bf16(x P);
+ *   O (Omega), x_O, W_O             the transformed channels kept in FP16 (QuantWAMs
+ *                                   sec. 3.1, Eq. (3) Top-K mask; Fig. 1(d); sec. 4.2
+ *                                   "Quantization configuration" exception path);
+ *   Q4                              NVFP4: e2m1 codes, one unsigned e4m3 scale per 16
+ *                                   consecutive K elements, one fp32 tensor scale
+ *                                   (LatentQuant abstract; QuantWAMs sec. 4.2 "Backend":
+ *                                   NVFP4 W4A4 kernels).  Activations use one fp32 scale per
+ *                                   row, computed at run time (FoldQuantVLA, Key Contribution 2:
+ *                                   dynamic per-token quantisation); weights one per tensor.
+ *   NVFP4 rounding: g = amax / 2688; sc = e4m3_rn_satfinite((bmax / 6) / g);
+ *   d = dec(sc) * g; code = e2m1_rn_satfinite(v / d) (0 when d == 0); each step one
+ *   IEEE fp32 operation.
+ *
+ * Conventions for every entry point:
+ *   - Device pointers must be 16-byte aligned.  "host" / "device" is stated per argument.
+ *   - All calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream)
+ *     unless stated otherwise.  Inputs are not modified.
+ *   - Errors are returned as wq_status and never abort the process; wq_last_error()
+ *     returns a thread-local message for the last failure.
+ *   - NaN / Inf inputs are outside the contract.
+ *   - Supported shapes: K % 64 == 0 and 64 <= K <= 16384; N % 16 == 0; rank in
+ *     {0, 16, 32, 64}; n_outliers in {0, 16, 32, 64}; M >= 0 (M == 0 is a no-op).
+ *     Anything else returns WQ_ERR_UNSUPPORTED.
+ */
+#ifndef WQ_H_
+#define WQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define WQ_API __attribute__((visibility("default")))
+
+typedef struct wq_weights *wq_weights_t;   /* opaque; owns library-allocated device memory */
+
+typedef enum wq_status {
+    WQ_OK = 0,
+    WQ_ERR_INVALID = -1,       /* null pointer, negative size, unsorted Omega, bad enum  */
+    WQ_ERR_UNSUPPORTED = -2,   /* shape or option outside the supported set               */
+    WQ_ERR_CUDA = -3,          /* a CUDA runtime call failed (message in wq_last_error)   */
+    WQ_ERR_OOM = -4,           /* device or host allocation failed                        */
+    WQ_ERR_TIMEOUT = -5        /* a kernel gave up waiting on one of its barriers         */
+} wq_status;
+
+enum { WQ_MODE_W4A4 = 0, WQ_MODE_W8A8 = 1 };
+enum { WQ_SCALE_LAYOUT_ROWMAJOR = 0, WQ_SCALE_LAYOUT_MMA = 1 };
+
+typedef struct wq_config {
+    int K;            /* input features (reduction dimension)                              */
+    int N;            /* output features                                                   */
+    int rank;         /* low-rank branch rank r (0 disables the branch)                    */
+    int n_outliers;   /* |Omega|, channels of the rotated basis kept in fp16 (0 disables)  */
+    int rotate;       /* 1: block-64 Walsh-Hadamard rotation; 0: none                     */
+    int mode;         /* WQ_MODE_W4A4 (only mode implemented by wq_linear_forward)         */
+} wq_config;
+
+/*
+ * Fold and quantise one projection's weights (offline; FoldQuantVLA Key Contribution 1
+ * "consistent folding"; Q-WAM ASP; QuantWAMs sec. 3.1 exception channels).
+ *   cfg     host, shape and options.
+ *   W       host fp32 [K, N] row-major (math convention y = x W).
+ *   bias    host fp32 [N] or NULL.
+ *   s       host fp32 [K] smoothing factors (> 0) or NULL for s = 1.
+ *   L1, L2  host fp32 [K, r] and [r, N] (top-r factors of diag(s) W); NULL when r == 0.
+ *   omega   host int32 [n_outliers], strictly ascending channel indices of the rotated
+ *           basis, each < K; NULL when n_outliers == 0.
+ *   stream  uploads are enqueued on it; the handle is usable by later work on any stream
+ *           after the call returns (the call synchronises its uploads).
+ *   out     receives the handle; free it with wq_free_weights().
+ */
+WQ_API wq_status wq_prepare_weights(const wq_config *cfg, const float *W, const float *bias,
+                                    const float *s, const float *L1, const float *L2,
+                                    const int32_t *omega, void *stream, wq_weights_t *out);
+
+/* Copy the handle's configuration into *cfg (host). */
+WQ_API wq_status wq_get_config(wq_weights_t h, wq_config *cfg);
+
+/*
+ * Bytes of device scratch that wq_linear_forward needs for M rows (the quantised
+ * activations, their scales, per-row scales, U and x_Omega).  Returns 0 for a NULL handle.
+ */
+WQ_API size_t wq_workspace_bytes(wq_weights_t h, int M);
+
+/*
+ * The hot path: y = projection(x).
+ *   x          device bf16 [M, K] row-major.
+ *   y          device bf16 [M, N] row-major (written entirely; may not alias x).
+ *   workspace  device scratch of at least wq_workspace_bytes(h, M) bytes, 256-byte aligned,
+ *              owned by the caller; must not be used concurrently by another call.
+ * Two kernels run on `stream`: the fused smooth + FWHT + NVFP4 activation quantiser and
+ * the tcgen05 block-scaled FP4 GEMM with the fused epilogue (dequantisation, low-rank
+ * branch, outlier slice, bias).
+ */
+WQ_API wq_status wq_linear_forward(wq_weights_t h, const void *x, int M, void *y,
+                                   void *workspace, size_t workspace_bytes, void *stream);
+
+/* Bytes of device scratch wq_linear_forward_host needs (workspace + x and y staging). */
+WQ_API size_t wq_host_workspace_bytes(wq_weights_t h, int M);
+
+/*
+ * End-to-end variant over HOST buffers: copies x (host bf16 [M, K], preferably pinned)
+ * to the device, runs wq_linear_forward, copies y back to host bf16 [M, N].  Both copies
+ * and the kernels are enqueued on `stream`; y is valid after the stream synchronises.
+ * workspace: device, at least wq_host_workspace_bytes(h, M) bytes.
+ */
+WQ_API wq_status wq_linear_forward_host(wq_weights_t h, const void *x_host, int M, void *y_host,
+                                        void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Run only the activation quantiser (for parity checks and for callers that keep the
+ * quantised activations).  All outputs are device pointers:
+ *   codes   uint8 [M, K/2]; element 2i of a row in the low nibble of byte i.
+ *   scales  e4m3 bytes: WQ_SCALE_LAYOUT_ROWMAJOR -> [M, K/16];
+ *           WQ_SCALE_LAYOUT_MMA -> ceil(M/128) x (K/64) atoms of 512 bytes, atom (mb, kb)
+ *           at offset (mb * K/64 + kb) * 512, row r of the 128-row block and 16-block j of
+ *           the 64-block at byte (r % 32) * 16 + (r / 32) * 4 + j (the tcgen05
+ *           block-scale layout the GEMM consumes).
+ *   gscale  fp32 [M] per-row tensor scales.
+ *   x_omega fp16 [M, n_outliers]; required when n_outliers > 0 (NULL otherwise).
+ *   u       bf16 [M, rank] or NULL (not computed when NULL).
+ */
+WQ_API wq_status wq_quantize_activations(wq_weights_t h, const void *x, int M, int scale_layout,
+                                         uint8_t *codes, uint8_t *scales, float *gscale,
+                                         void *x_omega, void *u, void *stream);
+
+/*
+ * Copy the prepared weights back to host memory in canonical layouts (synchronous):
+ *   codes uint8 [N, K/2]; scales e4m3 [N, K/16]; gW fp32 scalar; P bf16 [K, r];
+ *   Q bf16 [r, N]; W_omega fp16 [n_outliers, N].  Any output may be NULL.
+ */
+WQ_API wq_status wq_export_weights(wq_weights_t h, uint8_t *codes, uint8_t *scales, float *gW,
+                                   uint16_t *P, uint16_t *Q, uint16_t *W_omega);
+
+/*
+ * Synchronise `stream` and report whether a kernel of this handle set its device error
+ * flag (a barrier wait that exceeded its time limit).  Clears the flag.
+ * Returns WQ_OK or WQ_ERR_TIMEOUT (or WQ_ERR_CUDA).
+ */
+WQ_API wq_status wq_check_device_error(wq_weights_t h, void *stream);
+
+/* Release the handle and its device memory (synchronises the device first).  NULL is a no-op. */
+WQ_API void wq_free_weights(wq_weights_t h);
+
+/* Thread-local description of the last error ("" if none). */
+WQ_API const char *wq_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* WQ_H_ */

@@ -1,0 +1,221 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Bar (written here, derived in the design notes):
+  * weight and activation codes, e4m3 scales, fp32 row/tensor scales, fp16 outlier
+    values: bit-exact;
+  * U = bf16(x P): within one bf16 ulp (fp32 vs fp64 accumulation before one rounding);
+  * y: |y_gpu - y_oracle| <= 1e-3 (|y| + ||x_row|| ||w_col|| / sqrt(K)) + 2^-8 |y|
+    (fp32 accumulation vs fp64, plus the bf16 rounding of the output).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import w4a4_nvfp4_quantized_wq_b300 as wq
+import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from w4a4_nvfp4_quantized_wq_b300 import build
+    build.build_library()
+    torch.cuda.set_device(0)
+
+
+def x_dev(bits: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def prep(L):
+    return wq.wq_prepare_weights(L.spec.K, L.spec.N, L.W, L.bias, L.s, L.L1, L.L2,
+                                 L.omega if L.omega.size else None, rotate=L.rotate)
+
+
+def y_tolerance(L, y_ref, rows=None):
+    x = L.x_f32 if rows is None else L.x_f32[rows]
+    xn = np.linalg.norm(x.astype(np.float64), axis=1)[:, None]
+    wn = np.linalg.norm(L.W.astype(np.float64), axis=0)[None, :]
+    return 1e-3 * (np.abs(y_ref) + xn * wn / np.sqrt(L.spec.K)) + 2.0 ** -8 * np.abs(y_ref)
+
+
+def assert_y_close(L, y_gpu, y_ref, rows=None):
+    y = y_gpu.float().cpu().numpy().astype(np.float64)
+    tol = y_tolerance(L, y_ref, rows)
+    err = np.abs(y - y_ref)
+    bad = err > tol
+    assert not bad.any(), (f"{bad.sum()} of {bad.size} outside tolerance; worst excess "
+                           f"{np.max(err - tol):.3g} at {np.unravel_index(np.argmax(err - tol), err.shape)}")
+    return float(np.max(err / np.maximum(tol, 1e-30)))
+
+
+def bf16_ulp_close(a_bits, b_bits):
+    a = wl.bf16_from_bits(a_bits).astype(np.float64)
+    b = wl.bf16_from_bits(b_bits).astype(np.float64)
+    ulp = np.maximum(np.spacing(wl.bf16_from_bits(b_bits)).astype(np.float64) * 65536.0, 2.0 ** -133)
+    return np.abs(a - b) <= ulp
+
+
+CASES = {
+    "tiny_full": ("tiny", dict()),
+    "expert_small": ("expert", dict(M=50, K=1024, N=512)),
+    "ragged_m130": ("expert", dict(M=130, K=256, N=384, rank=16)),
+    "dit_r32_o64_ragged_n": ("video_dit", dict(M=200, K=512, N=272, rank=32, n_omega=64)),
+    "backbone_r0": ("backbone", dict(layer=0, M=129, K=2048, N=256)),
+    "no_rotate_o16": ("video_dit", dict(M=64, K=1536, N=128, rank=32, n_omega=16, rotate=False)),
+    "no_smooth_r64": ("expert", dict(M=33, K=640, N=160, rank=64, smooth=False)),
+    "min_k64_n16_m1": ("expert", dict(M=1, K=64, N=16, rank=0)),
+    "multi_tile_kstage_tail": ("expert", dict(M=260, K=1088, N=400, rank=16)),
+}
+
+
+def layer(case):
+    name, kw = CASES[case]
+    return wl.make_layer_inputs(name, **kw)
+
+
+@pytest.mark.parametrize("case", list(CASES))
+def test_weights_bitexact(case):
+    L = layer(case)
+    w = prep(L)
+    ex = wq.wq_export_weights(w)
+    o = oracle.prepare_weights(L.W, L.s, L.L1, L.L2, L.omega, L.rotate)
+    assert np.float32(ex["gW"]) == np.float32(o.gW)
+    assert np.array_equal(ex["scales"], o.scales)
+    assert np.array_equal(ex["codes"], o.codes)
+    assert np.array_equal(ex["P"], o.P) and np.array_equal(ex["Q"], o.Q)
+    assert np.array_equal(ex["W_omega"], o.W_omega)
+
+
+@pytest.mark.parametrize("case", list(CASES))
+def test_activation_quant_bitexact(case):
+    L = layer(case)
+    w = prep(L)
+    x = x_dev(L.x_bits)
+    codes, scales, g, xo, u = wq.wq_quantize_activations(w, x, wq.WQ_SCALE_LAYOUT_ROWMAJOR)
+    codes2, sf_mma, g2, _, _ = wq.wq_quantize_activations(w, x, wq.WQ_SCALE_LAYOUT_MMA)
+    torch.cuda.synchronize()
+    aq = oracle.quantize_act(L.x_bits, L.s, L.rotate, L.omega)
+    assert np.array_equal(g.cpu().numpy(), aq.g)
+    assert np.array_equal(scales.cpu().numpy(), aq.scales)
+    assert np.array_equal(codes.cpu().numpy(), aq.codes)
+    M, K = L.x_bits.shape
+    assert np.array_equal(wq.mma_scales_to_rowmajor(sf_mma.cpu().numpy(), M, K), aq.scales)
+    assert np.array_equal(codes2.cpu().numpy(), aq.codes) and np.array_equal(g2.cpu().numpy(), aq.g)
+    if L.omega.size:
+        assert np.array_equal(xo.cpu().view(torch.int16).numpy().view(np.uint16), aq.x_omega)
+    if L.rank:
+        o = oracle.prepare_weights(L.W, L.s, L.L1, L.L2, L.omega, L.rotate)
+        U = oracle.lowrank_act(L.x_bits, o.P)
+        ug = u.cpu().view(torch.int16).numpy().view(np.uint16)
+        assert bf16_ulp_close(ug, U).all()
+
+
+@pytest.mark.parametrize("case", list(CASES))
+def test_forward_parity(case):
+    L = layer(case)
+    w = prep(L)
+    y = wq.wq_linear_forward(w, x_dev(L.x_bits))
+    wq.wq_check_device_error(w)
+    y_ref, *_ = oracle.reference_forward(L)
+    assert_y_close(L, y, y_ref)
+
+
+def test_forward_is_deterministic_and_host_path_matches():
+    L = layer("dit_r32_o64_ragged_n")
+    w = prep(L)
+    x = x_dev(L.x_bits)
+    y1 = wq.wq_linear_forward(w, x)
+    y2 = wq.wq_linear_forward(w, x)
+    M = x.shape[0]
+    xh = x.cpu().pin_memory()
+    yh = torch.empty((M, L.spec.N), dtype=torch.bfloat16).pin_memory()
+    ws = torch.empty(wq.wq_host_workspace_bytes(w, M), dtype=torch.uint8, device="cuda")
+    wq.wq_linear_forward_host(w, xh, yh, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
+    assert torch.equal(y1.cpu(), yh)
+
+
+def test_zero_rows_and_empty_batch():
+    L = wl.make_layer_inputs("expert", M=40, K=256, N=128, rank=16)
+    bits = L.x_bits.copy()
+    bits[3] = 0
+    bits[17] = 0x8000            # -0.0 everywhere
+    L.x_bits = bits
+    w = prep(L)
+    y = wq.wq_linear_forward(w, x_dev(bits))
+    _, _, g, _, _ = wq.wq_quantize_activations(w, x_dev(bits))
+    torch.cuda.synchronize()
+    assert g[3].item() == 0.0 and g[17].item() == 0.0
+    y_ref, *_ = oracle.reference_forward(L)
+    assert_y_close(L, y, y_ref)
+    empty = torch.empty((0, 256), dtype=torch.bfloat16, device="cuda")
+    y0 = wq.wq_linear_forward(w, empty)
+    assert y0.shape == (0, 128)
+
+
+def test_rounding_ties_through_the_quantiser():
+    """With s = 1 and no rotation the quantiser sees x itself.  A row holding 2688 has
+    g = 1 exactly; blocks with maximum 6 * 2^j get scale 2^j, so the other values sit
+    exactly on e2m1 midpoints, on grid points, just beside them, and at +-0."""
+    K = 256
+    rows = []
+    mids = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 0.5, 1.0, 3.0, 4.0, 0.2, 0.3, 5.5, 7.0]
+    for j in range(-3, 4):
+        r = np.zeros(K, np.float32)
+        r[0] = 2688.0
+        for b in range(1, K // 16):
+            blk = np.array(mids + [6.0], np.float32) * np.float32(2.0 ** j)
+            blk *= np.where(np.arange(16) % 2 == (b % 2), -1.0, 1.0).astype(np.float32)
+            r[16 * b:16 * b + 16] = blk
+        r[17] = -0.0
+        r[18] = 0.0
+        rows.append(r)
+    x = np.stack(rows)
+    bits = wl.bf16_bits(x)
+    assert np.array_equal(wl.bf16_from_bits(bits), x)
+    W = np.random.default_rng(0).standard_normal((K, 64)).astype(np.float32) * 0.02
+    w = wq.wq_prepare_weights(K, 64, W, rotate=False)
+    codes, scales, g, _, _ = wq.wq_quantize_activations(w, x_dev(bits))
+    torch.cuda.synchronize()
+    aq = oracle.quantize_act(bits, None, False)
+    assert np.all(aq.g == 1.0)
+    assert np.array_equal(scales.cpu().numpy(), aq.scales)
+    assert np.array_equal(codes.cpu().numpy(), aq.codes)
+
+
+# ------------------------------------------------------------------ full sizes
+def _sampled_rows(M, n, seed):
+    return np.sort(np.random.default_rng(seed).choice(M, size=n, replace=False))
+
+
+@pytest.mark.parametrize("layer_idx", [0, 1])
+def test_expert_batch1_full_size(layer_idx):
+    L = wl.make_layer_inputs("expert", layer=layer_idx)
+    w = prep(L)
+    y = wq.wq_linear_forward(w, x_dev(L.x_bits))
+    wq.wq_check_device_error(w)
+    y_ref, *_ = oracle.reference_forward(L)
+    assert_y_close(L, y, y_ref)
+
+
+@pytest.mark.parametrize("wl_name,layer_idx", [("video_dit", 0), ("video_dit", 1), ("video_dit", 2),
+                                               ("video_dit", 3), ("backbone", 0), ("backbone", 2)])
+def test_full_size_sampled_rows(wl_name, layer_idx):
+    L = wl.make_layer_inputs(wl_name, layer=layer_idx)
+    w = prep(L)
+    x = x_dev(L.x_bits)
+    y = wq.wq_linear_forward(w, x)
+    codes, scales, g, xo, _ = wq.wq_quantize_activations(w, x)
+    wq.wq_check_device_error(w)
+    rows = _sampled_rows(L.M, 24, 100 + layer_idx)
+    y_ref, aq, _, _ = oracle.reference_forward(L, rows=rows)
+    assert np.array_equal(codes.cpu().numpy()[rows], aq.codes)
+    assert np.array_equal(scales.cpu().numpy()[rows], aq.scales)
+    assert np.array_equal(g.cpu().numpy()[rows], aq.g)
+    assert_y_close(L, y[torch.from_numpy(rows).cuda()], y_ref, rows)

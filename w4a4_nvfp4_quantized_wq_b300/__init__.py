@@ -1,0 +1,236 @@
+"""Python binding of libwq (include/wq.h): argument marshalling only.
+
+Every computation runs in the library's CUDA kernels; PyTorch provides device
+memory and streams.  The functions keep the C names.  If ``libwq.so`` has not
+been built, importing the binding's functions raises immediately: there is no
+fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libwq.so")
+
+WQ_OK, WQ_ERR_INVALID, WQ_ERR_UNSUPPORTED, WQ_ERR_CUDA, WQ_ERR_OOM, WQ_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
+WQ_MODE_W4A4, WQ_MODE_W8A8 = 0, 1
+WQ_SCALE_LAYOUT_ROWMAJOR, WQ_SCALE_LAYOUT_MMA = 0, 1
+
+EXPORTED = ["wq_prepare_weights", "wq_get_config", "wq_workspace_bytes", "wq_linear_forward",
+            "wq_host_workspace_bytes", "wq_linear_forward_host", "wq_quantize_activations",
+            "wq_export_weights", "wq_check_device_error", "wq_free_weights", "wq_last_error"]
+
+
+class WqError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"wq status {status}: {msg}")
+        self.status = status
+
+
+class wq_config(ctypes.Structure):
+    _fields_ = [("K", ctypes.c_int), ("N", ctypes.c_int), ("rank", ctypes.c_int),
+                ("n_outliers", ctypes.c_int), ("rotate", ctypes.c_int), ("mode", ctypes.c_int)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libwq.so (raises if it was not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} not found: build it with "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        L.wq_prepare_weights.argtypes = [ctypes.POINTER(wq_config), P, P, P, P, P, P, P, ctypes.POINTER(P)]
+        L.wq_prepare_weights.restype = I
+        L.wq_get_config.argtypes = [P, ctypes.POINTER(wq_config)]
+        L.wq_get_config.restype = I
+        L.wq_workspace_bytes.argtypes = [P, I]
+        L.wq_workspace_bytes.restype = S
+        L.wq_host_workspace_bytes.argtypes = [P, I]
+        L.wq_host_workspace_bytes.restype = S
+        L.wq_linear_forward.argtypes = [P, P, I, P, P, S, P]
+        L.wq_linear_forward.restype = I
+        L.wq_linear_forward_host.argtypes = [P, P, I, P, P, S, P]
+        L.wq_linear_forward_host.restype = I
+        L.wq_quantize_activations.argtypes = [P, P, I, I, P, P, P, P, P, P]
+        L.wq_quantize_activations.restype = I
+        L.wq_export_weights.argtypes = [P, P, P, P, P, P, P]
+        L.wq_export_weights.restype = I
+        L.wq_check_device_error.argtypes = [P, P]
+        L.wq_check_device_error.restype = I
+        L.wq_free_weights.argtypes = [P]
+        L.wq_free_weights.restype = None
+        L.wq_last_error.argtypes = []
+        L.wq_last_error.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def wq_last_error() -> str:
+    return lib().wq_last_error().decode()
+
+
+def _check(status: int):
+    if status != WQ_OK:
+        raise WqError(status, wq_last_error())
+
+
+def _host(a, dtype):
+    if a is None:
+        return None, None
+    arr = np.ascontiguousarray(a, dtype=dtype)
+    return arr, arr.ctypes.data_as(ctypes.c_void_p)
+
+
+def _stream_ptr(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+@dataclass
+class Weights:
+    """Owner of a wq_weights_t handle."""
+    handle: int
+    cfg: wq_config
+
+    def __del__(self):
+        if getattr(self, "handle", None) and _lib is not None:
+            _lib.wq_free_weights(ctypes.c_void_p(self.handle))
+            self.handle = None
+
+    @property
+    def K(self):
+        return self.cfg.K
+
+    @property
+    def N(self):
+        return self.cfg.N
+
+
+def wq_prepare_weights(K: int, N: int, W, bias=None, s=None, L1=None, L2=None, omega=None,
+                       rotate: bool = True, mode: int = WQ_MODE_W4A4, stream=None) -> Weights:
+    """Fold and quantise one projection (host inputs, numpy or CPU tensors)."""
+    rank = 0 if L1 is None else int(np.shape(L1)[1])
+    n_out = 0 if omega is None else int(np.size(omega))
+    cfg = wq_config(K, N, rank, n_out, int(bool(rotate)), mode)
+    keep = []
+    ptrs = []
+    for a, dt in ((W, np.float32), (bias, np.float32), (s, np.float32), (L1, np.float32),
+                  (L2, np.float32), (omega, np.int32)):
+        if a is not None and hasattr(a, "numpy"):
+            a = a.detach().cpu().numpy()
+        arr, p = _host(a, dt)
+        keep.append(arr)
+        ptrs.append(p)
+    out = ctypes.c_void_p()
+    _check(lib().wq_prepare_weights(ctypes.byref(cfg), *ptrs, ctypes.c_void_p(_stream_ptr(stream)),
+                                    ctypes.byref(out)))
+    return Weights(out.value, cfg)
+
+
+def wq_get_config(w: Weights) -> wq_config:
+    cfg = wq_config()
+    _check(lib().wq_get_config(ctypes.c_void_p(w.handle), ctypes.byref(cfg)))
+    return cfg
+
+
+def wq_workspace_bytes(w: Weights, M: int) -> int:
+    return int(lib().wq_workspace_bytes(ctypes.c_void_p(w.handle), int(M)))
+
+
+def wq_host_workspace_bytes(w: Weights, M: int) -> int:
+    return int(lib().wq_host_workspace_bytes(ctypes.c_void_p(w.handle), int(M)))
+
+
+def _alloc_workspace(nbytes: int, device):
+    import torch
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def wq_linear_forward(w: Weights, x, y=None, workspace=None, stream=None):
+    """y[M, N] (bf16, device) = projection(x[M, K] bf16, device)."""
+    import torch
+    assert x.dtype == torch.bfloat16 and x.is_cuda and x.is_contiguous() and x.shape[-1] == w.K
+    M = x.shape[0]
+    if y is None:
+        y = torch.empty((M, w.N), dtype=torch.bfloat16, device=x.device)
+    if workspace is None:
+        workspace = _alloc_workspace(wq_workspace_bytes(w, M), x.device)
+    _check(lib().wq_linear_forward(ctypes.c_void_p(w.handle), ctypes.c_void_p(x.data_ptr()), M,
+                                   ctypes.c_void_p(y.data_ptr()), ctypes.c_void_p(workspace.data_ptr()),
+                                   workspace.numel(), ctypes.c_void_p(_stream_ptr(stream))))
+    return y
+
+
+def wq_linear_forward_host(w: Weights, x_host, y_host, workspace, stream=None):
+    """End-to-end call on host (pinned) bf16 tensors; y_host is valid after the stream syncs."""
+    M = x_host.shape[0]
+    _check(lib().wq_linear_forward_host(ctypes.c_void_p(w.handle), ctypes.c_void_p(x_host.data_ptr()), M,
+                                        ctypes.c_void_p(y_host.data_ptr()), ctypes.c_void_p(workspace.data_ptr()),
+                                        workspace.numel(), ctypes.c_void_p(_stream_ptr(stream))))
+    return y_host
+
+
+def wq_quantize_activations(w: Weights, x, scale_layout: int = WQ_SCALE_LAYOUT_ROWMAJOR, stream=None):
+    """Run the activation quantiser alone; returns device tensors (codes, scales, g, x_omega, u)."""
+    import torch
+    M, K = x.shape
+    dev = x.device
+    codes = torch.empty((M, K // 2), dtype=torch.uint8, device=dev)
+    if scale_layout == WQ_SCALE_LAYOUT_MMA:
+        scales = torch.zeros(((M + 127) // 128) * (K // 64) * 512, dtype=torch.uint8, device=dev)
+    else:
+        scales = torch.empty((M, K // 16), dtype=torch.uint8, device=dev)
+    g = torch.empty(M, dtype=torch.float32, device=dev)
+    xo = torch.empty((M, w.cfg.n_outliers), dtype=torch.float16, device=dev) if w.cfg.n_outliers else None
+    u = torch.empty((M, w.cfg.rank), dtype=torch.bfloat16, device=dev) if w.cfg.rank else None
+    _check(lib().wq_quantize_activations(
+        ctypes.c_void_p(w.handle), ctypes.c_void_p(x.data_ptr()), M, int(scale_layout),
+        ctypes.c_void_p(codes.data_ptr()), ctypes.c_void_p(scales.data_ptr()), ctypes.c_void_p(g.data_ptr()),
+        ctypes.c_void_p(xo.data_ptr() if xo is not None else None),
+        ctypes.c_void_p(u.data_ptr() if u is not None else None), ctypes.c_void_p(_stream_ptr(stream))))
+    return codes, scales, g, xo, u
+
+
+def wq_export_weights(w: Weights) -> dict:
+    """Prepared weights copied back to host in canonical layouts."""
+    K, N, r, no = w.cfg.K, w.cfg.N, w.cfg.rank, w.cfg.n_outliers
+    codes = np.zeros((N, K // 2), np.uint8)
+    scales = np.zeros((N, K // 16), np.uint8)
+    gW = np.zeros(1, np.float32)
+    P = np.zeros((K, r), np.uint16)
+    Q = np.zeros((r, N), np.uint16)
+    Wo = np.zeros((no, N), np.uint16)
+    vp = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+    _check(lib().wq_export_weights(ctypes.c_void_p(w.handle), vp(codes), vp(scales), vp(gW), vp(P), vp(Q), vp(Wo)))
+    return dict(codes=codes, scales=scales, gW=float(gW[0]), P=P, Q=Q, W_omega=Wo)
+
+
+def wq_check_device_error(w: Weights, stream=None):
+    _check(lib().wq_check_device_error(ctypes.c_void_p(w.handle), ctypes.c_void_p(_stream_ptr(stream))))
+
+
+def wq_free_weights(w: Weights):
+    if w.handle:
+        lib().wq_free_weights(ctypes.c_void_p(w.handle))
+        w.handle = None
+
+
+def mma_scales_to_rowmajor(sf_mma: np.ndarray, M: int, K: int) -> np.ndarray:
+    """Decode the documented tcgen05 block-scale layout (wq.h) into [M, K/16]."""
+    sf = np.asarray(sf_mma, np.uint8).reshape(-1)
+    m = np.arange(M)[:, None]
+    b = np.arange(K // 16)[None, :]
+    off = ((m // 128) * (K // 64) + b // 4) * 512 + (m % 32) * 16 + ((m % 128) // 32) * 4 + (b % 4)
+    return sf[off]

@@ -1,0 +1,532 @@
+// wq_api.cu -- the C ABI declared in include/wq.h: argument checks, offline weight folding
+// and NVFP4 quantisation (host, fp64 fold), device residency of the prepared weights,
+// tensor-map construction and the two-kernel forward.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp4.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <thread>
+#include <vector>
+
+#include "wq_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+wq_status fail(wq_status s, const std::string& msg) {
+    g_last_error = msg;
+    return s;
+}
+
+wq_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(WQ_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+#define WQ_CUDA(call, what)                                  \
+    do {                                                     \
+        cudaError_t e_ = (call);                             \
+        if (e_ != cudaSuccess) return cuda_fail(e_, what);   \
+    } while (0)
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+uint16_t bf16_bits(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
+uint16_t f16_bits(float f) { return __half_as_ushort(__float2half_rn(f)); }
+
+float e4m3_value(uint32_t c) {
+    const uint32_t e = (c >> 3) & 15u, m = c & 7u;
+    if (e == 0) return static_cast<float>(m) * 0.001953125f;
+    return std::ldexp(1.0f + static_cast<float>(m) / 8.0f, static_cast<int>(e) - 7);
+}
+
+// In-place block-64 Walsh-Hadamard transform (fp64) of a strided vector: butterflies at
+// strides 1, 2, 4, 8, 16, 32, then the 1/8 normalisation.
+void fwht64_f64(double* v, size_t stride) {
+    for (int h = 1; h < 64; h <<= 1)
+        for (int i = 0; i < 64; ++i)
+            if ((i & h) == 0) {
+                const double a = v[i * stride], b = v[(i + h) * stride];
+                v[i * stride] = a + b;
+                v[(i + h) * stride] = a - b;
+            }
+    for (int i = 0; i < 64; ++i) v[i * stride] = v[i * stride] * 0.125;
+}
+
+template <typename F>
+void parallel_for(size_t n, F&& f) {
+    unsigned nt = std::max(1u, std::min(32u, std::thread::hardware_concurrency()));
+    if (n < 64) nt = 1;
+    std::vector<std::thread> th;
+    const size_t chunk = (n + nt - 1) / nt;
+    for (unsigned t = 0; t < nt; ++t) {
+        const size_t lo = t * chunk, hi = std::min(n, lo + chunk);
+        if (lo >= hi) break;
+        th.emplace_back([&f, lo, hi] { for (size_t i = lo; i < hi; ++i) f(i); });
+    }
+    for (auto& x : th) x.join();
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+CUtensorMapSwizzle swizzle_for_row_bytes(uint32_t b) {
+    return b == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : (b == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
+}
+
+}  // namespace
+
+namespace wq {
+
+bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner, uint64_t outer,
+                    uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle,
+                    const char** why) {
+    EncodeTiledFn fn = get_encode_fn();
+    if (!fn) { *why = "cuTensorMapEncodeTiled unavailable"; return false; }
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) { *why = "cuTensorMapEncodeTiled failed"; return false; }
+    return true;
+}
+
+ActWorkspace carve_workspace(void* base, int M, int K, int r, int n_out) {
+    ActWorkspace w;
+    const size_t m_pad = align_up(static_cast<size_t>(M), kBlockM);
+    size_t off = 0;
+    auto take = [&](size_t bytes) { const size_t o = off; off = align_up(off + bytes, 1024); return o; };
+    const size_t o_codes = take(static_cast<size_t>(M) * K / 2);
+    const size_t o_sf = take(m_pad / kBlockM * (K / 64) * kSfAtom);
+    const size_t o_g = take(static_cast<size_t>(M) * 4);
+    const size_t o_u = take(static_cast<size_t>(M) * r * 2);
+    const size_t o_xo = take(static_cast<size_t>(M) * n_out * 2);
+    w.bytes = off;
+    if (base) {
+        uint8_t* b = static_cast<uint8_t*>(base);
+        w.codes = b + o_codes;
+        w.sf = b + o_sf;
+        w.g = reinterpret_cast<float*>(b + o_g);
+        w.u = reinterpret_cast<uint16_t*>(b + o_u);
+        w.xo = reinterpret_cast<uint16_t*>(b + o_xo);
+    }
+    return w;
+}
+
+}  // namespace wq
+
+struct wq_weights {
+    wq_config cfg{};
+    int device = 0;
+    int num_sms = 0;
+    float gW = 0.0f;
+    uint8_t* d_codes = nullptr;    // [N, K/2]
+    uint8_t* d_sf = nullptr;       // MMA layout, ceil(N/128) * K/64 atoms
+    float* d_bias = nullptr;       // [N]
+    float* d_inv_s = nullptr;      // [K]
+    int16_t* d_omega_pos = nullptr;// [K]
+    uint16_t* d_P = nullptr;       // [K, r] bf16
+    uint16_t* d_Qt = nullptr;      // [N, r] bf16
+    uint16_t* d_WOt = nullptr;     // [N, n_out] fp16
+    int* d_err = nullptr;
+    CUtensorMap tmB{}, tmQ{}, tmWO{};
+    // activation / output tensor maps, re-encoded when the buffers change
+    std::mutex mu;
+    const void* key_ws = nullptr;
+    const void* key_y = nullptr;
+    int key_M = -1;
+    CUtensorMap tmA{}, tmU{}, tmXO{}, tmY{};
+};
+
+namespace {
+
+wq_status check_config(const wq_config* c) {
+    if (!c) return fail(WQ_ERR_INVALID, "cfg is NULL");
+    if (c->K <= 0 || c->N <= 0 || c->rank < 0 || c->n_outliers < 0)
+        return fail(WQ_ERR_INVALID, "negative or zero size in cfg");
+    if (c->mode != WQ_MODE_W4A4) return fail(WQ_ERR_UNSUPPORTED, "only WQ_MODE_W4A4 is implemented");
+    if (c->rotate != 0 && c->rotate != 1) return fail(WQ_ERR_INVALID, "rotate must be 0 or 1");
+    if (c->K % 64 || c->K > 16384) return fail(WQ_ERR_UNSUPPORTED, "K must be a multiple of 64 and <= 16384");
+    if (c->N % 16) return fail(WQ_ERR_UNSUPPORTED, "N must be a multiple of 16");
+    if (!(c->rank == 0 || c->rank == 16 || c->rank == 32 || c->rank == 64))
+        return fail(WQ_ERR_UNSUPPORTED, "rank must be 0, 16, 32 or 64");
+    if (!(c->n_outliers == 0 || c->n_outliers == 16 || c->n_outliers == 32 || c->n_outliers == 64))
+        return fail(WQ_ERR_UNSUPPORTED, "n_outliers must be 0, 16, 32 or 64");
+    return WQ_OK;
+}
+
+void free_device(wq_weights* h) {
+    cudaFree(h->d_codes);
+    cudaFree(h->d_sf);
+    cudaFree(h->d_bias);
+    cudaFree(h->d_inv_s);
+    cudaFree(h->d_omega_pos);
+    cudaFree(h->d_P);
+    cudaFree(h->d_Qt);
+    cudaFree(h->d_WOt);
+    cudaFree(h->d_err);
+}
+
+template <typename T>
+wq_status upload(T** dst, const void* src, size_t bytes, cudaStream_t st) {
+    if (bytes == 0) return WQ_OK;
+    if (cudaMalloc(reinterpret_cast<void**>(dst), bytes) != cudaSuccess)
+        return fail(WQ_ERR_OOM, "cudaMalloc of " + std::to_string(bytes) + " bytes failed");
+    WQ_CUDA(cudaMemcpyAsync(*dst, src, bytes, cudaMemcpyHostToDevice, st), "weight upload");
+    return WQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+WQ_API const char* wq_last_error(void) { return g_last_error.c_str(); }
+
+WQ_API wq_status wq_get_config(wq_weights_t h, wq_config* cfg) {
+    if (!h || !cfg) return fail(WQ_ERR_INVALID, "NULL argument");
+    *cfg = h->cfg;
+    return WQ_OK;
+}
+
+WQ_API wq_status wq_prepare_weights(const wq_config* cfg, const float* W, const float* bias, const float* s,
+                                    const float* L1, const float* L2, const int32_t* omega, void* stream,
+                                    wq_weights_t* out) {
+    g_last_error.clear();
+    if (!out) return fail(WQ_ERR_INVALID, "out is NULL");
+    *out = nullptr;
+    wq_status st = check_config(cfg);
+    if (st != WQ_OK) return st;
+    if (!W) return fail(WQ_ERR_INVALID, "W is NULL");
+    const int K = cfg->K, N = cfg->N, r = cfg->rank, no = cfg->n_outliers;
+    if (r > 0 && (!L1 || !L2)) return fail(WQ_ERR_INVALID, "rank > 0 needs L1 and L2");
+    if (no > 0 && !omega) return fail(WQ_ERR_INVALID, "n_outliers > 0 needs omega");
+    for (int j = 0; j < no; ++j) {
+        if (omega[j] < 0 || omega[j] >= K) return fail(WQ_ERR_INVALID, "omega index out of range");
+        if (j > 0 && omega[j] <= omega[j - 1]) return fail(WQ_ERR_INVALID, "omega must be strictly ascending");
+    }
+    if (s)
+        for (int k = 0; k < K; ++k)
+            if (!(s[k] > 0.0f) || !std::isfinite(s[k])) return fail(WQ_ERR_INVALID, "s must be finite and > 0");
+
+    // ---- smoothing inverse and the 16-bit low-rank factors
+    std::vector<float> inv_s(s ? K : 0);
+    for (int k = 0; k < (s ? K : 0); ++k) inv_s[k] = 1.0f / s[k];
+    std::vector<uint16_t> P(static_cast<size_t>(K) * r), Qt(static_cast<size_t>(N) * r);
+    for (int k = 0; k < K; ++k)
+        for (int j = 0; j < r; ++j) {
+            float l = L1[static_cast<size_t>(k) * r + j];
+            if (s) l = l * inv_s[k];
+            P[static_cast<size_t>(k) * r + j] = bf16_bits(l);
+        }
+    std::vector<float> Pf(P.size()), Qf(static_cast<size_t>(r) * N);
+    for (size_t i = 0; i < P.size(); ++i) Pf[i] = __bfloat162float(__ushort_as_bfloat16(P[i]));
+    for (int j = 0; j < r; ++j)
+        for (int n = 0; n < N; ++n) {
+            const uint16_t b = bf16_bits(L2[static_cast<size_t>(j) * N + n]);
+            Qt[static_cast<size_t>(n) * r + j] = b;
+            Qf[static_cast<size_t>(j) * N + n] = __bfloat162float(__ushort_as_bfloat16(b));
+        }
+
+    // ---- fold: R' = FWHT_64( diag(s) (W - P Q) ) along K, fp64, rounded once to fp32
+    std::vector<float> Rp(static_cast<size_t>(K) * N);
+    parallel_for(static_cast<size_t>(N), [&](size_t n) {
+        std::vector<double> col(K);
+        for (int k = 0; k < K; ++k) {
+            double lr = 0.0;
+            for (int j = 0; j < r; ++j)
+                lr += static_cast<double>(Pf[static_cast<size_t>(k) * r + j]) *
+                      static_cast<double>(Qf[static_cast<size_t>(j) * N + n]);
+            const double t = static_cast<double>(W[static_cast<size_t>(k) * N + n]) - lr;
+            col[k] = s ? static_cast<double>(s[k]) * t : t;
+        }
+        if (cfg->rotate)
+            for (int b = 0; b < K / 64; ++b) fwht64_f64(col.data() + 64 * b, 1);
+        for (int k = 0; k < K; ++k) Rp[static_cast<size_t>(k) * N + n] = static_cast<float>(col[k]);
+    });
+
+    // ---- the fp16 outlier rows of the rotated basis
+    std::vector<uint16_t> WOt(static_cast<size_t>(N) * no);
+    std::vector<int16_t> omega_pos(no ? K : 0, -1);
+    for (int j = 0; j < no; ++j) {
+        omega_pos[omega[j]] = static_cast<int16_t>(j);
+        for (int n = 0; n < N; ++n) {
+            float& v = Rp[static_cast<size_t>(omega[j]) * N + n];
+            WOt[static_cast<size_t>(n) * no + j] = f16_bits(v);
+            v = 0.0f;
+        }
+    }
+
+    // ---- NVFP4 with one fp32 scale for the tensor; column n quantised along K
+    float amax = 0.0f;
+    for (float v : Rp) amax = std::max(amax, std::fabs(v));
+    const float gW = amax / 2688.0f;
+    const size_t n_pad = align_up(static_cast<size_t>(N), wq::kBlockM);
+    std::vector<uint8_t> codes(static_cast<size_t>(N) * K / 2);
+    std::vector<uint8_t> sf_mma(n_pad / wq::kBlockM * (K / 64) * wq::kSfAtom, 0);
+    parallel_for(static_cast<size_t>(N), [&](size_t n) {
+        for (int b = 0; b < K / 16; ++b) {
+            float v[16], bmax = 0.0f;
+            for (int i = 0; i < 16; ++i) {
+                v[i] = Rp[static_cast<size_t>(16 * b + i) * N + n];
+                bmax = std::max(bmax, std::fabs(v[i]));
+            }
+            uint32_t sc = 0;
+            if (gW != 0.0f) {
+                const float t = bmax / 6.0f;
+                sc = static_cast<uint32_t>(__nv_cvt_float_to_fp8(t / gW, __NV_SATFINITE, __NV_E4M3));
+            }
+            const float d = e4m3_value(sc) * gW;
+            for (int i = 0; i < 16; i += 2) {
+                uint32_t c0 = 0, c1 = 0;
+                if (d != 0.0f) {
+                    c0 = __nv_cvt_float_to_fp4(v[i] / d, __NV_E2M1, cudaRoundNearest) & 15u;
+                    c1 = __nv_cvt_float_to_fp4(v[i + 1] / d, __NV_E2M1, cudaRoundNearest) & 15u;
+                }
+                codes[n * (K / 2) + 8 * b + i / 2] = static_cast<uint8_t>(c0 | (c1 << 4));
+            }
+            const size_t row = n, kb = static_cast<size_t>(b) / 4;
+            const size_t off = ((row / wq::kBlockM) * (K / 64) + kb) * wq::kSfAtom + (row % 32) * 16 +
+                               ((row % wq::kBlockM) / 32) * 4 + (b % 4);
+            sf_mma[off] = static_cast<uint8_t>(sc);
+        }
+    });
+
+    // ---- device residency
+    wq_weights* h = new (std::nothrow) wq_weights();
+    if (!h) return fail(WQ_ERR_OOM, "host allocation failed");
+    h->cfg = *cfg;
+    h->gW = gW;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    auto bail = [&](wq_status e) { free_device(h); delete h; return e; };
+    if (cudaGetDevice(&h->device) != cudaSuccess) return bail(fail(WQ_ERR_CUDA, "cudaGetDevice failed"));
+    cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
+    std::vector<float> bias_f(N, 0.0f);
+    if (bias) std::copy(bias, bias + N, bias_f.begin());
+    if ((st = upload(&h->d_codes, codes.data(), codes.size(), cs)) != WQ_OK) return bail(st);
+    if ((st = upload(&h->d_sf, sf_mma.data(), sf_mma.size(), cs)) != WQ_OK) return bail(st);
+    if (bias && (st = upload(&h->d_bias, bias_f.data(), N * 4, cs)) != WQ_OK) return bail(st);
+    if (s && (st = upload(&h->d_inv_s, inv_s.data(), K * 4, cs)) != WQ_OK) return bail(st);
+    if (no && (st = upload(&h->d_omega_pos, omega_pos.data(), K * 2, cs)) != WQ_OK) return bail(st);
+    if (r && (st = upload(&h->d_P, P.data(), P.size() * 2, cs)) != WQ_OK) return bail(st);
+    if (r && (st = upload(&h->d_Qt, Qt.data(), Qt.size() * 2, cs)) != WQ_OK) return bail(st);
+    if (no && (st = upload(&h->d_WOt, WOt.data(), WOt.size() * 2, cs)) != WQ_OK) return bail(st);
+    if (cudaMalloc(&h->d_err, sizeof(int)) != cudaSuccess) return bail(fail(WQ_ERR_OOM, "cudaMalloc failed"));
+    if (cudaMemsetAsync(h->d_err, 0, sizeof(int), cs) != cudaSuccess) return bail(fail(WQ_ERR_CUDA, "memset"));
+    if (cudaStreamSynchronize(cs) != cudaSuccess) return bail(fail(WQ_ERR_CUDA, "upload synchronise failed"));
+
+    const char* why = "";
+    if (!wq::encode_tmap_2d(&h->tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, h->d_codes, K / 2, N, K / 2, 128, 128,
+                            CU_TENSOR_MAP_SWIZZLE_128B, &why))
+        return bail(fail(WQ_ERR_CUDA, why));
+    if (r && !wq::encode_tmap_2d(&h->tmQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h->d_Qt, r, N, 2 * r, r, 128,
+                                 swizzle_for_row_bytes(2 * r), &why))
+        return bail(fail(WQ_ERR_CUDA, why));
+    if (no && !wq::encode_tmap_2d(&h->tmWO, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, h->d_WOt, no, N, 2 * no, no, 128,
+                                  swizzle_for_row_bytes(2 * no), &why))
+        return bail(fail(WQ_ERR_CUDA, why));
+    *out = h;
+    return WQ_OK;
+}
+
+WQ_API size_t wq_workspace_bytes(wq_weights_t h, int M) {
+    if (!h || M < 0) return 0;
+    return wq::carve_workspace(nullptr, M, h->cfg.K, h->cfg.rank, h->cfg.n_outliers).bytes;
+}
+
+WQ_API size_t wq_host_workspace_bytes(wq_weights_t h, int M) {
+    if (!h || M < 0) return 0;
+    return wq_workspace_bytes(h, M) + align_up(static_cast<size_t>(M) * h->cfg.K * 2, 1024) +
+           align_up(static_cast<size_t>(M) * h->cfg.N * 2, 1024);
+}
+
+static wq_status run_quant(wq_weights_t h, const void* x, int M, int layout, uint8_t* codes, uint8_t* sf, float* g,
+                           uint16_t* xo, uint16_t* u, cudaStream_t st) {
+    wq::QuantArgs qa{};
+    qa.x = x;
+    qa.M = M;
+    qa.K = h->cfg.K;
+    qa.inv_s = h->d_inv_s;
+    qa.rotate = h->cfg.rotate;
+    qa.omega_pos = h->d_omega_pos;
+    qa.n_out = xo ? h->cfg.n_outliers : 0;
+    qa.xo = xo;
+    qa.P = h->d_P;
+    qa.r = u ? h->cfg.rank : 0;
+    qa.u = u;
+    qa.codes = codes;
+    qa.sf = sf;
+    qa.sf_layout = layout;
+    qa.g = g;
+    const cudaError_t e = wq::launch_quantize_act(qa, st);
+    if (e != cudaSuccess) return cuda_fail(e, "activation quantiser launch");
+    return WQ_OK;
+}
+
+WQ_API wq_status wq_quantize_activations(wq_weights_t h, const void* x, int M, int scale_layout, uint8_t* codes,
+                                         uint8_t* scales, float* gscale, void* x_omega, void* u, void* stream) {
+    if (!h) return fail(WQ_ERR_INVALID, "NULL handle");
+    if (M < 0) return fail(WQ_ERR_INVALID, "M < 0");
+    if (M == 0) return WQ_OK;
+    if (!x || !codes || !scales || !gscale) return fail(WQ_ERR_INVALID, "NULL buffer");
+    if (h->cfg.n_outliers > 0 && !x_omega)
+        return fail(WQ_ERR_INVALID, "x_omega is required when n_outliers > 0 (the kept channels are zeroed)");
+    if (scale_layout != WQ_SCALE_LAYOUT_ROWMAJOR && scale_layout != WQ_SCALE_LAYOUT_MMA)
+        return fail(WQ_ERR_INVALID, "bad scale_layout");
+    if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(codes) | reinterpret_cast<uintptr_t>(scales)) & 15)
+        return fail(WQ_ERR_INVALID, "device buffers must be 16-byte aligned");
+    return run_quant(h, x, M, scale_layout, codes, scales, gscale,
+                     h->cfg.n_outliers ? static_cast<uint16_t*>(x_omega) : nullptr,
+                     h->cfg.rank ? static_cast<uint16_t*>(u) : nullptr, static_cast<cudaStream_t>(stream));
+}
+
+WQ_API wq_status wq_linear_forward(wq_weights_t h, const void* x, int M, void* y, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+    if (!h) return fail(WQ_ERR_INVALID, "NULL handle");
+    if (M < 0) return fail(WQ_ERR_INVALID, "M < 0");
+    if (M == 0) return WQ_OK;
+    if (!x || !y || !workspace) return fail(WQ_ERR_INVALID, "NULL buffer");
+    if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15)
+        return fail(WQ_ERR_INVALID, "x and y must be 16-byte aligned");
+    if (reinterpret_cast<uintptr_t>(workspace) & 255) return fail(WQ_ERR_INVALID, "workspace must be 256-byte aligned");
+    const int K = h->cfg.K, N = h->cfg.N, r = h->cfg.rank, no = h->cfg.n_outliers;
+    const wq::ActWorkspace ws = wq::carve_workspace(workspace, M, K, r, no);
+    if (workspace_bytes < ws.bytes) return fail(WQ_ERR_INVALID, "workspace too small");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    wq_status s = run_quant(h, x, M, WQ_SCALE_LAYOUT_MMA, ws.codes, ws.sf, ws.g, no ? ws.xo : nullptr,
+                            r ? ws.u : nullptr, st);
+    if (s != WQ_OK) return s;
+
+    wq::GemmArgs ga{};
+    {
+        std::lock_guard<std::mutex> lk(h->mu);
+        if (h->key_ws != workspace || h->key_y != y || h->key_M != M) {
+            const char* why = "";
+            bool ok = wq::encode_tmap_2d(&h->tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, ws.codes, K / 2, M, K / 2, 128, 128,
+                                         CU_TENSOR_MAP_SWIZZLE_128B, &why) &&
+                      wq::encode_tmap_2d(&h->tmY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, y, N, M, 2ull * N, 64, 32,
+                                         CU_TENSOR_MAP_SWIZZLE_128B, &why);
+            if (ok && r)
+                ok = wq::encode_tmap_2d(&h->tmU, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ws.u, r, M, 2 * r, r, 128,
+                                        swizzle_for_row_bytes(2 * r), &why);
+            if (ok && no)
+                ok = wq::encode_tmap_2d(&h->tmXO, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws.xo, no, M, 2 * no, no, 128,
+                                        swizzle_for_row_bytes(2 * no), &why);
+            if (!ok) {
+                h->key_ws = nullptr;
+                return fail(WQ_ERR_CUDA, why);
+            }
+            h->key_ws = workspace;
+            h->key_y = y;
+            h->key_M = M;
+        }
+        ga.M = M; ga.N = N; ga.K = K; ga.r = r; ga.n_out = no;
+        ga.tmA = &h->tmA; ga.tmB = &h->tmB; ga.tmU = &h->tmU; ga.tmQ = &h->tmQ;
+        ga.tmXO = &h->tmXO; ga.tmWO = &h->tmWO; ga.tmY = &h->tmY;
+        ga.sfa = ws.sf; ga.sfb = h->d_sf; ga.gA = ws.g; ga.gW = h->gW; ga.bias = h->d_bias;
+        ga.err = h->d_err; ga.num_sms = h->num_sms;
+        const cudaError_t e = wq::launch_gemm(ga, st);
+        if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
+    }
+    return WQ_OK;
+}
+
+WQ_API wq_status wq_linear_forward_host(wq_weights_t h, const void* x_host, int M, void* y_host, void* workspace,
+                                        size_t workspace_bytes, void* stream) {
+    if (!h) return fail(WQ_ERR_INVALID, "NULL handle");
+    if (M < 0) return fail(WQ_ERR_INVALID, "M < 0");
+    if (M == 0) return WQ_OK;
+    if (!x_host || !y_host || !workspace) return fail(WQ_ERR_INVALID, "NULL buffer");
+    if (workspace_bytes < wq_host_workspace_bytes(h, M)) return fail(WQ_ERR_INVALID, "workspace too small");
+    const size_t wsb = wq_workspace_bytes(h, M);
+    const size_t xb = static_cast<size_t>(M) * h->cfg.K * 2, yb = static_cast<size_t>(M) * h->cfg.N * 2;
+    uint8_t* base = static_cast<uint8_t*>(workspace);
+    void* dx = base + wsb;
+    void* dy = base + wsb + align_up(xb, 1024);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    WQ_CUDA(cudaMemcpyAsync(dx, x_host, xb, cudaMemcpyHostToDevice, st), "x upload");
+    const wq_status s = wq_linear_forward(h, dx, M, dy, workspace, wsb, stream);
+    if (s != WQ_OK) return s;
+    WQ_CUDA(cudaMemcpyAsync(y_host, dy, yb, cudaMemcpyDeviceToHost, st), "y download");
+    return WQ_OK;
+}
+
+WQ_API wq_status wq_export_weights(wq_weights_t h, uint8_t* codes, uint8_t* scales, float* gW, uint16_t* P,
+                                   uint16_t* Q, uint16_t* W_omega) {
+    if (!h) return fail(WQ_ERR_INVALID, "NULL handle");
+    const int K = h->cfg.K, N = h->cfg.N, r = h->cfg.rank, no = h->cfg.n_outliers;
+    if (codes) WQ_CUDA(cudaMemcpy(codes, h->d_codes, static_cast<size_t>(N) * K / 2, cudaMemcpyDeviceToHost), "export");
+    if (scales) {
+        const size_t n_pad = align_up(static_cast<size_t>(N), wq::kBlockM);
+        std::vector<uint8_t> sf(n_pad / wq::kBlockM * (K / 64) * wq::kSfAtom);
+        WQ_CUDA(cudaMemcpy(sf.data(), h->d_sf, sf.size(), cudaMemcpyDeviceToHost), "export");
+        for (int n = 0; n < N; ++n)
+            for (int b = 0; b < K / 16; ++b)
+                scales[static_cast<size_t>(n) * (K / 16) + b] =
+                    sf[((static_cast<size_t>(n) / 128) * (K / 64) + b / 4) * wq::kSfAtom + (n % 32) * 16 +
+                       ((n % 128) / 32) * 4 + (b % 4)];
+    }
+    if (gW) *gW = h->gW;
+    if (P && r) WQ_CUDA(cudaMemcpy(P, h->d_P, static_cast<size_t>(K) * r * 2, cudaMemcpyDeviceToHost), "export");
+    if (Q && r) {
+        std::vector<uint16_t> qt(static_cast<size_t>(N) * r);
+        WQ_CUDA(cudaMemcpy(qt.data(), h->d_Qt, qt.size() * 2, cudaMemcpyDeviceToHost), "export");
+        for (int n = 0; n < N; ++n)
+            for (int j = 0; j < r; ++j) Q[static_cast<size_t>(j) * N + n] = qt[static_cast<size_t>(n) * r + j];
+    }
+    if (W_omega && no) {
+        std::vector<uint16_t> wt(static_cast<size_t>(N) * no);
+        WQ_CUDA(cudaMemcpy(wt.data(), h->d_WOt, wt.size() * 2, cudaMemcpyDeviceToHost), "export");
+        for (int n = 0; n < N; ++n)
+            for (int j = 0; j < no; ++j) W_omega[static_cast<size_t>(j) * N + n] = wt[static_cast<size_t>(n) * no + j];
+    }
+    return WQ_OK;
+}
+
+WQ_API wq_status wq_check_device_error(wq_weights_t h, void* stream) {
+    if (!h) return fail(WQ_ERR_INVALID, "NULL handle");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    WQ_CUDA(cudaStreamSynchronize(st), "stream synchronise");
+    int v = 0;
+    WQ_CUDA(cudaMemcpy(&v, h->d_err, sizeof(int), cudaMemcpyDeviceToHost), "error flag read");
+    if (v != 0) {
+        WQ_CUDA(cudaMemset(h->d_err, 0, sizeof(int)), "error flag clear");
+        return fail(WQ_ERR_TIMEOUT, "kernel barrier wait timed out (site " + std::to_string(v) + ")");
+    }
+    return WQ_OK;
+}
+
+WQ_API void wq_free_weights(wq_weights_t h) {
+    if (!h) return;
+    cudaDeviceSynchronize();
+    free_device(h);
+    delete h;
+}
+
+}  // extern "C"

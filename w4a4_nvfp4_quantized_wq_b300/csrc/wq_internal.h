@@ -1,0 +1,73 @@
+// wq_internal.h -- internal declarations shared by the host API and the kernel launchers.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/wq.h"
+
+namespace wq {
+
+constexpr int kBlockM = 128;        // GEMM tile rows (tcgen05 M)
+constexpr int kBlockN = 128;        // GEMM tile columns (tcgen05 N)
+constexpr int kStageK = 256;        // K elements per pipeline stage (128 bytes of fp4)
+constexpr int kSfAtom = 512;        // bytes of one 128-row x 64-K block-scale atom
+
+// Device-side layout of one activation workspace for M rows.
+struct ActWorkspace {
+    uint8_t* codes = nullptr;       // [M, K/2]
+    uint8_t* sf = nullptr;          // MMA layout, ceil(M/128) * K/64 atoms
+    float* g = nullptr;             // [M]
+    uint16_t* u = nullptr;          // [M, r] bf16
+    uint16_t* xo = nullptr;         // [M, n_outliers] fp16
+    size_t bytes = 0;
+};
+
+ActWorkspace carve_workspace(void* base, int M, int K, int r, int n_out);
+
+struct QuantArgs {
+    const void* x;                  // bf16 [M, K]
+    int M, K;
+    const float* inv_s;             // [K] or null
+    int rotate;
+    const int16_t* omega_pos;       // [K] -1 or slot, null when n_out == 0
+    int n_out;
+    uint16_t* xo;                   // fp16 [M, n_out]
+    const uint16_t* P;              // bf16 [K, r]
+    int r;
+    uint16_t* u;                    // bf16 [M, r]
+    uint8_t* codes;                 // [M, K/2]
+    uint8_t* sf;                    // scales, layout per `sf_layout`
+    int sf_layout;                  // WQ_SCALE_LAYOUT_*
+    float* g;                       // [M]
+};
+
+cudaError_t launch_quantize_act(const QuantArgs& a, cudaStream_t stream);
+
+struct GemmArgs {
+    int M, N, K, r, n_out;
+    const CUtensorMap* tmA;   // activation codes [M, K/2] u8, box 128x128, swizzle 128B
+    const CUtensorMap* tmB;   // weight codes     [N, K/2] u8, box 128x128, swizzle 128B
+    const CUtensorMap* tmU;   // U      [M, r]     bf16, box r x 128
+    const CUtensorMap* tmQ;   // Q^T    [N, r]     bf16, box r x 128
+    const CUtensorMap* tmXO;  // x_O    [M, n_out] fp16, box n_out x 128
+    const CUtensorMap* tmWO;  // W_O^T  [N, n_out] fp16, box n_out x 128
+    const CUtensorMap* tmY;   // y      [M, N]     bf16, box 64 x 32, swizzle 128B
+    const uint8_t* sfa;       // activation scales, MMA layout
+    const uint8_t* sfb;       // weight scales, MMA layout
+    const float* gA;          // [M]
+    float gW;
+    const float* bias;        // [N] or null
+    int* err;                 // device error flag
+    int num_sms;
+};
+
+cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream);
+
+// cuTensorMapEncodeTiled obtained from the driver at run time (no libcuda link).
+bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
+                    uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                    CUtensorMapSwizzle swizzle, const char** why);
+
+}  // namespace wq
