@@ -1,0 +1,463 @@
+#!/usr/bin/env python
+"""Benchmark of the W4A4 NVFP4 fused projection (one JSON line on rank 0).
+
+Default workload: the action-expert projections at batch 1 (M = 50 tokens; up
+1024 -> 4096 and down 4096 -> 1024; rank-32 low-rank branch; block-64 FWHT;
+eight outlier channels x20), seeded synthetic inputs.  A step is one pass of the
+whole hot path over the batch: for every layer the fused activation quantiser and
+the tcgen05 NVFP4 GEMM with its fused epilogue (two kernels per layer), replayed as
+one CUDA graph.  L2 is flushed (a 256 MiB write) before every timed step, outside
+the step's CUDA events, so weights and activations come from HBM.
+
+--impl reference times the CPU oracle (the slow, plain reference implementation)
+on the same workload, a bounded row sample per step, on the host cores.
+Multi-GPU (torchrun): every rank runs an independent replica of the workload on its
+own GPU (weak scaling, no collective on the data path); rank 0 prints the line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "W4A4 NVFP4 fused-projection TFLOPS & tokens/s; % of FP4/HBM roofline"
+FLUSH_BYTES = 256 << 20
+WORKLOAD_TEXT = {
+    "expert": "action-expert projections, batch 1: M=50 tokens, up 1024->4096 + down 4096->1024, "
+              "rank-32 bf16 branch, block-64 FWHT, smoothing, NVFP4 W4A4",
+    "video_dit": "video DiT block: M=16384 tokens, QKV 1536->4608, o 1536->1536, up 1536->8960, "
+                 "down 8960->1536, rank 32, 64 fp16 outlier channels, NVFP4 W4A4",
+    "tiny": "single projection M=8, K=256 -> N=512, rank 16",
+    "backbone": "language backbone prefill M=768: QKV 2048->6144 and gate/up 2048->32768 (W4A4 layers)",
+}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["wq", "reference"], default="wq")
+    ap.add_argument("--workload", default="expert", choices=list(WORKLOAD_TEXT))
+    ap.add_argument("--kernel-iters", type=int, default=200)
+    ap.add_argument("--cpu-baseline-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return ws, int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def layers_of(name):
+    import workloads as wl
+    w = wl.WORKLOADS[name]
+    idx = [i for i, s in enumerate(w.layers) if s.mode == "w4a4"]
+    return w, idx
+
+
+class ClockSampler:
+    """Samples SM clock and throttle reasons through NVML while the timed region runs."""
+
+    REASONS = {"hw_slowdown": 0x8, "hw_thermal_slowdown": 0x40, "sw_thermal_slowdown": 0x20,
+               "sw_power_cap": 0x4, "hw_power_brake_slowdown": 0x80}
+
+    def __init__(self, dev_index: int):
+        self.samples, self.reasons, self.ok = [], set(), False
+        self.max_mhz = None
+        self._stop = threading.Event()
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self._nv = pynvml
+            self._h = pynvml.nvmlDeviceGetHandleByIndex(dev_index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception:
+            self.ok = False
+
+    def _run(self):
+        nv = self._nv
+        while not self._stop.is_set():
+            try:
+                self.samples.append(nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM))
+                fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                    getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+                r = fn(self._h)
+                for k, bit in self.REASONS.items():
+                    if r & bit:
+                        self.reasons.add(k)
+            except Exception:
+                pass
+            time.sleep(0.002)
+
+    def __enter__(self):
+        if self.ok:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        self._stop.set()
+        if self.ok:
+            self._t.join()
+
+    def record(self):
+        return {"sm_mhz": float(statistics.median(self.samples)) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+                "samples": len(self.samples), "source": "NVML" if self.ok else "unavailable"}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
+
+
+def gemm_algorithmic_bytes(M, K, N, r, n_out, bias):
+    """Bytes the fused GEMM must move once: fp4 codes + e4m3 scales of A and W, row scales,
+    the 16-bit side operands, bias and the bf16 output."""
+    a = M * K // 2 + M * K // 16 + 4 * M
+    w = N * K // 2 + N * K // 16
+    side = 2 * M * r + 2 * N * r + 2 * M * n_out + 2 * N * n_out
+    return a + w + side + (4 * N if bias else 0) + 2 * M * N
+
+
+def quant_algorithmic_bytes(M, K, r, n_out, smooth):
+    """Bytes of the activation quantiser: bf16 x in, fp4 codes + scales + row scale out,
+    the low-rank factor, U and x_O out."""
+    return 2 * M * K + M * K // 2 + M * K // 16 + 4 * M + 2 * K * r + 2 * M * r + 2 * M * n_out + \
+        (4 * K if smooth else 0)
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("ptx.cuh", "wq_gemm.cu", "wq_quant.cu"):
+        h.update(open(os.path.join(ROOT, "w4a4_nvfp4_quantized_wq_b300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """dram bytes per launch from the committed ncu summary, if it was taken on this source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+        e = d.get(workload, {}).get(kernel)
+        if e and e.get("source_hash") == kernel_source_hash():
+            return e.get("dram_bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+# ------------------------------------------------------------------ oracle (CPU) timing
+def oracle_layer_data(name):
+    import workloads as wl
+    w, idx = layers_of(name)
+    return [wl.make_layer_inputs(name, layer=i) for i in idx]
+
+
+def time_oracle(layers, budget_s: float, n_threads: int, min_passes=1):
+    """Time the oracle's per-token work (quantiser, low-rank, forward) on row samples;
+    returns (tokens/s, rows per pass, passes, seconds)."""
+    import oracle
+    prepared = [(L, oracle.prepare_weights(L.W, L.s, L.L1, L.L2, L.omega, L.rotate, n_threads)) for L in layers]
+
+    def one(rows):
+        for L, wqo in prepared:
+            xb = L.x_bits[rows]
+            aq = oracle.quantize_act(xb, L.s, L.rotate, L.omega, n_threads=n_threads)
+            U = oracle.lowrank_act(xb, wqo.P) if wqo.P.shape[1] else None
+            oracle.linear_forward(aq, wqo, U, L.bias, n_threads=n_threads)
+
+    M = layers[0].M
+    t0 = time.perf_counter()
+    one(np.arange(min(M, 8)))
+    t_row = (time.perf_counter() - t0) / min(M, 8)
+    rows_per_pass = int(max(1, min(M, budget_s / max(t_row, 1e-9) / max(min_passes, 1))))
+    rows = np.sort(np.random.default_rng(7).choice(M, size=rows_per_pass, replace=False))
+    passes, t0 = 0, time.perf_counter()
+    while True:
+        one(rows)
+        passes += 1
+        el = time.perf_counter() - t0
+        if passes >= min_passes and el >= budget_s * 0.5:
+            break
+        if el > budget_s * 3:
+            break
+    el = time.perf_counter() - t0
+    return rows_per_pass * passes / el, rows_per_pass, passes, el
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    n_threads = os.cpu_count() or 1
+    layers = oracle_layer_data(args.workload)
+    import oracle as orc
+    prepared = [(L, orc.prepare_weights(L.W, L.s, L.L1, L.L2, L.omega, L.rotate, n_threads)) for L in layers]
+    M = layers[0].M
+    # size each step's row sample so that warmup + steps fit in about a minute
+    t0 = time.perf_counter()
+    rows = np.arange(min(M, 4))
+
+    def step(rows):
+        for L, wqo in prepared:
+            xb = L.x_bits[rows]
+            aq = orc.quantize_act(xb, L.s, L.rotate, L.omega, n_threads=n_threads)
+            U = orc.lowrank_act(xb, wqo.P) if wqo.P.shape[1] else None
+            orc.linear_forward(aq, wqo, U, L.bias, n_threads=n_threads)
+
+    step(rows)
+    t_row = (time.perf_counter() - t0) / len(rows)
+    per_step = 60.0 / max(1, args.steps + args.warmup)
+    n_rows = int(max(1, min(M, per_step / max(t_row, 1e-9))))
+    rng = np.random.default_rng(11)
+    for _ in range(args.warmup):
+        step(np.sort(rng.choice(M, n_rows, replace=False)))
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step(np.sort(rng.choice(M, n_rows, replace=False)))
+    el = time.perf_counter() - t0
+    tok_s = n_rows * args.steps / el
+    flops = sum(2.0 * n_rows * L.spec.K * L.spec.N for L in layers) * args.steps
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tok_s, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)", "tflops": flops / el / 1e12,
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "M": M, "rows_per_step": n_rows},
+        "cpu_baseline": {"value": tok_s, "unit": "tokens/s", "cores": n_threads, "kind": "oracle",
+                         "sample": f"{n_rows} of {M} rows per step, all layers, {args.steps} steps"},
+        "e2e": {"value": tok_s, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_wq(args):
+    import torch
+    ws, rank, local_rank = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    from w4a4_nvfp4_quantized_wq_b300 import build as wqbuild
+    wqbuild.build_library()
+    import w4a4_nvfp4_quantized_wq_b300 as wq
+    import workloads as wl
+
+    wlw, idx = layers_of(args.workload)
+    layers = [wl.make_layer_inputs(args.workload, layer=i) for i in idx]
+    M = wlw.M
+    stream = torch.cuda.Stream(device=dev)
+    H = []
+    for L in layers:
+        w = wq.wq_prepare_weights(L.spec.K, L.spec.N, L.W, L.bias, L.s, L.L1, L.L2,
+                                  L.omega if L.omega.size else None, rotate=L.rotate)
+        x = torch.from_numpy(L.x_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+        y = torch.empty((M, L.spec.N), dtype=torch.bfloat16, device=dev)
+        wsb = torch.empty(max(256, wq.wq_workspace_bytes(w, M)), dtype=torch.uint8, device=dev)
+        H.append(dict(L=L, w=w, x=x, y=y, ws=wsb))
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step():
+        for h in H:
+            wq.wq_linear_forward(h["w"], h["x"], h["y"], h["ws"], stream)
+
+    with torch.cuda.stream(stream):
+        step()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+    torch.cuda.synchronize()
+    for h in H:
+        wq.wq_check_device_error(h["w"])
+
+    # ---------------- timed region: exactly K steps
+    K, W = args.steps, args.warmup
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    with torch.cuda.stream(stream):
+        for _ in range(W):
+            flush.zero_()
+            graph.replay()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local_rank)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    with sampler:
+        with torch.cuda.stream(stream):
+            for i in range(K):
+                flush.zero_()
+                ev[i][0].record(stream)
+                graph.replay()
+                ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = float(sum(step_ms))
+    if ws > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+        dist.barrier()
+    for h in H:
+        wq.wq_check_device_error(h["w"])
+    tokens = M * K * ws
+    tok_s = tokens / (total_ms / 1e3)
+    flops_step = sum(2.0 * M * h["L"].spec.K * h["L"].spec.N for h in H)
+    tflops = flops_step * K * ws / (total_ms / 1e3) / 1e12
+
+    # ---------------- per-kernel timing (roofline of the dominant kernel)
+    iters = args.kernel_iters
+    per_kernel = {}
+    for li, h in enumerate(H):
+        L, w = h["L"], h["w"]
+        codes, sf, g, xo, u = wq.wq_quantize_activations(h["w"], h["x"], wq.WQ_SCALE_LAYOUT_MMA, stream)
+        torch.cuda.synchronize()
+        for kname in ("quant", "gemm"):
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+            with torch.cuda.stream(stream):
+                for i in range(iters + 3):
+                    flush.zero_()
+                    if i >= 3:
+                        evs[i - 3][0].record(stream)
+                    if kname == "quant":
+                        wq.wq_quantize_activations_into(w, h["x"], codes, sf, g, xo, u, stream)
+                    else:
+                        wq.wq_linear_forward_quantized(w, codes, sf, g, u, xo, h["y"], stream)
+                    if i >= 3:
+                        evs[i - 3][1].record(stream)
+            torch.cuda.synchronize()
+            ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+            spec = L.spec
+            if kname == "gemm":
+                byts = gemm_algorithmic_bytes(M, spec.K, spec.N, L.rank, L.omega.size, L.bias is not None)
+                flops = 2.0 * M * spec.K * spec.N
+            else:
+                byts = quant_algorithmic_bytes(M, spec.K, L.rank, L.omega.size, L.s is not None)
+                flops = 0.0
+            per_kernel[(kname, li)] = dict(ms=ms, bytes=byts, flops=flops)
+    tot = {k: sum(v["ms"] for (kk, _), v in per_kernel.items() if kk == k) for k in ("quant", "gemm")}
+    dom = max(tot, key=tot.get)
+    dom_ms = tot[dom]
+    dom_bytes = sum(v["bytes"] for (kk, _), v in per_kernel.items() if kk == dom)
+    dom_flops = sum(v["flops"] for (kk, _), v in per_kernel.items() if kk == dom)
+    peaks, peak_kind = measured_peaks()
+    n_launch = len(H)
+    hbm_achieved = dom_bytes / (dom_ms / 1e3) / 1e9
+    roofline = {"kernel": "nvfp4_gemm_kernel" if dom == "gemm" else "quantize_act_kernel",
+                "bound": "hbm", "achieved": hbm_achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": hbm_achieved / peaks["hbm_gbs"],
+                "traffic": profiled_traffic(dom, args.workload),
+                "peak_source": f"{peak_kind} HBM copy bandwidth",
+                "bytes_per_launch": dom_bytes / n_launch, "us_per_launch": 1e3 * dom_ms / n_launch,
+                "share_of_kernel_time": dom_ms / sum(tot.values())}
+    if dom == "gemm" and dom_flops:
+        fp4_peak = peaks.get("bf16_tflops", 1800.0) * 6.0   # nominal fp4 : bf16 dense ratio 13.5 : 2.25
+        achieved_tf = dom_flops / (dom_ms / 1e3) / 1e12
+        roofline["fp4_tensor"] = {"achieved": achieved_tf, "peak": fp4_peak, "unit": "TFLOP/s",
+                                  "frac": achieved_tf / fp4_peak,
+                                  "peak_source": f"{peak_kind} bf16 x 6 (nominal fp4:bf16 ratio)"}
+    kernels = {f"{k}[{wlw.layers[idx[li]].name}]": {"us": 1e3 * v["ms"], "bytes": v["bytes"],
+                                                   "GB/s": v["bytes"] / (v["ms"] / 1e3) / 1e9}
+               for (k, li), v in per_kernel.items()}
+
+    # ---------------- end to end through the host-buffer entry point
+    e2e = None
+    try:
+        hb = []
+        for h in H:
+            L = h["L"]
+            xh = h["x"].cpu().pin_memory()
+            yh = torch.empty((M, L.spec.N), dtype=torch.bfloat16).pin_memory()
+            wsh = torch.empty(wq.wq_host_workspace_bytes(h["w"], M), dtype=torch.uint8, device=dev)
+            hb.append((h["w"], xh, yh, wsh))
+        ke = max(10, min(K, 500))
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(ke)]
+        with torch.cuda.stream(stream):
+            for i in range(ke + 3):
+                flush.zero_()
+                if i >= 3:
+                    evs[i - 3][0].record(stream)
+                for w, xh, yh, wsh in hb:
+                    wq.wq_linear_forward_host(w, xh, yh, wsh, stream)
+                if i >= 3:
+                    evs[i - 3][1].record(stream)
+        torch.cuda.synchronize()
+        e_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+        e2e = {"value": M * ws / (e_ms / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": sum(2 * M * h["L"].spec.K for h in H),
+               "d2h_bytes_per_step": sum(2 * M * h["L"].spec.N for h in H),
+               "ms_per_step": e_ms, "api": "wq_linear_forward_host (pinned host x and y)"}
+    except Exception as exc:  # reported, not hidden
+        e2e = {"value": None, "unit": "tokens/s", "error": repr(exc)}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline and ws == 1:
+        n_threads = os.cpu_count() or 1
+        try:
+            tps, rows, passes, el = time_oracle(layers, args.cpu_baseline_seconds, n_threads)
+            cpu = {"value": tps, "unit": "tokens/s", "cores": n_threads, "kind": "oracle",
+                   "sample": f"{rows} of {M} rows x {passes} passes over all {len(layers)} layers "
+                             f"({el:.1f} s, weights prepared beforehand)"}
+        except Exception as exc:
+            cpu = {"value": None, "error": repr(exc)}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": tok_s, "unit": "tokens/s", "n_gpus": ws, "steps": K, "warmup": W,
+            "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "nvfp4 (e2m1 x e2m1, ue4m3 scales, f32 accumulate)", "data": "synthetic (seeded)",
+            "tflops": tflops,
+            "config": {"workload": WORKLOAD_TEXT[args.workload], "M": M,
+                       "layers": [f"{h['L'].spec.name} {h['L'].spec.K}->{h['L'].spec.N}" for h in H],
+                       "l2": "flushed before every step (256 MiB write, outside the step events)",
+                       "parallelism": f"replicas x{ws}", "cuda_graph": True},
+            "roofline": roofline, "kernels": kernels,
+            "cpu_baseline": cpu, "e2e": e2e,
+            "clocks": sampler.record(),
+            "gpu_launches": 2 * len(H) * K,
+            "wall_s_timed_region": wall,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_wq(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -144,6 +144,17 @@ WQ_API wq_status wq_quantize_activations(wq_weights_t h, const void *x, int M, i
                                          void *x_omega, void *u, void *stream);
 
 /*
+ * GEMM + fused epilogue alone, on activations already quantised by
+ * wq_quantize_activations(..., WQ_SCALE_LAYOUT_MMA, ...).  All pointers are device:
+ *   codes [M, K/2], scales_mma (MMA layout), gscale [M], u bf16 [M, rank] (required when
+ *   rank > 0), x_omega fp16 [M, n_outliers] (required when n_outliers > 0), y bf16 [M, N].
+ * One kernel runs on `stream`.
+ */
+WQ_API wq_status wq_linear_forward_quantized(wq_weights_t h, const uint8_t *codes, const uint8_t *scales_mma,
+                                             const float *gscale, const void *u, const void *x_omega, int M,
+                                             void *y, void *stream);
+
+/*
  * Copy the prepared weights back to host memory in canonical layouts (synchronous):
  *   codes uint8 [N, K/2]; scales e4m3 [N, K/16]; gW fp32 scalar; P bf16 [K, r];
  *   Q bf16 [r, N]; W_omega fp16 [n_outliers, N].  Any output may be NULL.

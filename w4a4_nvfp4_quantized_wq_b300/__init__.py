@@ -23,6 +23,7 @@ WQ_SCALE_LAYOUT_ROWMAJOR, WQ_SCALE_LAYOUT_MMA = 0, 1
 
 EXPORTED = ["wq_prepare_weights", "wq_get_config", "wq_workspace_bytes", "wq_linear_forward",
             "wq_host_workspace_bytes", "wq_linear_forward_host", "wq_quantize_activations",
+            "wq_linear_forward_quantized",
             "wq_export_weights", "wq_check_device_error", "wq_free_weights", "wq_last_error"]
 
 
@@ -63,6 +64,8 @@ def lib() -> ctypes.CDLL:
         L.wq_linear_forward_host.restype = I
         L.wq_quantize_activations.argtypes = [P, P, I, I, P, P, P, P, P, P]
         L.wq_quantize_activations.restype = I
+        L.wq_linear_forward_quantized.argtypes = [P, P, P, P, P, P, I, P, P]
+        L.wq_linear_forward_quantized.restype = I
         L.wq_export_weights.argtypes = [P, P, P, P, P, P, P]
         L.wq_export_weights.restype = I
         L.wq_check_device_error.argtypes = [P, P]
@@ -201,6 +204,27 @@ def wq_quantize_activations(w: Weights, x, scale_layout: int = WQ_SCALE_LAYOUT_R
         ctypes.c_void_p(xo.data_ptr() if xo is not None else None),
         ctypes.c_void_p(u.data_ptr() if u is not None else None), ctypes.c_void_p(_stream_ptr(stream))))
     return codes, scales, g, xo, u
+
+
+def wq_quantize_activations_into(w: Weights, x, codes, scales, g, x_omega=None, u=None,
+                                 stream=None, scale_layout: int = WQ_SCALE_LAYOUT_MMA):
+    """wq_quantize_activations into caller-owned device tensors."""
+    ptr = lambda t: ctypes.c_void_p(t.data_ptr() if t is not None else None)
+    _check(lib().wq_quantize_activations(ctypes.c_void_p(w.handle), ptr(x), x.shape[0], int(scale_layout),
+                                         ptr(codes), ptr(scales), ptr(g), ptr(x_omega), ptr(u),
+                                         ctypes.c_void_p(_stream_ptr(stream))))
+
+
+def wq_linear_forward_quantized(w: Weights, codes, scales_mma, g, u=None, x_omega=None, y=None, stream=None):
+    """GEMM + epilogue on activations quantised with WQ_SCALE_LAYOUT_MMA (device tensors)."""
+    import torch
+    M = codes.shape[0]
+    if y is None:
+        y = torch.empty((M, w.N), dtype=torch.bfloat16, device=codes.device)
+    ptr = lambda t: ctypes.c_void_p(t.data_ptr() if t is not None else None)
+    _check(lib().wq_linear_forward_quantized(ctypes.c_void_p(w.handle), ptr(codes), ptr(scales_mma), ptr(g),
+                                             ptr(u), ptr(x_omega), M, ptr(y), ctypes.c_void_p(_stream_ptr(stream))))
+    return y
 
 
 def wq_export_weights(w: Weights) -> dict:

@@ -158,7 +158,9 @@ struct wq_weights {
     CUtensorMap tmB{}, tmQ{}, tmWO{};
     // activation / output tensor maps, re-encoded when the buffers change
     std::mutex mu;
-    const void* key_ws = nullptr;
+    const void* key_codes = nullptr;
+    const void* key_u = nullptr;
+    const void* key_xo = nullptr;
     const void* key_y = nullptr;
     int key_M = -1;
     CUtensorMap tmA{}, tmU{}, tmXO{}, tmY{};
@@ -405,6 +407,43 @@ WQ_API wq_status wq_quantize_activations(wq_weights_t h, const void* x, int M, i
                      h->cfg.rank ? static_cast<uint16_t*>(u) : nullptr, static_cast<cudaStream_t>(stream));
 }
 
+static wq_status run_gemm(wq_weights_t h, const uint8_t* codes, const uint8_t* sf, const float* g,
+                          const uint16_t* u, const uint16_t* xo, int M, void* y, cudaStream_t st) {
+    const int K = h->cfg.K, N = h->cfg.N, r = h->cfg.rank, no = h->cfg.n_outliers;
+    std::lock_guard<std::mutex> lk(h->mu);
+    if (h->key_codes != codes || h->key_u != u || h->key_xo != xo || h->key_y != y || h->key_M != M) {
+        const char* why = "";
+        bool ok = wq::encode_tmap_2d(&h->tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, K / 2, M, K / 2, 128, 128,
+                                     CU_TENSOR_MAP_SWIZZLE_128B, &why) &&
+                  wq::encode_tmap_2d(&h->tmY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, y, N, M, 2ull * N, 64, 32,
+                                     CU_TENSOR_MAP_SWIZZLE_128B, &why);
+        if (ok && r)
+            ok = wq::encode_tmap_2d(&h->tmU, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, u, r, M, 2 * r, r, 128,
+                                    swizzle_for_row_bytes(2 * r), &why);
+        if (ok && no)
+            ok = wq::encode_tmap_2d(&h->tmXO, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xo, no, M, 2 * no, no, 128,
+                                    swizzle_for_row_bytes(2 * no), &why);
+        if (!ok) {
+            h->key_codes = nullptr;
+            return fail(WQ_ERR_CUDA, why);
+        }
+        h->key_codes = codes;
+        h->key_u = u;
+        h->key_xo = xo;
+        h->key_y = y;
+        h->key_M = M;
+    }
+    wq::GemmArgs ga{};
+    ga.M = M; ga.N = N; ga.K = K; ga.r = r; ga.n_out = no;
+    ga.tmA = &h->tmA; ga.tmB = &h->tmB; ga.tmU = &h->tmU; ga.tmQ = &h->tmQ;
+    ga.tmXO = &h->tmXO; ga.tmWO = &h->tmWO; ga.tmY = &h->tmY;
+    ga.sfa = sf; ga.sfb = h->d_sf; ga.gA = g; ga.gW = h->gW; ga.bias = h->d_bias;
+    ga.err = h->d_err; ga.num_sms = h->num_sms;
+    const cudaError_t e = wq::launch_gemm(ga, st);
+    if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
+    return WQ_OK;
+}
+
 WQ_API wq_status wq_linear_forward(wq_weights_t h, const void* x, int M, void* y, void* workspace,
                                    size_t workspace_bytes, void* stream) {
     if (!h) return fail(WQ_ERR_INVALID, "NULL handle");
@@ -422,39 +461,23 @@ WQ_API wq_status wq_linear_forward(wq_weights_t h, const void* x, int M, void* y
     wq_status s = run_quant(h, x, M, WQ_SCALE_LAYOUT_MMA, ws.codes, ws.sf, ws.g, no ? ws.xo : nullptr,
                             r ? ws.u : nullptr, st);
     if (s != WQ_OK) return s;
+    return run_gemm(h, ws.codes, ws.sf, ws.g, ws.u, ws.xo, M, y, st);
+}
 
-    wq::GemmArgs ga{};
-    {
-        std::lock_guard<std::mutex> lk(h->mu);
-        if (h->key_ws != workspace || h->key_y != y || h->key_M != M) {
-            const char* why = "";
-            bool ok = wq::encode_tmap_2d(&h->tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, ws.codes, K / 2, M, K / 2, 128, 128,
-                                         CU_TENSOR_MAP_SWIZZLE_128B, &why) &&
-                      wq::encode_tmap_2d(&h->tmY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, y, N, M, 2ull * N, 64, 32,
-                                         CU_TENSOR_MAP_SWIZZLE_128B, &why);
-            if (ok && r)
-                ok = wq::encode_tmap_2d(&h->tmU, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ws.u, r, M, 2 * r, r, 128,
-                                        swizzle_for_row_bytes(2 * r), &why);
-            if (ok && no)
-                ok = wq::encode_tmap_2d(&h->tmXO, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws.xo, no, M, 2 * no, no, 128,
-                                        swizzle_for_row_bytes(2 * no), &why);
-            if (!ok) {
-                h->key_ws = nullptr;
-                return fail(WQ_ERR_CUDA, why);
-            }
-            h->key_ws = workspace;
-            h->key_y = y;
-            h->key_M = M;
-        }
-        ga.M = M; ga.N = N; ga.K = K; ga.r = r; ga.n_out = no;
-        ga.tmA = &h->tmA; ga.tmB = &h->tmB; ga.tmU = &h->tmU; ga.tmQ = &h->tmQ;
-        ga.tmXO = &h->tmXO; ga.tmWO = &h->tmWO; ga.tmY = &h->tmY;
-        ga.sfa = ws.sf; ga.sfb = h->d_sf; ga.gA = ws.g; ga.gW = h->gW; ga.bias = h->d_bias;
-        ga.err = h->d_err; ga.num_sms = h->num_sms;
-        const cudaError_t e = wq::launch_gemm(ga, st);
-        if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
-    }
-    return WQ_OK;
+WQ_API wq_status wq_linear_forward_quantized(wq_weights_t h, const uint8_t* codes, const uint8_t* scales_mma,
+                                             const float* gscale, const void* u, const void* x_omega, int M,
+                                             void* y, void* stream) {
+    if (!h) return fail(WQ_ERR_INVALID, "NULL handle");
+    if (M < 0) return fail(WQ_ERR_INVALID, "M < 0");
+    if (M == 0) return WQ_OK;
+    if (!codes || !scales_mma || !gscale || !y) return fail(WQ_ERR_INVALID, "NULL buffer");
+    if (h->cfg.rank > 0 && !u) return fail(WQ_ERR_INVALID, "u is required when rank > 0");
+    if (h->cfg.n_outliers > 0 && !x_omega) return fail(WQ_ERR_INVALID, "x_omega is required when n_outliers > 0");
+    if ((reinterpret_cast<uintptr_t>(codes) | reinterpret_cast<uintptr_t>(scales_mma) |
+         reinterpret_cast<uintptr_t>(u) | reinterpret_cast<uintptr_t>(x_omega) | reinterpret_cast<uintptr_t>(y)) & 15)
+        return fail(WQ_ERR_INVALID, "device buffers must be 16-byte aligned");
+    return run_gemm(h, codes, scales_mma, gscale, static_cast<const uint16_t*>(u),
+                    static_cast<const uint16_t*>(x_omega), M, y, static_cast<cudaStream_t>(stream));
 }
 
 WQ_API wq_status wq_linear_forward_host(wq_weights_t h, const void* x_host, int M, void* y_host, void* workspace,

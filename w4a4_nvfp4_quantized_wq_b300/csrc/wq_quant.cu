@@ -207,12 +207,13 @@ __global__ void __launch_bounds__(kThreads) quantize_act_kernel(const QuantArgs 
 #pragma unroll
             for (int j = 0; j < R; ++j) s_u[rloc][wrow][j] = acc[j];
         __syncthreads();
-        if (t < R && row_ok) {
-            float s = 0.0f;
+        if (row_ok)
+            for (int j = t; j < R; j += TPR) {
+                float s = 0.0f;
 #pragma unroll
-            for (int w = 0; w < WPR; ++w) s += s_u[rloc][w][t];
-            a.u[static_cast<size_t>(row) * R + t] = __bfloat16_as_ushort(__float2bfloat16_rn(s));
-        }
+                for (int w = 0; w < WPR; ++w) s += s_u[rloc][w][j];
+                a.u[static_cast<size_t>(row) * R + j] = __bfloat16_as_ushort(__float2bfloat16_rn(s));
+            }
     }
 }
 
