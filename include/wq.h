@@ -172,6 +172,26 @@ WQ_API wq_status wq_check_device_error(wq_weights_t h, void *stream);
 /* Release the handle and its device memory (synchronises the device first).  NULL is a no-op. */
 WQ_API void wq_free_weights(wq_weights_t h);
 
+/*
+ * Forward without any device allocation by the caller or the library.
+ * No counterpart on the pages: this entry point exists for deployment hosts that cannot
+ * call cudaMalloc or hand out scratch buffers after start-up -- for instance a plugin
+ * whose host engine owns every device allocation, or a real-time control loop that
+ * forbids allocation once running so that its latency stays predictable.
+ *   x, y    device bf16 [M, K] and [M, N], owned by the caller as in wq_linear_forward.
+ * Scratch comes from one static device array of WQ_NOALLOC_SCRATCH_BYTES bytes, linked
+ * into the library; every GPU that loads the library holds it until the process exits.
+ * The first call on a device looks up that array's device address (a one-time set-up);
+ * make that first call before any stream capture.  All calls share the one array and it
+ * keeps the last call's contents (nothing in it needs to start at zero), so calls whose
+ * kernels overlap on the GPU -- on different streams, or through different handles --
+ * race with each other: serialise them.  A call whose scratch need
+ * wq_workspace_bytes(h, M) exceeds WQ_NOALLOC_SCRATCH_BYTES returns WQ_ERR_UNSUPPORTED.
+ * It allocates nothing itself and otherwise behaves exactly like wq_linear_forward.
+ */
+#define WQ_NOALLOC_SCRATCH_BYTES (16u << 20)
+WQ_API wq_status wq_linear_forward_noalloc(wq_weights_t h, const void *x, int M, void *y, void *stream);
+
 /* Thread-local description of the last error ("" if none). */
 WQ_API const char *wq_last_error(void);
 

@@ -23,7 +23,7 @@ WQ_SCALE_LAYOUT_ROWMAJOR, WQ_SCALE_LAYOUT_MMA = 0, 1
 
 EXPORTED = ["wq_prepare_weights", "wq_get_config", "wq_workspace_bytes", "wq_linear_forward",
             "wq_host_workspace_bytes", "wq_linear_forward_host", "wq_quantize_activations",
-            "wq_linear_forward_quantized",
+            "wq_linear_forward_quantized", "wq_linear_forward_noalloc",
             "wq_export_weights", "wq_check_device_error", "wq_free_weights", "wq_last_error"]
 
 
@@ -66,6 +66,8 @@ def lib() -> ctypes.CDLL:
         L.wq_quantize_activations.restype = I
         L.wq_linear_forward_quantized.argtypes = [P, P, P, P, P, P, I, P, P]
         L.wq_linear_forward_quantized.restype = I
+        L.wq_linear_forward_noalloc.argtypes = [P, P, I, P, P]
+        L.wq_linear_forward_noalloc.restype = I
         L.wq_export_weights.argtypes = [P, P, P, P, P, P, P]
         L.wq_export_weights.restype = I
         L.wq_check_device_error.argtypes = [P, P]
@@ -173,6 +175,17 @@ def wq_linear_forward(w: Weights, x, y=None, workspace=None, stream=None):
     _check(lib().wq_linear_forward(ctypes.c_void_p(w.handle), ctypes.c_void_p(x.data_ptr()), M,
                                    ctypes.c_void_p(y.data_ptr()), ctypes.c_void_p(workspace.data_ptr()),
                                    workspace.numel(), ctypes.c_void_p(_stream_ptr(stream))))
+    return y
+
+
+NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def wq_linear_forward_noalloc(w: Weights, x, y, stream=None):
+    """Forward for callers that cannot allocate: scratch is the library's static device
+    array (NOALLOC_SCRATCH_BYTES); x and y are caller-owned device tensors."""
+    _check(lib().wq_linear_forward_noalloc(ctypes.c_void_p(w.handle), ctypes.c_void_p(x.data_ptr()), x.shape[0],
+                                           ctypes.c_void_p(y.data_ptr()), ctypes.c_void_p(_stream_ptr(stream))))
     return y
 
 

@@ -101,6 +101,8 @@ CUtensorMapSwizzle swizzle_for_row_bytes(uint32_t b) {
 
 namespace wq {
 
+void set_last_error(const char* msg) { g_last_error = msg; }
+
 bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner, uint64_t outer,
                     uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle,
                     const char** why) {

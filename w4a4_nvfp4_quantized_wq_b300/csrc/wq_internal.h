@@ -65,6 +65,9 @@ struct GemmArgs {
 
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream);
 
+// Record a message for wq_last_error() (thread-local).
+void set_last_error(const char* msg);
+
 // cuTensorMapEncodeTiled obtained from the driver at run time (no libcuda link).
 bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
                     uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
