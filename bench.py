@@ -52,6 +52,7 @@ def parse_args():
     ap.add_argument("--kernel-iters", type=int, default=200)
     ap.add_argument("--cpu-baseline-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only-layer", default=None, help="run one named layer of the workload (profiling)")
     return ap.parse_args()
 
 
@@ -77,7 +78,10 @@ class ClockSampler:
     def __init__(self, dev_index: int):
         self.samples, self.reasons, self.ok = [], set(), False
         self.max_mhz = None
+        self.source = "unavailable"
+        self.dev_index = dev_index
         self._stop = threading.Event()
+        self._proc = None
         try:
             import pynvml
             pynvml.nvmlInit()
@@ -85,10 +89,14 @@ class ClockSampler:
             self._h = pynvml.nvmlDeviceGetHandleByIndex(dev_index)
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
             self.ok = True
-        except Exception:
+            self.source = "NVML"
+        except Exception as exc:
             self.ok = False
+            self.source = f"nvidia-smi (NVML python binding failed: {type(exc).__name__})"
 
     def _run(self):
+        if not self.ok:
+            return self._run_smi()
         nv = self._nv
         while not self._stop.is_set():
             try:
@@ -103,21 +111,46 @@ class ClockSampler:
                 pass
             time.sleep(0.002)
 
+    def _run_smi(self):
+        import subprocess
+        q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self._proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev_index), f"--query-gpu={q}",
+                                           "--format=csv,noheader,nounits", "-lms", "20"],
+                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.source = "unavailable"
+            return
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self._proc.stdout:
+            f = [x.strip() for x in line.split(",")]
+            try:
+                self.samples.append(float(f[0]))
+                self.max_mhz = float(f[1])
+                for n, v in zip(names, f[2:6]):
+                    if v.lower() == "active":
+                        self.reasons.add(n)
+            except (ValueError, IndexError):
+                pass
+
     def __enter__(self):
-        if self.ok:
-            self._t = threading.Thread(target=self._run, daemon=True)
-            self._t.start()
+        self._t = threading.Thread(target=self._run, daemon=True)
+        self._t.start()
+        if not self.ok:
+            time.sleep(0.3)          # let nvidia-smi start sampling before the timed work
         return self
 
     def __exit__(self, *a):
         self._stop.set()
-        if self.ok:
-            self._t.join()
+        if self._proc is not None:
+            self._proc.terminate()
+        self._t.join(timeout=5)
 
     def record(self):
         return {"sm_mhz": float(statistics.median(self.samples)) if self.samples else None,
                 "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
-                "samples": len(self.samples), "source": "NVML" if self.ok else "unavailable"}
+                "samples": len(self.samples), "source": self.source}
 
 
 def measured_peaks():
@@ -268,6 +301,8 @@ def run_wq(args):
     import workloads as wl
 
     wlw, idx = layers_of(args.workload)
+    if args.only_layer:
+        idx = [i for i in idx if wlw.layers[i].name == args.only_layer]
     layers = [wl.make_layer_inputs(args.workload, layer=i) for i in idx]
     M = wlw.M
     stream = torch.cuda.Stream(device=dev)

@@ -121,8 +121,50 @@ def test_activation_quant_bitexact(case):
         assert u_close(ug, U, L.x_bits, o.P).all()
 
 
+@pytest.mark.parametrize("case,split", [("expert_small", 1), ("expert_small", 4), ("expert_small", 16),
+                                        ("dit_r32_o64_ragged_n", 2), ("dit_r32_o64_ragged_n", 8),
+                                        ("no_smooth_r64", 1), ("no_smooth_r64", 2), ("backbone_r0", 1),
+                                        ("multi_tile_kstage_tail", 1), ("multi_tile_kstage_tail", 16)])
+def test_activation_quant_split(case, split, monkeypatch):
+    """The quantiser with a row tile's K range on one CTA or spread over a cluster (the row
+    amax and the low-rank partial sums then go through distributed shared memory)."""
+    monkeypatch.setenv("WQ_QUANT_SPLIT", str(split))
+    L = layer(case)
+    w = prep(L)
+    x = x_dev(L.x_bits)
+    codes, scales, g, xo, u = wq.wq_quantize_activations(w, x, wq.WQ_SCALE_LAYOUT_ROWMAJOR)
+    torch.cuda.synchronize()
+    aq = oracle.quantize_act(L.x_bits, L.s, L.rotate, L.omega)
+    assert np.array_equal(g.cpu().numpy(), aq.g)
+    assert np.array_equal(scales.cpu().numpy(), aq.scales)
+    assert np.array_equal(codes.cpu().numpy(), aq.codes)
+    if L.omega.size:
+        assert np.array_equal(xo.cpu().view(torch.int16).numpy().view(np.uint16), aq.x_omega)
+    if L.rank:
+        o = oracle.prepare_weights(L.W, L.s, L.L1, L.L2, L.omega, L.rotate)
+        U = oracle.lowrank_act(L.x_bits, o.P)
+        ug = u.cpu().view(torch.int16).numpy().view(np.uint16)
+        assert u_close(ug, U, L.x_bits, o.P).all()
+
+
 @pytest.mark.parametrize("case", list(CASES))
 def test_forward_parity(case):
+    L = layer(case)
+    w = prep(L)
+    y = wq.wq_linear_forward(w, x_dev(L.x_bits))
+    wq.wq_check_device_error(w)
+    y_ref, *_ = oracle.reference_forward(L)
+    assert_y_close(L, y, y_ref)
+
+
+@pytest.mark.parametrize("case,split", [("expert_small", 1), ("expert_small", 2), ("expert_small", 4),
+                                        ("multi_tile_kstage_tail", 1), ("multi_tile_kstage_tail", 2),
+                                        ("multi_tile_kstage_tail", 4), ("dit_r32_o64_ragged_n", 2),
+                                        ("backbone_r0", 8), ("no_smooth_r64", 2), ("min_k64_n16_m1", 1)])
+def test_forward_parity_split_k(case, split, monkeypatch):
+    """Both GEMM schedules: one persistent CTA per tile (split 1) and the K range of a tile
+    spread over a cluster with the DSMEM reduction (split > 1)."""
+    monkeypatch.setenv("WQ_GEMM_SPLIT", str(split))
     L = layer(case)
     w = prep(L)
     y = wq.wq_linear_forward(w, x_dev(L.x_bits))

@@ -11,6 +11,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -154,6 +155,7 @@ struct wq_weights {
     float* d_inv_s = nullptr;      // [K]
     int16_t* d_omega_pos = nullptr;// [K]
     uint16_t* d_P = nullptr;       // [K, r] bf16
+    uint32_t* d_Pfrag = nullptr;   // P in mma.sync m16n8k16 B-fragment order
     uint16_t* d_Qt = nullptr;      // [N, r] bf16
     uint16_t* d_WOt = nullptr;     // [N, n_out] fp16
     int* d_err = nullptr;
@@ -166,6 +168,10 @@ struct wq_weights {
     const void* key_y = nullptr;
     int key_M = -1;
     CUtensorMap tmA{}, tmU{}, tmXO{}, tmY{};
+    std::mutex mu_x;
+    const void* key_x = nullptr;
+    int key_xM = -1;
+    CUtensorMap tmX{};
 };
 
 namespace {
@@ -192,6 +198,7 @@ void free_device(wq_weights* h) {
     cudaFree(h->d_inv_s);
     cudaFree(h->d_omega_pos);
     cudaFree(h->d_P);
+    cudaFree(h->d_Pfrag);
     cudaFree(h->d_Qt);
     cudaFree(h->d_WOt);
     cudaFree(h->d_err);
@@ -248,6 +255,23 @@ WQ_API wq_status wq_prepare_weights(const wq_config* cfg, const float* W, const 
             if (s) l = l * inv_s[k];
             P[static_cast<size_t>(k) * r + j] = bf16_bits(l);
         }
+    // P as the B operand of mma.sync.m16n8k16 (k16 x n8 tiles): for 64-block kb, n-tile nt,
+    // lane (g = lane / 4, c = lane % 4) and k16 step f, the lane's two registers hold
+    // {P[k][j], P[k+1][j]} and {P[k+8][j], P[k+9][j]} with k = 64 kb + 16 f + 2 c, j = 8 nt + g.
+    std::vector<uint32_t> Pfrag(static_cast<size_t>(K) * r / 2);
+    if (r > 0) {
+        const int NT = r / 8;
+        for (int kb = 0; kb < K / 64; ++kb)
+            for (int nt = 0; nt < NT; ++nt)
+                for (int lane = 0; lane < 32; ++lane)
+                    for (int f = 0; f < 4; ++f) {
+                        const int g = lane / 4, c = lane % 4, j = 8 * nt + g, k = 64 * kb + 16 * f + 2 * c;
+                        auto at = [&](int kk) { return static_cast<uint32_t>(P[static_cast<size_t>(kk) * r + j]); };
+                        const size_t o = ((static_cast<size_t>(kb) * NT + nt) * 32 + lane) * 8 + 2 * f;
+                        Pfrag[o] = at(k) | (at(k + 1) << 16);
+                        Pfrag[o + 1] = at(k + 8) | (at(k + 9) << 16);
+                    }
+    }
     std::vector<float> Pf(P.size()), Qf(static_cast<size_t>(r) * N);
     for (size_t i = 0; i < P.size(); ++i) Pf[i] = __bfloat162float(__ushort_as_bfloat16(P[i]));
     for (int j = 0; j < r; ++j)
@@ -338,6 +362,7 @@ WQ_API wq_status wq_prepare_weights(const wq_config* cfg, const float* W, const 
     if (s && (st = upload(&h->d_inv_s, inv_s.data(), K * 4, cs)) != WQ_OK) return bail(st);
     if (no && (st = upload(&h->d_omega_pos, omega_pos.data(), K * 2, cs)) != WQ_OK) return bail(st);
     if (r && (st = upload(&h->d_P, P.data(), P.size() * 2, cs)) != WQ_OK) return bail(st);
+    if (r && (st = upload(&h->d_Pfrag, Pfrag.data(), Pfrag.size() * 4, cs)) != WQ_OK) return bail(st);
     if (r && (st = upload(&h->d_Qt, Qt.data(), Qt.size() * 2, cs)) != WQ_OK) return bail(st);
     if (no && (st = upload(&h->d_WOt, WOt.data(), WOt.size() * 2, cs)) != WQ_OK) return bail(st);
     if (cudaMalloc(&h->d_err, sizeof(int)) != cudaSuccess) return bail(fail(WQ_ERR_OOM, "cudaMalloc failed"));
@@ -372,6 +397,22 @@ WQ_API size_t wq_host_workspace_bytes(wq_weights_t h, int M) {
 static wq_status run_quant(wq_weights_t h, const void* x, int M, int layout, uint8_t* codes, uint8_t* sf, float* g,
                            uint16_t* xo, uint16_t* u, cudaStream_t st) {
     wq::QuantArgs qa{};
+    {
+        std::lock_guard<std::mutex> lk(h->mu_x);
+        if (h->key_x != x || h->key_xM != M) {
+            const char* why = "";
+            if (!wq::encode_tmap_2d(&h->tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, h->cfg.K, M, 2ull * h->cfg.K, 64, 32,
+                                    CU_TENSOR_MAP_SWIZZLE_128B, &why)) {
+                h->key_x = nullptr;
+                return fail(WQ_ERR_CUDA, why);
+            }
+            h->key_x = x;
+            h->key_xM = M;
+        }
+        qa.tmX = &h->tmX;
+    }
+    qa.pfrag = h->d_Pfrag;
+    qa.err = h->d_err;
     qa.x = x;
     qa.M = M;
     qa.K = h->cfg.K;
@@ -387,6 +428,7 @@ static wq_status run_quant(wq_weights_t h, const void* x, int M, int layout, uin
     qa.sf = sf;
     qa.sf_layout = layout;
     qa.g = g;
+    qa.num_sms = h->num_sms;
     const cudaError_t e = wq::launch_quantize_act(qa, st);
     if (e != cudaSuccess) return cuda_fail(e, "activation quantiser launch");
     return WQ_OK;
@@ -441,6 +483,10 @@ static wq_status run_gemm(wq_weights_t h, const uint8_t* codes, const uint8_t* s
     ga.tmXO = &h->tmXO; ga.tmWO = &h->tmWO; ga.tmY = &h->tmY;
     ga.sfa = sf; ga.sfb = h->d_sf; ga.gA = g; ga.gW = h->gW; ga.bias = h->d_bias;
     ga.err = h->d_err; ga.num_sms = h->num_sms;
+    ga.y = y;
+    // WQ_GEMM_SPLIT=<1|2|4|8|16> pins the number of CTAs per output tile (tuning and tests)
+    const char* fs = std::getenv("WQ_GEMM_SPLIT");
+    ga.force_split = fs ? std::atoi(fs) : 0;
     const cudaError_t e = wq::launch_gemm(ga, st);
     if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
     return WQ_OK;
@@ -455,7 +501,7 @@ WQ_API wq_status wq_linear_forward(wq_weights_t h, const void* x, int M, void* y
     if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15)
         return fail(WQ_ERR_INVALID, "x and y must be 16-byte aligned");
     if (reinterpret_cast<uintptr_t>(workspace) & 255) return fail(WQ_ERR_INVALID, "workspace must be 256-byte aligned");
-    const int K = h->cfg.K, N = h->cfg.N, r = h->cfg.rank, no = h->cfg.n_outliers;
+    const int K = h->cfg.K, r = h->cfg.rank, no = h->cfg.n_outliers;
     const wq::ActWorkspace ws = wq::carve_workspace(workspace, M, K, r, no);
     if (workspace_bytes < ws.bytes) return fail(WQ_ERR_INVALID, "workspace too small");
     cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -4,7 +4,7 @@
 // (QuantWAMs sec. 4.2 "Backend": NVFP4 W4A4 kernels plus the 16-bit exception path for the
 // kept channels; Q-WAM abstract: the 16-bit low-rank branch runs as a dense matmul too.)
 //
-// One persistent CTA per SM, 6 warps:
+// One persistent CTA per SM, 10 warps:
 //   warp 0    TMA producer: A/B code tiles (128 x 256 fp4, 128B swizzle) and the block-scale
 //             atoms into an S-stage shared-memory ring; the side operands (U, Q^T, x_O, W_O^T)
 //             once per tile.
@@ -12,23 +12,57 @@
 //             TMEM, 4 x tcgen05.mma (K = 64 each) per stage, then the 16-bit side MMAs
 //             (kind::f16) into a separate TMEM accumulator; tcgen05.commit frees smem stages
 //             and publishes finished accumulators.
-//   warps 2-5 epilogue: tcgen05.ld of the fp32 accumulators (lane quadrant = warp % 4),
-//             scale, add side + bias, bf16, swizzled smem staging, TMA store.
+//   warps 2-9 epilogue: two warps per TMEM lane quadrant (quadrant = warp % 4), each owning
+//             64 of the tile's 128 columns: tcgen05.ld of the fp32 accumulators, scale, add
+//             side + bias, bf16, swizzled smem staging, one TMA store per warp.
 // TMEM (512 columns): accumulator buffers at 0 and 128 (double buffered so the epilogue of
 // tile t overlaps the main loop of tile t+1), side accumulator at 256, scale-factor slots
 // (32 columns per ring stage) after that.
+//
+// Few output tiles (batch-1 shapes): the K range of one tile is split over a thread-block
+// cluster of `split` CTAs (2..16).  Each CTA accumulates its K slice in TMEM, writes
+// alpha * acc (rank 0 adds the side branch and bias) to its shared memory, and after a
+// cluster barrier every CTA reduces a slice of the tile's rows over all peers through
+// distributed shared memory, in rank order (deterministic), and stores bf16.
+//
+// The kernel is launched as a programmatic dependent of the activation quantiser: weight
+// tiles are requested before griddepcontrol.wait, activation tiles after it.  It lets the
+// next grid in the stream start its prologue early.
 #include <cuda_bf16.h>
+
+#include <cstdlib>
+#include <map>
+#include <mutex>
+#include <tuple>
 
 #include "ptx.cuh"
 #include "wq_internal.h"
 
+#ifdef WQ_TRACE
+// Timeline probes for kernel development builds only (never defined in the product build).
+__device__ unsigned long long g_wq_trace[4096 * 16];
+#define WQ_TRACE_AT(slot) (g_wq_trace[blockIdx.x * 16 + (slot)] = wq::global_timer_ns())
+__device__ unsigned long long g_wq_tile_trace[64 * 8];
+#define WQ_TILE_AT(tl, slot) do { if (blockIdx.x == 0 && (tl) < 64) g_wq_tile_trace[(tl) * 8 + (slot)] = wq::global_timer_ns(); } while (0)
+extern "C" WQ_API int wq_tile_trace_read(void* host, size_t bytes) {
+    return static_cast<int>(cudaMemcpyFromSymbol(host, g_wq_tile_trace, bytes));
+}
+extern "C" WQ_API int wq_trace_read(void* host, size_t bytes) {
+    return static_cast<int>(cudaMemcpyFromSymbol(host, g_wq_trace, bytes));
+}
+#else
+#define WQ_TRACE_AT(slot) ((void)0)
+#define WQ_TILE_AT(tl, slot) ((void)0)
+#endif
+
 namespace wq {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kEpiWarps = 8;
 constexpr uint32_t kTileBytes = 128 * 128;               // 128 rows x 128 bytes (256 fp4)
 constexpr uint32_t kStageBytes = 2 * kTileBytes + 2 * 4 * kSfAtom;
-constexpr uint32_t kYHalfBytes = 32 * 128;               // 32 rows x 64 bf16
+constexpr uint32_t kYHalfBytes = 32 * 128;               // one warp's 32 rows x 64 bf16
 constexpr uint32_t kYBytes = 4 * 2 * kYHalfBytes;
 constexpr uint32_t kBarBytes = 256;
 constexpr uint32_t kMaxSmem = 232448;
@@ -42,6 +76,8 @@ struct Plan {
 
 struct KParams {
     int M, N, K, r, n_out, stages;
+    int split;                       // CTAs per output tile (cluster x size); 1 = persistent
+    __nv_bfloat16* y;                // output, written directly by the split-K reduction
     uint32_t u_bytes, xo_bytes, off_side, off_y, off_bar, sf_col;
     const uint8_t* sfa;
     const uint8_t* sfb;
@@ -51,7 +87,7 @@ struct KParams {
     int* err;
 };
 
-Plan make_plan(int r, int n_out) {
+Plan make_plan(int r, int n_out, int max_stages = 8) {
     Plan p{};
     p.u_bytes = 128u * 2u * static_cast<uint32_t>(r);
     p.xo_bytes = 128u * 2u * static_cast<uint32_t>(n_out);
@@ -61,7 +97,7 @@ Plan make_plan(int r, int n_out) {
     const int tmem_slots = static_cast<int>((512 - p.sf_col) / 32);
     int s = static_cast<int>((kMaxSmem - 1024 - side - kYBytes - kBarBytes) / kStageBytes);
     if (s > tmem_slots) s = tmem_slots;
-    if (s > 8) s = 8;
+    if (s > max_stages) s = max_stages;
     p.stages = s;
     p.off_side = static_cast<uint32_t>(s) * kStageBytes;
     p.off_y = p.off_side + side;
@@ -107,24 +143,31 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
     const int M = p.M, N = p.N;
-    const bool has_side = (p.r + p.n_out) > 0;
     const int n_tiles = (N + 127) / 128;
     const int tiles = ((M + 127) / 128) * n_tiles;
     const int num_kb = p.K / 64;
     const int num_kt = (num_kb + 3) / 4;
+    const bool split = p.split > 1;
+    const uint32_t rank = split ? cluster_ctarank() : 0u;
+    const int tile_first = split ? static_cast<int>(blockIdx.x) / p.split : static_cast<int>(blockIdx.x);
+    const int tile_step = split ? tiles : static_cast<int>(gridDim.x);
+    const int kt_lo = split ? static_cast<int>(rank) * num_kt / p.split : 0;
+    const int kt_hi = split ? (static_cast<int>(rank) + 1) * num_kt / p.split : num_kt;
+    const bool has_side = (p.r + p.n_out) > 0 && rank == 0;
 
     if (threadIdx.x == 0) {
+        WQ_TRACE_AT(0);
         for (int s = 0; s < S; ++s) {
             mbar_init(bar_full + 8u * s, 1);
             mbar_init(bar_empty + 8u * s, 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_tfull + 8u * b, 1);
-            mbar_init(bar_tempty + 8u * b, 4);
+            mbar_init(bar_tempty + 8u * b, kEpiWarps);
         }
         mbar_init(bar_sfull, 1);
         mbar_init(bar_sempty, 1);
-        mbar_init(bar_stempty, 4);
+        mbar_init(bar_stempty, kEpiWarps);
         mbar_init(bar_final, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -142,6 +185,10 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    if (threadIdx.x == 0) WQ_TRACE_AT(1);
+    // the next kernel in the stream may begin its prologue; it waits for this grid to
+    // complete before it touches memory
+    griddep_launch_dependents();
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -149,10 +196,40 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             int stage = 0;
             uint32_t ph = 0, sph = 0;
             uint32_t issued = 0, issued_ph = 0;       // per-stage "ever armed" bit and its parity
-            bool ok = true;
-            for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+            bool ok = true, first = true;
+            for (int tile = tile_first; tile < tiles && ok; tile += tile_step) {
                 const int mb = tile / n_tiles, nb = tile % n_tiles;
-                for (int kt = 0; kt < num_kt; ++kt) {
+                int kt = kt_lo;
+                if (first) {
+                    // weights of the first stages go out before the previous grid finishes
+                    first = false;
+                    const int pre = min(S, kt_hi - kt_lo);
+                    for (int i = 0; i < pre; ++i) {
+                        const int kb0 = (kt_lo + i) * 4, nkb = min(4, num_kb - kb0);
+                        const uint32_t fb = bar_full + 8u * i;
+                        const uint32_t sA = base + static_cast<uint32_t>(i) * kStageBytes;
+                        mbar_arrive_expect_tx(fb, 2 * kTileBytes + 2u * nkb * kSfAtom);
+                        tma_load_2d(sA + kTileBytes, &tmB, (kt_lo + i) * 128, nb * 128, fb);
+                        bulk_load(sA + 2 * kTileBytes + 4 * kSfAtom,
+                                  p.sfb + (static_cast<size_t>(nb) * num_kb + kb0) * kSfAtom, nkb * kSfAtom, fb);
+                        issued |= 1u << i;
+                    }
+                    WQ_TRACE_AT(2);
+                    griddep_wait();
+                    WQ_TRACE_AT(3);
+                    for (int i = 0; i < pre; ++i) {
+                        const int kb0 = (kt_lo + i) * 4, nkb = min(4, num_kb - kb0);
+                        const uint32_t fb = bar_full + 8u * i;
+                        const uint32_t sA = base + static_cast<uint32_t>(i) * kStageBytes;
+                        tma_load_2d(sA, &tmA, (kt_lo + i) * 128, mb * 128, fb);
+                        bulk_load(sA + 2 * kTileBytes, p.sfa + (static_cast<size_t>(mb) * num_kb + kb0) * kSfAtom,
+                                  nkb * kSfAtom, fb);
+                    }
+                    kt += pre;
+                    stage = pre % S;
+                    ph = pre == S ? 1u : 0u;
+                }
+                for (; kt < kt_hi; ++kt) {
                     if (!mbar_wait(bar_empty + 8u * stage, ph ^ 1u, abort_flag, p.err, 1)) { ok = false; break; }
                     const int kb0 = kt * 4;
                     const int nkb = min(4, num_kb - kb0);
@@ -201,35 +278,53 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             uint32_t ph = 0, sph = 0;
             int tl = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x, ++tl) {
+            for (int tile = tile_first; tile < tiles && ok; tile += tile_step, ++tl) {
                 const int buf = tl & 1;
                 const uint32_t aph = (static_cast<uint32_t>(tl) >> 1) & 1u;
                 if (!mbar_wait(bar_tempty + 8u * buf, aph ^ 1u, abort_flag, p.err, 4)) { ok = false; break; }
+                WQ_TILE_AT(tl, 0);
                 tc_fence_after();
                 const uint32_t d_acc = tmem + 128u * buf;
-                for (int kt = 0; kt < num_kt; ++kt) {
+                // The scale factors of stage k+1 are copied into TMEM right after the MMAs of stage k
+                // are issued, so the copies overlap the MMAs instead of sitting in front of them.
+                auto copy_scales = [&](int stg, int ktx) {
+                    const int nkbx = min(4, num_kb - ktx * 4);
+                    const uint32_t sAx = base + static_cast<uint32_t>(stg) * kStageBytes;
+                    const uint32_t sfx = tmem + p.sf_col + 32u * stg;
+                    for (int kb = 0; kb < nkbx; ++kb) {
+                        tmem_cp_32x128b_x4(sfx + 4u * kb, smem_desc(sAx + 2 * kTileBytes + kSfAtom * kb, 0, 128, 0));
+                        tmem_cp_32x128b_x4(sfx + 16u + 4u * kb,
+                                           smem_desc(sAx + 2 * kTileBytes + 4 * kSfAtom + kSfAtom * kb, 0, 128, 0));
+                    }
+                };
+                for (int kt = kt_lo; kt < kt_hi; ++kt) {
                     if (!mbar_wait(bar_full + 8u * stage, ph, abort_flag, p.err, 5)) { ok = false; break; }
+                    if (tl == 0 && kt == kt_lo) WQ_TRACE_AT(4);
                     tc_fence_after();
                     const int nkb = min(4, num_kb - kt * 4);
                     const uint32_t sA = base + static_cast<uint32_t>(stage) * kStageBytes;
                     const uint32_t sf_t = tmem + p.sf_col + 32u * stage;
-                    for (int kb = 0; kb < nkb; ++kb) {
-                        tmem_cp_32x128b_x4(sf_t + 4u * kb, smem_desc(sA + 2 * kTileBytes + kSfAtom * kb, 0, 128, 0));
-                        tmem_cp_32x128b_x4(sf_t + 16u + 4u * kb,
-                                           smem_desc(sA + 2 * kTileBytes + 4 * kSfAtom + kSfAtom * kb, 0, 128, 0));
-                    }
+                    if (kt == kt_lo) copy_scales(stage, kt);
                     const uint64_t ad = smem_desc(sA, 16, 1024, 2);
                     const uint64_t bd = smem_desc(sA + kTileBytes, 16, 1024, 2);
                     for (int kb = 0; kb < nkb; ++kb)
                         mma_nvf4(d_acc, ad + 2u * kb, bd + 2u * kb, idesc_fp4, sf_t + 4u * kb, sf_t + 16u + 4u * kb,
-                                 (kt | kb) != 0 ? 1u : 0u);
+                                 (kt != kt_lo || kb != 0) ? 1u : 0u);
                     tc_commit(bar_empty + 8u * stage);
                     if (++stage == S) { stage = 0; ph ^= 1u; }
+                    if (kt + 1 < kt_hi) {
+                        if (!mbar_wait(bar_full + 8u * stage, ph, abort_flag, p.err, 5)) { ok = false; break; }
+                        tc_fence_after();
+                        copy_scales(stage, kt + 1);
+                    }
                 }
                 if (!ok) break;
+                WQ_TILE_AT(tl, 1);
                 if (has_side) {
                     if (!mbar_wait(bar_sfull, sph, abort_flag, p.err, 6)) { ok = false; break; }
+                    WQ_TILE_AT(tl, 2);
                     if (!mbar_wait(bar_stempty, sph ^ 1u, abort_flag, p.err, 7)) { ok = false; break; }
+                    WQ_TILE_AT(tl, 3);
                     tc_fence_after();
                     const uint32_t d_side = tmem + 256u;
                     const uint32_t sU = base + p.off_side;
@@ -252,107 +347,239 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     sph ^= 1u;
                 }
                 tc_commit(bar_tfull + 8u * buf);
+                if (tl == 0) WQ_TRACE_AT(5);
             }
             // every MMA this thread issued has completed before TMEM is released
             tc_commit(bar_final);
             mbar_wait(bar_final, 0, abort_flag, p.err, 8);
         }
     } else {
-        // ------------------------------------------------------------ epilogue (warps 2..5)
+        // ------------------------------------------------------------ epilogue (warps 2..9)
         const int q = warp & 3;                        // TMEM lane quadrant of this warp
-        const uint32_t ystage = base + p.off_y + static_cast<uint32_t>(q) * 2u * kYHalfBytes;
+        const int hh = (warp - 2) >> 2;                // column half: 0 -> cols 0..63, 1 -> 64..127
+        const uint32_t ystage = base + p.off_y + static_cast<uint32_t>(warp - 2) * kYHalfBytes;
         const uint32_t t_lane = static_cast<uint32_t>(q * 32) << 16;
+        const int row_t = q * 32 + lane;
         int tl = 0;
-        for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++tl) {
+        griddep_wait();                                // gA is written by the previous grid
+        for (int tile = tile_first; tile < tiles; tile += tile_step, ++tl) {
             const int mb = tile / n_tiles, nb = tile % n_tiles;
             const int buf = tl & 1;
             const uint32_t aph = (static_cast<uint32_t>(tl) >> 1) & 1u;
-            if (!mbar_wait(bar_tfull + 8u * buf, aph, abort_flag, p.err, 9)) break;
-            tc_fence_after();
-            if (lane == 0) bulk_wait_group_read0();     // staging free again
-            __syncwarp();
-            const int row = mb * 128 + q * 32 + lane;
+            const int row = mb * 128 + row_t;
             const float alpha = row < M ? __fmul_rn(__ldg(p.gA + row), p.gW) : 0.0f;
-            for (int ch = 0; ch < 4; ++ch) {
-                uint32_t acc[32], sd[32];
-                tmem_ld_32x32b_x32(tmem + 128u * buf + 32u * ch + t_lane, acc);
-                if (has_side) tmem_ld_32x32b_x32(tmem + 256u + 32u * ch + t_lane, sd);
-                tmem_wait_ld();
-                uint32_t packed[16];
+            const bool add_bias = p.bias != nullptr && !split;
+            if (!mbar_wait(bar_tfull + 8u * buf, aph, abort_flag, p.err, 9)) break;
+            if (tl == 0 && threadIdx.x == 64) WQ_TRACE_AT(6);
+            if (threadIdx.x == 64) WQ_TILE_AT(tl, 4);
+            tc_fence_after();
+            if (!split) {
+                if (lane == 0) bulk_wait_group_read0(); // staging free again
+                __syncwarp();
+            }
+            for (int ch = 0; ch < 2; ++ch) {
+                const int c0 = hh * 64 + ch * 32;       // first column of this chunk in the tile
+                float4 bv[8];
+                if (add_bias) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int n0 = nb * 128 + ch * 32 + 2 * i;
-                    float y0 = alpha * __uint_as_float(acc[2 * i]);
-                    float y1 = alpha * __uint_as_float(acc[2 * i + 1]);
-                    if (has_side) {
-                        y0 += __uint_as_float(sd[2 * i]);
-                        y1 += __uint_as_float(sd[2 * i + 1]);
+                    for (int j = 0; j < 8; ++j) {
+                        const int n = nb * 128 + c0 + 4 * j;
+                        bv[j] = n < N ? __ldg(reinterpret_cast<const float4*>(p.bias + n)) : make_float4(0.f, 0.f, 0.f, 0.f);
                     }
-                    if (p.bias != nullptr) {
-                        if (n0 < N) y0 += __ldg(p.bias + n0);
-                        if (n0 + 1 < N) y1 += __ldg(p.bias + n0 + 1);
-                    }
-                    packed[i] = pack_bf16x2(y0, y1);
                 }
-                const uint32_t hb = ystage + static_cast<uint32_t>(ch >> 1) * kYHalfBytes + lane * 128u;
+                uint32_t acc[32], sd[32];
+                tmem_ld_32x32b_x32(tmem + 128u * buf + static_cast<uint32_t>(c0) + t_lane, acc);
+                if (has_side) tmem_ld_32x32b_x32(tmem + 256u + static_cast<uint32_t>(c0) + t_lane, sd);
+                tmem_wait_ld();
+                float v[32];
 #pragma unroll
-                for (int jj = 0; jj < 4; ++jj) {
-                    const uint32_t j = static_cast<uint32_t>((ch & 1) * 4 + jj);
-                    st_shared_v4(hb + ((j ^ (lane & 7u)) << 4), packed[4 * jj], packed[4 * jj + 1],
-                                 packed[4 * jj + 2], packed[4 * jj + 3]);
+                for (int i = 0; i < 32; ++i) {
+                    v[i] = alpha * __uint_as_float(acc[i]);
+                    if (has_side) v[i] += __uint_as_float(sd[i]);
+                }
+                if (add_bias) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        v[4 * j] += bv[j].x; v[4 * j + 1] += bv[j].y; v[4 * j + 2] += bv[j].z; v[4 * j + 3] += bv[j].w;
+                    }
+                }
+                if (split) {
+                    // fp32 partial of this CTA's K slice -> shared memory, rows swizzled by 16 B
+                    if (row < M) {
+                        const uint32_t prow = base + static_cast<uint32_t>(row_t) * 512u;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const uint32_t c4 = static_cast<uint32_t>(c0 / 4 + j);
+                            st_shared_v4f(prow + ((c4 ^ (static_cast<uint32_t>(row_t) & 7u)) << 4), v[4 * j],
+                                          v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                        }
+                    }
+                } else {
+                    const uint32_t hb = ystage + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                        const uint32_t j = static_cast<uint32_t>(ch * 4 + jj);
+                        st_shared_v4(hb + ((j ^ (static_cast<uint32_t>(lane) & 7u)) << 4),
+                                     pack_bf16x2(v[8 * jj], v[8 * jj + 1]), pack_bf16x2(v[8 * jj + 2], v[8 * jj + 3]),
+                                     pack_bf16x2(v[8 * jj + 4], v[8 * jj + 5]), pack_bf16x2(v[8 * jj + 6], v[8 * jj + 7]));
+                    }
                 }
             }
             tc_fence_before();
+            if (split) {
+                if (threadIdx.x == 64) WQ_TRACE_AT(7);
+                break;                                 // one tile per cluster
+            }
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(bar_tempty + 8u * buf);
                 if (has_side) mbar_arrive(bar_stempty);
             }
+            if (threadIdx.x == 64) WQ_TILE_AT(tl, 5);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
                 const int y0 = mb * 128 + q * 32;
-                if (y0 < M) {
-                    tma_store_2d(&tmY, ystage, nb * 128, y0);
-                    if (nb * 128 + 64 < N) tma_store_2d(&tmY, ystage + kYHalfBytes, nb * 128 + 64, y0);
-                }
+                if (y0 < M && nb * 128 + hh * 64 < N) tma_store_2d(&tmY, ystage, nb * 128 + hh * 64, y0);
                 bulk_commit_group();
             }
         }
         if (lane == 0) bulk_wait_group0();
     }
 
+    if (split) {
+        cluster_sync();                                // every partial of the cluster is in smem
+        if (threadIdx.x == 64) WQ_TRACE_AT(8);
+        if (warp >= 2 && tile_first < tiles) {
+            const int t = threadIdx.x - 64;             // 0 .. 255
+            const int mb = tile_first / n_tiles, nb = tile_first % n_tiles;
+            const int valid = min(128, M - mb * 128);
+            const int per = (valid + p.split - 1) / p.split;
+            const int r0 = static_cast<int>(rank) * per;
+            const int r1 = min(valid, r0 + per);
+            for (int it = t; it < (r1 - r0) * 32; it += 32 * kEpiWarps) {
+                const int row_t = r0 + it / 32;
+                const uint32_t c4 = static_cast<uint32_t>(it % 32);
+                const uint32_t off = base + static_cast<uint32_t>(row_t) * 512u +
+                                     ((c4 ^ (static_cast<uint32_t>(row_t) & 7u)) << 4);
+                float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int qr = 0; qr < p.split; ++qr) {
+                    const float4 v = ld_dsmem_v4(mapa_shared(off, static_cast<uint32_t>(qr)));
+                    a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
+                }
+                const int n0 = nb * 128 + static_cast<int>(c4) * 4;
+                if (n0 < N) {
+                    if (p.bias != nullptr) {
+                        const float4 b = __ldg(reinterpret_cast<const float4*>(p.bias + n0));
+                        a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+                    }
+                    uint2 o;
+                    o.x = pack_bf16x2(a.x, a.y);
+                    o.y = pack_bf16x2(a.z, a.w);
+                    *reinterpret_cast<uint2*>(p.y + static_cast<size_t>(mb * 128 + row_t) * N + n0) = o;
+                }
+            }
+        }
+        if (threadIdx.x == 64) WQ_TRACE_AT(9);
+        cluster_sync();                                // peers are done reading this CTA's partial
+    }
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
+    if (threadIdx.x == 0) WQ_TRACE_AT(10);
 }
 
 }  // namespace
 
+// Largest cluster size (power of two, <= 16, <= number of K stages) that keeps every tile's
+// cluster resident at once; 1 when the tiles alone fill the GPU.
+int choose_split_uncached(int tiles, int num_kt, int num_sms, size_t smem) {
+    if (tiles * 2 > num_sms) return 1;
+    for (int s = 16; s >= 2; s >>= 1) {
+        if (s > num_kt || tiles * s > num_sms) continue;
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(static_cast<unsigned>(tiles * s));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = static_cast<unsigned>(s);
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, nvfp4_gemm_kernel, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            continue;
+        }
+        if (n >= tiles) return s;
+    }
+    return 1;
+}
+
+int choose_split(int tiles, int num_kt, int num_sms, size_t smem) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, int, int, size_t>, int> cache;
+    const auto key = std::make_tuple(tiles, num_kt, num_sms, smem);
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+    const int s = choose_split_uncached(tiles, num_kt, num_sms, smem);
+    cache[key] = s;
+    return s;
+}
+
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
     if (a.M <= 0) return cudaSuccess;
-    const Plan pl = make_plan(a.r, a.n_out);
+    // WQ_GEMM_STAGES=<n> caps the shared-memory ring depth (tuning)
+    const char* ms = std::getenv("WQ_GEMM_STAGES");
+    const Plan pl = make_plan(a.r, a.n_out, ms ? std::atoi(ms) : 8);
     if (pl.stages < 2) return cudaErrorInvalidConfiguration;
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(nvfp4_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(kMaxSmem));
         if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(nvfp4_gemm_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
         attr_set = true;
     }
+    const int tiles = ((a.M + 127) / 128) * ((a.N + 127) / 128);
+    const int num_kt = (a.K / 64 + 3) / 4;
+    const int split = a.force_split > 0 ? a.force_split : choose_split(tiles, num_kt, a.num_sms, pl.total);
+    if (split > num_kt || split > 16 || (split & (split - 1))) return cudaErrorInvalidValue;
     KParams kp{};
+    kp.split = split;
+    kp.y = static_cast<__nv_bfloat16*>(a.y);
     kp.M = a.M; kp.N = a.N; kp.K = a.K; kp.r = a.r; kp.n_out = a.n_out; kp.stages = pl.stages;
     kp.u_bytes = pl.u_bytes; kp.xo_bytes = pl.xo_bytes; kp.off_side = pl.off_side; kp.off_y = pl.off_y;
     kp.off_bar = pl.off_bar; kp.sf_col = pl.sf_col;
     kp.sfa = a.sfa; kp.sfb = a.sfb; kp.gA = a.gA; kp.gW = a.gW; kp.bias = a.bias; kp.err = a.err;
-    const int tiles = ((a.M + 127) / 128) * ((a.N + 127) / 128);
-    const int grid = tiles < a.num_sms ? tiles : a.num_sms;
-    nvfp4_gemm_kernel<<<grid, kThreads, pl.total, st>>>(*a.tmA, *a.tmB, *a.tmU, *a.tmQ, *a.tmXO, *a.tmWO,
-                                                         *a.tmY, kp);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(split > 1 ? tiles * split : (tiles < a.num_sms ? tiles : a.num_sms)));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = pl.total;
+    cfg.stream = st;
+    cudaLaunchAttribute at[2];
+    int na = 0;
+    at[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    if (split > 1) {
+        at[na].id = cudaLaunchAttributeClusterDimension;
+        at[na].val.clusterDim.x = static_cast<unsigned>(split);
+        at[na].val.clusterDim.y = 1;
+        at[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    cfg.attrs = at;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, nvfp4_gemm_kernel, *a.tmA, *a.tmB, *a.tmU, *a.tmQ, *a.tmXO, *a.tmWO, *a.tmY,
+                              kp);
 }
 
 }  // namespace wq

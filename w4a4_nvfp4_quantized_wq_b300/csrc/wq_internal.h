@@ -28,6 +28,9 @@ ActWorkspace carve_workspace(void* base, int M, int K, int r, int n_out);
 
 struct QuantArgs {
     const void* x;                  // bf16 [M, K]
+    const CUtensorMap* tmX;         // x as [M, K] bf16, box 64 x 32, swizzle 128B
+    const uint32_t* pfrag;          // P in mma.sync B-fragment order (see wq_api.cu)
+    int* err;                       // device error flag
     int M, K;
     const float* inv_s;             // [K] or null
     int rotate;
@@ -41,6 +44,7 @@ struct QuantArgs {
     uint8_t* sf;                    // scales, layout per `sf_layout`
     int sf_layout;                  // WQ_SCALE_LAYOUT_*
     float* g;                       // [M]
+    int num_sms;                    // used to spread small batches over more CTAs
 };
 
 cudaError_t launch_quantize_act(const QuantArgs& a, cudaStream_t stream);
@@ -61,6 +65,8 @@ struct GemmArgs {
     const float* bias;        // [N] or null
     int* err;                 // device error flag
     int num_sms;
+    void* y;                  // bf16 [M, N] (written directly by the split-K reduction)
+    int force_split;          // 0: choose; otherwise CTAs per tile (power of two <= 16)
 };
 
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream);
