@@ -38,7 +38,8 @@ WORKLOAD_TEXT = {
     "video_dit": "video DiT block: M=16384 tokens, QKV 1536->4608, o 1536->1536, up 1536->8960, "
                  "down 8960->1536, rank 32, 64 fp16 outlier channels, NVFP4 W4A4",
     "tiny": "single projection M=8, K=256 -> N=512, rank 16",
-    "backbone": "language backbone prefill M=768: QKV 2048->6144 and gate/up 2048->32768 (W4A4 layers)",
+    "backbone": "language backbone prefill M=768: QKV 2048->6144 and gate/up 2048->32768 in W4A4, "
+                "o_proj 2048->2048 and down 16384->2048 in W8A8 (int8 codes held as bf16)",
 }
 
 
@@ -65,8 +66,7 @@ def dist_env():
 def layers_of(name):
     import workloads as wl
     w = wl.WORKLOADS[name]
-    idx = [i for i, s in enumerate(w.layers) if s.mode == "w4a4"]
-    return w, idx
+    return w, list(range(len(w.layers)))
 
 
 class ClockSampler:
@@ -170,6 +170,16 @@ def gemm_algorithmic_bytes(M, K, N, r, n_out, bias):
     return a + w + side + (4 * N if bias else 0) + 2 * M * N
 
 
+def gemm8_algorithmic_bytes(M, K, N, bias):
+    """8-bit layer: int8 codes of A and W (one byte each), per-row and per-column scales,
+    bias, bf16 output."""
+    return M * K + 4 * M + N * K + 4 * N + (4 * N if bias else 0) + 2 * M * N
+
+
+def quant8_algorithmic_bytes(M, K, smooth):
+    return 2 * M * K + M * K + 4 * M + (4 * K if smooth else 0)
+
+
 def quant_algorithmic_bytes(M, K, r, n_out, smooth):
     """Bytes of the activation quantiser: bf16 x in, fp4 codes + scales + row scale out,
     the low-rank factor, U and x_O out."""
@@ -210,11 +220,16 @@ def time_oracle(layers, budget_s: float, n_threads: int, min_passes=1):
     """Time the oracle's per-token work (quantiser, low-rank, forward) on row samples;
     returns (tokens/s, rows per pass, passes, seconds)."""
     import oracle
-    prepared = [(L, oracle.prepare_weights(L.W, L.s, L.L1, L.L2, L.omega, L.rotate, n_threads)) for L in layers]
+    prepared = [(L, oracle.prepare_weights_int8(L.W, L.s, L.rotate, n_threads) if L.spec.mode == "w8a8" else
+                 oracle.prepare_weights(L.W, L.s, L.L1, L.L2, L.omega, L.rotate, n_threads)) for L in layers]
 
     def one(rows):
         for L, wqo in prepared:
             xb = L.x_bits[rows]
+            if L.spec.mode == "w8a8":
+                oracle.linear_forward_w8a8(oracle.quantize_act_int8(xb, L.s, L.rotate, n_threads), wqo, L.bias,
+                                           n_threads)
+                continue
             aq = oracle.quantize_act(xb, L.s, L.rotate, L.omega, n_threads=n_threads)
             U = oracle.lowrank_act(xb, wqo.P) if wqo.P.shape[1] else None
             oracle.linear_forward(aq, wqo, U, L.bias, n_threads=n_threads)
@@ -247,7 +262,8 @@ def run_reference(args):
     n_threads = os.cpu_count() or 1
     layers = oracle_layer_data(args.workload)
     import oracle as orc
-    prepared = [(L, orc.prepare_weights(L.W, L.s, L.L1, L.L2, L.omega, L.rotate, n_threads)) for L in layers]
+    prepared = [(L, orc.prepare_weights_int8(L.W, L.s, L.rotate, n_threads) if L.spec.mode == "w8a8" else
+                 orc.prepare_weights(L.W, L.s, L.L1, L.L2, L.omega, L.rotate, n_threads)) for L in layers]
     M = layers[0].M
     # size each step's row sample so that warmup + steps fit in about a minute
     t0 = time.perf_counter()
@@ -256,6 +272,9 @@ def run_reference(args):
     def step(rows):
         for L, wqo in prepared:
             xb = L.x_bits[rows]
+            if L.spec.mode == "w8a8":
+                orc.linear_forward_w8a8(orc.quantize_act_int8(xb, L.s, L.rotate, n_threads), wqo, L.bias, n_threads)
+                continue
             aq = orc.quantize_act(xb, L.s, L.rotate, L.omega, n_threads=n_threads)
             U = orc.lowrank_act(xb, wqo.P) if wqo.P.shape[1] else None
             orc.linear_forward(aq, wqo, U, L.bias, n_threads=n_threads)
@@ -308,8 +327,11 @@ def run_wq(args):
     stream = torch.cuda.Stream(device=dev)
     H = []
     for L in layers:
-        w = wq.wq_prepare_weights(L.spec.K, L.spec.N, L.W, L.bias, L.s, L.L1, L.L2,
-                                  L.omega if L.omega.size else None, rotate=L.rotate)
+        if L.spec.mode == "w8a8":
+            w = wq.wq_prepare_weights(L.spec.K, L.spec.N, L.W, L.bias, L.s, rotate=L.rotate, mode=wq.WQ_MODE_W8A8)
+        else:
+            w = wq.wq_prepare_weights(L.spec.K, L.spec.N, L.W, L.bias, L.s, L.L1, L.L2,
+                                      L.omega if L.omega.size else None, rotate=L.rotate)
         x = torch.from_numpy(L.x_bits.view(np.int16)).view(torch.bfloat16).to(dev)
         y = torch.empty((M, L.spec.N), dtype=torch.bfloat16, device=dev)
         wsb = torch.empty(max(256, wq.wq_workspace_bytes(w, M)), dtype=torch.uint8, device=dev)
@@ -318,7 +340,10 @@ def run_wq(args):
 
     def step():
         for h in H:
-            wq.wq_linear_forward(h["w"], h["x"], h["y"], h["ws"], stream)
+            if h["L"].spec.mode == "w8a8":
+                wq.wq_linear_forward_w8a8(h["w"], h["x"], h["y"], h["ws"], stream)
+            else:
+                wq.wq_linear_forward(h["w"], h["x"], h["y"], h["ws"], stream)
 
     with torch.cuda.stream(stream):
         step()
@@ -373,7 +398,12 @@ def run_wq(args):
     per_kernel = {}
     for li, h in enumerate(H):
         L, w = h["L"], h["w"]
-        codes, sf, g, xo, u = wq.wq_quantize_activations(h["w"], h["x"], wq.WQ_SCALE_LAYOUT_MMA, stream)
+        w8 = L.spec.mode == "w8a8"
+        if w8:
+            codes, g = wq.wq_quantize_activations_w8a8(w, h["x"], stream)
+            sf = xo = u = None
+        else:
+            codes, sf, g, xo, u = wq.wq_quantize_activations(h["w"], h["x"], wq.WQ_SCALE_LAYOUT_MMA, stream)
         torch.cuda.synchronize()
         for kname in ("quant", "gemm"):
             evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
@@ -382,7 +412,13 @@ def run_wq(args):
                     flush.zero_()
                     if i >= 3:
                         evs[i - 3][0].record(stream)
-                    if kname == "quant":
+                    if kname == "quant" and w8:
+                        wq.lib().wq_quantize_activations_w8a8(
+                            __import__("ctypes").c_void_p(w.handle), __import__("ctypes").c_void_p(h["x"].data_ptr()),
+                            M, __import__("ctypes").c_void_p(codes.data_ptr()),
+                            __import__("ctypes").c_void_p(g.data_ptr()),
+                            __import__("ctypes").c_void_p(stream.cuda_stream))
+                    elif kname == "quant":
                         wq.wq_quantize_activations_into(w, h["x"], codes, sf, g, xo, u, stream)
                     else:
                         wq.wq_linear_forward_quantized(w, codes, sf, g, u, xo, h["y"], stream)
@@ -392,10 +428,12 @@ def run_wq(args):
             ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
             spec = L.spec
             if kname == "gemm":
-                byts = gemm_algorithmic_bytes(M, spec.K, spec.N, L.rank, L.omega.size, L.bias is not None)
+                byts = gemm8_algorithmic_bytes(M, spec.K, spec.N, L.bias is not None) if w8 else \
+                    gemm_algorithmic_bytes(M, spec.K, spec.N, L.rank, L.omega.size, L.bias is not None)
                 flops = 2.0 * M * spec.K * spec.N
             else:
-                byts = quant_algorithmic_bytes(M, spec.K, L.rank, L.omega.size, L.s is not None)
+                byts = quant8_algorithmic_bytes(M, spec.K, L.s is not None) if w8 else \
+                    quant_algorithmic_bytes(M, spec.K, L.rank, L.omega.size, L.s is not None)
                 flops = 0.0
             per_kernel[(kname, li)] = dict(ms=ms, bytes=byts, flops=flops)
     tot = {k: sum(v["ms"] for (kk, _), v in per_kernel.items() if kk == k) for k in ("quant", "gemm")}

@@ -65,13 +65,18 @@ typedef enum wq_status {
 enum { WQ_MODE_W4A4 = 0, WQ_MODE_W8A8 = 1 };
 enum { WQ_SCALE_LAYOUT_ROWMAJOR = 0, WQ_SCALE_LAYOUT_MMA = 1 };
 
+/* mode = WQ_MODE_W8A8 selects the selective 8-bit path (FoldQuantVLA, Key Contribution 3:
+ * attention-output and FFN down projections kept at W8A8) in the same smoothed + rotated basis:
+ * per-row activation scale a = amax / 127, per-output-column weight scale w = amax / 127,
+ * q = round-half-even(v / scale) clamped to [-127, 127]; y = a[m] w[n] (sum_k qa qw) + b.
+ * rank and n_outliers must be 0 in this mode. */
 typedef struct wq_config {
     int K;            /* input features (reduction dimension)                              */
     int N;            /* output features                                                   */
     int rank;         /* low-rank branch rank r (0 disables the branch)                    */
     int n_outliers;   /* |Omega|, channels of the rotated basis kept in fp16 (0 disables)  */
     int rotate;       /* 1: block-64 Walsh-Hadamard rotation; 0: none                     */
-    int mode;         /* WQ_MODE_W4A4 (only mode implemented by wq_linear_forward)         */
+    int mode;         /* WQ_MODE_W4A4 (wq_linear_forward) or WQ_MODE_W8A8 (..._w8a8)      */
 } wq_config;
 
 /*
@@ -145,7 +150,9 @@ WQ_API wq_status wq_quantize_activations(wq_weights_t h, const void *x, int M, i
 
 /*
  * GEMM + fused epilogue alone, on activations already quantised by
- * wq_quantize_activations(..., WQ_SCALE_LAYOUT_MMA, ...).  All pointers are device:
+ * wq_quantize_activations(..., WQ_SCALE_LAYOUT_MMA, ...) (or, for a W8A8 handle, by
+ * wq_quantize_activations_w8a8, with scales_mma NULL and gscale the per-row scale a).
+ * All pointers are device:
  *   codes [M, K/2], scales_mma (MMA layout), gscale [M], u bf16 [M, rank] (required when
  *   rank > 0), x_omega fp16 [M, n_outliers] (required when n_outliers > 0), y bf16 [M, N].
  * One kernel runs on `stream`.
@@ -153,6 +160,25 @@ WQ_API wq_status wq_quantize_activations(wq_weights_t h, const void *x, int M, i
 WQ_API wq_status wq_linear_forward_quantized(wq_weights_t h, const uint8_t *codes, const uint8_t *scales_mma,
                                              const float *gscale, const void *u, const void *x_omega, int M,
                                              void *y, void *stream);
+
+/*
+ * The selective 8-bit projection (handle prepared with mode WQ_MODE_W8A8): the 8-bit variant of
+ * the fused quantiser, then the tcgen05 GEMM on the int8 codes (held as exact bf16 integers,
+ * kind::f16, fp32 accumulation) with the epilogue y = a[m] w[n] acc + b.
+ *   x, y, workspace  as for wq_linear_forward (workspace: wq_workspace_bytes(h, M)).
+ */
+WQ_API wq_status wq_linear_forward_w8a8(wq_weights_t h, const void *x, int M, void *y,
+                                        void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * The 8-bit quantiser alone (W8A8 handles), device outputs:
+ *   codes  bf16 [M, K] holding the integers q in [-127, 127];  scale fp32 [M] (a = amax / 127).
+ */
+WQ_API wq_status wq_quantize_activations_w8a8(wq_weights_t h, const void *x, int M, void *codes,
+                                              float *scale, void *stream);
+
+/* W8A8 weights back to host (synchronous): q int8 [N, K] (K-major), w fp32 [N]. */
+WQ_API wq_status wq_export_weights_w8a8(wq_weights_t h, int8_t *q, float *w);
 
 /*
  * Copy the prepared weights back to host memory in canonical layouts (synchronous):

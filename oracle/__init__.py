@@ -66,6 +66,12 @@ def lib() -> ctypes.CDLL:
             L.orc_linear_forward.restype = i32
             L.orc_forward_noquant.argtypes = [P, P, i64, i64, i64, P, P, i32, P, P, P, i32, P, P]
             L.orc_forward_noquant.restype = i32
+            L.orc_quantize_act_int8.argtypes = [P, i64, i64, P, i32, P, P, i32]
+            L.orc_quantize_act_int8.restype = i32
+            L.orc_quantize_weights_int8.argtypes = [P, i64, i64, P, P]
+            L.orc_quantize_weights_int8.restype = i32
+            L.orc_linear_forward_w8a8.argtypes = [P, P, i64, P, P, i64, i64, P, P, i32]
+            L.orc_linear_forward_w8a8.restype = i32
             _lib = L
     return _lib
 
@@ -268,3 +274,51 @@ def reference_forward(layer, n_threads: int = 0, rows: Optional[np.ndarray] = No
     U = lowrank_act(x_bits, wq.P) if wq.P.shape[1] else None
     y = linear_forward(aq, wq, U, layer.bias, n_threads=n_threads)
     return y, aq, wq, U
+
+
+# ------------------------------------------------------------------ W8A8
+@dataclass
+class Int8Quant:
+    q: np.ndarray            # int8 [rows, K]
+    scale: np.ndarray        # fp32 [rows]
+
+
+def quantize_act_int8(x_bits, s, rotate, n_threads: int = 0) -> Int8Quant:
+    """Symmetric per-token int8 of the transformed activations (FoldQuantVLA, Key
+    Contribution 3: selective W8A8 in the shared basis)."""
+    x_bits = _c(x_bits, np.uint16)
+    M, K = x_bits.shape
+    inv_s = inv_smoothing(s)
+    q = np.zeros((M, K), np.int8)
+    a = np.zeros(M, np.float32)
+    rc = lib().orc_quantize_act_int8(_p(x_bits), M, K, _p(inv_s), int(rotate), _p(q), _p(a), int(n_threads))
+    if rc:
+        raise ValueError(f"orc_quantize_act_int8 failed: {rc}")
+    return Int8Quant(q, a)
+
+
+def prepare_weights_int8(W, s, rotate, n_threads: int = 0) -> Int8Quant:
+    """Fold smoothing + rotation into W (Proposition 1), then per-output-channel int8."""
+    wq = prepare_weights(W, s, None, None, None, rotate, n_threads)
+    K, N = wq.Rp.shape
+    q = np.zeros((N, K), np.int8)
+    w = np.zeros(N, np.float32)
+    lib().orc_quantize_weights_int8(_p(np.ascontiguousarray(wq.Rp)), K, N, _p(q), _p(w))
+    return Int8Quant(q, w)
+
+
+def linear_forward_w8a8(aq: Int8Quant, wq8: Int8Quant, bias, n_threads: int = 0) -> np.ndarray:
+    M, K = aq.q.shape
+    N = wq8.q.shape[0]
+    y = np.zeros((M, N), np.float64)
+    bias = _c(bias, np.float32)
+    lib().orc_linear_forward_w8a8(_p(aq.q), _p(aq.scale), M, _p(wq8.q), _p(wq8.scale), N, K, _p(bias), _p(y),
+                                  int(n_threads))
+    return y
+
+
+def reference_forward_w8a8(layer, n_threads: int = 0, rows=None):
+    x_bits = layer.x_bits if rows is None else layer.x_bits[rows]
+    wq8 = prepare_weights_int8(layer.W, layer.s, layer.rotate, n_threads)
+    aq = quantize_act_int8(x_bits, layer.s, layer.rotate, n_threads)
+    return linear_forward_w8a8(aq, wq8, layer.bias, n_threads), aq, wq8

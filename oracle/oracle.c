@@ -491,3 +491,95 @@ int orc_forward_noquant(const float *xt, const float *xo, long M, long K, long N
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------ W8A8 (INT8) */
+/* Selective 8-bit projections (FoldQuantVLA, Key Contribution 3: o_proj and down_proj kept at
+ * W8A8) in the same transformed basis as the 4-bit layers (Key Contribution 1: one basis for
+ * every consumer).  Symmetric int8: per row of the activations, per output column of the
+ * weights, scale = amax / 127, q = round-half-even(v / scale) clamped to [-127, 127]; both
+ * steps one IEEE fp32 operation.  The product is accumulated exactly in int64. */
+
+static int8_t int8_rne(float v, float scale)
+{
+    if (scale == 0.0f) return 0;
+    float t = v / scale;
+    double r = nearbyint((double)t);          /* default rounding mode: nearest even */
+    if (r > 127.0) r = 127.0;
+    if (r < -127.0) r = -127.0;
+    return (int8_t)r;
+}
+
+float orc_int8_scale(float amax) { return amax / 127.0f; }
+
+/* x bf16 [M, K] -> q int8 [M, K], a fp32 [M] (smoothing and rotation as for W4A4). */
+int orc_quantize_act_int8(const uint16_t *x_bf16, long M, long K, const float *inv_s, int rotate,
+                          int8_t *q, float *a, int n_threads)
+{
+    if (K % 16 || (rotate && K % 64)) return -1;
+#ifdef _OPENMP
+    if (n_threads > 0) omp_set_num_threads(n_threads);
+#else
+    (void)n_threads;
+#endif
+    int rc = 0;
+#pragma omp parallel
+    {
+        float *xt = (float *)malloc(sizeof(float) * (size_t)K);
+        if (!xt) {
+#pragma omp atomic write
+            rc = -4;
+        } else {
+#pragma omp for schedule(static)
+            for (long m = 0; m < M; ++m) {
+                orc_act_transform_row(x_bf16 + m * K, K, inv_s, rotate, xt);
+                float amax = 0.0f;
+                for (long k = 0; k < K; ++k) {
+                    float v = fabsf(xt[k]);
+                    if (v > amax) amax = v;
+                }
+                float s = orc_int8_scale(amax);
+                a[m] = s;
+                for (long k = 0; k < K; ++k) q[m * K + k] = int8_rne(xt[k], s);
+            }
+            free(xt);
+        }
+    }
+    return rc;
+}
+
+/* Folded weight Rp fp32 [K, N] -> q int8 [N, K] (K-major), w fp32 [N]. */
+int orc_quantize_weights_int8(const float *Rp, long K, long N, int8_t *q, float *w)
+{
+    for (long n = 0; n < N; ++n) {
+        float amax = 0.0f;
+        for (long k = 0; k < K; ++k) {
+            float v = fabsf(Rp[k * N + n]);
+            if (v > amax) amax = v;
+        }
+        float s = orc_int8_scale(amax);
+        w[n] = s;
+        for (long k = 0; k < K; ++k) q[n * K + k] = int8_rne(Rp[k * N + n], s);
+    }
+    return 0;
+}
+
+/* y[m][n] = (sum_k qa[m][k] qw[n][k]) * a[m] * w[n] + b[n]; exact int64 sum, fp64 epilogue. */
+int orc_linear_forward_w8a8(const int8_t *qa, const float *a, long M, const int8_t *qw, const float *w, long N,
+                            long K, const float *bias, double *y, int n_threads)
+{
+#ifdef _OPENMP
+    if (n_threads > 0) omp_set_num_threads(n_threads);
+#else
+    (void)n_threads;
+#endif
+#pragma omp parallel for schedule(static)
+    for (long m = 0; m < M; ++m)
+        for (long n = 0; n < N; ++n) {
+            int64_t acc = 0;
+            for (long k = 0; k < K; ++k) acc += (int64_t)qa[m * K + k] * (int64_t)qw[n * K + k];
+            double v = (double)acc * (double)a[m] * (double)w[n];
+            if (bias) v += (double)bias[n];
+            y[m * N + n] = v;
+        }
+    return 0;
+}

@@ -43,7 +43,8 @@ def _cfg(K=256, N=128, r=0, no=0, rot=1, mode=0):
     (dict(N=24), wq.WQ_ERR_UNSUPPORTED),
     (dict(r=8), wq.WQ_ERR_UNSUPPORTED),
     (dict(no=20), wq.WQ_ERR_UNSUPPORTED),
-    (dict(mode=1), wq.WQ_ERR_UNSUPPORTED),
+    (dict(mode=1, r=16), wq.WQ_ERR_UNSUPPORTED),
+    (dict(mode=2), wq.WQ_ERR_INVALID),
     (dict(rot=2), wq.WQ_ERR_INVALID),
     (dict(K=-64), wq.WQ_ERR_INVALID),
 ])

@@ -23,7 +23,8 @@ WQ_SCALE_LAYOUT_ROWMAJOR, WQ_SCALE_LAYOUT_MMA = 0, 1
 
 EXPORTED = ["wq_prepare_weights", "wq_get_config", "wq_workspace_bytes", "wq_linear_forward",
             "wq_host_workspace_bytes", "wq_linear_forward_host", "wq_quantize_activations",
-            "wq_linear_forward_quantized", "wq_linear_forward_noalloc",
+            "wq_linear_forward_quantized", "wq_linear_forward_noalloc", "wq_linear_forward_w8a8",
+            "wq_quantize_activations_w8a8", "wq_export_weights_w8a8",
             "wq_export_weights", "wq_check_device_error", "wq_free_weights", "wq_last_error"]
 
 
@@ -68,6 +69,12 @@ def lib() -> ctypes.CDLL:
         L.wq_linear_forward_quantized.restype = I
         L.wq_linear_forward_noalloc.argtypes = [P, P, I, P, P]
         L.wq_linear_forward_noalloc.restype = I
+        L.wq_linear_forward_w8a8.argtypes = [P, P, I, P, P, S, P]
+        L.wq_linear_forward_w8a8.restype = I
+        L.wq_quantize_activations_w8a8.argtypes = [P, P, I, P, P, P]
+        L.wq_quantize_activations_w8a8.restype = I
+        L.wq_export_weights_w8a8.argtypes = [P, P, P]
+        L.wq_export_weights_w8a8.restype = I
         L.wq_export_weights.argtypes = [P, P, P, P, P, P, P]
         L.wq_export_weights.restype = I
         L.wq_check_device_error.argtypes = [P, P]
@@ -271,3 +278,39 @@ def mma_scales_to_rowmajor(sf_mma: np.ndarray, M: int, K: int) -> np.ndarray:
     b = np.arange(K // 16)[None, :]
     off = ((m // 128) * (K // 64) + b // 4) * 512 + (m % 32) * 16 + ((m % 128) // 32) * 4 + (b % 4)
     return sf[off]
+
+
+# ------------------------------------------------------------------ selective 8-bit layers
+def wq_linear_forward_w8a8(w: Weights, x, y=None, workspace=None, stream=None):
+    """y[M, N] bf16 = W8A8 projection of x[M, K] bf16 (handle prepared with WQ_MODE_W8A8)."""
+    import torch
+    assert x.dtype == torch.bfloat16 and x.is_cuda and x.is_contiguous() and x.shape[-1] == w.K
+    M = x.shape[0]
+    if y is None:
+        y = torch.empty((M, w.N), dtype=torch.bfloat16, device=x.device)
+    if workspace is None:
+        workspace = _alloc_workspace(wq_workspace_bytes(w, M), x.device)
+    _check(lib().wq_linear_forward_w8a8(ctypes.c_void_p(w.handle), ctypes.c_void_p(x.data_ptr()), M,
+                                        ctypes.c_void_p(y.data_ptr()), ctypes.c_void_p(workspace.data_ptr()),
+                                        workspace.numel(), ctypes.c_void_p(_stream_ptr(stream))))
+    return y
+
+
+def wq_quantize_activations_w8a8(w: Weights, x, stream=None):
+    """8-bit quantiser alone: (codes bf16 [M, K] holding integers, scale fp32 [M]) on the device."""
+    import torch
+    M, K = x.shape
+    codes = torch.empty((M, K), dtype=torch.bfloat16, device=x.device)
+    scale = torch.empty(M, dtype=torch.float32, device=x.device)
+    _check(lib().wq_quantize_activations_w8a8(ctypes.c_void_p(w.handle), ctypes.c_void_p(x.data_ptr()), M,
+                                              ctypes.c_void_p(codes.data_ptr()), ctypes.c_void_p(scale.data_ptr()),
+                                              ctypes.c_void_p(_stream_ptr(stream))))
+    return codes, scale
+
+
+def wq_export_weights_w8a8(w: Weights):
+    q = np.zeros((w.N, w.K), np.int8)
+    sc = np.zeros(w.N, np.float32)
+    _check(lib().wq_export_weights_w8a8(ctypes.c_void_p(w.handle), q.ctypes.data_as(ctypes.c_void_p),
+                                        sc.ctypes.data_as(ctypes.c_void_p)))
+    return q, sc

@@ -159,6 +159,7 @@ struct wq_weights {
     uint16_t* d_Qt = nullptr;      // [N, r] bf16
     uint16_t* d_WOt = nullptr;     // [N, n_out] fp16
     int* d_err = nullptr;
+    float* d_colscale = nullptr;   // W8A8: per-output-column weight scale [N]
     CUtensorMap tmB{}, tmQ{}, tmWO{};
     // activation / output tensor maps, re-encoded when the buffers change
     std::mutex mu;
@@ -180,7 +181,9 @@ wq_status check_config(const wq_config* c) {
     if (!c) return fail(WQ_ERR_INVALID, "cfg is NULL");
     if (c->K <= 0 || c->N <= 0 || c->rank < 0 || c->n_outliers < 0)
         return fail(WQ_ERR_INVALID, "negative or zero size in cfg");
-    if (c->mode != WQ_MODE_W4A4) return fail(WQ_ERR_UNSUPPORTED, "only WQ_MODE_W4A4 is implemented");
+    if (c->mode != WQ_MODE_W4A4 && c->mode != WQ_MODE_W8A8) return fail(WQ_ERR_INVALID, "unknown mode");
+    if (c->mode == WQ_MODE_W8A8 && (c->rank != 0 || c->n_outliers != 0))
+        return fail(WQ_ERR_UNSUPPORTED, "WQ_MODE_W8A8 takes rank 0 and no outlier channels");
     if (c->rotate != 0 && c->rotate != 1) return fail(WQ_ERR_INVALID, "rotate must be 0 or 1");
     if (c->K % 64 || c->K > 16384) return fail(WQ_ERR_UNSUPPORTED, "K must be a multiple of 64 and <= 16384");
     if (c->N % 16) return fail(WQ_ERR_UNSUPPORTED, "N must be a multiple of 16");
@@ -202,6 +205,7 @@ void free_device(wq_weights* h) {
     cudaFree(h->d_Qt);
     cudaFree(h->d_WOt);
     cudaFree(h->d_err);
+    cudaFree(h->d_colscale);
 }
 
 template <typename T>
@@ -310,6 +314,47 @@ WQ_API wq_status wq_prepare_weights(const wq_config* cfg, const float* W, const 
         }
     }
 
+    if (cfg->mode == WQ_MODE_W8A8) {
+        // ---- symmetric int8 per output column (kept as exact bf16 integers, K-major)
+        std::vector<uint16_t> q8(static_cast<size_t>(N) * K);
+        std::vector<float> wsc(N);
+        parallel_for(static_cast<size_t>(N), [&](size_t n) {
+            float am = 0.0f;
+            for (int k = 0; k < K; ++k) am = std::max(am, std::fabs(Rp[static_cast<size_t>(k) * N + n]));
+            const float sc = am / 127.0f;
+            wsc[n] = sc;
+            for (int k = 0; k < K; ++k) {
+                float r = 0.0f;
+                if (sc != 0.0f) r = std::nearbyint(Rp[static_cast<size_t>(k) * N + n] / sc);
+                r = std::min(127.0f, std::max(-127.0f, r));
+                q8[n * K + k] = bf16_bits(r);
+            }
+        });
+        wq_weights* h = new (std::nothrow) wq_weights();
+        if (!h) return fail(WQ_ERR_OOM, "host allocation failed");
+        h->cfg = *cfg;
+        h->gW = 1.0f;
+        cudaStream_t cs = static_cast<cudaStream_t>(stream);
+        auto bail = [&](wq_status e) { free_device(h); delete h; return e; };
+        if (cudaGetDevice(&h->device) != cudaSuccess) return bail(fail(WQ_ERR_CUDA, "cudaGetDevice failed"));
+        cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
+        std::vector<float> bias_f(N, 0.0f);
+        if (bias) std::copy(bias, bias + N, bias_f.begin());
+        if ((st = upload(&h->d_codes, q8.data(), q8.size() * 2, cs)) != WQ_OK) return bail(st);
+        if ((st = upload(&h->d_colscale, wsc.data(), N * 4, cs)) != WQ_OK) return bail(st);
+        if (bias && (st = upload(&h->d_bias, bias_f.data(), N * 4, cs)) != WQ_OK) return bail(st);
+        if (s && (st = upload(&h->d_inv_s, inv_s.data(), K * 4, cs)) != WQ_OK) return bail(st);
+        if (cudaMalloc(&h->d_err, sizeof(int)) != cudaSuccess) return bail(fail(WQ_ERR_OOM, "cudaMalloc failed"));
+        if (cudaMemsetAsync(h->d_err, 0, sizeof(int), cs) != cudaSuccess) return bail(fail(WQ_ERR_CUDA, "memset"));
+        if (cudaStreamSynchronize(cs) != cudaSuccess) return bail(fail(WQ_ERR_CUDA, "upload synchronise failed"));
+        const char* why = "";
+        if (!wq::encode_tmap_2d(&h->tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h->d_codes, K, N, 2ull * K, 64, 128,
+                                CU_TENSOR_MAP_SWIZZLE_128B, &why))
+            return bail(fail(WQ_ERR_CUDA, why));
+        *out = h;
+        return WQ_OK;
+    }
+
     // ---- NVFP4 with one fp32 scale for the tensor; column n quantised along K
     float amax = 0.0f;
     for (float v : Rp) amax = std::max(amax, std::fabs(v));
@@ -383,8 +428,13 @@ WQ_API wq_status wq_prepare_weights(const wq_config* cfg, const float* W, const 
     return WQ_OK;
 }
 
+static size_t w8_workspace_bytes(int M, int K) {
+    return align_up(static_cast<size_t>(M) * K * 2, 1024) + align_up(static_cast<size_t>(M) * 4, 1024);
+}
+
 WQ_API size_t wq_workspace_bytes(wq_weights_t h, int M) {
     if (!h || M < 0) return 0;
+    if (h->cfg.mode == WQ_MODE_W8A8) return w8_workspace_bytes(M, h->cfg.K);
     return wq::carve_workspace(nullptr, M, h->cfg.K, h->cfg.rank, h->cfg.n_outliers).bytes;
 }
 
@@ -429,6 +479,7 @@ static wq_status run_quant(wq_weights_t h, const void* x, int M, int layout, uin
     qa.sf_layout = layout;
     qa.g = g;
     qa.num_sms = h->num_sms;
+    qa.int8 = h->cfg.mode == WQ_MODE_W8A8;
     const cudaError_t e = wq::launch_quantize_act(qa, st);
     if (e != cudaSuccess) return cuda_fail(e, "activation quantiser launch");
     return WQ_OK;
@@ -440,6 +491,7 @@ WQ_API wq_status wq_quantize_activations(wq_weights_t h, const void* x, int M, i
     if (M < 0) return fail(WQ_ERR_INVALID, "M < 0");
     if (M == 0) return WQ_OK;
     if (!x || !codes || !scales || !gscale) return fail(WQ_ERR_INVALID, "NULL buffer");
+    if (h->cfg.mode != WQ_MODE_W4A4) return fail(WQ_ERR_INVALID, "W8A8 handle: use wq_quantize_activations_w8a8");
     if (h->cfg.n_outliers > 0 && !x_omega)
         return fail(WQ_ERR_INVALID, "x_omega is required when n_outliers > 0 (the kept channels are zeroed)");
     if (scale_layout != WQ_SCALE_LAYOUT_ROWMAJOR && scale_layout != WQ_SCALE_LAYOUT_MMA)
@@ -457,8 +509,11 @@ static wq_status run_gemm(wq_weights_t h, const uint8_t* codes, const uint8_t* s
     std::lock_guard<std::mutex> lk(h->mu);
     if (h->key_codes != codes || h->key_u != u || h->key_xo != xo || h->key_y != y || h->key_M != M) {
         const char* why = "";
-        bool ok = wq::encode_tmap_2d(&h->tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, K / 2, M, K / 2, 128, 128,
-                                     CU_TENSOR_MAP_SWIZZLE_128B, &why) &&
+        const bool w8 = h->cfg.mode == WQ_MODE_W8A8;
+        bool ok = (w8 ? wq::encode_tmap_2d(&h->tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, codes, K, M, 2ull * K, 64, 128,
+                                           CU_TENSOR_MAP_SWIZZLE_128B, &why)
+                      : wq::encode_tmap_2d(&h->tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, K / 2, M, K / 2, 128, 128,
+                                           CU_TENSOR_MAP_SWIZZLE_128B, &why)) &&
                   wq::encode_tmap_2d(&h->tmY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, y, N, M, 2ull * N, 64, 32,
                                      CU_TENSOR_MAP_SWIZZLE_128B, &why);
         if (ok && r)
@@ -484,6 +539,8 @@ static wq_status run_gemm(wq_weights_t h, const uint8_t* codes, const uint8_t* s
     ga.sfa = sf; ga.sfb = h->d_sf; ga.gA = g; ga.gW = h->gW; ga.bias = h->d_bias;
     ga.err = h->d_err; ga.num_sms = h->num_sms;
     ga.y = y;
+    ga.w8 = h->cfg.mode == WQ_MODE_W8A8;
+    ga.colscale = h->d_colscale;
     // WQ_GEMM_SPLIT=<1|2|4|8|16> pins the number of CTAs per output tile (tuning and tests)
     const char* fs = std::getenv("WQ_GEMM_SPLIT");
     ga.force_split = fs ? std::atoi(fs) : 0;
@@ -501,6 +558,7 @@ WQ_API wq_status wq_linear_forward(wq_weights_t h, const void* x, int M, void* y
     if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15)
         return fail(WQ_ERR_INVALID, "x and y must be 16-byte aligned");
     if (reinterpret_cast<uintptr_t>(workspace) & 255) return fail(WQ_ERR_INVALID, "workspace must be 256-byte aligned");
+    if (h->cfg.mode != WQ_MODE_W4A4) return fail(WQ_ERR_INVALID, "W8A8 handle: use wq_linear_forward_w8a8");
     const int K = h->cfg.K, r = h->cfg.rank, no = h->cfg.n_outliers;
     const wq::ActWorkspace ws = wq::carve_workspace(workspace, M, K, r, no);
     if (workspace_bytes < ws.bytes) return fail(WQ_ERR_INVALID, "workspace too small");
@@ -518,7 +576,8 @@ WQ_API wq_status wq_linear_forward_quantized(wq_weights_t h, const uint8_t* code
     if (!h) return fail(WQ_ERR_INVALID, "NULL handle");
     if (M < 0) return fail(WQ_ERR_INVALID, "M < 0");
     if (M == 0) return WQ_OK;
-    if (!codes || !scales_mma || !gscale || !y) return fail(WQ_ERR_INVALID, "NULL buffer");
+    const bool w8 = h->cfg.mode == WQ_MODE_W8A8;
+    if (!codes || (!scales_mma && !w8) || !gscale || !y) return fail(WQ_ERR_INVALID, "NULL buffer");
     if (h->cfg.rank > 0 && !u) return fail(WQ_ERR_INVALID, "u is required when rank > 0");
     if (h->cfg.n_outliers > 0 && !x_omega) return fail(WQ_ERR_INVALID, "x_omega is required when n_outliers > 0");
     if ((reinterpret_cast<uintptr_t>(codes) | reinterpret_cast<uintptr_t>(scales_mma) |
@@ -526,6 +585,53 @@ WQ_API wq_status wq_linear_forward_quantized(wq_weights_t h, const uint8_t* code
         return fail(WQ_ERR_INVALID, "device buffers must be 16-byte aligned");
     return run_gemm(h, codes, scales_mma, gscale, static_cast<const uint16_t*>(u),
                     static_cast<const uint16_t*>(x_omega), M, y, static_cast<cudaStream_t>(stream));
+}
+
+WQ_API wq_status wq_linear_forward_w8a8(wq_weights_t h, const void* x, int M, void* y, void* workspace,
+                                        size_t workspace_bytes, void* stream) {
+    if (!h) return fail(WQ_ERR_INVALID, "NULL handle");
+    if (h->cfg.mode != WQ_MODE_W8A8) return fail(WQ_ERR_INVALID, "handle was not prepared with WQ_MODE_W8A8");
+    if (M < 0) return fail(WQ_ERR_INVALID, "M < 0");
+    if (M == 0) return WQ_OK;
+    if (!x || !y || !workspace) return fail(WQ_ERR_INVALID, "NULL buffer");
+    if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15)
+        return fail(WQ_ERR_INVALID, "x and y must be 16-byte aligned");
+    if (reinterpret_cast<uintptr_t>(workspace) & 255) return fail(WQ_ERR_INVALID, "workspace must be 256-byte aligned");
+    const int K = h->cfg.K;
+    if (workspace_bytes < w8_workspace_bytes(M, K)) return fail(WQ_ERR_INVALID, "workspace too small");
+    uint8_t* codes = static_cast<uint8_t*>(workspace);
+    float* a = reinterpret_cast<float*>(codes + align_up(static_cast<size_t>(M) * K * 2, 1024));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    wq_status s = run_quant(h, x, M, WQ_SCALE_LAYOUT_ROWMAJOR, codes, nullptr, a, nullptr, nullptr, st);
+    if (s != WQ_OK) return s;
+    return run_gemm(h, codes, nullptr, a, nullptr, nullptr, M, y, st);
+}
+
+WQ_API wq_status wq_quantize_activations_w8a8(wq_weights_t h, const void* x, int M, void* codes, float* scale,
+                                              void* stream) {
+    if (!h) return fail(WQ_ERR_INVALID, "NULL handle");
+    if (h->cfg.mode != WQ_MODE_W8A8) return fail(WQ_ERR_INVALID, "handle was not prepared with WQ_MODE_W8A8");
+    if (M < 0) return fail(WQ_ERR_INVALID, "M < 0");
+    if (M == 0) return WQ_OK;
+    if (!x || !codes || !scale) return fail(WQ_ERR_INVALID, "NULL buffer");
+    if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(codes)) & 15)
+        return fail(WQ_ERR_INVALID, "device buffers must be 16-byte aligned");
+    return run_quant(h, x, M, WQ_SCALE_LAYOUT_ROWMAJOR, static_cast<uint8_t*>(codes), nullptr, scale, nullptr,
+                     nullptr, static_cast<cudaStream_t>(stream));
+}
+
+WQ_API wq_status wq_export_weights_w8a8(wq_weights_t h, int8_t* q, float* w) {
+    if (!h) return fail(WQ_ERR_INVALID, "NULL handle");
+    if (h->cfg.mode != WQ_MODE_W8A8) return fail(WQ_ERR_INVALID, "handle was not prepared with WQ_MODE_W8A8");
+    const int K = h->cfg.K, N = h->cfg.N;
+    if (q) {
+        std::vector<uint16_t> b(static_cast<size_t>(N) * K);
+        WQ_CUDA(cudaMemcpy(b.data(), h->d_codes, b.size() * 2, cudaMemcpyDeviceToHost), "export");
+        for (size_t i = 0; i < b.size(); ++i)
+            q[i] = static_cast<int8_t>(__bfloat162float(__ushort_as_bfloat16(b[i])));
+    }
+    if (w) WQ_CUDA(cudaMemcpy(w, h->d_colscale, static_cast<size_t>(N) * 4, cudaMemcpyDeviceToHost), "export");
+    return WQ_OK;
 }
 
 WQ_API wq_status wq_linear_forward_host(wq_weights_t h, const void* x_host, int M, void* y_host, void* workspace,
@@ -542,7 +648,8 @@ WQ_API wq_status wq_linear_forward_host(wq_weights_t h, const void* x_host, int 
     void* dy = base + wsb + align_up(xb, 1024);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     WQ_CUDA(cudaMemcpyAsync(dx, x_host, xb, cudaMemcpyHostToDevice, st), "x upload");
-    const wq_status s = wq_linear_forward(h, dx, M, dy, workspace, wsb, stream);
+    const wq_status s = h->cfg.mode == WQ_MODE_W8A8 ? wq_linear_forward_w8a8(h, dx, M, dy, workspace, wsb, stream)
+                                                    : wq_linear_forward(h, dx, M, dy, workspace, wsb, stream);
     if (s != WQ_OK) return s;
     WQ_CUDA(cudaMemcpyAsync(y_host, dy, yb, cudaMemcpyDeviceToHost, st), "y download");
     return WQ_OK;
@@ -551,6 +658,7 @@ WQ_API wq_status wq_linear_forward_host(wq_weights_t h, const void* x_host, int 
 WQ_API wq_status wq_export_weights(wq_weights_t h, uint8_t* codes, uint8_t* scales, float* gW, uint16_t* P,
                                    uint16_t* Q, uint16_t* W_omega) {
     if (!h) return fail(WQ_ERR_INVALID, "NULL handle");
+    if (h->cfg.mode != WQ_MODE_W4A4) return fail(WQ_ERR_INVALID, "W8A8 handle: use wq_export_weights_w8a8");
     const int K = h->cfg.K, N = h->cfg.N, r = h->cfg.rank, no = h->cfg.n_outliers;
     if (codes) WQ_CUDA(cudaMemcpy(codes, h->d_codes, static_cast<size_t>(N) * K / 2, cudaMemcpyDeviceToHost), "export");
     if (scales) {

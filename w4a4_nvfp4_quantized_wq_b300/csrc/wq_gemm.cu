@@ -25,6 +25,11 @@
 // cluster barrier every CTA reduces a slice of the tile's rows over all peers through
 // distributed shared memory, in rank order (deterministic), and stores bf16.
 //
+// kW8 = true runs the same pipeline on the selective 8-bit layers (FoldQuantVLA, Key
+// Contribution 3): int8 codes stored as bf16 (|q| <= 127 is exact in bf16, products are
+// exact in fp32) through tcgen05.mma kind::f16, 64 K per stage, no block scales, epilogue
+// y = a[m] w[n] acc + b.
+//
 // The kernel is launched as a programmatic dependent of the activation quantiser: weight
 // tiles are requested before griddepcontrol.wait, activation tiles after it.  It lets the
 // next grid in the stream start its prologue early.
@@ -84,10 +89,13 @@ struct KParams {
     const float* gA;
     float gW;
     const float* bias;
+    const float* colscale;           // per-output-column scale (8-bit layers) or null
     int* err;
 };
 
-Plan make_plan(int r, int n_out, int max_stages = 8) {
+__host__ __device__ constexpr uint32_t stage_bytes(bool w8) { return w8 ? 2 * kTileBytes : kStageBytes; }
+
+Plan make_plan(int r, int n_out, int max_stages, bool w8) {
     Plan p{};
     p.u_bytes = 128u * 2u * static_cast<uint32_t>(r);
     p.xo_bytes = 128u * 2u * static_cast<uint32_t>(n_out);
@@ -95,11 +103,11 @@ Plan make_plan(int r, int n_out, int max_stages = 8) {
     const bool has_side = side > 0;
     p.sf_col = has_side ? 384 : 256;
     const int tmem_slots = static_cast<int>((512 - p.sf_col) / 32);
-    int s = static_cast<int>((kMaxSmem - 1024 - side - kYBytes - kBarBytes) / kStageBytes);
+    int s = static_cast<int>((kMaxSmem - 1024 - side - kYBytes - kBarBytes) / stage_bytes(w8));
     if (s > tmem_slots) s = tmem_slots;
     if (s > max_stages) s = max_stages;
     p.stages = s;
-    p.off_side = static_cast<uint32_t>(s) * kStageBytes;
+    p.off_side = static_cast<uint32_t>(s) * stage_bytes(w8);
     p.off_y = p.off_side + side;
     p.off_bar = p.off_y + kYBytes;
     p.total = p.off_bar + kBarBytes + 1024;
@@ -119,6 +127,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+template <bool kW8>
 __global__ void __launch_bounds__(kThreads, 1)
 nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmQ,
@@ -145,8 +154,10 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     const int M = p.M, N = p.N;
     const int n_tiles = (N + 127) / 128;
     const int tiles = ((M + 127) / 128) * n_tiles;
+    constexpr uint32_t kSB = stage_bytes(kW8);
+    constexpr int kStageX = kW8 ? 64 : 128;           // TMA x extent of a stage (elements)
     const int num_kb = p.K / 64;
-    const int num_kt = (num_kb + 3) / 4;
+    const int num_kt = kW8 ? num_kb : (num_kb + 3) / 4;
     const bool split = p.split > 1;
     const uint32_t rank = split ? cluster_ctarank() : 0u;
     const int tile_first = split ? static_cast<int>(blockIdx.x) / p.split : static_cast<int>(blockIdx.x);
@@ -207,11 +218,12 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     for (int i = 0; i < pre; ++i) {
                         const int kb0 = (kt_lo + i) * 4, nkb = min(4, num_kb - kb0);
                         const uint32_t fb = bar_full + 8u * i;
-                        const uint32_t sA = base + static_cast<uint32_t>(i) * kStageBytes;
-                        mbar_arrive_expect_tx(fb, 2 * kTileBytes + 2u * nkb * kSfAtom);
-                        tma_load_2d(sA + kTileBytes, &tmB, (kt_lo + i) * 128, nb * 128, fb);
-                        bulk_load(sA + 2 * kTileBytes + 4 * kSfAtom,
-                                  p.sfb + (static_cast<size_t>(nb) * num_kb + kb0) * kSfAtom, nkb * kSfAtom, fb);
+                        const uint32_t sA = base + static_cast<uint32_t>(i) * kSB;
+                        mbar_arrive_expect_tx(fb, 2 * kTileBytes + (kW8 ? 0u : 2u * nkb * kSfAtom));
+                        tma_load_2d(sA + kTileBytes, &tmB, (kt_lo + i) * kStageX, nb * 128, fb);
+                        if (!kW8)
+                            bulk_load(sA + 2 * kTileBytes + 4 * kSfAtom,
+                                      p.sfb + (static_cast<size_t>(nb) * num_kb + kb0) * kSfAtom, nkb * kSfAtom, fb);
                         issued |= 1u << i;
                     }
                     WQ_TRACE_AT(2);
@@ -220,10 +232,11 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     for (int i = 0; i < pre; ++i) {
                         const int kb0 = (kt_lo + i) * 4, nkb = min(4, num_kb - kb0);
                         const uint32_t fb = bar_full + 8u * i;
-                        const uint32_t sA = base + static_cast<uint32_t>(i) * kStageBytes;
-                        tma_load_2d(sA, &tmA, (kt_lo + i) * 128, mb * 128, fb);
-                        bulk_load(sA + 2 * kTileBytes, p.sfa + (static_cast<size_t>(mb) * num_kb + kb0) * kSfAtom,
-                                  nkb * kSfAtom, fb);
+                        const uint32_t sA = base + static_cast<uint32_t>(i) * kSB;
+                        tma_load_2d(sA, &tmA, (kt_lo + i) * kStageX, mb * 128, fb);
+                        if (!kW8)
+                            bulk_load(sA + 2 * kTileBytes,
+                                      p.sfa + (static_cast<size_t>(mb) * num_kb + kb0) * kSfAtom, nkb * kSfAtom, fb);
                     }
                     kt += pre;
                     stage = pre % S;
@@ -234,14 +247,16 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     const int kb0 = kt * 4;
                     const int nkb = min(4, num_kb - kb0);
                     const uint32_t fb = bar_full + 8u * stage;
-                    const uint32_t sA = base + static_cast<uint32_t>(stage) * kStageBytes;
-                    mbar_arrive_expect_tx(fb, 2 * kTileBytes + 2u * nkb * kSfAtom);
-                    tma_load_2d(sA, &tmA, kt * 128, mb * 128, fb);
-                    tma_load_2d(sA + kTileBytes, &tmB, kt * 128, nb * 128, fb);
-                    bulk_load(sA + 2 * kTileBytes, p.sfa + (static_cast<size_t>(mb) * num_kb + kb0) * kSfAtom,
-                              nkb * kSfAtom, fb);
-                    bulk_load(sA + 2 * kTileBytes + 4 * kSfAtom,
-                              p.sfb + (static_cast<size_t>(nb) * num_kb + kb0) * kSfAtom, nkb * kSfAtom, fb);
+                    const uint32_t sA = base + static_cast<uint32_t>(stage) * kSB;
+                    mbar_arrive_expect_tx(fb, 2 * kTileBytes + (kW8 ? 0u : 2u * nkb * kSfAtom));
+                    tma_load_2d(sA, &tmA, kt * kStageX, mb * 128, fb);
+                    tma_load_2d(sA + kTileBytes, &tmB, kt * kStageX, nb * 128, fb);
+                    if (!kW8) {
+                        bulk_load(sA + 2 * kTileBytes, p.sfa + (static_cast<size_t>(mb) * num_kb + kb0) * kSfAtom,
+                                  nkb * kSfAtom, fb);
+                        bulk_load(sA + 2 * kTileBytes + 4 * kSfAtom,
+                                  p.sfb + (static_cast<size_t>(nb) * num_kb + kb0) * kSfAtom, nkb * kSfAtom, fb);
+                    }
                     issued |= 1u << stage;
                     issued_ph = (issued_ph & ~(1u << stage)) | (ph << stage);
                     if (++stage == S) { stage = 0; ph ^= 1u; }
@@ -288,8 +303,9 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 // The scale factors of stage k+1 are copied into TMEM right after the MMAs of stage k
                 // are issued, so the copies overlap the MMAs instead of sitting in front of them.
                 auto copy_scales = [&](int stg, int ktx) {
+                    if (kW8) return;
                     const int nkbx = min(4, num_kb - ktx * 4);
-                    const uint32_t sAx = base + static_cast<uint32_t>(stg) * kStageBytes;
+                    const uint32_t sAx = base + static_cast<uint32_t>(stg) * kSB;
                     const uint32_t sfx = tmem + p.sf_col + 32u * stg;
                     for (int kb = 0; kb < nkbx; ++kb) {
                         tmem_cp_32x128b_x4(sfx + 4u * kb, smem_desc(sAx + 2 * kTileBytes + kSfAtom * kb, 0, 128, 0));
@@ -301,15 +317,20 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     if (!mbar_wait(bar_full + 8u * stage, ph, abort_flag, p.err, 5)) { ok = false; break; }
                     if (tl == 0 && kt == kt_lo) WQ_TRACE_AT(4);
                     tc_fence_after();
-                    const int nkb = min(4, num_kb - kt * 4);
-                    const uint32_t sA = base + static_cast<uint32_t>(stage) * kStageBytes;
+                    const int nkb = kW8 ? 4 : min(4, num_kb - kt * 4);
+                    const uint32_t sA = base + static_cast<uint32_t>(stage) * kSB;
                     const uint32_t sf_t = tmem + p.sf_col + 32u * stage;
                     if (kt == kt_lo) copy_scales(stage, kt);
                     const uint64_t ad = smem_desc(sA, 16, 1024, 2);
                     const uint64_t bd = smem_desc(sA + kTileBytes, 16, 1024, 2);
-                    for (int kb = 0; kb < nkb; ++kb)
-                        mma_nvf4(d_acc, ad + 2u * kb, bd + 2u * kb, idesc_fp4, sf_t + 4u * kb, sf_t + 16u + 4u * kb,
-                                 (kt != kt_lo || kb != 0) ? 1u : 0u);
+                    for (int kb = 0; kb < nkb; ++kb) {
+                        const uint32_t accum = (kt != kt_lo || kb != 0) ? 1u : 0u;
+                        if (kW8)
+                            mma_f16(d_acc, ad + 2u * kb, bd + 2u * kb, idesc_bf16, accum);
+                        else
+                            mma_nvf4(d_acc, ad + 2u * kb, bd + 2u * kb, idesc_fp4, sf_t + 4u * kb,
+                                     sf_t + 16u + 4u * kb, accum);
+                    }
                     tc_commit(bar_empty + 8u * stage);
                     if (++stage == S) { stage = 0; ph ^= 1u; }
                     if (kt + 1 < kt_hi) {
@@ -379,7 +400,14 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             }
             for (int ch = 0; ch < 2; ++ch) {
                 const int c0 = hh * 64 + ch * 32;       // first column of this chunk in the tile
-                float4 bv[8];
+                float4 bv[8], cv[8];
+                if (p.colscale != nullptr) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int n = nb * 128 + c0 + 4 * j;
+                        cv[j] = n < N ? __ldg(reinterpret_cast<const float4*>(p.colscale + n)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                }
                 if (add_bias) {
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
@@ -395,6 +423,10 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     v[i] = alpha * __uint_as_float(acc[i]);
+                    if (p.colscale != nullptr) {
+                        const float4& cq = cv[i / 4];
+                        v[i] *= (i % 4 == 0) ? cq.x : (i % 4 == 1) ? cq.y : (i % 4 == 2) ? cq.z : cq.w;
+                    }
                     if (has_side) v[i] += __uint_as_float(sd[i]);
                 }
                 if (add_bias) {
@@ -492,10 +524,9 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     if (threadIdx.x == 0) WQ_TRACE_AT(10);
 }
 
-}  // namespace
-
 // Largest cluster size (power of two, <= 16, <= number of K stages) that keeps every tile's
 // cluster resident at once; 1 when the tiles alone fill the GPU.
+template <bool kW8>
 int choose_split_uncached(int tiles, int num_kt, int num_sms, size_t smem) {
     if (tiles * 2 > num_sms) return 1;
     for (int s = 16; s >= 2; s >>= 1) {
@@ -512,7 +543,7 @@ int choose_split_uncached(int tiles, int num_kt, int num_sms, size_t smem) {
         cfg.attrs = at;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, nvfp4_gemm_kernel, &cfg) != cudaSuccess) {
+        if (cudaOccupancyMaxActiveClusters(&n, nvfp4_gemm_kernel<kW8>, &cfg) != cudaSuccess) {
             cudaGetLastError();
             continue;
         }
@@ -521,6 +552,7 @@ int choose_split_uncached(int tiles, int num_kt, int num_sms, size_t smem) {
     return 1;
 }
 
+template <bool kW8>
 int choose_split(int tiles, int num_kt, int num_sms, size_t smem) {
     static std::mutex mu;
     static std::map<std::tuple<int, int, int, size_t>, int> cache;
@@ -528,29 +560,29 @@ int choose_split(int tiles, int num_kt, int num_sms, size_t smem) {
     std::lock_guard<std::mutex> lk(mu);
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
-    const int s = choose_split_uncached(tiles, num_kt, num_sms, smem);
+    const int s = choose_split_uncached<kW8>(tiles, num_kt, num_sms, smem);
     cache[key] = s;
     return s;
 }
 
-cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
-    if (a.M <= 0) return cudaSuccess;
+template <bool kW8>
+cudaError_t launch_gemm_t(const GemmArgs& a, cudaStream_t st) {
     // WQ_GEMM_STAGES=<n> caps the shared-memory ring depth (tuning)
     const char* ms = std::getenv("WQ_GEMM_STAGES");
-    const Plan pl = make_plan(a.r, a.n_out, ms ? std::atoi(ms) : 8);
+    const Plan pl = make_plan(a.r, a.n_out, ms ? std::atoi(ms) : 8, kW8);
     if (pl.stages < 2) return cudaErrorInvalidConfiguration;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(nvfp4_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(nvfp4_gemm_kernel<kW8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(kMaxSmem));
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(nvfp4_gemm_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        e = cudaFuncSetAttribute(nvfp4_gemm_kernel<kW8>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     const int tiles = ((a.M + 127) / 128) * ((a.N + 127) / 128);
-    const int num_kt = (a.K / 64 + 3) / 4;
-    const int split = a.force_split > 0 ? a.force_split : choose_split(tiles, num_kt, a.num_sms, pl.total);
+    const int num_kt = kW8 ? a.K / 64 : (a.K / 64 + 3) / 4;
+    const int split = a.force_split > 0 ? a.force_split : choose_split<kW8>(tiles, num_kt, a.num_sms, pl.total);
     if (split > num_kt || split > 16 || (split & (split - 1))) return cudaErrorInvalidValue;
     KParams kp{};
     kp.split = split;
@@ -558,7 +590,8 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
     kp.M = a.M; kp.N = a.N; kp.K = a.K; kp.r = a.r; kp.n_out = a.n_out; kp.stages = pl.stages;
     kp.u_bytes = pl.u_bytes; kp.xo_bytes = pl.xo_bytes; kp.off_side = pl.off_side; kp.off_y = pl.off_y;
     kp.off_bar = pl.off_bar; kp.sf_col = pl.sf_col;
-    kp.sfa = a.sfa; kp.sfb = a.sfb; kp.gA = a.gA; kp.gW = a.gW; kp.bias = a.bias; kp.err = a.err;
+    kp.sfa = a.sfa; kp.sfb = a.sfb; kp.gA = a.gA; kp.gW = a.gW; kp.bias = a.bias; kp.colscale = a.colscale;
+    kp.err = a.err;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(split > 1 ? tiles * split : (tiles < a.num_sms ? tiles : a.num_sms)));
     cfg.blockDim = dim3(kThreads);
@@ -578,8 +611,15 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
     }
     cfg.attrs = at;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, nvfp4_gemm_kernel, *a.tmA, *a.tmB, *a.tmU, *a.tmQ, *a.tmXO, *a.tmWO, *a.tmY,
-                              kp);
+    return cudaLaunchKernelEx(&cfg, nvfp4_gemm_kernel<kW8>, *a.tmA, *a.tmB, *a.tmU, *a.tmQ, *a.tmXO, *a.tmWO,
+                              *a.tmY, kp);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
+    if (a.M <= 0) return cudaSuccess;
+    return a.w8 ? launch_gemm_t<true>(a, st) : launch_gemm_t<false>(a, st);
 }
 
 }  // namespace wq

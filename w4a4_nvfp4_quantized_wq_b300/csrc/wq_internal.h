@@ -45,6 +45,7 @@ struct QuantArgs {
     int sf_layout;                  // WQ_SCALE_LAYOUT_*
     float* g;                       // [M]
     int num_sms;                    // used to spread small batches over more CTAs
+    bool int8 = false;              // 8-bit layer: codes are int8 values stored as bf16 [M, K]
 };
 
 cudaError_t launch_quantize_act(const QuantArgs& a, cudaStream_t stream);
@@ -67,6 +68,8 @@ struct GemmArgs {
     int num_sms;
     void* y;                  // bf16 [M, N] (written directly by the split-K reduction)
     int force_split;          // 0: choose; otherwise CTAs per tile (power of two <= 16)
+    bool w8 = false;          // 8-bit layer: A/W are int8 codes stored as bf16 [., K]
+    const float* colscale = nullptr;  // 8-bit layer: per-output-column scale [N]
 };
 
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream);

@@ -24,6 +24,10 @@
 // in the slot; the row amax is accumulated.  Pass 2 reads the transformed blocks back and
 // writes the codes, scales and outlier values.  Across a cluster the row amax and the U
 // partial sums are combined through distributed shared memory.
+//
+// kInt8 = true is the selective 8-bit variant (FoldQuantVLA, Key Contribution 3) in the same
+// basis: a = amax / 127 per row, q = round-half-even(xt / a) clamped to [-127, 127], written as
+// exact bf16 integers [M, K] for the 8-bit GEMM.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -206,7 +210,7 @@ __device__ __forceinline__ uint32_t e2m1_codes8(const float (&v)[8], float d) {
     return word;
 }
 
-template <int R>
+template <int R, bool kInt8>
 __global__ void __launch_bounds__(kThreads) quantize_kernel(const __grid_constant__ CUtensorMap tmX, const QParams p) {
     constexpr int NT = R / 8 > 0 ? R / 8 : 1;       // n8 tiles of U
     constexpr int NTW = NT > 4 ? NT / 4 : 1;        // n-tiles per warp
@@ -441,7 +445,7 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const __grid_constan
             }
         }
     }
-    const float gsc = __fdiv_rn(amax, 2688.0f);
+    const float gsc = __fdiv_rn(amax, kInt8 ? 127.0f : 2688.0f);
     if (threadIdx.x == 0) WQ_QTRACE_AT(4);
     if (rank == 0 && c == 0 && row_ok) p.g[row] = gsc;
 
@@ -452,6 +456,24 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const __grid_constan
         float v[8];
         ld_shared_v8f(blk + static_cast<uint32_t>(rloc) * (kRowWords * 4u) + c * 32u, v);
         if (p.n_out > 0) split_outliers(v, s_opos + i * 64 + c * 8, row, row_ok, p);
+        if constexpr (kInt8) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float t[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float r = gsc != 0.0f ? rintf(__fdiv_rn(v[2 * q + e], gsc)) : 0.0f;
+                    t[e] = fminf(fmaxf(r, -127.0f), 127.0f);
+                }
+                const __nv_bfloat162 h = __floats2bfloat162_rn(t[0], t[1]);
+                pk[q] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            if (row_ok)
+                *reinterpret_cast<uint4*>(p.codes + (static_cast<size_t>(row) * K + kb * 64 + c * 8) * 2) =
+                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            continue;
+        }
         float cm = 0.0f;
 #pragma unroll
         for (int e = 0; e < 8; ++e) cm = fmaxf(cm, fabsf(v[e]));
@@ -498,16 +520,16 @@ Choice choose(int M, int K, int num_sms) {
     return Choice{cs, (nblk + cs - 1) / cs};
 }
 
-template <int R>
+template <int R, bool kInt8>
 cudaError_t launch_r(const CUtensorMap& tm, const QParams& qp, cudaStream_t st) {
     const Layout lay = make_layout(qp.max_nb, R);
     static bool attr_set = false;
     if (!attr_set) {
         const Layout worst = make_layout(kMaxBlocks, R);
-        cudaError_t e = cudaFuncSetAttribute(quantize_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(quantize_kernel<R, kInt8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(worst.total));
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(quantize_kernel<R>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        e = cudaFuncSetAttribute(quantize_kernel<R, kInt8>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
@@ -530,7 +552,7 @@ cudaError_t launch_r(const CUtensorMap& tm, const QParams& qp, cudaStream_t st) 
     }
     cfg.attrs = at;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, quantize_kernel<R>, tm, qp);
+    return cudaLaunchKernelEx(&cfg, quantize_kernel<R, kInt8>, tm, qp);
 }
 
 }  // namespace
@@ -552,11 +574,12 @@ cudaError_t launch_quantize_act(const QuantArgs& a, cudaStream_t st) {
     qp.inv_s = a.inv_s; qp.rotate = a.rotate; qp.omega_pos = a.omega_pos; qp.n_out = a.n_out; qp.xo = a.xo;
     qp.pfrag = a.pfrag; qp.u = a.u; qp.codes = a.codes; qp.sf = a.sf; qp.sf_layout = a.sf_layout; qp.g = a.g;
     qp.err = a.err;
+    if (a.int8) return a.r == 0 && a.n_out == 0 ? launch_r<0, true>(*a.tmX, qp, st) : cudaErrorInvalidValue;
     switch (a.r) {
-        case 0: return launch_r<0>(*a.tmX, qp, st);
-        case 16: return launch_r<16>(*a.tmX, qp, st);
-        case 32: return launch_r<32>(*a.tmX, qp, st);
-        case 64: return launch_r<64>(*a.tmX, qp, st);
+        case 0: return launch_r<0, false>(*a.tmX, qp, st);
+        case 16: return launch_r<16, false>(*a.tmX, qp, st);
+        case 32: return launch_r<32, false>(*a.tmX, qp, st);
+        case 64: return launch_r<64, false>(*a.tmX, qp, st);
         default: return cudaErrorInvalidValue;
     }
 }
