@@ -38,6 +38,8 @@ WORKLOAD_TEXT = {
     "video_dit": "video DiT block: M=16384 tokens, QKV 1536->4608, o 1536->1536, up 1536->8960, "
                  "down 8960->1536, rank 32, 64 fp16 outlier channels, NVFP4 W4A4",
     "tiny": "single projection M=8, K=256 -> N=512, rank 16",
+    "vae_conv": "Wan-style VAE Conv3d 3x3x3, C 384->384, input 1x384x5x60x104, padding 1: implicit GEMM "
+                "M=31200 voxels, K=10368, N=384, NVFP4 with a per-tensor activation scale",
     "backbone": "language backbone prefill M=768: QKV 2048->6144 and gate/up 2048->32768 in W4A4, "
                 "o_proj 2048->2048 and down 16384->2048 in W8A8 (int8 codes held as bf16)",
 }
@@ -524,10 +526,156 @@ def run_wq(args):
         dist.destroy_process_group()
 
 
+def run_conv(args):
+    """The VAE Conv3d workload: one step = |x| maxima + voxel quantiser + implicit GEMM."""
+    import torch
+    ws_, rank, local_rank = dist_env()
+    if ws_ > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    from w4a4_nvfp4_quantized_wq_b300 import build as wqbuild
+    wqbuild.build_library()
+    import w4a4_nvfp4_quantized_wq_b300 as wq
+    import workloads as wl
+    xb, w = wl.make_conv_inputs()
+    _, C, D, H, W = xb.shape
+    V, N, K = D * H * W, w.shape[0], 27 * C
+    hw = wq.wq_prepare_conv3d(w)
+    x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).to(dev)
+    y = torch.empty((1, N, D, H, W), dtype=torch.bfloat16, device=dev)
+    wsb = torch.empty(wq.wq_conv3d_workspace_bytes(hw, D, H, W), dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        wq.wq_conv3d_forward(hw, x, y, wsb, stream)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            wq.wq_conv3d_forward(hw, x, y, wsb, stream)
+    torch.cuda.synchronize()
+    wq.wq_check_device_error(hw)
+    Ksteps, Wu = args.steps, args.warmup
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Ksteps)]
+    with torch.cuda.stream(stream):
+        for _ in range(Wu):
+            flush.zero_()
+            graph.replay()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local_rank)
+    if ws_ > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    with sampler:
+        with torch.cuda.stream(stream):
+            for i in range(Ksteps):
+                flush.zero_()
+                ev[i][0].record(stream)
+                graph.replay()
+                ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    total_ms = float(sum(a.elapsed_time(b) for a, b in ev))
+    if ws_ > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    flops = 2.0 * V * N * K
+    # per-kernel: the quantiser pair alone, the whole forward; the GEMM is the difference
+    times = {}
+    for kname in ("quant", "forward"):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.kernel_iters)]
+        codes = torch.empty((V, C // 2), dtype=torch.uint8, device=dev)
+        scales = torch.empty((V, C // 16), dtype=torch.uint8, device=dev)
+        gx = torch.empty(1, dtype=torch.float32, device=dev)
+        import ctypes
+        with torch.cuda.stream(stream):
+            for i in range(args.kernel_iters + 3):
+                flush.zero_()
+                if i >= 3:
+                    evs[i - 3][0].record(stream)
+                if kname == "quant":
+                    wq.lib().wq_quantize_conv3d_input(
+                        ctypes.c_void_p(hw.handle), ctypes.c_void_p(x.data_ptr()), D, H, W,
+                        ctypes.c_void_p(codes.data_ptr()), ctypes.c_void_p(scales.data_ptr()),
+                        ctypes.c_void_p(gx.data_ptr()), ctypes.c_void_p(wsb.data_ptr()), wsb.numel(),
+                        ctypes.c_void_p(stream.cuda_stream))
+                else:
+                    wq.wq_conv3d_forward(hw, x, y, wsb, stream)
+                if i >= 3:
+                    evs[i - 3][1].record(stream)
+        torch.cuda.synchronize()
+        times[kname] = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    gemm_ms = times["forward"] - times["quant"]
+    peaks, peak_kind = measured_peaks()
+    fp4_peak = peaks.get("bf16_tflops", 1800.0) * 6.0
+    ach = flops / (gemm_ms / 1e3) / 1e12
+    qbytes = 2 * 2 * C * V + V * C // 2 + V * C // 16          # x read twice (maxima + quantiser), codes out
+    roofline = {"kernel": "conv_gemm_kernel", "bound": "tensor", "achieved": ach, "peak": fp4_peak,
+                "unit": "TFLOP/s", "frac": ach / fp4_peak, "traffic": profiled_traffic("conv_gemm", "vae_conv"),
+                "peak_source": f"{peak_kind} bf16 x 6 (nominal fp4:bf16 ratio)",
+                "flops_per_launch": flops, "us_per_launch": 1e3 * gemm_ms,
+                "share_of_kernel_time": gemm_ms / times["forward"]}
+    kernels = {"conv_quant (maxima + quantiser)": {"us": 1e3 * times["quant"], "bytes": qbytes,
+                                                    "GB/s": qbytes / (times["quant"] / 1e3) / 1e9},
+               "conv_gemm (forward - quantiser)": {"us": 1e3 * gemm_ms, "TFLOP/s": ach}}
+    # end to end: pinned host x -> device, forward, y -> pinned host
+    xh = x.cpu().pin_memory()
+    yh = torch.empty(y.shape, dtype=torch.bfloat16).pin_memory()
+    ke = max(5, min(Ksteps, 50))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(ke)]
+    with torch.cuda.stream(stream):
+        for i in range(ke):
+            flush.zero_()
+            evs[i][0].record(stream)
+            x.copy_(xh, non_blocking=True)
+            wq.wq_conv3d_forward(hw, x, y, wsb, stream)
+            yh.copy_(y, non_blocking=True)
+            evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    e_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline and ws_ == 1:
+        import oracle
+        nth = os.cpu_count() or 1
+        vox = np.sort(np.random.default_rng(5).choice(V, 16, replace=False))
+        t0 = time.perf_counter()
+        passes = 0
+        while True:
+            oracle.conv3d_reference(xb, w, vox, nth)
+            passes += 1
+            if time.perf_counter() - t0 > args.cpu_baseline_seconds * 0.5:
+                break
+        el = time.perf_counter() - t0
+        cpu = {"value": 16 * passes / el, "unit": "voxels/s", "cores": nth, "kind": "oracle",
+               "sample": f"16 of {V} output voxels x {passes} passes, all 384 channels, input and weight "
+                         f"quantisation included ({el:.1f} s)"}
+    if rank == 0:
+        line = {"metric": METRIC, "value": V * ws_ / (total_ms / Ksteps / 1e3), "unit": "voxels/s",
+                "n_gpus": ws_, "steps": Ksteps, "warmup": Wu, "ms_per_step": total_ms / Ksteps,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "nvfp4 (e2m1 x e2m1, ue4m3 scales, f32 accumulate)", "data": "synthetic (seeded)",
+                "tflops": flops * Ksteps * ws_ / (total_ms / 1e3) / 1e12,
+                "config": {"workload": WORKLOAD_TEXT["vae_conv"], "M": V, "N": N, "K": K,
+                           "l2": "flushed before every step (256 MiB write, outside the step events)",
+                           "parallelism": f"replicas x{ws_}", "cuda_graph": True},
+                "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu,
+                "e2e": {"value": V * ws_ / (e_ms / 1e3), "unit": "voxels/s",
+                        "h2d_bytes_per_step": 2 * C * V, "d2h_bytes_per_step": 2 * N * V, "ms_per_step": e_ms,
+                        "api": "pinned host x -> device, wq_conv3d_forward, y -> pinned host"},
+                "clocks": sampler.record(), "gpu_launches": 3 * Ksteps}
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "vae_conv":
+        run_conv(args)
     else:
         run_wq(args)
 

@@ -181,6 +181,35 @@ WQ_API wq_status wq_quantize_activations_w8a8(wq_weights_t h, const void *x, int
 WQ_API wq_status wq_export_weights_w8a8(wq_weights_t h, int8_t *q, float *w);
 
 /*
+ * The video VAE's 3x3x3 convolution, zero padding 1, batch 1, as an NVFP4 implicit GEMM
+ * (LatentQuant, Abstract: NVFP4 execution of the Wan VAE).  The input is quantised once per
+ * voxel along channels (16-channel blocks, e4m3 scales) with ONE fp32 scale for the whole
+ * tensor (a GEMM row gathers 27 voxels, so a per-voxel scale would not factor out); no
+ * smoothing or rotation.  The weight is NVFP4 per output channel along K = (kd, kh, kw, c_in)
+ * with one fp32 scale per tensor.  y[n, v] = gx gw sum_{taps, c} A . W, bf16.
+ *   w       host fp32 [C_out, C_in, 3, 3, 3];  C_in % 128 == 0, C_out % 16 == 0,
+ *           27 C_in <= 16384.
+ */
+WQ_API wq_status wq_prepare_conv3d(const float *w, int C_in, int C_out, void *stream, wq_weights_t *out);
+
+/* Device scratch for wq_conv3d_forward / wq_quantize_conv3d_input (D H W voxels). */
+WQ_API size_t wq_conv3d_workspace_bytes(wq_weights_t h, int D, int H, int W);
+
+/*
+ *   x  device bf16 NCDHW [1, C_in, D, H, W];  y  device bf16 NCDHW [1, C_out, D, H, W];
+ *   D H W % 8 == 0.  Three kernels on `stream`: |x| maxima, the per-voxel quantiser, the
+ *   implicit GEMM (A rows gathered per tap by cp.async, zero-filled in the padding).
+ */
+WQ_API wq_status wq_conv3d_forward(wq_weights_t h, const void *x, int D, int H, int W, void *y,
+                                   void *workspace, size_t workspace_bytes, void *stream);
+
+/* The conv input quantiser alone: codes [V, C_in/2], scales [V, C_in/16], g (one float),
+ * all device; voxel v = (d H + h) W + w. */
+WQ_API wq_status wq_quantize_conv3d_input(wq_weights_t h, const void *x, int D, int H, int W,
+                                          uint8_t *codes, uint8_t *scales, float *g,
+                                          void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Copy the prepared weights back to host memory in canonical layouts (synchronous):
  *   codes uint8 [N, K/2]; scales e4m3 [N, K/16]; gW fp32 scalar; P bf16 [K, r];
  *   Q bf16 [r, N]; W_omega fp16 [n_outliers, N].  Any output may be NULL.

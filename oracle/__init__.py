@@ -66,6 +66,8 @@ def lib() -> ctypes.CDLL:
             L.orc_linear_forward.restype = i32
             L.orc_forward_noquant.argtypes = [P, P, i64, i64, i64, P, P, i32, P, P, P, i32, P, P]
             L.orc_forward_noquant.restype = i32
+            L.orc_conv3d_forward.argtypes = [P, P, f32, i64, i64, i64, i64, P, P, f32, i64, P, i64, P, i32]
+            L.orc_conv3d_forward.restype = i32
             L.orc_quantize_act_int8.argtypes = [P, i64, i64, P, i32, P, P, i32]
             L.orc_quantize_act_int8.restype = i32
             L.orc_quantize_weights_int8.argtypes = [P, i64, i64, P, P]
@@ -322,3 +324,27 @@ def reference_forward_w8a8(layer, n_threads: int = 0, rows=None):
     wq8 = prepare_weights_int8(layer.W, layer.s, layer.rotate, n_threads)
     aq = quantize_act_int8(x_bits, layer.s, layer.rotate, n_threads)
     return linear_forward_w8a8(aq, wq8, layer.bias, n_threads), aq, wq8
+
+
+# ------------------------------------------------------------------ Conv3d (VAE)
+def conv_weight_matrix(w: np.ndarray) -> np.ndarray:
+    """[C_out, C_in, 3, 3, 3] -> W [K = (kd, kh, kw, c_in), N = C_out] (math y = x W)."""
+    Co, Ci = w.shape[:2]
+    return np.ascontiguousarray(np.transpose(w, (2, 3, 4, 1, 0)).reshape(27 * Ci, Co), dtype=np.float32)
+
+
+def conv3d_reference(x_bits_ncdhw: np.ndarray, w: np.ndarray, vox: np.ndarray, n_threads: int = 0):
+    """LatentQuant, Abstract (NVFP4 execution of the VAE): quantise the input once per voxel
+    (one tensor scale), the weight per output channel along (kd, kh, kw, c_in), and convolve
+    the dequantised values directly with zero padding 1.  Returns (y [n_vox, C_out] fp64,
+    activation ActQuant over voxels, weight WeightQuant)."""
+    _, C, D, H, W = x_bits_ncdhw.shape
+    xv = np.ascontiguousarray(x_bits_ncdhw.reshape(C, D * H * W).T)          # voxels x channels
+    aq = quantize_act(xv, None, False, None, per_tensor=True, n_threads=n_threads)
+    wq = prepare_weights(conv_weight_matrix(w), None, None, None, None, False, n_threads)
+    vox = np.ascontiguousarray(vox, dtype=np.int64)
+    N = w.shape[0]
+    y = np.zeros((vox.size, N), np.float64)
+    lib().orc_conv3d_forward(_p(aq.codes), _p(aq.scales), np.float32(aq.g[0]), C, D, H, W, _p(wq.codes),
+                             _p(wq.scales), np.float32(wq.gW), N, _p(vox), vox.size, _p(y), int(n_threads))
+    return y, aq, wq

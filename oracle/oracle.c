@@ -583,3 +583,48 @@ int orc_linear_forward_w8a8(const int8_t *qa, const float *a, long M, const int8
         }
     return 0;
 }
+
+/* ------------------------------------------------------------------ Conv3d */
+/* NVFP4 execution of the video VAE's 3x3x3 convolutions (LatentQuant, Abstract).  Plainest
+ * reading: the input tensor is quantised once, per voxel along channels (16-channel blocks)
+ * with one fp32 scale for the whole tensor (an implicit-GEMM row mixes 27 voxels, so a
+ * per-voxel scale would not factor out); no smoothing, rotation, low-rank or kept channels.
+ * The weight [C_out, C_in, 3, 3, 3] is laid out as K = (kd, kh, kw, c_in) and quantised per
+ * output channel along K with one fp32 scale per tensor.  The convolution itself is the
+ * direct definition with zero padding 1, on the dequantised values, accumulated in fp64. */
+
+/* xq: codes [V, C/2] and scales [V, C/16] of the voxels (V = D H W, voxel v = (d H + h) W + w),
+ * gx the tensor scale; wq: codes [N, 27 C / 2], scales [N, 27 C / 16], gw.
+ * Computes y[n][v] for the listed voxels (y is [n_vox, N]). */
+int orc_conv3d_forward(const uint8_t *xcodes, const uint8_t *xscales, float gx, long C, long D, long H, long W,
+                       const uint8_t *wcodes, const uint8_t *wscales, float gw, long N,
+                       const int64_t *vox, long n_vox, double *y, int n_threads)
+{
+    const long K = 27 * C;
+#ifdef _OPENMP
+    if (n_threads > 0) omp_set_num_threads(n_threads);
+#else
+    (void)n_threads;
+#endif
+#pragma omp parallel for schedule(static)
+    for (long i = 0; i < n_vox; ++i) {
+        const long v = vox[i];
+        const long d = v / (H * W), h = (v / W) % H, w = v % W;
+        for (long n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int kd = 0; kd < 3; ++kd)
+                for (int kh = 0; kh < 3; ++kh)
+                    for (int kw = 0; kw < 3; ++kw) {
+                        const long di = d + kd - 1, hi = h + kh - 1, wi = w + kw - 1;
+                        if (di < 0 || di >= D || hi < 0 || hi >= H || wi < 0 || wi >= W) continue;
+                        const long vin = (di * H + hi) * W + wi;
+                        const long k0 = ((kd * 3 + kh) * 3 + kw) * C;
+                        for (long c = 0; c < C; ++c)
+                            acc += nvfp4_elem(xcodes + vin * (C / 2), xscales + vin * (C / 16), c) *
+                                   nvfp4_elem(wcodes + n * (K / 2), wscales + n * (K / 16), k0 + c);
+                    }
+            y[i * N + n] = acc * (double)gx * (double)gw;
+        }
+    }
+    return 0;
+}

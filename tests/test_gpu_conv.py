@@ -1,0 +1,70 @@
+"""GPU parity of the VAE Conv3d implicit GEMM against the direct-convolution oracle.
+
+Bar: input voxel codes, scales and the tensor scale bit-exact; weight codes/scales bit-exact;
+y within 1e-3 (|y| + ||a_row|| ||w_col|| / sqrt(K)) + 2^-8 |y|, with a_row the row of the
+implicit GEMM (the 27 voxels a tap reaches, zero in the padding).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import w4a4_nvfp4_quantized_wq_b300 as wq
+import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from w4a4_nvfp4_quantized_wq_b300 import build
+    build.build_library()
+    torch.cuda.set_device(0)
+
+
+def run_case(T, H, W, C_in, C_out, vox=None):
+    xb, w = wl.make_conv_inputs(T=T, H=H, W=W, C_in=C_in, C_out=C_out)
+    V = T * H * W
+    hw = wq.wq_prepare_conv3d(w)
+    x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
+    y = wq.wq_conv3d_forward(hw, x)
+    codes, scales, g = wq.wq_quantize_conv3d_input(hw, x)
+    wq.wq_check_device_error(hw)
+    if vox is None:
+        vox = np.arange(V)
+    y_ref, aq, wqo = oracle.conv3d_reference(xb, w, vox)
+    assert np.float32(g.item()) == aq.g[0]
+    assert np.array_equal(scales.cpu().numpy(), aq.scales)
+    assert np.array_equal(codes.cpu().numpy(), aq.codes)
+    ex = wq.wq_export_weights(hw)
+    assert np.array_equal(ex["codes"], wqo.codes) and np.array_equal(ex["scales"], wqo.scales)
+    # tolerance from the implicit-GEMM rows of the original input
+    xf = wl.bf16_from_bits(xb)[0].astype(np.float64)                 # [C, T, H, W]
+    xp = np.zeros((C_in, T + 2, H + 2, W + 2))
+    xp[:, 1:-1, 1:-1, 1:-1] = xf
+    d, h, ww = vox // (H * W), (vox // W) % H, vox % W
+    an = np.sqrt(sum((xp[:, d + kd, h + kh, ww + kw] ** 2).sum(axis=0)
+                     for kd in range(3) for kh in range(3) for kw in range(3)))
+    wn = np.linalg.norm(oracle.conv_weight_matrix(w).astype(np.float64), axis=0)
+    tol = 1e-3 * (np.abs(y_ref) + an[:, None] * wn[None, :] / np.sqrt(27 * C_in)) + 2.0 ** -8 * np.abs(y_ref)
+    yg = y[0].reshape(C_out, V).float().cpu().numpy().astype(np.float64)[:, vox].T
+    err = np.abs(yg - y_ref)
+    assert (err <= tol).all(), f"{(err > tol).sum()} of {err.size} outside tolerance, worst {np.max(err - tol):.3g}"
+
+
+def test_conv3d_small_all_voxels():
+    run_case(3, 5, 8, 128, 32)
+
+
+def test_conv3d_several_tiles_partial_n():
+    run_case(2, 7, 24, 256, 48)
+
+
+def test_conv3d_vae_full_size_sampled():
+    T, H, W = 5, 60, 104
+    rng = np.random.default_rng(9)
+    corners = [0, W - 1, (H - 1) * W, H * W - 1, (T - 1) * H * W, T * H * W - 1, 2 * H * W + 30 * W + 50]
+    vox = np.unique(np.concatenate([corners, rng.choice(T * H * W, 25, replace=False)]))
+    run_case(T, H, W, 384, 384, vox)

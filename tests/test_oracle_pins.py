@@ -337,3 +337,42 @@ def test_w8a8_error_is_small_against_unquantised_product():
     e8 = np.linalg.norm(y8 - ref) / np.linalg.norm(ref)
     e4 = np.linalg.norm(y4 - ref) / np.linalg.norm(ref)
     assert e8 < 0.02 and e8 < e4, (e8, e4)
+
+
+# ------------------------------------------------------------------ Conv3d
+def _dequant_rows(codes, scales, K):
+    return _dequant(codes, scales, K)
+
+
+def test_conv3d_equals_dequantised_im2col_gemm():
+    """The direct convolution equals an explicit numpy im2col of the dequantised voxels times
+    the dequantised weight matrix (an independent construction of the same sum)."""
+    xb, w = wlmod.make_conv_inputs(T=3, H=5, W=6, C_in=32, C_out=16)
+    _, C, D, H, W = xb.shape
+    vox = np.arange(D * H * W)
+    y, aq, wq = oracle.conv3d_reference(xb, w, vox)
+    X = _dequant_rows(aq.codes, aq.scales, C) * np.float64(aq.g[0])           # [V, C]
+    Wd = _dequant_rows(wq.codes, wq.scales, 27 * C) * np.float64(wq.gW)      # [N, K]
+    Xp = np.zeros((D + 2, H + 2, W + 2, C))
+    Xp[1:-1, 1:-1, 1:-1] = X.reshape(D, H, W, C)
+    cols = np.stack([Xp[kd:kd + D, kh:kh + H, kw:kw + W].reshape(-1, C)
+                     for kd in range(3) for kh in range(3) for kw in range(3)], axis=1).reshape(-1, 27 * C)
+    ref = cols @ Wd.T
+    np.testing.assert_allclose(y, ref, rtol=1e-10, atol=1e-10 * np.abs(ref).max())
+
+
+def test_conv3d_single_voxel_impulse_gives_flipped_kernel():
+    """One non-zero input voxel in the middle: each output voxel next to it sees exactly one tap
+    (zero padding and the tap order are both exercised)."""
+    C, N = 16, 8
+    x = np.zeros((1, C, 3, 3, 3), np.float32)
+    x[0, :, 1, 1, 1] = np.linspace(1, 2, C, dtype=np.float32)
+    w = np.random.default_rng(3).standard_normal((N, C, 3, 3, 3)).astype(np.float32)
+    y, aq, wq = oracle.conv3d_reference(wlmod.bf16_bits(x), w, np.arange(27))
+    X = _dequant_rows(aq.codes, aq.scales, C) * np.float64(aq.g[0])
+    Wd = (_dequant_rows(wq.codes, wq.scales, 27 * C) * np.float64(wq.gW)).reshape(N, 3, 3, 3, C)
+    for v in range(27):
+        d, h, ww = v // 9, (v // 3) % 3, v % 3
+        kd, kh, kw = 1 + 1 - d, 1 + 1 - h, 1 + 1 - ww       # input voxel (1,1,1) = output + k - 1
+        ref = Wd[:, kd, kh, kw, :] @ X[13]
+        np.testing.assert_allclose(y[v], ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())

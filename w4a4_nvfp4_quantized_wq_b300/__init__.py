@@ -24,7 +24,8 @@ WQ_SCALE_LAYOUT_ROWMAJOR, WQ_SCALE_LAYOUT_MMA = 0, 1
 EXPORTED = ["wq_prepare_weights", "wq_get_config", "wq_workspace_bytes", "wq_linear_forward",
             "wq_host_workspace_bytes", "wq_linear_forward_host", "wq_quantize_activations",
             "wq_linear_forward_quantized", "wq_linear_forward_noalloc", "wq_linear_forward_w8a8",
-            "wq_quantize_activations_w8a8", "wq_export_weights_w8a8",
+            "wq_quantize_activations_w8a8", "wq_export_weights_w8a8", "wq_prepare_conv3d",
+            "wq_conv3d_workspace_bytes", "wq_conv3d_forward", "wq_quantize_conv3d_input",
             "wq_export_weights", "wq_check_device_error", "wq_free_weights", "wq_last_error"]
 
 
@@ -75,6 +76,14 @@ def lib() -> ctypes.CDLL:
         L.wq_quantize_activations_w8a8.restype = I
         L.wq_export_weights_w8a8.argtypes = [P, P, P]
         L.wq_export_weights_w8a8.restype = I
+        L.wq_prepare_conv3d.argtypes = [P, I, I, P, ctypes.POINTER(P)]
+        L.wq_prepare_conv3d.restype = I
+        L.wq_conv3d_workspace_bytes.argtypes = [P, I, I, I]
+        L.wq_conv3d_workspace_bytes.restype = S
+        L.wq_conv3d_forward.argtypes = [P, P, I, I, I, P, P, S, P]
+        L.wq_conv3d_forward.restype = I
+        L.wq_quantize_conv3d_input.argtypes = [P, P, I, I, I, P, P, P, P, S, P]
+        L.wq_quantize_conv3d_input.restype = I
         L.wq_export_weights.argtypes = [P, P, P, P, P, P, P]
         L.wq_export_weights.restype = I
         L.wq_check_device_error.argtypes = [P, P]
@@ -314,3 +323,52 @@ def wq_export_weights_w8a8(w: Weights):
     _check(lib().wq_export_weights_w8a8(ctypes.c_void_p(w.handle), q.ctypes.data_as(ctypes.c_void_p),
                                         sc.ctypes.data_as(ctypes.c_void_p)))
     return q, sc
+
+
+# ------------------------------------------------------------------ VAE Conv3d
+@dataclass
+class ConvWeights(Weights):
+    C_in: int = 0
+
+
+def wq_prepare_conv3d(w, stream=None) -> ConvWeights:
+    """Quantise a [C_out, C_in, 3, 3, 3] fp32 kernel for the implicit-GEMM Conv3d."""
+    w = np.ascontiguousarray(w.detach().cpu().numpy() if hasattr(w, "numpy") else w, dtype=np.float32)
+    Co, Ci = w.shape[:2]
+    out = ctypes.c_void_p()
+    _check(lib().wq_prepare_conv3d(w.ctypes.data_as(ctypes.c_void_p), Ci, Co,
+                                   ctypes.c_void_p(_stream_ptr(stream)), ctypes.byref(out)))
+    return ConvWeights(out.value, wq_config(27 * Ci, Co, 0, 0, 0, WQ_MODE_W4A4), Ci)
+
+
+def wq_conv3d_workspace_bytes(w: ConvWeights, D: int, H: int, W: int) -> int:
+    return int(lib().wq_conv3d_workspace_bytes(ctypes.c_void_p(w.handle), D, H, W))
+
+
+def wq_conv3d_forward(w: ConvWeights, x, y=None, workspace=None, stream=None):
+    """y [1, C_out, D, H, W] bf16 = conv3d(x [1, C_in, D, H, W] bf16), 3x3x3, padding 1."""
+    import torch
+    _, C, D, H, W = x.shape
+    if y is None:
+        y = torch.empty((1, w.N, D, H, W), dtype=torch.bfloat16, device=x.device)
+    if workspace is None:
+        workspace = _alloc_workspace(wq_conv3d_workspace_bytes(w, D, H, W), x.device)
+    _check(lib().wq_conv3d_forward(ctypes.c_void_p(w.handle), ctypes.c_void_p(x.data_ptr()), D, H, W,
+                                   ctypes.c_void_p(y.data_ptr()), ctypes.c_void_p(workspace.data_ptr()),
+                                   workspace.numel(), ctypes.c_void_p(_stream_ptr(stream))))
+    return y
+
+
+def wq_quantize_conv3d_input(w: ConvWeights, x, stream=None):
+    import torch
+    _, C, D, H, W = x.shape
+    V = D * H * W
+    codes = torch.empty((V, C // 2), dtype=torch.uint8, device=x.device)
+    scales = torch.empty((V, C // 16), dtype=torch.uint8, device=x.device)
+    g = torch.empty(1, dtype=torch.float32, device=x.device)
+    ws = _alloc_workspace(wq_conv3d_workspace_bytes(w, D, H, W), x.device)
+    _check(lib().wq_quantize_conv3d_input(ctypes.c_void_p(w.handle), ctypes.c_void_p(x.data_ptr()), D, H, W,
+                                          ctypes.c_void_p(codes.data_ptr()), ctypes.c_void_p(scales.data_ptr()),
+                                          ctypes.c_void_p(g.data_ptr()), ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+                                          ctypes.c_void_p(_stream_ptr(stream))))
+    return codes, scales, g

@@ -160,6 +160,8 @@ struct wq_weights {
     uint16_t* d_WOt = nullptr;     // [N, n_out] fp16
     int* d_err = nullptr;
     float* d_colscale = nullptr;   // W8A8: per-output-column weight scale [N]
+    int conv_cin = 0;              // Conv3d handles: input channels (K = 27 conv_cin)
+    CUtensorMap tmBconv{};         // Conv3d: weight codes with 64-byte boxes
     CUtensorMap tmB{}, tmQ{}, tmWO{};
     // activation / output tensor maps, re-encoded when the buffers change
     std::mutex mu;
@@ -631,6 +633,93 @@ WQ_API wq_status wq_export_weights_w8a8(wq_weights_t h, int8_t* q, float* w) {
             q[i] = static_cast<int8_t>(__bfloat162float(__ushort_as_bfloat16(b[i])));
     }
     if (w) WQ_CUDA(cudaMemcpy(w, h->d_colscale, static_cast<size_t>(N) * 4, cudaMemcpyDeviceToHost), "export");
+    return WQ_OK;
+}
+
+WQ_API wq_status wq_prepare_conv3d(const float* w, int C_in, int C_out, void* stream, wq_weights_t* out) {
+    g_last_error.clear();
+    if (!out) return fail(WQ_ERR_INVALID, "out is NULL");
+    *out = nullptr;
+    if (!w) return fail(WQ_ERR_INVALID, "w is NULL");
+    if (C_in <= 0 || C_out <= 0) return fail(WQ_ERR_INVALID, "channel counts must be positive");
+    if (C_in % 128 || C_out % 16 || 27 * C_in > 16384)
+        return fail(WQ_ERR_UNSUPPORTED, "need C_in % 128 == 0, C_out % 16 == 0 and 27 C_in <= 16384");
+    const int K = 27 * C_in, N = C_out;
+    std::vector<float> Wm(static_cast<size_t>(K) * N);      // [K = (kd, kh, kw, c_in), N]
+    for (int n = 0; n < N; ++n)
+        for (int c = 0; c < C_in; ++c)
+            for (int t = 0; t < 27; ++t)
+                Wm[(static_cast<size_t>(t) * C_in + c) * N + n] = w[(static_cast<size_t>(n) * C_in + c) * 27 + t];
+    wq_config cfg{K, N, 0, 0, 0, WQ_MODE_W4A4};
+    wq_weights_t h = nullptr;
+    const wq_status st = wq_prepare_weights(&cfg, Wm.data(), nullptr, nullptr, nullptr, nullptr, nullptr, stream, &h);
+    if (st != WQ_OK) return st;
+    h->conv_cin = C_in;
+    const char* why = "";
+    if (!wq::encode_tmap_2d(&h->tmBconv, CU_TENSOR_MAP_DATA_TYPE_UINT8, h->d_codes, K / 2, N, K / 2, 64, 128,
+                            CU_TENSOR_MAP_SWIZZLE_64B, &why)) {
+        wq_free_weights(h);
+        return fail(WQ_ERR_CUDA, why);
+    }
+    *out = h;
+    return WQ_OK;
+}
+
+WQ_API size_t wq_conv3d_workspace_bytes(wq_weights_t h, int D, int H, int W) {
+    if (!h || h->conv_cin == 0 || D <= 0 || H <= 0 || W <= 0) return 0;
+    return wq::conv_workspace_bytes(h->conv_cin, D * H * W, h->num_sms);
+}
+
+static wq_status conv_args(wq_weights_t h, const void* x, int D, int H, int W, void* ws, size_t ws_bytes,
+                           wq::ConvArgs* a) {
+    if (!h) return fail(WQ_ERR_INVALID, "NULL handle");
+    if (h->conv_cin == 0) return fail(WQ_ERR_INVALID, "handle was not prepared with wq_prepare_conv3d");
+    if (!x || !ws) return fail(WQ_ERR_INVALID, "NULL buffer");
+    if (D <= 0 || H <= 0 || W <= 0) return fail(WQ_ERR_INVALID, "bad spatial size");
+    const int V = D * H * W;
+    if (V % 8) return fail(WQ_ERR_UNSUPPORTED, "D H W must be a multiple of 8");
+    if ((reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(ws) & 255))
+        return fail(WQ_ERR_INVALID, "x must be 16-byte and the workspace 256-byte aligned");
+    if (ws_bytes < wq_conv3d_workspace_bytes(h, D, H, W)) return fail(WQ_ERR_INVALID, "workspace too small");
+    const int C = h->conv_cin;
+    uint8_t* b = static_cast<uint8_t*>(ws);
+    auto al = [](size_t v) { return (v + 1023) / 1024 * 1024; };
+    a->x = x; a->C = C; a->D = D; a->H = H; a->W = W; a->V = V; a->N = h->cfg.N;
+    a->partial = reinterpret_cast<float*>(b);
+    a->g = a->partial + 2 * h->num_sms;
+    a->codes = b + al(static_cast<size_t>(2 * h->num_sms + 1) * 4);
+    a->scales = a->codes + al(static_cast<size_t>(V) * C / 2);
+    a->tmB = &h->tmBconv; a->sfb = h->d_sf; a->gw = h->gW; a->err = h->d_err; a->num_sms = h->num_sms;
+    return WQ_OK;
+}
+
+WQ_API wq_status wq_conv3d_forward(wq_weights_t h, const void* x, int D, int H, int W, void* y, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+    wq::ConvArgs a{};
+    wq_status s = conv_args(h, x, D, H, W, workspace, workspace_bytes, &a);
+    if (s != WQ_OK) return s;
+    if (!y || (reinterpret_cast<uintptr_t>(y) & 15)) return fail(WQ_ERR_INVALID, "y must be a 16-byte aligned buffer");
+    a.y = y;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = wq::launch_conv_quant(a, st);
+    if (e != cudaSuccess) return cuda_fail(e, "conv quantiser launch");
+    e = wq::launch_conv_gemm(a, st);
+    if (e != cudaSuccess) return cuda_fail(e, "conv GEMM launch");
+    return WQ_OK;
+}
+
+WQ_API wq_status wq_quantize_conv3d_input(wq_weights_t h, const void* x, int D, int H, int W, uint8_t* codes,
+                                          uint8_t* scales, float* g, void* workspace, size_t workspace_bytes,
+                                          void* stream) {
+    wq::ConvArgs a{};
+    wq_status s = conv_args(h, x, D, H, W, workspace, workspace_bytes, &a);
+    if (s != WQ_OK) return s;
+    if (!codes || !scales || !g) return fail(WQ_ERR_INVALID, "NULL output");
+    if ((reinterpret_cast<uintptr_t>(codes) & 15) || (reinterpret_cast<uintptr_t>(scales) & 3))
+        return fail(WQ_ERR_INVALID, "codes must be 16-byte and scales 4-byte aligned");
+    a.codes = codes; a.scales = scales; a.g = g;
+    const cudaError_t e = wq::launch_conv_quant(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "conv quantiser launch");
     return WQ_OK;
 }
 

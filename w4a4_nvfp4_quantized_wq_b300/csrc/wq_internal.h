@@ -74,6 +74,25 @@ struct GemmArgs {
 
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream);
 
+struct ConvArgs {
+    const void* x;            // bf16 NCDHW [1, C, D, H, W]
+    int C, D, H, W, V, N;     // V = D H W voxels, N output channels
+    float* partial;           // [2 num_sms] per-CTA maxima of |x|
+    float* g;                 // tensor scale of the input
+    uint8_t* codes;           // [V, C/2]
+    uint8_t* scales;          // [V, C/16]
+    const CUtensorMap* tmB;   // weight codes [N, 27 C / 2] u8, box 64 x 128, swizzle 64B
+    const uint8_t* sfb;       // weight scales, MMA layout
+    float gw;
+    void* y;                  // bf16 NCDHW [1, N, D, H, W]
+    int* err;
+    int num_sms;
+};
+
+size_t conv_workspace_bytes(int C, int V, int num_sms);
+cudaError_t launch_conv_quant(const ConvArgs& a, cudaStream_t stream);
+cudaError_t launch_conv_gemm(const ConvArgs& a, cudaStream_t stream);
+
 // Record a message for wq_last_error() (thread-local).
 void set_last_error(const char* msg);
 
