@@ -122,12 +122,14 @@ def test_activation_quant_bitexact(case):
 
 
 @pytest.mark.parametrize("case,split", [("expert_small", 1), ("expert_small", 4), ("expert_small", 16),
-                                        ("dit_r32_o64_ragged_n", 2), ("dit_r32_o64_ragged_n", 8),
-                                        ("no_smooth_r64", 1), ("no_smooth_r64", 2), ("backbone_r0", 1),
-                                        ("multi_tile_kstage_tail", 1), ("multi_tile_kstage_tail", 16)])
+                                        ("dit_r32_o64_ragged_n", 2), ("dit_r32_o64_ragged_n", 3),
+                                        ("dit_r32_o64_ragged_n", 8), ("no_smooth_r64", 1), ("no_smooth_r64", 5),
+                                        ("backbone_r0", 2), ("multi_tile_kstage_tail", 3),
+                                        ("multi_tile_kstage_tail", 16)])
 def test_activation_quant_split(case, split, monkeypatch):
-    """The quantiser with a row tile's K range on one CTA or spread over a cluster (the row
-    amax and the low-rank partial sums then go through distributed shared memory)."""
+    """The quantiser with a row tile's K range on one CTA or spread over a cluster of 2..16
+    CTAs, including sizes that split the blocks unevenly (the row amax and the low-rank
+    partial sums then go through distributed shared memory)."""
     monkeypatch.setenv("WQ_QUANT_SPLIT", str(split))
     L = layer(case)
     w = prep(L)
@@ -137,6 +139,32 @@ def test_activation_quant_split(case, split, monkeypatch):
     aq = oracle.quantize_act(L.x_bits, L.s, L.rotate, L.omega)
     assert np.array_equal(g.cpu().numpy(), aq.g)
     assert np.array_equal(scales.cpu().numpy(), aq.scales)
+    assert np.array_equal(codes.cpu().numpy(), aq.codes)
+    if L.omega.size:
+        assert np.array_equal(xo.cpu().view(torch.int16).numpy().view(np.uint16), aq.x_omega)
+    if L.rank:
+        o = oracle.prepare_weights(L.W, L.s, L.L1, L.L2, L.omega, L.rotate)
+        U = oracle.lowrank_act(L.x_bits, o.P)
+        ug = u.cpu().view(torch.int16).numpy().view(np.uint16)
+        assert u_close(ug, U, L.x_bits, o.P).all()
+
+
+@pytest.mark.parametrize("case", list(CASES))
+@pytest.mark.parametrize("schedule", ["stream", "cluster"])
+def test_activation_quant_schedules(case, schedule, monkeypatch):
+    """Both quantiser schedules on every case: persistent CTAs that stream each row tile's
+    blocks twice (the second pass recomputes the transform) and clusters that keep the
+    transformed blocks resident."""
+    monkeypatch.setenv("WQ_QUANT_SCHEDULE", schedule)
+    L = layer(case)
+    w = prep(L)
+    x = x_dev(L.x_bits)
+    codes, scales, g, xo, u = wq.wq_quantize_activations(w, x, wq.WQ_SCALE_LAYOUT_MMA)
+    torch.cuda.synchronize()
+    wq.wq_check_device_error(w)
+    aq = oracle.quantize_act(L.x_bits, L.s, L.rotate, L.omega)
+    assert np.array_equal(g.cpu().numpy(), aq.g)
+    assert np.array_equal(wq.mma_scales_to_rowmajor(scales.cpu().numpy(), L.M, L.spec.K), aq.scales)
     assert np.array_equal(codes.cpu().numpy(), aq.codes)
     if L.omega.size:
         assert np.array_equal(xo.cpu().view(torch.int16).numpy().view(np.uint16), aq.x_omega)
@@ -233,6 +261,53 @@ def test_rounding_ties_through_the_quantiser():
     assert np.array_equal(wl.bf16_from_bits(bits), x)
     W = np.random.default_rng(0).standard_normal((K, 64)).astype(np.float32) * 0.02
     w = wq.wq_prepare_weights(K, 64, W, rotate=False)
+    codes, scales, g, _, _ = wq.wq_quantize_activations(w, x_dev(bits))
+    torch.cuda.synchronize()
+    aq = oracle.quantize_act(bits, None, False)
+    assert np.all(aq.g == 1.0)
+    assert np.array_equal(scales.cpu().numpy(), aq.scales)
+    assert np.array_equal(codes.cpu().numpy(), aq.codes)
+
+
+def _e4m3_midpoints():
+    """Every midpoint between neighbouring positive e4m3 values (subnormal and normal)."""
+    vals = []
+    for e in range(16):
+        for m in range(8):
+            if e == 15 and m == 7:
+                continue                      # NaN
+            vals.append(m * 2.0 ** -9 if e == 0 else (1 + m / 8) * 2.0 ** (e - 7))
+    vals = sorted(set(vals))
+    return [(a + b) / 2 for a, b in zip(vals[:-1], vals[1:])]
+
+
+@pytest.mark.parametrize("schedule", ["stream", "cluster"])
+def test_scale_ties_through_the_quantiser(schedule, monkeypatch):
+    """Block maxima at 6 x every e4m3 midpoint (and one bf16 step either side) in rows with
+    g = 1: (bmax / 6) / g lands exactly on the scale's rounding boundaries, where the fast
+    reciprocal path has to hand over to the exact divisions."""
+    monkeypatch.setenv("WQ_QUANT_SCHEDULE", schedule)
+    K = 512
+    targets = []
+    for mid in _e4m3_midpoints():
+        v = np.float32(6.0 * mid)
+        b = int(wl.bf16_bits(np.array([v], np.float32))[0])
+        for d in (-1, 0, 1):
+            targets.append(float(wl.bf16_from_bits(np.array([b + d], np.uint16))[0]))
+    per_row = K // 16 - 1
+    rows = []
+    for i in range(0, len(targets), per_row):
+        r = np.zeros(K, np.float32)
+        r[0] = 2688.0
+        for j, t in enumerate(targets[i:i + per_row]):
+            blk = np.linspace(0.0, t, 16, dtype=np.float32)
+            blk[-1] = t
+            r[16 * (j + 1):16 * (j + 2)] = wl.bf16_from_bits(wl.bf16_bits(blk))
+        rows.append(r)
+    x = np.stack(rows)
+    bits = wl.bf16_bits(x)
+    W = np.random.default_rng(1).standard_normal((K, 32)).astype(np.float32) * 0.02
+    w = wq.wq_prepare_weights(K, 32, W, rotate=False)
     codes, scales, g, _, _ = wq.wq_quantize_activations(w, x_dev(bits))
     torch.cuda.synchronize()
     aq = oracle.quantize_act(bits, None, False)

@@ -152,8 +152,8 @@ struct wq_weights {
     uint8_t* d_codes = nullptr;    // [N, K/2]
     uint8_t* d_sf = nullptr;       // MMA layout, ceil(N/128) * K/64 atoms
     float* d_bias = nullptr;       // [N]
-    float* d_inv_s = nullptr;      // [K]
-    int16_t* d_omega_pos = nullptr;// [K]
+    float* d_inv_s = nullptr;      // [K], quantiser pair order (see pair_order)
+    uint32_t* d_omega_blk = nullptr;// [K/64][4]: Omega bit mask (2 words), index of its first channel, 0
     uint16_t* d_P = nullptr;       // [K, r] bf16
     uint32_t* d_Pfrag = nullptr;   // P in mma.sync m16n8k16 B-fragment order
     uint16_t* d_Qt = nullptr;      // [N, r] bf16
@@ -201,7 +201,7 @@ void free_device(wq_weights* h) {
     cudaFree(h->d_sf);
     cudaFree(h->d_bias);
     cudaFree(h->d_inv_s);
-    cudaFree(h->d_omega_pos);
+    cudaFree(h->d_omega_blk);
     cudaFree(h->d_P);
     cudaFree(h->d_Pfrag);
     cudaFree(h->d_Qt);
@@ -220,6 +220,19 @@ wq_status upload(T** dst, const void* src, size_t bytes, cudaStream_t st) {
 }
 
 }  // namespace
+
+// Per 32-channel half of each 64-block, channels k and k + 16 side by side (k = 0..15): the
+// order in which a quantiser lane holds its channels as packed pairs.
+template <typename T>
+static std::vector<T> pair_order(const std::vector<T>& v) {
+    std::vector<T> o(v.size());
+    for (size_t h = 0; h < v.size() / 32; ++h)
+        for (size_t k = 0; k < 16; ++k) {
+            o[32 * h + 2 * k] = v[32 * h + k];
+            o[32 * h + 2 * k + 1] = v[32 * h + k + 16];
+        }
+    return o;
+}
 
 extern "C" {
 
@@ -254,6 +267,7 @@ WQ_API wq_status wq_prepare_weights(const wq_config* cfg, const float* W, const 
     // ---- smoothing inverse and the 16-bit low-rank factors
     std::vector<float> inv_s(s ? K : 0);
     for (int k = 0; k < (s ? K : 0); ++k) inv_s[k] = 1.0f / s[k];
+    const std::vector<float> inv_s_pairs = pair_order(inv_s);
     std::vector<uint16_t> P(static_cast<size_t>(K) * r), Qt(static_cast<size_t>(N) * r);
     for (int k = 0; k < K; ++k)
         for (int j = 0; j < r; ++j) {
@@ -306,9 +320,14 @@ WQ_API wq_status wq_prepare_weights(const wq_config* cfg, const float* W, const 
 
     // ---- the fp16 outlier rows of the rotated basis
     std::vector<uint16_t> WOt(static_cast<size_t>(N) * no);
-    std::vector<int16_t> omega_pos(no ? K : 0, -1);
+    // per 64-block of K: which channels are kept (bit mask) and the x_O index of the first one
+    std::vector<uint32_t> omega_blk(no ? static_cast<size_t>(K / 64) * 4 : 0, 0u);
+    for (int j = no - 1; j >= 0; --j) {
+        const int b = omega[j] / 64, e = omega[j] % 64;
+        omega_blk[4 * b + e / 32] |= 1u << (e % 32);
+        omega_blk[4 * b + 2] = static_cast<uint32_t>(j);
+    }
     for (int j = 0; j < no; ++j) {
-        omega_pos[omega[j]] = static_cast<int16_t>(j);
         for (int n = 0; n < N; ++n) {
             float& v = Rp[static_cast<size_t>(omega[j]) * N + n];
             WOt[static_cast<size_t>(n) * no + j] = f16_bits(v);
@@ -345,7 +364,7 @@ WQ_API wq_status wq_prepare_weights(const wq_config* cfg, const float* W, const 
         if ((st = upload(&h->d_codes, q8.data(), q8.size() * 2, cs)) != WQ_OK) return bail(st);
         if ((st = upload(&h->d_colscale, wsc.data(), N * 4, cs)) != WQ_OK) return bail(st);
         if (bias && (st = upload(&h->d_bias, bias_f.data(), N * 4, cs)) != WQ_OK) return bail(st);
-        if (s && (st = upload(&h->d_inv_s, inv_s.data(), K * 4, cs)) != WQ_OK) return bail(st);
+        if (s && (st = upload(&h->d_inv_s, inv_s_pairs.data(), K * 4, cs)) != WQ_OK) return bail(st);
         if (cudaMalloc(&h->d_err, sizeof(int)) != cudaSuccess) return bail(fail(WQ_ERR_OOM, "cudaMalloc failed"));
         if (cudaMemsetAsync(h->d_err, 0, sizeof(int), cs) != cudaSuccess) return bail(fail(WQ_ERR_CUDA, "memset"));
         if (cudaStreamSynchronize(cs) != cudaSuccess) return bail(fail(WQ_ERR_CUDA, "upload synchronise failed"));
@@ -406,8 +425,8 @@ WQ_API wq_status wq_prepare_weights(const wq_config* cfg, const float* W, const 
     if ((st = upload(&h->d_codes, codes.data(), codes.size(), cs)) != WQ_OK) return bail(st);
     if ((st = upload(&h->d_sf, sf_mma.data(), sf_mma.size(), cs)) != WQ_OK) return bail(st);
     if (bias && (st = upload(&h->d_bias, bias_f.data(), N * 4, cs)) != WQ_OK) return bail(st);
-    if (s && (st = upload(&h->d_inv_s, inv_s.data(), K * 4, cs)) != WQ_OK) return bail(st);
-    if (no && (st = upload(&h->d_omega_pos, omega_pos.data(), K * 2, cs)) != WQ_OK) return bail(st);
+    if (s && (st = upload(&h->d_inv_s, inv_s_pairs.data(), K * 4, cs)) != WQ_OK) return bail(st);
+    if (no && (st = upload(&h->d_omega_blk, omega_blk.data(), omega_blk.size() * 4, cs)) != WQ_OK) return bail(st);
     if (r && (st = upload(&h->d_P, P.data(), P.size() * 2, cs)) != WQ_OK) return bail(st);
     if (r && (st = upload(&h->d_Pfrag, Pfrag.data(), Pfrag.size() * 4, cs)) != WQ_OK) return bail(st);
     if (r && (st = upload(&h->d_Qt, Qt.data(), Qt.size() * 2, cs)) != WQ_OK) return bail(st);
@@ -453,7 +472,7 @@ static wq_status run_quant(wq_weights_t h, const void* x, int M, int layout, uin
         std::lock_guard<std::mutex> lk(h->mu_x);
         if (h->key_x != x || h->key_xM != M) {
             const char* why = "";
-            if (!wq::encode_tmap_2d(&h->tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, h->cfg.K, M, 2ull * h->cfg.K, 64, 32,
+            if (!wq::encode_tmap_2d(&h->tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, h->cfg.K, M, 2ull * h->cfg.K, 64, 16,
                                     CU_TENSOR_MAP_SWIZZLE_128B, &why)) {
                 h->key_x = nullptr;
                 return fail(WQ_ERR_CUDA, why);
@@ -470,7 +489,7 @@ static wq_status run_quant(wq_weights_t h, const void* x, int M, int layout, uin
     qa.K = h->cfg.K;
     qa.inv_s = h->d_inv_s;
     qa.rotate = h->cfg.rotate;
-    qa.omega_pos = h->d_omega_pos;
+    qa.omega_blk = h->d_omega_blk;
     qa.n_out = xo ? h->cfg.n_outliers : 0;
     qa.xo = xo;
     qa.P = h->d_P;

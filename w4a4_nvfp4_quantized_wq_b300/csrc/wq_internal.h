@@ -28,13 +28,13 @@ ActWorkspace carve_workspace(void* base, int M, int K, int r, int n_out);
 
 struct QuantArgs {
     const void* x;                  // bf16 [M, K]
-    const CUtensorMap* tmX;         // x as [M, K] bf16, box 64 x 32, swizzle 128B
+    const CUtensorMap* tmX;         // x as [M, K] bf16, box 64 x 16, swizzle 128B
     const uint32_t* pfrag;          // P in mma.sync B-fragment order (see wq_api.cu)
     int* err;                       // device error flag
     int M, K;
-    const float* inv_s;             // [K] or null
+    const float* inv_s;             // [K] or null; per 32-channel half, pairs (s_k, s_k+16), k = 0..15
     int rotate;
-    const int16_t* omega_pos;       // [K] -1 or slot, null when n_out == 0
+    const uint32_t* omega_blk;      // [K/64][4]: kept-channel mask (lo, hi), x_O index of the first, 0
     int n_out;
     uint16_t* xo;                   // fp16 [M, n_out]
     const uint16_t* P;              // bf16 [K, r]

@@ -4,8 +4,7 @@
 // via the FWHT with beta = 64, dynamic per-token quantisation; QuantWAMs sec. 3.1 Eq. (1):
 // the quantiser sees x R S^-1 and the Top-K channels of that basis stay in FP16):
 //   xs   = fp32(x) * inv_s                       (one fp32 multiply)
-//   xt   = FWHT64(xs) per 64-block               (strides 1,2,4 in registers; 8,16,32 across
-//                                                 lanes by shuffles; then * 1/8)
+//   xt   = FWHT64(xs) per 64-block, then * 1/8   (Sylvester order, strides 1..32)
 //   x_O  = fp16(xt[O]); xt[O] = 0                (outlier split)
 //   g    = amax(|xt|) / 2688                     (fp32 tensor scale of the row)
 //   sc_b = e4m3((bmax_b / 6) / g), d_b = dec(sc_b) * g, code = e2m1(xt / d_b)
@@ -13,17 +12,22 @@
 // Every rounding step is an explicit _rn intrinsic so no multiply-add contraction can
 // change a bit.
 //
-// A CTA owns a tile of 32 rows and a range of at most kMaxBlocks 64-column blocks of K (the
-// K range of a row tile is split over a thread-block cluster when K is long or the batch is
-// small).  Warp 8 streams the tile's blocks into shared memory with TMA (one 4 KiB,
-// 128-byte-swizzled box per block, each loaded once, into a 9 KiB slot).  Warps 0-7 make two
-// passes over the resident blocks.  Pass 1: the raw bf16 block feeds ldmatrix + mma.sync for
-// U; each thread (one row x 8 channels) smooths its channels and runs FWHT strides 1,2,4 in
-// registers, the block is transposed through its slot (fp32, rows padded to 72 words so both
-// orders are bank-conflict free) for strides 8,16,32, and the transformed fp32 block is left
-// in the slot; the row amax is accumulated.  Pass 2 reads the transformed blocks back and
-// writes the codes, scales and outlier values.  Across a cluster the row amax and the U
-// partial sums are combined through distributed shared memory.
+// Rows go in tiles of 16, 64-column blocks of K as 2 KiB TMA boxes (128-byte swizzle).  In a
+// warp, lane l owns row l % 16 and half l / 16 of a block (32 channels): FWHT strides 1..16
+// run in its registers, stride 32 is one shuffle with lane l ^ 16.  Each block goes through
+//   pass 1: smoothing, FWHT, the kept channels (fp16 values out), the 16-element maxima
+//           without them, the row amax; the block's share of U (mma.sync on the raw box,
+//           every n-tile of P) is added to the warp's partial in shared memory;
+//   pass 2: e4m3 scales and e2m1 codes (16 bytes per lane; a row's 32 bytes of a block form
+//           one sector), after the row amax of the whole row is known.
+// Two schedules:
+//   cluster (few rows): a CTA owns one row tile and a K range of at most 16 blocks (the K
+//           range of a tile is spread over a thread-block cluster); warp 8 loads every block
+//           once, the transformed fp32 block waits in its slot between the passes, and the
+//           row amax and U partials are combined through distributed shared memory;
+//   stream (many rows): persistent CTAs walk row tiles; warp 8 streams every block of a
+//           tile twice through a ring of shared-memory slots (the second time from L2), and
+//           pass 2 recomputes the transform instead of keeping it.
 //
 // kInt8 = true is the selective 8-bit variant (FoldQuantVLA, Key Contribution 3) in the same
 // basis: a = amax / 127 per row, q = round-half-even(xt / a) clamped to [-127, 127], written as
@@ -39,26 +43,44 @@
 
 #ifdef WQ_TRACE
 // Timeline probes for kernel development builds only (never defined in the product build).
-__device__ unsigned long long g_wq_qtrace[4096 * 8];
-#define WQ_QTRACE_AT(slot) (g_wq_qtrace[blockIdx.x * 8 + (slot)] = wq::global_timer_ns())
+__device__ unsigned long long g_wq_qtrace[8192 * 8];
+#define WQ_QTRACE_AT(slot) do { if (blockIdx.x < 8192) g_wq_qtrace[blockIdx.x * 8 + (slot)] = wq::global_timer_ns(); } while (0)
 extern "C" WQ_API int wq_qtrace_read(void* host, size_t bytes) {
     return static_cast<int>(cudaMemcpyFromSymbol(host, g_wq_qtrace, bytes));
 }
+__device__ unsigned long long g_wq_qphase[16];
+extern "C" WQ_API int wq_qphase_read(void* host, size_t bytes) {
+    return static_cast<int>(cudaMemcpyFromSymbol(host, g_wq_qphase, bytes));
+}
+#define QPH_DECL unsigned long long qph_[8] = {0, 0, 0, 0, 0, 0, 0, 0}; long long qpt_ = clock64()
+#define QPH(i) do { const long long n_ = clock64(); qph_[i] += n_ - qpt_; qpt_ = n_; } while (0)
+#define QPH_FLUSH do { if (lane == 0) { for (int i_ = 0; i_ < 8; ++i_) atomicAdd(&g_wq_qphase[i_], qph_[i_]); atomicAdd(&g_wq_qphase[8], 1ull); } } while (0)
 #else
 #define WQ_QTRACE_AT(slot) ((void)0)
+#define QPH_DECL ((void)0)
+#define QPH(i) ((void)0)
+#define QPH_FLUSH ((void)0)
 #endif
 
 namespace wq {
 namespace {
 
-constexpr int kRows = 32;                 // rows per tile
-constexpr int kConsumerWarps = 8;         // 32 rows x 8 chunks = 256 threads
+constexpr int kRows = 16;                 // rows per tile
+constexpr int kConsumerWarps = 8;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr uint32_t kBlockBytes = kRows * 128;          // one TMA box: 32 rows x 64 bf16
-constexpr uint32_t kRowWords = 72;                      // fp32 row stride of a slot (64 + 8 pad)
-constexpr uint32_t kSlotBytes = 9216;                   // 32 x 72 x 4, a multiple of 1024
-constexpr int kTargetBlocks = 8;          // blocks per CTA aimed for (74 KiB: three CTAs per SM)
-constexpr int kMaxBlocks = 20;
+constexpr uint32_t kBoxBytes = kRows * 128;            // one TMA box: 16 rows x 64 bf16
+constexpr uint32_t kRowBytes = 272;                     // fp32 row: 64 values + 16 B pad
+constexpr uint32_t kF32Off = kBoxBytes;                 // transformed rows (cluster schedule)
+constexpr uint32_t kMaxOff = kF32Off + kRows * kRowBytes;   // 6400: four 16-block maxima per row
+constexpr uint32_t kSlotBytes = 7168;                   // a multiple of 1024 (TMA swizzle alignment)
+constexpr int kMaxBlocks = 16;                          // blocks of one CTA (cluster schedule)
+#ifndef WQ_QUANT_RING
+#define WQ_QUANT_RING 16
+#endif
+#ifndef WQ_QUANT_MINB
+#define WQ_QUANT_MINB 3
+#endif
+constexpr int kRing = WQ_QUANT_RING;                    // ring slots (stream schedule)
 constexpr unsigned kFullMask = 0xFFFFFFFFu;
 
 struct QParams {
@@ -69,7 +91,7 @@ struct QParams {
     int row_tiles;
     const float* inv_s;
     int rotate;
-    const int16_t* omega_pos;
+    const uint32_t* omega_blk;   // per block: kept-channel mask (2 words), x_O index of the first
     int n_out;
     uint16_t* xo;
     const uint32_t* pfrag;   // low-rank factor P in mma.sync B-fragment order
@@ -81,114 +103,345 @@ struct QParams {
     int* err;
 };
 
-struct Layout {
-    uint32_t off_invs, off_opos, off_bar, off_amax, off_u, off_abort, total;
-};
-
-__host__ __device__ inline Layout make_layout(int max_nb, int r) {
-    Layout l{};
-    l.off_invs = static_cast<uint32_t>(max_nb) * kSlotBytes;            // inv_s slice, 256 B per block
-    l.off_opos = l.off_invs + 256u * static_cast<uint32_t>(max_nb);    // Omega slot slice, 128 B per block
-    l.off_bar = l.off_opos + 128u * static_cast<uint32_t>(max_nb);
-    l.off_amax = l.off_bar + 8u * static_cast<uint32_t>(max_nb + 1);
-    l.off_amax = (l.off_amax + 15u) & ~15u;
-    l.off_u = l.off_amax + 4u * kRows;
-    l.off_abort = l.off_u + 4u * kRows * static_cast<uint32_t>(r > 0 ? r : 1);
-    l.total = l.off_abort + 16u + 1024u;
-    return l;
-}
-
-__device__ __forceinline__ void bf16x8_to_f32(const uint4& raw, float (&f)[8]) {
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        f[2 * i] = __uint_as_float(w[i] << 16);
-        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
-}
-
+// ------------------------------------------------------------------ shared-memory helpers
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
     uint4 v;
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
     return v;
 }
-
-// Smoothing and FWHT strides 1, 2, 4 of this thread's 8 channels (s_invs: their 8 entries of
-// the shared-memory copy of inv_s).
-__device__ __forceinline__ void transform_low(const uint4& raw, const float* s_invs, const QParams& p, float (&v)[8]) {
-    bf16x8_to_f32(raw, v);
-    if (p.inv_s != nullptr) {
-        const float4* sp = reinterpret_cast<const float4*>(s_invs);
-        const float4 s0 = sp[0], s1 = sp[1];
-        const float s[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-#pragma unroll
-        for (int e = 0; e < 8; ++e) v[e] = __fmul_rn(v[e], s[e]);
-    }
-    if (p.rotate) {
-#pragma unroll
-        for (int h = 1; h < 8; h <<= 1) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                if ((e & h) == 0) {
-                    const float a = v[e], b = v[e + h];
-                    v[e] = __fadd_rn(a, b);
-                    v[e + h] = __fsub_rn(a, b);
-                }
-        }
-    }
+__device__ __forceinline__ float4 ld_shared_v4f(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr) : "memory");
+    return v;
 }
-
-// FWHT strides 8, 16, 32 and the 1/8 scale, on the 8 channels c, c+8, ..., c+56 of a row
-// (the partner of channel c + 8j at stride 8h is channel c + 8 (j ^ h)).
-__device__ __forceinline__ void transform_high(float (&w)[8]) {
-#pragma unroll
-    for (int h = 1; h < 8; h <<= 1) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            if ((j & h) == 0) {
-                const float a = w[j], b = w[j + h];
-                w[j] = __fadd_rn(a, b);
-                w[j + h] = __fsub_rn(a, b);
-            }
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) w[j] = __fmul_rn(w[j], 0.125f);
+__device__ __forceinline__ float2 ld_shared_v2f(uint32_t addr) {
+    float2 v;
+    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+    return v;
 }
-
-__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
-    asm volatile("st.shared.f32 [%0], %1;" :: "r"(addr), "f"(v) : "memory");
+__device__ __forceinline__ void st_shared_v2f(uint32_t addr, float a, float b) {
+    asm volatile("st.shared.v2.f32 [%0], {%1, %2};" :: "r"(addr), "f"(a), "f"(b) : "memory");
 }
 __device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
     float v;
     asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
     return v;
 }
-__device__ __forceinline__ void ld_shared_v8f(uint32_t addr, float (&v)[8]) {
-    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]) : "r"(addr) : "memory");
-    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v[4]), "=f"(v[5]), "=f"(v[6]), "=f"(v[7]) : "r"(addr + 16u) : "memory");
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
+    asm volatile("st.shared.f32 [%0], %1;" :: "r"(addr), "f"(v) : "memory");
 }
 
-// zero the kept channels; in pass 2 also store their fp16 values (s_opos: the 8 slot entries)
-__device__ __forceinline__ void split_outliers(float (&v)[8], const int16_t* s_opos, int row, bool store,
-                                               const QParams& p) {
-    const uint4 pw = *reinterpret_cast<const uint4*>(s_opos);
-    const uint32_t w[4] = {pw.x, pw.y, pw.z, pw.w};
+// ------------------------------------------------------------------ packed fp32 pairs
+// A lane's 32 channels of a block are held as 16 pairs P[k] = (channel k, channel k + 16) of
+// its half, so the FWHT butterflies at strides 1..8 and the elementwise multiplies run as
+// packed two-lane fp32 instructions; each lane is rounded to nearest on its own, exactly as
+// the scalar operation would be.
+typedef unsigned long long f2;
+__device__ __forceinline__ f2 pk2(float lo, float hi) {
+    f2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float lo2(f2 x) {
+    float a, b;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(x));
+    (void)b;
+    return a;
+}
+__device__ __forceinline__ float hi2(f2 x) {
+    float a, b;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(x));
+    (void)a;
+    return b;
+}
+__device__ __forceinline__ f2 add2(f2 a, f2 b) {
+    f2 r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f2 sub2(f2 a, f2 b) {
+    f2 r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f2 mul2(f2 a, f2 b) {
+    f2 r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {   // RN(a b + c) per lane
+    f2 r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
+// ------------------------------------------------------------------ per-block steps
+// Row r, half `half` of a raw 16 x 64 bf16 box (128-byte swizzle: 16-byte chunk c of row r at
+// c ^ (r % 8)) -> 16 pairs of smoothed and rotated values.  invs: shared address of the
+// block's 64 inv_s values stored pair-wise (per half: s_k, s_k+16 for k = 0..15), or 0.
+// FWHT in the pages' order: strides 1, 2, 4, 8 between pairs, 16 inside a pair, 32 with the
+// partner lane (lane ^ 16 holds the other half of the row: a + b there, a - b here, as one
+// fused multiply-add with an exact +-1 product), then the exact 1/8 normalisation.
+__device__ __forceinline__ void load_transform(uint32_t box, int r, int half, uint32_t invs, int rotate,
+                                               f2 (&P)[16]) {
+    uint32_t w[4][4];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        const int pos = static_cast<int16_t>((w[e / 2] >> (16 * (e & 1))) & 0xFFFFu);
-        if (pos >= 0) {
-            if (store) p.xo[static_cast<size_t>(row) * p.n_out + pos] = __half_as_ushort(__float2half_rn(v[e]));
-            v[e] = 0.0f;
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t c = static_cast<uint32_t>(4 * half + j);
+        const uint4 q = ld_shared_v4(box + static_cast<uint32_t>(r) * 128u + ((c ^ (static_cast<uint32_t>(r) & 7u)) << 4));
+        w[j][0] = q.x; w[j][1] = q.y; w[j][2] = q.z; w[j][3] = q.w;
+    }
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        const uint32_t a = w[k / 8][(k % 8) / 2], b = w[2 + k / 8][(k % 8) / 2];
+        P[k] = (k & 1) ? pk2(__uint_as_float(a & 0xFFFF0000u), __uint_as_float(b & 0xFFFF0000u))
+                       : pk2(__uint_as_float(a << 16), __uint_as_float(b << 16));
+    }
+    if (invs != 0u) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float4 sv = ld_shared_v4f(invs + 128u * half + 16u * j);
+            P[2 * j] = mul2(P[2 * j], pk2(sv.x, sv.y));
+            P[2 * j + 1] = mul2(P[2 * j + 1], pk2(sv.z, sv.w));
+        }
+    }
+    if (rotate) {
+#pragma unroll
+        for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+                if ((k & h) == 0) {
+                    const f2 a = P[k], b = P[k + h];
+                    P[k] = add2(a, b);
+                    P[k + h] = sub2(a, b);
+                }
+        }
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const float a = lo2(P[k]), b = hi2(P[k]);
+            P[k] = pk2(__fadd_rn(a, b), __fsub_rn(a, b));
+        }
+        const float sgn = half ? -1.0f : 1.0f;
+        const f2 sg = pk2(sgn, sgn);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const f2 o = pk2(__shfl_xor_sync(kFullMask, lo2(P[k]), 16), __shfl_xor_sync(kFullMask, hi2(P[k]), 16));
+            P[k] = fma2(P[k], sg, o);
+        }
+        const f2 c8 = pk2(0.125f, 0.125f);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) P[k] = mul2(P[k], c8);
+    }
+}
+
+// Zero the kept channels of this half (bit e of `mine`: channel e): a kept channel becomes +0
+// and every other value keeps all its bits, the sign of a zero included.
+__device__ __forceinline__ void apply_keep(f2 (&P)[16], uint32_t mine) {
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        const uint32_t a = ((mine >> k) & 1u) - 1u;          // channel k: 0 if kept, else all ones
+        const uint32_t b = ((mine >> (k + 16)) & 1u) - 1u;   // channel k + 16
+        P[k] &= (static_cast<f2>(b) << 32) | a;
+    }
+}
+
+// e4m3(RN(RN(bm / 6) / g)), the block scale.  t = RN(RN(bm c6) rg) with c6 = RN(1/6) and
+// rg = RN(1/g) is within 6 ulp-units of 2^-24 (relative) of the two-division value, so when
+// t (1 - 2^-20) and t (1 + 2^-20) convert to the same code, that value (which lies between
+// them; the conversion is monotone) converts to it too.  Otherwise, and when a product could
+// leave the normal range, the two divisions are done.
+__device__ __forceinline__ uint32_t scale_code(float bm, float g, float rg) {
+    if (g == 0.0f || bm == 0.0f) return 0u;
+    const float u = __fmul_rn(bm, 0.16666667163372040f);
+    if (rg < 3.0e38f && u >= 1.0e-36f) {
+        const float t = __fmul_rn(u, rg);
+        const uint32_t lo = cvt_e4m3(__fmul_rn(t, 0.99999904632568359f));
+        const uint32_t hi = cvt_e4m3(__fmul_rn(t, 1.00000095367431641f));
+        if (lo == hi) return lo;
+    }
+    return cvt_e4m3(__fdiv_rn(__fdiv_rn(bm, 6.0f), g));
+}
+
+// Maxima of |x| over the half's two 16-element blocks (channels 0..15: the pairs' first lanes).
+__device__ __forceinline__ void absmax_pairs(const f2 (&P)[16], float& ma, float& mb) {
+    ma = 0.0f;
+    mb = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        ma = fmaxf(ma, fabsf(lo2(P[k])));
+        mb = fmaxf(mb, fabsf(hi2(P[k])));
+    }
+}
+
+// Codes of channels (k, k+1) of both 16-blocks of the half (pairs P0 = P[k], P1 = P[k+1]), by
+// the reciprocal-and-bracket argument of e2m1_codes8_r, two blocks per packed multiply.
+__device__ __forceinline__ void codes_2x2(f2 P0, f2 P1, f2 rr, float da, float db, uint32_t& ca, uint32_t& cb) {
+    const f2 mlo = pk2(0.99999952316284180f, 0.99999952316284180f);
+    const f2 mhi = pk2(1.00000047683715820f, 1.00000047683715820f);
+    const f2 q0 = mul2(P0, rr), q1 = mul2(P1, rr);
+    const f2 l0 = mul2(q0, mlo), l1 = mul2(q1, mlo), h0 = mul2(q0, mhi), h1 = mul2(q1, mhi);
+    const uint32_t alo = cvt_e2m1x2(lo2(l0), lo2(l1)), ahi = cvt_e2m1x2(lo2(h0), lo2(h1));
+    const uint32_t blo = cvt_e2m1x2(hi2(l0), hi2(l1)), bhi = cvt_e2m1x2(hi2(h0), hi2(h1));
+    ca = alo == ahi ? alo : cvt_e2m1x2(__fdiv_rn(lo2(P0), da), __fdiv_rn(lo2(P1), da));
+    cb = blo == bhi ? blo : cvt_e2m1x2(__fdiv_rn(hi2(P0), db), __fdiv_rn(hi2(P1), db));
+}
+
+// Pull block kb's slice of the packed P (NT KiB) towards this SM's L1, one 128-byte line per
+// lane, ahead of the U step that reads it.
+template <int NT>
+__device__ __forceinline__ void prefetch_block_consts(const QParams& p, int kb, int lane) {
+    if (kb >= p.nblk) return;
+    if constexpr (NT > 0) {
+        const char* pf = reinterpret_cast<const char*>(p.pfrag) + static_cast<size_t>(kb) * NT * 1024;
+#pragma unroll
+        for (int l = lane; l < NT * 8; l += 32)
+            asm volatile("prefetch.global.L1 [%0];" :: "l"(pf + 128 * l));
+    }
+}
+
+// The block's share of U = x P: A = the raw 16 x 64 box, every n-tile of P.  Each
+// (block, n-tile) is accumulated on the tensor cores from zero and added to the warp's
+// partial (shared memory, mma fragment order, 512 B per n-tile) with an fp32 add, so the
+// tensor-core accumulation depth stays at 64 whatever K is.
+template <int NT>
+__device__ __forceinline__ void u_step(uint32_t box, int lane, int kb, const uint32_t* pfrag, uint32_t upart, bool first) {
+    uint32_t a[4][4];
+    const uint32_t arow = static_cast<uint32_t>((lane & 7) + 8 * ((lane >> 3) & 1));
+#pragma unroll
+    for (int f = 0; f < 4; ++f) {
+        const uint32_t chunk = static_cast<uint32_t>(2 * f + (lane >> 4));
+        ldmatrix_x4(box + arow * 128u + ((chunk ^ (arow & 7u)) << 4), a[f][0], a[f][1], a[f][2], a[f][3]);
+    }
+    __syncwarp();                          // the box is read before a partial may land on it
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const uint4* pb = reinterpret_cast<const uint4*>(pfrag + (static_cast<size_t>(kb * NT + nt) * 32 + lane) * 8);
+        const uint4 q0 = __ldg(pb), q1 = __ldg(pb + 1);
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_bf16_16816(acc, a[0][0], a[0][1], a[0][2], a[0][3], q0.x, q0.y);
+        mma_bf16_16816(acc, a[1][0], a[1][1], a[1][2], a[1][3], q0.z, q0.w);
+        mma_bf16_16816(acc, a[2][0], a[2][1], a[2][2], a[2][3], q1.x, q1.y);
+        mma_bf16_16816(acc, a[3][0], a[3][1], a[3][2], a[3][3], q1.z, q1.w);
+        const uint32_t ua = upart + (static_cast<uint32_t>(nt) * 32u + lane) * 16u;
+        if (first) {
+            st_shared_v4f(ua, acc[0], acc[1], acc[2], acc[3]);
+        } else {
+            const float4 o = ld_shared_v4f(ua);
+            st_shared_v4f(ua, __fadd_rn(o.x, acc[0]), __fadd_rn(o.y, acc[1]), __fadd_rn(o.z, acc[2]), __fadd_rn(o.w, acc[3]));
         }
     }
 }
 
+// Codes and scales of this lane's half row of block kb (maxima bma, bmb of its two 16-blocks).
+__device__ __forceinline__ void emit_nvfp4(const f2 (&P)[16], float bma, float bmb, float gsc, float rg, int row,
+                                           bool row_ok, int kb, int half, const QParams& p) {
+    const uint32_t sa = scale_code(bma, gsc, rg), sb = scale_code(bmb, gsc, rg);
+    const float da = __fmul_rn(dec_e4m3(sa), gsc), db = __fmul_rn(dec_e4m3(sb), gsc);
+    const float ra = __frcp_rn(da), rb = __frcp_rn(db);
+    uint32_t wa[2] = {0u, 0u}, wb[2] = {0u, 0u};     // channels 0..7, 8..15 / 16..23, 24..31
+    if (ra < 3.0e38f && rb < 3.0e38f) {
+        // both blocks have a non-zero, non-tiny scale: packed path
+        const f2 rr = pk2(ra, rb);
+#pragma unroll
+        for (int k = 0; k < 16; k += 2) {
+            uint32_t ca, cb;
+            codes_2x2(P[k], P[k + 1], rr, da, db, ca, cb);
+            wa[k / 8] |= ca << (8 * ((k / 2) % 4));
+            wb[k / 8] |= cb << (8 * ((k / 2) % 4));
+        }
+    } else {
+        float va[16], vb[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            va[k] = lo2(P[k]);
+            vb[k] = hi2(P[k]);
+        }
+        if (da != 0.0f) {
+            wa[0] = e2m1_codes8_r(va, da, ra);
+            wa[1] = e2m1_codes8_r(va + 8, da, ra);
+        }
+        if (db != 0.0f) {
+            wb[0] = e2m1_codes8_r(vb, db, rb);
+            wb[1] = e2m1_codes8_r(vb + 8, db, rb);
+        }
+    }
+    const uint32_t s2 = sa | (sb << 8);
+    const uint32_t s2o = __shfl_xor_sync(kFullMask, s2, 16);
+    if (row_ok) {
+        const int K = p.K;
+        *reinterpret_cast<uint4*>(p.codes + static_cast<size_t>(row) * (K / 2) + kb * 32 + 16 * half) =
+            make_uint4(wa[0], wa[1], wb[0], wb[1]);
+        if (half == 0) {
+            size_t off;
+            if (p.sf_layout == WQ_SCALE_LAYOUT_MMA)
+                off = (static_cast<size_t>(row / kBlockM) * (K / 64) + kb) * kSfAtom + (row % 32) * 16 +
+                      ((row % kBlockM) / 32) * 4;
+            else
+                off = static_cast<size_t>(row) * (K / 16) + kb * 4;
+            *reinterpret_cast<uint32_t*>(p.sf + off) = s2 | (s2o << 16);
+        }
+    }
+}
+
+// 8-bit values of this lane's half row of block kb as exact bf16 integers (ra = RN(1 / gsc)).
+__device__ __forceinline__ void emit_int8(const f2 (&P)[16], float gsc, float ra, int row, bool row_ok, int kb,
+                                          int half, const QParams& p) {
+    float va[16], vb[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        va[k] = lo2(P[k]);
+        vb[k] = hi2(P[k]);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(p.codes + (static_cast<size_t>(row) * p.K + kb * 64 + 32 * half) * 2);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        float q[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (gsc != 0.0f) int8_values8_r(j < 2 ? va + 8 * j : vb + 8 * (j - 2), gsc, ra, q);
+        uint32_t pkw[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(q[2 * e], q[2 * e + 1]);
+            pkw[e] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        if (row_ok) dst[j] = make_uint4(pkw[0], pkw[1], pkw[2], pkw[3]);
+    }
+}
+
+// U entry of fragment index idx = (nt 32 + lane) 4 + e: row gq + 8 (e / 2), column
+// 8 nt + 2 cq + e % 2, with gq = lane / 4, cq = lane % 4.
+__device__ __forceinline__ void frag_pos(int idx, int& rr, int& cc) {
+    const int nt = idx / 128, ln = (idx / 4) % 32, e = idx % 4;
+    rr = (ln >> 2) + 8 * (e >> 1);
+    cc = 8 * nt + 2 * (ln & 3) + (e & 1);
+}
+
+// ==================================================================== cluster schedule
+struct Layout {
+    uint32_t off_invs, off_omega, off_bar, off_amax, off_rmax, off_upart, off_u, off_abort, total;
+};
+
+__host__ __device__ inline Layout make_layout(int max_nb, int r) {
+    Layout l{};
+    const uint32_t nb = static_cast<uint32_t>(max_nb);
+    const uint32_t nt = static_cast<uint32_t>(r / 8);
+    l.off_invs = nb * kSlotBytes;                  // inv_s slice, 256 B per block
+    l.off_omega = l.off_invs + 256u * nb;          // Omega table slice, 16 B per block
+    l.off_bar = l.off_omega + 16u * nb;
+    l.off_amax = (l.off_bar + 8u * (nb + 1u) + 15u) & ~15u;
+    l.off_rmax = l.off_amax + 4u * kRows * kConsumerWarps;
+    // per warp, the U partial in mma fragment order (nt x 512 B); up to rank 32 it fits the
+    // raw box of the warp's first block, which nothing reads after the warp's own U step
+    l.off_upart = l.off_rmax + 4u * kRows;
+    l.off_u = l.off_upart + (nt * 512u > kBoxBytes ? kConsumerWarps * nt * 512u : 0u);
+    l.off_abort = l.off_u + 4u * kRows * static_cast<uint32_t>(r > 0 ? r : 1);
+    l.total = l.off_abort + 16u + 1024u;
+    return l;
+}
+
 template <int R, bool kInt8>
-__global__ void __launch_bounds__(kThreads) quantize_kernel(const __grid_constant__ CUtensorMap tmX, const QParams p) {
-    constexpr int NT = R / 8 > 0 ? R / 8 : 1;       // n8 tiles of U
-    constexpr int NTW = NT > 4 ? NT / 4 : 1;        // n-tiles per warp
+__global__ void __launch_bounds__(kThreads, R == 64 ? 2 : 3)
+quantize_kernel(const __grid_constant__ CUtensorMap tmX, const QParams p) {
+    constexpr int NT = R / 8;                       // n8 tiles of U
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -196,11 +449,17 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const __grid_constan
     const Layout lay = make_layout(p.max_nb, R);
     const uint32_t bar_full = base + lay.off_bar;
     const uint32_t bar_const = bar_full + 8u * static_cast<uint32_t>(p.max_nb);
-    const float* s_invs = reinterpret_cast<const float*>(base_ptr + lay.off_invs);
-    const int16_t* s_opos = reinterpret_cast<const int16_t*>(base_ptr + lay.off_opos);
+    const uint32_t s_invs = base + lay.off_invs;
+    const uint32_t* s_omega = reinterpret_cast<const uint32_t*>(base_ptr + lay.off_omega);
     float* s_amax = reinterpret_cast<float*>(base_ptr + lay.off_amax);
+    float* s_rmax = reinterpret_cast<float*>(base_ptr + lay.off_rmax);
     float* s_u = reinterpret_cast<float*>(base_ptr + lay.off_u);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + lay.off_abort);
+    auto upart = [&](int w) -> uint32_t {
+        return static_cast<uint32_t>(NT) * 512u > kBoxBytes
+                   ? base + lay.off_upart + static_cast<uint32_t>(w) * static_cast<uint32_t>(NT) * 512u
+                   : base + static_cast<uint32_t>(w) * kSlotBytes;
+    };
 
     griddep_launch_dependents();          // the GEMM may start streaming its weights now
 
@@ -210,7 +469,6 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const __grid_constan
     const int tile = clustered ? static_cast<int>(blockIdx.x) / p.csplit : static_cast<int>(blockIdx.x);
     const int kb_lo = static_cast<int>(rank) * p.nblk / p.csplit;
     const int nb = (static_cast<int>(rank) + 1) * p.nblk / p.csplit - kb_lo;
-    const int K = p.K;
 
     if (threadIdx.x == 0) {
         WQ_QTRACE_AT(0);
@@ -227,16 +485,16 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const __grid_constan
         if (lane == 0) {
             tma_prefetch_desc(&tmX);
             griddep_wait();                // x and this grid's outputs belong to the previous grid
-            // this CTA's slices of inv_s and of the Omega slot table
-            const uint32_t cbytes = (p.inv_s ? 256u * nb : 0u) + (p.n_out ? 128u * nb : 0u);
-            mbar_arrive_expect_tx(bar_const, cbytes);
-            if (p.inv_s) bulk_load(base + lay.off_invs, p.inv_s + kb_lo * 64, 256u * nb, bar_const);
-            if (p.n_out) bulk_load(base + lay.off_opos, p.omega_pos + kb_lo * 64, 128u * nb, bar_const);
             for (int i = 0; i < nb; ++i) {
                 const uint32_t fb = bar_full + 8u * i;
-                mbar_arrive_expect_tx(fb, kBlockBytes);
+                mbar_arrive_expect_tx(fb, kBoxBytes);
                 tma_load_2d(base + static_cast<uint32_t>(i) * kSlotBytes, &tmX, (kb_lo + i) * 64, tile * kRows, fb);
             }
+            // this CTA's slices of inv_s and of the Omega table
+            const uint32_t cbytes = (p.inv_s ? 256u * nb : 0u) + (p.n_out ? 16u * nb : 0u);
+            mbar_arrive_expect_tx(bar_const, cbytes);
+            if (p.inv_s) bulk_load(s_invs, p.inv_s + kb_lo * 64, 256u * nb, bar_const);
+            if (p.n_out) bulk_load(base + lay.off_omega, p.omega_blk + kb_lo * 4, 16u * nb, bar_const);
             WQ_QTRACE_AT(1);
             // every copy has landed before this CTA can finish
             for (int i = 0; i < nb; ++i) mbar_wait(bar_full + 8u * i, 0, abort_flag, p.err, 11);
@@ -252,252 +510,347 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const __grid_constan
     }
 
     // ---------------------------------------------------------------- consumers (warps 0-7)
-    const int rloc = warp * 4 + (lane >> 3);            // row of the tile
-    const int c = lane & 7;                              // chunk of the block
-    const int row = tile * kRows + rloc;
+    const int r = lane & 15, half = lane >> 4;
+    const int row = tile * kRows + r;
     const bool row_ok = row < p.M;
-    const uint32_t my_off = static_cast<uint32_t>(rloc) * 128u + ((static_cast<uint32_t>(c) ^ (rloc & 7u)) << 4);
+    const int active = nb < kConsumerWarps ? nb : kConsumerWarps;   // warps that own blocks
+    // waits are made warp-uniform so every shuffle below has all 32 lanes
+    bool ok = __all_sync(kFullMask, mbar_wait(bar_const, 0, abort_flag, p.err, 14));
 
-    // pass 1: row amax and the low-rank projection
+    // ---- pass 1
     float amax = 0.0f;
-    float uacc[NTW][4];
+    for (int i = warp; i < nb; i += kConsumerWarps) prefetch_block_consts<NT>(p, kb_lo + i, lane);
+    for (int i = warp; ok && i < nb; i += kConsumerWarps) {
+        if (!__all_sync(kFullMask, mbar_wait(bar_full + 8u * i, 0, abort_flag, p.err, 12))) { ok = false; break; }
+        if (threadIdx.x == 0) WQ_QTRACE_AT(2);
+        const uint32_t slot = base + static_cast<uint32_t>(i) * kSlotBytes;
+        f2 P[16];
+        load_transform(slot, r, half, p.inv_s ? s_invs + static_cast<uint32_t>(i) * 256u : 0u, p.rotate, P);
+        const uint32_t rowb = slot + kF32Off + static_cast<uint32_t>(r) * kRowBytes + 128u * half;
 #pragma unroll
-    for (int j = 0; j < NTW; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) uacc[j][e] = 0.0f;
-    const int mt = warp & 1;                             // 16-row half of the tile for mma
-    bool ok = mbar_wait(bar_const, 0, abort_flag, p.err, 14);
-    // low-rank B fragments, prefetched one block ahead
-    uint4 bq[NTW][2];
-    auto load_bq = [&](int kb) {
-        if constexpr (R > 0) {
-#pragma unroll
-            for (int j = 0; j < NTW; ++j) {
-                const int nt = (warp >> 1) + 4 * j;
-                if (nt < NT) {
-                    const uint4* pb = reinterpret_cast<const uint4*>(
-                        p.pfrag + (static_cast<size_t>(kb * NT + nt) * 32 + lane) * 8);
-                    bq[j][0] = __ldg(pb);
-                    bq[j][1] = __ldg(pb + 1);
-                }
+        for (int j = 0; j < 8; ++j)
+            st_shared_v4f(rowb + 16u * j, lo2(P[2 * j]), hi2(P[2 * j]), lo2(P[2 * j + 1]), hi2(P[2 * j + 1]));
+        const uint32_t m0 = p.n_out ? s_omega[4 * i] : 0u, m1 = p.n_out ? s_omega[4 * i + 1] : 0u;
+        const uint32_t mine = half ? m1 : m0;
+        if (mine != 0u) {
+            // kept channels: fp16 value out and +0 in the slot (channel e of the half is float
+            // 2 (e % 16) + e / 16 of the stored row-half), +0 in the registers
+            uint32_t idx = s_omega[4 * i + 2] + (half ? static_cast<uint32_t>(__popc(m0)) : 0u);
+            uint16_t* xrow = p.xo + static_cast<size_t>(row) * p.n_out;
+            for (uint32_t m = mine; m != 0u; m &= m - 1u, ++idx) {
+                const uint32_t e = static_cast<uint32_t>(__ffs(m) - 1);
+                const uint32_t a = rowb + 4u * (2u * (e & 15u) + (e >> 4));
+                if (row_ok) xrow[idx] = __half_as_ushort(__float2half_rn(ld_shared_f32(a)));
+                st_shared_f32(a, 0.0f);
             }
+            apply_keep(P, mine);
         }
-    };
-    load_bq(kb_lo);
-    for (int i = 0; ok && i < nb; ++i) {
-        if (!mbar_wait(bar_full + 8u * i, 0, abort_flag, p.err, 12)) { ok = false; break; }
-        if (i == 0 && threadIdx.x == 0) WQ_QTRACE_AT(2);
-        const uint32_t blk = base + static_cast<uint32_t>(i) * kSlotBytes;
-        const int kb = kb_lo + i;
-        if constexpr (R > 0) {
-            uint4 bcur[NTW][2];
-#pragma unroll
-            for (int j = 0; j < NTW; ++j) {
-                bcur[j][0] = bq[j][0];
-                bcur[j][1] = bq[j][1];
-            }
-            if (i + 1 < nb) load_bq(kb + 1);
-            // each 64-column block is accumulated on the tensor cores from zero and then added
-            // to the running sum with an fp32 add, so the tensor-core accumulation depth stays
-            // at 64 products whatever K is
-            float blk_acc[NTW][4];
-#pragma unroll
-            for (int j = 0; j < NTW; ++j)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) blk_acc[j][e] = 0.0f;
-            const uint32_t arow = static_cast<uint32_t>(16 * mt + (lane & 7) + 8 * ((lane >> 3) & 1));
-#pragma unroll
-            for (int f = 0; f < 4; ++f) {
-                const uint32_t chunk = static_cast<uint32_t>(2 * f + (lane >> 4));
-                uint32_t a0, a1, a2, a3;
-                ldmatrix_x4(blk + arow * 128u + ((chunk ^ (arow & 7u)) << 4), a0, a1, a2, a3);
-#pragma unroll
-                for (int j = 0; j < NTW; ++j) {
-                    const int nt = (warp >> 1) + 4 * j;
-                    if (nt < NT) {
-                        const uint4& q = bcur[j][f >> 1];
-                        const uint32_t b0 = (f & 1) ? q.z : q.x;
-                        const uint32_t b1 = (f & 1) ? q.w : q.y;
-                        mma_bf16_16816(blk_acc[j], a0, a1, a2, a3, b0, b1);
-                    }
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < NTW; ++j)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) uacc[j][e] = __fadd_rn(uacc[j][e], blk_acc[j][e]);
-        }
-        const uint4 raw = ld_shared_v4(blk + my_off);
-        // every warp has read the slot's bf16 rows before any warp writes fp32 rows over them
-        // (fp32 row r spans the bytes of bf16 rows 2.25 r .. 2.25 r + 2, owned by other warps)
-        named_bar_sync(1, kConsumerWarps * 32);
-        float v[8];
-        transform_low(raw, s_invs + i * 64 + c * 8, p, v);
-        const uint32_t rowb = blk + static_cast<uint32_t>(rloc) * (kRowWords * 4u);
-        if (p.rotate) {
-            // transpose through the slot: write channels 8c..8c+7, read c, c+8, ..., c+56
-            st_shared_v4f(rowb + c * 32u, v[0], v[1], v[2], v[3]);
-            st_shared_v4f(rowb + c * 32u + 16u, v[4], v[5], v[6], v[7]);
-            __syncwarp();
-            float w[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) w[j] = ld_shared_f32(rowb + (c + 8u * j) * 4u);
-            transform_high(w);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) st_shared_f32(rowb + (c + 8u * j) * 4u, w[j]);
-            if (p.n_out == 0) {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(w[j]));
+        float ma, mb;
+        absmax_pairs(P, ma, mb);
+        st_shared_v2f(slot + kMaxOff + static_cast<uint32_t>(r) * 16u + 8u * half, ma, mb);
+        amax = fmaxf(amax, fmaxf(ma, mb));
+        if constexpr (R > 0) u_step<NT>(slot, lane, kb_lo + i, p.pfrag, upart(warp), i == warp);
+    }
+
+    // ---- row amax and U over the CTA's warps (in warp order), then over the cluster
+    if (threadIdx.x == 0) WQ_QTRACE_AT(3);
+    amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 16));
+    if (half == 0) s_amax[warp * kRows + r] = amax;
+    named_bar_sync(1, kConsumerWarps * 32);
+    amax = 0.0f;
+    for (int w = 0; w < active; ++w) amax = fmaxf(amax, s_amax[w * kRows + r]);
+    if constexpr (R > 0) {
+        for (int idx = threadIdx.x; idx < NT * 128; idx += kConsumerWarps * 32) {
+            float sum = 0.0f;
+            for (int w = 0; w < active; ++w) sum = __fadd_rn(sum, ld_shared_f32(upart(w) + 4u * idx));
+            int rr, cc;
+            frag_pos(idx, rr, cc);
+            if (clustered) {
+                s_u[rr * R + cc] = sum;
             } else {
-                __syncwarp();
-                ld_shared_v8f(rowb + c * 32u, v);
+                const int rg = tile * kRows + rr;
+                if (rg < p.M) p.u[static_cast<size_t>(rg) * R + cc] = __bfloat16_as_ushort(__float2bfloat16_rn(sum));
             }
-        } else {
-            st_shared_v4f(rowb + c * 32u, v[0], v[1], v[2], v[3]);
-            st_shared_v4f(rowb + c * 32u + 16u, v[4], v[5], v[6], v[7]);
-        }
-        if (!p.rotate || p.n_out > 0) {
-            if (p.n_out > 0) split_outliers(v, s_opos + i * 64 + c * 8, row, false, p);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(v[e]));
         }
     }
-    __syncwarp();
-    amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 2));
-    amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 4));
-    if (threadIdx.x == 0) WQ_QTRACE_AT(3);
-
-    const int gq = lane >> 2, cq = lane & 3;             // mma fragment row / column pair
     if (clustered) {
-        if (c == 0) s_amax[rloc] = amax;
-        if constexpr (R > 0) {
-#pragma unroll
-            for (int j = 0; j < NTW; ++j) {
-                const int nt = (warp >> 1) + 4 * j;
-                if (nt < NT) {
-                    const int col = 8 * nt + 2 * cq;
-                    s_u[(16 * mt + gq) * R + col] = uacc[j][0];
-                    s_u[(16 * mt + gq) * R + col + 1] = uacc[j][1];
-                    s_u[(16 * mt + gq + 8) * R + col] = uacc[j][2];
-                    s_u[(16 * mt + gq + 8) * R + col + 1] = uacc[j][3];
-                }
-            }
-        }
+        if (warp == 0 && half == 0) s_rmax[r] = amax;
         cluster_arrive();
         cluster_wait();
+        // all peers' values are requested before any is used, so the remote reads overlap
+        float pv[16];
+        const uint32_t la = smem_u32(s_rmax + r);
+#pragma unroll
+        for (int qr = 0; qr < 16; ++qr)
+            if (qr < p.csplit) pv[qr] = ld_dsmem_f32(mapa_shared(la, static_cast<uint32_t>(qr)));
         float a = 0.0f;
-        const uint32_t la = smem_u32(s_amax + rloc);
-        for (int qr = 0; qr < p.csplit; ++qr) a = fmaxf(a, ld_dsmem_f32(mapa_shared(la, static_cast<uint32_t>(qr))));
+#pragma unroll
+        for (int qr = 0; qr < 16; ++qr)
+            if (qr < p.csplit) a = fmaxf(a, pv[qr]);
         amax = a;
         if constexpr (R > 0) {
-            // every rank reduces an interleaved share of the tile's U entries
-            {
-                for (int idx = threadIdx.x * p.csplit + static_cast<int>(rank); idx < kRows * R;
-                     idx += kConsumerWarps * 32 * p.csplit) {
-                    const int rr = idx / R, cc = idx % R;
-                    const uint32_t la2 = smem_u32(s_u + idx);
-                    float sum = 0.0f;
-                    for (int qr = 0; qr < p.csplit; ++qr) sum += ld_dsmem_f32(mapa_shared(la2, static_cast<uint32_t>(qr)));
-                    const int rg = tile * kRows + rr;
-                    if (rg < p.M) p.u[static_cast<size_t>(rg) * R + cc] = __bfloat16_as_ushort(__float2bfloat16_rn(sum));
-                }
-            }
-        }
-    } else if constexpr (R > 0) {
+            // every rank reduces an interleaved share of the tile's U entries, in rank order
+            for (int idx = threadIdx.x * p.csplit + static_cast<int>(rank); idx < kRows * R;
+                 idx += kConsumerWarps * 32 * p.csplit) {
+                const uint32_t la2 = smem_u32(s_u + idx);
 #pragma unroll
-        for (int j = 0; j < NTW; ++j) {
-            const int nt = (warp >> 1) + 4 * j;
-            if (nt < NT) {
-                const int col = 8 * nt + 2 * cq;
-                const int r0 = tile * kRows + 16 * mt + gq, r1 = r0 + 8;
-                if (r0 < p.M)
-                    *reinterpret_cast<__nv_bfloat162*>(p.u + static_cast<size_t>(r0) * R + col) =
-                        __floats2bfloat162_rn(uacc[j][0], uacc[j][1]);
-                if (r1 < p.M)
-                    *reinterpret_cast<__nv_bfloat162*>(p.u + static_cast<size_t>(r1) * R + col) =
-                        __floats2bfloat162_rn(uacc[j][2], uacc[j][3]);
+                for (int qr = 0; qr < 16; ++qr)
+                    if (qr < p.csplit) pv[qr] = ld_dsmem_f32(mapa_shared(la2, static_cast<uint32_t>(qr)));
+                float sum = 0.0f;
+#pragma unroll
+                for (int qr = 0; qr < 16; ++qr)
+                    if (qr < p.csplit) sum += pv[qr];
+                const int rg = tile * kRows + idx / R;
+                if (rg < p.M) p.u[static_cast<size_t>(rg) * R + idx % R] = __bfloat16_as_ushort(__float2bfloat16_rn(sum));
             }
         }
     }
     const float gsc = __fdiv_rn(amax, kInt8 ? 127.0f : 2688.0f);
+    const float rg_inv = __frcp_rn(gsc);
+    if (rank == 0 && warp == 0 && half == 0 && row_ok) p.g[row] = gsc;
     if (threadIdx.x == 0) WQ_QTRACE_AT(4);
-    if (rank == 0 && c == 0 && row_ok) p.g[row] = gsc;
 
-    // pass 2: codes, scales and the kept channels, from the resident blocks
-    for (int i = 0; ok && i < nb; ++i) {
-        const uint32_t blk = base + static_cast<uint32_t>(i) * kSlotBytes;
-        const int kb = kb_lo + i;
-        float v[8];
-        ld_shared_v8f(blk + static_cast<uint32_t>(rloc) * (kRowWords * 4u) + c * 32u, v);
-        if (p.n_out > 0) split_outliers(v, s_opos + i * 64 + c * 8, row, row_ok, p);
-        if constexpr (kInt8) {
-            uint32_t pk[4];
+    // ---- pass 2: codes and scales from the resident transformed rows
+    for (int i = warp; ok && i < nb; i += kConsumerWarps) {
+        const uint32_t slot = base + static_cast<uint32_t>(i) * kSlotBytes;
+        const uint32_t rowb = slot + kF32Off + static_cast<uint32_t>(r) * kRowBytes + 128u * half;
+        f2 P[16];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float t[2];
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const float r = gsc != 0.0f ? rintf(__fdiv_rn(v[2 * q + e], gsc)) : 0.0f;
-                    t[e] = fminf(fmaxf(r, -127.0f), 127.0f);
-                }
-                const __nv_bfloat162 h = __floats2bfloat162_rn(t[0], t[1]);
-                pk[q] = *reinterpret_cast<const uint32_t*>(&h);
-            }
-            if (row_ok)
-                *reinterpret_cast<uint4*>(p.codes + (static_cast<size_t>(row) * K + kb * 64 + c * 8) * 2) =
-                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            continue;
+        for (int j = 0; j < 8; ++j) {
+            const float4 t = ld_shared_v4f(rowb + 16u * j);
+            P[2 * j] = pk2(t.x, t.y);
+            P[2 * j + 1] = pk2(t.z, t.w);
         }
-        float cm = 0.0f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) cm = fmaxf(cm, fabsf(v[e]));
-        const float bm = fmaxf(cm, __shfl_xor_sync(kFullMask, cm, 1));
-        uint32_t sc = 0;
-        if (gsc != 0.0f) sc = cvt_e4m3(__fdiv_rn(__fdiv_rn(bm, 6.0f), gsc));
-        const float d = __fmul_rn(dec_e4m3(sc), gsc);
-        const uint32_t word = d != 0.0f ? e2m1_codes8(v, d) : 0u;
-        if (row_ok) *reinterpret_cast<uint32_t*>(p.codes + static_cast<size_t>(row) * (K / 2) + kb * 32 + 4 * c) = word;
-        const uint32_t s1 = __shfl_down_sync(kFullMask, sc, 2);
-        const uint32_t s2 = __shfl_down_sync(kFullMask, sc, 4);
-        const uint32_t s3 = __shfl_down_sync(kFullMask, sc, 6);
-        if (row_ok && c == 0) {
-            const uint32_t w4 = sc | (s1 << 8) | (s2 << 16) | (s3 << 24);
-            size_t off;
-            if (p.sf_layout == WQ_SCALE_LAYOUT_MMA)
-                off = (static_cast<size_t>(row / kBlockM) * (K / 64) + kb) * kSfAtom + (row % 32) * 16 +
-                      ((row % kBlockM) / 32) * 4;
-            else
-                off = static_cast<size_t>(row) * (K / 16) + kb * 4;
-            *reinterpret_cast<uint32_t*>(p.sf + off) = w4;
+        if constexpr (kInt8) {
+            emit_int8(P, gsc, rg_inv, row, row_ok, kb_lo + i, half, p);
+        } else {
+            const float2 bm = ld_shared_v2f(slot + kMaxOff + static_cast<uint32_t>(r) * 16u + 8u * half);
+            emit_nvfp4(P, bm.x, bm.y, gsc, rg_inv, row, row_ok, kb_lo + i, half, p);
         }
     }
     if (threadIdx.x == 0) WQ_QTRACE_AT(5);
     if (clustered) {
-        cluster_arrive();                 // peers are done reading this CTA's s_amax / s_u
+        cluster_arrive();                 // peers are done reading this CTA's s_rmax / s_u
         cluster_wait();
     }
     if (threadIdx.x == 0) WQ_QTRACE_AT(6);
+}
+
+// ==================================================================== stream schedule
+struct SLayout {
+    uint32_t off_invs, off_omega, off_amax, off_upart, off_bar, off_abort, total;
+};
+
+__host__ __device__ inline SLayout make_stream_layout(int K, int r) {
+    SLayout l{};
+    const uint32_t nblk = static_cast<uint32_t>(K / 64);
+    l.off_invs = kRing * kBoxBytes;                 // ring of raw boxes
+    l.off_omega = l.off_invs + 256u * nblk;         // all of inv_s
+    l.off_amax = l.off_omega + 16u * nblk;          // the Omega table
+    l.off_upart = l.off_amax + 4u * kRows * kConsumerWarps;
+    l.off_bar = l.off_upart + kConsumerWarps * static_cast<uint32_t>(r / 8) * 512u;
+    l.off_abort = l.off_bar + 8u * (2 * kRing + 1);
+    l.total = l.off_abort + 16u + 1024u;
+    return l;
+}
+
+template <int R, bool kInt8>
+__global__ void __launch_bounds__(kThreads, R == 64 ? 2 : WQ_QUANT_MINB)
+quantize_stream_kernel(const __grid_constant__ CUtensorMap tmX, const QParams p) {
+    constexpr int NT = R / 8;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    const uint32_t base = (raw_addr + 1023u) & ~1023u;
+    uint8_t* base_ptr = smem_raw + (base - raw_addr);
+    const SLayout lay = make_stream_layout(p.K, R);
+    const uint32_t bar_full = base + lay.off_bar;
+    const uint32_t bar_empty = bar_full + 8u * kRing;
+    const uint32_t bar_const = bar_empty + 8u * kRing;
+    const uint32_t s_invs = base + lay.off_invs;
+    const uint32_t* s_omega = reinterpret_cast<const uint32_t*>(base_ptr + lay.off_omega);
+    float* s_amax = reinterpret_cast<float*>(base_ptr + lay.off_amax);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + lay.off_abort);
+    const int nblk = p.nblk;
+
+    griddep_launch_dependents();
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kRing; ++i) {
+            mbar_init(bar_full + 8u * i, 1);
+            mbar_init(bar_empty + 8u * i, 1);
+        }
+        mbar_init(bar_const, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------------ producer: every block
+        // of each of this CTA's row tiles, twice, in the order the consumer warps take them
+        if (lane == 0) {
+            tma_prefetch_desc(&tmX);
+            griddep_wait();
+            const uint32_t cbytes = (p.inv_s ? 256u * nblk : 0u) + (p.n_out ? 16u * nblk : 0u);
+            mbar_arrive_expect_tx(bar_const, cbytes);
+            if (p.inv_s) bulk_load(s_invs, p.inv_s, 256u * nblk, bar_const);
+            if (p.n_out) bulk_load(base + lay.off_omega, p.omega_blk, 16u * nblk, bar_const);
+            uint32_t q = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < p.row_tiles; tile += gridDim.x)
+                for (int pass = 0; ok && pass < 2; ++pass)
+                    for (int kb = 0; kb < nblk; ++kb, ++q) {
+                        const uint32_t s = q % kRing;
+                        if (q >= kRing && !mbar_wait(bar_empty + 8u * s, ((q / kRing) - 1u) & 1u, abort_flag, p.err, 21)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(bar_full + 8u * s, kBoxBytes);
+                        tma_load_2d(base + s * kBoxBytes, &tmX, kb * 64, tile * kRows, bar_full + 8u * s);
+                    }
+            // every copy has landed before this CTA can finish
+            for (uint32_t t = q > kRing ? q - kRing : 0u; t < q; ++t)
+                mbar_wait(bar_full + 8u * (t % kRing), (t / kRing) & 1u, abort_flag, p.err, 22);
+            mbar_wait(bar_const, 0, abort_flag, p.err, 23);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers (warps 0-7)
+    const int r = lane & 15, half = lane >> 4;
+    const int active = nblk < kConsumerWarps ? nblk : kConsumerWarps;
+    const uint32_t upart = base + lay.off_upart + static_cast<uint32_t>(warp * NT) * 512u;
+    bool ok = __all_sync(kFullMask, mbar_wait(bar_const, 0, abort_flag, p.err, 24));
+    uint32_t q0 = 0;                                   // ring sequence number of the tile's first block
+    QPH_DECL;
+    // every warp runs every tile's barriers, also after a failed wait (ok == false skips work)
+    for (int tile = blockIdx.x; tile < p.row_tiles; tile += gridDim.x) {
+        const int row = tile * kRows + r;
+        const bool row_ok = row < p.M;
+        uint16_t* xrow = p.xo + static_cast<size_t>(row) * p.n_out;
+        // ---- pass 1
+        float amax = 0.0f;
+        if (tile == static_cast<int>(blockIdx.x)) prefetch_block_consts<NT>(p, warp, lane);
+        for (int kb = warp; ok && kb < nblk; kb += kConsumerWarps) {
+            const uint32_t q = q0 + static_cast<uint32_t>(kb), s = q % kRing;
+            prefetch_block_consts<NT>(p, kb + kConsumerWarps < nblk ? kb + kConsumerWarps : warp, lane);
+            QPH(3);
+            if (!__all_sync(kFullMask, mbar_wait(bar_full + 8u * s, (q / kRing) & 1u, abort_flag, p.err, 25))) {
+                ok = false;
+                break;
+            }
+            QPH(0);
+            const uint32_t box = base + s * kBoxBytes;
+            f2 P[16];
+            load_transform(box, r, half, p.inv_s ? s_invs + static_cast<uint32_t>(kb) * 256u : 0u, p.rotate, P);
+            QPH(1);
+            if constexpr (R > 0) u_step<NT>(box, lane, kb, p.pfrag, upart, kb == warp);
+            QPH(2);
+            const uint32_t m0 = p.n_out ? s_omega[4 * kb] : 0u, m1 = p.n_out ? s_omega[4 * kb + 1] : 0u;
+            if ((m0 | m1) != 0u) {
+                // kept channels: fp16 values out through a copy in the consumed box (lane l
+                // writes its 32 channels as fp16 pairs at l * 64 B), +0 in the registers
+                __syncwarp();                  // every lane is done reading the box
+                const uint32_t sc = box + static_cast<uint32_t>(lane) * 64u;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t hw[4];
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const __half2 h2 = __floats2half2_rn(lo2(P[4 * j + t]), hi2(P[4 * j + t]));
+                        hw[t] = *reinterpret_cast<const uint32_t*>(&h2);
+                    }
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(sc + 16u * j), "r"(hw[0]), "r"(hw[1]),
+                                 "r"(hw[2]), "r"(hw[3]) : "memory");
+                }
+                const uint32_t mine = half ? m1 : m0;
+                uint32_t idx = s_omega[4 * kb + 2] + (half ? static_cast<uint32_t>(__popc(m0)) : 0u);
+                for (uint32_t m = mine; m != 0u; m &= m - 1u, ++idx) {
+                    const uint32_t e = static_cast<uint32_t>(__ffs(m) - 1);
+                    uint16_t hv;
+                    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(hv) : "r"(sc + 4u * (e & 15u) + 2u * (e >> 4)) : "memory");
+                    if (row_ok) xrow[idx] = hv;
+                }
+                if (mine != 0u) apply_keep(P, mine);
+            }
+            float ma, mb;
+            absmax_pairs(P, ma, mb);
+            amax = fmaxf(amax, fmaxf(ma, mb));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_empty + 8u * s);
+        }
+        QPH(3);
+        // ---- row amax and U over the warps, in warp order
+        amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 16));
+        if (half == 0) s_amax[warp * kRows + r] = amax;
+        named_bar_sync(1, kConsumerWarps * 32);
+        amax = 0.0f;
+        for (int w = 0; w < active; ++w) amax = fmaxf(amax, s_amax[w * kRows + r]);
+        if constexpr (R > 0) {
+            for (int idx = threadIdx.x; idx < NT * 128; idx += kConsumerWarps * 32) {
+                float sum = 0.0f;
+                for (int w = 0; w < active; ++w)
+                    sum = __fadd_rn(sum, ld_shared_f32(base + lay.off_upart + static_cast<uint32_t>(w * NT) * 512u + 4u * idx));
+                int rr, cc;
+                frag_pos(idx, rr, cc);
+                const int rg = tile * kRows + rr;
+                if (rg < p.M) p.u[static_cast<size_t>(rg) * R + cc] = __bfloat16_as_ushort(__float2bfloat16_rn(sum));
+            }
+        }
+        named_bar_sync(1, kConsumerWarps * 32);        // maxima and partials are free again
+        const float gsc = __fdiv_rn(amax, kInt8 ? 127.0f : 2688.0f);
+        const float rg_inv = __frcp_rn(gsc);
+        if (warp == 0 && half == 0 && row_ok) p.g[row] = gsc;
+        q0 += static_cast<uint32_t>(nblk);
+        QPH(4);
+        // ---- pass 2: the blocks again (from L2), transform recomputed
+        for (int kb = warp; ok && kb < nblk; kb += kConsumerWarps) {
+            const uint32_t q = q0 + static_cast<uint32_t>(kb), s = q % kRing;
+            QPH(7);
+            if (!__all_sync(kFullMask, mbar_wait(bar_full + 8u * s, (q / kRing) & 1u, abort_flag, p.err, 26))) {
+                ok = false;
+                break;
+            }
+            QPH(5);
+            f2 P[16];
+            load_transform(base + s * kBoxBytes, r, half, p.inv_s ? s_invs + static_cast<uint32_t>(kb) * 256u : 0u,
+                           p.rotate, P);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_empty + 8u * s);
+            QPH(6);
+            const uint32_t m0 = p.n_out ? s_omega[4 * kb] : 0u, m1 = p.n_out ? s_omega[4 * kb + 1] : 0u;
+            if ((half ? m1 : m0) != 0u) apply_keep(P, half ? m1 : m0);
+            if constexpr (kInt8) {
+                emit_int8(P, gsc, rg_inv, row, row_ok, kb, half, p);
+            } else {
+                float ma, mb;
+                absmax_pairs(P, ma, mb);
+                emit_nvfp4(P, ma, mb, gsc, rg_inv, row, row_ok, kb, half, p);
+            }
+        }
+        q0 += static_cast<uint32_t>(nblk);
+        QPH(7);
+    }
+    QPH_FLUSH;
 }
 
 struct Choice {
     int csplit, max_nb;
 };
 
-Choice choose(int M, int K, int num_sms) {
+// Cluster schedule: at most one 64-block per consumer warp where the cluster size allows (at
+// most 16 CTAs per row tile); K = 16384 gives 16 blocks per CTA.
+Choice choose(int K) {
     const int nblk = K / 64;
-    const int row_tiles = (M + kRows - 1) / kRows;
-    int cs = 1;
-    while (cs < 16 && (nblk + cs - 1) / cs > kTargetBlocks) cs <<= 1;
-    // small batches: spread a row tile's K range over more CTAs
-    while (cs < 16 && row_tiles * cs * 2 <= num_sms && nblk >= 2 * cs) cs <<= 1;
-    if (cs > nblk) cs = nblk;
+    int cs = (nblk + kConsumerWarps - 1) / kConsumerWarps;
+    if (cs > 16) cs = 16;
+    if (cs < 1) cs = 1;
     return Choice{cs, (nblk + cs - 1) / cs};
 }
 
 template <int R, bool kInt8>
-cudaError_t launch_r(const CUtensorMap& tm, const QParams& qp, cudaStream_t st) {
-    const Layout lay = make_layout(qp.max_nb, R);
+cudaError_t launch_r(const CUtensorMap& tm, const QParams& qp, bool stream, int num_sms, cudaStream_t st) {
     static bool attr_set = false;
     if (!attr_set) {
         const Layout worst = make_layout(kMaxBlocks, R);
@@ -506,18 +859,46 @@ cudaError_t launch_r(const CUtensorMap& tm, const QParams& qp, cudaStream_t st) 
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(quantize_kernel<R, kInt8>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
+        const SLayout sworst = make_stream_layout(16384, R);
+        e = cudaFuncSetAttribute(quantize_stream_kernel<R, kInt8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(sworst.total));
+        if (e != cudaSuccess) return e;
         attr_set = true;
     }
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(static_cast<unsigned>(qp.row_tiles * qp.csplit));
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = lay.total;
     cfg.stream = st;
     cudaLaunchAttribute at[2];
     int na = 0;
     at[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     at[na].val.programmaticStreamSerializationAllowed = 1;
     ++na;
+    if (stream) {
+        const SLayout lay = make_stream_layout(qp.K, R);
+        int per_sm = 0;
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quantize_stream_kernel<R, kInt8>, kThreads,
+                                                                      lay.total);
+        if (e != cudaSuccess) return e;
+        if (per_sm < 1) return cudaErrorInvalidConfiguration;
+        // a row tile is re-read from L2 by its second pass: keep the tiles in flight well
+        // inside the L2 (16 rows x K bf16 each)
+        const long long tile_bytes = 32ll * qp.K;
+        while (per_sm > 1 && static_cast<long long>(per_sm) * num_sms * tile_bytes > (96ll << 20)) --per_sm;
+        // WQ_QUANT_CTAS_PER_SM=<n> overrides the residency (tuning)
+        if (const char* fc = std::getenv("WQ_QUANT_CTAS_PER_SM")) {
+            const int v = std::atoi(fc);
+            if (v >= 1 && v <= per_sm + 8) per_sm = v;
+        }
+        const int grid = qp.row_tiles < per_sm * num_sms ? qp.row_tiles : per_sm * num_sms;
+        cfg.gridDim = dim3(static_cast<unsigned>(grid));
+        cfg.dynamicSmemBytes = lay.total;
+        cfg.attrs = at;
+        cfg.numAttrs = na;
+        return cudaLaunchKernelEx(&cfg, quantize_stream_kernel<R, kInt8>, tm, qp);
+    }
+    const Layout lay = make_layout(qp.max_nb, R);
+    cfg.gridDim = dim3(static_cast<unsigned>(qp.row_tiles * qp.csplit));
+    cfg.dynamicSmemBytes = lay.total;
     if (qp.csplit > 1) {
         at[na].id = cudaLaunchAttributeClusterDimension;
         at[na].val.clusterDim.x = static_cast<unsigned>(qp.csplit);
@@ -534,27 +915,34 @@ cudaError_t launch_r(const CUtensorMap& tm, const QParams& qp, cudaStream_t st) 
 
 cudaError_t launch_quantize_act(const QuantArgs& a, cudaStream_t st) {
     if (a.M <= 0) return cudaSuccess;
-    Choice ch = choose(a.M, a.K, a.num_sms);
-    // WQ_QUANT_SPLIT=<n> pins the CTAs per row tile (tuning and tests)
+    Choice ch = choose(a.K);
+    const int row_tiles = (a.M + kRows - 1) / kRows;
+    // many row tiles: the persistent stream schedule; few: spread K over clusters
+    bool stream = row_tiles >= 2 * a.num_sms;
+    // WQ_QUANT_SCHEDULE=stream|cluster and WQ_QUANT_SPLIT=<n> pin the schedule and the CTAs
+    // per row tile of the cluster schedule (tuning and tests)
+    if (const char* fm = std::getenv("WQ_QUANT_SCHEDULE")) {
+        if (fm[0] == 's') stream = true;
+        if (fm[0] == 'c') stream = false;
+    }
     if (const char* fs = std::getenv("WQ_QUANT_SPLIT")) {
         const int v = std::atoi(fs);
         const int nblk = a.K / 64;
-        if (v >= 1 && v <= 16 && (v & (v - 1)) == 0 && v <= nblk && (nblk + v - 1) / v <= kMaxBlocks)
-            ch = Choice{v, (nblk + v - 1) / v};
+        if (v >= 1 && v <= 16 && v <= nblk && (nblk + v - 1) / v <= kMaxBlocks) ch = Choice{v, (nblk + v - 1) / v};
     }
     if (ch.max_nb > kMaxBlocks) return cudaErrorInvalidValue;
     QParams qp{};
     qp.M = a.M; qp.K = a.K; qp.nblk = a.K / 64; qp.csplit = ch.csplit; qp.max_nb = ch.max_nb;
-    qp.row_tiles = (a.M + kRows - 1) / kRows;
-    qp.inv_s = a.inv_s; qp.rotate = a.rotate; qp.omega_pos = a.omega_pos; qp.n_out = a.n_out; qp.xo = a.xo;
+    qp.row_tiles = row_tiles;
+    qp.inv_s = a.inv_s; qp.rotate = a.rotate; qp.omega_blk = a.omega_blk; qp.n_out = a.n_out; qp.xo = a.xo;
     qp.pfrag = a.pfrag; qp.u = a.u; qp.codes = a.codes; qp.sf = a.sf; qp.sf_layout = a.sf_layout; qp.g = a.g;
     qp.err = a.err;
-    if (a.int8) return a.r == 0 && a.n_out == 0 ? launch_r<0, true>(*a.tmX, qp, st) : cudaErrorInvalidValue;
+    if (a.int8) return a.r == 0 && a.n_out == 0 ? launch_r<0, true>(*a.tmX, qp, stream, a.num_sms, st) : cudaErrorInvalidValue;
     switch (a.r) {
-        case 0: return launch_r<0, false>(*a.tmX, qp, st);
-        case 16: return launch_r<16, false>(*a.tmX, qp, st);
-        case 32: return launch_r<32, false>(*a.tmX, qp, st);
-        case 64: return launch_r<64, false>(*a.tmX, qp, st);
+        case 0: return launch_r<0, false>(*a.tmX, qp, stream, a.num_sms, st);
+        case 16: return launch_r<16, false>(*a.tmX, qp, stream, a.num_sms, st);
+        case 32: return launch_r<32, false>(*a.tmX, qp, stream, a.num_sms, st);
+        case 64: return launch_r<64, false>(*a.tmX, qp, stream, a.num_sms, st);
         default: return cudaErrorInvalidValue;
     }
 }
