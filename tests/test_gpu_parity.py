@@ -185,6 +185,21 @@ def test_forward_parity(case):
     assert_y_close(L, y, y_ref)
 
 
+@pytest.mark.parametrize("case", list(CASES))
+@pytest.mark.parametrize("wide", ["1", "0"])
+def test_forward_parity_gemm_schedules(case, wide, monkeypatch):
+    """Both GEMM schedules on every case: 256 x 256 tiles on CTA pairs (tcgen05 cta_group::2,
+    single-buffered accumulator, side branch computed into the drained accumulator) and
+    128 x 128 tiles on single CTAs; partial tiles in M and N included."""
+    monkeypatch.setenv("WQ_GEMM_WIDE", wide)
+    L = layer(case)
+    w = prep(L)
+    y = wq.wq_linear_forward(w, x_dev(L.x_bits))
+    wq.wq_check_device_error(w)
+    y_ref, *_ = oracle.reference_forward(L)
+    assert_y_close(L, y, y_ref)
+
+
 @pytest.mark.parametrize("case,split", [("expert_small", 1), ("expert_small", 2), ("expert_small", 4),
                                         ("multi_tile_kstage_tail", 1), ("multi_tile_kstage_tail", 2),
                                         ("multi_tile_kstage_tail", 4), ("dit_r32_o64_ragged_n", 2),

@@ -77,6 +77,18 @@ def test_w8a8_split_k_schedules(split, monkeypatch):
     check_y(L, y, y_ref)
 
 
+@pytest.mark.parametrize("case", list(CASES8))
+def test_w8a8_pair_schedule(case, monkeypatch):
+    """The 8-bit layers on the CTA-pair schedule (256 x 256 tiles, kind::f16 pair MMAs)."""
+    monkeypatch.setenv("WQ_GEMM_WIDE", "1")
+    L = wl.make_layer_inputs("backbone", **CASES8[case])
+    w = prep8(L)
+    y = wq.wq_linear_forward_w8a8(w, x_dev(L.x_bits))
+    wq.wq_check_device_error(w)
+    y_ref, *_ = oracle.reference_forward_w8a8(L)
+    check_y(L, y, y_ref)
+
+
 @pytest.mark.parametrize("layer_idx", [1, 3])
 def test_w8a8_full_size_sampled_rows(layer_idx):
     L = wl.make_layer_inputs("backbone", layer=layer_idx)

@@ -314,9 +314,9 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     }
                 };
                 for (int kt = kt_lo; kt < kt_hi; ++kt) {
+                    // (TMA-filled stages need no tcgen05 fence: the mbarrier completion orders them)
                     if (!mbar_wait(bar_full + 8u * stage, ph, abort_flag, p.err, 5)) { ok = false; break; }
                     if (tl == 0 && kt == kt_lo) WQ_TRACE_AT(4);
-                    tc_fence_after();
                     const int nkb = kW8 ? 4 : min(4, num_kb - kt * 4);
                     const uint32_t sA = base + static_cast<uint32_t>(stage) * kSB;
                     const uint32_t sf_t = tmem + p.sf_col + 32u * stage;
@@ -335,7 +335,6 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     if (++stage == S) { stage = 0; ph ^= 1u; }
                     if (kt + 1 < kt_hi) {
                         if (!mbar_wait(bar_full + 8u * stage, ph, abort_flag, p.err, 5)) { ok = false; break; }
-                        tc_fence_after();
                         copy_scales(stage, kt + 1);
                     }
                 }
@@ -494,11 +493,18 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 const uint32_t c4 = static_cast<uint32_t>(it % 32);
                 const uint32_t off = base + static_cast<uint32_t>(row_t) * 512u +
                                      ((c4 ^ (static_cast<uint32_t>(row_t) & 7u)) << 4);
+                // every peer's partial is requested before any is added, so the remote reads
+                // overlap; the sum is still taken in rank order
+                float4 pv[16];
+#pragma unroll
+                for (int qr = 0; qr < 16; ++qr)
+                    if (qr < p.split) pv[qr] = ld_dsmem_v4(mapa_shared(off, static_cast<uint32_t>(qr)));
                 float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int qr = 0; qr < p.split; ++qr) {
-                    const float4 v = ld_dsmem_v4(mapa_shared(off, static_cast<uint32_t>(qr)));
-                    a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
-                }
+#pragma unroll
+                for (int qr = 0; qr < 16; ++qr)
+                    if (qr < p.split) {
+                        a.x += pv[qr].x; a.y += pv[qr].y; a.z += pv[qr].z; a.w += pv[qr].w;
+                    }
                 const int n0 = nb * 128 + static_cast<int>(c4) * 4;
                 if (n0 < N) {
                     if (p.bias != nullptr) {
@@ -619,6 +625,14 @@ cudaError_t launch_gemm_t(const GemmArgs& a, cudaStream_t st) {
 
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
     if (a.M <= 0) return cudaSuccess;
+    // 128 x 128 tiles on single CTAs (split-K over clusters when the tiles alone cannot fill
+    // the GPU) by default; WQ_GEMM_WIDE=1 selects the CTA-pair schedule with 256 x 256 tiles.
+    // The pair schedule is bit-for-bit tested but not yet faster: its five-stage ring cannot
+    // cover the L2 latency at the pair's data rate, and its single accumulator serialises the
+    // side branch with the main loop.
+    bool wide = false;
+    if (const char* fw = std::getenv("WQ_GEMM_WIDE")) wide = fw[0] == '1' && a.force_split == 0;
+    if (wide) return launch_gemm_wide(a, st);
     return a.w8 ? launch_gemm_t<true>(a, st) : launch_gemm_t<false>(a, st);
 }
 

@@ -1,0 +1,472 @@
+// wq_gemm2.cu -- the block-scaled NVFP4 GEMM on CTA pairs: 256 x 256 output tiles computed by
+// tcgen05.mma.cta_group::2 (M = 256 over the two CTAs of a cluster, N = 256), for batches
+// with enough tiles to fill the GPU.  Same operation and epilogue as wq_gemm.cu:
+//     y = gA[m] gW acc4 + (U Q + x_O W_O) + b        -> bf16
+// (QuantWAMs sec. 4.2 "Backend"; Q-WAM abstract for the 16-bit low-rank branch).
+//
+// Per CTA of a pair (rank c), 10 warps:
+//   warp 0    TMA producer: its 128 rows of the A tile and its 128 of the 256 B rows, its A
+//             scale atoms and all 256 rows' B scale atoms (each CTA's TMEM needs the whole
+//             tile's B scales), into an S-stage ring; after the K stages of a tile, the side
+//             operands (U with this CTA's Q^T rows; x_O with its W_O^T rows) as extra stages.
+//   warp 1    rank 0: TMEM (collective over the pair) and the single MMA-issuing thread:
+//             per stage tcgen05.cp.cta_group::2 of the scales (each CTA copies its own shared
+//             memory into its own TMEM) and the pair MMAs, whose completion frees the stage
+//             in both CTAs (multicast commit).  rank 1: relays "stage full" of its own ring to
+//             rank 0's barrier, since an mbarrier can only be waited on in its own CTA.
+//   warps 2-9 epilogue: two warps per TMEM lane quadrant, 128 columns each.  The 256-column
+//             accumulator fills TMEM's first half (the other half holds five stages of scale
+//             factors), so it is single-buffered: the epilogue drains it into registers and
+//             releases it at once; with a side branch the pair MMAs then compute U Q + x_O W_O
+//             into the same columns, which the epilogue adds chunk by chunk before the bf16
+//             tile leaves through per-warp staging and TMA stores.
+// Every wait is bounded (see ptx.cuh); a CTA that gives up records its error code and the
+// pair still meets at the final cluster barrier before TMEM is released.
+//
+// kW8 = true runs the selective 8-bit layers (int8 values held as bf16) through
+// kind::f16 pair MMAs, 64 K per stage, no scale factors.
+#include <cuda_bf16.h>
+
+#include <cstdlib>
+
+#include "ptx.cuh"
+#include "wq_internal.h"
+
+#ifdef WQ_TRACE
+// Wait-time counters for kernel development builds only (never defined in the product build).
+__device__ unsigned long long g_wq_wtrace[16];
+extern "C" WQ_API int wq_wtrace_read(void* host, size_t bytes) {
+    return static_cast<int>(cudaMemcpyFromSymbol(host, g_wq_wtrace, bytes));
+}
+#define WT_T0(v) const unsigned long long v = wq::global_timer_ns()
+#define WT_ADD(i, t0) atomicAdd(&g_wq_wtrace[i], wq::global_timer_ns() - (t0))
+#else
+#define WT_T0(v) ((void)0)
+#define WT_ADD(i, t0) ((void)0)
+#endif
+
+namespace wq {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kEpiWarps = 8;
+constexpr uint32_t kHalf = 128 * 128;                   // 128 rows x 128 bytes
+constexpr uint32_t kSfaOff = 2 * kHalf;                 // 4 A atoms (this CTA's rows)
+constexpr uint32_t kSfbOff = kSfaOff + 4 * kSfAtom;     // 4 atoms of B rows 0..127, then 4 of 128..255
+constexpr uint32_t kStage4 = kSfbOff + 8 * kSfAtom;     // 38 KiB, a multiple of 1 KiB
+constexpr uint32_t kStage8 = 2 * kHalf;
+constexpr uint32_t kSideB = 16384;                      // offset of the B-side operand in a side stage
+constexpr uint32_t kYWarp = 32 * 128;                   // per-warp staging: 32 rows x 64 bf16
+constexpr uint32_t kYBytes = kEpiWarps * kYWarp;
+constexpr uint32_t kMaxSmem = 232448;
+constexpr uint32_t kSfCol = 256;                        // first scale-factor column
+constexpr uint32_t kSfSlot = 48;                        // columns per stage: 4 x 4 (A) + 4 x 8 (B)
+constexpr int kMaxStages = 5;                           // 256 + 5 x 48 <= 512 TMEM columns
+
+struct WParams {
+    int M, N, K, r, n_out, stages;
+    int num_kb, num_kt;
+    int nrb_a, nrb_b;        // 128-row atom blocks of the activation / weight scales
+    uint32_t off_y, off_bar;
+    const uint8_t* sfa;
+    const uint8_t* sfb;
+    const float* gA;
+    float gW;
+    const float* bias;
+    const float* colscale;
+    int* err;
+};
+
+__host__ __device__ constexpr uint32_t stage_bytes(bool w8) { return w8 ? kStage8 : kStage4; }
+
+__device__ __forceinline__ uint32_t swizzle_mode_for_row_bytes(uint32_t row_bytes) {
+    return row_bytes == 128 ? 2u : (row_bytes == 64 ? 4u : 6u);
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+template <bool kW8>
+__global__ void __launch_bounds__(kThreads, 1)
+wide_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmQ,
+                 const __grid_constant__ CUtensorMap tmXO, const __grid_constant__ CUtensorMap tmWO,
+                 const __grid_constant__ CUtensorMap tmY, const WParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    const uint32_t base = (raw_addr + 1023u) & ~1023u;
+    uint8_t* base_ptr = smem_raw + (base - raw_addr);
+    constexpr uint32_t SB = stage_bytes(kW8);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t rank = cluster_ctarank();
+    const int S = p.stages;
+    const uint32_t bar_full = base + p.off_bar;
+    const uint32_t bar_pfull = bar_full + 8u * S;        // rank 0: the peer's stage is full
+    const uint32_t bar_empty = bar_pfull + 8u * S;
+    const uint32_t bar_tfull = bar_empty + 8u * S;
+    const uint32_t bar_tempty = bar_tfull + 8u;          // rank 0: both epilogues drained the accumulator
+    const uint32_t bar_sfull = bar_tempty + 8u;
+    const uint32_t bar_sempty = bar_sfull + 8u;          // rank 0: both epilogues read the side results
+    const uint32_t bar_final = bar_sempty + 8u;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + p.off_bar + 8u * (3 * S + 5));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+    const int M = p.M, N = p.N;
+    const int nnt = (N + 255) / 256;
+    const int tiles = ((M + 255) / 256) * nnt;
+    const int pair = static_cast<int>(blockIdx.x) / 2, npairs = static_cast<int>(gridDim.x) / 2;
+    const bool has_side = (p.r + p.n_out) > 0;
+    const int side_stages = (p.r > 0 ? 1 : 0) + (p.n_out > 0 ? 1 : 0);
+    const int num_kt = p.num_kt;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(bar_full + 8u * s, 1);
+            mbar_init(bar_pfull + 8u * s, 1);
+            mbar_init(bar_empty + 8u * s, 1);
+        }
+        mbar_init(bar_tfull, 1);
+        mbar_init(bar_tempty, 2 * kEpiWarps);
+        mbar_init(bar_sfull, 1);
+        mbar_init(bar_sempty, 2 * kEpiWarps);
+        mbar_init(bar_final, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmY);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(tmem_holder), 512);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();                 // both CTAs' barriers exist before any remote arrive
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    griddep_launch_dependents();
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer (each CTA)
+        if (lane == 0) {
+            uint32_t q = 0;
+            bool ok = true, dep = false;
+            for (int tile = pair; ok && tile < tiles; tile += npairs) {
+                const int mb = tile / nnt, nb = tile % nnt;
+                const int mrow = mb * 256 + static_cast<int>(rank) * 128, nrow = nb * 256 + static_cast<int>(rank) * 128;
+                const int ra = min(mb * 2 + static_cast<int>(rank), p.nrb_a - 1);
+                const int rb0 = min(nb * 2, p.nrb_b - 1), rb1 = min(nb * 2 + 1, p.nrb_b - 1);
+                for (int kt = 0; kt < num_kt + side_stages; ++kt, ++q) {
+                    const uint32_t s = q % static_cast<uint32_t>(S);
+                    WT_T0(tw0);
+                    if (q >= static_cast<uint32_t>(S) &&
+                        !mbar_wait(bar_empty + 8u * s, ((q / S) - 1u) & 1u, abort_flag, p.err, 31)) {
+                        ok = false;
+                        break;
+                    }
+                    WT_ADD(0, tw0);
+                    const uint32_t sA = base + s * SB, fb = bar_full + 8u * s;
+                    if (kt < num_kt) {
+                        if (kW8) {
+                            mbar_arrive_expect_tx(fb, 2 * kHalf);
+                            tma_load_2d(sA + kHalf, &tmB, kt * 64, nrow, fb);
+                            if (!dep) { griddep_wait(); dep = true; }
+                            tma_load_2d(sA, &tmA, kt * 64, mrow, fb);
+                        } else {
+                            const int kb0 = kt * 4, nkb = min(4, p.num_kb - kb0);
+                            mbar_arrive_expect_tx(fb, 2 * kHalf + 3u * nkb * kSfAtom);
+                            tma_load_2d(sA + kHalf, &tmB, kt * 128, nrow, fb);
+                            bulk_load(sA + kSfbOff, p.sfb + (static_cast<size_t>(rb0) * p.num_kb + kb0) * kSfAtom,
+                                      nkb * kSfAtom, fb);
+                            bulk_load(sA + kSfbOff + 4 * kSfAtom, p.sfb + (static_cast<size_t>(rb1) * p.num_kb + kb0) * kSfAtom,
+                                      nkb * kSfAtom, fb);
+                            if (!dep) { griddep_wait(); dep = true; }
+                            tma_load_2d(sA, &tmA, kt * 128, mrow, fb);
+                            bulk_load(sA + kSfaOff, p.sfa + (static_cast<size_t>(ra) * p.num_kb + kb0) * kSfAtom,
+                                      nkb * kSfAtom, fb);
+                        }
+                    } else if (kt == num_kt && p.r > 0) {
+                        mbar_arrive_expect_tx(fb, 512u * p.r);
+                        tma_load_2d(sA, &tmU, 0, mrow, fb);
+                        tma_load_2d(sA + kSideB, &tmQ, 0, nrow, fb);
+                    } else {
+                        mbar_arrive_expect_tx(fb, 512u * p.n_out);
+                        tma_load_2d(sA, &tmXO, 0, mrow, fb);
+                        tma_load_2d(sA + kSideB, &tmWO, 0, nrow, fb);
+                    }
+                }
+            }
+            // never leave with copies still landing in shared memory
+            const uint32_t first = q > static_cast<uint32_t>(S) ? q - S : 0u;
+            for (uint32_t t = first; t < q; ++t)
+                mbar_wait(bar_full + 8u * (t % S), (t / S) & 1u, abort_flag, p.err, 32);
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && rank != 0) {
+            // ------------------------------------------------------------ rank 1: relay
+            const uint32_t pfull0 = mapa_shared(bar_pfull, 0);
+            uint32_t q = 0;
+            bool ok = true;
+            for (int tile = pair; ok && tile < tiles; tile += npairs)
+                for (int kt = 0; kt < num_kt + side_stages; ++kt, ++q) {
+                    const uint32_t s = q % static_cast<uint32_t>(S);
+                    WT_T0(tw0);
+                    if (!mbar_wait(bar_full + 8u * s, (q / S) & 1u, abort_flag, p.err, 33)) { ok = false; break; }
+                    WT_ADD(1, tw0);
+                    mbar_arrive_cluster(pfull0 + 8u * s);
+                }
+        } else if (lane == 0) {
+            // ------------------------------------------------------------ rank 0: MMA issuer
+            const uint32_t mn = ((256u >> 3) << 17) | ((256u >> 4) << 24);   // M = 256 (pair), N = 256
+            const uint32_t idesc_fp4 = (1u << 7) | (1u << 10) | mn;
+            const uint32_t idesc_bf16 = (1u << 4) | (1u << 7) | (1u << 10) | mn;
+            const uint32_t idesc_f16 = (1u << 4) | mn;
+            uint32_t q = 0;
+            int tl = 0;
+            bool ok = true;
+            for (int tile = pair; ok && tile < tiles; tile += npairs, ++tl) {
+                WT_T0(tw0);
+                if (tl > 0) {
+                    // the accumulator columns are free once both epilogues have read the last tile
+                    if (!mbar_wait(has_side ? bar_sempty : bar_tempty, static_cast<uint32_t>(tl - 1) & 1u, abort_flag,
+                                   p.err, 34)) { ok = false; break; }
+                }
+                WT_ADD(2, tw0);
+                WT_T0(tmain);
+                tc_fence_after();
+                for (int kt = 0; kt < num_kt; ++kt, ++q) {
+                    const uint32_t s = q % static_cast<uint32_t>(S), ph = (q / S) & 1u;
+                    WT_T0(tw1);
+                    if (!mbar_wait(bar_full + 8u * s, ph, abort_flag, p.err, 35)) { ok = false; break; }
+                    WT_ADD(3, tw1);
+                    WT_T0(tw2);
+                    if (!mbar_wait(bar_pfull + 8u * s, ph, abort_flag, p.err, 36)) { ok = false; break; }
+                    WT_ADD(4, tw2);
+                    // (TMA-filled stages need no tcgen05 fence: the mbarrier completion orders them)
+                    const uint32_t sA = base + s * SB;
+                    const uint64_t ad = smem_desc(sA, 16, 1024, 2), bd = smem_desc(sA + kHalf, 16, 1024, 2);
+                    if (kW8) {
+#pragma unroll
+                        for (int kb = 0; kb < 4; ++kb)
+                            mma_f16_pair(tmem, ad + 2u * kb, bd + 2u * kb, idesc_bf16, (kt | kb) != 0 ? 1u : 0u);
+                    } else {
+                        const int nkb = min(4, p.num_kb - kt * 4);
+                        const uint32_t slot = tmem + kSfCol + kSfSlot * s;
+                        for (int kb = 0; kb < nkb; ++kb) {
+                            tmem_cp_pair_32x128b_x4(slot + 4u * kb, smem_desc(sA + kSfaOff + kSfAtom * kb, 0, 128, 0));
+                            tmem_cp_pair_32x128b_x4(slot + 16u + 8u * kb, smem_desc(sA + kSfbOff + kSfAtom * kb, 0, 128, 0));
+                            tmem_cp_pair_32x128b_x4(slot + 20u + 8u * kb,
+                                                    smem_desc(sA + kSfbOff + 4 * kSfAtom + kSfAtom * kb, 0, 128, 0));
+                        }
+                        for (int kb = 0; kb < nkb; ++kb)
+                            mma_nvf4_pair(tmem, ad + 2u * kb, bd + 2u * kb, idesc_fp4, slot + 4u * kb, slot + 16u + 8u * kb,
+                                          (kt | kb) != 0 ? 1u : 0u);
+                    }
+                    tc_commit_pair_mc(bar_empty + 8u * s, 0x3);
+                }
+                if (!ok) break;
+                tc_commit_pair_mc(bar_tfull, 0x3);
+                WT_ADD(5, tmain);
+                if (has_side) {
+                    WT_T0(tw3);
+                    if (!mbar_wait(bar_tempty, static_cast<uint32_t>(tl) & 1u, abort_flag, p.err, 37)) { ok = false; break; }
+                    WT_ADD(6, tw3);
+                    tc_fence_after();
+                    uint32_t acc = 0;
+                    for (int st = 0; st < side_stages; ++st, ++q) {
+                        const uint32_t s = q % static_cast<uint32_t>(S), ph = (q / S) & 1u;
+                        if (!mbar_wait(bar_full + 8u * s, ph, abort_flag, p.err, 38) ||
+                            !mbar_wait(bar_pfull + 8u * s, ph, abort_flag, p.err, 39)) { ok = false; break; }
+                        const uint32_t sA = base + s * SB;
+                        const bool lowrank = st == 0 && p.r > 0;
+                        const uint32_t rb = 2u * static_cast<uint32_t>(lowrank ? p.r : p.n_out);
+                        const uint32_t sw = swizzle_mode_for_row_bytes(rb);
+                        const uint64_t xd = smem_desc(sA, 16, 8 * rb, sw), wd = smem_desc(sA + kSideB, 16, 8 * rb, sw);
+                        for (uint32_t j = 0; j < rb / 32u; ++j, acc = 1)
+                            mma_f16_pair(tmem, xd + 2u * j, wd + 2u * j, lowrank ? idesc_bf16 : idesc_f16, acc);
+                        tc_commit_pair_mc(bar_empty + 8u * s, 0x3);
+                    }
+                    if (!ok) break;
+                    tc_commit_pair_mc(bar_sfull, 0x3);
+                }
+            }
+            // every MMA this thread issued has completed before TMEM is released
+            tc_commit_pair(bar_final);
+            mbar_wait(bar_final, 0, abort_flag, p.err, 40);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue (warps 2..9)
+        const int qd = warp & 3;                          // TMEM lane quadrant
+        const int hh = (warp - 2) >> 2;                   // column half of the 256-wide tile
+        const uint32_t ystage = base + p.off_y + static_cast<uint32_t>(warp - 2) * kYWarp;
+        const uint32_t t_lane = static_cast<uint32_t>(qd * 32) << 16;
+        const uint32_t tempty0 = mapa_shared(bar_tempty, 0), sempty0 = mapa_shared(bar_sempty, 0);
+        griddep_wait();                                   // gA is written by the previous grid
+        int tl = 0;
+        for (int tile = pair; tile < tiles; tile += npairs, ++tl) {
+            const int mb = tile / nnt, nb = tile % nnt;
+            const int row0 = mb * 256 + static_cast<int>(rank) * 128 + qd * 32;
+            const int row = row0 + lane;
+            const float alpha = row < M ? __fmul_rn(__ldg(p.gA + row), p.gW) : 0.0f;
+            WT_T0(te0);
+            if (!mbar_wait(bar_tfull, static_cast<uint32_t>(tl) & 1u, abort_flag, p.err, 41)) break;
+            if (lane == 0) WT_ADD(7, te0);
+            WT_T0(te1);
+            tc_fence_after();
+            uint32_t a0[32], a1[32], a2[32], a3[32];
+            const uint32_t tcol = tmem + t_lane + 128u * hh;
+            tmem_ld_32x32b_x32(tcol, a0);
+            tmem_ld_32x32b_x32(tcol + 32u, a1);
+            tmem_ld_32x32b_x32(tcol + 64u, a2);
+            tmem_ld_32x32b_x32(tcol + 96u, a3);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(tempty0);
+            if (has_side) {
+                WT_T0(te2);
+                if (!mbar_wait(bar_sfull, static_cast<uint32_t>(tl) & 1u, abort_flag, p.err, 42)) break;
+                if (lane == 0) WT_ADD(8, te2);
+                tc_fence_after();
+            }
+            // finish every column first (the side results are read here), hand the accumulator
+            // back, then store: the stores overlap the next tile's main loop
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint32_t* acc = j == 0 ? a0 : (j == 1 ? a1 : (j == 2 ? a2 : a3));
+                const int c0 = 128 * hh + 32 * j;              // first column of the chunk in the tile
+                uint32_t sd[32];
+                if (has_side) {
+                    tmem_ld_32x32b_x32(tmem + t_lane + static_cast<uint32_t>(c0), sd);
+                    tmem_wait_ld();
+                }
+                const int n0 = nb * 256 + c0;
+#pragma unroll
+                for (int g4 = 0; g4 < 8; ++g4) {
+                    const int n = n0 + 4 * g4;
+                    float v[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) v[e] = alpha * __uint_as_float(acc[4 * g4 + e]);
+                    if (p.colscale != nullptr) {
+                        const float4 cs = n < N ? __ldg(reinterpret_cast<const float4*>(p.colscale + n))
+                                                : make_float4(0.f, 0.f, 0.f, 0.f);
+                        v[0] *= cs.x; v[1] *= cs.y; v[2] *= cs.z; v[3] *= cs.w;
+                    }
+                    if (has_side) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) v[e] += __uint_as_float(sd[4 * g4 + e]);
+                    }
+                    if (p.bias != nullptr) {
+                        const float4 b = n < N ? __ldg(reinterpret_cast<const float4*>(p.bias + n))
+                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+                        v[0] += b.x; v[1] += b.y; v[2] += b.z; v[3] += b.w;
+                    }
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) acc[4 * g4 + e] = __float_as_uint(v[e]);
+                }
+            }
+            if (has_side) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(sempty0);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t* acc = j == 0 ? a0 : (j == 1 ? a1 : (j == 2 ? a2 : a3));
+                if ((j & 1) == 0) {
+                    if (lane == 0) bulk_wait_group_read0();   // the staging buffer is free again
+                    __syncwarp();
+                }
+                const uint32_t hb = ystage + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const uint32_t ch = static_cast<uint32_t>((j & 1) * 4 + jj);
+                    const float* f = reinterpret_cast<const float*>(acc) + 8 * jj;
+                    st_shared_v4(hb + ((ch ^ (static_cast<uint32_t>(lane) & 7u)) << 4), pack_bf16x2(f[0], f[1]),
+                                 pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+                }
+                if (j & 1) {
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        const int x0 = nb * 256 + 128 * hh + 64 * (j >> 1);
+                        if (row0 < M && x0 < N) tma_store_2d(&tmY, ystage, x0, row0);
+                        bulk_commit_group();
+                    }
+                }
+            }
+            if (lane == 0) WT_ADD(9, te1);
+        }
+        if (lane == 0) bulk_wait_group0();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();                 // the pair's MMAs (issued by rank 0) are complete in both TMEMs
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc_pair(tmem, 512);
+}
+
+}  // namespace
+
+int wide_gemm_tiles(int M, int N) { return ((M + 255) / 256) * ((N + 255) / 256); }
+
+cudaError_t launch_gemm_wide(const GemmArgs& a, cudaStream_t st) {
+    if (a.M <= 0) return cudaSuccess;
+    const bool w8 = a.w8;
+    const uint32_t SB = stage_bytes(w8);
+    int S = static_cast<int>((kMaxSmem - kYBytes - 2048) / SB);
+    if (S > kMaxStages && !w8) S = kMaxStages;
+    if (S > 8) S = 8;
+    if (S < 2) return cudaErrorInvalidConfiguration;
+    WParams p{};
+    p.M = a.M; p.N = a.N; p.K = a.K; p.r = a.r; p.n_out = a.n_out; p.stages = S;
+    p.num_kb = a.K / 64;
+    p.num_kt = w8 ? a.K / 64 : (p.num_kb + 3) / 4;
+    p.nrb_a = (a.M + 127) / 128;
+    p.nrb_b = (a.N + 127) / 128;
+    p.off_y = static_cast<uint32_t>(S) * SB;
+    p.off_bar = p.off_y + kYBytes;
+    p.sfa = a.sfa; p.sfb = a.sfb; p.gA = a.gA; p.gW = a.gW; p.bias = a.bias; p.colscale = a.colscale;
+    p.err = a.err;
+    const uint32_t total = p.off_bar + 8u * (3 * S + 5) + 16u + 1024u;
+    static bool attr_set[2] = {false, false};
+    if (!attr_set[w8]) {
+        const cudaError_t e = w8 ? cudaFuncSetAttribute(wide_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                        static_cast<int>(kMaxSmem))
+                                 : cudaFuncSetAttribute(wide_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                        static_cast<int>(kMaxSmem));
+        if (e != cudaSuccess) return e;
+        attr_set[w8] = true;
+    }
+    const int tiles = wide_gemm_tiles(a.M, a.N);
+    const int pairs = tiles < a.num_sms / 2 ? tiles : a.num_sms / 2;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = total;
+    cfg.stream = st;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    at[1].id = cudaLaunchAttributeClusterDimension;
+    at[1].val.clusterDim.x = 2;
+    at[1].val.clusterDim.y = 1;
+    at[1].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 2;
+    if (w8)
+        return cudaLaunchKernelEx(&cfg, wide_gemm_kernel<true>, *a.tmA, *a.tmB, *a.tmU, *a.tmQ, *a.tmXO, *a.tmWO,
+                                  *a.tmY, p);
+    return cudaLaunchKernelEx(&cfg, wide_gemm_kernel<false>, *a.tmA, *a.tmB, *a.tmU, *a.tmQ, *a.tmXO, *a.tmWO, *a.tmY, p);
+}
+
+}  // namespace wq

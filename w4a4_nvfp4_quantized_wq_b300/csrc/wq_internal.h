@@ -73,6 +73,9 @@ struct GemmArgs {
 };
 
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream);
+// CTA-pair schedule (256 x 256 tiles) for batches with many output tiles (wq_gemm2.cu).
+cudaError_t launch_gemm_wide(const GemmArgs& a, cudaStream_t stream);
+int wide_gemm_tiles(int M, int N);
 
 struct ConvArgs {
     const void* x;            // bf16 NCDHW [1, C, D, H, W]
