@@ -65,6 +65,24 @@ def dist_env():
     return ws, int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0"))
 
 
+def job_time_ms(local_ms: float, ws: int, device=None) -> float:
+    """Time of the whole job: the slowest rank's time for the same number of steps (every rank
+    times exactly K steps between barriers).  One rank: its own time."""
+    if ws <= 1:
+        return float(local_ms)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(local_ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank_step: float, steps: int, ws: int, job_ms: float) -> float:
+    """Whole-job units per second: every rank processed `units_per_rank_step` units per step
+    (independent replicas, weak scaling), divided by the job time."""
+    return units_per_rank_step * steps * ws / (job_ms / 1e3)
+
+
 def layers_of(name):
     import workloads as wl
     w = wl.WORKLOADS[name]
@@ -381,17 +399,13 @@ def run_wq(args):
         torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    total_ms = float(sum(step_ms))
+    total_ms = job_time_ms(float(sum(step_ms)), ws, dev)
     if ws > 1:
         import torch.distributed as dist
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
         dist.barrier()
     for h in H:
         wq.wq_check_device_error(h["w"])
-    tokens = M * K * ws
-    tok_s = tokens / (total_ms / 1e3)
+    tok_s = job_throughput(M, K, ws, total_ms)
     flops_step = sum(2.0 * M * h["L"].spec.K * h["L"].spec.N for h in H)
     tflops = flops_step * K * ws / (total_ms / 1e3) / 1e12
 
@@ -576,12 +590,7 @@ def run_conv(args):
                 graph.replay()
                 ev[i][1].record(stream)
         torch.cuda.synchronize()
-    total_ms = float(sum(a.elapsed_time(b) for a, b in ev))
-    if ws_ > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = job_time_ms(float(sum(a.elapsed_time(b) for a, b in ev)), ws_, dev)
     flops = 2.0 * V * N * K
     # per-kernel: the quantiser pair alone, the whole forward; the GEMM is the difference
     times = {}
@@ -654,7 +663,7 @@ def run_conv(args):
                "sample": f"16 of {V} output voxels x {passes} passes, all 384 channels, input and weight "
                          f"quantisation included ({el:.1f} s)"}
     if rank == 0:
-        line = {"metric": METRIC, "value": V * ws_ / (total_ms / Ksteps / 1e3), "unit": "voxels/s",
+        line = {"metric": METRIC, "value": job_throughput(V, Ksteps, ws_, total_ms), "unit": "voxels/s",
                 "n_gpus": ws_, "steps": Ksteps, "warmup": Wu, "ms_per_step": total_ms / Ksteps,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "nvfp4 (e2m1 x e2m1, ue4m3 scales, f32 accumulate)", "data": "synthetic (seeded)",
