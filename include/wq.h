@@ -114,10 +114,22 @@ WQ_API size_t wq_workspace_bytes(wq_weights_t h, int M);
  *              owned by the caller; must not be used concurrently by another call.
  * Two kernels run on `stream`: the fused smooth + FWHT + NVFP4 activation quantiser and
  * the tcgen05 block-scaled FP4 GEMM with the fused epilogue (dequantisation, low-rank
- * branch, outlier slice, bias).
+ * branch, outlier slice, bias).  With the environment variable WQ_FUSED=1, a small batch
+ * (see wq_forward_path) runs both in one thread-block-cluster kernel instead; the results
+ * agree with the two-kernel path within the stated y tolerance (the row scales, codes and
+ * scales are identical; fp32 partial sums may associate differently).
  */
 WQ_API wq_status wq_linear_forward(wq_weights_t h, const void *x, int M, void *y,
                                    void *workspace, size_t workspace_bytes, void *stream);
+
+#define WQ_PATH_TWO_KERNEL 0   /* quantiser kernel, then GEMM kernel */
+#define WQ_PATH_FUSED 1        /* one cluster kernel (M <= 64, rank <= 32, K % 128 == 0) */
+/*
+ * Which path wq_linear_forward takes for M rows under the current environment (host query;
+ * it may ask the CUDA runtime how many clusters fit on the device).  Returns a WQ_PATH_*
+ * value, or WQ_ERR_INVALID for a NULL handle or M < 0.
+ */
+WQ_API int wq_forward_path(wq_weights_t h, int M);
 
 /* Bytes of device scratch wq_linear_forward_host needs (workspace + x and y staging). */
 WQ_API size_t wq_host_workspace_bytes(wq_weights_t h, int M);
@@ -223,6 +235,22 @@ WQ_API wq_status wq_export_weights(wq_weights_t h, uint8_t *codes, uint8_t *scal
  * Returns WQ_OK or WQ_ERR_TIMEOUT (or WQ_ERR_CUDA).
  */
 WQ_API wq_status wq_check_device_error(wq_weights_t h, void *stream);
+
+/*
+ * Self-test of the failure path that every kernel relies on (no counterpart on the pages).
+ * One CTA waits on an mbarrier that nothing arrives on: the wait gives up after its limit
+ * (WQ_WAIT_NS, 2 s of global time), records its site code in a device error flag and, through
+ * the CTA's abort flag, releases a second waiter that started 0.5 s later before that waiter's
+ * own limit.  No fault is raised and the context stays usable.  Synchronises the device.
+ *   site       host int, out: the recorded site code (91 when the path works as designed)
+ *   waited_ms  host double[2], out: how long the two waits lasted (the second one counted
+ *              from its start, 0.5 s before its wait)
+ *   released   host int, out: how many of the two waits returned without an arrival (2)
+ * Returns WQ_ERR_TIMEOUT when a wait ran out (the status a forward reports through
+ * wq_check_device_error in the same situation), WQ_OK if none did, WQ_ERR_CUDA on a launch
+ * or copy failure, WQ_ERR_INVALID for a NULL output pointer.
+ */
+WQ_API wq_status wq_selftest_wait_timeout(int *site, double *waited_ms, int *released);
 
 /* Release the handle and its device memory (synchronises the device first).  NULL is a no-op. */
 WQ_API void wq_free_weights(wq_weights_t h);

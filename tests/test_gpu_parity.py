@@ -186,12 +186,32 @@ def test_forward_parity(case):
 
 
 @pytest.mark.parametrize("case", list(CASES))
+@pytest.mark.parametrize("fused", ["1", "0"])
+def test_forward_parity_fused_and_two_kernel_paths(case, fused, monkeypatch):
+    """With WQ_FUSED=1, small batches (M <= 64, rank <= 32, K % 128 == 0) run quantiser and
+    GEMM fused in one cluster kernel (codes built in shared memory, row maxima and U partials
+    across the cluster, split-K partials summed in rank order); WQ_FUSED=0 keeps the
+    two-kernel path on the same case.  The path actually taken is checked first."""
+    monkeypatch.setenv("WQ_FUSED", fused)
+    L = layer(case)
+    w = prep(L)
+    eligible = L.M <= 64 and L.rank in (0, 16, 32) and L.spec.K % 128 == 0
+    expected = wq.WQ_PATH_FUSED if fused == "1" and eligible else wq.WQ_PATH_TWO_KERNEL
+    assert wq.wq_forward_path(w, L.M) == expected
+    y = wq.wq_linear_forward(w, x_dev(L.x_bits))
+    wq.wq_check_device_error(w)
+    y_ref, *_ = oracle.reference_forward(L)
+    assert_y_close(L, y, y_ref)
+
+
+@pytest.mark.parametrize("case", list(CASES))
 @pytest.mark.parametrize("wide", ["1", "0"])
 def test_forward_parity_gemm_schedules(case, wide, monkeypatch):
     """Both GEMM schedules on every case: 256 x 256 tiles on CTA pairs (tcgen05 cta_group::2,
     single-buffered accumulator, side branch computed into the drained accumulator) and
     128 x 128 tiles on single CTAs; partial tiles in M and N included."""
     monkeypatch.setenv("WQ_GEMM_WIDE", wide)
+    monkeypatch.setenv("WQ_FUSED", "0")              # small batches too run the GEMM under test
     L = layer(case)
     w = prep(L)
     y = wq.wq_linear_forward(w, x_dev(L.x_bits))
@@ -208,6 +228,7 @@ def test_forward_parity_split_k(case, split, monkeypatch):
     """Both GEMM schedules: one persistent CTA per tile (split 1) and the K range of a tile
     spread over a cluster with the DSMEM reduction (split > 1)."""
     monkeypatch.setenv("WQ_GEMM_SPLIT", str(split))
+    monkeypatch.setenv("WQ_FUSED", "0")
     L = layer(case)
     w = prep(L)
     y = wq.wq_linear_forward(w, x_dev(L.x_bits))

@@ -35,7 +35,7 @@ def _rank(rank, ws, port, out):
 
 def test_replica_job_time_is_the_slowest_rank_and_value_counts_all_ranks():
     ws, port = 2, _free_port()
-    manager = mp.Manager()
+    manager = mp.get_context("spawn").Manager()
     out = manager.dict()
     mp.spawn(_rank, args=(ws, port, out), nprocs=ws, join=True)
     for rank in range(ws):
@@ -77,7 +77,7 @@ def _ref_rank(rank, ws, port, out):
 
 def test_reference_arm_non_zero_ranks_exit_without_work():
     ws, port = 2, _free_port()
-    manager = mp.Manager()
+    manager = mp.get_context("spawn").Manager()
     out = manager.dict()
     mp.spawn(_ref_rank, args=(ws, port, out), nprocs=ws, join=True)
     assert out[1] == "returned"

@@ -20,13 +20,15 @@ LIB_PATH = os.path.join(_HERE, "libwq.so")
 WQ_OK, WQ_ERR_INVALID, WQ_ERR_UNSUPPORTED, WQ_ERR_CUDA, WQ_ERR_OOM, WQ_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
 WQ_MODE_W4A4, WQ_MODE_W8A8 = 0, 1
 WQ_SCALE_LAYOUT_ROWMAJOR, WQ_SCALE_LAYOUT_MMA = 0, 1
+WQ_PATH_TWO_KERNEL, WQ_PATH_FUSED = 0, 1
 
 EXPORTED = ["wq_prepare_weights", "wq_get_config", "wq_workspace_bytes", "wq_linear_forward",
             "wq_host_workspace_bytes", "wq_linear_forward_host", "wq_quantize_activations",
             "wq_linear_forward_quantized", "wq_linear_forward_noalloc", "wq_linear_forward_w8a8",
             "wq_quantize_activations_w8a8", "wq_export_weights_w8a8", "wq_prepare_conv3d",
             "wq_conv3d_workspace_bytes", "wq_conv3d_forward", "wq_quantize_conv3d_input",
-            "wq_export_weights", "wq_check_device_error", "wq_free_weights", "wq_last_error"]
+            "wq_export_weights", "wq_check_device_error", "wq_free_weights", "wq_last_error",
+            "wq_forward_path", "wq_selftest_wait_timeout"]
 
 
 class WqError(RuntimeError):
@@ -88,6 +90,10 @@ def lib() -> ctypes.CDLL:
         L.wq_export_weights.restype = I
         L.wq_check_device_error.argtypes = [P, P]
         L.wq_check_device_error.restype = I
+        L.wq_forward_path.argtypes = [P, I]
+        L.wq_forward_path.restype = I
+        L.wq_selftest_wait_timeout.argtypes = [ctypes.POINTER(I), ctypes.POINTER(ctypes.c_double), ctypes.POINTER(I)]
+        L.wq_selftest_wait_timeout.restype = I
         L.wq_free_weights.argtypes = [P]
         L.wq_free_weights.restype = None
         L.wq_last_error.argtypes = []
@@ -268,6 +274,22 @@ def wq_export_weights(w: Weights) -> dict:
     vp = lambda a: a.ctypes.data_as(ctypes.c_void_p)
     _check(lib().wq_export_weights(ctypes.c_void_p(w.handle), vp(codes), vp(scales), vp(gW), vp(P), vp(Q), vp(Wo)))
     return dict(codes=codes, scales=scales, gW=float(gW[0]), P=P, Q=Q, W_omega=Wo)
+
+
+def wq_forward_path(w: Weights, M: int) -> int:
+    """WQ_PATH_TWO_KERNEL or WQ_PATH_FUSED: the path wq_linear_forward takes for M rows."""
+    r = lib().wq_forward_path(ctypes.c_void_p(w.handle), M)
+    if r < 0:
+        _check(r)
+    return r
+
+
+def wq_selftest_wait_timeout():
+    """Run the bounded-wait self-test; returns (status, site, waited_ms pair, released) without raising."""
+    site, released = ctypes.c_int(0), ctypes.c_int(0)
+    waited = (ctypes.c_double * 2)()
+    st = lib().wq_selftest_wait_timeout(ctypes.byref(site), waited, ctypes.byref(released))
+    return st, site.value, (waited[0], waited[1]), released.value
 
 
 def wq_check_device_error(w: Weights, stream=None):

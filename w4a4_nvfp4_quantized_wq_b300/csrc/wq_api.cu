@@ -161,7 +161,7 @@ struct wq_weights {
     int* d_err = nullptr;
     float* d_colscale = nullptr;   // W8A8: per-output-column weight scale [N]
     int conv_cin = 0;              // Conv3d handles: input channels (K = 27 conv_cin)
-    CUtensorMap tmBconv{};         // Conv3d: weight codes with 64-byte boxes
+    CUtensorMap tmBconv{};         // weight codes with 64-byte boxes (Conv3d, fused small-batch path)
     CUtensorMap tmB{}, tmQ{}, tmWO{};
     // activation / output tensor maps, re-encoded when the buffers change
     std::mutex mu;
@@ -437,7 +437,9 @@ WQ_API wq_status wq_prepare_weights(const wq_config* cfg, const float* W, const 
 
     const char* why = "";
     if (!wq::encode_tmap_2d(&h->tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, h->d_codes, K / 2, N, K / 2, 128, 128,
-                            CU_TENSOR_MAP_SWIZZLE_128B, &why))
+                            CU_TENSOR_MAP_SWIZZLE_128B, &why) ||
+        !wq::encode_tmap_2d(&h->tmBconv, CU_TENSOR_MAP_DATA_TYPE_UINT8, h->d_codes, K / 2, N, K / 2, 64, 128,
+                            CU_TENSOR_MAP_SWIZZLE_64B, &why))
         return bail(fail(WQ_ERR_CUDA, why));
     if (r && !wq::encode_tmap_2d(&h->tmQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h->d_Qt, r, N, 2 * r, r, 128,
                                  swizzle_for_row_bytes(2 * r), &why))
@@ -465,21 +467,28 @@ WQ_API size_t wq_host_workspace_bytes(wq_weights_t h, int M) {
            align_up(static_cast<size_t>(M) * h->cfg.N * 2, 1024);
 }
 
+// x as [M, K] bf16 in 16-row x 64-channel boxes (re-encoded when x or M changes).
+static wq_status x_map(wq_weights_t h, const void* x, int M) {
+    std::lock_guard<std::mutex> lk(h->mu_x);
+    if (h->key_x != x || h->key_xM != M) {
+        const char* why = "";
+        if (!wq::encode_tmap_2d(&h->tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, h->cfg.K, M, 2ull * h->cfg.K, 64, 16,
+                                CU_TENSOR_MAP_SWIZZLE_128B, &why)) {
+            h->key_x = nullptr;
+            return fail(WQ_ERR_CUDA, why);
+        }
+        h->key_x = x;
+        h->key_xM = M;
+    }
+    return WQ_OK;
+}
+
 static wq_status run_quant(wq_weights_t h, const void* x, int M, int layout, uint8_t* codes, uint8_t* sf, float* g,
                            uint16_t* xo, uint16_t* u, cudaStream_t st) {
     wq::QuantArgs qa{};
     {
-        std::lock_guard<std::mutex> lk(h->mu_x);
-        if (h->key_x != x || h->key_xM != M) {
-            const char* why = "";
-            if (!wq::encode_tmap_2d(&h->tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, h->cfg.K, M, 2ull * h->cfg.K, 64, 16,
-                                    CU_TENSOR_MAP_SWIZZLE_128B, &why)) {
-                h->key_x = nullptr;
-                return fail(WQ_ERR_CUDA, why);
-            }
-            h->key_x = x;
-            h->key_xM = M;
-        }
+        const wq_status s = x_map(h, x, M);
+        if (s != WQ_OK) return s;
         qa.tmX = &h->tmX;
     }
     qa.pfrag = h->d_Pfrag;
@@ -570,6 +579,21 @@ static wq_status run_gemm(wq_weights_t h, const uint8_t* codes, const uint8_t* s
     return WQ_OK;
 }
 
+namespace {
+bool use_fused(wq_weights_t h, int M, int& nb, int& cs) {
+    const char* ff = std::getenv("WQ_FUSED");
+    return h->cfg.mode == WQ_MODE_W4A4 && ff && ff[0] == '1' &&
+           wq::fused_plan(M, h->cfg.K, h->cfg.N, h->cfg.rank, h->cfg.n_outliers, nb, cs);
+}
+}  // namespace
+
+WQ_API int wq_forward_path(wq_weights_t h, int M) {
+    if (!h) return fail(WQ_ERR_INVALID, "NULL handle");
+    if (M < 0) return fail(WQ_ERR_INVALID, "M < 0");
+    int nb = 0, cs = 0;
+    return M > 0 && use_fused(h, M, nb, cs) ? WQ_PATH_FUSED : WQ_PATH_TWO_KERNEL;
+}
+
 WQ_API wq_status wq_linear_forward(wq_weights_t h, const void* x, int M, void* y, void* workspace,
                                    size_t workspace_bytes, void* stream) {
     if (!h) return fail(WQ_ERR_INVALID, "NULL handle");
@@ -585,6 +609,23 @@ WQ_API wq_status wq_linear_forward(wq_weights_t h, const void* x, int M, void* y
     if (workspace_bytes < ws.bytes) return fail(WQ_ERR_INVALID, "workspace too small");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
+    // WQ_FUSED=1: small batches run quantiser and GEMM fused in one cluster kernel.  Opt-in:
+    // on the measured batch-1 layers the two-kernel pair overlapped by programmatic dependent
+    // launch is faster (the fused kernel's one-CTA-per-SM footprint also keeps the next
+    // layer's quantiser from starting early).
+    int nb = 0, cs = 0;
+    if (use_fused(h, M, nb, cs)) {
+        wq_status s = x_map(h, x, M);
+        if (s != WQ_OK) return s;
+        wq::FusedArgs fa{};
+        fa.M = M; fa.K = K; fa.N = h->cfg.N; fa.r = r; fa.n_out = no; fa.nb = nb; fa.cs = cs;
+        fa.tmX = &h->tmX; fa.tmB = nb == 4 ? &h->tmB : &h->tmBconv; fa.tmQ = &h->tmQ; fa.tmWO = &h->tmWO;
+        fa.inv_s = h->d_inv_s; fa.rotate = h->cfg.rotate; fa.omega_blk = h->d_omega_blk; fa.pfrag = h->d_Pfrag;
+        fa.sfb = h->d_sf; fa.gW = h->gW; fa.bias = h->d_bias; fa.y = y; fa.err = h->d_err;
+        const cudaError_t e = wq::launch_fused(fa, st);
+        if (e != cudaSuccess) return cuda_fail(e, "fused forward launch");
+        return WQ_OK;
+    }
     wq_status s = run_quant(h, x, M, WQ_SCALE_LAYOUT_MMA, ws.codes, ws.sf, ws.g, no ? ws.xo : nullptr,
                             r ? ws.u : nullptr, st);
     if (s != WQ_OK) return s;

@@ -77,6 +77,28 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream);
 cudaError_t launch_gemm_wide(const GemmArgs& a, cudaStream_t stream);
 int wide_gemm_tiles(int M, int N);
 
+// The whole W4A4 forward of a small batch in one kernel (wq_fused.cu).
+struct FusedArgs {
+    int M, K, N, r, n_out;
+    int nb, cs;                     // 64-blocks per CTA, CTAs per cluster (from fused_plan)
+    const CUtensorMap* tmX;         // x [M, K] bf16, box 64 x 16, swizzle 128B
+    const CUtensorMap* tmB;         // weight codes, box (32 nb bytes) x 128, swizzle of that width
+    const CUtensorMap* tmQ;         // Q^T    [N, r]     bf16, box r x 128
+    const CUtensorMap* tmWO;        // W_O^T  [N, n_out] fp16, box n_out x 128
+    const float* inv_s;             // pair order, or null
+    int rotate;
+    const uint32_t* omega_blk;
+    const uint32_t* pfrag;
+    const uint8_t* sfb;             // weight scales, MMA layout
+    float gW;
+    const float* bias;
+    void* y;                        // bf16 [M, N]
+    int* err;
+};
+
+bool fused_plan(int M, int K, int N, int r, int n_out, int& nb, int& cs);
+cudaError_t launch_fused(const FusedArgs& a, cudaStream_t stream);
+
 struct ConvArgs {
     const void* x;            // bf16 NCDHW [1, C, D, H, W]
     int C, D, H, W, V, N;     // V = D H W voxels, N output channels

@@ -38,6 +38,7 @@
 #include <cstdlib>
 
 #include "ptx.cuh"
+#include "quant_block.cuh"
 #include "quant_math.cuh"
 #include "wq_internal.h"
 
@@ -103,189 +104,6 @@ struct QParams {
     int* err;
 };
 
-// ------------------------------------------------------------------ shared-memory helpers
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
-    uint4 v;
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
-    return v;
-}
-__device__ __forceinline__ float4 ld_shared_v4f(uint32_t addr) {
-    float4 v;
-    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr) : "memory");
-    return v;
-}
-__device__ __forceinline__ float2 ld_shared_v2f(uint32_t addr) {
-    float2 v;
-    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
-    return v;
-}
-__device__ __forceinline__ void st_shared_v2f(uint32_t addr, float a, float b) {
-    asm volatile("st.shared.v2.f32 [%0], {%1, %2};" :: "r"(addr), "f"(a), "f"(b) : "memory");
-}
-__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
-}
-__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
-    asm volatile("st.shared.f32 [%0], %1;" :: "r"(addr), "f"(v) : "memory");
-}
-
-// ------------------------------------------------------------------ packed fp32 pairs
-// A lane's 32 channels of a block are held as 16 pairs P[k] = (channel k, channel k + 16) of
-// its half, so the FWHT butterflies at strides 1..8 and the elementwise multiplies run as
-// packed two-lane fp32 instructions; each lane is rounded to nearest on its own, exactly as
-// the scalar operation would be.
-typedef unsigned long long f2;
-__device__ __forceinline__ f2 pk2(float lo, float hi) {
-    f2 r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ float lo2(f2 x) {
-    float a, b;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(x));
-    (void)b;
-    return a;
-}
-__device__ __forceinline__ float hi2(f2 x) {
-    float a, b;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(x));
-    (void)a;
-    return b;
-}
-__device__ __forceinline__ f2 add2(f2 a, f2 b) {
-    f2 r;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ f2 sub2(f2 a, f2 b) {
-    f2 r;
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ f2 mul2(f2 a, f2 b) {
-    f2 r;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {   // RN(a b + c) per lane
-    f2 r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-    return r;
-}
-
-// ------------------------------------------------------------------ per-block steps
-// Row r, half `half` of a raw 16 x 64 bf16 box (128-byte swizzle: 16-byte chunk c of row r at
-// c ^ (r % 8)) -> 16 pairs of smoothed and rotated values.  invs: shared address of the
-// block's 64 inv_s values stored pair-wise (per half: s_k, s_k+16 for k = 0..15), or 0.
-// FWHT in the pages' order: strides 1, 2, 4, 8 between pairs, 16 inside a pair, 32 with the
-// partner lane (lane ^ 16 holds the other half of the row: a + b there, a - b here, as one
-// fused multiply-add with an exact +-1 product), then the exact 1/8 normalisation.
-__device__ __forceinline__ void load_transform(uint32_t box, int r, int half, uint32_t invs, int rotate,
-                                               f2 (&P)[16]) {
-    uint32_t w[4][4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const uint32_t c = static_cast<uint32_t>(4 * half + j);
-        const uint4 q = ld_shared_v4(box + static_cast<uint32_t>(r) * 128u + ((c ^ (static_cast<uint32_t>(r) & 7u)) << 4));
-        w[j][0] = q.x; w[j][1] = q.y; w[j][2] = q.z; w[j][3] = q.w;
-    }
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-        const uint32_t a = w[k / 8][(k % 8) / 2], b = w[2 + k / 8][(k % 8) / 2];
-        P[k] = (k & 1) ? pk2(__uint_as_float(a & 0xFFFF0000u), __uint_as_float(b & 0xFFFF0000u))
-                       : pk2(__uint_as_float(a << 16), __uint_as_float(b << 16));
-    }
-    if (invs != 0u) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const float4 sv = ld_shared_v4f(invs + 128u * half + 16u * j);
-            P[2 * j] = mul2(P[2 * j], pk2(sv.x, sv.y));
-            P[2 * j + 1] = mul2(P[2 * j + 1], pk2(sv.z, sv.w));
-        }
-    }
-    if (rotate) {
-#pragma unroll
-        for (int h = 1; h < 16; h <<= 1) {
-#pragma unroll
-            for (int k = 0; k < 16; ++k)
-                if ((k & h) == 0) {
-                    const f2 a = P[k], b = P[k + h];
-                    P[k] = add2(a, b);
-                    P[k + h] = sub2(a, b);
-                }
-        }
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            const float a = lo2(P[k]), b = hi2(P[k]);
-            P[k] = pk2(__fadd_rn(a, b), __fsub_rn(a, b));
-        }
-        const float sgn = half ? -1.0f : 1.0f;
-        const f2 sg = pk2(sgn, sgn);
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            const f2 o = pk2(__shfl_xor_sync(kFullMask, lo2(P[k]), 16), __shfl_xor_sync(kFullMask, hi2(P[k]), 16));
-            P[k] = fma2(P[k], sg, o);
-        }
-        const f2 c8 = pk2(0.125f, 0.125f);
-#pragma unroll
-        for (int k = 0; k < 16; ++k) P[k] = mul2(P[k], c8);
-    }
-}
-
-// Zero the kept channels of this half (bit e of `mine`: channel e): a kept channel becomes +0
-// and every other value keeps all its bits, the sign of a zero included.
-__device__ __forceinline__ void apply_keep(f2 (&P)[16], uint32_t mine) {
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-        const uint32_t a = ((mine >> k) & 1u) - 1u;          // channel k: 0 if kept, else all ones
-        const uint32_t b = ((mine >> (k + 16)) & 1u) - 1u;   // channel k + 16
-        P[k] &= (static_cast<f2>(b) << 32) | a;
-    }
-}
-
-// e4m3(RN(RN(bm / 6) / g)), the block scale.  t = RN(RN(bm c6) rg) with c6 = RN(1/6) and
-// rg = RN(1/g) is within 6 ulp-units of 2^-24 (relative) of the two-division value, so when
-// t (1 - 2^-20) and t (1 + 2^-20) convert to the same code, that value (which lies between
-// them; the conversion is monotone) converts to it too.  Otherwise, and when a product could
-// leave the normal range, the two divisions are done.
-__device__ __forceinline__ uint32_t scale_code(float bm, float g, float rg) {
-    if (g == 0.0f || bm == 0.0f) return 0u;
-    const float u = __fmul_rn(bm, 0.16666667163372040f);
-    if (rg < 3.0e38f && u >= 1.0e-36f) {
-        const float t = __fmul_rn(u, rg);
-        const uint32_t lo = cvt_e4m3(__fmul_rn(t, 0.99999904632568359f));
-        const uint32_t hi = cvt_e4m3(__fmul_rn(t, 1.00000095367431641f));
-        if (lo == hi) return lo;
-    }
-    return cvt_e4m3(__fdiv_rn(__fdiv_rn(bm, 6.0f), g));
-}
-
-// Maxima of |x| over the half's two 16-element blocks (channels 0..15: the pairs' first lanes).
-__device__ __forceinline__ void absmax_pairs(const f2 (&P)[16], float& ma, float& mb) {
-    ma = 0.0f;
-    mb = 0.0f;
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-        ma = fmaxf(ma, fabsf(lo2(P[k])));
-        mb = fmaxf(mb, fabsf(hi2(P[k])));
-    }
-}
-
-// Codes of channels (k, k+1) of both 16-blocks of the half (pairs P0 = P[k], P1 = P[k+1]), by
-// the reciprocal-and-bracket argument of e2m1_codes8_r, two blocks per packed multiply.
-__device__ __forceinline__ void codes_2x2(f2 P0, f2 P1, f2 rr, float da, float db, uint32_t& ca, uint32_t& cb) {
-    const f2 mlo = pk2(0.99999952316284180f, 0.99999952316284180f);
-    const f2 mhi = pk2(1.00000047683715820f, 1.00000047683715820f);
-    const f2 q0 = mul2(P0, rr), q1 = mul2(P1, rr);
-    const f2 l0 = mul2(q0, mlo), l1 = mul2(q1, mlo), h0 = mul2(q0, mhi), h1 = mul2(q1, mhi);
-    const uint32_t alo = cvt_e2m1x2(lo2(l0), lo2(l1)), ahi = cvt_e2m1x2(lo2(h0), lo2(h1));
-    const uint32_t blo = cvt_e2m1x2(hi2(l0), hi2(l1)), bhi = cvt_e2m1x2(hi2(h0), hi2(h1));
-    ca = alo == ahi ? alo : cvt_e2m1x2(__fdiv_rn(lo2(P0), da), __fdiv_rn(lo2(P1), da));
-    cb = blo == bhi ? blo : cvt_e2m1x2(__fdiv_rn(hi2(P0), db), __fdiv_rn(hi2(P1), db));
-}
-
 // Pull block kb's slice of the packed P (NT KiB) towards this SM's L1, one 128-byte line per
 // lane, ahead of the U step that reads it.
 template <int NT>
@@ -299,78 +117,18 @@ __device__ __forceinline__ void prefetch_block_consts(const QParams& p, int kb, 
     }
 }
 
-// The block's share of U = x P: A = the raw 16 x 64 box, every n-tile of P.  Each
-// (block, n-tile) is accumulated on the tensor cores from zero and added to the warp's
-// partial (shared memory, mma fragment order, 512 B per n-tile) with an fp32 add, so the
-// tensor-core accumulation depth stays at 64 whatever K is.
-template <int NT>
-__device__ __forceinline__ void u_step(uint32_t box, int lane, int kb, const uint32_t* pfrag, uint32_t upart, bool first) {
-    uint32_t a[4][4];
-    const uint32_t arow = static_cast<uint32_t>((lane & 7) + 8 * ((lane >> 3) & 1));
-#pragma unroll
-    for (int f = 0; f < 4; ++f) {
-        const uint32_t chunk = static_cast<uint32_t>(2 * f + (lane >> 4));
-        ldmatrix_x4(box + arow * 128u + ((chunk ^ (arow & 7u)) << 4), a[f][0], a[f][1], a[f][2], a[f][3]);
-    }
-    __syncwarp();                          // the box is read before a partial may land on it
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        const uint4* pb = reinterpret_cast<const uint4*>(pfrag + (static_cast<size_t>(kb * NT + nt) * 32 + lane) * 8);
-        const uint4 q0 = __ldg(pb), q1 = __ldg(pb + 1);
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_bf16_16816(acc, a[0][0], a[0][1], a[0][2], a[0][3], q0.x, q0.y);
-        mma_bf16_16816(acc, a[1][0], a[1][1], a[1][2], a[1][3], q0.z, q0.w);
-        mma_bf16_16816(acc, a[2][0], a[2][1], a[2][2], a[2][3], q1.x, q1.y);
-        mma_bf16_16816(acc, a[3][0], a[3][1], a[3][2], a[3][3], q1.z, q1.w);
-        const uint32_t ua = upart + (static_cast<uint32_t>(nt) * 32u + lane) * 16u;
-        if (first) {
-            st_shared_v4f(ua, acc[0], acc[1], acc[2], acc[3]);
-        } else {
-            const float4 o = ld_shared_v4f(ua);
-            st_shared_v4f(ua, __fadd_rn(o.x, acc[0]), __fadd_rn(o.y, acc[1]), __fadd_rn(o.z, acc[2]), __fadd_rn(o.w, acc[3]));
-        }
-    }
-}
-
-// Codes and scales of this lane's half row of block kb (maxima bma, bmb of its two 16-blocks).
+// Codes and scales of this lane's half row of block kb to global memory.
+template <bool kOut>
 __device__ __forceinline__ void emit_nvfp4(const f2 (&P)[16], float bma, float bmb, float gsc, float rg, int row,
                                            bool row_ok, int kb, int half, const QParams& p) {
-    const uint32_t sa = scale_code(bma, gsc, rg), sb = scale_code(bmb, gsc, rg);
-    const float da = __fmul_rn(dec_e4m3(sa), gsc), db = __fmul_rn(dec_e4m3(sb), gsc);
-    const float ra = __frcp_rn(da), rb = __frcp_rn(db);
-    uint32_t wa[2] = {0u, 0u}, wb[2] = {0u, 0u};     // channels 0..7, 8..15 / 16..23, 24..31
-    if (ra < 3.0e38f && rb < 3.0e38f) {
-        // both blocks have a non-zero, non-tiny scale: packed path
-        const f2 rr = pk2(ra, rb);
-#pragma unroll
-        for (int k = 0; k < 16; k += 2) {
-            uint32_t ca, cb;
-            codes_2x2(P[k], P[k + 1], rr, da, db, ca, cb);
-            wa[k / 8] |= ca << (8 * ((k / 2) % 4));
-            wb[k / 8] |= cb << (8 * ((k / 2) % 4));
-        }
-    } else {
-        float va[16], vb[16];
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            va[k] = lo2(P[k]);
-            vb[k] = hi2(P[k]);
-        }
-        if (da != 0.0f) {
-            wa[0] = e2m1_codes8_r(va, da, ra);
-            wa[1] = e2m1_codes8_r(va + 8, da, ra);
-        }
-        if (db != 0.0f) {
-            wb[0] = e2m1_codes8_r(vb, db, rb);
-            wb[1] = e2m1_codes8_r(vb + 8, db, rb);
-        }
-    }
+    uint32_t w[4], sa, sb;
+    nvfp4_half_codes<kOut>(P, bma, bmb, gsc, rg, w, sa, sb);
     const uint32_t s2 = sa | (sb << 8);
     const uint32_t s2o = __shfl_xor_sync(kFullMask, s2, 16);
     if (row_ok) {
         const int K = p.K;
         *reinterpret_cast<uint4*>(p.codes + static_cast<size_t>(row) * (K / 2) + kb * 32 + 16 * half) =
-            make_uint4(wa[0], wa[1], wb[0], wb[1]);
+            make_uint4(w[0], w[1], w[2], w[3]);
         if (half == 0) {
             size_t off;
             if (p.sf_layout == WQ_SCALE_LAYOUT_MMA)
@@ -384,6 +142,7 @@ __device__ __forceinline__ void emit_nvfp4(const f2 (&P)[16], float bma, float b
 }
 
 // 8-bit values of this lane's half row of block kb as exact bf16 integers (ra = RN(1 / gsc)).
+template <bool kOut>
 __device__ __forceinline__ void emit_int8(const f2 (&P)[16], float gsc, float ra, int row, bool row_ok, int kb,
                                           int half, const QParams& p) {
     float va[16], vb[16];
@@ -396,7 +155,7 @@ __device__ __forceinline__ void emit_int8(const f2 (&P)[16], float gsc, float ra
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         float q[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        if (gsc != 0.0f) int8_values8_r(j < 2 ? va + 8 * j : vb + 8 * (j - 2), gsc, ra, q);
+        if (gsc != 0.0f) int8_values8_r<kOut>(j < 2 ? va + 8 * j : vb + 8 * (j - 2), gsc, ra, q);
         uint32_t pkw[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -405,14 +164,6 @@ __device__ __forceinline__ void emit_int8(const f2 (&P)[16], float gsc, float ra
         }
         if (row_ok) dst[j] = make_uint4(pkw[0], pkw[1], pkw[2], pkw[3]);
     }
-}
-
-// U entry of fragment index idx = (nt 32 + lane) 4 + e: row gq + 8 (e / 2), column
-// 8 nt + 2 cq + e % 2, with gq = lane / 4, cq = lane % 4.
-__device__ __forceinline__ void frag_pos(int idx, int& rr, int& cc) {
-    const int nt = idx / 128, ln = (idx / 4) % 32, e = idx % 4;
-    rr = (ln >> 2) + 8 * (e >> 1);
-    cc = 8 * nt + 2 * (ln & 3) + (e & 1);
 }
 
 // ==================================================================== cluster schedule
@@ -622,10 +373,10 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmX, const QParams p) {
             P[2 * j + 1] = pk2(t.z, t.w);
         }
         if constexpr (kInt8) {
-            emit_int8(P, gsc, rg_inv, row, row_ok, kb_lo + i, half, p);
+            emit_int8<true>(P, gsc, rg_inv, row, row_ok, kb_lo + i, half, p);
         } else {
             const float2 bm = ld_shared_v2f(slot + kMaxOff + static_cast<uint32_t>(r) * 16u + 8u * half);
-            emit_nvfp4(P, bm.x, bm.y, gsc, rg_inv, row, row_ok, kb_lo + i, half, p);
+            emit_nvfp4<true>(P, bm.x, bm.y, gsc, rg_inv, row, row_ok, kb_lo + i, half, p);
         }
     }
     if (threadIdx.x == 0) WQ_QTRACE_AT(5);
@@ -822,11 +573,11 @@ quantize_stream_kernel(const __grid_constant__ CUtensorMap tmX, const QParams p)
             const uint32_t m0 = p.n_out ? s_omega[4 * kb] : 0u, m1 = p.n_out ? s_omega[4 * kb + 1] : 0u;
             if ((half ? m1 : m0) != 0u) apply_keep(P, half ? m1 : m0);
             if constexpr (kInt8) {
-                emit_int8(P, gsc, rg_inv, row, row_ok, kb, half, p);
+                emit_int8<false>(P, gsc, rg_inv, row, row_ok, kb, half, p);
             } else {
                 float ma, mb;
                 absmax_pairs(P, ma, mb);
-                emit_nvfp4(P, ma, mb, gsc, rg_inv, row, row_ok, kb, half, p);
+                emit_nvfp4<false>(P, ma, mb, gsc, rg_inv, row, row_ok, kb, half, p);
             }
         }
         q0 += static_cast<uint32_t>(nblk);
