@@ -131,6 +131,24 @@ WQ_API wq_status wq_linear_forward(wq_weights_t h, const void *x, int M, void *y
  */
 WQ_API int wq_forward_path(wq_weights_t h, int M);
 
+#define WQ_QUANT_CLUSTER 0  /* a 16-row tile per cluster, K spread over its CTAs (few rows) */
+#define WQ_QUANT_STREAM 1   /* persistent CTAs streaming row tiles (at least 2 x SMs of them) */
+/*
+ * Which activation-quantiser schedule M rows take (host query).  Returns a WQ_QUANT_* value,
+ * or WQ_ERR_INVALID for a NULL handle or M < 0.
+ */
+WQ_API int wq_quant_schedule(wq_weights_t h, int M);
+
+#define WQ_GEMM_SINGLE 0   /* 128 x 128 tiles, one persistent CTA per SM */
+#define WQ_GEMM_SPLITK 1   /* 128 x 128 tiles, K split over a thread-block cluster (few tiles) */
+#define WQ_GEMM_WIDE 2     /* 256 x 256 tiles on CTA pairs (4-bit layers with K >= 4096) */
+/*
+ * Which GEMM schedule the two-kernel path (and wq_linear_forward_quantized) uses for M rows
+ * under the current environment (host query; it may ask the CUDA runtime how many clusters
+ * fit).  Returns a WQ_GEMM_* value, or WQ_ERR_INVALID / WQ_ERR_CUDA.
+ */
+WQ_API int wq_gemm_schedule(wq_weights_t h, int M);
+
 /* Bytes of device scratch wq_linear_forward_host needs (workspace + x and y staging). */
 WQ_API size_t wq_host_workspace_bytes(wq_weights_t h, int M);
 

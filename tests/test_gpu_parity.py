@@ -214,6 +214,8 @@ def test_forward_parity_gemm_schedules(case, wide, monkeypatch):
     monkeypatch.setenv("WQ_FUSED", "0")              # small batches too run the GEMM under test
     L = layer(case)
     w = prep(L)
+    sched = wq.wq_gemm_schedule(w, L.M)
+    assert (sched == wq.WQ_GEMM_WIDE) == (wide == "1")
     y = wq.wq_linear_forward(w, x_dev(L.x_bits))
     wq.wq_check_device_error(w)
     y_ref, *_ = oracle.reference_forward(L)
@@ -381,4 +383,19 @@ def test_full_size_sampled_rows(wl_name, layer_idx):
     assert np.array_equal(codes.cpu().numpy()[rows], aq.codes)
     assert np.array_equal(scales.cpu().numpy()[rows], aq.scales)
     assert np.array_equal(g.cpu().numpy()[rows], aq.g)
+    assert_y_close(L, y[torch.from_numpy(rows).cuda()], y_ref, rows)
+
+
+@pytest.mark.parametrize("wide", ["1", "0"])
+def test_full_size_long_k_both_gemm_schedules(wide, monkeypatch):
+    """The video-DiT down projection (M = 16384, K = 8960) on the CTA-pair schedule (its
+    default) and on the single-CTA schedule, at full size, on sampled rows."""
+    monkeypatch.setenv("WQ_GEMM_WIDE", wide)
+    L = wl.make_layer_inputs("video_dit", layer=3)
+    w = prep(L)
+    assert (wq.wq_gemm_schedule(w, L.M) == wq.WQ_GEMM_WIDE) == (wide == "1")
+    y = wq.wq_linear_forward(w, x_dev(L.x_bits))
+    wq.wq_check_device_error(w)
+    rows = _sampled_rows(L.M, 16, 300)
+    y_ref, *_ = oracle.reference_forward(L, rows=rows)
     assert_y_close(L, y[torch.from_numpy(rows).cuda()], y_ref, rows)

@@ -21,6 +21,8 @@ WQ_OK, WQ_ERR_INVALID, WQ_ERR_UNSUPPORTED, WQ_ERR_CUDA, WQ_ERR_OOM, WQ_ERR_TIMEO
 WQ_MODE_W4A4, WQ_MODE_W8A8 = 0, 1
 WQ_SCALE_LAYOUT_ROWMAJOR, WQ_SCALE_LAYOUT_MMA = 0, 1
 WQ_PATH_TWO_KERNEL, WQ_PATH_FUSED = 0, 1
+WQ_GEMM_SINGLE, WQ_GEMM_SPLITK, WQ_GEMM_WIDE = 0, 1, 2
+WQ_QUANT_CLUSTER, WQ_QUANT_STREAM = 0, 1
 
 EXPORTED = ["wq_prepare_weights", "wq_get_config", "wq_workspace_bytes", "wq_linear_forward",
             "wq_host_workspace_bytes", "wq_linear_forward_host", "wq_quantize_activations",
@@ -28,7 +30,8 @@ EXPORTED = ["wq_prepare_weights", "wq_get_config", "wq_workspace_bytes", "wq_lin
             "wq_quantize_activations_w8a8", "wq_export_weights_w8a8", "wq_prepare_conv3d",
             "wq_conv3d_workspace_bytes", "wq_conv3d_forward", "wq_quantize_conv3d_input",
             "wq_export_weights", "wq_check_device_error", "wq_free_weights", "wq_last_error",
-            "wq_forward_path", "wq_selftest_wait_timeout"]
+            "wq_forward_path", "wq_selftest_wait_timeout", "wq_gemm_schedule",
+            "wq_quant_schedule"]
 
 
 class WqError(RuntimeError):
@@ -92,6 +95,10 @@ def lib() -> ctypes.CDLL:
         L.wq_check_device_error.restype = I
         L.wq_forward_path.argtypes = [P, I]
         L.wq_forward_path.restype = I
+        L.wq_gemm_schedule.argtypes = [P, I]
+        L.wq_gemm_schedule.restype = I
+        L.wq_quant_schedule.argtypes = [P, I]
+        L.wq_quant_schedule.restype = I
         L.wq_selftest_wait_timeout.argtypes = [ctypes.POINTER(I), ctypes.POINTER(ctypes.c_double), ctypes.POINTER(I)]
         L.wq_selftest_wait_timeout.restype = I
         L.wq_free_weights.argtypes = [P]
@@ -279,6 +286,22 @@ def wq_export_weights(w: Weights) -> dict:
 def wq_forward_path(w: Weights, M: int) -> int:
     """WQ_PATH_TWO_KERNEL or WQ_PATH_FUSED: the path wq_linear_forward takes for M rows."""
     r = lib().wq_forward_path(ctypes.c_void_p(w.handle), M)
+    if r < 0:
+        _check(r)
+    return r
+
+
+def wq_gemm_schedule(w: Weights, M: int) -> int:
+    """WQ_GEMM_SINGLE, WQ_GEMM_SPLITK or WQ_GEMM_WIDE: the GEMM schedule for M rows."""
+    r = lib().wq_gemm_schedule(ctypes.c_void_p(w.handle), M)
+    if r < 0:
+        _check(r)
+    return r
+
+
+def wq_quant_schedule(w: Weights, M: int) -> int:
+    """WQ_QUANT_CLUSTER or WQ_QUANT_STREAM: the activation-quantiser schedule for M rows."""
+    r = lib().wq_quant_schedule(ctypes.c_void_p(w.handle), M)
     if r < 0:
         _check(r)
     return r

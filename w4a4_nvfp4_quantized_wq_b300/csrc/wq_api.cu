@@ -587,6 +587,26 @@ bool use_fused(wq_weights_t h, int M, int& nb, int& cs) {
 }
 }  // namespace
 
+WQ_API int wq_quant_schedule(wq_weights_t h, int M) {
+    if (!h) return fail(WQ_ERR_INVALID, "NULL handle");
+    if (M < 0) return fail(WQ_ERR_INVALID, "M < 0");
+    return wq::quant_stream_schedule(M, h->num_sms) ? WQ_QUANT_STREAM : WQ_QUANT_CLUSTER;
+}
+
+WQ_API int wq_gemm_schedule(wq_weights_t h, int M) {
+    if (!h) return fail(WQ_ERR_INVALID, "NULL handle");
+    if (M < 0) return fail(WQ_ERR_INVALID, "M < 0");
+    wq::GemmArgs ga{};
+    ga.M = M > 0 ? M : 1; ga.N = h->cfg.N; ga.K = h->cfg.K; ga.r = h->cfg.rank; ga.n_out = h->cfg.n_outliers;
+    ga.w8 = h->cfg.mode == WQ_MODE_W8A8;
+    ga.num_sms = h->num_sms;
+    const char* fs = std::getenv("WQ_GEMM_SPLIT");
+    ga.force_split = fs ? std::atoi(fs) : 0;
+    const int s = wq::gemm_schedule(ga);
+    if (s < 0) return fail(WQ_ERR_CUDA, "GEMM schedule query failed");
+    return s;
+}
+
 WQ_API int wq_forward_path(wq_weights_t h, int M) {
     if (!h) return fail(WQ_ERR_INVALID, "NULL handle");
     if (M < 0) return fail(WQ_ERR_INVALID, "M < 0");

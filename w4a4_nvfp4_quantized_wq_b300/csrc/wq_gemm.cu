@@ -572,11 +572,7 @@ int choose_split(int tiles, int num_kt, int num_sms, size_t smem) {
 }
 
 template <bool kW8>
-cudaError_t launch_gemm_t(const GemmArgs& a, cudaStream_t st) {
-    // WQ_GEMM_STAGES=<n> caps the shared-memory ring depth (tuning)
-    const char* ms = std::getenv("WQ_GEMM_STAGES");
-    const Plan pl = make_plan(a.r, a.n_out, ms ? std::atoi(ms) : 8, kW8);
-    if (pl.stages < 2) return cudaErrorInvalidConfiguration;
+cudaError_t gemm_attributes() {
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(nvfp4_gemm_kernel<kW8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -586,9 +582,34 @@ cudaError_t launch_gemm_t(const GemmArgs& a, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
+    return cudaSuccess;
+}
+
+template <bool kW8>
+Plan gemm_plan(const GemmArgs& a) {
+    // WQ_GEMM_STAGES=<n> caps the shared-memory ring depth (tuning)
+    const char* ms = std::getenv("WQ_GEMM_STAGES");
+    return make_plan(a.r, a.n_out, ms ? std::atoi(ms) : 8, kW8);
+}
+
+// CTAs per output tile of the single-CTA schedule: the forced value, or the largest cluster
+// that keeps every tile's cluster resident (1 = persistent).
+template <bool kW8>
+int gemm_split(const GemmArgs& a, const Plan& pl) {
     const int tiles = ((a.M + 127) / 128) * ((a.N + 127) / 128);
     const int num_kt = kW8 ? a.K / 64 : (a.K / 64 + 3) / 4;
-    const int split = a.force_split > 0 ? a.force_split : choose_split<kW8>(tiles, num_kt, a.num_sms, pl.total);
+    return a.force_split > 0 ? a.force_split : choose_split<kW8>(tiles, num_kt, a.num_sms, pl.total);
+}
+
+template <bool kW8>
+cudaError_t launch_gemm_t(const GemmArgs& a, cudaStream_t st) {
+    const Plan pl = gemm_plan<kW8>(a);
+    if (pl.stages < 2) return cudaErrorInvalidConfiguration;
+    const cudaError_t ea = gemm_attributes<kW8>();
+    if (ea != cudaSuccess) return ea;
+    const int tiles = ((a.M + 127) / 128) * ((a.N + 127) / 128);
+    const int num_kt = kW8 ? a.K / 64 : (a.K / 64 + 3) / 4;
+    const int split = gemm_split<kW8>(a, pl);
     if (split > num_kt || split > 16 || (split & (split - 1))) return cudaErrorInvalidValue;
     KParams kp{};
     kp.split = split;
@@ -623,16 +644,33 @@ cudaError_t launch_gemm_t(const GemmArgs& a, cudaStream_t st) {
 
 }  // namespace
 
+// The pair schedule or not (see launch_gemm).
+bool use_wide(const GemmArgs& a) {
+    bool wide = !a.w8 && a.force_split == 0 && a.K >= 4096 && wide_gemm_tiles(a.M, a.N) >= a.num_sms / 2;
+    if (const char* fw = std::getenv("WQ_GEMM_WIDE")) wide = fw[0] == '1' && a.force_split == 0;
+    return wide;
+}
+
+int gemm_schedule(const GemmArgs& a) {
+    if (use_wide(a)) return 2;
+    if (a.w8) {
+        if (gemm_attributes<true>() != cudaSuccess) return -1;
+        return gemm_split<true>(a, gemm_plan<true>(a)) > 1 ? 1 : 0;
+    }
+    if (gemm_attributes<false>() != cudaSuccess) return -1;
+    return gemm_split<false>(a, gemm_plan<false>(a)) > 1 ? 1 : 0;
+}
+
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
     if (a.M <= 0) return cudaSuccess;
-    // 128 x 128 tiles on single CTAs (split-K over clusters when the tiles alone cannot fill
-    // the GPU) by default; WQ_GEMM_WIDE=1 selects the CTA-pair schedule with 256 x 256 tiles.
-    // The pair schedule is bit-for-bit tested but not yet faster: its five-stage ring cannot
-    // cover the L2 latency at the pair's data rate, and its single accumulator serialises the
-    // side branch with the main loop.
-    bool wide = false;
-    if (const char* fw = std::getenv("WQ_GEMM_WIDE")) wide = fw[0] == '1' && a.force_split == 0;
-    if (wide) return launch_gemm_wide(a, st);
+    // Two schedules.  128 x 128 tiles on single CTAs (split-K over clusters when the tiles
+    // alone cannot fill the GPU), bound by the tcgen05 issue of one N = 128 MMA and two scale
+    // copies per 64-deep K block.  256 x 256 tiles on CTA pairs: N = 256 pair MMAs need about
+    // 0.7x the issue time per flop, but the accumulator is single-buffered, so each tile pays
+    // the drain and the side branch (a few us) before the next main loop.  The pair schedule
+    // therefore wins on long K: it is chosen for 4-bit layers with K >= 4096 whose 256 x 256
+    // tiles fill every SM pair.  WQ_GEMM_WIDE=0/1 pins the choice (tests and tuning).
+    if (use_wide(a)) return launch_gemm_wide(a, st);
     return a.w8 ? launch_gemm_t<true>(a, st) : launch_gemm_t<false>(a, st);
 }
 

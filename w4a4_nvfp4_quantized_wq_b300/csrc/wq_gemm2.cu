@@ -34,7 +34,7 @@
 
 #ifdef WQ_TRACE
 // Wait-time counters for kernel development builds only (never defined in the product build).
-__device__ unsigned long long g_wq_wtrace[16];
+__device__ unsigned long long g_wq_wtrace[16];   // 10: drain, 11: side read, 12: stores
 extern "C" WQ_API int wq_wtrace_read(void* host, size_t bytes) {
     return static_cast<int>(cudaMemcpyFromSymbol(host, g_wq_wtrace, bytes));
 }
@@ -316,6 +316,15 @@ wide_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             const int row0 = mb * 256 + static_cast<int>(rank) * 128 + qd * 32;
             const int row = row0 + lane;
             const float alpha = row < M ? __fmul_rn(__ldg(p.gA + row), p.gW) : 0.0f;
+            // this warp's 128 bias (and column-scale) values, one float4 per lane, fetched before
+            // the accumulator wait so that their latency hides behind the main loop; the column
+            // loop below takes them from the owning lane by shuffle
+            const int nl = nb * 256 + 128 * hh + 4 * lane;
+            const float4 bias4 = (p.bias != nullptr && nl < N) ? __ldg(reinterpret_cast<const float4*>(p.bias + nl))
+                                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 cs4 = (p.colscale != nullptr && nl < N)
+                                   ? __ldg(reinterpret_cast<const float4*>(p.colscale + nl))
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
             WT_T0(te0);
             if (!mbar_wait(bar_tfull, static_cast<uint32_t>(tl) & 1u, abort_flag, p.err, 41)) break;
             if (lane == 0) WT_ADD(7, te0);
@@ -331,6 +340,7 @@ wide_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(tempty0);
+            if (lane == 0) WT_ADD(10, te1);
             if (has_side) {
                 WT_T0(te2);
                 if (!mbar_wait(bar_sfull, static_cast<uint32_t>(tl) & 1u, abort_flag, p.err, 42)) break;
@@ -339,6 +349,7 @@ wide_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             }
             // finish every column first (the side results are read here), hand the accumulator
             // back, then store: the stores overlap the next tile's main loop
+            WT_T0(te3);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 uint32_t* acc = j == 0 ? a0 : (j == 1 ? a1 : (j == 2 ? a2 : a3));
@@ -348,26 +359,27 @@ wide_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     tmem_ld_32x32b_x32(tmem + t_lane + static_cast<uint32_t>(c0), sd);
                     tmem_wait_ld();
                 }
-                const int n0 = nb * 256 + c0;
 #pragma unroll
                 for (int g4 = 0; g4 < 8; ++g4) {
-                    const int n = n0 + 4 * g4;
+                    const int src = 8 * j + g4;                    // lane holding columns c0 + 4 g4 ..
                     float v[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) v[e] = alpha * __uint_as_float(acc[4 * g4 + e]);
                     if (p.colscale != nullptr) {
-                        const float4 cs = n < N ? __ldg(reinterpret_cast<const float4*>(p.colscale + n))
-                                                : make_float4(0.f, 0.f, 0.f, 0.f);
-                        v[0] *= cs.x; v[1] *= cs.y; v[2] *= cs.z; v[3] *= cs.w;
+                        v[0] *= __shfl_sync(0xFFFFFFFFu, cs4.x, src);
+                        v[1] *= __shfl_sync(0xFFFFFFFFu, cs4.y, src);
+                        v[2] *= __shfl_sync(0xFFFFFFFFu, cs4.z, src);
+                        v[3] *= __shfl_sync(0xFFFFFFFFu, cs4.w, src);
                     }
                     if (has_side) {
 #pragma unroll
                         for (int e = 0; e < 4; ++e) v[e] += __uint_as_float(sd[4 * g4 + e]);
                     }
                     if (p.bias != nullptr) {
-                        const float4 b = n < N ? __ldg(reinterpret_cast<const float4*>(p.bias + n))
-                                               : make_float4(0.f, 0.f, 0.f, 0.f);
-                        v[0] += b.x; v[1] += b.y; v[2] += b.z; v[3] += b.w;
+                        v[0] += __shfl_sync(0xFFFFFFFFu, bias4.x, src);
+                        v[1] += __shfl_sync(0xFFFFFFFFu, bias4.y, src);
+                        v[2] += __shfl_sync(0xFFFFFFFFu, bias4.z, src);
+                        v[3] += __shfl_sync(0xFFFFFFFFu, bias4.w, src);
                     }
 #pragma unroll
                     for (int e = 0; e < 4; ++e) acc[4 * g4 + e] = __float_as_uint(v[e]);
@@ -378,6 +390,8 @@ wide_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(sempty0);
             }
+            if (lane == 0) WT_ADD(11, te3);
+            WT_T0(te4);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const uint32_t* acc = j == 0 ? a0 : (j == 1 ? a1 : (j == 2 ? a2 : a3));
@@ -403,6 +417,7 @@ wide_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     }
                 }
             }
+            if (lane == 0) WT_ADD(12, te4);
             if (lane == 0) WT_ADD(9, te1);
         }
         if (lane == 0) bulk_wait_group0();

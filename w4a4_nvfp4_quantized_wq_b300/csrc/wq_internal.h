@@ -49,6 +49,8 @@ struct QuantArgs {
 };
 
 cudaError_t launch_quantize_act(const QuantArgs& a, cudaStream_t stream);
+// True when M rows take the persistent stream schedule (else the cluster schedule).
+bool quant_stream_schedule(int M, int num_sms);
 
 struct GemmArgs {
     int M, N, K, r, n_out;
@@ -73,6 +75,9 @@ struct GemmArgs {
 };
 
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream);
+// 0: 128 x 128 tiles on persistent single CTAs; 1: split-K clusters; 2: 256 x 256 tiles on CTA
+// pairs; -1 on a CUDA error.  Only the shape, mode, SM count and force_split of `a` are read.
+int gemm_schedule(const GemmArgs& a);
 // CTA-pair schedule (256 x 256 tiles) for batches with many output tiles (wq_gemm2.cu).
 cudaError_t launch_gemm_wide(const GemmArgs& a, cudaStream_t stream);
 int wide_gemm_tiles(int M, int N);

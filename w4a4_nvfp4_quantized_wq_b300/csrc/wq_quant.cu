@@ -664,18 +664,23 @@ cudaError_t launch_r(const CUtensorMap& tm, const QParams& qp, bool stream, int 
 
 }  // namespace
 
-cudaError_t launch_quantize_act(const QuantArgs& a, cudaStream_t st) {
-    if (a.M <= 0) return cudaSuccess;
-    Choice ch = choose(a.K);
-    const int row_tiles = (a.M + kRows - 1) / kRows;
+bool quant_stream_schedule(int M, int num_sms) {
     // many row tiles: the persistent stream schedule; few: spread K over clusters
-    bool stream = row_tiles >= 2 * a.num_sms;
-    // WQ_QUANT_SCHEDULE=stream|cluster and WQ_QUANT_SPLIT=<n> pin the schedule and the CTAs
-    // per row tile of the cluster schedule (tuning and tests)
+    bool stream = (M + kRows - 1) / kRows >= 2 * num_sms;
+    // WQ_QUANT_SCHEDULE=stream|cluster pins the schedule (tuning and tests)
     if (const char* fm = std::getenv("WQ_QUANT_SCHEDULE")) {
         if (fm[0] == 's') stream = true;
         if (fm[0] == 'c') stream = false;
     }
+    return stream;
+}
+
+cudaError_t launch_quantize_act(const QuantArgs& a, cudaStream_t st) {
+    if (a.M <= 0) return cudaSuccess;
+    Choice ch = choose(a.K);
+    const int row_tiles = (a.M + kRows - 1) / kRows;
+    const bool stream = quant_stream_schedule(a.M, a.num_sms);
+    // WQ_QUANT_SPLIT=<n> pins the CTAs per row tile of the cluster schedule (tuning and tests)
     if (const char* fs = std::getenv("WQ_QUANT_SPLIT")) {
         const int v = std::atoi(fs);
         const int nblk = a.K / 64;
