@@ -396,7 +396,7 @@ __host__ __device__ inline SLayout make_stream_layout(int K, int r) {
     SLayout l{};
     const uint32_t nblk = static_cast<uint32_t>(K / 64);
     l.off_invs = kRing * kBoxBytes;                 // ring of raw boxes
-    l.off_omega = l.off_invs + 256u * nblk;         // all of inv_s
+    l.off_omega = l.off_invs + 256u * kRing;        // each ring slot's block of inv_s
     l.off_amax = l.off_omega + 16u * nblk;          // the Omega table
     l.off_upart = l.off_amax + 4u * kRows * kConsumerWarps;
     l.off_bar = l.off_upart + kConsumerWarps * static_cast<uint32_t>(r / 8) * 512u;
@@ -443,9 +443,8 @@ quantize_stream_kernel(const __grid_constant__ CUtensorMap tmX, const QParams p)
         if (lane == 0) {
             tma_prefetch_desc(&tmX);
             griddep_wait();
-            const uint32_t cbytes = (p.inv_s ? 256u * nblk : 0u) + (p.n_out ? 16u * nblk : 0u);
+            const uint32_t cbytes = p.n_out ? 16u * nblk : 0u;
             mbar_arrive_expect_tx(bar_const, cbytes);
-            if (p.inv_s) bulk_load(s_invs, p.inv_s, 256u * nblk, bar_const);
             if (p.n_out) bulk_load(base + lay.off_omega, p.omega_blk, 16u * nblk, bar_const);
             uint32_t q = 0;
             bool ok = true;
@@ -457,8 +456,10 @@ quantize_stream_kernel(const __grid_constant__ CUtensorMap tmX, const QParams p)
                             ok = false;
                             break;
                         }
-                        mbar_arrive_expect_tx(bar_full + 8u * s, kBoxBytes);
+                        // the box and the block's 64 inv_s values travel together
+                        mbar_arrive_expect_tx(bar_full + 8u * s, kBoxBytes + (p.inv_s ? 256u : 0u));
                         tma_load_2d(base + s * kBoxBytes, &tmX, kb * 64, tile * kRows, bar_full + 8u * s);
+                        if (p.inv_s) bulk_load(s_invs + 256u * s, p.inv_s + 64 * kb, 256u, bar_full + 8u * s);
                     }
             // every copy has landed before this CTA can finish
             for (uint32_t t = q > kRing ? q - kRing : 0u; t < q; ++t)
@@ -494,7 +495,7 @@ quantize_stream_kernel(const __grid_constant__ CUtensorMap tmX, const QParams p)
             QPH(0);
             const uint32_t box = base + s * kBoxBytes;
             f2 P[16];
-            load_transform(box, r, half, p.inv_s ? s_invs + static_cast<uint32_t>(kb) * 256u : 0u, p.rotate, P);
+            load_transform(box, r, half, p.inv_s ? s_invs + 256u * s : 0u, p.rotate, P);
             QPH(1);
             if constexpr (R > 0) u_step<NT>(box, lane, kb, p.pfrag, upart, kb == warp);
             QPH(2);
@@ -565,8 +566,7 @@ quantize_stream_kernel(const __grid_constant__ CUtensorMap tmX, const QParams p)
             }
             QPH(5);
             f2 P[16];
-            load_transform(base + s * kBoxBytes, r, half, p.inv_s ? s_invs + static_cast<uint32_t>(kb) * 256u : 0u,
-                           p.rotate, P);
+            load_transform(base + s * kBoxBytes, r, half, p.inv_s ? s_invs + 256u * s : 0u, p.rotate, P);
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_empty + 8u * s);
             QPH(6);
@@ -631,10 +631,10 @@ cudaError_t launch_r(const CUtensorMap& tm, const QParams& qp, bool stream, int 
                                                                       lay.total);
         if (e != cudaSuccess) return e;
         if (per_sm < 1) return cudaErrorInvalidConfiguration;
-        // a row tile is re-read from L2 by its second pass: keep the tiles in flight well
-        // inside the L2 (16 rows x K bf16 each)
-        const long long tile_bytes = 32ll * qp.K;
-        while (per_sm > 1 && static_cast<long long>(per_sm) * num_sms * tile_bytes > (96ll << 20)) --per_sm;
+        // Every resident CTA is used even when the row tiles in flight outgrow the L2 and part of
+        // the second pass comes from DRAM: the kernel is latency-bound with DRAM well below its
+        // peak, so more warps per SM pay more than the extra reads cost (K = 8960: 383 us at two
+        // CTAs per SM, 339 us at three).
         // WQ_QUANT_CTAS_PER_SM=<n> overrides the residency (tuning)
         if (const char* fc = std::getenv("WQ_QUANT_CTAS_PER_SM")) {
             const int v = std::atoi(fc);
