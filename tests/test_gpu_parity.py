@@ -226,10 +226,13 @@ def test_forward_parity_gemm_schedules(case, wide, monkeypatch):
                                         ("multi_tile_kstage_tail", 1), ("multi_tile_kstage_tail", 2),
                                         ("multi_tile_kstage_tail", 4), ("dit_r32_o64_ragged_n", 2),
                                         ("backbone_r0", 8), ("no_smooth_r64", 2), ("min_k64_n16_m1", 1)])
-def test_forward_parity_split_k(case, split, monkeypatch):
+@pytest.mark.parametrize("push", ["1", "0"])
+def test_forward_parity_split_k(case, split, push, monkeypatch):
     """Both GEMM schedules: one persistent CTA per tile (split 1) and the K range of a tile
-    spread over a cluster with the DSMEM reduction (split > 1)."""
+    spread over a cluster (split > 1), its rank-ordered reduction in both forms: partial rows
+    pushed into the reducing rank's shared memory, or pulled from every peer."""
     monkeypatch.setenv("WQ_GEMM_SPLIT", str(split))
+    monkeypatch.setenv("WQ_GEMM_PUSH", push)
     monkeypatch.setenv("WQ_FUSED", "0")
     L = layer(case)
     w = prep(L)

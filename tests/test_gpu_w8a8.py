@@ -68,8 +68,10 @@ def test_w8a8_codes_scales_and_output(case):
 
 
 @pytest.mark.parametrize("split", [1, 2, 8])
-def test_w8a8_split_k_schedules(split, monkeypatch):
+@pytest.mark.parametrize("push", ["1", "0"])
+def test_w8a8_split_k_schedules(split, push, monkeypatch):
     monkeypatch.setenv("WQ_GEMM_SPLIT", str(split))
+    monkeypatch.setenv("WQ_GEMM_PUSH", push)
     L = wl.make_layer_inputs("backbone", **CASES8["oproj_small"])
     w = prep8(L)
     y = wq.wq_linear_forward_w8a8(w, x_dev(L.x_bits))

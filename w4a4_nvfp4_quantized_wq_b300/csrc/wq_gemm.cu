@@ -20,10 +20,13 @@
 // (32 columns per ring stage) after that.
 //
 // Few output tiles (batch-1 shapes): the K range of one tile is split over a thread-block
-// cluster of `split` CTAs (2..16).  Each CTA accumulates its K slice in TMEM, writes
-// alpha * acc (rank 0 adds the side branch and bias) to its shared memory, and after a
-// cluster barrier every CTA reduces a slice of the tile's rows over all peers through
-// distributed shared memory, in rank order (deterministic), and stores bf16.
+// cluster of `split` CTAs (2..16).  Each CTA accumulates its K slice in TMEM and every CTA
+// reduces a slice of the tile's rows over all peers, in rank order (deterministic), and
+// stores bf16.  Push form (the default when the ring stages a CTA never fills can hold the
+// rows): each CTA stores each row of alpha * acc (rank 0 adds the side branch) straight into
+// the shared memory of the rank that reduces it, one slot per sender, and after one cluster
+// barrier the sums read local shared memory.  Pull form: each CTA keeps its partial and the
+// reducing ranks read every peer's through distributed shared memory between two barriers.
 //
 // kW8 = true runs the same pipeline on the selective 8-bit layers (FoldQuantVLA, Key
 // Contribution 3): int8 codes stored as bf16 (|q| <= 127 is exact in bf16, products are
@@ -84,6 +87,7 @@ struct KParams {
     int split;                       // CTAs per output tile (cluster x size); 1 = persistent
     __nv_bfloat16* y;                // output, written directly by the split-K reduction
     uint32_t u_bytes, xo_bytes, off_side, off_y, off_bar, sf_col;
+    uint32_t off_recv;               // split-K push form: receive slots (in unused ring stages); 0 = pull
     const uint8_t* sfa;
     const uint8_t* sfb;
     const float* gA;
@@ -120,6 +124,12 @@ __device__ __forceinline__ uint32_t swizzle_mode_for_row_bytes(uint32_t row_byte
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+__device__ __forceinline__ float4 lds_v4f(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr) : "memory");
+    return v;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -194,6 +204,11 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     }
     tc_fence_before();
     __syncthreads();
+    // push form: peers store into this CTA's shared memory only once every CTA of the cluster
+    // has started (this barrier is waited right before the first remote store)
+    const bool push = split && p.off_recv != 0u;
+    if (push) cluster_arrive();
+    bool start_waited = false;        // each thread waits on that barrier exactly once
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
     if (threadIdx.x == 0) WQ_TRACE_AT(1);
@@ -435,15 +450,37 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     }
                 }
                 if (split) {
-                    // fp32 partial of this CTA's K slice -> shared memory, rows swizzled by 16 B
+                    // fp32 partial of this CTA's K slice, rows swizzled by 16 B: pushed to the
+                    // slot (this rank, row) of the rank that reduces the row, or kept here
                     if (row < M) {
-                        const uint32_t prow = base + static_cast<uint32_t>(row_t) * 512u;
+                        if (push) {
+                            if (!start_waited) {
+                                cluster_wait();            // every CTA of the cluster has started
+                                start_waited = true;
+                            }
+                            const int valid = min(128, M - mb * 128);
+                            const int per = (valid + p.split - 1) / p.split;
+                            const int owner = row_t / per;
+                            const uint32_t drow = static_cast<uint32_t>(static_cast<int>(rank) * per + row_t - owner * per);
+                            const uint32_t prow = base + p.off_recv + drow * 512u;
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const uint32_t c4 = static_cast<uint32_t>(c0 / 4 + j);
-                            st_shared_v4f(prow + ((c4 ^ (static_cast<uint32_t>(row_t) & 7u)) << 4), v[4 * j],
-                                          v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                            for (int j = 0; j < 8; ++j) {
+                                const uint32_t c4 = static_cast<uint32_t>(c0 / 4 + j);
+                                st_dsmem_v4f(mapa_shared(prow + ((c4 ^ (drow & 7u)) << 4), static_cast<uint32_t>(owner)),
+                                             v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                            }
+                        } else {
+                            const uint32_t prow = base + static_cast<uint32_t>(row_t) * 512u;
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const uint32_t c4 = static_cast<uint32_t>(c0 / 4 + j);
+                                st_shared_v4f(prow + ((c4 ^ (static_cast<uint32_t>(row_t) & 7u)) << 4), v[4 * j],
+                                              v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                            }
                         }
+                    } else if (push && !start_waited) {
+                        cluster_wait();
+                        start_waited = true;
                     }
                 } else {
                     const uint32_t hb = ystage + static_cast<uint32_t>(lane) * 128u;
@@ -479,7 +516,8 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     }
 
     if (split) {
-        cluster_sync();                                // every partial of the cluster is in smem
+        if (push && !start_waited) cluster_wait();     // the start barrier, for every other thread
+        cluster_sync();                                // every partial of the cluster is in place
         if (threadIdx.x == 64) WQ_TRACE_AT(8);
         if (warp >= 2 && tile_first < tiles) {
             const int t = threadIdx.x - 64;             // 0 .. 255
@@ -491,14 +529,25 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             for (int it = t; it < (r1 - r0) * 32; it += 32 * kEpiWarps) {
                 const int row_t = r0 + it / 32;
                 const uint32_t c4 = static_cast<uint32_t>(it % 32);
-                const uint32_t off = base + static_cast<uint32_t>(row_t) * 512u +
-                                     ((c4 ^ (static_cast<uint32_t>(row_t) & 7u)) << 4);
-                // every peer's partial is requested before any is added, so the remote reads
-                // overlap; the sum is still taken in rank order
                 float4 pv[16];
+                if (push) {
+                    // the slots (sender qr, row) of this rank's receive area
 #pragma unroll
-                for (int qr = 0; qr < 16; ++qr)
-                    if (qr < p.split) pv[qr] = ld_dsmem_v4(mapa_shared(off, static_cast<uint32_t>(qr)));
+                    for (int qr = 0; qr < 16; ++qr)
+                        if (qr < p.split) {
+                            const uint32_t drow = static_cast<uint32_t>(qr * per + it / 32);
+                            pv[qr] = lds_v4f(base + p.off_recv + drow * 512u + ((c4 ^ (drow & 7u)) << 4));
+                        }
+                } else {
+                    // every peer's partial is requested before any is added, so the remote
+                    // reads overlap
+                    const uint32_t off = base + static_cast<uint32_t>(row_t) * 512u +
+                                         ((c4 ^ (static_cast<uint32_t>(row_t) & 7u)) << 4);
+#pragma unroll
+                    for (int qr = 0; qr < 16; ++qr)
+                        if (qr < p.split) pv[qr] = ld_dsmem_v4(mapa_shared(off, static_cast<uint32_t>(qr)));
+                }
+                // the sum is taken in rank order either way
                 float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                 for (int qr = 0; qr < 16; ++qr)
@@ -519,7 +568,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             }
         }
         if (threadIdx.x == 64) WQ_TRACE_AT(9);
-        cluster_sync();                                // peers are done reading this CTA's partial
+        if (!push) cluster_sync();                     // peers are done reading this CTA's partial
     }
     tc_fence_before();
     __syncthreads();
@@ -611,8 +660,22 @@ cudaError_t launch_gemm_t(const GemmArgs& a, cudaStream_t st) {
     const int num_kt = kW8 ? a.K / 64 : (a.K / 64 + 3) / 4;
     const int split = gemm_split<kW8>(a, pl);
     if (split > num_kt || split > 16 || (split & (split - 1))) return cudaErrorInvalidValue;
+    // split-K push form: the receive slots (per rows x split senders x 512 B) go in ring stages
+    // no CTA of the cluster fills; WQ_GEMM_PUSH=0 keeps the pull form (tests and tuning)
+    uint32_t off_recv = 0;
+    if (split > 1) {
+        const int valid = a.M < 128 ? a.M : 128;
+        const int per = (valid + split - 1) / split;
+        const int used = (num_kt + split - 1) / split;
+        const uint32_t need = static_cast<uint32_t>(per * split) * 512u;
+        if (used < pl.stages && static_cast<uint32_t>(pl.stages - used) * stage_bytes(kW8) >= need)
+            off_recv = static_cast<uint32_t>(used) * stage_bytes(kW8);
+        if (const char* fp = std::getenv("WQ_GEMM_PUSH"))
+            if (fp[0] == '0') off_recv = 0;
+    }
     KParams kp{};
     kp.split = split;
+    kp.off_recv = off_recv;
     kp.y = static_cast<__nv_bfloat16*>(a.y);
     kp.M = a.M; kp.N = a.N; kp.K = a.K; kp.r = a.r; kp.n_out = a.n_out; kp.stages = pl.stages;
     kp.u_bytes = pl.u_bytes; kp.xo_bytes = pl.xo_bytes; kp.off_side = pl.off_side; kp.off_y = pl.off_y;
