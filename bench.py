@@ -379,6 +379,10 @@ def run_wq(args):
     for h in H:
         wq.wq_check_device_error(h["w"])
 
+    # kernels this library launches per step: one per layer on the fused path, else two
+    launches_per_step = sum(1 if (h["L"].spec.mode != "w8a8" and wq.wq_forward_path(h["w"], M) == wq.WQ_PATH_FUSED)
+                            else 2 for h in H)
+
     # ---------------- timed region: exactly K steps
     K, W = args.steps, args.warmup
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
@@ -540,7 +544,7 @@ def run_wq(args):
             "roofline": roofline, "kernels": kernels,
             "cpu_baseline": cpu, "e2e": e2e,
             "clocks": sampler.record(),
-            "gpu_launches": 2 * len(H) * K,
+            "gpu_launches": launches_per_step * K,
             "wall_s_timed_region": wall,
         }
         print(json.dumps(line), flush=True)
