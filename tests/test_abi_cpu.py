@@ -89,3 +89,22 @@ def test_null_handle_calls_fail_cleanly():
     assert L.wq_quantize_activations(None, None, 4, 0, None, None, None, None, None, None) == wq.WQ_ERR_INVALID
     assert L.wq_export_weights(None, None, None, None, None, None, None) == wq.WQ_ERR_INVALID
     L.wq_free_weights(None)
+
+
+def test_path_queries_and_self_test_reject_bad_arguments():
+    """The host queries of the path a forward takes, and the wait self-test's output checks,
+    fail with status codes (and a message) before any device work."""
+    L = wq.lib()
+    for fn in (L.wq_forward_path, L.wq_gemm_schedule, L.wq_quant_schedule):
+        assert fn(None, 16) == wq.WQ_ERR_INVALID
+        assert wq.wq_last_error()
+    assert L.wq_selftest_wait_timeout(None, None, None) == wq.WQ_ERR_INVALID
+    assert "NULL" in wq.wq_last_error()
+
+
+def test_path_constants_match_the_header():
+    txt = open(os.path.join(ROOT, "include", "wq.h")).read()
+    defs = dict(re.findall(r"#define\s+(WQ_\w+)\s+(-?\d+)", txt))
+    for name in ("WQ_PATH_TWO_KERNEL", "WQ_PATH_FUSED", "WQ_GEMM_SINGLE", "WQ_GEMM_SPLITK", "WQ_GEMM_WIDE",
+                 "WQ_QUANT_CLUSTER", "WQ_QUANT_STREAM"):
+        assert int(defs[name]) == getattr(wq, name), name
