@@ -62,6 +62,16 @@ def test_conv3d_several_tiles_partial_n():
     run_case(2, 7, 24, 256, 48)
 
 
+def test_conv3d_two_column_tiles_partial():
+    """A work item with two column tiles, the second partial (C_out = 160)."""
+    run_case(2, 6, 16, 128, 160)
+
+
+def test_conv3d_column_groups_of_three_and_one():
+    """C_out = 512: four column tiles, split into a work item of three and one of one."""
+    run_case(2, 6, 16, 128, 512)
+
+
 def test_conv3d_vae_full_size_sampled():
     T, H, W = 5, 60, 104
     rng = np.random.default_rng(9)

@@ -9,11 +9,13 @@
 //   conv_amax_kernel   per-CTA maxima of |x| (the tensor scale's pre-pass)
 //   conv_quant_kernel  64-voxel x C tiles of the NCDHW input, transposed through shared
 //                      memory, quantised per voxel -> voxel-major codes [V, C/2], scales [V, C/16]
-//   conv_gemm_kernel   persistent tcgen05 GEMM: M = voxels, N = C_out, K = 27 C_in.  A stage is
-//                      128 channels of one tap.  Warps 2-5 gather the A rows (one output voxel
+//   conv_gemm_kernel   persistent tcgen05 GEMM: M = voxels, N = C_out, K = 27 C_in.  A work item
+//                      is 128 voxels by up to three 128-column tiles (three TMEM accumulators),
+//                      so every gathered A stage feeds the MMAs of all of them.  A stage is 128
+//                      channels of one tap.  Warps 2-5 gather the A rows (one output voxel
 //                      each) with cp.async -- zero-filled where the tap falls in the padding --
 //                      into the 64-byte-swizzled K-major layout and the scale atoms; warp 0
-//                      brings the weight tile by TMA; warp 1 issues tcgen05.cp + mxf4nvf4 MMAs;
+//                      brings the weight tiles by TMA; warp 1 issues tcgen05.cp + mxf4nvf4 MMAs;
 //                      warps 6-9 scale the TMEM accumulators and store bf16 NCDHW.
 #include <cuda_bf16.h>
 
@@ -28,7 +30,12 @@ constexpr int kAmaxThreads = 256;
 constexpr int kVox = 64;                      // voxels per quantiser tile
 constexpr int kConvThreads = 320;
 constexpr uint32_t kATile = 128 * 64;         // 128 rows x 64 bytes (128 fp4 channels)
-constexpr uint32_t kCStage = 2 * kATile + 4 * kSfAtom;
+constexpr int kGroup = 3;                     // column tiles per work item (TMEM accumulators)
+// stage: A tile, kGroup weight tiles, 2 A scale atoms, 2 scale atoms per weight tile
+constexpr uint32_t kCStage = (1 + kGroup) * kATile + 2 * (1 + kGroup) * kSfAtom;
+constexpr uint32_t kSfbOff = (1 + kGroup) * kATile + 2 * kSfAtom;
+constexpr uint32_t kSfCols = 8 * (1 + kGroup);   // TMEM scale columns per stage
+constexpr int kMaxStagesTmem = static_cast<int>((512 - 128 * kGroup) / kSfCols);
 constexpr int kGatherDepth = 2;               // stages of cp.async in flight per gather thread
 constexpr uint32_t kConvMaxSmem = 232448;
 
@@ -148,26 +155,31 @@ conv_gemm_kernel(const __grid_constant__ CUtensorMap tmB, const ConvParams p) {
     const uint32_t bar_full = base + off_bar;
     const uint32_t bar_empty = bar_full + 8u * S;
     const uint32_t bar_tfull = bar_empty + 8u * S;
-    const uint32_t bar_tempty = bar_tfull + 16u;
-    const uint32_t bar_final = bar_tempty + 16u;
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + off_bar + 8u * (2 * S + 5));
+    const uint32_t bar_tempty = bar_tfull + 8u;
+    const uint32_t bar_final = bar_tempty + 8u;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + off_bar + 8u * (2 * S + 3));
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
     const int n_tiles = (p.N + 127) / 128;
-    const int tiles = ((p.V + 127) / 128) * n_tiles;
+    const int n_groups = (n_tiles + kGroup - 1) / kGroup;
+    const int items = ((p.V + 127) / 128) * n_groups;
     const int cpt = p.C / 128;                      // stages per tap
-    const int nst = 27 * cpt;                       // stages per tile
+    const int nst = 27 * cpt;                       // stages per item
     const int num_kb = p.K / 64;
+    // work item -> row block and its column tiles [nb0, nb0 + ng)
+    auto item_rc = [&](int item, int& mb, int& nb0, int& ng) {
+        mb = item / n_groups;
+        nb0 = (item % n_groups) * kGroup;
+        ng = min(kGroup, n_tiles - nb0);
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(bar_full + 8u * s, 1 + 128);  // TMA arrival + one per gather thread
             mbar_init(bar_empty + 8u * s, 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(bar_tfull + 8u * b, 1);
-            mbar_init(bar_tempty + 8u * b, 4);
-        }
+        mbar_init(bar_tfull, 1);
+        mbar_init(bar_tempty, 4);
         mbar_init(bar_final, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -188,16 +200,19 @@ conv_gemm_kernel(const __grid_constant__ CUtensorMap tmB, const ConvParams p) {
             int stage = 0;
             uint32_t ph = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
-                const int nb = tile % n_tiles;
+            for (int item = blockIdx.x; item < items && ok; item += gridDim.x) {
+                int mb, nb0, ng;
+                item_rc(item, mb, nb0, ng);
                 for (int s = 0; s < nst; ++s) {
                     if (!mbar_wait(bar_empty + 8u * stage, ph ^ 1u, abort_flag, p.err, 21)) { ok = false; break; }
                     const uint32_t fb = bar_full + 8u * stage;
                     const uint32_t st = base + static_cast<uint32_t>(stage) * kCStage;
-                    mbar_arrive_expect_tx(fb, kATile + 2 * kSfAtom);
-                    tma_load_2d(st + kATile, &tmB, s * 64, nb * 128, fb);
-                    bulk_load(st + 2 * kATile + 2 * kSfAtom, p.sfb + (static_cast<size_t>(nb) * num_kb + 2 * s) * kSfAtom,
-                              2 * kSfAtom, fb);
+                    mbar_arrive_expect_tx(fb, static_cast<uint32_t>(ng) * (kATile + 2 * kSfAtom));
+                    for (int g = 0; g < ng; ++g) {
+                        tma_load_2d(st + static_cast<uint32_t>(1 + g) * kATile, &tmB, s * 64, (nb0 + g) * 128, fb);
+                        bulk_load(st + kSfbOff + static_cast<uint32_t>(2 * g) * kSfAtom,
+                                  p.sfb + (static_cast<size_t>(nb0 + g) * num_kb + 2 * s) * kSfAtom, 2 * kSfAtom, fb);
+                    }
                     if (++stage == S) { stage = 0; ph ^= 1u; }
                 }
             }
@@ -210,8 +225,9 @@ conv_gemm_kernel(const __grid_constant__ CUtensorMap tmB, const ConvParams p) {
         int pend[kGatherDepth + 1];
         int npend = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
-            const int mb = tile / n_tiles;
+        for (int item = blockIdx.x; item < items && ok; item += gridDim.x) {
+            int mb, nb0, ng;
+            item_rc(item, mb, nb0, ng);
             const int m = mb * 128 + r;
             const bool m_ok = m < p.V;
             const int d = m / (p.H * p.W), h = (m / p.W) % p.H, w = m % p.W;
@@ -230,7 +246,8 @@ conv_gemm_kernel(const __grid_constant__ CUtensorMap tmB, const ConvParams p) {
                     cp_async16(st + static_cast<uint32_t>(r) * 64u + ((static_cast<uint32_t>(j) ^ sw) << 4), src + 16 * j,
                                valid ? 16u : 0u);
                 const uint8_t* ssrc = p.xscales + vin * (p.C / 16) + cc * 8;
-                const uint32_t sfa = st + 2 * kATile + static_cast<uint32_t>(r % 32) * 16u + static_cast<uint32_t>(r / 32) * 4u;
+                const uint32_t sfa = st + (1 + kGroup) * kATile + static_cast<uint32_t>(r % 32) * 16u +
+                                     static_cast<uint32_t>(r / 32) * 4u;
                 cp_async4(sfa, ssrc, valid ? 4u : 0u);
                 cp_async4(sfa + kSfAtom, ssrc + 4, valid ? 4u : 0u);
                 cp_async_commit();
@@ -255,32 +272,39 @@ conv_gemm_kernel(const __grid_constant__ CUtensorMap tmB, const ConvParams p) {
             int stage = 0, tl = 0;
             uint32_t ph = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x, ++tl) {
-                const int buf = tl & 1;
-                const uint32_t aph = (static_cast<uint32_t>(tl) >> 1) & 1u;
-                if (!mbar_wait(bar_tempty + 8u * buf, aph ^ 1u, abort_flag, p.err, 23)) { ok = false; break; }
+            for (int item = blockIdx.x; item < items && ok; item += gridDim.x, ++tl) {
+                int mb, nb0, ng;
+                item_rc(item, mb, nb0, ng);
+                // one set of accumulators: the epilogue has drained the previous item
+                if (!mbar_wait(bar_tempty, (static_cast<uint32_t>(tl) & 1u) ^ 1u, abort_flag, p.err, 23)) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
-                const uint32_t d_acc = tmem + 128u * buf;
                 for (int s = 0; s < nst; ++s) {
                     if (!mbar_wait(bar_full + 8u * stage, ph, abort_flag, p.err, 24)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t st = base + static_cast<uint32_t>(stage) * kCStage;
-                    const uint32_t sf_t = tmem + 256u + 16u * stage;
+                    // scale slot of the stage: A at +4 kb, weight tile g at +8 + 8 g + 4 kb
+                    const uint32_t sf_t = tmem + 128u * kGroup + kSfCols * static_cast<uint32_t>(stage);
                     for (int kb = 0; kb < 2; ++kb) {
-                        tmem_cp_32x128b_x4(sf_t + 4u * kb, smem_desc(st + 2 * kATile + kSfAtom * kb, 0, 128, 0));
-                        tmem_cp_32x128b_x4(sf_t + 8u + 4u * kb,
-                                           smem_desc(st + 2 * kATile + 2 * kSfAtom + kSfAtom * kb, 0, 128, 0));
+                        tmem_cp_32x128b_x4(sf_t + 4u * kb, smem_desc(st + (1 + kGroup) * kATile + kSfAtom * kb, 0, 128, 0));
+                        for (int g = 0; g < ng; ++g)
+                            tmem_cp_32x128b_x4(sf_t + 8u + 8u * g + 4u * kb,
+                                               smem_desc(st + kSfbOff + kSfAtom * (2 * g + kb), 0, 128, 0));
                     }
                     const uint64_t ad = smem_desc(st, 16, 512, 4);            // 64-byte swizzle, 8-row groups
-                    const uint64_t bd = smem_desc(st + kATile, 16, 512, 4);
                     for (int kb = 0; kb < 2; ++kb)
-                        mma_nvf4(d_acc, ad + 2u * kb, bd + 2u * kb, idesc, sf_t + 4u * kb, sf_t + 8u + 4u * kb,
-                                 (s | kb) != 0 ? 1u : 0u);
+                        for (int g = 0; g < ng; ++g) {
+                            const uint64_t bd = smem_desc(st + static_cast<uint32_t>(1 + g) * kATile, 16, 512, 4);
+                            mma_nvf4(tmem + 128u * g, ad + 2u * kb, bd + 2u * kb, idesc, sf_t + 4u * kb,
+                                     sf_t + 8u + 8u * g + 4u * kb, (s | kb) != 0 ? 1u : 0u);
+                        }
                     tc_commit(bar_empty + 8u * stage);
                     if (++stage == S) { stage = 0; ph ^= 1u; }
                 }
                 if (!ok) break;
-                tc_commit(bar_tfull + 8u * buf);
+                tc_commit(bar_tfull);
             }
             tc_commit(bar_final);
             mbar_wait(bar_final, 0, abort_flag, p.err, 25);
@@ -291,29 +315,29 @@ conv_gemm_kernel(const __grid_constant__ CUtensorMap tmB, const ConvParams p) {
         const uint32_t t_lane = static_cast<uint32_t>(q * 32) << 16;
         const float alpha = __fmul_rn(__ldg(p.gx), p.gw);
         int tl = 0;
-        for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++tl) {
-            const int mb = tile / n_tiles, nb = tile % n_tiles;
-            const int buf = tl & 1;
-            const uint32_t aph = (static_cast<uint32_t>(tl) >> 1) & 1u;
-            if (!mbar_wait(bar_tfull + 8u * buf, aph, abort_flag, p.err, 26)) break;
+        for (int item = blockIdx.x; item < items; item += gridDim.x, ++tl) {
+            int mb, nb0, ng;
+            item_rc(item, mb, nb0, ng);
+            if (!mbar_wait(bar_tfull, static_cast<uint32_t>(tl) & 1u, abort_flag, p.err, 26)) break;
             tc_fence_after();
             const int m = mb * 128 + q * 32 + lane;
-            for (int ch = 0; ch < 4; ++ch) {
-                uint32_t acc[32];
-                tmem_ld_32x32b_x32(tmem + 128u * buf + 32u * ch + t_lane, acc);
-                tmem_wait_ld();
-                if (m < p.V) {
+            for (int g = 0; g < ng; ++g)
+                for (int ch = 0; ch < 4; ++ch) {
+                    uint32_t acc[32];
+                    tmem_ld_32x32b_x32(tmem + 128u * g + 32u * ch + t_lane, acc);
+                    tmem_wait_ld();
+                    if (m < p.V) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int n = nb * 128 + ch * 32 + i;
-                        if (n < p.N)
-                            p.y[static_cast<size_t>(n) * p.V + m] = __float2bfloat16_rn(alpha * __uint_as_float(acc[i]));
+                        for (int i = 0; i < 32; ++i) {
+                            const int n = (nb0 + g) * 128 + ch * 32 + i;
+                            if (n < p.N)
+                                p.y[static_cast<size_t>(n) * p.V + m] = __float2bfloat16_rn(alpha * __uint_as_float(acc[i]));
+                        }
                     }
                 }
-            }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_tempty + 8u * buf);
+            if (lane == 0) mbar_arrive(bar_tempty);
         }
     }
 
@@ -354,7 +378,9 @@ cudaError_t launch_conv_quant(const ConvArgs& a, cudaStream_t st) {
 
 cudaError_t launch_conv_gemm(const ConvArgs& a, cudaStream_t st) {
     int stages = static_cast<int>((kConvMaxSmem - 1024 - 256) / kCStage);
-    if (stages > 14) stages = 14;
+    if (stages > kMaxStagesTmem) stages = kMaxStagesTmem;   // scale slots beside the accumulators
+    // a gather thread holds kGatherDepth stages unsignalled while it waits for a free one
+    if (stages <= kGatherDepth + 1) return cudaErrorInvalidConfiguration;
     const size_t smem = static_cast<size_t>(stages) * kCStage + 256 + 1024;
     static bool attr = false;
     if (!attr) {
@@ -367,8 +393,9 @@ cudaError_t launch_conv_gemm(const ConvArgs& a, cudaStream_t st) {
     p.C = a.C; p.D = a.D; p.H = a.H; p.W = a.W; p.V = a.V; p.N = a.N; p.K = 27 * a.C; p.stages = stages;
     p.xcodes = a.codes; p.xscales = a.scales; p.gx = a.g; p.gw = a.gw; p.sfb = a.sfb;
     p.y = static_cast<__nv_bfloat16*>(a.y); p.err = a.err;
-    const int tiles = ((a.V + 127) / 128) * ((a.N + 127) / 128);
-    const int grid = tiles < a.num_sms ? tiles : a.num_sms;
+    const int n_tiles = (a.N + 127) / 128;
+    const int items = ((a.V + 127) / 128) * ((n_tiles + kGroup - 1) / kGroup);
+    const int grid = items < a.num_sms ? items : a.num_sms;
     conv_gemm_kernel<<<grid, kConvThreads, smem, st>>>(*a.tmB, p);
     return cudaGetLastError();
 }
