@@ -41,7 +41,11 @@
  * Parity pins (tests/test_oracle_pins.py): FWHT against the dense Sylvester
  * matrix, self-inverse and orthonormality; e2m1/e4m3 encoders exhaustively
  * against an independent IEEE ulp-grid rounding; round trips of representable
- * blocks; Proposition 1 folding invariance; reduction to a plain matmul.
+ * blocks; Proposition 1 folding invariance; reduction to a plain matmul;
+ * bf16 rounding of fp64 values and U = bf16(x P) against exact rational
+ * arithmetic rounded once (ties and their fp64 neighbours included); x_Omega
+ * against the dense Sylvester product on exactly transformable rows; the int8
+ * weight quantiser against numpy.
  */
 #include <math.h>
 #include <stdint.h>

@@ -376,3 +376,177 @@ def test_conv3d_single_voxel_impulse_gives_flipped_kernel():
         kd, kh, kw = 1 + 1 - d, 1 + 1 - h, 1 + 1 - ww       # input voxel (1,1,1) = output + k - 1
         ref = Wd[:, kd, kh, kw, :] @ X[13]
         np.testing.assert_allclose(y[v], ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+
+
+# ------------------------------------------------------------------ 16-bit roundings and side outputs
+# Independent single-rounding reference: exact rational arithmetic (fractions.Fraction),
+# round-half-even on the integer significand.  Shares nothing with the oracle's C code.
+from fractions import Fraction  # noqa: E402
+
+
+def _round_half_even(q: Fraction) -> int:
+    fl = q.numerator // q.denominator
+    rem = q - fl
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
+        fl += 1
+    return fl
+
+
+def _exact_bf16_bits(v) -> int:
+    """bf16 (8-bit significand, 8-bit exponent, subnormals down to 2^-133) nearest to the
+    exact value v (a Fraction or a float), ties to the even significand."""
+    neg = (v < 0) if isinstance(v, Fraction) else bool(np.signbit(v))
+    sign = 0x8000 if neg else 0
+    a = abs(Fraction(v))
+    if a == 0:
+        return sign
+    e = 0                                   # a = m 2^e with m in [1, 2)
+    while a >= 2 ** (e + 1):
+        e += 1
+    while a < Fraction(2) ** e:
+        e -= 1
+    q = max(e - 7, -133)                    # quantum of the significand (or of a subnormal)
+    n = _round_half_even(a / Fraction(2) ** q)
+    val = n * Fraction(2) ** q
+    if val >= Fraction(2) ** 128:            # beyond the largest finite: infinity
+        return sign | 0x7F80
+    bits = np.array([float(val)], np.float32).view(np.uint32)[0]
+    return sign | int(bits >> 16)
+
+
+def test_bf16_from_f64_single_rounding_on_values_not_in_fp32():
+    """orc_bf16_from_f64 rounds an fp64 value to bf16 ONCE.  The inputs are not fp32
+    values, and about half sit just beside a bf16 midpoint, where rounding through fp32
+    first (double rounding) gives the wrong neighbour."""
+    L = oracle.lib()
+    rng = np.random.default_rng(31)
+    vals = []
+    for _ in range(3000):
+        e = int(rng.integers(-120, 120))
+        sig = 1 + int(rng.integers(0, 128)) / 128 + 2.0 ** -8     # a bf16 midpoint
+        off = float(rng.choice([1, -1])) * 2.0 ** -int(rng.integers(25, 52))
+        vals.append(float(rng.choice([1, -1])) * (sig + off) * 2.0 ** e)
+    vals += list(rng.standard_normal(3000) * 10.0 ** rng.uniform(-35, 35, 3000))
+    vals += [1 + 2 ** -8 + 2 ** -52, 1 + 2 ** -8 - 2 ** -52, 1 + 2 ** -8, 1 + 3 * 2 ** -8,
+             2.0 ** -133 * 0.5000001, 2.0 ** -133 * 0.5, 2.0 ** -133 * 1.5, 2.0 ** -140, -0.0]
+    assert any(np.float64(np.float32(v)) != v for v in vals)
+    bad = [(v, L.orc_bf16_from_f64(v), _exact_bf16_bits(v)) for v in vals
+           if L.orc_bf16_from_f64(v) != _exact_bf16_bits(v)]
+    assert not bad, bad[:5]
+    # the pin distinguishes single from double rounding on these inputs
+    double = [v for v in vals if torch.tensor([v], dtype=torch.float64).float().bfloat16().view(torch.uint16).item()
+              != _exact_bf16_bits(v)]
+    assert len(double) > 500
+
+
+def test_lowrank_act_equals_exact_product_rounded_once():
+    """U = bf16(x P) (Q-WAM abstract, the 16-bit branch's down-projection): against the
+    exact rational x P, rounded once to bf16 by the independent routine above.  P is the
+    oracle's own bf16(L1 / s) factor, itself checked against torch's conversion."""
+    L = wlmod.make_layer_inputs("expert", M=6, K=128, N=32, rank=16)
+    wq = oracle.prepare_weights(L.W, L.s, L.L1, L.L2, None, True)
+    inv_s = (np.float32(1.0) / L.s).astype(np.float32)
+    P_ref = torch.from_numpy((L.L1 * inv_s[:, None]).astype(np.float32)).bfloat16().view(torch.uint16).numpy()
+    assert np.array_equal(wq.P, P_ref)
+    U = oracle.lowrank_act(L.x_bits, wq.P)
+    xf, Pf = wlmod.bf16_from_bits(L.x_bits), wlmod.bf16_from_bits(wq.P)
+    for m in range(L.M):
+        for j in range(16):
+            exact = sum(Fraction(float(a)) * Fraction(float(b)) for a, b in zip(xf[m], Pf[:, j]))
+            assert U[m, j] == _exact_bf16_bits(exact), (m, j)
+
+
+def test_lowrank_act_ties_and_neighbours():
+    """Rows built so that x P lands exactly on a bf16 midpoint, or one fp64 ulp beside it:
+    the midpoint goes to the even significand, the neighbours go their own way."""
+    K = 16
+    P = np.zeros((K, 2), np.float32)
+    P[:, 0] = 1.0
+    P[:3, 1] = [2.0, -1.0, 1.0]
+    Pb = wlmod.bf16_bits(P)
+    rows = [[1.0, 2.0 ** -8], [1.0, 2.0 ** -8, 2.0 ** -52], [1.0, 2.0 ** -8, -(2.0 ** -52)],
+            [1.0, 3 * 2.0 ** -8], [1.0, 3 * 2.0 ** -8, -(2.0 ** -52)], [-3.0, -(2.0 ** -7)]]
+    x = np.zeros((len(rows), K), np.float32)
+    for i, r in enumerate(rows):
+        x[i, :len(r)] = r
+    xb = wlmod.bf16_bits(x)
+    assert np.array_equal(wlmod.bf16_from_bits(xb), x)          # every entry is a bf16 value
+    U = oracle.lowrank_act(xb, Pb)
+    want0 = [_exact_bf16_bits(sum(Fraction(float(v)) for v in r)) for r in rows]
+    assert U[:, 0].tolist() == want0
+    # tie -> even: 1 + 2^-8 -> 1.0; the +ulp neighbour -> 1 + 2^-7; 1 + 3 2^-8 -> 1 + 2^-6
+    assert want0[:5] == [0x3F80, 0x3F81, 0x3F80, 0x3F82, 0x3F81]
+    want1 = [_exact_bf16_bits(sum(Fraction(float(v)) * Fraction(float(p)) for v, p in zip(x[i], P[:, 1])))
+             for i in range(len(rows))]
+    assert U[:, 1].tolist() == want1
+
+
+def test_outlier_slice_values_and_zeroed_codes():
+    """x_Omega (QuantWAMs sec. 3.1 Eq. (3), Fig. 1(d)): the fp16 values of the transformed
+    channels in Omega, taken before they are zeroed, in Omega's order; those channels then
+    quantise to code 0.  Inputs are small integers and powers-of-two smoothing, so the
+    block FWHT is exact and equals the dense Sylvester product computed by numpy."""
+    rng = np.random.default_rng(41)
+    M, K = 5, 256
+    x = rng.integers(-900, 900, (M, K)).astype(np.float32)
+    x[:, ::7] *= 8                                            # some larger channels
+    x = np.clip(x, -255 * 32, 255 * 32)
+    xb = wlmod.bf16_bits(x)
+    xf = wlmod.bf16_from_bits(xb).astype(np.float64)
+    s = (2.0 ** rng.integers(-2, 3, K)).astype(np.float32)
+    omega = np.sort(rng.choice(K, 24, replace=False)).astype(np.int32)
+    aq = oracle.quantize_act(xb, s, True, omega)
+    H = hadamard(64).astype(np.float64) / 8.0
+    xt = ((xf / s.astype(np.float64)).reshape(M, K // 64, 64) @ H).reshape(M, K)
+    want = xt[:, omega].astype(np.float16).view(np.uint16)
+    assert np.array_equal(aq.x_omega, want)
+    assert np.any(np.abs(xt[:, omega]) > 2048)                # values that round in fp16
+    codes = np.empty((M, K), np.uint8)
+    codes[:, 0::2] = aq.codes & 15
+    codes[:, 1::2] = aq.codes >> 4
+    assert not codes[:, omega].any()                          # kept channels: +0 codes
+    kept = np.ones(K, bool)
+    kept[omega] = False
+    assert codes[:, kept].any()
+
+
+def test_outlier_slice_on_random_rows_within_one_fp16_ulp():
+    """Same pin on Gaussian rows with real smoothing: the fp32 block transform differs from the
+    fp64 dense product by a few fp32 ulps, so x_Omega is at most one fp16 ulp from fp16 of the
+    dense value and equal to it almost everywhere."""
+    L = wlmod.make_layer_inputs("video_dit", M=64, K=512, N=16, rank=0, n_omega=32)
+    aq = oracle.quantize_act(L.x_bits, L.s, True, L.omega)
+    H = hadamard(64).astype(np.float64) / 8.0
+    xs = wlmod.bf16_from_bits(L.x_bits) * (np.float32(1.0) / L.s)
+    xt = (xs.astype(np.float64).reshape(64, 8, 64) @ H).reshape(64, 512)
+    want = xt[:, L.omega].astype(np.float16)
+    got = aq.x_omega.view(np.float16)
+    ulp = np.spacing(np.abs(want).astype(np.float16))
+    assert np.all(np.abs(got.astype(np.float64) - want.astype(np.float64)) <= ulp.astype(np.float64))
+    assert np.mean(got == want) > 0.99
+
+
+def test_int8_weight_quantiser_against_numpy():
+    """Per-output-column int8 of the folded weight (FoldQuantVLA, Key Contribution 3):
+    w[n] = fp32(amax_k |Rp[k, n]| / 127); q = clamp(round-half-even(fp32(Rp / w)), +-127)."""
+    rng = np.random.default_rng(43)
+    K, N = 192, 40
+    Rp = (rng.standard_normal((K, N)) * 10 ** rng.uniform(-3, 1, N)[None, :]).astype(np.float32)
+    Rp[:, 5] = 0.0
+    Rp[:, 7] = np.float32(1.0)
+    # entries exactly half-way between two integers after the division
+    Rp[::9, 11] = (np.arange(0, K, 9) % 50 + 0.5).astype(np.float32)
+    Rp[0, 11] = 127.0
+    q = np.zeros((N, K), np.int8)
+    w = np.zeros(N, np.float32)
+    L = oracle.lib()
+    L.orc_quantize_weights_int8(Rp.ctypes.data_as(ctypes.c_void_p), K, N, q.ctypes.data_as(ctypes.c_void_p),
+                                w.ctypes.data_as(ctypes.c_void_p))
+    w_ref = (np.abs(Rp).max(axis=0) / np.float32(127.0)).astype(np.float32)
+    assert np.array_equal(w, w_ref)
+    with np.errstate(invalid="ignore", divide="ignore"):
+        t = (Rp / w_ref[None, :]).astype(np.float32)
+    q_ref = np.where(w_ref[None, :] == 0, 0, np.clip(np.round(t.astype(np.float64)), -127, 127)).astype(np.int8).T
+    assert np.array_equal(q, q_ref)
+    assert q[11, 9] == 10 and q[11, 18] == 18                  # 9.5 -> 10, 18.5 -> 18 (ties to even)
+    assert not q[5].any() and np.all(q[7] == 127)
