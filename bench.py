@@ -1,13 +1,16 @@
 #!/usr/bin/env python
 """Benchmark of the W4A4 NVFP4 fused projection (one JSON line on rank 0).
 
-Default workload: the action-expert projections at batch 1 (M = 50 tokens; up
-1024 -> 4096 and down 4096 -> 1024; rank-32 low-rank branch; block-64 FWHT;
-eight outlier channels x20), seeded synthetic inputs.  A step is one pass of the
-whole hot path over the batch: for every layer the fused activation quantiser and
-the tcgen05 NVFP4 GEMM with its fused epilogue (two kernels per layer), replayed as
-one CUDA graph.  L2 is flushed (a 256 MiB write) before every timed step, outside
-the step's CUDA events, so weights and activations come from HBM.
+Default workload: the video diffusion-transformer block (M = 16384 tokens; QKV
+1536 -> 4608, o 1536 -> 1536, FFN up 1536 -> 8960 and down 8960 -> 1536; rank-32
+low-rank branch; the 64 highest-energy channels kept in fp16; block-64 FWHT;
+smoothing), the largest configuration of the workload set, on seeded synthetic
+inputs.  A step is one pass of the whole hot path over the batch: for every layer
+the fused activation quantiser and the tcgen05 NVFP4 GEMM with its fused epilogue
+(two kernels per layer), replayed as one CUDA graph.  L2 is flushed (a 256 MiB
+write) before every timed step, outside the step's CUDA events, so weights and
+activations come from HBM.  Other workloads: --workload expert | backbone |
+vae_conv | tiny.  --mma-peak prints the tensor-core issue-rate table instead.
 
 --impl reference times the CPU oracle (the slow, plain reference implementation)
 on the same workload, a bounded row sample per step, on the host cores.
@@ -48,15 +51,23 @@ WORKLOAD_TEXT = {
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=None, help="timed steps (default: by workload)")
+    ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", choices=["wq", "reference"], default="wq")
-    ap.add_argument("--workload", default="expert", choices=list(WORKLOAD_TEXT))
-    ap.add_argument("--kernel-iters", type=int, default=200)
+    ap.add_argument("--workload", default="video_dit", choices=list(WORKLOAD_TEXT))
+    ap.add_argument("--kernel-iters", type=int, default=None)
+    ap.add_argument("--mma-peak", action="store_true", help="tensor-core issue-rate table (one JSON line)")
     ap.add_argument("--cpu-baseline-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only-layer", default=None, help="run one named layer of the workload (profiling)")
-    return ap.parse_args()
+    a = ap.parse_args()
+    # defaults keep the timed region to seconds (a video-DiT step is ~1 ms, an expert step ~30 us)
+    d_steps, d_warm, d_iters = {"video_dit": (200, 10, 30), "vae_conv": (200, 10, 50), "backbone": (500, 20, 100),
+                                "expert": (2000, 50, 200), "tiny": (2000, 50, 200)}[a.workload]
+    a.steps = d_steps if a.steps is None else a.steps
+    a.warmup = d_warm if a.warmup is None else a.warmup
+    a.kernel_iters = d_iters if a.kernel_iters is None else a.kernel_iters
+    return a
 
 
 # ------------------------------------------------------------------ helpers
@@ -181,6 +192,48 @@ def measured_peaks():
     return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
 
 
+def fp4_peak_tflops(peaks):
+    """Dense FP4 tensor peak for the roofline: the measured bf16 burst peak times the nominal
+    fp4 : bf16 ratio (13.5 : 2.25 = 6), the rule for a contraction whose own dtype has no
+    measured peak."""
+    return peaks.get("bf16_tflops", 1800.0) * 6.0
+
+
+def kernel_roofline(flops, nbytes, ms, peaks):
+    """Roofline time of one launch = max(flops / P_fp4, bytes / HBM); bound = the larger term;
+    frac = roofline time / measured time."""
+    p4 = fp4_peak_tflops(peaks) * 1e12
+    hbm = peaks["hbm_gbs"] * 1e9
+    t_tensor = flops / p4 if flops else 0.0
+    t_hbm = nbytes / hbm
+    bound = "tensor" if t_tensor > t_hbm else "hbm"
+    t_roof = max(t_tensor, t_hbm)
+    return {"bound": bound, "roofline_us": 1e6 * t_roof, "measured_us": 1e3 * ms,
+            "frac": t_roof / (ms / 1e3) if ms > 0 else None}
+
+
+def queued_event_times(fn, iters, stream, flush, chunk=25, sleep_cycles=20_000_000):
+    """Device time of `fn`'s launches, each after an L2 flush, with CUDA events on the launching
+    stream.  Every chunk of launches is queued behind a device-side sleep, so the GPU never waits
+    for the host to enqueue the launch the start event precedes (host enqueue stays out of the
+    measured span).  Returns the per-launch times in ms."""
+    import torch
+    out = []
+    for c0 in range(0, iters, chunk):
+        n = min(chunk, iters - c0)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(sleep_cycles)
+            for i in range(n):
+                flush.zero_()
+                evs[i][0].record(stream)
+                fn()
+                evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        out += [a.elapsed_time(b) for a, b in evs]
+    return out
+
+
 def gemm_algorithmic_bytes(M, K, N, r, n_out, bias):
     """Bytes the fused GEMM must move once: fp4 codes + e4m3 scales of A and W, row scales,
     the 16-bit side operands, bias and the bf16 output."""
@@ -201,10 +254,10 @@ def quant8_algorithmic_bytes(M, K, smooth):
 
 
 def quant_algorithmic_bytes(M, K, r, n_out, smooth):
-    """Bytes of the activation quantiser: bf16 x in, fp4 codes + scales + row scale out,
-    the low-rank factor, U and x_O out."""
-    return 2 * M * K + M * K // 2 + M * K // 16 + 4 * M + 2 * K * r + 2 * M * r + 2 * M * n_out + \
-        (4 * K if smooth else 0)
+    """Bytes the activation quantiser must move: bf16 x in (2 B/elt); fp4 codes + e4m3 scales
+    (0.5625 B/elt) and the fp32 row scale (4 B/row) out; its 16-bit side outputs U and x_O out
+    (2 B per value).  The per-layer constants (inv_s, P) are left out."""
+    return 2 * M * K + M * K // 2 + M * K // 16 + 4 * M + 2 * M * r + 2 * M * n_out
 
 
 def kernel_source_hash():
@@ -417,9 +470,11 @@ def run_wq(args):
     flops_step = sum(2.0 * M * h["L"].spec.K * h["L"].spec.N for h in H)
     tflops = flops_step * K * ws / (total_ms / 1e3) / 1e12
 
-    # ---------------- per-kernel timing (roofline of the dominant kernel)
+    # ---------------- per-kernel timing and roofline (each launch alone, L2 flushed before it)
+    import ctypes
+    peaks, peak_kind = measured_peaks()
     iters = args.kernel_iters
-    per_kernel = {}
+    per_kernel = []
     for li, h in enumerate(H):
         L, w = h["L"], h["w"]
         w8 = L.spec.mode == "w8a8"
@@ -429,66 +484,67 @@ def run_wq(args):
         else:
             codes, sf, g, xo, u = wq.wq_quantize_activations(h["w"], h["x"], wq.WQ_SCALE_LAYOUT_MMA, stream)
         torch.cuda.synchronize()
-        for kname in ("quant", "gemm"):
-            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
-            with torch.cuda.stream(stream):
-                for i in range(iters + 3):
-                    flush.zero_()
-                    if i >= 3:
-                        evs[i - 3][0].record(stream)
-                    if kname == "quant" and w8:
-                        wq.lib().wq_quantize_activations_w8a8(
-                            __import__("ctypes").c_void_p(w.handle), __import__("ctypes").c_void_p(h["x"].data_ptr()),
-                            M, __import__("ctypes").c_void_p(codes.data_ptr()),
-                            __import__("ctypes").c_void_p(g.data_ptr()),
-                            __import__("ctypes").c_void_p(stream.cuda_stream))
-                    elif kname == "quant":
-                        wq.wq_quantize_activations_into(w, h["x"], codes, sf, g, xo, u, stream)
-                    else:
-                        wq.wq_linear_forward_quantized(w, codes, sf, g, u, xo, h["y"], stream)
-                    if i >= 3:
-                        evs[i - 3][1].record(stream)
-            torch.cuda.synchronize()
-            ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
-            spec = L.spec
+
+        def quant_fn(w=w, h=h, codes=codes, sf=sf, g=g, xo=xo, u=u, w8=w8):
+            if w8:
+                wq.lib().wq_quantize_activations_w8a8(ctypes.c_void_p(w.handle), ctypes.c_void_p(h["x"].data_ptr()),
+                                                      M, ctypes.c_void_p(codes.data_ptr()),
+                                                      ctypes.c_void_p(g.data_ptr()),
+                                                      ctypes.c_void_p(stream.cuda_stream))
+            else:
+                wq.wq_quantize_activations_into(w, h["x"], codes, sf, g, xo, u, stream)
+
+        def gemm_fn(w=w, h=h, codes=codes, sf=sf, g=g, xo=xo, u=u):
+            wq.wq_linear_forward_quantized(w, codes, sf, g, u, xo, h["y"], stream)
+
+        spec = L.spec
+        for kname, fn in (("quant", quant_fn), ("gemm", gemm_fn)):
+            fn()                                            # warm (tensor maps cached)
+            times = queued_event_times(fn, iters, stream, flush)
+            ms = statistics.median(times)
             if kname == "gemm":
                 byts = gemm8_algorithmic_bytes(M, spec.K, spec.N, L.bias is not None) if w8 else \
                     gemm_algorithmic_bytes(M, spec.K, spec.N, L.rank, L.omega.size, L.bias is not None)
                 flops = 2.0 * M * spec.K * spec.N
+                kern = ("wide_gemm_kernel" if wq.wq_gemm_schedule(w, M) == wq.WQ_GEMM_WIDE else "nvfp4_gemm_kernel")
             else:
                 byts = quant8_algorithmic_bytes(M, spec.K, L.s is not None) if w8 else \
                     quant_algorithmic_bytes(M, spec.K, L.rank, L.omega.size, L.s is not None)
                 flops = 0.0
-            if kname == "gemm":
-                kern = "wide_gemm_kernel" if wq.wq_gemm_schedule(w, M) == wq.WQ_GEMM_WIDE else "nvfp4_gemm_kernel"
-            else:
-                kern = "quantize_stream_kernel" if wq.wq_quant_schedule(w, M) == wq.WQ_QUANT_STREAM else "quantize_kernel"
-            per_kernel[(kname, li)] = dict(ms=ms, bytes=byts, flops=flops, kernel=kern)
-    tot = {k: sum(v["ms"] for (kk, _), v in per_kernel.items() if kk == k) for k in ("quant", "gemm")}
-    dom = max(tot, key=tot.get)
-    dom_ms = tot[dom]
-    dom_bytes = sum(v["bytes"] for (kk, _), v in per_kernel.items() if kk == dom)
-    dom_flops = sum(v["flops"] for (kk, _), v in per_kernel.items() if kk == dom)
-    peaks, peak_kind = measured_peaks()
-    n_launch = len(H)
-    hbm_achieved = dom_bytes / (dom_ms / 1e3) / 1e9
-    dom_kernel = "+".join(sorted({v["kernel"] for (kk, _), v in per_kernel.items() if kk == dom}))
-    roofline = {"kernel": dom_kernel,
-                "bound": "hbm", "achieved": hbm_achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": hbm_achieved / peaks["hbm_gbs"],
-                "traffic": profiled_traffic(dom_kernel, args.workload),
-                "peak_source": f"{peak_kind} HBM copy bandwidth",
-                "bytes_per_launch": dom_bytes / n_launch, "us_per_launch": 1e3 * dom_ms / n_launch,
-                "share_of_kernel_time": dom_ms / sum(tot.values())}
-    if dom == "gemm" and dom_flops:
-        fp4_peak = peaks.get("bf16_tflops", 1800.0) * 6.0   # nominal fp4 : bf16 dense ratio 13.5 : 2.25
-        achieved_tf = dom_flops / (dom_ms / 1e3) / 1e12
-        roofline["fp4_tensor"] = {"achieved": achieved_tf, "peak": fp4_peak, "unit": "TFLOP/s",
-                                  "frac": achieved_tf / fp4_peak,
-                                  "peak_source": f"{peak_kind} bf16 x 6 (nominal fp4:bf16 ratio)"}
-    kernels = {f"{k}[{wlw.layers[idx[li]].name}]": {"kernel": v["kernel"], "us": 1e3 * v["ms"], "bytes": v["bytes"],
-                                                   "GB/s": v["bytes"] / (v["ms"] / 1e3) / 1e9}
-               for (k, li), v in per_kernel.items()}
+                kern = ("quantize_stream_kernel" if wq.wq_quant_schedule(w, M) == wq.WQ_QUANT_STREAM
+                        else "quantize_kernel")
+            rl = kernel_roofline(flops, byts, ms, peaks)
+            per_kernel.append(dict(name=f"{kname}[{spec.name}]", kernel=kern, ms=ms, bytes=byts, flops=flops,
+                                   spread_us=[1e3 * min(times), 1e3 * max(times)], **rl))
+    dom = max(per_kernel, key=lambda k: k["ms"])
+    tot_ms = sum(k["ms"] for k in per_kernel)
+    if dom["bound"] == "tensor":
+        ach = dom["flops"] / (dom["ms"] / 1e3) / 1e12
+        peak, unit, src = fp4_peak_tflops(peaks), "TFLOP/s", \
+            f"{peak_kind} bf16 burst {peaks.get('bf16_tflops')} TFLOP/s x 6 (nominal fp4 : bf16 ratio)"
+    else:
+        ach = dom["bytes"] / (dom["ms"] / 1e3) / 1e9
+        peak, unit, src = peaks["hbm_gbs"], "GB/s", f"{peak_kind} HBM copy bandwidth"
+    try:
+        mb_tf, mb_ns, mb_mhz = wq.wq_mma_peak("fp4", 256, True, 0, 0, 8192, 0, False, 1)
+        microbench = {"tflops": mb_tf, "ns_per_mma": mb_ns, "sm_mhz": mb_mhz,
+                      "form": "tcgen05.mma.cta_group::2 kind::mxf4nvf4 M256 N256 K64, no scale copies"}
+    except Exception as exc:  # reported, not hidden
+        microbench = {"error": repr(exc)}
+    roofline = {"kernel": f"{dom['name']} {dom['kernel']}", "bound": dom["bound"], "achieved": ach, "peak": peak,
+                "unit": unit, "frac": ach / peak,
+                "traffic": profiled_traffic(dom["kernel"], args.workload),
+                "peak_source": src,
+                "bytes_per_launch": dom["bytes"], "flops_per_launch": dom["flops"],
+                "us_per_launch": 1e3 * dom["ms"], "share_of_kernel_time": dom["ms"] / tot_ms,
+                "step": {"roofline_us": sum(k["roofline_us"] for k in per_kernel), "measured_us": 1e3 * tot_ms,
+                         "frac": sum(k["roofline_us"] for k in per_kernel) / (1e3 * tot_ms)},
+                "fp4_mma_microbench": microbench}
+    kernels = {k["name"]: {"kernel": k["kernel"], "us": 1e3 * k["ms"], "min_max_us": k["spread_us"],
+                           "bytes": k["bytes"], "flops": k["flops"], "bound": k["bound"],
+                           "roofline_us": k["roofline_us"], "frac": k["frac"],
+                           "GB/s": k["bytes"] / (k["ms"] / 1e3) / 1e9,
+                           "TFLOP/s": k["flops"] / (k["ms"] / 1e3) / 1e12} for k in per_kernel}
 
     # ---------------- end to end through the host-buffer entry point
     e2e = None
@@ -572,7 +628,7 @@ def run_conv(args):
     hw = wq.wq_prepare_conv3d(w)
     x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).to(dev)
     y = torch.empty((1, N, D, H, W), dtype=torch.bfloat16, device=dev)
-    wsb = torch.empty(wq.wq_conv3d_workspace_bytes(hw, D, H, W), dtype=torch.uint8, device=dev)
+    wsb = torch.empty(wq.wq_conv3d_workspace_bytes(hw, 1, D, H, W), dtype=torch.uint8, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
@@ -606,44 +662,38 @@ def run_conv(args):
     total_ms = job_time_ms(float(sum(a.elapsed_time(b) for a, b in ev)), ws_, dev)
     flops = 2.0 * V * N * K
     # per-kernel: the quantiser pair alone, the whole forward; the GEMM is the difference
-    times = {}
-    for kname in ("quant", "forward"):
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.kernel_iters)]
-        codes = torch.empty((V, C // 2), dtype=torch.uint8, device=dev)
-        scales = torch.empty((V, C // 16), dtype=torch.uint8, device=dev)
-        gx = torch.empty(1, dtype=torch.float32, device=dev)
-        import ctypes
-        with torch.cuda.stream(stream):
-            for i in range(args.kernel_iters + 3):
-                flush.zero_()
-                if i >= 3:
-                    evs[i - 3][0].record(stream)
-                if kname == "quant":
-                    wq.lib().wq_quantize_conv3d_input(
-                        ctypes.c_void_p(hw.handle), ctypes.c_void_p(x.data_ptr()), D, H, W,
-                        ctypes.c_void_p(codes.data_ptr()), ctypes.c_void_p(scales.data_ptr()),
-                        ctypes.c_void_p(gx.data_ptr()), ctypes.c_void_p(wsb.data_ptr()), wsb.numel(),
-                        ctypes.c_void_p(stream.cuda_stream))
-                else:
-                    wq.wq_conv3d_forward(hw, x, y, wsb, stream)
-                if i >= 3:
-                    evs[i - 3][1].record(stream)
-        torch.cuda.synchronize()
-        times[kname] = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    import ctypes
+    codes = torch.empty((V, C // 2), dtype=torch.uint8, device=dev)
+    scales = torch.empty((V, C // 16), dtype=torch.uint8, device=dev)
+    gx = torch.empty(1, dtype=torch.float32, device=dev)
+
+    def quant_fn():
+        wq.lib().wq_quantize_conv3d_input(
+            ctypes.c_void_p(hw.handle), ctypes.c_void_p(x.data_ptr()), 1, D, H, W,
+            ctypes.c_void_p(codes.data_ptr()), ctypes.c_void_p(scales.data_ptr()),
+            ctypes.c_void_p(gx.data_ptr()), ctypes.c_void_p(wsb.data_ptr()), wsb.numel(),
+            ctypes.c_void_p(stream.cuda_stream))
+
+    def fwd_fn():
+        wq.wq_conv3d_forward(hw, x, y, wsb, stream)
+
+    times = {"quant": statistics.median(queued_event_times(quant_fn, args.kernel_iters, stream, flush)),
+             "forward": statistics.median(queued_event_times(fwd_fn, args.kernel_iters, stream, flush))}
     gemm_ms = times["forward"] - times["quant"]
     peaks, peak_kind = measured_peaks()
-    fp4_peak = peaks.get("bf16_tflops", 1800.0) * 6.0
+    fp4_peak = fp4_peak_tflops(peaks)
     ach = flops / (gemm_ms / 1e3) / 1e12
     qbytes = 2 * 2 * C * V + V * C // 2 + V * C // 16          # x read twice (maxima + quantiser), codes out
-    roofline = {"kernel": "conv_gemm_kernel", "bound": "tensor", "achieved": ach, "peak": fp4_peak,
+    gbytes = V * C // 2 + V * C // 16 + N * K // 2 + N * K // 16 + 2 * N * V   # codes in (once), weights, y out
+    rl = kernel_roofline(flops, gbytes, gemm_ms, peaks)
+    roofline = {"kernel": "conv_gemm_kernel", "bound": rl["bound"], "achieved": ach, "peak": fp4_peak,
                 "unit": "TFLOP/s", "frac": ach / fp4_peak, "traffic": profiled_traffic("conv_gemm_kernel", "vae_conv"),
-                "peak_source": f"{peak_kind} bf16 x 6 (nominal fp4:bf16 ratio)",
-                "flops_per_launch": flops, "us_per_launch": 1e3 * gemm_ms,
+                "peak_source": f"{peak_kind} bf16 burst {peaks.get('bf16_tflops')} TFLOP/s x 6 (nominal fp4 : bf16 ratio)",
+                "flops_per_launch": flops, "bytes_per_launch": gbytes, "us_per_launch": 1e3 * gemm_ms,
                 "share_of_kernel_time": gemm_ms / times["forward"]}
     kernels = {"conv_quant (maxima + quantiser)": {"us": 1e3 * times["quant"], "bytes": qbytes,
                                                     "GB/s": qbytes / (times["quant"] / 1e3) / 1e9},
-               "conv_gemm (forward - quantiser)": {"us": 1e3 * gemm_ms, "TFLOP/s": ach}}
+               "conv_gemm (forward - quantiser)": {"us": 1e3 * gemm_ms, "TFLOP/s": ach, **rl}}
     # end to end: pinned host x -> device, forward, y -> pinned host
     xh = x.cpu().pin_memory()
     yh = torch.empty(y.shape, dtype=torch.bfloat16).pin_memory()
@@ -692,9 +742,44 @@ def run_conv(args):
         print(json.dumps(line), flush=True)
 
 
+def run_mma_peak(args):
+    """Tensor-core issue rate of each instruction form the kernels use (one JSON line)."""
+    import torch
+    torch.cuda.set_device(0)
+    from w4a4_nvfp4_quantized_wq_b300 import build as wqbuild
+    wqbuild.build_library()
+    import w4a4_nvfp4_quantized_wq_b300 as wq
+    rows = []
+    # (kind, N, pair, copies per MMA, copy shape, feeder, zero operands, accumulators)
+    forms = [("fp4", 256, True, 0, 0, 0, 0, 1), ("fp4", 256, False, 0, 0, 0, 0, 1), ("fp4", 128, False, 0, 0, 0, 0, 1),
+             ("fp4", 128, True, 0, 0, 0, 0, 1), ("fp4", 192, False, 0, 0, 0, 0, 1), ("fp4", 64, False, 0, 0, 0, 0, 1),
+             ("bf16", 256, False, 0, 0, 0, 0, 1), ("bf16", 128, False, 0, 0, 0, 0, 1), ("bf16", 256, True, 0, 0, 0, 0, 1),
+             ("fp8", 256, False, 0, 0, 0, 0, 1), ("fp8", 256, True, 0, 0, 0, 0, 1),
+             ("fp4", 256, False, 0, 0, 0, 1, 1), ("fp8", 256, False, 0, 0, 0, 1, 1), ("bf16", 256, False, 0, 0, 0, 1, 1),
+             ("fp4", 128, False, 0, 0, 0, 0, 2), ("fp8", 256, False, 0, 0, 0, 0, 2), ("bf16", 256, False, 0, 0, 0, 0, 2),
+             ("fp4", 256, True, 3, 0, 0, 0, 1), ("fp4", 256, False, 1, 0, 0, 0, 1), ("fp4", 256, False, 3, 0, 0, 0, 1),
+             ("fp4", 256, False, 1, 1, 0, 0, 1), ("fp4", 256, True, 1, 1, 0, 0, 1),
+             ("fp4", 256, False, 1, 0, 1, 0, 1), ("fp4", 256, False, 3, 0, 1, 0, 1), ("fp4", 256, True, 3, 0, 1, 0, 1),
+             ("fp4", 256, False, 1, 0, 2, 0, 1), ("fp4", 256, False, 3, 0, 2, 0, 1)]
+    for kind, n, pair, copies, shape, feeder, zero, accs in forms:
+        best = None
+        for _ in range(3):
+            t, ns, mhz = wq.wq_mma_peak(kind, n, pair, copies, shape, 8192, feeder, zero, accs)
+            if best is None or t > best[0]:
+                best = (t, ns, mhz)
+        rows.append({"kind": kind, "M": 256 if pair else 128, "N": n, "cta_pair": pair, "copies_per_mma": copies,
+                     "copy_shape": ["32x128b.warpx4", "128x256b"][shape],
+                     "feeder": ["mma thread", "other warp", "tcgen05.st warps"][feeder], "zero_operands": bool(zero),
+                     "accumulators": accs, "tflops": best[0], "ns_per_mma": best[1], "sm_mhz": best[2]})
+    peaks, kind_ = measured_peaks()
+    print(json.dumps({"mma_peak": rows, "bf16_cublas_tflops": peaks.get("bf16_tflops"), "peaks": kind_}), flush=True)
+
+
 def main():
     args = parse_args()
-    if args.impl == "reference":
+    if args.mma_peak:
+        run_mma_peak(args)
+    elif args.impl == "reference":
         run_reference(args)
     elif args.workload == "vae_conv":
         run_conv(args)

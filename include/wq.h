@@ -35,9 +35,13 @@
  *   - Errors are returned as wq_status and never abort the process; wq_last_error()
  *     returns a thread-local message for the last failure.
  *   - NaN / Inf inputs are outside the contract.
- *   - Supported shapes: K % 64 == 0 and 64 <= K <= 16384; N % 16 == 0; rank in
- *     {0, 16, 32, 64}; n_outliers in {0, 16, 32, 64}; M >= 0 (M == 0 is a no-op).
- *     Anything else returns WQ_ERR_UNSUPPORTED.
+ *   - Supported shapes: K % 64 == 0 and 64 <= K <= 16384; N % 16 == 0; 0 <= rank <= 64;
+ *     0 <= n_outliers <= 64 (QuantWAMs sec. 4.2 keeps the top 2% of the input channels);
+ *     M >= 0 (M == 0 is a no-op).  Anything else returns WQ_ERR_UNSUPPORTED.
+ *   - Every launching entry point must be called with the handle's device current (the device
+ *     that was current at wq_prepare_*); otherwise it returns WQ_ERR_INVALID.
+ *   - A handle caches the tensor maps of the buffers it last saw; calls on one handle from
+ *     several host threads are serialised by the handle and are safe.
  */
 #ifndef WQ_H_
 #define WQ_H_
@@ -64,6 +68,14 @@ typedef enum wq_status {
 
 enum { WQ_MODE_W4A4 = 0, WQ_MODE_W8A8 = 1 };
 enum { WQ_SCALE_LAYOUT_ROWMAJOR = 0, WQ_SCALE_LAYOUT_MMA = 1 };
+/* Granularity of the activations' fp32 tensor scale g (4-bit layers):
+ *   ROW     one g per row, from that row's amax at run time (FoldQuantVLA, Key Contribution 2:
+ *           dynamic per-token quantisation; the default);
+ *   TENSOR  one g for the whole [M, K] batch, from its amax at run time (two quantiser launches:
+ *           the maximum, then the codes);
+ *   STATIC  one calibrated g (wq_config.act_gscale) fixed at preparation; one pass, no amax.
+ * g = amax / 2688 in the first two; the block scales and codes follow from g as in every mode. */
+enum { WQ_ACT_SCALE_ROW = 0, WQ_ACT_SCALE_TENSOR = 1, WQ_ACT_SCALE_STATIC = 2 };
 
 /* mode = WQ_MODE_W8A8 selects the selective 8-bit path (FoldQuantVLA, Key Contribution 3:
  * attention-output and FFN down projections kept at W8A8) in the same smoothed + rotated basis:
@@ -77,6 +89,8 @@ typedef struct wq_config {
     int n_outliers;   /* |Omega|, channels of the rotated basis kept in fp16 (0 disables)  */
     int rotate;       /* 1: block-64 Walsh-Hadamard rotation; 0: none                     */
     int mode;         /* WQ_MODE_W4A4 (wq_linear_forward) or WQ_MODE_W8A8 (..._w8a8)      */
+    int act_scale;    /* WQ_ACT_SCALE_* (4-bit layers; W8A8 takes WQ_ACT_SCALE_ROW)        */
+    float act_gscale; /* WQ_ACT_SCALE_STATIC: the calibrated g (> 0, finite); else ignored */
 } wq_config;
 
 /*
@@ -99,6 +113,14 @@ WQ_API wq_status wq_prepare_weights(const wq_config *cfg, const float *W, const 
 
 /* Copy the handle's configuration into *cfg (host). */
 WQ_API wq_status wq_get_config(wq_weights_t h, wq_config *cfg);
+
+/*
+ * Row strides (in elements) of the 16-bit side operands that wq_quantize_activations writes
+ * and wq_linear_forward_quantized reads: U is bf16 [M, *u_ld] and x_Omega fp16 [M, *xo_ld], where
+ * each stride is the configured count (rank, n_outliers) rounded up to 16, 32 or 64 (0 when the
+ * count is 0).  The columns beyond the count are written as zeros.  Host outputs; either may be NULL.
+ */
+WQ_API wq_status wq_side_strides(wq_weights_t h, int *u_ld, int *xo_ld);
 
 /*
  * Bytes of device scratch that wq_linear_forward needs for M rows (the quantised
@@ -149,6 +171,20 @@ WQ_API int wq_quant_schedule(wq_weights_t h, int M);
  */
 WQ_API int wq_gemm_schedule(wq_weights_t h, int M);
 
+/*
+ * Schedule knobs for tests and tuning (no counterpart on the pages; results never depend on them
+ * beyond the stated tolerances).  Each knob starts from the environment variable of the same name,
+ * read once at the library's first use, and afterwards changes only through this call.
+ *   "WQ_FUSED" 0/1; "WQ_GEMM_SPLIT" 0 (auto) or 1..16; "WQ_GEMM_WIDE" -1 (auto), 0, 1;
+ *   "WQ_GEMM_PUSH" -1 (auto) or 0 (pull form); "WQ_GEMM_STAGES" 0 (auto) or a ring depth;
+ *   "WQ_QUANT_SCHEDULE" -1 (auto), 0 (cluster), 1 (stream); "WQ_QUANT_SPLIT" 0 (auto) or 1..16;
+ *   "WQ_QUANT_CTAS_PER_SM" 0 (auto) or a count.
+ * Process-wide; takes effect for launches issued after it returns.  Returns WQ_ERR_INVALID for an
+ * unknown name.  wq_get_tuning returns the current value (or WQ_ERR_INVALID's value for an unknown name).
+ */
+WQ_API wq_status wq_set_tuning(const char *name, int value);
+WQ_API int wq_get_tuning(const char *name);
+
 /* Bytes of device scratch wq_linear_forward_host needs (workspace + x and y staging). */
 WQ_API size_t wq_host_workspace_bytes(wq_weights_t h, int M);
 
@@ -170,9 +206,13 @@ WQ_API wq_status wq_linear_forward_host(wq_weights_t h, const void *x_host, int 
  *           at offset (mb * K/64 + kb) * 512, row r of the 128-row block and 16-block j of
  *           the 64-block at byte (r % 32) * 16 + (r / 32) * 4 + j (the tcgen05
  *           block-scale layout the GEMM consumes).
- *   gscale  fp32 [M] per-row tensor scales.
- *   x_omega fp16 [M, n_outliers]; required when n_outliers > 0 (NULL otherwise).
- *   u       bf16 [M, rank] or NULL (not computed when NULL).
+ *   gscale  fp32 [M] tensor scales, one per row (equal in every row for WQ_ACT_SCALE_TENSOR and
+ *           WQ_ACT_SCALE_STATIC).
+ *   x_omega fp16 [M, xo_ld] (wq_side_strides); required when n_outliers > 0 (NULL otherwise).
+ *   u       bf16 [M, u_ld] (wq_side_strides) or NULL (not computed when NULL).
+ * For WQ_ACT_SCALE_TENSOR handles the batch maximum is gathered in a 4-byte device word owned by
+ * the handle, so two such calls on one handle must not overlap on the GPU (wq_linear_forward keeps
+ * that word in its workspace instead and has no such restriction).
  */
 WQ_API wq_status wq_quantize_activations(wq_weights_t h, const void *x, int M, int scale_layout,
                                          uint8_t *codes, uint8_t *scales, float *gscale,
@@ -211,38 +251,43 @@ WQ_API wq_status wq_quantize_activations_w8a8(wq_weights_t h, const void *x, int
 WQ_API wq_status wq_export_weights_w8a8(wq_weights_t h, int8_t *q, float *w);
 
 /*
- * The video VAE's 3x3x3 convolution, zero padding 1, batch 1, as an NVFP4 implicit GEMM
- * (LatentQuant, Abstract: NVFP4 execution of the Wan VAE).  The input is quantised once per
- * voxel along channels (16-channel blocks, e4m3 scales) with ONE fp32 scale for the whole
- * tensor (a GEMM row gathers 27 voxels, so a per-voxel scale would not factor out); no
- * smoothing or rotation.  The weight is NVFP4 per output channel along K = (kd, kh, kw, c_in)
- * with one fp32 scale per tensor.  y[n, v] = gx gw sum_{taps, c} A . W, bf16.
- *   w       host fp32 [C_out, C_in, 3, 3, 3];  C_in % 128 == 0, C_out % 16 == 0,
- *           27 C_in <= 16384.
+ * A video VAE's 3D convolution as an NVFP4 implicit GEMM (LatentQuant, Abstract: NVFP4 execution
+ * of the Wan VAE).  The input is quantised once per voxel along channels (16-channel blocks,
+ * e4m3 scales) with ONE fp32 scale for the whole [B, C_in, D, H, W] tensor (a GEMM row gathers
+ * 27 voxels, so a per-voxel scale would not factor out); no smoothing or rotation.  The weight
+ * is NVFP4 per output channel along K = (kd, kh, kw, c_in) with one fp32 scale per tensor.
+ * y[b, n, v] = gx gw sum_{taps, c} A . W, bf16, stride 1, zero padding `pad`.
+ *   w       host fp32 [C_out, C_in, kt, kh, kw];  C_in % 128 == 0, C_out % 16 == 0,
+ *           kt kh kw C_in <= 16384.
+ *   kt, kh, kw, pad  kernel extent and zero padding; the kernels implement the VAE's
+ *           3 x 3 x 3 with padding 1 (the "same" convolution of the decoder's residual
+ *           blocks) and return WQ_ERR_UNSUPPORTED for anything else.
  */
-WQ_API wq_status wq_prepare_conv3d(const float *w, int C_in, int C_out, void *stream, wq_weights_t *out);
+WQ_API wq_status wq_prepare_conv3d(const float *w, int C_in, int C_out, int kt, int kh, int kw, int pad,
+                                   void *stream, wq_weights_t *out);
 
-/* Device scratch for wq_conv3d_forward / wq_quantize_conv3d_input (D H W voxels). */
-WQ_API size_t wq_conv3d_workspace_bytes(wq_weights_t h, int D, int H, int W);
+/* Device scratch for wq_conv3d_forward / wq_quantize_conv3d_input (B D H W voxels). */
+WQ_API size_t wq_conv3d_workspace_bytes(wq_weights_t h, int B, int D, int H, int W);
 
 /*
- *   x  device bf16 NCDHW [1, C_in, D, H, W];  y  device bf16 NCDHW [1, C_out, D, H, W];
- *   D H W % 8 == 0.  Three kernels on `stream`: |x| maxima, the per-voxel quantiser, the
- *   implicit GEMM (A rows gathered per tap by cp.async, zero-filled in the padding).
+ *   x  device bf16 NCDHW [B, C_in, D, H, W];  y  device bf16 NCDHW [B, C_out, D, H, W];
+ *   B >= 1, D H W % 8 == 0.  Three kernels on `stream`: |x| maxima, the per-voxel quantiser,
+ *   the implicit GEMM (A rows gathered per tap by cp.async, zero-filled in the padding; taps
+ *   never cross from one sample of the batch into another).
  */
-WQ_API wq_status wq_conv3d_forward(wq_weights_t h, const void *x, int D, int H, int W, void *y,
+WQ_API wq_status wq_conv3d_forward(wq_weights_t h, const void *x, int B, int D, int H, int W, void *y,
                                    void *workspace, size_t workspace_bytes, void *stream);
 
 /* The conv input quantiser alone: codes [V, C_in/2], scales [V, C_in/16], g (one float),
- * all device; voxel v = (d H + h) W + w. */
-WQ_API wq_status wq_quantize_conv3d_input(wq_weights_t h, const void *x, int D, int H, int W,
+ * all device; V = B D H W voxels numbered v = b D H W + (d H + h) W + w. */
+WQ_API wq_status wq_quantize_conv3d_input(wq_weights_t h, const void *x, int B, int D, int H, int W,
                                           uint8_t *codes, uint8_t *scales, float *g,
                                           void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Copy the prepared weights back to host memory in canonical layouts (synchronous):
- *   codes uint8 [N, K/2]; scales e4m3 [N, K/16]; gW fp32 scalar; P bf16 [K, r];
- *   Q bf16 [r, N]; W_omega fp16 [n_outliers, N].  Any output may be NULL.
+ *   codes uint8 [N, K/2]; scales e4m3 [N, K/16]; gW fp32 scalar; P bf16 [K, rank];
+ *   Q bf16 [rank, N]; W_omega fp16 [n_outliers, N].  Any output may be NULL.
  */
 WQ_API wq_status wq_export_weights(wq_weights_t h, uint8_t *codes, uint8_t *scales, float *gW,
                                    uint16_t *P, uint16_t *Q, uint16_t *W_omega);
@@ -270,6 +315,29 @@ WQ_API wq_status wq_check_device_error(wq_weights_t h, void *stream);
  */
 WQ_API wq_status wq_selftest_wait_timeout(int *site, double *waited_ms, int *released);
 
+/*
+ * Tensor-core issue-rate microbenchmark (no counterpart on the pages; a measurement utility).
+ * On the current device, one thread per CTA (kind of MMA below) or per CTA pair issues `iters`
+ * dense tcgen05.mma instructions back to back on fixed shared-memory operands into one TMEM
+ * accumulator, with `copies` tcgen05.cp copies of scale atoms before each, on every SM at once,
+ * timed on the device.  Synchronous; allocates and frees a few bytes of device memory.
+ *   kind        0 = kind::mxf4nvf4 block-scaled e2m1 (K = 64 per instruction), 1 = kind::f16 bf16
+ *               (K = 16), 2 = kind::f8f6f4 e4m3 (K = 32)
+ *   n           N of the instruction, a multiple of 16 in [64, 256]; M = 128, or 256 with pair != 0
+ *   copies      0..3 copies per MMA; copy_shape 0 = 32x128b.warpx4 (512 B), 1 = 128x256b (4 KiB)
+ *   iters       1 .. 2^22 instructions per CTA
+ *   feeder      who issues the copies: 0 the MMA thread (ordered before each MMA); 1 another warp,
+ *               concurrently; 2 warps 1-3 write the same TMEM columns with tcgen05.st from registers
+ *               instead (single CTA, copy_shape 0 only)
+ *   zero_data   1: all-zero operands (0: a fixed pseudo-random pattern)
+ *   accs        1, or 2 accumulators alternated instruction by instruction (N <= 128 for kind 0)
+ *   tflops      host out: dense TFLOP/s summed over all SMs (2 M N K per instruction)
+ *   ns_per_mma  host out: mean ns per instruction;  sm_mhz  host out: mean SM clock during the run
+ * Returns WQ_ERR_INVALID for a bad argument, WQ_ERR_CUDA / WQ_ERR_TIMEOUT on a failed run.
+ */
+WQ_API wq_status wq_mma_peak(int kind, int n, int pair, int copies, int copy_shape, int iters, int feeder,
+                             int zero_data, int accs, double *tflops, double *ns_per_mma, double *sm_mhz);
+
 /* Release the handle and its device memory (synchronises the device first).  NULL is a no-op. */
 WQ_API void wq_free_weights(wq_weights_t h);
 
@@ -284,7 +352,7 @@ WQ_API void wq_free_weights(wq_weights_t h);
  * into the library; every GPU that loads the library holds it until the process exits.
  * The first call on a device looks up that array's device address (a one-time set-up);
  * make that first call before any stream capture.  All calls share the one array and it
- * keeps the last call's contents (nothing in it needs to start at zero), so calls whose
+ * keeps the last call's contents (what must start at zero, the call clears), so calls whose
  * kernels overlap on the GPU -- on different streams, or through different handles --
  * race with each other: serialise them.  A call whose scratch need
  * wq_workspace_bytes(h, M) exceeds WQ_NOALLOC_SCRATCH_BYTES returns WQ_ERR_UNSUPPORTED.

@@ -148,9 +148,10 @@ class ActQuant:
 
 def quantize_act(x_bits: np.ndarray, s: Optional[np.ndarray], rotate: bool,
                  omega: Optional[np.ndarray] = None, per_tensor: bool = False,
-                 keep_xt: bool = False, n_threads: int = 0) -> ActQuant:
+                 keep_xt: bool = False, n_threads: int = 0, static_g: Optional[float] = None) -> ActQuant:
     """Smoothing -> block FWHT -> outlier split -> NVFP4 (FoldQuantVLA contribution 2;
-    QuantWAMs sec. 3.1 Eq. (1))."""
+    QuantWAMs sec. 3.1 Eq. (1)).  Tensor scale: per row (default), one per batch from its
+    amax (per_tensor), or a fixed calibrated g (static_g)."""
     x_bits = _c(x_bits, np.uint16)
     M, K = x_bits.shape
     inv_s = inv_smoothing(s)
@@ -158,11 +159,17 @@ def quantize_act(x_bits: np.ndarray, s: Optional[np.ndarray], rotate: bool,
     no = int(omega.size)
     codes = np.zeros((M, K // 2), np.uint8)
     scales = np.zeros((M, K // 16), np.uint8)
-    g = np.zeros(1 if per_tensor else M, np.float32)
+    g = np.zeros(1 if (per_tensor or static_g is not None) else M, np.float32)
+    mode = 0
+    if static_g is not None:
+        g[0] = np.float32(static_g)
+        mode = 2
+    elif per_tensor:
+        mode = 1
     xo = np.zeros((M, no), np.uint16)
     xt = np.zeros((M, K), np.float32) if keep_xt else None
     rc = lib().orc_quantize_act(_p(x_bits), M, K, _p(inv_s), int(rotate), _p(omega), no,
-                                int(per_tensor), _p(codes), _p(scales), _p(g), _p(xo), _p(xt),
+                                mode, _p(codes), _p(scales), _p(g), _p(xo), _p(xt),
                                 int(n_threads))
     if rc:
         raise ValueError(f"orc_quantize_act failed: {rc}")
@@ -335,16 +342,27 @@ def conv_weight_matrix(w: np.ndarray) -> np.ndarray:
 
 def conv3d_reference(x_bits_ncdhw: np.ndarray, w: np.ndarray, vox: np.ndarray, n_threads: int = 0):
     """LatentQuant, Abstract (NVFP4 execution of the VAE): quantise the input once per voxel
-    (one tensor scale), the weight per output channel along (kd, kh, kw, c_in), and convolve
-    the dequantised values directly with zero padding 1.  Returns (y [n_vox, C_out] fp64,
-    activation ActQuant over voxels, weight WeightQuant)."""
-    _, C, D, H, W = x_bits_ncdhw.shape
-    xv = np.ascontiguousarray(x_bits_ncdhw.reshape(C, D * H * W).T)          # voxels x channels
+    (one tensor scale over the whole [B, C, D, H, W] input), the weight per output channel along
+    (kd, kh, kw, c_in), and convolve each sample's dequantised values directly with zero padding 1.
+    vox indexes voxels over the batch, v = b D H W + (d H + h) W + w.  Returns (y [n_vox, C_out]
+    fp64, activation ActQuant over all voxels, weight WeightQuant)."""
+    B, C, D, H, W = x_bits_ncdhw.shape
+    V1 = D * H * W
+    xv = np.ascontiguousarray(x_bits_ncdhw.reshape(B, C, V1).transpose(0, 2, 1).reshape(B * V1, C))
     aq = quantize_act(xv, None, False, None, per_tensor=True, n_threads=n_threads)
     wq = prepare_weights(conv_weight_matrix(w), None, None, None, None, False, n_threads)
     vox = np.ascontiguousarray(vox, dtype=np.int64)
     N = w.shape[0]
     y = np.zeros((vox.size, N), np.float64)
-    lib().orc_conv3d_forward(_p(aq.codes), _p(aq.scales), np.float32(aq.g[0]), C, D, H, W, _p(wq.codes),
-                             _p(wq.scales), np.float32(wq.gW), N, _p(vox), vox.size, _p(y), int(n_threads))
+    for b in range(B):
+        sel = np.flatnonzero(vox // V1 == b)
+        if sel.size == 0:
+            continue
+        local = np.ascontiguousarray(vox[sel] % V1, dtype=np.int64)
+        codes = np.ascontiguousarray(aq.codes[b * V1:(b + 1) * V1])
+        scales = np.ascontiguousarray(aq.scales[b * V1:(b + 1) * V1])
+        yb = np.zeros((sel.size, N), np.float64)
+        lib().orc_conv3d_forward(_p(codes), _p(scales), np.float32(aq.g[0]), C, D, H, W, _p(wq.codes),
+                                 _p(wq.scales), np.float32(wq.gW), N, _p(local), local.size, _p(yb), int(n_threads))
+        y[sel] = yb
     return y, aq, wq

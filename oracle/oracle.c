@@ -258,7 +258,9 @@ void orc_act_transform_row(const uint16_t *x_bf16, long K, const float *inv_s, i
 
 /* Quantise M activation rows.
  *   per_tensor == 0: one g per row (dynamic per-token); g[m] written for each row.
- *   per_tensor != 0: one g over all rows; g[0] written.
+ *   per_tensor == 1: one g over all rows from their amax; g[0] written.
+ *   per_tensor == 2: one fixed g for all rows, read from g[0] (a calibrated scale: the
+ *                    NVFP4 block scales stay dynamic, only the fp32 tensor scale is fixed).
  * x_omega (nullable when n_omega == 0): fp16 bits [M, n_omega] of the transformed
  * values at the outlier channels, which are then zeroed before quantisation.
  * xt_out (nullable): the transformed rows after the outlier split, fp32 [M, K]. */
@@ -285,7 +287,9 @@ int orc_quantize_act(const uint16_t *x_bf16, long M, long K, const float *inv_s,
         }
     }
     float gt = 0.0f;
-    if (per_tensor) {
+    if (per_tensor == 2) {
+        gt = g[0];
+    } else if (per_tensor) {
         float amax = 0.0f;
         for (long i = 0; i < M * K; ++i) {
             float a = fabsf(xt[i]);

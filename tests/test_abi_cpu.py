@@ -33,22 +33,29 @@ def test_library_exports_every_declared_symbol():
         assert hasattr(L, name), name
 
 
-def _cfg(K=256, N=128, r=0, no=0, rot=1, mode=0):
-    return wq.wq_config(K, N, r, no, rot, mode)
+def _cfg(K=256, N=128, r=0, no=0, rot=1, mode=0, act=0, g=0.0):
+    return wq.wq_config(K, N, r, no, rot, mode, act, g)
 
 
 @pytest.mark.parametrize("cfg,status", [
     (dict(K=100), wq.WQ_ERR_UNSUPPORTED),
     (dict(K=32768), wq.WQ_ERR_UNSUPPORTED),
     (dict(N=24), wq.WQ_ERR_UNSUPPORTED),
-    (dict(r=8), wq.WQ_ERR_UNSUPPORTED),
-    (dict(no=20), wq.WQ_ERR_UNSUPPORTED),
+    (dict(r=65), wq.WQ_ERR_UNSUPPORTED),
+    (dict(no=65), wq.WQ_ERR_UNSUPPORTED),
+    (dict(K=64, no=64, r=0), None),                      # accepted shape (checked below to succeed)
     (dict(mode=1, r=16), wq.WQ_ERR_UNSUPPORTED),
+    (dict(mode=1, act=1), wq.WQ_ERR_UNSUPPORTED),
     (dict(mode=2), wq.WQ_ERR_INVALID),
     (dict(rot=2), wq.WQ_ERR_INVALID),
     (dict(K=-64), wq.WQ_ERR_INVALID),
+    (dict(act=3), wq.WQ_ERR_INVALID),
+    (dict(act=2, g=0.0), wq.WQ_ERR_INVALID),
+    (dict(act=2, g=float("inf")), wq.WQ_ERR_INVALID),
 ])
 def test_prepare_rejects_bad_config(cfg, status):
+    if status is None:
+        pytest.skip("accepted configuration: preparing it needs a device")
     c = _cfg(**cfg)
     W = np.zeros((max(c.K, 1), max(c.N, 1)), np.float32)
     out = ctypes.c_void_p()
@@ -108,3 +115,46 @@ def test_path_constants_match_the_header():
     for name in ("WQ_PATH_TWO_KERNEL", "WQ_PATH_FUSED", "WQ_GEMM_SINGLE", "WQ_GEMM_SPLITK", "WQ_GEMM_WIDE",
                  "WQ_QUANT_CLUSTER", "WQ_QUANT_STREAM"):
         assert int(defs[name]) == getattr(wq, name), name
+
+
+def test_tuning_knobs_through_the_abi():
+    """Schedule knobs: the environment is read once, then wq_set_tuning alone changes them."""
+    L = wq.lib()
+    old = L.wq_get_tuning(b"WQ_QUANT_SPLIT")
+    assert L.wq_set_tuning(b"WQ_QUANT_SPLIT", 4) == wq.WQ_OK
+    assert L.wq_get_tuning(b"WQ_QUANT_SPLIT") == 4
+    os.environ["WQ_QUANT_SPLIT"] = "8"              # no longer read
+    try:
+        assert L.wq_get_tuning(b"WQ_QUANT_SPLIT") == 4
+    finally:
+        del os.environ["WQ_QUANT_SPLIT"]
+    assert L.wq_set_tuning(b"WQ_QUANT_SPLIT", old) == wq.WQ_OK
+    assert L.wq_set_tuning(b"WQ_NOT_A_KNOB", 1) == wq.WQ_ERR_INVALID
+    assert "unknown" in wq.wq_last_error()
+    assert L.wq_get_tuning(b"WQ_NOT_A_KNOB") == wq.WQ_ERR_INVALID
+    assert L.wq_set_tuning(None, 1) == wq.WQ_ERR_INVALID
+
+
+def test_new_entry_points_reject_bad_arguments_before_device_work():
+    L = wq.lib()
+    u, x = ctypes.c_int(7), ctypes.c_int(7)
+    assert L.wq_side_strides(None, ctypes.byref(u), ctypes.byref(x)) == wq.WQ_ERR_INVALID
+    assert L.wq_conv3d_workspace_bytes(None, 1, 8, 8, 8) == 0
+    d = ctypes.c_double()
+    for args in [(3, 256, 0, 0, 0, 16, 0, 0, 1), (0, 100, 0, 0, 0, 16, 0, 0, 1), (0, 256, 0, 4, 0, 16, 0, 0, 1),
+                 (0, 256, 0, 0, 2, 16, 0, 0, 1), (0, 256, 0, 0, 0, 0, 0, 0, 1), (0, 256, 0, 1, 0, 16, 3, 0, 1),
+                 (0, 256, 0, 1, 1, 16, 2, 0, 1), (0, 256, 0, 0, 0, 16, 0, 0, 2), (0, 128, 0, 0, 0, 16, 0, 0, 3)]:
+        assert L.wq_mma_peak(*args, ctypes.byref(d), ctypes.byref(d), ctypes.byref(d)) == wq.WQ_ERR_INVALID
+    w = np.zeros((16, 128, 3, 3, 3), np.float32)
+    out = ctypes.c_void_p()
+    vp = w.ctypes.data_as(ctypes.c_void_p)
+    assert L.wq_prepare_conv3d(vp, 128, 16, 1, 3, 3, 1, None, ctypes.byref(out)) == wq.WQ_ERR_UNSUPPORTED
+    assert L.wq_prepare_conv3d(vp, 128, 16, 3, 3, 3, 0, None, ctypes.byref(out)) == wq.WQ_ERR_UNSUPPORTED
+    assert L.wq_prepare_conv3d(vp, 128, 16, 3, 3, 3, -1, None, ctypes.byref(out)) == wq.WQ_ERR_INVALID
+    assert out.value is None
+
+
+def test_side_width_rule_in_the_binding_docs():
+    """The stored widths of U and x_Omega: counts rounded up to 16, 32 or 64."""
+    txt = open(os.path.join(ROOT, "include", "wq.h")).read()
+    assert "rounded up to 16, 32 or 64" in txt

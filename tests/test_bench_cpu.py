@@ -26,10 +26,9 @@ def test_w4a4_byte_counts_match_the_arrays(kw):
     U = oracle.lowrank_act(L.x_bits, o.P) if r else np.zeros((L.M, 0), np.uint16)
     x_omega = aq.x_omega if n_out else np.zeros((L.M, 0), np.uint16)
     W_omega = o.W_omega if n_out else np.zeros((0, L.spec.N), np.uint16)
-    inv_s = np.zeros(L.spec.K, np.float32) if smooth else np.zeros(0, np.float32)
-    # quantiser: x, P and inv_s in; codes, scales, row scales, U and x_O out
-    q_bytes = L.x_bits.nbytes + o.P.nbytes + inv_s.nbytes + aq.codes.nbytes + aq.scales.nbytes + aq.g.nbytes + \
-        U.nbytes + x_omega.nbytes
+    # quantiser: x in; codes, scales, row scales, U and x_O out (the per-layer constants P and
+    # inv_s are not counted)
+    q_bytes = L.x_bits.nbytes + aq.codes.nbytes + aq.scales.nbytes + aq.g.nbytes + U.nbytes + x_omega.nbytes
     assert bench.quant_algorithmic_bytes(L.M, L.spec.K, r, n_out, smooth) == q_bytes
     # GEMM: both operands with their scales, the row scales, the side operands, bias, y out
     y_bytes = L.M * L.spec.N * 2
@@ -64,3 +63,26 @@ def test_traffic_figure_is_used_only_for_the_code_it_measured(tmp_path, monkeypa
     assert bench.profiled_traffic("k", "w") == 123.0
     assert bench.profiled_traffic("old", "w") is None
     assert bench.profiled_traffic("missing", "w") is None
+
+
+def test_kernel_roofline_picks_the_binding_term():
+    """Roofline time of a launch = max(flops / P_fp4, bytes / HBM), P_fp4 = 6 x measured bf16."""
+    peaks = {"hbm_gbs": 1000.0, "bf16_tflops": 100.0}
+    assert bench.fp4_peak_tflops(peaks) == 600.0
+    r = bench.kernel_roofline(6e11, 1e6, 2.0, peaks)            # 1 ms of tensor time, 1 us of HBM time
+    assert r["bound"] == "tensor" and abs(r["roofline_us"] - 1000.0) < 1e-9 and abs(r["frac"] - 0.5) < 1e-12
+    r = bench.kernel_roofline(6e8, 1e9, 4.0, peaks)             # 1 us of tensor time, 1 ms of HBM time
+    assert r["bound"] == "hbm" and abs(r["roofline_us"] - 1000.0) < 1e-9 and abs(r["frac"] - 0.25) < 1e-12
+    r = bench.kernel_roofline(0.0, 2e6, 1.0, peaks)
+    assert r["bound"] == "hbm" and abs(r["frac"] - 0.002) < 1e-12
+
+
+def test_default_workload_is_the_largest_config():
+    import sys as _s
+    argv = _s.argv
+    try:
+        _s.argv = ["bench.py"]
+        a = bench.parse_args()
+    finally:
+        _s.argv = argv
+    assert a.workload == "video_dit" and a.warmup >= 3 and a.steps >= 1

@@ -76,7 +76,18 @@ CASES = {
     "no_smooth_r64": ("expert", dict(M=33, K=640, N=160, rank=64, smooth=False)),
     "min_k64_n16_m1": ("expert", dict(M=1, K=64, N=16, rank=0)),
     "multi_tile_kstage_tail": ("expert", dict(M=260, K=1088, N=400, rank=16)),
+    # QuantWAMs sec. 4.2 keeps the top 2% of the input channels: 41 of 2048; ranks that are not
+    # a side-MMA width (stored zero-padded to 16 / 32 / 64)
+    "top2pct_o41_r24": ("video_dit", dict(M=96, K=2048, N=256, rank=24, n_omega=41)),
+    "o5_r8": ("video_dit", dict(M=40, K=512, N=192, rank=8, n_omega=5)),
+    "o64_r40_no_rotate": ("video_dit", dict(M=150, K=1024, N=144, rank=40, n_omega=64, rotate=False)),
 }
+
+
+def side_out(t, count):
+    """The first `count` columns of a strided side output, and its padding (must be zero)."""
+    a = t.cpu().view(torch.int16).numpy().view(np.uint16)
+    return a[:, :count], a[:, count:]
 
 
 def layer(case):
@@ -112,13 +123,19 @@ def test_activation_quant_bitexact(case):
     M, K = L.x_bits.shape
     assert np.array_equal(wq.mma_scales_to_rowmajor(sf_mma.cpu().numpy(), M, K), aq.scales)
     assert np.array_equal(codes2.cpu().numpy(), aq.codes) and np.array_equal(g2.cpu().numpy(), aq.g)
+    check_side(L, xo, u, aq)
+
+
+def check_side(L, xo, u, aq):
+    """x_Omega bit-exact and U within its bound, in their strided layouts (padding zero)."""
     if L.omega.size:
-        assert np.array_equal(xo.cpu().view(torch.int16).numpy().view(np.uint16), aq.x_omega)
+        got, pad = side_out(xo, L.omega.size)
+        assert np.array_equal(got, aq.x_omega) and not pad.any()
     if L.rank:
         o = oracle.prepare_weights(L.W, L.s, L.L1, L.L2, L.omega, L.rotate)
         U = oracle.lowrank_act(L.x_bits, o.P)
-        ug = u.cpu().view(torch.int16).numpy().view(np.uint16)
-        assert u_close(ug, U, L.x_bits, o.P).all()
+        ug, pad = side_out(u, L.rank)
+        assert u_close(ug, U, L.x_bits, o.P).all() and not pad.any()
 
 
 @pytest.mark.parametrize("case,split", [("expert_small", 1), ("expert_small", 4), ("expert_small", 16),
@@ -126,11 +143,11 @@ def test_activation_quant_bitexact(case):
                                         ("dit_r32_o64_ragged_n", 8), ("no_smooth_r64", 1), ("no_smooth_r64", 5),
                                         ("backbone_r0", 2), ("multi_tile_kstage_tail", 3),
                                         ("multi_tile_kstage_tail", 16)])
-def test_activation_quant_split(case, split, monkeypatch):
+def test_activation_quant_split(case, split, tuning):
     """The quantiser with a row tile's K range on one CTA or spread over a cluster of 2..16
     CTAs, including sizes that split the blocks unevenly (the row amax and the low-rank
     partial sums then go through distributed shared memory)."""
-    monkeypatch.setenv("WQ_QUANT_SPLIT", str(split))
+    tuning("WQ_QUANT_SPLIT", str(split))
     L = layer(case)
     w = prep(L)
     x = x_dev(L.x_bits)
@@ -140,22 +157,16 @@ def test_activation_quant_split(case, split, monkeypatch):
     assert np.array_equal(g.cpu().numpy(), aq.g)
     assert np.array_equal(scales.cpu().numpy(), aq.scales)
     assert np.array_equal(codes.cpu().numpy(), aq.codes)
-    if L.omega.size:
-        assert np.array_equal(xo.cpu().view(torch.int16).numpy().view(np.uint16), aq.x_omega)
-    if L.rank:
-        o = oracle.prepare_weights(L.W, L.s, L.L1, L.L2, L.omega, L.rotate)
-        U = oracle.lowrank_act(L.x_bits, o.P)
-        ug = u.cpu().view(torch.int16).numpy().view(np.uint16)
-        assert u_close(ug, U, L.x_bits, o.P).all()
+    check_side(L, xo, u, aq)
 
 
 @pytest.mark.parametrize("case", list(CASES))
 @pytest.mark.parametrize("schedule", ["stream", "cluster"])
-def test_activation_quant_schedules(case, schedule, monkeypatch):
+def test_activation_quant_schedules(case, schedule, tuning):
     """Both quantiser schedules on every case: persistent CTAs that stream each row tile's
     blocks twice (the second pass recomputes the transform) and clusters that keep the
     transformed blocks resident."""
-    monkeypatch.setenv("WQ_QUANT_SCHEDULE", schedule)
+    tuning("WQ_QUANT_SCHEDULE", schedule)
     L = layer(case)
     w = prep(L)
     x = x_dev(L.x_bits)
@@ -166,13 +177,7 @@ def test_activation_quant_schedules(case, schedule, monkeypatch):
     assert np.array_equal(g.cpu().numpy(), aq.g)
     assert np.array_equal(wq.mma_scales_to_rowmajor(scales.cpu().numpy(), L.M, L.spec.K), aq.scales)
     assert np.array_equal(codes.cpu().numpy(), aq.codes)
-    if L.omega.size:
-        assert np.array_equal(xo.cpu().view(torch.int16).numpy().view(np.uint16), aq.x_omega)
-    if L.rank:
-        o = oracle.prepare_weights(L.W, L.s, L.L1, L.L2, L.omega, L.rotate)
-        U = oracle.lowrank_act(L.x_bits, o.P)
-        ug = u.cpu().view(torch.int16).numpy().view(np.uint16)
-        assert u_close(ug, U, L.x_bits, o.P).all()
+    check_side(L, xo, u, aq)
 
 
 @pytest.mark.parametrize("case", list(CASES))
@@ -187,15 +192,15 @@ def test_forward_parity(case):
 
 @pytest.mark.parametrize("case", list(CASES))
 @pytest.mark.parametrize("fused", ["1", "0"])
-def test_forward_parity_fused_and_two_kernel_paths(case, fused, monkeypatch):
+def test_forward_parity_fused_and_two_kernel_paths(case, fused, tuning):
     """With WQ_FUSED=1, small batches (M <= 64, rank <= 32, K % 128 == 0) run quantiser and
     GEMM fused in one cluster kernel (codes built in shared memory, row maxima and U partials
     across the cluster, split-K partials summed in rank order); WQ_FUSED=0 keeps the
     two-kernel path on the same case.  The path actually taken is checked first."""
-    monkeypatch.setenv("WQ_FUSED", fused)
+    tuning("WQ_FUSED", fused)
     L = layer(case)
     w = prep(L)
-    eligible = L.M <= 64 and L.rank in (0, 16, 32) and L.spec.K % 128 == 0
+    eligible = L.M <= 64 and L.rank <= 32 and L.spec.K % 128 == 0
     expected = wq.WQ_PATH_FUSED if fused == "1" and eligible else wq.WQ_PATH_TWO_KERNEL
     assert wq.wq_forward_path(w, L.M) == expected
     y = wq.wq_linear_forward(w, x_dev(L.x_bits))
@@ -206,12 +211,12 @@ def test_forward_parity_fused_and_two_kernel_paths(case, fused, monkeypatch):
 
 @pytest.mark.parametrize("case", list(CASES))
 @pytest.mark.parametrize("wide", ["1", "0"])
-def test_forward_parity_gemm_schedules(case, wide, monkeypatch):
+def test_forward_parity_gemm_schedules(case, wide, tuning):
     """Both GEMM schedules on every case: 256 x 256 tiles on CTA pairs (tcgen05 cta_group::2,
     single-buffered accumulator, side branch computed into the drained accumulator) and
     128 x 128 tiles on single CTAs; partial tiles in M and N included."""
-    monkeypatch.setenv("WQ_GEMM_WIDE", wide)
-    monkeypatch.setenv("WQ_FUSED", "0")              # small batches too run the GEMM under test
+    tuning("WQ_GEMM_WIDE", wide)
+    tuning("WQ_FUSED", "0")              # small batches too run the GEMM under test
     L = layer(case)
     w = prep(L)
     sched = wq.wq_gemm_schedule(w, L.M)
@@ -227,13 +232,13 @@ def test_forward_parity_gemm_schedules(case, wide, monkeypatch):
                                         ("multi_tile_kstage_tail", 4), ("dit_r32_o64_ragged_n", 2),
                                         ("backbone_r0", 8), ("no_smooth_r64", 2), ("min_k64_n16_m1", 1)])
 @pytest.mark.parametrize("push", ["1", "0"])
-def test_forward_parity_split_k(case, split, push, monkeypatch):
+def test_forward_parity_split_k(case, split, push, tuning):
     """Both GEMM schedules: one persistent CTA per tile (split 1) and the K range of a tile
     spread over a cluster (split > 1), its rank-ordered reduction in both forms: partial rows
     pushed into the reducing rank's shared memory, or pulled from every peer."""
-    monkeypatch.setenv("WQ_GEMM_SPLIT", str(split))
-    monkeypatch.setenv("WQ_GEMM_PUSH", push)
-    monkeypatch.setenv("WQ_FUSED", "0")
+    tuning("WQ_GEMM_SPLIT", str(split))
+    tuning("WQ_GEMM_PUSH", push)
+    tuning("WQ_FUSED", "0")
     L = layer(case)
     w = prep(L)
     y = wq.wq_linear_forward(w, x_dev(L.x_bits))
@@ -323,11 +328,11 @@ def _e4m3_midpoints():
 
 
 @pytest.mark.parametrize("schedule", ["stream", "cluster"])
-def test_scale_ties_through_the_quantiser(schedule, monkeypatch):
+def test_scale_ties_through_the_quantiser(schedule, tuning):
     """Block maxima at 6 x every e4m3 midpoint (and one bf16 step either side) in rows with
     g = 1: (bmax / 6) / g lands exactly on the scale's rounding boundaries, where the fast
     reciprocal path has to hand over to the exact divisions."""
-    monkeypatch.setenv("WQ_QUANT_SCHEDULE", schedule)
+    tuning("WQ_QUANT_SCHEDULE", schedule)
     K = 512
     targets = []
     for mid in _e4m3_midpoints():
@@ -362,6 +367,18 @@ def _sampled_rows(M, n, seed):
     return np.sort(np.random.default_rng(seed).choice(M, size=n, replace=False))
 
 
+def _tile_rows(M, seed):
+    """One row in every 128-row GEMM tile (a seeded position inside it), the first and the last
+    row of the batch, and the last row of each 256-row pair tile."""
+    rng = np.random.default_rng(seed)
+    rows = {0, M - 1}
+    for t in range(0, M, 128):
+        rows.add(t + int(rng.integers(0, min(128, M - t))))
+    for t in range(255, M, 256):
+        rows.add(t)
+    return np.array(sorted(rows))
+
+
 @pytest.mark.parametrize("layer_idx", [0, 1])
 def test_expert_batch1_full_size(layer_idx):
     L = wl.make_layer_inputs("expert", layer=layer_idx)
@@ -374,31 +391,92 @@ def test_expert_batch1_full_size(layer_idx):
 
 @pytest.mark.parametrize("wl_name,layer_idx", [("video_dit", 0), ("video_dit", 1), ("video_dit", 2),
                                                ("video_dit", 3), ("backbone", 0), ("backbone", 2)])
-def test_full_size_sampled_rows(wl_name, layer_idx):
+def test_full_size_every_row_and_tile(wl_name, layer_idx):
+    """Full workload sizes in the launch configuration the benchmark times: codes, scales, row
+    scales and x_Omega of EVERY row bit-exact against the oracle's quantiser (both quantiser
+    schedules agree with it), and y on one row of every 128-row tile (plus the batch's first and
+    last rows and the last row of every pair tile) within tolerance."""
     L = wl.make_layer_inputs(wl_name, layer=layer_idx)
     w = prep(L)
     x = x_dev(L.x_bits)
     y = wq.wq_linear_forward(w, x)
     codes, scales, g, xo, _ = wq.wq_quantize_activations(w, x)
     wq.wq_check_device_error(w)
-    rows = _sampled_rows(L.M, 24, 100 + layer_idx)
-    y_ref, aq, _, _ = oracle.reference_forward(L, rows=rows)
-    assert np.array_equal(codes.cpu().numpy()[rows], aq.codes)
-    assert np.array_equal(scales.cpu().numpy()[rows], aq.scales)
-    assert np.array_equal(g.cpu().numpy()[rows], aq.g)
+    aq = oracle.quantize_act(L.x_bits, L.s, L.rotate, L.omega)
+    assert np.array_equal(g.cpu().numpy(), aq.g)
+    assert np.array_equal(scales.cpu().numpy(), aq.scales)
+    assert np.array_equal(codes.cpu().numpy(), aq.codes)
+    if L.omega.size:
+        got, pad = side_out(xo, L.omega.size)
+        assert np.array_equal(got, aq.x_omega) and not pad.any()
+    rows = _tile_rows(L.M, 100 + layer_idx)
+    y_ref, *_ = oracle.reference_forward(L, rows=rows)
     assert_y_close(L, y[torch.from_numpy(rows).cuda()], y_ref, rows)
 
 
 @pytest.mark.parametrize("wide", ["1", "0"])
-def test_full_size_long_k_both_gemm_schedules(wide, monkeypatch):
+def test_full_size_long_k_both_gemm_schedules(wide, tuning):
     """The video-DiT down projection (M = 16384, K = 8960) on the CTA-pair schedule (its
     default) and on the single-CTA schedule, at full size, on sampled rows."""
-    monkeypatch.setenv("WQ_GEMM_WIDE", wide)
+    tuning("WQ_GEMM_WIDE", wide)
     L = wl.make_layer_inputs("video_dit", layer=3)
     w = prep(L)
     assert (wq.wq_gemm_schedule(w, L.M) == wq.WQ_GEMM_WIDE) == (wide == "1")
     y = wq.wq_linear_forward(w, x_dev(L.x_bits))
     wq.wq_check_device_error(w)
-    rows = _sampled_rows(L.M, 16, 300)
+    rows = _tile_rows(L.M, 300)
     y_ref, *_ = oracle.reference_forward(L, rows=rows)
     assert_y_close(L, y[torch.from_numpy(rows).cuda()], y_ref, rows)
+
+
+# ------------------------------------------------------------------ batch-wide tensor scales
+ACT_CASES = ["expert_small", "dit_r32_o64_ragged_n", "top2pct_o41_r24", "multi_tile_kstage_tail"]
+
+
+@pytest.mark.parametrize("case", ACT_CASES)
+@pytest.mark.parametrize("mode", ["tensor", "static"])
+def test_batch_tensor_scale_modes(case, mode):
+    """WQ_ACT_SCALE_TENSOR (one g from the whole batch's amax, two quantiser launches) and
+    WQ_ACT_SCALE_STATIC (a calibrated g, one pass): codes, scales and g bit-exact against the
+    oracle's per-tensor and fixed-g modes, x_Omega and U as in the per-row mode, y within
+    tolerance of the oracle forward with that g."""
+    L = layer(case)
+    if mode == "static":
+        # a calibrated g: the amax of a different batch of the same distribution, / 2688
+        cal = wl.make_layer_inputs(CASES[case][0], **dict(CASES[case][1], M=64))
+        ref = oracle.quantize_act(cal.x_bits, L.s, L.rotate, L.omega, per_tensor=True)
+        g_cal = float(ref.g[0])
+        w = wq.wq_prepare_weights(L.spec.K, L.spec.N, L.W, L.bias, L.s, L.L1, L.L2,
+                                  L.omega if L.omega.size else None, rotate=L.rotate,
+                                  act_scale=wq.WQ_ACT_SCALE_STATIC, act_gscale=g_cal)
+        aq = oracle.quantize_act(L.x_bits, L.s, L.rotate, L.omega, static_g=g_cal)
+    else:
+        w = wq.wq_prepare_weights(L.spec.K, L.spec.N, L.W, L.bias, L.s, L.L1, L.L2,
+                                  L.omega if L.omega.size else None, rotate=L.rotate,
+                                  act_scale=wq.WQ_ACT_SCALE_TENSOR)
+        aq = oracle.quantize_act(L.x_bits, L.s, L.rotate, L.omega, per_tensor=True)
+    x = x_dev(L.x_bits)
+    codes, scales, g, xo, u = wq.wq_quantize_activations(w, x)
+    y = wq.wq_linear_forward(w, x)
+    torch.cuda.synchronize()
+    wq.wq_check_device_error(w)
+    assert np.all(g.cpu().numpy() == aq.g[0])
+    assert np.array_equal(scales.cpu().numpy(), aq.scales)
+    assert np.array_equal(codes.cpu().numpy(), aq.codes)
+    check_side(L, xo, u, aq)
+    wqo = oracle.prepare_weights(L.W, L.s, L.L1, L.L2, L.omega, L.rotate)
+    U = oracle.lowrank_act(L.x_bits, wqo.P) if L.rank else None
+    y_ref = oracle.linear_forward(aq, wqo, U, L.bias, per_tensor_act=True)
+    assert_y_close(L, y, y_ref)
+
+
+def test_side_strides_and_tuning_roundtrip():
+    L = layer("top2pct_o41_r24")
+    w = prep(L)
+    assert wq.wq_side_strides(w) == (32, 64)
+    old = wq.wq_get_tuning("WQ_GEMM_WIDE")
+    wq.wq_set_tuning("WQ_GEMM_WIDE", 1)
+    assert wq.wq_get_tuning("WQ_GEMM_WIDE") == 1
+    wq.wq_set_tuning("WQ_GEMM_WIDE", old)
+    with pytest.raises(wq.WqError):
+        wq.wq_set_tuning("WQ_NO_SUCH_KNOB", 1)

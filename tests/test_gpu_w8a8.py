@@ -69,9 +69,9 @@ def test_w8a8_codes_scales_and_output(case):
 
 @pytest.mark.parametrize("split", [1, 2, 8])
 @pytest.mark.parametrize("push", ["1", "0"])
-def test_w8a8_split_k_schedules(split, push, monkeypatch):
-    monkeypatch.setenv("WQ_GEMM_SPLIT", str(split))
-    monkeypatch.setenv("WQ_GEMM_PUSH", push)
+def test_w8a8_split_k_schedules(split, push, tuning):
+    tuning("WQ_GEMM_SPLIT", str(split))
+    tuning("WQ_GEMM_PUSH", push)
     L = wl.make_layer_inputs("backbone", **CASES8["oproj_small"])
     w = prep8(L)
     y = wq.wq_linear_forward_w8a8(w, x_dev(L.x_bits))
@@ -80,9 +80,9 @@ def test_w8a8_split_k_schedules(split, push, monkeypatch):
 
 
 @pytest.mark.parametrize("case", list(CASES8))
-def test_w8a8_pair_schedule(case, monkeypatch):
+def test_w8a8_pair_schedule(case, tuning):
     """The 8-bit layers on the CTA-pair schedule (256 x 256 tiles, kind::f16 pair MMAs)."""
-    monkeypatch.setenv("WQ_GEMM_WIDE", "1")
+    tuning("WQ_GEMM_WIDE", "1")
     L = wl.make_layer_inputs("backbone", **CASES8[case])
     w = prep8(L)
     y = wq.wq_linear_forward_w8a8(w, x_dev(L.x_bits))

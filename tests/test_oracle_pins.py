@@ -550,3 +550,36 @@ def test_int8_weight_quantiser_against_numpy():
     assert np.array_equal(q, q_ref)
     assert q[11, 9] == 10 and q[11, 18] == 18                  # 9.5 -> 10, 18.5 -> 18 (ties to even)
     assert not q[5].any() and np.all(q[7] == 127)
+
+
+def test_batch_and_fixed_tensor_scales():
+    """The two batch-wide tensor-scale modes: per_tensor takes g = amax of the whole batch / 2688;
+    a fixed g is used as given (block scales still from each block).  Against closed forms on rows
+    whose transform is exact, and against the brute-force block rule of the per-row test."""
+    rng = np.random.default_rng(51)
+    M, K = 6, 128
+    x = rng.integers(-60, 60, (M, K)).astype(np.float32)
+    x[2, 5] = 3000.0                                  # the batch maximum (no rotation, s = 1)
+    bits = wlmod.bf16_bits(x)
+    xf = wlmod.bf16_from_bits(bits)
+    per = oracle.quantize_act(bits, None, False, per_tensor=True)
+    assert per.g.shape == (1,) and per.g[0] == np.float32(np.float32(np.abs(xf).max()) / np.float32(2688.0))
+    # a fixed g equal to the batch's own gives the per-tensor result exactly
+    fixed = oracle.quantize_act(bits, None, False, static_g=float(per.g[0]))
+    assert np.array_equal(fixed.codes, per.codes) and np.array_equal(fixed.scales, per.scales)
+    # a fixed power-of-two g: every block scale is the nearest e4m3 of bmax / 6 / g
+    g = np.float32(2.0 ** -3)
+    st = oracle.quantize_act(bits, None, False, static_g=float(g))
+    assert st.g[0] == g
+    sv = np.array([oracle.e4m3_decode(k) for k in range(127)])
+    for m in range(M):
+        for b in range(K // 16):
+            t = np.float32(np.float32(np.abs(xf[m, 16 * b:16 * b + 16]).max()) / np.float32(6.0)) / g
+            dist = np.abs(sv - np.float64(t))
+            best = np.flatnonzero(dist == dist.min())
+            want = 126 if t >= 448 else (best[0] if len(best) == 1 else best[best % 2 == 0][0])
+            assert st.scales[m, b] == want
+    # saturation: a fixed g far below the data clamps the scale at 448 and the codes at +-6
+    sat = oracle.quantize_act(bits, None, False, static_g=1e-6)
+    assert sat.scales[2, 0] == 0x7E
+    assert (sat.codes[2, 2] & 15) in (7, 15) or (sat.codes[2, 2] >> 4) in (7, 15)

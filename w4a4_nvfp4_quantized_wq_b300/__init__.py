@@ -23,6 +23,7 @@ WQ_SCALE_LAYOUT_ROWMAJOR, WQ_SCALE_LAYOUT_MMA = 0, 1
 WQ_PATH_TWO_KERNEL, WQ_PATH_FUSED = 0, 1
 WQ_GEMM_SINGLE, WQ_GEMM_SPLITK, WQ_GEMM_WIDE = 0, 1, 2
 WQ_QUANT_CLUSTER, WQ_QUANT_STREAM = 0, 1
+WQ_ACT_SCALE_ROW, WQ_ACT_SCALE_TENSOR, WQ_ACT_SCALE_STATIC = 0, 1, 2
 
 EXPORTED = ["wq_prepare_weights", "wq_get_config", "wq_workspace_bytes", "wq_linear_forward",
             "wq_host_workspace_bytes", "wq_linear_forward_host", "wq_quantize_activations",
@@ -31,7 +32,7 @@ EXPORTED = ["wq_prepare_weights", "wq_get_config", "wq_workspace_bytes", "wq_lin
             "wq_conv3d_workspace_bytes", "wq_conv3d_forward", "wq_quantize_conv3d_input",
             "wq_export_weights", "wq_check_device_error", "wq_free_weights", "wq_last_error",
             "wq_forward_path", "wq_selftest_wait_timeout", "wq_gemm_schedule",
-            "wq_quant_schedule"]
+            "wq_quant_schedule", "wq_side_strides", "wq_set_tuning", "wq_get_tuning", "wq_mma_peak"]
 
 
 class WqError(RuntimeError):
@@ -42,7 +43,8 @@ class WqError(RuntimeError):
 
 class wq_config(ctypes.Structure):
     _fields_ = [("K", ctypes.c_int), ("N", ctypes.c_int), ("rank", ctypes.c_int),
-                ("n_outliers", ctypes.c_int), ("rotate", ctypes.c_int), ("mode", ctypes.c_int)]
+                ("n_outliers", ctypes.c_int), ("rotate", ctypes.c_int), ("mode", ctypes.c_int),
+                ("act_scale", ctypes.c_int), ("act_gscale", ctypes.c_float)]
 
 
 _lib = None
@@ -61,6 +63,12 @@ def lib() -> ctypes.CDLL:
         L.wq_prepare_weights.restype = I
         L.wq_get_config.argtypes = [P, ctypes.POINTER(wq_config)]
         L.wq_get_config.restype = I
+        L.wq_side_strides.argtypes = [P, ctypes.POINTER(I), ctypes.POINTER(I)]
+        L.wq_side_strides.restype = I
+        L.wq_set_tuning.argtypes = [ctypes.c_char_p, I]
+        L.wq_set_tuning.restype = I
+        L.wq_get_tuning.argtypes = [ctypes.c_char_p]
+        L.wq_get_tuning.restype = I
         L.wq_workspace_bytes.argtypes = [P, I]
         L.wq_workspace_bytes.restype = S
         L.wq_host_workspace_bytes.argtypes = [P, I]
@@ -81,13 +89,13 @@ def lib() -> ctypes.CDLL:
         L.wq_quantize_activations_w8a8.restype = I
         L.wq_export_weights_w8a8.argtypes = [P, P, P]
         L.wq_export_weights_w8a8.restype = I
-        L.wq_prepare_conv3d.argtypes = [P, I, I, P, ctypes.POINTER(P)]
+        L.wq_prepare_conv3d.argtypes = [P, I, I, I, I, I, I, P, ctypes.POINTER(P)]
         L.wq_prepare_conv3d.restype = I
-        L.wq_conv3d_workspace_bytes.argtypes = [P, I, I, I]
+        L.wq_conv3d_workspace_bytes.argtypes = [P, I, I, I, I]
         L.wq_conv3d_workspace_bytes.restype = S
-        L.wq_conv3d_forward.argtypes = [P, P, I, I, I, P, P, S, P]
+        L.wq_conv3d_forward.argtypes = [P, P, I, I, I, I, P, P, S, P]
         L.wq_conv3d_forward.restype = I
-        L.wq_quantize_conv3d_input.argtypes = [P, P, I, I, I, P, P, P, P, S, P]
+        L.wq_quantize_conv3d_input.argtypes = [P, P, I, I, I, I, P, P, P, P, S, P]
         L.wq_quantize_conv3d_input.restype = I
         L.wq_export_weights.argtypes = [P, P, P, P, P, P, P]
         L.wq_export_weights.restype = I
@@ -101,6 +109,9 @@ def lib() -> ctypes.CDLL:
         L.wq_quant_schedule.restype = I
         L.wq_selftest_wait_timeout.argtypes = [ctypes.POINTER(I), ctypes.POINTER(ctypes.c_double), ctypes.POINTER(I)]
         L.wq_selftest_wait_timeout.restype = I
+        D = ctypes.POINTER(ctypes.c_double)
+        L.wq_mma_peak.argtypes = [I, I, I, I, I, I, I, I, I, D, D, D]
+        L.wq_mma_peak.restype = I
         L.wq_free_weights.argtypes = [P]
         L.wq_free_weights.restype = None
         L.wq_last_error.argtypes = []
@@ -153,11 +164,12 @@ class Weights:
 
 
 def wq_prepare_weights(K: int, N: int, W, bias=None, s=None, L1=None, L2=None, omega=None,
-                       rotate: bool = True, mode: int = WQ_MODE_W4A4, stream=None) -> Weights:
+                       rotate: bool = True, mode: int = WQ_MODE_W4A4, stream=None,
+                       act_scale: int = WQ_ACT_SCALE_ROW, act_gscale: float = 0.0) -> Weights:
     """Fold and quantise one projection (host inputs, numpy or CPU tensors)."""
     rank = 0 if L1 is None else int(np.shape(L1)[1])
     n_out = 0 if omega is None else int(np.size(omega))
-    cfg = wq_config(K, N, rank, n_out, int(bool(rotate)), mode)
+    cfg = wq_config(K, N, rank, n_out, int(bool(rotate)), mode, int(act_scale), float(act_gscale))
     keep = []
     ptrs = []
     for a, dt in ((W, np.float32), (bias, np.float32), (s, np.float32), (L1, np.float32),
@@ -177,6 +189,22 @@ def wq_get_config(w: Weights) -> wq_config:
     cfg = wq_config()
     _check(lib().wq_get_config(ctypes.c_void_p(w.handle), ctypes.byref(cfg)))
     return cfg
+
+
+def wq_side_strides(w: Weights):
+    """(u_ld, xo_ld): row strides of U and x_Omega in the quantiser's outputs."""
+    u, xo = ctypes.c_int(0), ctypes.c_int(0)
+    _check(lib().wq_side_strides(ctypes.c_void_p(w.handle), ctypes.byref(u), ctypes.byref(xo)))
+    return u.value, xo.value
+
+
+def wq_set_tuning(name: str, value: int):
+    """Pin a schedule knob (tests and tuning); -1 / 0 restores the automatic choice."""
+    _check(lib().wq_set_tuning(name.encode(), int(value)))
+
+
+def wq_get_tuning(name: str) -> int:
+    return int(lib().wq_get_tuning(name.encode()))
 
 
 def wq_workspace_bytes(w: Weights, M: int) -> int:
@@ -228,7 +256,8 @@ def wq_linear_forward_host(w: Weights, x_host, y_host, workspace, stream=None):
 
 
 def wq_quantize_activations(w: Weights, x, scale_layout: int = WQ_SCALE_LAYOUT_ROWMAJOR, stream=None):
-    """Run the activation quantiser alone; returns device tensors (codes, scales, g, x_omega, u)."""
+    """Run the activation quantiser alone; returns device tensors (codes, scales, g, x_omega, u);
+    x_omega is [M, xo_ld] and u [M, u_ld] (wq_side_strides), zero beyond the configured counts."""
     import torch
     M, K = x.shape
     dev = x.device
@@ -238,8 +267,9 @@ def wq_quantize_activations(w: Weights, x, scale_layout: int = WQ_SCALE_LAYOUT_R
     else:
         scales = torch.empty((M, K // 16), dtype=torch.uint8, device=dev)
     g = torch.empty(M, dtype=torch.float32, device=dev)
-    xo = torch.empty((M, w.cfg.n_outliers), dtype=torch.float16, device=dev) if w.cfg.n_outliers else None
-    u = torch.empty((M, w.cfg.rank), dtype=torch.bfloat16, device=dev) if w.cfg.rank else None
+    u_ld, xo_ld = wq_side_strides(w)
+    xo = torch.empty((M, xo_ld), dtype=torch.float16, device=dev) if w.cfg.n_outliers else None
+    u = torch.empty((M, u_ld), dtype=torch.bfloat16, device=dev) if w.cfg.rank else None
     _check(lib().wq_quantize_activations(
         ctypes.c_void_p(w.handle), ctypes.c_void_p(x.data_ptr()), M, int(scale_layout),
         ctypes.c_void_p(codes.data_ptr()), ctypes.c_void_p(scales.data_ptr()), ctypes.c_void_p(g.data_ptr()),
@@ -315,6 +345,19 @@ def wq_selftest_wait_timeout():
     return st, site.value, (waited[0], waited[1]), released.value
 
 
+MMA_KIND = {"fp4": 0, "bf16": 1, "fp8": 2}
+
+
+def wq_mma_peak(kind: str = "fp4", n: int = 256, pair: bool = False, copies: int = 0, copy_shape: int = 0,
+                iters: int = 8192, feeder: int = 0, zero_data: bool = False, accs: int = 1):
+    """Tensor-core issue-rate microbenchmark on the current device (synchronous): returns
+    (TFLOP/s over all SMs, ns per MMA instruction, mean SM MHz during the run)."""
+    t, ns, mhz = ctypes.c_double(), ctypes.c_double(), ctypes.c_double()
+    _check(lib().wq_mma_peak(MMA_KIND[kind], n, int(bool(pair)), copies, copy_shape, iters, feeder,
+                             int(bool(zero_data)), accs, ctypes.byref(t), ctypes.byref(ns), ctypes.byref(mhz)))
+    return t.value, ns.value, mhz.value
+
+
 def wq_check_device_error(w: Weights, stream=None):
     _check(lib().wq_check_device_error(ctypes.c_void_p(w.handle), ctypes.c_void_p(_stream_ptr(stream))))
 
@@ -376,29 +419,29 @@ class ConvWeights(Weights):
     C_in: int = 0
 
 
-def wq_prepare_conv3d(w, stream=None) -> ConvWeights:
-    """Quantise a [C_out, C_in, 3, 3, 3] fp32 kernel for the implicit-GEMM Conv3d."""
+def wq_prepare_conv3d(w, pad: int = 1, stream=None) -> ConvWeights:
+    """Quantise a [C_out, C_in, kt, kh, kw] fp32 kernel for the implicit-GEMM Conv3d."""
     w = np.ascontiguousarray(w.detach().cpu().numpy() if hasattr(w, "numpy") else w, dtype=np.float32)
-    Co, Ci = w.shape[:2]
+    Co, Ci, kt, kh, kw = w.shape
     out = ctypes.c_void_p()
-    _check(lib().wq_prepare_conv3d(w.ctypes.data_as(ctypes.c_void_p), Ci, Co,
+    _check(lib().wq_prepare_conv3d(w.ctypes.data_as(ctypes.c_void_p), Ci, Co, kt, kh, kw, int(pad),
                                    ctypes.c_void_p(_stream_ptr(stream)), ctypes.byref(out)))
-    return ConvWeights(out.value, wq_config(27 * Ci, Co, 0, 0, 0, WQ_MODE_W4A4), Ci)
+    return ConvWeights(out.value, wq_config(kt * kh * kw * Ci, Co, 0, 0, 0, WQ_MODE_W4A4, 0, 0.0), Ci)
 
 
-def wq_conv3d_workspace_bytes(w: ConvWeights, D: int, H: int, W: int) -> int:
-    return int(lib().wq_conv3d_workspace_bytes(ctypes.c_void_p(w.handle), D, H, W))
+def wq_conv3d_workspace_bytes(w: ConvWeights, B: int, D: int, H: int, W: int) -> int:
+    return int(lib().wq_conv3d_workspace_bytes(ctypes.c_void_p(w.handle), B, D, H, W))
 
 
 def wq_conv3d_forward(w: ConvWeights, x, y=None, workspace=None, stream=None):
-    """y [1, C_out, D, H, W] bf16 = conv3d(x [1, C_in, D, H, W] bf16), 3x3x3, padding 1."""
+    """y [B, C_out, D, H, W] bf16 = conv3d(x [B, C_in, D, H, W] bf16), 3x3x3, padding 1."""
     import torch
-    _, C, D, H, W = x.shape
+    B, C, D, H, W = x.shape
     if y is None:
-        y = torch.empty((1, w.N, D, H, W), dtype=torch.bfloat16, device=x.device)
+        y = torch.empty((B, w.N, D, H, W), dtype=torch.bfloat16, device=x.device)
     if workspace is None:
-        workspace = _alloc_workspace(wq_conv3d_workspace_bytes(w, D, H, W), x.device)
-    _check(lib().wq_conv3d_forward(ctypes.c_void_p(w.handle), ctypes.c_void_p(x.data_ptr()), D, H, W,
+        workspace = _alloc_workspace(wq_conv3d_workspace_bytes(w, B, D, H, W), x.device)
+    _check(lib().wq_conv3d_forward(ctypes.c_void_p(w.handle), ctypes.c_void_p(x.data_ptr()), B, D, H, W,
                                    ctypes.c_void_p(y.data_ptr()), ctypes.c_void_p(workspace.data_ptr()),
                                    workspace.numel(), ctypes.c_void_p(_stream_ptr(stream))))
     return y
@@ -406,13 +449,13 @@ def wq_conv3d_forward(w: ConvWeights, x, y=None, workspace=None, stream=None):
 
 def wq_quantize_conv3d_input(w: ConvWeights, x, stream=None):
     import torch
-    _, C, D, H, W = x.shape
-    V = D * H * W
+    B, C, D, H, W = x.shape
+    V = B * D * H * W
     codes = torch.empty((V, C // 2), dtype=torch.uint8, device=x.device)
     scales = torch.empty((V, C // 16), dtype=torch.uint8, device=x.device)
     g = torch.empty(1, dtype=torch.float32, device=x.device)
-    ws = _alloc_workspace(wq_conv3d_workspace_bytes(w, D, H, W), x.device)
-    _check(lib().wq_quantize_conv3d_input(ctypes.c_void_p(w.handle), ctypes.c_void_p(x.data_ptr()), D, H, W,
+    ws = _alloc_workspace(wq_conv3d_workspace_bytes(w, B, D, H, W), x.device)
+    _check(lib().wq_quantize_conv3d_input(ctypes.c_void_p(w.handle), ctypes.c_void_p(x.data_ptr()), B, D, H, W,
                                           ctypes.c_void_p(codes.data_ptr()), ctypes.c_void_p(scales.data_ptr()),
                                           ctypes.c_void_p(g.data_ptr()), ctypes.c_void_p(ws.data_ptr()), ws.numel(),
                                           ctypes.c_void_p(_stream_ptr(stream))))

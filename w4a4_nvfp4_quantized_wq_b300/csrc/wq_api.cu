@@ -9,6 +9,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
@@ -104,6 +105,49 @@ namespace wq {
 
 void set_last_error(const char* msg) { g_last_error = msg; }
 
+namespace {
+struct KnobDef {
+    const char* name;
+    int dflt;
+};
+constexpr KnobDef kKnobs[kTuneCount] = {
+    {"WQ_FUSED", 0},          {"WQ_GEMM_SPLIT", 0},     {"WQ_GEMM_WIDE", -1},        {"WQ_GEMM_PUSH", -1},
+    {"WQ_GEMM_STAGES", 0},    {"WQ_QUANT_SCHEDULE", -1}, {"WQ_QUANT_SPLIT", 0},      {"WQ_QUANT_CTAS_PER_SM", 0},
+};
+std::once_flag g_knob_once;
+}  // namespace
+std::atomic<int> g_knob[kTuneCount];
+namespace {
+
+// The environment is read once; afterwards only wq_set_tuning changes a knob.
+void init_knobs() {
+    std::call_once(g_knob_once, [] {
+        for (int k = 0; k < kTuneCount; ++k) {
+            int v = kKnobs[k].dflt;
+            if (const char* e = std::getenv(kKnobs[k].name)) {
+                if (k == kTuneQuantSchedule && (e[0] == 's' || e[0] == 'c'))
+                    v = e[0] == 's' ? 1 : 0;
+                else if (e[0] != '\0')
+                    v = std::atoi(e);
+            }
+            g_knob[k].store(v, std::memory_order_relaxed);
+        }
+    });
+}
+
+int knob_index(const char* name) {
+    if (!name) return -1;
+    for (int k = 0; k < kTuneCount; ++k)
+        if (std::strcmp(name, kKnobs[k].name) == 0) return k;
+    return -1;
+}
+}  // namespace
+
+int tune(TuneKnob k) {
+    init_knobs();
+    return g_knob[k].load(std::memory_order_relaxed);
+}
+
 bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner, uint64_t outer,
                     uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle,
                     const char** why) {
@@ -130,6 +174,7 @@ ActWorkspace carve_workspace(void* base, int M, int K, int r, int n_out) {
     const size_t o_g = take(static_cast<size_t>(M) * 4);
     const size_t o_u = take(static_cast<size_t>(M) * r * 2);
     const size_t o_xo = take(static_cast<size_t>(M) * n_out * 2);
+    const size_t o_amax = take(16);
     w.bytes = off;
     if (base) {
         uint8_t* b = static_cast<uint8_t*>(base);
@@ -138,6 +183,7 @@ ActWorkspace carve_workspace(void* base, int M, int K, int r, int n_out) {
         w.g = reinterpret_cast<float*>(b + o_g);
         w.u = reinterpret_cast<uint16_t*>(b + o_u);
         w.xo = reinterpret_cast<uint16_t*>(b + o_xo);
+        w.amax = reinterpret_cast<unsigned int*>(b + o_amax);
     }
     return w;
 }
@@ -160,6 +206,9 @@ struct wq_weights {
     uint16_t* d_WOt = nullptr;     // [N, n_out] fp16
     int* d_err = nullptr;
     float* d_colscale = nullptr;   // W8A8: per-output-column weight scale [N]
+    int r_pad = 0;                 // stored rank: side_width(rank) (U, P, Q^T columns)
+    int no_pad = 0;                // stored outlier width: side_width(n_outliers) (x_O, W_O^T columns)
+    unsigned int* d_amax = nullptr;// WQ_ACT_SCALE_TENSOR: running batch maximum of wq_quantize_activations
     int conv_cin = 0;              // Conv3d handles: input channels (K = 27 conv_cin)
     CUtensorMap tmBconv{};         // weight codes with 64-byte boxes (Conv3d, fused small-batch path)
     CUtensorMap tmB{}, tmQ{}, tmWO{};
@@ -177,6 +226,10 @@ struct wq_weights {
     CUtensorMap tmX{};
 };
 
+namespace wq {
+int handle_device(wq_weights_t h) { return h->device; }
+}  // namespace wq
+
 namespace {
 
 wq_status check_config(const wq_config* c) {
@@ -189,10 +242,14 @@ wq_status check_config(const wq_config* c) {
     if (c->rotate != 0 && c->rotate != 1) return fail(WQ_ERR_INVALID, "rotate must be 0 or 1");
     if (c->K % 64 || c->K > 16384) return fail(WQ_ERR_UNSUPPORTED, "K must be a multiple of 64 and <= 16384");
     if (c->N % 16) return fail(WQ_ERR_UNSUPPORTED, "N must be a multiple of 16");
-    if (!(c->rank == 0 || c->rank == 16 || c->rank == 32 || c->rank == 64))
-        return fail(WQ_ERR_UNSUPPORTED, "rank must be 0, 16, 32 or 64");
-    if (!(c->n_outliers == 0 || c->n_outliers == 16 || c->n_outliers == 32 || c->n_outliers == 64))
-        return fail(WQ_ERR_UNSUPPORTED, "n_outliers must be 0, 16, 32 or 64");
+    if (c->rank > 64) return fail(WQ_ERR_UNSUPPORTED, "rank must be <= 64");
+    if (c->n_outliers > 64 || c->n_outliers > c->K) return fail(WQ_ERR_UNSUPPORTED, "n_outliers must be <= 64 and <= K");
+    if (c->act_scale != WQ_ACT_SCALE_ROW && c->act_scale != WQ_ACT_SCALE_TENSOR && c->act_scale != WQ_ACT_SCALE_STATIC)
+        return fail(WQ_ERR_INVALID, "unknown act_scale");
+    if (c->mode == WQ_MODE_W8A8 && c->act_scale != WQ_ACT_SCALE_ROW)
+        return fail(WQ_ERR_UNSUPPORTED, "WQ_MODE_W8A8 takes WQ_ACT_SCALE_ROW");
+    if (c->act_scale == WQ_ACT_SCALE_STATIC && !(c->act_gscale > 0.0f && std::isfinite(c->act_gscale)))
+        return fail(WQ_ERR_INVALID, "WQ_ACT_SCALE_STATIC needs a finite act_gscale > 0");
     return WQ_OK;
 }
 
@@ -208,6 +265,7 @@ void free_device(wq_weights* h) {
     cudaFree(h->d_WOt);
     cudaFree(h->d_err);
     cudaFree(h->d_colscale);
+    cudaFree(h->d_amax);
 }
 
 template <typename T>
@@ -254,6 +312,9 @@ WQ_API wq_status wq_prepare_weights(const wq_config* cfg, const float* W, const 
     if (st != WQ_OK) return st;
     if (!W) return fail(WQ_ERR_INVALID, "W is NULL");
     const int K = cfg->K, N = cfg->N, r = cfg->rank, no = cfg->n_outliers;
+    // stored widths of the side operands: the extra columns of P, Q^T and W_O^T are zero, so
+    // the extra U columns are exact zeros and x_O's extra columns meet zero weights
+    const int rp = wq::side_width(r), nop = wq::side_width(no);
     if (r > 0 && (!L1 || !L2)) return fail(WQ_ERR_INVALID, "rank > 0 needs L1 and L2");
     if (no > 0 && !omega) return fail(WQ_ERR_INVALID, "n_outliers > 0 needs omega");
     for (int j = 0; j < no; ++j) {
@@ -268,36 +329,38 @@ WQ_API wq_status wq_prepare_weights(const wq_config* cfg, const float* W, const 
     std::vector<float> inv_s(s ? K : 0);
     for (int k = 0; k < (s ? K : 0); ++k) inv_s[k] = 1.0f / s[k];
     const std::vector<float> inv_s_pairs = pair_order(inv_s);
-    std::vector<uint16_t> P(static_cast<size_t>(K) * r), Qt(static_cast<size_t>(N) * r);
+    std::vector<uint16_t> P(static_cast<size_t>(K) * rp, 0), Qt(static_cast<size_t>(N) * rp, 0);
     for (int k = 0; k < K; ++k)
         for (int j = 0; j < r; ++j) {
             float l = L1[static_cast<size_t>(k) * r + j];
             if (s) l = l * inv_s[k];
-            P[static_cast<size_t>(k) * r + j] = bf16_bits(l);
+            P[static_cast<size_t>(k) * rp + j] = bf16_bits(l);
         }
     // P as the B operand of mma.sync.m16n8k16 (k16 x n8 tiles): for 64-block kb, n-tile nt,
     // lane (g = lane / 4, c = lane % 4) and k16 step f, the lane's two registers hold
     // {P[k][j], P[k+1][j]} and {P[k+8][j], P[k+9][j]} with k = 64 kb + 16 f + 2 c, j = 8 nt + g.
-    std::vector<uint32_t> Pfrag(static_cast<size_t>(K) * r / 2);
+    std::vector<uint32_t> Pfrag(static_cast<size_t>(K) * rp / 2);
     if (r > 0) {
-        const int NT = r / 8;
+        const int NT = rp / 8;
         for (int kb = 0; kb < K / 64; ++kb)
             for (int nt = 0; nt < NT; ++nt)
                 for (int lane = 0; lane < 32; ++lane)
                     for (int f = 0; f < 4; ++f) {
                         const int g = lane / 4, c = lane % 4, j = 8 * nt + g, k = 64 * kb + 16 * f + 2 * c;
-                        auto at = [&](int kk) { return static_cast<uint32_t>(P[static_cast<size_t>(kk) * r + j]); };
+                        auto at = [&](int kk) { return static_cast<uint32_t>(P[static_cast<size_t>(kk) * rp + j]); };
                         const size_t o = ((static_cast<size_t>(kb) * NT + nt) * 32 + lane) * 8 + 2 * f;
                         Pfrag[o] = at(k) | (at(k + 1) << 16);
                         Pfrag[o + 1] = at(k + 8) | (at(k + 9) << 16);
                     }
     }
-    std::vector<float> Pf(P.size()), Qf(static_cast<size_t>(r) * N);
-    for (size_t i = 0; i < P.size(); ++i) Pf[i] = __bfloat162float(__ushort_as_bfloat16(P[i]));
+    std::vector<float> Pf(static_cast<size_t>(K) * r), Qf(static_cast<size_t>(r) * N);
+    for (int k = 0; k < K; ++k)
+        for (int j = 0; j < r; ++j)
+            Pf[static_cast<size_t>(k) * r + j] = __bfloat162float(__ushort_as_bfloat16(P[static_cast<size_t>(k) * rp + j]));
     for (int j = 0; j < r; ++j)
         for (int n = 0; n < N; ++n) {
             const uint16_t b = bf16_bits(L2[static_cast<size_t>(j) * N + n]);
-            Qt[static_cast<size_t>(n) * r + j] = b;
+            Qt[static_cast<size_t>(n) * rp + j] = b;
             Qf[static_cast<size_t>(j) * N + n] = __bfloat162float(__ushort_as_bfloat16(b));
         }
 
@@ -319,7 +382,7 @@ WQ_API wq_status wq_prepare_weights(const wq_config* cfg, const float* W, const 
     });
 
     // ---- the fp16 outlier rows of the rotated basis
-    std::vector<uint16_t> WOt(static_cast<size_t>(N) * no);
+    std::vector<uint16_t> WOt(static_cast<size_t>(N) * nop, 0);
     // per 64-block of K: which channels are kept (bit mask) and the x_O index of the first one
     std::vector<uint32_t> omega_blk(no ? static_cast<size_t>(K / 64) * 4 : 0, 0u);
     for (int j = no - 1; j >= 0; --j) {
@@ -330,7 +393,7 @@ WQ_API wq_status wq_prepare_weights(const wq_config* cfg, const float* W, const 
     for (int j = 0; j < no; ++j) {
         for (int n = 0; n < N; ++n) {
             float& v = Rp[static_cast<size_t>(omega[j]) * N + n];
-            WOt[static_cast<size_t>(n) * no + j] = f16_bits(v);
+            WOt[static_cast<size_t>(n) * nop + j] = f16_bits(v);
             v = 0.0f;
         }
     }
@@ -416,6 +479,8 @@ WQ_API wq_status wq_prepare_weights(const wq_config* cfg, const float* W, const 
     if (!h) return fail(WQ_ERR_OOM, "host allocation failed");
     h->cfg = *cfg;
     h->gW = gW;
+    h->r_pad = rp;
+    h->no_pad = nop;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     auto bail = [&](wq_status e) { free_device(h); delete h; return e; };
     if (cudaGetDevice(&h->device) != cudaSuccess) return bail(fail(WQ_ERR_CUDA, "cudaGetDevice failed"));
@@ -433,6 +498,9 @@ WQ_API wq_status wq_prepare_weights(const wq_config* cfg, const float* W, const 
     if (no && (st = upload(&h->d_WOt, WOt.data(), WOt.size() * 2, cs)) != WQ_OK) return bail(st);
     if (cudaMalloc(&h->d_err, sizeof(int)) != cudaSuccess) return bail(fail(WQ_ERR_OOM, "cudaMalloc failed"));
     if (cudaMemsetAsync(h->d_err, 0, sizeof(int), cs) != cudaSuccess) return bail(fail(WQ_ERR_CUDA, "memset"));
+    if (cfg->act_scale == WQ_ACT_SCALE_TENSOR &&
+        cudaMalloc(reinterpret_cast<void**>(&h->d_amax), 16) != cudaSuccess)
+        return bail(fail(WQ_ERR_OOM, "cudaMalloc failed"));
     if (cudaStreamSynchronize(cs) != cudaSuccess) return bail(fail(WQ_ERR_CUDA, "upload synchronise failed"));
 
     const char* why = "";
@@ -441,11 +509,11 @@ WQ_API wq_status wq_prepare_weights(const wq_config* cfg, const float* W, const 
         !wq::encode_tmap_2d(&h->tmBconv, CU_TENSOR_MAP_DATA_TYPE_UINT8, h->d_codes, K / 2, N, K / 2, 64, 128,
                             CU_TENSOR_MAP_SWIZZLE_64B, &why))
         return bail(fail(WQ_ERR_CUDA, why));
-    if (r && !wq::encode_tmap_2d(&h->tmQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h->d_Qt, r, N, 2 * r, r, 128,
-                                 swizzle_for_row_bytes(2 * r), &why))
+    if (r && !wq::encode_tmap_2d(&h->tmQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h->d_Qt, rp, N, 2 * rp, rp, 128,
+                                 swizzle_for_row_bytes(2 * rp), &why))
         return bail(fail(WQ_ERR_CUDA, why));
-    if (no && !wq::encode_tmap_2d(&h->tmWO, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, h->d_WOt, no, N, 2 * no, no, 128,
-                                  swizzle_for_row_bytes(2 * no), &why))
+    if (no && !wq::encode_tmap_2d(&h->tmWO, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, h->d_WOt, nop, N, 2 * nop, nop, 128,
+                                  swizzle_for_row_bytes(2 * nop), &why))
         return bail(fail(WQ_ERR_CUDA, why));
     *out = h;
     return WQ_OK;
@@ -458,7 +526,28 @@ static size_t w8_workspace_bytes(int M, int K) {
 WQ_API size_t wq_workspace_bytes(wq_weights_t h, int M) {
     if (!h || M < 0) return 0;
     if (h->cfg.mode == WQ_MODE_W8A8) return w8_workspace_bytes(M, h->cfg.K);
-    return wq::carve_workspace(nullptr, M, h->cfg.K, h->cfg.rank, h->cfg.n_outliers).bytes;
+    return wq::carve_workspace(nullptr, M, h->cfg.K, h->r_pad, h->no_pad).bytes;
+}
+
+WQ_API wq_status wq_side_strides(wq_weights_t h, int* u_ld, int* xo_ld) {
+    if (!h) return fail(WQ_ERR_INVALID, "NULL handle");
+    if (u_ld) *u_ld = h->r_pad;
+    if (xo_ld) *xo_ld = h->no_pad;
+    return WQ_OK;
+}
+
+WQ_API wq_status wq_set_tuning(const char* name, int value) {
+    const int k = wq::knob_index(name);
+    if (k < 0) return fail(WQ_ERR_INVALID, std::string("unknown tuning knob ") + (name ? name : "(null)"));
+    wq::tune(static_cast<wq::TuneKnob>(k));             // the environment is read first, once
+    wq::g_knob[k].store(value, std::memory_order_relaxed);
+    return WQ_OK;
+}
+
+WQ_API int wq_get_tuning(const char* name) {
+    const int k = wq::knob_index(name);
+    if (k < 0) return fail(WQ_ERR_INVALID, std::string("unknown tuning knob ") + (name ? name : "(null)"));
+    return wq::tune(static_cast<wq::TuneKnob>(k));
 }
 
 WQ_API size_t wq_host_workspace_bytes(wq_weights_t h, int M) {
@@ -467,8 +556,21 @@ WQ_API size_t wq_host_workspace_bytes(wq_weights_t h, int M) {
            align_up(static_cast<size_t>(M) * h->cfg.N * 2, 1024);
 }
 
-// x as [M, K] bf16 in 16-row x 64-channel boxes (re-encoded when x or M changes).
-static wq_status x_map(wq_weights_t h, const void* x, int M) {
+// Launching entry points run on the handle's device only: its weights, error flag and scratch
+// live there.
+static wq_status check_device(wq_weights_t h) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return fail(WQ_ERR_CUDA, "cudaGetDevice failed");
+    if (dev != h->device)
+        return fail(WQ_ERR_INVALID, "the current device (" + std::to_string(dev) + ") is not the handle's device (" +
+                                        std::to_string(h->device) + ")");
+    return WQ_OK;
+}
+
+// x as [M, K] bf16 in 16-row x 64-channel boxes (re-encoded when x or M changes).  The map is
+// copied out under the lock: the launch passes it by value, so a concurrent call on the same
+// handle that re-encodes the cached map cannot change what this launch reads.
+static wq_status x_map(wq_weights_t h, const void* x, int M, CUtensorMap* out) {
     std::lock_guard<std::mutex> lk(h->mu_x);
     if (h->key_x != x || h->key_xM != M) {
         const char* why = "";
@@ -480,16 +582,24 @@ static wq_status x_map(wq_weights_t h, const void* x, int M) {
         h->key_x = x;
         h->key_xM = M;
     }
+    *out = h->tmX;
     return WQ_OK;
 }
 
 static wq_status run_quant(wq_weights_t h, const void* x, int M, int layout, uint8_t* codes, uint8_t* sf, float* g,
-                           uint16_t* xo, uint16_t* u, cudaStream_t st) {
+                           uint16_t* xo, uint16_t* u, unsigned int* amax, cudaStream_t st) {
     wq::QuantArgs qa{};
+    CUtensorMap tmx;
     {
-        const wq_status s = x_map(h, x, M);
+        const wq_status s = x_map(h, x, M, &tmx);
         if (s != WQ_OK) return s;
-        qa.tmX = &h->tmX;
+        qa.tmX = &tmx;
+    }
+    qa.act_scale = h->cfg.act_scale;
+    qa.static_g = h->cfg.act_gscale;
+    if (qa.act_scale == WQ_ACT_SCALE_TENSOR) {
+        qa.amax_bits = amax;
+        WQ_CUDA(cudaMemsetAsync(amax, 0, sizeof(unsigned int), st), "batch maximum reset");
     }
     qa.pfrag = h->d_Pfrag;
     qa.err = h->d_err;
@@ -500,9 +610,10 @@ static wq_status run_quant(wq_weights_t h, const void* x, int M, int layout, uin
     qa.rotate = h->cfg.rotate;
     qa.omega_blk = h->d_omega_blk;
     qa.n_out = xo ? h->cfg.n_outliers : 0;
+    qa.xo_ld = h->no_pad;
     qa.xo = xo;
     qa.P = h->d_P;
-    qa.r = u ? h->cfg.rank : 0;
+    qa.r = u ? h->r_pad : 0;
     qa.u = u;
     qa.codes = codes;
     qa.sf = sf;
@@ -528,14 +639,15 @@ WQ_API wq_status wq_quantize_activations(wq_weights_t h, const void* x, int M, i
         return fail(WQ_ERR_INVALID, "bad scale_layout");
     if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(codes) | reinterpret_cast<uintptr_t>(scales)) & 15)
         return fail(WQ_ERR_INVALID, "device buffers must be 16-byte aligned");
+    if (const wq_status d = check_device(h)) return d;
     return run_quant(h, x, M, scale_layout, codes, scales, gscale,
                      h->cfg.n_outliers ? static_cast<uint16_t*>(x_omega) : nullptr,
-                     h->cfg.rank ? static_cast<uint16_t*>(u) : nullptr, static_cast<cudaStream_t>(stream));
+                     h->cfg.rank ? static_cast<uint16_t*>(u) : nullptr, h->d_amax, static_cast<cudaStream_t>(stream));
 }
 
 static wq_status run_gemm(wq_weights_t h, const uint8_t* codes, const uint8_t* sf, const float* g,
                           const uint16_t* u, const uint16_t* xo, int M, void* y, cudaStream_t st) {
-    const int K = h->cfg.K, N = h->cfg.N, r = h->cfg.rank, no = h->cfg.n_outliers;
+    const int K = h->cfg.K, N = h->cfg.N, r = h->r_pad, no = h->no_pad, no_real = h->cfg.n_outliers;
     std::lock_guard<std::mutex> lk(h->mu);
     if (h->key_codes != codes || h->key_u != u || h->key_xo != xo || h->key_y != y || h->key_M != M) {
         const char* why = "";
@@ -549,8 +661,9 @@ static wq_status run_gemm(wq_weights_t h, const uint8_t* codes, const uint8_t* s
         if (ok && r)
             ok = wq::encode_tmap_2d(&h->tmU, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, u, r, M, 2 * r, r, 128,
                                     swizzle_for_row_bytes(2 * r), &why);
+        // x_O's columns beyond the real count are read as zeros (outside the map's extent)
         if (ok && no)
-            ok = wq::encode_tmap_2d(&h->tmXO, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xo, no, M, 2 * no, no, 128,
+            ok = wq::encode_tmap_2d(&h->tmXO, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xo, no_real, M, 2 * no, no, 128,
                                     swizzle_for_row_bytes(2 * no), &why);
         if (!ok) {
             h->key_codes = nullptr;
@@ -571,9 +684,7 @@ static wq_status run_gemm(wq_weights_t h, const uint8_t* codes, const uint8_t* s
     ga.y = y;
     ga.w8 = h->cfg.mode == WQ_MODE_W8A8;
     ga.colscale = h->d_colscale;
-    // WQ_GEMM_SPLIT=<1|2|4|8|16> pins the number of CTAs per output tile (tuning and tests)
-    const char* fs = std::getenv("WQ_GEMM_SPLIT");
-    ga.force_split = fs ? std::atoi(fs) : 0;
+    ga.force_split = wq::tune(wq::kTuneGemmSplit);     // 0: choose (tests and tuning pin it)
     const cudaError_t e = wq::launch_gemm(ga, st);
     if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
     return WQ_OK;
@@ -581,15 +692,16 @@ static wq_status run_gemm(wq_weights_t h, const uint8_t* codes, const uint8_t* s
 
 namespace {
 bool use_fused(wq_weights_t h, int M, int& nb, int& cs) {
-    const char* ff = std::getenv("WQ_FUSED");
-    return h->cfg.mode == WQ_MODE_W4A4 && ff && ff[0] == '1' &&
-           wq::fused_plan(M, h->cfg.K, h->cfg.N, h->cfg.rank, h->cfg.n_outliers, nb, cs);
+    return h->cfg.mode == WQ_MODE_W4A4 && h->cfg.act_scale == WQ_ACT_SCALE_ROW && wq::tune(wq::kTuneFused) == 1 &&
+           wq::fused_plan(M, h->cfg.K, h->cfg.N, h->r_pad, h->no_pad, nb, cs);
 }
 }  // namespace
 
 WQ_API int wq_quant_schedule(wq_weights_t h, int M) {
     if (!h) return fail(WQ_ERR_INVALID, "NULL handle");
     if (M < 0) return fail(WQ_ERR_INVALID, "M < 0");
+    // batch-wide tensor scales take the stream kernel (its two-launch and one-pass forms)
+    if (h->cfg.act_scale != WQ_ACT_SCALE_ROW) return WQ_QUANT_STREAM;
     return wq::quant_stream_schedule(M, h->num_sms) ? WQ_QUANT_STREAM : WQ_QUANT_CLUSTER;
 }
 
@@ -597,11 +709,10 @@ WQ_API int wq_gemm_schedule(wq_weights_t h, int M) {
     if (!h) return fail(WQ_ERR_INVALID, "NULL handle");
     if (M < 0) return fail(WQ_ERR_INVALID, "M < 0");
     wq::GemmArgs ga{};
-    ga.M = M > 0 ? M : 1; ga.N = h->cfg.N; ga.K = h->cfg.K; ga.r = h->cfg.rank; ga.n_out = h->cfg.n_outliers;
+    ga.M = M > 0 ? M : 1; ga.N = h->cfg.N; ga.K = h->cfg.K; ga.r = h->r_pad; ga.n_out = h->no_pad;
     ga.w8 = h->cfg.mode == WQ_MODE_W8A8;
     ga.num_sms = h->num_sms;
-    const char* fs = std::getenv("WQ_GEMM_SPLIT");
-    ga.force_split = fs ? std::atoi(fs) : 0;
+    ga.force_split = wq::tune(wq::kTuneGemmSplit);
     const int s = wq::gemm_schedule(ga);
     if (s < 0) return fail(WQ_ERR_CUDA, "GEMM schedule query failed");
     return s;
@@ -624,7 +735,8 @@ WQ_API wq_status wq_linear_forward(wq_weights_t h, const void* x, int M, void* y
         return fail(WQ_ERR_INVALID, "x and y must be 16-byte aligned");
     if (reinterpret_cast<uintptr_t>(workspace) & 255) return fail(WQ_ERR_INVALID, "workspace must be 256-byte aligned");
     if (h->cfg.mode != WQ_MODE_W4A4) return fail(WQ_ERR_INVALID, "W8A8 handle: use wq_linear_forward_w8a8");
-    const int K = h->cfg.K, r = h->cfg.rank, no = h->cfg.n_outliers;
+    if (const wq_status d = check_device(h)) return d;
+    const int K = h->cfg.K, r = h->r_pad, no = h->no_pad;
     const wq::ActWorkspace ws = wq::carve_workspace(workspace, M, K, r, no);
     if (workspace_bytes < ws.bytes) return fail(WQ_ERR_INVALID, "workspace too small");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -635,11 +747,12 @@ WQ_API wq_status wq_linear_forward(wq_weights_t h, const void* x, int M, void* y
     // layer's quantiser from starting early).
     int nb = 0, cs = 0;
     if (use_fused(h, M, nb, cs)) {
-        wq_status s = x_map(h, x, M);
+        CUtensorMap tmx;
+        wq_status s = x_map(h, x, M, &tmx);
         if (s != WQ_OK) return s;
         wq::FusedArgs fa{};
         fa.M = M; fa.K = K; fa.N = h->cfg.N; fa.r = r; fa.n_out = no; fa.nb = nb; fa.cs = cs;
-        fa.tmX = &h->tmX; fa.tmB = nb == 4 ? &h->tmB : &h->tmBconv; fa.tmQ = &h->tmQ; fa.tmWO = &h->tmWO;
+        fa.tmX = &tmx; fa.tmB = nb == 4 ? &h->tmB : &h->tmBconv; fa.tmQ = &h->tmQ; fa.tmWO = &h->tmWO;
         fa.inv_s = h->d_inv_s; fa.rotate = h->cfg.rotate; fa.omega_blk = h->d_omega_blk; fa.pfrag = h->d_Pfrag;
         fa.sfb = h->d_sf; fa.gW = h->gW; fa.bias = h->d_bias; fa.y = y; fa.err = h->d_err;
         const cudaError_t e = wq::launch_fused(fa, st);
@@ -647,7 +760,7 @@ WQ_API wq_status wq_linear_forward(wq_weights_t h, const void* x, int M, void* y
         return WQ_OK;
     }
     wq_status s = run_quant(h, x, M, WQ_SCALE_LAYOUT_MMA, ws.codes, ws.sf, ws.g, no ? ws.xo : nullptr,
-                            r ? ws.u : nullptr, st);
+                            r ? ws.u : nullptr, ws.amax, st);
     if (s != WQ_OK) return s;
     return run_gemm(h, ws.codes, ws.sf, ws.g, ws.u, ws.xo, M, y, st);
 }
@@ -665,6 +778,7 @@ WQ_API wq_status wq_linear_forward_quantized(wq_weights_t h, const uint8_t* code
     if ((reinterpret_cast<uintptr_t>(codes) | reinterpret_cast<uintptr_t>(scales_mma) |
          reinterpret_cast<uintptr_t>(u) | reinterpret_cast<uintptr_t>(x_omega) | reinterpret_cast<uintptr_t>(y)) & 15)
         return fail(WQ_ERR_INVALID, "device buffers must be 16-byte aligned");
+    if (const wq_status d = check_device(h)) return d;
     return run_gemm(h, codes, scales_mma, gscale, static_cast<const uint16_t*>(u),
                     static_cast<const uint16_t*>(x_omega), M, y, static_cast<cudaStream_t>(stream));
 }
@@ -679,12 +793,13 @@ WQ_API wq_status wq_linear_forward_w8a8(wq_weights_t h, const void* x, int M, vo
     if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15)
         return fail(WQ_ERR_INVALID, "x and y must be 16-byte aligned");
     if (reinterpret_cast<uintptr_t>(workspace) & 255) return fail(WQ_ERR_INVALID, "workspace must be 256-byte aligned");
+    if (const wq_status d = check_device(h)) return d;
     const int K = h->cfg.K;
     if (workspace_bytes < w8_workspace_bytes(M, K)) return fail(WQ_ERR_INVALID, "workspace too small");
     uint8_t* codes = static_cast<uint8_t*>(workspace);
     float* a = reinterpret_cast<float*>(codes + align_up(static_cast<size_t>(M) * K * 2, 1024));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    wq_status s = run_quant(h, x, M, WQ_SCALE_LAYOUT_ROWMAJOR, codes, nullptr, a, nullptr, nullptr, st);
+    wq_status s = run_quant(h, x, M, WQ_SCALE_LAYOUT_ROWMAJOR, codes, nullptr, a, nullptr, nullptr, nullptr, st);
     if (s != WQ_OK) return s;
     return run_gemm(h, codes, nullptr, a, nullptr, nullptr, M, y, st);
 }
@@ -698,8 +813,9 @@ WQ_API wq_status wq_quantize_activations_w8a8(wq_weights_t h, const void* x, int
     if (!x || !codes || !scale) return fail(WQ_ERR_INVALID, "NULL buffer");
     if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(codes)) & 15)
         return fail(WQ_ERR_INVALID, "device buffers must be 16-byte aligned");
+    if (const wq_status d = check_device(h)) return d;
     return run_quant(h, x, M, WQ_SCALE_LAYOUT_ROWMAJOR, static_cast<uint8_t*>(codes), nullptr, scale, nullptr,
-                     nullptr, static_cast<cudaStream_t>(stream));
+                     nullptr, nullptr, static_cast<cudaStream_t>(stream));
 }
 
 WQ_API wq_status wq_export_weights_w8a8(wq_weights_t h, int8_t* q, float* w) {
@@ -716,12 +832,16 @@ WQ_API wq_status wq_export_weights_w8a8(wq_weights_t h, int8_t* q, float* w) {
     return WQ_OK;
 }
 
-WQ_API wq_status wq_prepare_conv3d(const float* w, int C_in, int C_out, void* stream, wq_weights_t* out) {
+WQ_API wq_status wq_prepare_conv3d(const float* w, int C_in, int C_out, int kt, int kh, int kw, int pad, void* stream,
+                                   wq_weights_t* out) {
     g_last_error.clear();
     if (!out) return fail(WQ_ERR_INVALID, "out is NULL");
     *out = nullptr;
     if (!w) return fail(WQ_ERR_INVALID, "w is NULL");
     if (C_in <= 0 || C_out <= 0) return fail(WQ_ERR_INVALID, "channel counts must be positive");
+    if (kt <= 0 || kh <= 0 || kw <= 0 || pad < 0) return fail(WQ_ERR_INVALID, "bad kernel extent or padding");
+    if (kt != 3 || kh != 3 || kw != 3 || pad != 1)
+        return fail(WQ_ERR_UNSUPPORTED, "the implicit GEMM implements a 3 x 3 x 3 kernel with padding 1");
     if (C_in % 128 || C_out % 16 || 27 * C_in > 16384)
         return fail(WQ_ERR_UNSUPPORTED, "need C_in % 128 == 0, C_out % 16 == 0 and 27 C_in <= 16384");
     const int K = 27 * C_in, N = C_out;
@@ -730,7 +850,7 @@ WQ_API wq_status wq_prepare_conv3d(const float* w, int C_in, int C_out, void* st
         for (int c = 0; c < C_in; ++c)
             for (int t = 0; t < 27; ++t)
                 Wm[(static_cast<size_t>(t) * C_in + c) * N + n] = w[(static_cast<size_t>(n) * C_in + c) * 27 + t];
-    wq_config cfg{K, N, 0, 0, 0, WQ_MODE_W4A4};
+    wq_config cfg{K, N, 0, 0, 0, WQ_MODE_W4A4, WQ_ACT_SCALE_ROW, 0.0f};
     wq_weights_t h = nullptr;
     const wq_status st = wq_prepare_weights(&cfg, Wm.data(), nullptr, nullptr, nullptr, nullptr, nullptr, stream, &h);
     if (st != WQ_OK) return st;
@@ -745,22 +865,25 @@ WQ_API wq_status wq_prepare_conv3d(const float* w, int C_in, int C_out, void* st
     return WQ_OK;
 }
 
-WQ_API size_t wq_conv3d_workspace_bytes(wq_weights_t h, int D, int H, int W) {
-    if (!h || h->conv_cin == 0 || D <= 0 || H <= 0 || W <= 0) return 0;
-    return wq::conv_workspace_bytes(h->conv_cin, D * H * W, h->num_sms);
+WQ_API size_t wq_conv3d_workspace_bytes(wq_weights_t h, int B, int D, int H, int W) {
+    if (!h || h->conv_cin == 0 || B <= 0 || D <= 0 || H <= 0 || W <= 0) return 0;
+    return wq::conv_workspace_bytes(h->conv_cin, B * D * H * W, h->num_sms);
 }
 
-static wq_status conv_args(wq_weights_t h, const void* x, int D, int H, int W, void* ws, size_t ws_bytes,
+static wq_status conv_args(wq_weights_t h, const void* x, int B, int D, int H, int W, void* ws, size_t ws_bytes,
                            wq::ConvArgs* a) {
     if (!h) return fail(WQ_ERR_INVALID, "NULL handle");
     if (h->conv_cin == 0) return fail(WQ_ERR_INVALID, "handle was not prepared with wq_prepare_conv3d");
     if (!x || !ws) return fail(WQ_ERR_INVALID, "NULL buffer");
-    if (D <= 0 || H <= 0 || W <= 0) return fail(WQ_ERR_INVALID, "bad spatial size");
-    const int V = D * H * W;
-    if (V % 8) return fail(WQ_ERR_UNSUPPORTED, "D H W must be a multiple of 8");
+    if (B <= 0 || D <= 0 || H <= 0 || W <= 0) return fail(WQ_ERR_INVALID, "bad batch or spatial size");
+    if ((D * H * W) % 8) return fail(WQ_ERR_UNSUPPORTED, "D H W must be a multiple of 8");
+    if (static_cast<long long>(B) * D * H * W * h->conv_cin >= (1ll << 31))
+        return fail(WQ_ERR_UNSUPPORTED, "the input must have fewer than 2^31 elements");
+    const int V = B * D * H * W;
     if ((reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(ws) & 255))
         return fail(WQ_ERR_INVALID, "x must be 16-byte and the workspace 256-byte aligned");
-    if (ws_bytes < wq_conv3d_workspace_bytes(h, D, H, W)) return fail(WQ_ERR_INVALID, "workspace too small");
+    if (ws_bytes < wq_conv3d_workspace_bytes(h, B, D, H, W)) return fail(WQ_ERR_INVALID, "workspace too small");
+    if (const wq_status d = check_device(h)) return d;
     const int C = h->conv_cin;
     uint8_t* b = static_cast<uint8_t*>(ws);
     auto al = [](size_t v) { return (v + 1023) / 1024 * 1024; };
@@ -773,10 +896,10 @@ static wq_status conv_args(wq_weights_t h, const void* x, int D, int H, int W, v
     return WQ_OK;
 }
 
-WQ_API wq_status wq_conv3d_forward(wq_weights_t h, const void* x, int D, int H, int W, void* y, void* workspace,
-                                   size_t workspace_bytes, void* stream) {
+WQ_API wq_status wq_conv3d_forward(wq_weights_t h, const void* x, int B, int D, int H, int W, void* y,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
     wq::ConvArgs a{};
-    wq_status s = conv_args(h, x, D, H, W, workspace, workspace_bytes, &a);
+    wq_status s = conv_args(h, x, B, D, H, W, workspace, workspace_bytes, &a);
     if (s != WQ_OK) return s;
     if (!y || (reinterpret_cast<uintptr_t>(y) & 15)) return fail(WQ_ERR_INVALID, "y must be a 16-byte aligned buffer");
     a.y = y;
@@ -788,11 +911,11 @@ WQ_API wq_status wq_conv3d_forward(wq_weights_t h, const void* x, int D, int H, 
     return WQ_OK;
 }
 
-WQ_API wq_status wq_quantize_conv3d_input(wq_weights_t h, const void* x, int D, int H, int W, uint8_t* codes,
+WQ_API wq_status wq_quantize_conv3d_input(wq_weights_t h, const void* x, int B, int D, int H, int W, uint8_t* codes,
                                           uint8_t* scales, float* g, void* workspace, size_t workspace_bytes,
                                           void* stream) {
     wq::ConvArgs a{};
-    wq_status s = conv_args(h, x, D, H, W, workspace, workspace_bytes, &a);
+    wq_status s = conv_args(h, x, B, D, H, W, workspace, workspace_bytes, &a);
     if (s != WQ_OK) return s;
     if (!codes || !scales || !g) return fail(WQ_ERR_INVALID, "NULL output");
     if ((reinterpret_cast<uintptr_t>(codes) & 15) || (reinterpret_cast<uintptr_t>(scales) & 3))
@@ -810,6 +933,7 @@ WQ_API wq_status wq_linear_forward_host(wq_weights_t h, const void* x_host, int 
     if (M == 0) return WQ_OK;
     if (!x_host || !y_host || !workspace) return fail(WQ_ERR_INVALID, "NULL buffer");
     if (workspace_bytes < wq_host_workspace_bytes(h, M)) return fail(WQ_ERR_INVALID, "workspace too small");
+    if (const wq_status d = check_device(h)) return d;
     const size_t wsb = wq_workspace_bytes(h, M);
     const size_t xb = static_cast<size_t>(M) * h->cfg.K * 2, yb = static_cast<size_t>(M) * h->cfg.N * 2;
     uint8_t* base = static_cast<uint8_t*>(workspace);
@@ -829,6 +953,7 @@ WQ_API wq_status wq_export_weights(wq_weights_t h, uint8_t* codes, uint8_t* scal
     if (!h) return fail(WQ_ERR_INVALID, "NULL handle");
     if (h->cfg.mode != WQ_MODE_W4A4) return fail(WQ_ERR_INVALID, "W8A8 handle: use wq_export_weights_w8a8");
     const int K = h->cfg.K, N = h->cfg.N, r = h->cfg.rank, no = h->cfg.n_outliers;
+    const int rp = h->r_pad, nop = h->no_pad;
     if (codes) WQ_CUDA(cudaMemcpy(codes, h->d_codes, static_cast<size_t>(N) * K / 2, cudaMemcpyDeviceToHost), "export");
     if (scales) {
         const size_t n_pad = align_up(static_cast<size_t>(N), wq::kBlockM);
@@ -841,24 +966,30 @@ WQ_API wq_status wq_export_weights(wq_weights_t h, uint8_t* codes, uint8_t* scal
                        ((n % 128) / 32) * 4 + (b % 4)];
     }
     if (gW) *gW = h->gW;
-    if (P && r) WQ_CUDA(cudaMemcpy(P, h->d_P, static_cast<size_t>(K) * r * 2, cudaMemcpyDeviceToHost), "export");
+    if (P && r) {
+        std::vector<uint16_t> pp(static_cast<size_t>(K) * rp);
+        WQ_CUDA(cudaMemcpy(pp.data(), h->d_P, pp.size() * 2, cudaMemcpyDeviceToHost), "export");
+        for (int k = 0; k < K; ++k)
+            for (int j = 0; j < r; ++j) P[static_cast<size_t>(k) * r + j] = pp[static_cast<size_t>(k) * rp + j];
+    }
     if (Q && r) {
-        std::vector<uint16_t> qt(static_cast<size_t>(N) * r);
+        std::vector<uint16_t> qt(static_cast<size_t>(N) * rp);
         WQ_CUDA(cudaMemcpy(qt.data(), h->d_Qt, qt.size() * 2, cudaMemcpyDeviceToHost), "export");
         for (int n = 0; n < N; ++n)
-            for (int j = 0; j < r; ++j) Q[static_cast<size_t>(j) * N + n] = qt[static_cast<size_t>(n) * r + j];
+            for (int j = 0; j < r; ++j) Q[static_cast<size_t>(j) * N + n] = qt[static_cast<size_t>(n) * rp + j];
     }
     if (W_omega && no) {
-        std::vector<uint16_t> wt(static_cast<size_t>(N) * no);
+        std::vector<uint16_t> wt(static_cast<size_t>(N) * nop);
         WQ_CUDA(cudaMemcpy(wt.data(), h->d_WOt, wt.size() * 2, cudaMemcpyDeviceToHost), "export");
         for (int n = 0; n < N; ++n)
-            for (int j = 0; j < no; ++j) W_omega[static_cast<size_t>(j) * N + n] = wt[static_cast<size_t>(n) * no + j];
+            for (int j = 0; j < no; ++j) W_omega[static_cast<size_t>(j) * N + n] = wt[static_cast<size_t>(n) * nop + j];
     }
     return WQ_OK;
 }
 
 WQ_API wq_status wq_check_device_error(wq_weights_t h, void* stream) {
     if (!h) return fail(WQ_ERR_INVALID, "NULL handle");
+    if (const wq_status d = check_device(h)) return d;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     WQ_CUDA(cudaStreamSynchronize(st), "stream synchronise");
     int v = 0;

@@ -1,8 +1,8 @@
-// wq_conv.cu -- the video VAE's 3x3x3 convolution (padding 1, batch 1) as an NVFP4 implicit GEMM
+// wq_conv.cu -- the video VAE's 3x3x3 convolution (padding 1, batch B) as an NVFP4 implicit GEMM
 // (LatentQuant, Abstract: NVFP4 execution of the Wan VAE).
 //
 // Reading taken: the input is quantised once, per voxel along channels (16-channel blocks, e4m3
-// scales) with one fp32 scale for the whole tensor -- a GEMM row gathers 27 voxels, so a
+// scales) with one fp32 scale for the whole [B, C, D, H, W] tensor -- a GEMM row gathers 27 voxels, so a
 // per-voxel scale would not factor out of the accumulator; no smoothing or rotation.  The
 // weight [C_out, C_in, 3, 3, 3] is the GEMM operand [N = C_out, K = (kd, kh, kw, c_in)].
 //
@@ -64,7 +64,9 @@ __global__ void __launch_bounds__(kAmaxThreads) conv_amax_kernel(const uint4* __
     }
 }
 
-__global__ void __launch_bounds__(256) conv_quant_kernel(const uint16_t* __restrict__ x, int C, int V,
+// Voxels are numbered over the batch: v = b V1 + (d H + h) W + w, V1 = D H W (a multiple of 8, so
+// an 8-voxel group never straddles two samples).
+__global__ void __launch_bounds__(256) conv_quant_kernel(const uint16_t* __restrict__ x, int C, int V, int V1,
                                                          const float* __restrict__ partial, int n_partial,
                                                          uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
                                                          float* __restrict__ g_out) {
@@ -90,7 +92,10 @@ __global__ void __launch_bounds__(256) conv_quant_kernel(const uint16_t* __restr
     for (int i = threadIdx.x; i < C * (kVox / 8); i += 256) {
         const int c = i / (kVox / 8), q = i % (kVox / 8);
         uint4 val = make_uint4(0, 0, 0, 0);
-        if (8 * q < nv) val = __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(c) * V + v0 + 8 * q));
+        if (8 * q < nv) {
+            const int gv = v0 + 8 * q, b = gv / V1, lv = gv % V1;
+            val = __ldg(reinterpret_cast<const uint4*>(x + (static_cast<size_t>(b) * C + c) * V1 + lv));
+        }
         *reinterpret_cast<uint4*>(tile + c * kVox + 8 * q) = val;
     }
     __syncthreads();
@@ -133,7 +138,7 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
 
 struct ConvParams {
-    int C, D, H, W, V, N, K, stages;
+    int C, D, H, W, V, V1, N, K, stages;     // V = B V1 voxels over the batch, V1 = D H W
     const uint8_t* xcodes;
     const uint8_t* xscales;
     const float* gx;
@@ -230,13 +235,14 @@ conv_gemm_kernel(const __grid_constant__ CUtensorMap tmB, const ConvParams p) {
             item_rc(item, mb, nb0, ng);
             const int m = mb * 128 + r;
             const bool m_ok = m < p.V;
-            const int d = m / (p.H * p.W), h = (m / p.W) % p.H, w = m % p.W;
+            const int bsm = m / p.V1, lm = m % p.V1;                 // sample, voxel in the sample
+            const int d = lm / (p.H * p.W), h = (lm / p.W) % p.H, w = lm % p.W;
             for (int s = 0; s < nst; ++s) {
                 const int tap = s / cpt, cc = s % cpt;
                 const int kd = tap / 9, kh = (tap / 3) % 3, kw = tap % 3;
                 const int di = d + kd - 1, hi = h + kh - 1, wi = w + kw - 1;
                 const bool valid = m_ok && di >= 0 && di < p.D && hi >= 0 && hi < p.H && wi >= 0 && wi < p.W;
-                const size_t vin = valid ? (static_cast<size_t>(di) * p.H + hi) * p.W + wi : 0;
+                const size_t vin = valid ? static_cast<size_t>(bsm) * p.V1 + (static_cast<size_t>(di) * p.H + hi) * p.W + wi : 0;
                 if (!mbar_wait(bar_empty + 8u * stage, ph ^ 1u, abort_flag, p.err, 22)) { ok = false; break; }
                 const uint32_t st = base + static_cast<uint32_t>(stage) * kCStage;
                 const uint8_t* src = p.xcodes + vin * (p.C / 2) + cc * 64;
@@ -327,11 +333,12 @@ conv_gemm_kernel(const __grid_constant__ CUtensorMap tmB, const ConvParams p) {
                     tmem_ld_32x32b_x32(tmem + 128u * g + 32u * ch + t_lane, acc);
                     tmem_wait_ld();
                     if (m < p.V) {
+                        const size_t ybase = static_cast<size_t>(m / p.V1) * p.N * p.V1 + m % p.V1;
 #pragma unroll
                         for (int i = 0; i < 32; ++i) {
                             const int n = (nb0 + g) * 128 + ch * 32 + i;
                             if (n < p.N)
-                                p.y[static_cast<size_t>(n) * p.V + m] = __float2bfloat16_rn(alpha * __uint_as_float(acc[i]));
+                                p.y[ybase + static_cast<size_t>(n) * p.V1] = __float2bfloat16_rn(alpha * __uint_as_float(acc[i]));
                         }
                     }
                 }
@@ -372,7 +379,8 @@ cudaError_t launch_conv_quant(const ConvArgs& a, cudaStream_t st) {
         attr = true;
     }
     conv_quant_kernel<<<(a.V + kVox - 1) / kVox, 256, smem, st>>>(static_cast<const uint16_t*>(a.x), a.C, a.V,
-                                                                 a.partial, grid_a, a.codes, a.scales, a.g);
+                                                                 a.D * a.H * a.W, a.partial, grid_a, a.codes,
+                                                                 a.scales, a.g);
     return cudaGetLastError();
 }
 
@@ -390,7 +398,8 @@ cudaError_t launch_conv_gemm(const ConvArgs& a, cudaStream_t st) {
         attr = true;
     }
     ConvParams p{};
-    p.C = a.C; p.D = a.D; p.H = a.H; p.W = a.W; p.V = a.V; p.N = a.N; p.K = 27 * a.C; p.stages = stages;
+    p.C = a.C; p.D = a.D; p.H = a.H; p.W = a.W; p.V = a.V; p.V1 = a.D * a.H * a.W; p.N = a.N; p.K = 27 * a.C;
+    p.stages = stages;
     p.xcodes = a.codes; p.xscales = a.scales; p.gx = a.g; p.gw = a.gw; p.sfb = a.sfb;
     p.y = static_cast<__nv_bfloat16*>(a.y); p.err = a.err;
     const int n_tiles = (a.N + 127) / 128;

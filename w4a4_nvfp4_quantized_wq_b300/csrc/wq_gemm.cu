@@ -636,9 +636,9 @@ cudaError_t gemm_attributes() {
 
 template <bool kW8>
 Plan gemm_plan(const GemmArgs& a) {
-    // WQ_GEMM_STAGES=<n> caps the shared-memory ring depth (tuning)
-    const char* ms = std::getenv("WQ_GEMM_STAGES");
-    return make_plan(a.r, a.n_out, ms ? std::atoi(ms) : 8, kW8);
+    // the WQ_GEMM_STAGES knob caps the shared-memory ring depth (tuning)
+    const int ms = tune(kTuneGemmStages);
+    return make_plan(a.r, a.n_out, ms > 0 ? ms : 8, kW8);
 }
 
 // CTAs per output tile of the single-CTA schedule: the forced value, or the largest cluster
@@ -661,7 +661,7 @@ cudaError_t launch_gemm_t(const GemmArgs& a, cudaStream_t st) {
     const int split = gemm_split<kW8>(a, pl);
     if (split > num_kt || split > 16 || (split & (split - 1))) return cudaErrorInvalidValue;
     // split-K push form: the receive slots (per rows x split senders x 512 B) go in ring stages
-    // no CTA of the cluster fills; WQ_GEMM_PUSH=0 keeps the pull form (tests and tuning)
+    // no CTA of the cluster fills; the WQ_GEMM_PUSH knob at 0 keeps the pull form (tests and tuning)
     uint32_t off_recv = 0;
     if (split > 1) {
         const int valid = a.M < 128 ? a.M : 128;
@@ -670,8 +670,7 @@ cudaError_t launch_gemm_t(const GemmArgs& a, cudaStream_t st) {
         const uint32_t need = static_cast<uint32_t>(per * split) * 512u;
         if (used < pl.stages && static_cast<uint32_t>(pl.stages - used) * stage_bytes(kW8) >= need)
             off_recv = static_cast<uint32_t>(used) * stage_bytes(kW8);
-        if (const char* fp = std::getenv("WQ_GEMM_PUSH"))
-            if (fp[0] == '0') off_recv = 0;
+        if (tune(kTuneGemmPush) == 0) off_recv = 0;
     }
     KParams kp{};
     kp.split = split;
@@ -710,7 +709,8 @@ cudaError_t launch_gemm_t(const GemmArgs& a, cudaStream_t st) {
 // The pair schedule or not (see launch_gemm).
 bool use_wide(const GemmArgs& a) {
     bool wide = !a.w8 && a.force_split == 0 && a.K >= 4096 && wide_gemm_tiles(a.M, a.N) >= a.num_sms / 2;
-    if (const char* fw = std::getenv("WQ_GEMM_WIDE")) wide = fw[0] == '1' && a.force_split == 0;
+    const int fw = tune(kTuneGemmWide);
+    if (fw >= 0) wide = fw == 1 && a.force_split == 0;
     return wide;
 }
 

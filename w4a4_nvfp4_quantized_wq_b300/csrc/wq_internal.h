@@ -19,12 +19,34 @@ struct ActWorkspace {
     uint8_t* codes = nullptr;       // [M, K/2]
     uint8_t* sf = nullptr;          // MMA layout, ceil(M/128) * K/64 atoms
     float* g = nullptr;             // [M]
-    uint16_t* u = nullptr;          // [M, r] bf16
-    uint16_t* xo = nullptr;         // [M, n_outliers] fp16
+    uint16_t* u = nullptr;          // [M, r] bf16 (r: stored rank)
+    uint16_t* xo = nullptr;         // [M, n_out] fp16 (n_out: stored width)
+    unsigned int* amax = nullptr;   // batch maximum of WQ_ACT_SCALE_TENSOR (fp32 bits)
     size_t bytes = 0;
 };
 
+// r and n_out are the stored widths (side_width of the configured counts).
 ActWorkspace carve_workspace(void* base, int M, int K, int r, int n_out);
+
+// Stored width of a 16-bit side operand (U columns, x_O columns): 0, 16, 32 or 64, the widths
+// the tcgen05 side MMAs and the 32/64/128-byte swizzled TMA boxes take; the columns beyond the
+// configured count hold zeros.
+inline int side_width(int n) { return n == 0 ? 0 : (n <= 16 ? 16 : (n <= 32 ? 32 : 64)); }
+
+// Schedule knobs (tests and tuning): taken from the environment once, at first use, and changed
+// afterwards only through wq_set_tuning.  -1 (or 0 where stated) means "choose automatically".
+enum TuneKnob {
+    kTuneFused = 0,        // WQ_FUSED: 1 = the fused small-batch kernel where it applies
+    kTuneGemmSplit,        // WQ_GEMM_SPLIT: CTAs per output tile of the single-CTA GEMM (0 = auto)
+    kTuneGemmWide,         // WQ_GEMM_WIDE: 1 / 0 pins the CTA-pair GEMM on / off
+    kTuneGemmPush,         // WQ_GEMM_PUSH: 0 = pull form of the split-K reduction
+    kTuneGemmStages,       // WQ_GEMM_STAGES: ring depth cap of the single-CTA GEMM (0 = auto)
+    kTuneQuantSchedule,    // WQ_QUANT_SCHEDULE: 1 = stream, 0 = cluster (or "stream" / "cluster")
+    kTuneQuantSplit,       // WQ_QUANT_SPLIT: CTAs per row tile of the cluster quantiser (0 = auto)
+    kTuneQuantCtasPerSm,   // WQ_QUANT_CTAS_PER_SM: resident stream-quantiser CTAs per SM (0 = auto)
+    kTuneCount
+};
+int tune(TuneKnob k);
 
 struct QuantArgs {
     const void* x;                  // bf16 [M, K]
@@ -35,10 +57,11 @@ struct QuantArgs {
     const float* inv_s;             // [K] or null; per 32-channel half, pairs (s_k, s_k+16), k = 0..15
     int rotate;
     const uint32_t* omega_blk;      // [K/64][4]: kept-channel mask (lo, hi), x_O index of the first, 0
-    int n_out;
-    uint16_t* xo;                   // fp16 [M, n_out]
+    int n_out;                      // kept channels (0: none)
+    int xo_ld;                      // row stride of x_O in elements (>= n_out; the columns beyond are zeroed)
+    uint16_t* xo;                   // fp16 [M, xo_ld]
     const uint16_t* P;              // bf16 [K, r]
-    int r;
+    int r;                          // stored rank (0, 16, 32 or 64); U columns beyond the rank are 0
     uint16_t* u;                    // bf16 [M, r]
     uint8_t* codes;                 // [M, K/2]
     uint8_t* sf;                    // scales, layout per `sf_layout`
@@ -46,6 +69,12 @@ struct QuantArgs {
     float* g;                       // [M]
     int num_sms;                    // used to spread small batches over more CTAs
     bool int8 = false;              // 8-bit layer: codes are int8 values stored as bf16 [M, K]
+    // Activation tensor scale: WQ_ACT_SCALE_ROW (one per row, from the row), WQ_ACT_SCALE_TENSOR
+    // (one for all M rows: a first launch takes the maximum, a second quantises) or
+    // WQ_ACT_SCALE_STATIC (the calibrated `static_g`, one pass).  Every mode writes g[m] per row.
+    int act_scale = WQ_ACT_SCALE_ROW;
+    float static_g = 0.0f;
+    unsigned int* amax_bits = nullptr;  // WQ_ACT_SCALE_TENSOR: running maximum (fp32 bits), zeroed by the caller
 };
 
 cudaError_t launch_quantize_act(const QuantArgs& a, cudaStream_t stream);
@@ -105,8 +134,8 @@ bool fused_plan(int M, int K, int N, int r, int n_out, int& nb, int& cs);
 cudaError_t launch_fused(const FusedArgs& a, cudaStream_t stream);
 
 struct ConvArgs {
-    const void* x;            // bf16 NCDHW [1, C, D, H, W]
-    int C, D, H, W, V, N;     // V = D H W voxels, N output channels
+    const void* x;            // bf16 NCDHW [B, C, D, H, W]
+    int C, D, H, W, V, N;     // V = B D H W voxels over the batch, N output channels
     float* partial;           // [2 num_sms] per-CTA maxima of |x|
     float* g;                 // tensor scale of the input
     uint8_t* codes;           // [V, C/2]
@@ -114,7 +143,7 @@ struct ConvArgs {
     const CUtensorMap* tmB;   // weight codes [N, 27 C / 2] u8, box 64 x 128, swizzle 64B
     const uint8_t* sfb;       // weight scales, MMA layout
     float gw;
-    void* y;                  // bf16 NCDHW [1, N, D, H, W]
+    void* y;                  // bf16 NCDHW [B, N, D, H, W]
     int* err;
     int num_sms;
 };
@@ -125,6 +154,9 @@ cudaError_t launch_conv_gemm(const ConvArgs& a, cudaStream_t stream);
 
 // Record a message for wq_last_error() (thread-local).
 void set_last_error(const char* msg);
+
+// The device a handle's memory lives on (the device current at its preparation).
+int handle_device(wq_weights_t h);
 
 // cuTensorMapEncodeTiled obtained from the driver at run time (no libcuda link).
 bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,

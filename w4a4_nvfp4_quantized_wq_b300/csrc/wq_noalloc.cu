@@ -46,6 +46,11 @@ extern "C" WQ_API wq_status wq_linear_forward_noalloc(wq_weights_t h, const void
         wq::set_last_error("wq_linear_forward_noalloc: cannot determine the current device");
         return WQ_ERR_CUDA;
     }
+    // the scratch must be the copy on the handle's device, where the kernels run
+    if (dev != wq::handle_device(h)) {
+        wq::set_last_error("wq_linear_forward_noalloc: the current device is not the handle's device");
+        return WQ_ERR_INVALID;
+    }
     void* scratch = nullptr;
     {
         std::lock_guard<std::mutex> lk(g_mu);

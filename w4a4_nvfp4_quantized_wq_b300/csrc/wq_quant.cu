@@ -94,6 +94,7 @@ struct QParams {
     int rotate;
     const uint32_t* omega_blk;   // per block: kept-channel mask (2 words), x_O index of the first
     int n_out;
+    int xo_ld;                   // row stride of x_O (columns n_out .. xo_ld-1 are written as zeros)
     uint16_t* xo;
     const uint32_t* pfrag;   // low-rank factor P in mma.sync B-fragment order
     uint16_t* u;
@@ -102,7 +103,24 @@ struct QParams {
     int sf_layout;
     float* g;
     int* err;
+    // stream kernel phase: 0 both passes with the row's own scale (WQ_ACT_SCALE_ROW); 1 first pass
+    // only, row maxima folded into *amax_bits; 2 second pass only, g from *amax_bits; 3 one pass
+    // with the fixed g = static_g (WQ_ACT_SCALE_STATIC)
+    int phase;
+    float static_g;
+    unsigned int* amax_bits;
 };
+
+// Zero the x_O columns beyond the kept channels for the rows of one tile (they meet zero weight
+// rows in the GEMM, which reads the full stored width).
+__device__ __forceinline__ void zero_xo_pad(const QParams& p, int tile, int tid, int nthreads) {
+    const int pad = p.xo_ld - p.n_out;
+    if (p.n_out == 0 || pad <= 0) return;
+    for (int i = tid; i < kRows * pad; i += nthreads) {
+        const int row = tile * kRows + i / pad;
+        if (row < p.M) p.xo[static_cast<size_t>(row) * p.xo_ld + p.n_out + i % pad] = 0;
+    }
+}
 
 // Pull block kb's slice of the packed P (NT KiB) towards this SM's L1, one 128-byte line per
 // lane, ahead of the U step that reads it.
@@ -287,7 +305,7 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmX, const QParams p) {
             // kept channels: fp16 value out and +0 in the slot (channel e of the half is float
             // 2 (e % 16) + e / 16 of the stored row-half), +0 in the registers
             uint32_t idx = s_omega[4 * i + 2] + (half ? static_cast<uint32_t>(__popc(m0)) : 0u);
-            uint16_t* xrow = p.xo + static_cast<size_t>(row) * p.n_out;
+            uint16_t* xrow = p.xo + static_cast<size_t>(row) * p.xo_ld;
             for (uint32_t m = mine; m != 0u; m &= m - 1u, ++idx) {
                 const uint32_t e = static_cast<uint32_t>(__ffs(m) - 1);
                 const uint32_t a = rowb + 4u * (2u * (e & 15u) + (e >> 4));
@@ -305,6 +323,7 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmX, const QParams p) {
 
     // ---- row amax and U over the CTA's warps (in warp order), then over the cluster
     if (threadIdx.x == 0) WQ_QTRACE_AT(3);
+    if (rank == 0) zero_xo_pad(p, tile, threadIdx.x, kConsumerWarps * 32);
     amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 16));
     if (half == 0) s_amax[warp * kRows + r] = amax;
     named_bar_sync(1, kConsumerWarps * 32);
@@ -448,8 +467,9 @@ quantize_stream_kernel(const __grid_constant__ CUtensorMap tmX, const QParams p)
             if (p.n_out) bulk_load(base + lay.off_omega, p.omega_blk, 16u * nblk, bar_const);
             uint32_t q = 0;
             bool ok = true;
+            const int passes = p.phase == 0 ? 2 : 1;
             for (int tile = blockIdx.x; ok && tile < p.row_tiles; tile += gridDim.x)
-                for (int pass = 0; ok && pass < 2; ++pass)
+                for (int pass = 0; ok && pass < passes; ++pass)
                     for (int kb = 0; kb < nblk; ++kb, ++q) {
                         const uint32_t s = q % kRing;
                         if (q >= kRing && !mbar_wait(bar_empty + 8u * s, ((q / kRing) - 1u) & 1u, abort_flag, p.err, 21)) {
@@ -474,114 +494,142 @@ quantize_stream_kernel(const __grid_constant__ CUtensorMap tmX, const QParams p)
     const int active = nblk < kConsumerWarps ? nblk : kConsumerWarps;
     const uint32_t upart = base + lay.off_upart + static_cast<uint32_t>(warp * NT) * 512u;
     bool ok = __all_sync(kFullMask, mbar_wait(bar_const, 0, abort_flag, p.err, 24));
+    const bool first_pass = p.phase != 2;     // smoothing, FWHT, U, x_O, maxima
+    const bool second_pass = p.phase == 0 || p.phase == 2;
+    // phase 2: the batch maximum was folded in by the previous grid; phase 3: the calibrated g
+    float g_fixed = p.static_g;
+    if (p.phase == 2) {
+        griddep_wait();
+        g_fixed = __fdiv_rn(__uint_as_float(*reinterpret_cast<volatile unsigned int*>(p.amax_bits)), 2688.0f);
+    }
+    float cta_amax = 0.0f;                             // phase 1: maximum over this CTA's rows
     uint32_t q0 = 0;                                   // ring sequence number of the tile's first block
     QPH_DECL;
     // every warp runs every tile's barriers, also after a failed wait (ok == false skips work)
     for (int tile = blockIdx.x; tile < p.row_tiles; tile += gridDim.x) {
         const int row = tile * kRows + r;
         const bool row_ok = row < p.M;
-        uint16_t* xrow = p.xo + static_cast<size_t>(row) * p.n_out;
-        // ---- pass 1
-        float amax = 0.0f;
-        if (tile == static_cast<int>(blockIdx.x)) prefetch_block_consts<NT>(p, warp, lane);
-        for (int kb = warp; ok && kb < nblk; kb += kConsumerWarps) {
-            const uint32_t q = q0 + static_cast<uint32_t>(kb), s = q % kRing;
-            prefetch_block_consts<NT>(p, kb + kConsumerWarps < nblk ? kb + kConsumerWarps : warp, lane);
-            QPH(3);
-            if (!__all_sync(kFullMask, mbar_wait(bar_full + 8u * s, (q / kRing) & 1u, abort_flag, p.err, 25))) {
-                ok = false;
-                break;
-            }
-            QPH(0);
-            const uint32_t box = base + s * kBoxBytes;
-            f2 P[16];
-            load_transform(box, r, half, p.inv_s ? s_invs + 256u * s : 0u, p.rotate, P);
-            QPH(1);
-            if constexpr (R > 0) u_step<NT>(box, lane, kb, p.pfrag, upart, kb == warp);
-            QPH(2);
-            const uint32_t m0 = p.n_out ? s_omega[4 * kb] : 0u, m1 = p.n_out ? s_omega[4 * kb + 1] : 0u;
-            if ((m0 | m1) != 0u) {
-                // kept channels: fp16 values out through a copy in the consumed box (lane l
-                // writes its 32 channels as fp16 pairs at l * 64 B), +0 in the registers
-                __syncwarp();                  // every lane is done reading the box
-                const uint32_t sc = box + static_cast<uint32_t>(lane) * 64u;
+        uint16_t* xrow = p.xo + static_cast<size_t>(row) * p.xo_ld;
+        float gsc = g_fixed;
+        float rg_inv = __frcp_rn(g_fixed);
+        if (first_pass) {
+            // ---- pass 1 (phase 3: the only pass, codes out with the fixed g)
+            float amax = 0.0f;
+            if (tile == static_cast<int>(blockIdx.x)) prefetch_block_consts<NT>(p, warp, lane);
+            for (int kb = warp; ok && kb < nblk; kb += kConsumerWarps) {
+                const uint32_t q = q0 + static_cast<uint32_t>(kb), s = q % kRing;
+                prefetch_block_consts<NT>(p, kb + kConsumerWarps < nblk ? kb + kConsumerWarps : warp, lane);
+                QPH(3);
+                if (!__all_sync(kFullMask, mbar_wait(bar_full + 8u * s, (q / kRing) & 1u, abort_flag, p.err, 25))) {
+                    ok = false;
+                    break;
+                }
+                QPH(0);
+                const uint32_t box = base + s * kBoxBytes;
+                f2 P[16];
+                load_transform(box, r, half, p.inv_s ? s_invs + 256u * s : 0u, p.rotate, P);
+                QPH(1);
+                if constexpr (R > 0) u_step<NT>(box, lane, kb, p.pfrag, upart, kb == warp);
+                QPH(2);
+                const uint32_t m0 = p.n_out ? s_omega[4 * kb] : 0u, m1 = p.n_out ? s_omega[4 * kb + 1] : 0u;
+                if ((m0 | m1) != 0u) {
+                    // kept channels: fp16 values out through a copy in the consumed box (lane l
+                    // writes its 32 channels as fp16 pairs at l * 64 B), +0 in the registers
+                    __syncwarp();                  // every lane is done reading the box
+                    const uint32_t sc = box + static_cast<uint32_t>(lane) * 64u;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    uint32_t hw[4];
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t hw[4];
 #pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        const __half2 h2 = __floats2half2_rn(lo2(P[4 * j + t]), hi2(P[4 * j + t]));
-                        hw[t] = *reinterpret_cast<const uint32_t*>(&h2);
+                        for (int t = 0; t < 4; ++t) {
+                            const __half2 h2 = __floats2half2_rn(lo2(P[4 * j + t]), hi2(P[4 * j + t]));
+                            hw[t] = *reinterpret_cast<const uint32_t*>(&h2);
+                        }
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(sc + 16u * j), "r"(hw[0]), "r"(hw[1]),
+                                     "r"(hw[2]), "r"(hw[3]) : "memory");
                     }
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(sc + 16u * j), "r"(hw[0]), "r"(hw[1]),
-                                 "r"(hw[2]), "r"(hw[3]) : "memory");
+                    const uint32_t mine = half ? m1 : m0;
+                    uint32_t idx = s_omega[4 * kb + 2] + (half ? static_cast<uint32_t>(__popc(m0)) : 0u);
+                    for (uint32_t m = mine; m != 0u; m &= m - 1u, ++idx) {
+                        const uint32_t e = static_cast<uint32_t>(__ffs(m) - 1);
+                        uint16_t hv;
+                        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(hv) : "r"(sc + 4u * (e & 15u) + 2u * (e >> 4)) : "memory");
+                        if (row_ok) xrow[idx] = hv;
+                    }
+                    if (mine != 0u) apply_keep(P, mine);
                 }
-                const uint32_t mine = half ? m1 : m0;
-                uint32_t idx = s_omega[4 * kb + 2] + (half ? static_cast<uint32_t>(__popc(m0)) : 0u);
-                for (uint32_t m = mine; m != 0u; m &= m - 1u, ++idx) {
-                    const uint32_t e = static_cast<uint32_t>(__ffs(m) - 1);
-                    uint16_t hv;
-                    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(hv) : "r"(sc + 4u * (e & 15u) + 2u * (e >> 4)) : "memory");
-                    if (row_ok) xrow[idx] = hv;
-                }
-                if (mine != 0u) apply_keep(P, mine);
-            }
-            float ma, mb;
-            absmax_pairs(P, ma, mb);
-            amax = fmaxf(amax, fmaxf(ma, mb));
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_empty + 8u * s);
-        }
-        QPH(3);
-        // ---- row amax and U over the warps, in warp order
-        amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 16));
-        if (half == 0) s_amax[warp * kRows + r] = amax;
-        named_bar_sync(1, kConsumerWarps * 32);
-        amax = 0.0f;
-        for (int w = 0; w < active; ++w) amax = fmaxf(amax, s_amax[w * kRows + r]);
-        if constexpr (R > 0) {
-            for (int idx = threadIdx.x; idx < NT * 128; idx += kConsumerWarps * 32) {
-                float sum = 0.0f;
-                for (int w = 0; w < active; ++w)
-                    sum = __fadd_rn(sum, ld_shared_f32(base + lay.off_upart + static_cast<uint32_t>(w * NT) * 512u + 4u * idx));
-                int rr, cc;
-                frag_pos(idx, rr, cc);
-                const int rg = tile * kRows + rr;
-                if (rg < p.M) p.u[static_cast<size_t>(rg) * R + cc] = __bfloat16_as_ushort(__float2bfloat16_rn(sum));
-            }
-        }
-        named_bar_sync(1, kConsumerWarps * 32);        // maxima and partials are free again
-        const float gsc = __fdiv_rn(amax, kInt8 ? 127.0f : 2688.0f);
-        const float rg_inv = __frcp_rn(gsc);
-        if (warp == 0 && half == 0 && row_ok) p.g[row] = gsc;
-        q0 += static_cast<uint32_t>(nblk);
-        QPH(4);
-        // ---- pass 2: the blocks again (from L2), transform recomputed
-        for (int kb = warp; ok && kb < nblk; kb += kConsumerWarps) {
-            const uint32_t q = q0 + static_cast<uint32_t>(kb), s = q % kRing;
-            QPH(7);
-            if (!__all_sync(kFullMask, mbar_wait(bar_full + 8u * s, (q / kRing) & 1u, abort_flag, p.err, 26))) {
-                ok = false;
-                break;
-            }
-            QPH(5);
-            f2 P[16];
-            load_transform(base + s * kBoxBytes, r, half, p.inv_s ? s_invs + 256u * s : 0u, p.rotate, P);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_empty + 8u * s);
-            QPH(6);
-            const uint32_t m0 = p.n_out ? s_omega[4 * kb] : 0u, m1 = p.n_out ? s_omega[4 * kb + 1] : 0u;
-            if ((half ? m1 : m0) != 0u) apply_keep(P, half ? m1 : m0);
-            if constexpr (kInt8) {
-                emit_int8<false>(P, gsc, rg_inv, row, row_ok, kb, half, p);
-            } else {
                 float ma, mb;
                 absmax_pairs(P, ma, mb);
-                emit_nvfp4<false>(P, ma, mb, gsc, rg_inv, row, row_ok, kb, half, p);
+                amax = fmaxf(amax, fmaxf(ma, mb));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_empty + 8u * s);
+                if constexpr (!kInt8)
+                    if (p.phase == 3) emit_nvfp4<false>(P, ma, mb, gsc, rg_inv, row, row_ok, kb, half, p);
             }
+            QPH(3);
+            // ---- row amax and U over the warps, in warp order
+            amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 16));
+            if (half == 0) s_amax[warp * kRows + r] = amax;
+            named_bar_sync(1, kConsumerWarps * 32);
+            amax = 0.0f;
+            for (int w = 0; w < active; ++w) amax = fmaxf(amax, s_amax[w * kRows + r]);
+            if constexpr (R > 0) {
+                for (int idx = threadIdx.x; idx < NT * 128; idx += kConsumerWarps * 32) {
+                    float sum = 0.0f;
+                    for (int w = 0; w < active; ++w)
+                        sum = __fadd_rn(sum, ld_shared_f32(base + lay.off_upart + static_cast<uint32_t>(w * NT) * 512u + 4u * idx));
+                    int rr, cc;
+                    frag_pos(idx, rr, cc);
+                    const int rg = tile * kRows + rr;
+                    if (rg < p.M) p.u[static_cast<size_t>(rg) * R + cc] = __bfloat16_as_ushort(__float2bfloat16_rn(sum));
+                }
+            }
+            zero_xo_pad(p, tile, threadIdx.x, kConsumerWarps * 32);
+            named_bar_sync(1, kConsumerWarps * 32);        // maxima and partials are free again
+            if (p.phase == 0) {
+                gsc = __fdiv_rn(amax, kInt8 ? 127.0f : 2688.0f);
+                rg_inv = __frcp_rn(gsc);
+            }
+            cta_amax = fmaxf(cta_amax, amax);
+            q0 += static_cast<uint32_t>(nblk);
         }
-        q0 += static_cast<uint32_t>(nblk);
+        if (warp == 0 && half == 0 && row_ok && p.phase != 1) p.g[row] = gsc;
+        QPH(4);
+        if (second_pass) {
+            // ---- pass 2: the blocks again (from L2), transform recomputed
+            for (int kb = warp; ok && kb < nblk; kb += kConsumerWarps) {
+                const uint32_t q = q0 + static_cast<uint32_t>(kb), s = q % kRing;
+                QPH(7);
+                if (!__all_sync(kFullMask, mbar_wait(bar_full + 8u * s, (q / kRing) & 1u, abort_flag, p.err, 26))) {
+                    ok = false;
+                    break;
+                }
+                QPH(5);
+                f2 P[16];
+                load_transform(base + s * kBoxBytes, r, half, p.inv_s ? s_invs + 256u * s : 0u, p.rotate, P);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_empty + 8u * s);
+                QPH(6);
+                const uint32_t m0 = p.n_out ? s_omega[4 * kb] : 0u, m1 = p.n_out ? s_omega[4 * kb + 1] : 0u;
+                if ((half ? m1 : m0) != 0u) apply_keep(P, half ? m1 : m0);
+                if constexpr (kInt8) {
+                    emit_int8<false>(P, gsc, rg_inv, row, row_ok, kb, half, p);
+                } else {
+                    float ma, mb;
+                    absmax_pairs(P, ma, mb);
+                    emit_nvfp4<false>(P, ma, mb, gsc, rg_inv, row, row_ok, kb, half, p);
+                }
+            }
+            q0 += static_cast<uint32_t>(nblk);
+        }
         QPH(7);
+    }
+    if (p.phase == 1 && warp == 0) {
+        // lanes 0..15 hold the maxima of the CTA's rows r; one atomic per CTA (non-negative
+        // floats order like their bit patterns)
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) cta_amax = fmaxf(cta_amax, __shfl_xor_sync(kFullMask, cta_amax, o));
+        if (lane == 0) atomicMax(p.amax_bits, __float_as_uint(cta_amax));
     }
     QPH_FLUSH;
 }
@@ -635,11 +683,9 @@ cudaError_t launch_r(const CUtensorMap& tm, const QParams& qp, bool stream, int 
         // the second pass comes from DRAM: the kernel is latency-bound with DRAM well below its
         // peak, so more warps per SM pay more than the extra reads cost (K = 8960: 383 us at two
         // CTAs per SM, 339 us at three).
-        // WQ_QUANT_CTAS_PER_SM=<n> overrides the residency (tuning)
-        if (const char* fc = std::getenv("WQ_QUANT_CTAS_PER_SM")) {
-            const int v = std::atoi(fc);
-            if (v >= 1 && v <= per_sm + 8) per_sm = v;
-        }
+        // the WQ_QUANT_CTAS_PER_SM knob overrides the residency (tuning)
+        const int v = tune(kTuneQuantCtasPerSm);
+        if (v >= 1 && v <= per_sm + 8) per_sm = v;
         const int grid = qp.row_tiles < per_sm * num_sms ? qp.row_tiles : per_sm * num_sms;
         cfg.gridDim = dim3(static_cast<unsigned>(grid));
         cfg.dynamicSmemBytes = lay.total;
@@ -667,11 +713,9 @@ cudaError_t launch_r(const CUtensorMap& tm, const QParams& qp, bool stream, int 
 bool quant_stream_schedule(int M, int num_sms) {
     // many row tiles: the persistent stream schedule; few: spread K over clusters
     bool stream = (M + kRows - 1) / kRows >= 2 * num_sms;
-    // WQ_QUANT_SCHEDULE=stream|cluster pins the schedule (tuning and tests)
-    if (const char* fm = std::getenv("WQ_QUANT_SCHEDULE")) {
-        if (fm[0] == 's') stream = true;
-        if (fm[0] == 'c') stream = false;
-    }
+    // the WQ_QUANT_SCHEDULE knob pins the schedule (tuning and tests)
+    const int fm = tune(kTuneQuantSchedule);
+    if (fm >= 0) stream = fm == 1;
     return stream;
 }
 
@@ -679,10 +723,12 @@ cudaError_t launch_quantize_act(const QuantArgs& a, cudaStream_t st) {
     if (a.M <= 0) return cudaSuccess;
     Choice ch = choose(a.K);
     const int row_tiles = (a.M + kRows - 1) / kRows;
-    const bool stream = quant_stream_schedule(a.M, a.num_sms);
-    // WQ_QUANT_SPLIT=<n> pins the CTAs per row tile of the cluster schedule (tuning and tests)
-    if (const char* fs = std::getenv("WQ_QUANT_SPLIT")) {
-        const int v = std::atoi(fs);
+    // batch-wide tensor scales run on the stream kernel: the maximum and the codes as two
+    // launches (TENSOR) or the codes in one pass (STATIC)
+    const bool stream = a.act_scale != WQ_ACT_SCALE_ROW || quant_stream_schedule(a.M, a.num_sms);
+    // the WQ_QUANT_SPLIT knob pins the CTAs per row tile of the cluster schedule (tuning and tests)
+    {
+        const int v = tune(kTuneQuantSplit);
         const int nblk = a.K / 64;
         if (v >= 1 && v <= 16 && v <= nblk && (nblk + v - 1) / v <= kMaxBlocks) ch = Choice{v, (nblk + v - 1) / v};
     }
@@ -691,16 +737,35 @@ cudaError_t launch_quantize_act(const QuantArgs& a, cudaStream_t st) {
     qp.M = a.M; qp.K = a.K; qp.nblk = a.K / 64; qp.csplit = ch.csplit; qp.max_nb = ch.max_nb;
     qp.row_tiles = row_tiles;
     qp.inv_s = a.inv_s; qp.rotate = a.rotate; qp.omega_blk = a.omega_blk; qp.n_out = a.n_out; qp.xo = a.xo;
+    qp.xo_ld = a.xo_ld > a.n_out ? a.xo_ld : a.n_out;
+    qp.phase = a.act_scale == WQ_ACT_SCALE_STATIC ? 3 : 0;
+    qp.static_g = a.static_g;
+    qp.amax_bits = a.amax_bits;
     qp.pfrag = a.pfrag; qp.u = a.u; qp.codes = a.codes; qp.sf = a.sf; qp.sf_layout = a.sf_layout; qp.g = a.g;
     qp.err = a.err;
-    if (a.int8) return a.r == 0 && a.n_out == 0 ? launch_r<0, true>(*a.tmX, qp, stream, a.num_sms, st) : cudaErrorInvalidValue;
-    switch (a.r) {
-        case 0: return launch_r<0, false>(*a.tmX, qp, stream, a.num_sms, st);
-        case 16: return launch_r<16, false>(*a.tmX, qp, stream, a.num_sms, st);
-        case 32: return launch_r<32, false>(*a.tmX, qp, stream, a.num_sms, st);
-        case 64: return launch_r<64, false>(*a.tmX, qp, stream, a.num_sms, st);
-        default: return cudaErrorInvalidValue;
+    if (a.int8)
+        return a.r == 0 && a.n_out == 0 && qp.phase == 0 ? launch_r<0, true>(*a.tmX, qp, stream, a.num_sms, st)
+                                                         : cudaErrorInvalidValue;
+    auto launch = [&](const QParams& q) -> cudaError_t {
+        switch (a.r) {
+            case 0: return launch_r<0, false>(*a.tmX, q, stream, a.num_sms, st);
+            case 16: return launch_r<16, false>(*a.tmX, q, stream, a.num_sms, st);
+            case 32: return launch_r<32, false>(*a.tmX, q, stream, a.num_sms, st);
+            case 64: return launch_r<64, false>(*a.tmX, q, stream, a.num_sms, st);
+            default: return cudaErrorInvalidValue;
+        }
+    };
+    if (a.act_scale == WQ_ACT_SCALE_TENSOR) {
+        if (!a.amax_bits) return cudaErrorInvalidValue;
+        QParams q1 = qp;
+        q1.phase = 1;                   // maxima (and U, x_O), no codes
+        const cudaError_t e = launch(q1);
+        if (e != cudaSuccess) return e;
+        QParams q2 = qp;
+        q2.phase = 2;                   // codes with the batch's g
+        return launch(q2);
     }
+    return launch(qp);
 }
 
 }  // namespace wq

@@ -242,8 +242,8 @@ def make_layer_inputs(workload: str, layer: int = 0, M: Optional[int] = None,
 
 
 def make_conv_inputs(T: Optional[int] = None, H: Optional[int] = None, W: Optional[int] = None,
-                     C_in: Optional[int] = None, C_out: Optional[int] = None):
-    """VAE Conv3d input (NCDHW bf16 bits, batch 1) and weights [C_out, C_in, 3, 3, 3] fp32."""
+                     C_in: Optional[int] = None, C_out: Optional[int] = None, B: int = 1):
+    """VAE Conv3d input (NCDHW bf16 bits, batch B) and weights [C_out, C_in, 3, 3, 3] fp32."""
     c = dict(CONV)
     T = c["T"] if T is None else T
     H = c["H"] if H is None else H
@@ -251,7 +251,7 @@ def make_conv_inputs(T: Optional[int] = None, H: Optional[int] = None, W: Option
     Ci = c["C_in"] if C_in is None else C_in
     Co = c["C_out"] if C_out is None else C_out
     g = _rng(c["seed"], 0, 1)
-    x = g.standard_normal((1, Ci, T, H, W_), dtype=np.float32)
+    x = g.standard_normal((B, Ci, T, H, W_), dtype=np.float32)
     x[:, outlier_channels(Ci, c["n_outlier_ch"])] *= np.float32(c["outlier_mult"])
     w = _rng(c["seed"], 0, 3).standard_normal((Co, Ci, 3, 3, 3), dtype=np.float32) * np.float32(0.02)
     return bf16_bits(x), w
