@@ -708,7 +708,7 @@ cudaError_t launch_gemm_t(const GemmArgs& a, cudaStream_t st) {
 
 // The pair schedule or not (see launch_gemm).
 bool use_wide(const GemmArgs& a) {
-    bool wide = !a.w8 && a.force_split == 0 && a.K >= 4096 && wide_gemm_tiles(a.M, a.N) >= a.num_sms / 2;
+    bool wide = !a.w8 && a.force_split == 0 && a.K >= 1024 && wide_gemm_tiles(a.M, a.N) >= a.num_sms / 2;
     const int fw = tune(kTuneGemmWide);
     if (fw >= 0) wide = fw == 1 && a.force_split == 0;
     return wide;
@@ -728,11 +728,12 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
     if (a.M <= 0) return cudaSuccess;
     // Two schedules.  128 x 128 tiles on single CTAs (split-K over clusters when the tiles
     // alone cannot fill the GPU), bound by the tcgen05 issue of one N = 128 MMA and two scale
-    // copies per 64-deep K block.  256 x 256 tiles on CTA pairs: N = 256 pair MMAs need about
-    // 0.7x the issue time per flop, but the accumulator is single-buffered, so each tile pays
-    // the drain and the side branch (a few us) before the next main loop.  The pair schedule
-    // therefore wins on long K: it is chosen for 4-bit layers with K >= 4096 whose 256 x 256
-    // tiles fill every SM pair.  WQ_GEMM_WIDE=0/1 pins the choice (tests and tuning).
+    // copies per 64-deep K block.  256 x 256 tiles on CTA pairs: an MMA costs the same issue
+    // time at N = 128 and N = 256, and the pair kernel feeds its scale copies from a warp of
+    // their own, so its MMA stream runs at the instruction rate; the accumulator is
+    // single-buffered, so each tile pays the drain and the side branch before the next main
+    // loop.  It is chosen for 4-bit layers with K >= 1024 whose 256 x 256 tiles fill every SM
+    // pair.  The WQ_GEMM_WIDE knob pins the choice (tests and tuning).
     if (use_wide(a)) return launch_gemm_wide(a, st);
     return a.w8 ? launch_gemm_t<true>(a, st) : launch_gemm_t<false>(a, st);
 }

@@ -9,11 +9,15 @@
 //             scale atoms and all 256 rows' B scale atoms (each CTA's TMEM needs the whole
 //             tile's B scales), into an S-stage ring; after the K stages of a tile, the side
 //             operands (U with this CTA's Q^T rows; x_O with its W_O^T rows) as extra stages.
-//   warp 1    rank 0: TMEM (collective over the pair) and the single MMA-issuing thread:
-//             per stage tcgen05.cp.cta_group::2 of the scales (each CTA copies its own shared
-//             memory into its own TMEM) and the pair MMAs, whose completion frees the stage
-//             in both CTAs (multicast commit).  rank 1: relays "stage full" of its own ring to
-//             rank 0's barrier, since an mbarrier can only be waited on in its own CTA.
+//   warp 1    rank 0: TMEM (collective over the pair) and the single MMA-issuing thread: the
+//             pair MMAs of a stage once its scales are in TMEM; their completion frees the
+//             stage in both CTAs (multicast commit).  rank 1: relays "stage full" of its own
+//             ring to rank 0's barrier, since an mbarrier can only be waited on in its own CTA.
+//   warp 10   rank 0: the scale feeder.  Once both CTAs' halves of a stage have landed it
+//             issues the stage's tcgen05.cp.cta_group::2 copies of the scale atoms (each CTA
+//             copies its own shared memory into its own TMEM) and commits them to the stage's
+//             "scales ready" barrier.  A tcgen05.cp issued by the MMA thread itself stalls its
+//             MMA stream (~60-90 ns per copy on B300); from another warp it costs the MMAs nothing.
 //   warps 2-9 epilogue: two warps per TMEM lane quadrant, 128 columns each.  The 256-column
 //             accumulator fills TMEM's first half (the other half holds five stages of scale
 //             factors), so it is single-buffered: the epilogue drains it into registers and
@@ -34,7 +38,7 @@
 
 #ifdef WQ_TRACE
 // Wait-time counters for kernel development builds only (never defined in the product build).
-__device__ unsigned long long g_wq_wtrace[16];   // 10: drain, 11: side read, 12: stores
+__device__ unsigned long long g_wq_wtrace[16];   // 10: drain, 11: side read, 12: stores, 13: scales ready
 extern "C" WQ_API int wq_wtrace_read(void* host, size_t bytes) {
     return static_cast<int>(cudaMemcpyFromSymbol(host, g_wq_wtrace, bytes));
 }
@@ -48,8 +52,9 @@ extern "C" WQ_API int wq_wtrace_read(void* host, size_t bytes) {
 namespace wq {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kEpiWarps = 8;
+constexpr int kScaleWarp = 10;
 constexpr uint32_t kHalf = 128 * 128;                   // 128 rows x 128 bytes
 constexpr uint32_t kSfaOff = 2 * kHalf;                 // 4 A atoms (this CTA's rows)
 constexpr uint32_t kSfbOff = kSfaOff + 4 * kSfAtom;     // 4 atoms of B rows 0..127, then 4 of 128..255
@@ -113,7 +118,9 @@ wide_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     const uint32_t bar_sfull = bar_tempty + 8u;
     const uint32_t bar_sempty = bar_sfull + 8u;          // rank 0: both epilogues read the side results
     const uint32_t bar_final = bar_sempty + 8u;
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + p.off_bar + 8u * (3 * S + 5));
+    const uint32_t bar_sready = bar_final + 8u;          // rank 0: the stage's scales are in TMEM
+    const uint32_t bar_sfinal = bar_sready + 8u * S;     // rank 0: the feeder's copies have all completed
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + p.off_bar + 8u * (4 * S + 6));
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
     const int M = p.M, N = p.N;
@@ -135,6 +142,8 @@ wide_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         mbar_init(bar_sfull, 1);
         mbar_init(bar_sempty, 2 * kEpiWarps);
         mbar_init(bar_final, 1);
+        for (int s = 0; s < S; ++s) mbar_init(bar_sready + 8u * s, 1);
+        mbar_init(bar_sfinal, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -209,6 +218,39 @@ wide_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             for (uint32_t t = first; t < q; ++t)
                 mbar_wait(bar_full + 8u * (t % S), (t / S) & 1u, abort_flag, p.err, 32);
         }
+    } else if (warp == kScaleWarp) {
+        // ------------------------------------------------------------ rank 0: scale feeder
+        if (!kW8 && lane == 0 && rank == 0) {
+            uint32_t q = 0;
+            bool ok = true;
+            // one arrival per use of a stage, side-operand stages included (no copies there), so
+            // the barrier's phase follows the same sequence number as the ring
+            for (int tile = pair; ok && tile < tiles; tile += npairs) {
+                for (int kt = 0; kt < num_kt + side_stages; ++kt, ++q) {
+                    const uint32_t s = q % static_cast<uint32_t>(S), ph = (q / S) & 1u;
+                    // the stage's MMAs of S uses ago completed before the producer refilled it,
+                    // so the stage's TMEM slot is free once its data has landed
+                    if (!mbar_wait(bar_full + 8u * s, ph, abort_flag, p.err, 43) ||
+                        !mbar_wait(bar_pfull + 8u * s, ph, abort_flag, p.err, 44)) { ok = false; break; }
+                    if (kt < num_kt) {
+                        const uint32_t sA = base + s * SB;
+                        const int nkb = min(4, p.num_kb - kt * 4);
+                        const uint32_t slot = tmem + kSfCol + kSfSlot * s;
+                        for (int kb = 0; kb < nkb; ++kb) {
+                            tmem_cp_pair_32x128b_x4(slot + 4u * kb, smem_desc(sA + kSfaOff + kSfAtom * kb, 0, 128, 0));
+                            tmem_cp_pair_32x128b_x4(slot + 16u + 8u * kb,
+                                                    smem_desc(sA + kSfbOff + kSfAtom * kb, 0, 128, 0));
+                            tmem_cp_pair_32x128b_x4(slot + 20u + 8u * kb,
+                                                    smem_desc(sA + kSfbOff + 4 * kSfAtom + kSfAtom * kb, 0, 128, 0));
+                        }
+                    }
+                    tc_commit_pair(bar_sready + 8u * s);
+                }
+            }
+            // every copy this thread issued has completed before TMEM is released
+            tc_commit_pair(bar_sfinal);
+            mbar_wait(bar_sfinal, 0, abort_flag, p.err, 46);
+        }
     } else if (warp == 1) {
         if (lane == 0 && rank != 0) {
             // ------------------------------------------------------------ rank 1: relay
@@ -260,12 +302,11 @@ wide_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     } else {
                         const int nkb = min(4, p.num_kb - kt * 4);
                         const uint32_t slot = tmem + kSfCol + kSfSlot * s;
-                        for (int kb = 0; kb < nkb; ++kb) {
-                            tmem_cp_pair_32x128b_x4(slot + 4u * kb, smem_desc(sA + kSfaOff + kSfAtom * kb, 0, 128, 0));
-                            tmem_cp_pair_32x128b_x4(slot + 16u + 8u * kb, smem_desc(sA + kSfbOff + kSfAtom * kb, 0, 128, 0));
-                            tmem_cp_pair_32x128b_x4(slot + 20u + 8u * kb,
-                                                    smem_desc(sA + kSfbOff + 4 * kSfAtom + kSfAtom * kb, 0, 128, 0));
-                        }
+                        // the scale feeder's copies of this stage have completed
+                        WT_T0(tw5);
+                        if (!mbar_wait(bar_sready + 8u * s, ph, abort_flag, p.err, 45)) { ok = false; break; }
+                        WT_ADD(13, tw5);
+                        tc_fence_after();
                         for (int kb = 0; kb < nkb; ++kb)
                             mma_nvf4_pair(tmem, ad + 2u * kb, bd + 2u * kb, idesc_fp4, slot + 4u * kb, slot + 16u + 8u * kb,
                                           (kt | kb) != 0 ? 1u : 0u);
@@ -347,48 +388,50 @@ wide_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 if (lane == 0) WT_ADD(8, te2);
                 tc_fence_after();
             }
-            // finish every column first (the side results are read here), hand the accumulator
-            // back, then store: the stores overlap the next tile's main loop
+            // before the accumulator goes back only the side results are folded in (v = alpha acc +
+            // side, chunk by chunk as they are read); column scales, bias and the bf16 stores follow
+            // after the release and overlap the next tile's main loop
             WT_T0(te3);
+            if (has_side) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t* acc = j == 0 ? a0 : (j == 1 ? a1 : (j == 2 ? a2 : a3));
+                    uint32_t sd[32];
+                    tmem_ld_32x32b_x32(tmem + t_lane + static_cast<uint32_t>(128 * hh + 32 * j), sd);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        acc[i] = __float_as_uint(__fadd_rn(__fmul_rn(alpha, __uint_as_float(acc[i])), __uint_as_float(sd[i])));
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(sempty0);
+            }
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 uint32_t* acc = j == 0 ? a0 : (j == 1 ? a1 : (j == 2 ? a2 : a3));
-                const int c0 = 128 * hh + 32 * j;              // first column of the chunk in the tile
-                uint32_t sd[32];
-                if (has_side) {
-                    tmem_ld_32x32b_x32(tmem + t_lane + static_cast<uint32_t>(c0), sd);
-                    tmem_wait_ld();
-                }
 #pragma unroll
                 for (int g4 = 0; g4 < 8; ++g4) {
-                    const int src = 8 * j + g4;                    // lane holding columns c0 + 4 g4 ..
+                    const int src = 8 * j + g4;                    // lane holding columns 32 j + 4 g4 ..
                     float v[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) v[e] = alpha * __uint_as_float(acc[4 * g4 + e]);
+                    for (int e = 0; e < 4; ++e)
+                        v[e] = has_side ? __uint_as_float(acc[4 * g4 + e]) : __fmul_rn(alpha, __uint_as_float(acc[4 * g4 + e]));
                     if (p.colscale != nullptr) {
-                        v[0] *= __shfl_sync(0xFFFFFFFFu, cs4.x, src);
-                        v[1] *= __shfl_sync(0xFFFFFFFFu, cs4.y, src);
-                        v[2] *= __shfl_sync(0xFFFFFFFFu, cs4.z, src);
-                        v[3] *= __shfl_sync(0xFFFFFFFFu, cs4.w, src);
-                    }
-                    if (has_side) {
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) v[e] += __uint_as_float(sd[4 * g4 + e]);
+                        v[0] = __fmul_rn(v[0], __shfl_sync(0xFFFFFFFFu, cs4.x, src));
+                        v[1] = __fmul_rn(v[1], __shfl_sync(0xFFFFFFFFu, cs4.y, src));
+                        v[2] = __fmul_rn(v[2], __shfl_sync(0xFFFFFFFFu, cs4.z, src));
+                        v[3] = __fmul_rn(v[3], __shfl_sync(0xFFFFFFFFu, cs4.w, src));
                     }
                     if (p.bias != nullptr) {
-                        v[0] += __shfl_sync(0xFFFFFFFFu, bias4.x, src);
-                        v[1] += __shfl_sync(0xFFFFFFFFu, bias4.y, src);
-                        v[2] += __shfl_sync(0xFFFFFFFFu, bias4.z, src);
-                        v[3] += __shfl_sync(0xFFFFFFFFu, bias4.w, src);
+                        v[0] = __fadd_rn(v[0], __shfl_sync(0xFFFFFFFFu, bias4.x, src));
+                        v[1] = __fadd_rn(v[1], __shfl_sync(0xFFFFFFFFu, bias4.y, src));
+                        v[2] = __fadd_rn(v[2], __shfl_sync(0xFFFFFFFFu, bias4.z, src));
+                        v[3] = __fadd_rn(v[3], __shfl_sync(0xFFFFFFFFu, bias4.w, src));
                     }
 #pragma unroll
                     for (int e = 0; e < 4; ++e) acc[4 * g4 + e] = __float_as_uint(v[e]);
                 }
-            }
-            if (has_side) {
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(sempty0);
             }
             if (lane == 0) WT_ADD(11, te3);
             WT_T0(te4);
@@ -452,7 +495,7 @@ cudaError_t launch_gemm_wide(const GemmArgs& a, cudaStream_t st) {
     p.off_bar = p.off_y + kYBytes;
     p.sfa = a.sfa; p.sfb = a.sfb; p.gA = a.gA; p.gW = a.gW; p.bias = a.bias; p.colscale = a.colscale;
     p.err = a.err;
-    const uint32_t total = p.off_bar + 8u * (3 * S + 5) + 16u + 1024u;
+    const uint32_t total = p.off_bar + 8u * (4 * S + 6) + 16u + 1024u;
     static bool attr_set[2] = {false, false};
     if (!attr_set[w8]) {
         const cudaError_t e = w8 ? cudaFuncSetAttribute(wide_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
