@@ -76,6 +76,13 @@ enum { WQ_SCALE_LAYOUT_ROWMAJOR = 0, WQ_SCALE_LAYOUT_MMA = 1 };
  *   STATIC  one calibrated g (wq_config.act_gscale) fixed at preparation; one pass, no amax.
  * g = amax / 2688 in the first two; the block scales and codes follow from g as in every mode. */
 enum { WQ_ACT_SCALE_ROW = 0, WQ_ACT_SCALE_TENSOR = 1, WQ_ACT_SCALE_STATIC = 2 };
+/* Order of the two activation transforms (4-bit layers with rotate = 1):
+ *   SMOOTH_ROTATE  xt = (x diag(1/s)) H, weight R' = H diag(s) (W - P Q), P = bf16(diag(1/s) L1)
+ *                  (FoldQuantVLA, Key Contribution 2: "channel scaling, block Hadamard"; default);
+ *   ROTATE_SMOOTH  xt = (x H) diag(1/s), weight R' = diag(s) H (W - P Q), P = bf16(H diag(1/s) L1)
+ *                  (QuantWAMs sec. 3.1 Eq. (1): A R S^-1).  L1, L2 are then the top-r factors of
+ *                  diag(s) H W and s is taken in the rotated basis. */
+enum { WQ_ORDER_SMOOTH_ROTATE = 0, WQ_ORDER_ROTATE_SMOOTH = 1 };
 
 /* mode = WQ_MODE_W8A8 selects the selective 8-bit path (FoldQuantVLA, Key Contribution 3:
  * attention-output and FFN down projections kept at W8A8) in the same smoothed + rotated basis:
@@ -91,6 +98,7 @@ typedef struct wq_config {
     int mode;         /* WQ_MODE_W4A4 (wq_linear_forward) or WQ_MODE_W8A8 (..._w8a8)      */
     int act_scale;    /* WQ_ACT_SCALE_* (4-bit layers; W8A8 takes WQ_ACT_SCALE_ROW)        */
     float act_gscale; /* WQ_ACT_SCALE_STATIC: the calibrated g (> 0, finite); else ignored */
+    int transform_order; /* WQ_ORDER_*: where the smoothing sits relative to the rotation  */
 } wq_config;
 
 /*
@@ -230,6 +238,31 @@ WQ_API wq_status wq_quantize_activations(wq_weights_t h, const void *x, int M, i
 WQ_API wq_status wq_linear_forward_quantized(wq_weights_t h, const uint8_t *codes, const uint8_t *scales_mma,
                                              const float *gscale, const void *u, const void *x_omega, int M,
                                              void *y, void *stream);
+
+/*
+ * Two chained 4-bit projections, with the second one's input quantised in the first one's GEMM
+ * epilogue (the consistent folding of FoldQuantVLA, Key Contribution 1: the next consumer's
+ * transform applied where its input is produced): no bf16 y is written and the second layer's
+ * activation quantiser does not run.  The epilogue takes each output value as the bf16 that
+ * wq_linear_forward would have stored, applies `next`'s smoothing and block-64 rotation along
+ * this layer's N, moves `next`'s kept channels to x_omega and codes the rest in NVFP4 with
+ * `next`'s fixed tensor scale -- bit-identical to wq_quantize_activations(next, that y).
+ * Then wq_linear_forward_quantized(next, codes, scales_mma, gscale, NULL, x_omega, ...) finishes
+ * the second layer.
+ *   h        this layer (W4A4).
+ *   next     the next layer: W4A4, next K == h's N, act_scale WQ_ACT_SCALE_STATIC (a per-row
+ *            scale would need the whole row, which no output tile holds), rank 0 (its low-rank
+ *            down-projection would need the whole row too); otherwise WQ_ERR_UNSUPPORTED.
+ *   x        device bf16 [M, K] (this layer's input).
+ *   codes    device uint8 [M, N/2]; scales_mma device, the MMA scale layout for K' = N;
+ *   gscale   device fp32 [M] (every entry next's g); x_omega device fp16 [M, xo_ld of next]
+ *            (required when next keeps channels, NULL otherwise).
+ *   workspace  device, wq_workspace_bytes(h, M) bytes, 256-byte aligned.
+ * Two kernels on `stream`: this layer's quantiser and its GEMM on the CTA-pair schedule.
+ */
+WQ_API wq_status wq_linear_forward_chain(wq_weights_t h, wq_weights_t next, const void *x, int M, uint8_t *codes,
+                                         uint8_t *scales_mma, float *gscale, void *x_omega, void *workspace,
+                                         size_t workspace_bytes, void *stream);
 
 /*
  * The selective 8-bit projection (handle prepared with mode WQ_MODE_W8A8): the 8-bit variant of

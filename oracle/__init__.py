@@ -74,8 +74,31 @@ def lib() -> ctypes.CDLL:
             L.orc_quantize_weights_int8.restype = i32
             L.orc_linear_forward_w8a8.argtypes = [P, P, i64, P, P, i64, i64, P, P, i32]
             L.orc_linear_forward_w8a8.restype = i32
+            L.orc_set_smooth_after.argtypes = [i32]
+            L.orc_set_smooth_after.restype = None
             _lib = L
     return _lib
+
+
+_order_lock = threading.RLock()
+
+
+class transform_order:
+    """Context for the transform order of the oracle calls made inside it: smooth_after=False is
+    smoothing then rotation (FoldQuantVLA, Key Contribution 2), True is rotation then smoothing
+    (QuantWAMs sec. 3.1 Eq. (1), A R S^-1)."""
+
+    def __init__(self, smooth_after: bool):
+        self.v = bool(smooth_after)
+
+    def __enter__(self):
+        _order_lock.acquire()
+        lib().orc_set_smooth_after(int(self.v))
+        return self
+
+    def __exit__(self, *a):
+        lib().orc_set_smooth_after(0)
+        _order_lock.release()
 
 
 def _p(a: Optional[np.ndarray]):
@@ -254,8 +277,13 @@ def linear_forward(aq: ActQuant, wq: WeightQuant, U: Optional[np.ndarray],
     return y
 
 
-def forward_noquant(x_bits, s, rotate, omega, wq: WeightQuant, bias) -> np.ndarray:
+def forward_noquant(x_bits, s, rotate, omega, wq: WeightQuant, bias, smooth_after: bool = False) -> np.ndarray:
     """The folded pipeline with quantisation disabled (FoldQuantVLA Proposition 1)."""
+    with transform_order(smooth_after):
+        return _forward_noquant(x_bits, s, rotate, omega, wq, bias)
+
+
+def _forward_noquant(x_bits, s, rotate, omega, wq: WeightQuant, bias) -> np.ndarray:
     x_bits = _c(x_bits, np.uint16)
     M, K = x_bits.shape
     N = wq.codes.shape[0]
@@ -278,11 +306,30 @@ def reference_forward(layer, n_threads: int = 0, rows: Optional[np.ndarray] = No
     ``rows`` restricts the activation side to a subset of rows (sampled parity)."""
     x_bits = layer.x_bits if rows is None else layer.x_bits[rows]
     rotate = layer.rotate
-    wq = prepare_weights(layer.W, layer.s, layer.L1, layer.L2, layer.omega, rotate, n_threads)
-    aq = quantize_act(x_bits, layer.s, rotate, layer.omega, n_threads=n_threads)
+    with transform_order(getattr(layer, "smooth_after", False)):
+        wq = prepare_weights(layer.W, layer.s, layer.L1, layer.L2, layer.omega, rotate, n_threads)
+        aq = quantize_act(x_bits, layer.s, rotate, layer.omega, n_threads=n_threads)
     U = lowrank_act(x_bits, wq.P) if wq.P.shape[1] else None
     y = linear_forward(aq, wq, U, layer.bias, n_threads=n_threads)
     return y, aq, wq, U
+
+
+def bf16_bits_from_f64(y: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns of fp64 values, one rounding to nearest even each."""
+    f = lib().orc_bf16_from_f64
+    flat = np.ascontiguousarray(y, np.float64).reshape(-1)
+    return np.array([f(float(v)) for v in flat], np.uint16).reshape(np.shape(y))
+
+
+def chain_quantize(y: np.ndarray, s_next, rotate_next: bool, omega_next, g_next: float,
+                   smooth_after: bool = False) -> ActQuant:
+    """The next layer's quantised input from this layer's output (FoldQuantVLA Key Contribution 1:
+    one basis per activation site, the consumer's transform applied where the input is made): the
+    fp64 output rounded once to bf16 (the value a bf16 activation tensor holds), then the next
+    layer's smoothing, rotation, kept-channel split and NVFP4 with its fixed tensor scale."""
+    bits = bf16_bits_from_f64(y)
+    with transform_order(smooth_after):
+        return quantize_act(bits, s_next, rotate_next, omega_next, static_g=g_next)
 
 
 # ------------------------------------------------------------------ W8A8

@@ -23,7 +23,11 @@
  *     unsigned e4m3 scale per 16 consecutive K elements, one fp32 tensor scale.
  *
  * Readings fixed here (the pages leave them open):
- *   - smoothing is applied before the rotation (xs = x * inv_s, then FWHT);
+ *   - smoothing is applied before the rotation (xs = x * inv_s, then FWHT) in the
+ *     default order (FoldQuantVLA, Key Contribution 2: "channel scaling, block
+ *     Hadamard"); the other order, rotation first (QuantWAMs sec. 3.1 Eq. (1):
+ *     A R S^-1), is the `smooth_after` flag: xt = FWHT(x) * inv_s, with the fold
+ *     R' = S H (W - P Q) and P = bf16(H S^-1 L1);
  *   - activations carry one fp32 scale per row, g = amax_row / (6 * 448);
  *     weights carry one per tensor;
  *   - block scale  sc = e4m3_rne_satfinite((bmax / 6) / g),
@@ -244,17 +248,27 @@ static double nvfp4_elem(const uint8_t *codes, const uint8_t *scales, long k)
 
 /* ------------------------------------------------------------------ activations */
 
-/* Transform one activation row: xs = fp32(x) * inv_s (fp32 multiply), then the
- * block-64 FWHT when rotate != 0.  Output fp32 [K]. */
+/* Transform one activation row.  Default order: xs = fp32(x) * inv_s (fp32 multiply),
+ * then the block-64 FWHT when rotate != 0.  smooth_after != 0 (QuantWAMs Eq. (1),
+ * A R S^-1): the FWHT of fp32(x) first, then the multiply by inv_s.  Output fp32 [K]. */
+static int g_smooth_after = 0;           /* set by the entry points below for one call */
+
 void orc_act_transform_row(const uint16_t *x_bf16, long K, const float *inv_s, int rotate, float *xt)
 {
+    int after = g_smooth_after && rotate;
     for (long k = 0; k < K; ++k) {
         float xv = orc_f32_from_bf16(x_bf16[k]);
-        xt[k] = inv_s ? xv * inv_s[k] : xv;
+        xt[k] = (inv_s && !after) ? xv * inv_s[k] : xv;
     }
     if (rotate)
         for (long b = 0; b < K / 64; ++b) orc_fwht64_f32(xt + 64 * b);
+    if (inv_s && after)
+        for (long k = 0; k < K; ++k) xt[k] = xt[k] * inv_s[k];
 }
+
+/* Select the transform order for the following calls (0: smooth, then rotate; 1: rotate,
+ * then smooth).  Not thread-safe across concurrent callers; the Python wrapper holds a lock. */
+void orc_set_smooth_after(int v) { g_smooth_after = v ? 1 : 0; }
 
 /* Quantise M activation rows.
  *   per_tensor == 0: one g per row (dynamic per-token); g[m] written for each row.
@@ -335,12 +349,27 @@ int orc_fold_weights(const float *W, long K, long N, const float *s,
                      uint16_t *P, uint16_t *Q, int n_threads)
 {
     if (K % 16 || (rotate && K % 64)) return -1;
-    for (long k = 0; k < K; ++k)
+    int after = g_smooth_after && rotate;
+    if (!after) {
+        for (long k = 0; k < K; ++k)
+            for (int j = 0; j < r; ++j) {
+                float l = L1[k * r + j];
+                if (s) l = l * (1.0f / s[k]);
+                P[k * r + j] = orc_bf16_from_f32(l);
+            }
+    } else {
+        /* P = H S^-1 L1: column j of L1 times inv_s = fp32(1/s), the block FWHT in fp64,
+         * one rounding to bf16 */
+        double *col = (double *)malloc(sizeof(double) * (size_t)K);
+        if (!col) return -4;
         for (int j = 0; j < r; ++j) {
-            float l = L1[k * r + j];
-            if (s) l = l * (1.0f / s[k]);
-            P[k * r + j] = orc_bf16_from_f32(l);
+            for (long k = 0; k < K; ++k)
+                col[k] = (double)L1[k * r + j] * (s ? (double)(1.0f / s[k]) : 1.0);
+            for (long b = 0; b < K / 64; ++b) orc_fwht64_f64(col + 64 * b, 1);
+            for (long k = 0; k < K; ++k) P[k * r + j] = orc_bf16_from_f64(col[k]);
         }
+        free(col);
+    }
     for (int j = 0; j < r; ++j)
         for (long n = 0; n < N; ++n) Q[(long)j * N + n] = orc_bf16_from_f32(L2[(long)j * N + n]);
 
@@ -358,12 +387,18 @@ int orc_fold_weights(const float *W, long K, long N, const float *s,
             for (int j = 0; j < r; ++j)
                 lr += (double)orc_f32_from_bf16(P[k * r + j]) * (double)orc_f32_from_bf16(Q[(long)j * N + n]);
             double t = (double)W[k * N + n] - lr;
-            R[k * N + n] = s ? (double)s[k] * t : t;
+            R[k * N + n] = (s && !after) ? (double)s[k] * t : t;
         }
     if (rotate) {
 #pragma omp parallel for schedule(static)
         for (long n = 0; n < N; ++n)
             for (long b = 0; b < K / 64; ++b) orc_fwht64_f64(R + (64 * b) * N + n, N);
+    }
+    if (s && after) {
+        /* R' = S H (W - P Q): the rotated rows scaled by s after the transform */
+#pragma omp parallel for schedule(static)
+        for (long k = 0; k < K; ++k)
+            for (long n = 0; n < N; ++n) R[k * N + n] = (double)s[k] * R[k * N + n];
     }
     for (long i = 0; i < K * N; ++i) Rp[i] = (float)R[i];
     free(R);

@@ -33,8 +33,8 @@ def test_library_exports_every_declared_symbol():
         assert hasattr(L, name), name
 
 
-def _cfg(K=256, N=128, r=0, no=0, rot=1, mode=0, act=0, g=0.0):
-    return wq.wq_config(K, N, r, no, rot, mode, act, g)
+def _cfg(K=256, N=128, r=0, no=0, rot=1, mode=0, act=0, g=0.0, order=0):
+    return wq.wq_config(K, N, r, no, rot, mode, act, g, order)
 
 
 @pytest.mark.parametrize("cfg,status", [
@@ -52,6 +52,8 @@ def _cfg(K=256, N=128, r=0, no=0, rot=1, mode=0, act=0, g=0.0):
     (dict(act=3), wq.WQ_ERR_INVALID),
     (dict(act=2, g=0.0), wq.WQ_ERR_INVALID),
     (dict(act=2, g=float("inf")), wq.WQ_ERR_INVALID),
+    (dict(order=2), wq.WQ_ERR_INVALID),
+    (dict(mode=1, order=1), wq.WQ_ERR_UNSUPPORTED),
 ])
 def test_prepare_rejects_bad_config(cfg, status):
     if status is None:

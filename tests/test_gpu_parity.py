@@ -32,9 +32,22 @@ def x_dev(bits: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
 
 
-def prep(L):
+def prep(L, **kw):
     return wq.wq_prepare_weights(L.spec.K, L.spec.N, L.W, L.bias, L.s, L.L1, L.L2,
-                                 L.omega if L.omega.size else None, rotate=L.rotate)
+                                 L.omega if L.omega.size else None, rotate=L.rotate,
+                                 transform_order=int(L.smooth_after), **kw)
+
+
+def oq(L, **kw):
+    """The oracle's activation quantiser in the layer's transform order."""
+    with oracle.transform_order(L.smooth_after):
+        return oracle.quantize_act(L.x_bits, L.s, L.rotate, L.omega, **kw)
+
+
+def ow(L):
+    """The oracle's weight fold and quantiser in the layer's transform order."""
+    with oracle.transform_order(L.smooth_after):
+        return oracle.prepare_weights(L.W, L.s, L.L1, L.L2, L.omega, L.rotate)
 
 
 def y_tolerance(L, y_ref, rows=None):
@@ -81,6 +94,9 @@ CASES = {
     "top2pct_o41_r24": ("video_dit", dict(M=96, K=2048, N=256, rank=24, n_omega=41)),
     "o5_r8": ("video_dit", dict(M=40, K=512, N=192, rank=8, n_omega=5)),
     "o64_r40_no_rotate": ("video_dit", dict(M=150, K=1024, N=144, rank=40, n_omega=64, rotate=False)),
+    # rotation first, then smoothing (QuantWAMs sec. 3.1 Eq. (1), A R S^-1)
+    "rot_smooth_r32_o16": ("video_dit", dict(M=96, K=1024, N=192, rank=32, n_omega=16, smooth_after=True)),
+    "rot_smooth_expert_r32": ("expert", dict(M=50, K=1024, N=256, rank=32, smooth_after=True)),
 }
 
 
@@ -100,7 +116,7 @@ def test_weights_bitexact(case):
     L = layer(case)
     w = prep(L)
     ex = wq.wq_export_weights(w)
-    o = oracle.prepare_weights(L.W, L.s, L.L1, L.L2, L.omega, L.rotate)
+    o = ow(L)
     assert np.float32(ex["gW"]) == np.float32(o.gW)
     assert np.array_equal(ex["scales"], o.scales)
     assert np.array_equal(ex["codes"], o.codes)
@@ -116,7 +132,7 @@ def test_activation_quant_bitexact(case):
     codes, scales, g, xo, u = wq.wq_quantize_activations(w, x, wq.WQ_SCALE_LAYOUT_ROWMAJOR)
     codes2, sf_mma, g2, _, _ = wq.wq_quantize_activations(w, x, wq.WQ_SCALE_LAYOUT_MMA)
     torch.cuda.synchronize()
-    aq = oracle.quantize_act(L.x_bits, L.s, L.rotate, L.omega)
+    aq = oq(L)
     assert np.array_equal(g.cpu().numpy(), aq.g)
     assert np.array_equal(scales.cpu().numpy(), aq.scales)
     assert np.array_equal(codes.cpu().numpy(), aq.codes)
@@ -132,7 +148,7 @@ def check_side(L, xo, u, aq):
         got, pad = side_out(xo, L.omega.size)
         assert np.array_equal(got, aq.x_omega) and not pad.any()
     if L.rank:
-        o = oracle.prepare_weights(L.W, L.s, L.L1, L.L2, L.omega, L.rotate)
+        o = ow(L)
         U = oracle.lowrank_act(L.x_bits, o.P)
         ug, pad = side_out(u, L.rank)
         assert u_close(ug, U, L.x_bits, o.P).all() and not pad.any()
@@ -153,7 +169,7 @@ def test_activation_quant_split(case, split, tuning):
     x = x_dev(L.x_bits)
     codes, scales, g, xo, u = wq.wq_quantize_activations(w, x, wq.WQ_SCALE_LAYOUT_ROWMAJOR)
     torch.cuda.synchronize()
-    aq = oracle.quantize_act(L.x_bits, L.s, L.rotate, L.omega)
+    aq = oq(L)
     assert np.array_equal(g.cpu().numpy(), aq.g)
     assert np.array_equal(scales.cpu().numpy(), aq.scales)
     assert np.array_equal(codes.cpu().numpy(), aq.codes)
@@ -173,7 +189,7 @@ def test_activation_quant_schedules(case, schedule, tuning):
     codes, scales, g, xo, u = wq.wq_quantize_activations(w, x, wq.WQ_SCALE_LAYOUT_MMA)
     torch.cuda.synchronize()
     wq.wq_check_device_error(w)
-    aq = oracle.quantize_act(L.x_bits, L.s, L.rotate, L.omega)
+    aq = oq(L)
     assert np.array_equal(g.cpu().numpy(), aq.g)
     assert np.array_equal(wq.mma_scales_to_rowmajor(scales.cpu().numpy(), L.M, L.spec.K), aq.scales)
     assert np.array_equal(codes.cpu().numpy(), aq.codes)
@@ -200,7 +216,7 @@ def test_forward_parity_fused_and_two_kernel_paths(case, fused, tuning):
     tuning("WQ_FUSED", fused)
     L = layer(case)
     w = prep(L)
-    eligible = L.M <= 64 and L.rank <= 32 and L.spec.K % 128 == 0
+    eligible = L.M <= 64 and L.rank <= 32 and L.spec.K % 128 == 0 and not L.smooth_after
     expected = wq.WQ_PATH_FUSED if fused == "1" and eligible else wq.WQ_PATH_TWO_KERNEL
     assert wq.wq_forward_path(w, L.M) == expected
     y = wq.wq_linear_forward(w, x_dev(L.x_bits))
@@ -402,7 +418,7 @@ def test_full_size_every_row_and_tile(wl_name, layer_idx):
     y = wq.wq_linear_forward(w, x)
     codes, scales, g, xo, _ = wq.wq_quantize_activations(w, x)
     wq.wq_check_device_error(w)
-    aq = oracle.quantize_act(L.x_bits, L.s, L.rotate, L.omega)
+    aq = oq(L)
     assert np.array_equal(g.cpu().numpy(), aq.g)
     assert np.array_equal(scales.cpu().numpy(), aq.scales)
     assert np.array_equal(codes.cpu().numpy(), aq.codes)
@@ -449,12 +465,12 @@ def test_batch_tensor_scale_modes(case, mode):
         w = wq.wq_prepare_weights(L.spec.K, L.spec.N, L.W, L.bias, L.s, L.L1, L.L2,
                                   L.omega if L.omega.size else None, rotate=L.rotate,
                                   act_scale=wq.WQ_ACT_SCALE_STATIC, act_gscale=g_cal)
-        aq = oracle.quantize_act(L.x_bits, L.s, L.rotate, L.omega, static_g=g_cal)
+        aq = oq(L, static_g=g_cal)
     else:
         w = wq.wq_prepare_weights(L.spec.K, L.spec.N, L.W, L.bias, L.s, L.L1, L.L2,
                                   L.omega if L.omega.size else None, rotate=L.rotate,
                                   act_scale=wq.WQ_ACT_SCALE_TENSOR)
-        aq = oracle.quantize_act(L.x_bits, L.s, L.rotate, L.omega, per_tensor=True)
+        aq = oq(L, per_tensor=True)
     x = x_dev(L.x_bits)
     codes, scales, g, xo, u = wq.wq_quantize_activations(w, x)
     y = wq.wq_linear_forward(w, x)
@@ -464,7 +480,7 @@ def test_batch_tensor_scale_modes(case, mode):
     assert np.array_equal(scales.cpu().numpy(), aq.scales)
     assert np.array_equal(codes.cpu().numpy(), aq.codes)
     check_side(L, xo, u, aq)
-    wqo = oracle.prepare_weights(L.W, L.s, L.L1, L.L2, L.omega, L.rotate)
+    wqo = ow(L)
     U = oracle.lowrank_act(L.x_bits, wqo.P) if L.rank else None
     y_ref = oracle.linear_forward(aq, wqo, U, L.bias, per_tensor_act=True)
     assert_y_close(L, y, y_ref)

@@ -583,3 +583,46 @@ def test_batch_and_fixed_tensor_scales():
     sat = oracle.quantize_act(bits, None, False, static_g=1e-6)
     assert sat.scales[2, 0] == 0x7E
     assert (sat.codes[2, 2] & 15) in (7, 15) or (sat.codes[2, 2] >> 4) in (7, 15)
+
+
+# ------------------------------------------------------------------ the rotate-then-smooth order
+@pytest.mark.parametrize("r,n_om", [(0, 0), (16, 0), (0, 16), (16, 16)])
+def test_folding_invariance_rotate_then_smooth(r, n_om):
+    """QuantWAMs sec. 3.1 Eq. (1) order, A R S^-1 (rotation first): with quantisation disabled
+    the folded graph x H S^-1 . S H (W - P Q) + x P Q (+ outliers) still computes x W + b
+    (FoldQuantVLA Proposition 1 in this order)."""
+    L = wlmod.make_layer_inputs("tiny", M=8, K=256, N=96, rank=r, n_omega=n_om, smooth_after=True)
+    with oracle.transform_order(True):
+        wq = oracle.prepare_weights(L.W, L.s, L.L1, L.L2, L.omega, True)
+    y = oracle.forward_noquant(L.x_bits, L.s, True, L.omega, wq, L.bias, smooth_after=True)
+    ref = L.x_f32.astype(np.float64) @ L.W.astype(np.float64)
+    if L.bias is not None:
+        ref += L.bias
+    assert np.max(np.abs(y - ref)) / np.max(np.abs(ref)) <= 1e-5
+
+
+def test_rotate_then_smooth_transform_against_dense_matrices():
+    """The activation transform in this order equals (x H) diag(1/s) from dense fp64 matrices on
+    integer rows with power-of-two smoothing (exact in fp32), and differs from the default order
+    there; P = bf16(H S^-1 L1) matches the dense product rounded once."""
+    rng = np.random.default_rng(61)
+    M, K = 4, 128
+    x = rng.integers(-500, 500, (M, K)).astype(np.float32)
+    bits = wlmod.bf16_bits(x)
+    s = (2.0 ** rng.integers(-2, 3, K)).astype(np.float32)
+    with oracle.transform_order(True):
+        aq = oracle.quantize_act(bits, s, True, keep_xt=True)
+    H = hadamard(64).astype(np.float64) / 8.0
+    xf = wlmod.bf16_from_bits(bits).astype(np.float64)
+    want = (xf.reshape(M, 2, 64) @ H).reshape(M, K) / s.astype(np.float64)
+    assert np.array_equal(aq.xt.astype(np.float64), want)
+    other = oracle.quantize_act(bits, s, True, keep_xt=True)
+    assert not np.array_equal(other.xt, aq.xt)
+    L1 = rng.standard_normal((K, 8)).astype(np.float32)
+    L2 = rng.standard_normal((8, 32)).astype(np.float32)
+    W = rng.standard_normal((K, 32)).astype(np.float32)
+    with oracle.transform_order(True):
+        wq = oracle.prepare_weights(W, s, L1, L2, None, True)
+    inv_s = (np.float32(1.0) / s).astype(np.float64)
+    Pd = (H @ (inv_s[:, None] * L1.astype(np.float64)).reshape(2, 64, 8)).reshape(K, 8)
+    assert np.array_equal(wq.P, np.array([[_exact_bf16_bits(float(v)) for v in row] for row in Pd], np.uint16))

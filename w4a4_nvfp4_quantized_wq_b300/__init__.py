@@ -24,6 +24,7 @@ WQ_PATH_TWO_KERNEL, WQ_PATH_FUSED = 0, 1
 WQ_GEMM_SINGLE, WQ_GEMM_SPLITK, WQ_GEMM_WIDE = 0, 1, 2
 WQ_QUANT_CLUSTER, WQ_QUANT_STREAM = 0, 1
 WQ_ACT_SCALE_ROW, WQ_ACT_SCALE_TENSOR, WQ_ACT_SCALE_STATIC = 0, 1, 2
+WQ_ORDER_SMOOTH_ROTATE, WQ_ORDER_ROTATE_SMOOTH = 0, 1
 
 EXPORTED = ["wq_prepare_weights", "wq_get_config", "wq_workspace_bytes", "wq_linear_forward",
             "wq_host_workspace_bytes", "wq_linear_forward_host", "wq_quantize_activations",
@@ -32,7 +33,8 @@ EXPORTED = ["wq_prepare_weights", "wq_get_config", "wq_workspace_bytes", "wq_lin
             "wq_conv3d_workspace_bytes", "wq_conv3d_forward", "wq_quantize_conv3d_input",
             "wq_export_weights", "wq_check_device_error", "wq_free_weights", "wq_last_error",
             "wq_forward_path", "wq_selftest_wait_timeout", "wq_gemm_schedule",
-            "wq_quant_schedule", "wq_side_strides", "wq_set_tuning", "wq_get_tuning", "wq_mma_peak"]
+            "wq_quant_schedule", "wq_side_strides", "wq_set_tuning", "wq_get_tuning", "wq_mma_peak",
+            "wq_linear_forward_chain"]
 
 
 class WqError(RuntimeError):
@@ -44,7 +46,7 @@ class WqError(RuntimeError):
 class wq_config(ctypes.Structure):
     _fields_ = [("K", ctypes.c_int), ("N", ctypes.c_int), ("rank", ctypes.c_int),
                 ("n_outliers", ctypes.c_int), ("rotate", ctypes.c_int), ("mode", ctypes.c_int),
-                ("act_scale", ctypes.c_int), ("act_gscale", ctypes.c_float)]
+                ("act_scale", ctypes.c_int), ("act_gscale", ctypes.c_float), ("transform_order", ctypes.c_int)]
 
 
 _lib = None
@@ -79,6 +81,8 @@ def lib() -> ctypes.CDLL:
         L.wq_linear_forward_host.restype = I
         L.wq_quantize_activations.argtypes = [P, P, I, I, P, P, P, P, P, P]
         L.wq_quantize_activations.restype = I
+        L.wq_linear_forward_chain.argtypes = [P, P, P, I, P, P, P, P, P, S, P]
+        L.wq_linear_forward_chain.restype = I
         L.wq_linear_forward_quantized.argtypes = [P, P, P, P, P, P, I, P, P]
         L.wq_linear_forward_quantized.restype = I
         L.wq_linear_forward_noalloc.argtypes = [P, P, I, P, P]
@@ -165,11 +169,13 @@ class Weights:
 
 def wq_prepare_weights(K: int, N: int, W, bias=None, s=None, L1=None, L2=None, omega=None,
                        rotate: bool = True, mode: int = WQ_MODE_W4A4, stream=None,
-                       act_scale: int = WQ_ACT_SCALE_ROW, act_gscale: float = 0.0) -> Weights:
+                       act_scale: int = WQ_ACT_SCALE_ROW, act_gscale: float = 0.0,
+                       transform_order: int = WQ_ORDER_SMOOTH_ROTATE) -> Weights:
     """Fold and quantise one projection (host inputs, numpy or CPU tensors)."""
     rank = 0 if L1 is None else int(np.shape(L1)[1])
     n_out = 0 if omega is None else int(np.size(omega))
-    cfg = wq_config(K, N, rank, n_out, int(bool(rotate)), mode, int(act_scale), float(act_gscale))
+    cfg = wq_config(K, N, rank, n_out, int(bool(rotate)), mode, int(act_scale), float(act_gscale),
+                    int(transform_order))
     keep = []
     ptrs = []
     for a, dt in ((W, np.float32), (bias, np.float32), (s, np.float32), (L1, np.float32),
@@ -299,6 +305,28 @@ def wq_linear_forward_quantized(w: Weights, codes, scales_mma, g, u=None, x_omeg
     return y
 
 
+def wq_linear_forward_chain(w: Weights, w_next: Weights, x, workspace=None, stream=None):
+    """Layer w on x, its output quantised in the GEMM epilogue for w_next: returns device
+    tensors (codes [M, N/2], scales in the MMA layout, g [M], x_omega [M, xo_ld] or None) that
+    wq_linear_forward_quantized(w_next, ...) consumes."""
+    import torch
+    M = x.shape[0]
+    N = w.N
+    dev = x.device
+    codes = torch.empty((M, N // 2), dtype=torch.uint8, device=dev)
+    scales = torch.zeros(((M + 127) // 128) * (N // 64) * 512, dtype=torch.uint8, device=dev)
+    g = torch.empty(M, dtype=torch.float32, device=dev)
+    _, xo_ld = wq_side_strides(w_next)
+    xo = torch.empty((M, xo_ld), dtype=torch.float16, device=dev) if w_next.cfg.n_outliers else None
+    if workspace is None:
+        workspace = _alloc_workspace(wq_workspace_bytes(w, M), dev)
+    ptr = lambda t: ctypes.c_void_p(t.data_ptr() if t is not None else None)
+    _check(lib().wq_linear_forward_chain(ctypes.c_void_p(w.handle), ctypes.c_void_p(w_next.handle), ptr(x), M,
+                                         ptr(codes), ptr(scales), ptr(g), ptr(xo), ptr(workspace), workspace.numel(),
+                                         ctypes.c_void_p(_stream_ptr(stream))))
+    return codes, scales, g, xo
+
+
 def wq_export_weights(w: Weights) -> dict:
     """Prepared weights copied back to host in canonical layouts."""
     K, N, r, no = w.cfg.K, w.cfg.N, w.cfg.rank, w.cfg.n_outliers
@@ -426,7 +454,7 @@ def wq_prepare_conv3d(w, pad: int = 1, stream=None) -> ConvWeights:
     out = ctypes.c_void_p()
     _check(lib().wq_prepare_conv3d(w.ctypes.data_as(ctypes.c_void_p), Ci, Co, kt, kh, kw, int(pad),
                                    ctypes.c_void_p(_stream_ptr(stream)), ctypes.byref(out)))
-    return ConvWeights(out.value, wq_config(kt * kh * kw * Ci, Co, 0, 0, 0, WQ_MODE_W4A4, 0, 0.0), Ci)
+    return ConvWeights(out.value, wq_config(kt * kh * kw * Ci, Co, 0, 0, 0, WQ_MODE_W4A4, 0, 0.0, 0), Ci)
 
 
 def wq_conv3d_workspace_bytes(w: ConvWeights, B: int, D: int, H: int, W: int) -> int:

@@ -93,8 +93,11 @@ __device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {   // RN(a b + c) per lane
 // FWHT in the pages' order: strides 1, 2, 4, 8 between pairs, 16 inside a pair, 32 with the
 // partner lane (lane ^ 16 holds the other half of the row: a + b there, a - b here, as one
 // fused multiply-add with an exact +-1 product), then the exact 1/8 normalisation.
+// rotate: bit 0 = the block FWHT; bit 1 = smooth after the rotation (QuantWAMs sec. 3.1
+// Eq. (1), A R S^-1) instead of before it (FoldQuantVLA, Key Contribution 2).
 __device__ __forceinline__ void load_transform(uint32_t box, int r, int half, uint32_t invs, int rotate,
                                                f2 (&P)[16]) {
+    const bool smooth_after = (rotate & 3) == 3;
     uint32_t w[4][4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -108,7 +111,7 @@ __device__ __forceinline__ void load_transform(uint32_t box, int r, int half, ui
         P[k] = (k & 1) ? pk2(__uint_as_float(a & 0xFFFF0000u), __uint_as_float(b & 0xFFFF0000u))
                        : pk2(__uint_as_float(a << 16), __uint_as_float(b << 16));
     }
-    if (invs != 0u) {
+    if (invs != 0u && !smooth_after) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const float4 sv = ld_shared_v4f(invs + 128u * half + 16u * j);
@@ -116,7 +119,7 @@ __device__ __forceinline__ void load_transform(uint32_t box, int r, int half, ui
             P[2 * j + 1] = mul2(P[2 * j + 1], pk2(sv.z, sv.w));
         }
     }
-    if (rotate) {
+    if (rotate & 1) {
 #pragma unroll
         for (int h = 1; h < 16; h <<= 1) {
 #pragma unroll
@@ -142,6 +145,15 @@ __device__ __forceinline__ void load_transform(uint32_t box, int r, int half, ui
         const f2 c8 = pk2(0.125f, 0.125f);
 #pragma unroll
         for (int k = 0; k < 16; ++k) P[k] = mul2(P[k], c8);
+        if (invs != 0u && smooth_after) {
+            // the same pair-ordered inv_s: rotation keeps channel positions
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float4 sv = ld_shared_v4f(invs + 128u * half + 16u * j);
+                P[2 * j] = mul2(P[2 * j], pk2(sv.x, sv.y));
+                P[2 * j + 1] = mul2(P[2 * j + 1], pk2(sv.z, sv.w));
+            }
+        }
     }
 }
 

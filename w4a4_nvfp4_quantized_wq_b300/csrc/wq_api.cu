@@ -43,6 +43,21 @@ wq_status cuda_fail(cudaError_t e, const char* what) {
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 uint16_t bf16_bits(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
+
+// bf16 of an fp64 value with one rounding to nearest even: first to fp32 rounding to odd (truncate,
+// then set the last bit when anything was cut off), which keeps the information a later
+// round-to-nearest at 8 bits needs, then fp32 -> bf16 round-to-nearest-even.
+uint16_t bf16_bits_from_f64(double v) {
+    float t = static_cast<float>(v);                      // nearest
+    if (static_cast<double>(t) != v && std::isfinite(t)) {
+        if (std::fabs(static_cast<double>(t)) > std::fabs(v)) t = std::nextafter(t, 0.0f);   // toward zero
+        uint32_t u;
+        std::memcpy(&u, &t, 4);
+        u |= 1u;                                          // sticky: inexact
+        std::memcpy(&t, &u, 4);
+    }
+    return bf16_bits(t);
+}
 uint16_t f16_bits(float f) { return __half_as_ushort(__float2half_rn(f)); }
 
 float e4m3_value(uint32_t c) {
@@ -250,6 +265,10 @@ wq_status check_config(const wq_config* c) {
         return fail(WQ_ERR_UNSUPPORTED, "WQ_MODE_W8A8 takes WQ_ACT_SCALE_ROW");
     if (c->act_scale == WQ_ACT_SCALE_STATIC && !(c->act_gscale > 0.0f && std::isfinite(c->act_gscale)))
         return fail(WQ_ERR_INVALID, "WQ_ACT_SCALE_STATIC needs a finite act_gscale > 0");
+    if (c->transform_order != WQ_ORDER_SMOOTH_ROTATE && c->transform_order != WQ_ORDER_ROTATE_SMOOTH)
+        return fail(WQ_ERR_INVALID, "unknown transform_order");
+    if (c->mode == WQ_MODE_W8A8 && c->transform_order != WQ_ORDER_SMOOTH_ROTATE)
+        return fail(WQ_ERR_UNSUPPORTED, "WQ_MODE_W8A8 takes WQ_ORDER_SMOOTH_ROTATE");
     return WQ_OK;
 }
 
@@ -329,13 +348,26 @@ WQ_API wq_status wq_prepare_weights(const wq_config* cfg, const float* W, const 
     std::vector<float> inv_s(s ? K : 0);
     for (int k = 0; k < (s ? K : 0); ++k) inv_s[k] = 1.0f / s[k];
     const std::vector<float> inv_s_pairs = pair_order(inv_s);
+    // rotation first (QuantWAMs Eq. (1)): smoothing applies in the rotated basis
+    const bool after = cfg->transform_order == WQ_ORDER_ROTATE_SMOOTH && cfg->rotate;
     std::vector<uint16_t> P(static_cast<size_t>(K) * rp, 0), Qt(static_cast<size_t>(N) * rp, 0);
-    for (int k = 0; k < K; ++k)
+    if (!after) {
+        for (int k = 0; k < K; ++k)
+            for (int j = 0; j < r; ++j) {
+                float l = L1[static_cast<size_t>(k) * r + j];
+                if (s) l = l * inv_s[k];
+                P[static_cast<size_t>(k) * rp + j] = bf16_bits(l);
+            }
+    } else {
+        // P = H diag(1/s) L1, fp64, one rounding to bf16
+        std::vector<double> col(K);
         for (int j = 0; j < r; ++j) {
-            float l = L1[static_cast<size_t>(k) * r + j];
-            if (s) l = l * inv_s[k];
-            P[static_cast<size_t>(k) * rp + j] = bf16_bits(l);
+            for (int k = 0; k < K; ++k)
+                col[k] = static_cast<double>(L1[static_cast<size_t>(k) * r + j]) * (s ? static_cast<double>(inv_s[k]) : 1.0);
+            for (int b = 0; b < K / 64; ++b) fwht64_f64(col.data() + 64 * b, 1);
+            for (int k = 0; k < K; ++k) P[static_cast<size_t>(k) * rp + j] = bf16_bits_from_f64(col[k]);
         }
+    }
     // P as the B operand of mma.sync.m16n8k16 (k16 x n8 tiles): for 64-block kb, n-tile nt,
     // lane (g = lane / 4, c = lane % 4) and k16 step f, the lane's two registers hold
     // {P[k][j], P[k+1][j]} and {P[k+8][j], P[k+9][j]} with k = 64 kb + 16 f + 2 c, j = 8 nt + g.
@@ -374,10 +406,12 @@ WQ_API wq_status wq_prepare_weights(const wq_config* cfg, const float* W, const 
                 lr += static_cast<double>(Pf[static_cast<size_t>(k) * r + j]) *
                       static_cast<double>(Qf[static_cast<size_t>(j) * N + n]);
             const double t = static_cast<double>(W[static_cast<size_t>(k) * N + n]) - lr;
-            col[k] = s ? static_cast<double>(s[k]) * t : t;
+            col[k] = (s && !after) ? static_cast<double>(s[k]) * t : t;
         }
         if (cfg->rotate)
             for (int b = 0; b < K / 64; ++b) fwht64_f64(col.data() + 64 * b, 1);
+        if (s && after)
+            for (int k = 0; k < K; ++k) col[k] = static_cast<double>(s[k]) * col[k];
         for (int k = 0; k < K; ++k) Rp[static_cast<size_t>(k) * N + n] = static_cast<float>(col[k]);
     });
 
@@ -607,7 +641,7 @@ static wq_status run_quant(wq_weights_t h, const void* x, int M, int layout, uin
     qa.M = M;
     qa.K = h->cfg.K;
     qa.inv_s = h->d_inv_s;
-    qa.rotate = h->cfg.rotate;
+    qa.rotate = h->cfg.rotate | (h->cfg.rotate && h->cfg.transform_order == WQ_ORDER_ROTATE_SMOOTH ? 2 : 0);
     qa.omega_blk = h->d_omega_blk;
     qa.n_out = xo ? h->cfg.n_outliers : 0;
     qa.xo_ld = h->no_pad;
@@ -646,7 +680,8 @@ WQ_API wq_status wq_quantize_activations(wq_weights_t h, const void* x, int M, i
 }
 
 static wq_status run_gemm(wq_weights_t h, const uint8_t* codes, const uint8_t* sf, const float* g,
-                          const uint16_t* u, const uint16_t* xo, int M, void* y, cudaStream_t st) {
+                          const uint16_t* u, const uint16_t* xo, int M, void* y, cudaStream_t st,
+                          const wq::ChainArgs* chain = nullptr) {
     const int K = h->cfg.K, N = h->cfg.N, r = h->r_pad, no = h->no_pad, no_real = h->cfg.n_outliers;
     std::lock_guard<std::mutex> lk(h->mu);
     if (h->key_codes != codes || h->key_u != u || h->key_xo != xo || h->key_y != y || h->key_M != M) {
@@ -685,6 +720,8 @@ static wq_status run_gemm(wq_weights_t h, const uint8_t* codes, const uint8_t* s
     ga.w8 = h->cfg.mode == WQ_MODE_W8A8;
     ga.colscale = h->d_colscale;
     ga.force_split = wq::tune(wq::kTuneGemmSplit);     // 0: choose (tests and tuning pin it)
+    ga.chain = chain;
+    if (chain) ga.force_split = 0;
     const cudaError_t e = wq::launch_gemm(ga, st);
     if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
     return WQ_OK;
@@ -692,7 +729,8 @@ static wq_status run_gemm(wq_weights_t h, const uint8_t* codes, const uint8_t* s
 
 namespace {
 bool use_fused(wq_weights_t h, int M, int& nb, int& cs) {
-    return h->cfg.mode == WQ_MODE_W4A4 && h->cfg.act_scale == WQ_ACT_SCALE_ROW && wq::tune(wq::kTuneFused) == 1 &&
+    return h->cfg.mode == WQ_MODE_W4A4 && h->cfg.act_scale == WQ_ACT_SCALE_ROW &&
+           h->cfg.transform_order == WQ_ORDER_SMOOTH_ROTATE && wq::tune(wq::kTuneFused) == 1 &&
            wq::fused_plan(M, h->cfg.K, h->cfg.N, h->r_pad, h->no_pad, nb, cs);
 }
 }  // namespace
@@ -763,6 +801,49 @@ WQ_API wq_status wq_linear_forward(wq_weights_t h, const void* x, int M, void* y
                             r ? ws.u : nullptr, ws.amax, st);
     if (s != WQ_OK) return s;
     return run_gemm(h, ws.codes, ws.sf, ws.g, ws.u, ws.xo, M, y, st);
+}
+
+WQ_API wq_status wq_linear_forward_chain(wq_weights_t h, wq_weights_t next, const void* x, int M, uint8_t* codes,
+                                         uint8_t* scales_mma, float* gscale, void* x_omega, void* workspace,
+                                         size_t workspace_bytes, void* stream) {
+    if (!h || !next) return fail(WQ_ERR_INVALID, "NULL handle");
+    if (M < 0) return fail(WQ_ERR_INVALID, "M < 0");
+    if (M == 0) return WQ_OK;
+    if (h->cfg.mode != WQ_MODE_W4A4 || next->cfg.mode != WQ_MODE_W4A4 || h->conv_cin || next->conv_cin)
+        return fail(WQ_ERR_INVALID, "both handles must be 4-bit linear layers");
+    if (next->cfg.K != h->cfg.N) return fail(WQ_ERR_INVALID, "next layer's K differs from this layer's N");
+    if (next->cfg.act_scale != WQ_ACT_SCALE_STATIC)
+        return fail(WQ_ERR_UNSUPPORTED, "the next layer needs a fixed tensor scale (WQ_ACT_SCALE_STATIC): no "
+                                        "output tile sees a whole row");
+    if (next->cfg.rank != 0)
+        return fail(WQ_ERR_UNSUPPORTED, "the next layer's low-rank branch needs its whole input row (rank must be 0)");
+    if (next->device != h->device) return fail(WQ_ERR_INVALID, "handles on different devices");
+    if (!x || !codes || !scales_mma || !gscale || !workspace || (next->cfg.n_outliers && !x_omega))
+        return fail(WQ_ERR_INVALID, "NULL buffer");
+    if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(codes) | reinterpret_cast<uintptr_t>(scales_mma) |
+         reinterpret_cast<uintptr_t>(x_omega)) & 15)
+        return fail(WQ_ERR_INVALID, "device buffers must be 16-byte aligned");
+    if (reinterpret_cast<uintptr_t>(workspace) & 255) return fail(WQ_ERR_INVALID, "workspace must be 256-byte aligned");
+    if (const wq_status d = check_device(h)) return d;
+    const wq::ActWorkspace ws = wq::carve_workspace(workspace, M, h->cfg.K, h->r_pad, h->no_pad);
+    if (workspace_bytes < ws.bytes) return fail(WQ_ERR_INVALID, "workspace too small");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    wq_status s = run_quant(h, x, M, WQ_SCALE_LAYOUT_MMA, ws.codes, ws.sf, ws.g, h->no_pad ? ws.xo : nullptr,
+                            h->r_pad ? ws.u : nullptr, ws.amax, st);
+    if (s != WQ_OK) return s;
+    wq::ChainArgs c{};
+    c.inv_s = next->d_inv_s;
+    c.rotate = next->cfg.rotate | (next->cfg.rotate && next->cfg.transform_order == WQ_ORDER_ROTATE_SMOOTH ? 2 : 0);
+    c.omega_blk = next->d_omega_blk;
+    c.n_out = next->cfg.n_outliers;
+    c.xo_ld = next->no_pad;
+    c.xo = static_cast<uint16_t*>(x_omega);
+    c.codes = codes;
+    c.sf = scales_mma;
+    c.g_out = gscale;
+    c.g = next->cfg.act_gscale;
+    // the output map is never used in this mode; it is keyed to the codes buffer
+    return run_gemm(h, ws.codes, ws.sf, ws.g, ws.u, ws.xo, M, codes, st, &c);
 }
 
 WQ_API wq_status wq_linear_forward_quantized(wq_weights_t h, const uint8_t* codes, const uint8_t* scales_mma,
@@ -850,7 +931,7 @@ WQ_API wq_status wq_prepare_conv3d(const float* w, int C_in, int C_out, int kt, 
         for (int c = 0; c < C_in; ++c)
             for (int t = 0; t < 27; ++t)
                 Wm[(static_cast<size_t>(t) * C_in + c) * N + n] = w[(static_cast<size_t>(n) * C_in + c) * 27 + t];
-    wq_config cfg{K, N, 0, 0, 0, WQ_MODE_W4A4, WQ_ACT_SCALE_ROW, 0.0f};
+    wq_config cfg{K, N, 0, 0, 0, WQ_MODE_W4A4, WQ_ACT_SCALE_ROW, 0.0f, WQ_ORDER_SMOOTH_ROTATE};
     wq_weights_t h = nullptr;
     const wq_status st = wq_prepare_weights(&cfg, Wm.data(), nullptr, nullptr, nullptr, nullptr, nullptr, stream, &h);
     if (st != WQ_OK) return st;

@@ -734,7 +734,7 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
     // single-buffered, so each tile pays the drain and the side branch before the next main
     // loop.  It is chosen for 4-bit layers with K >= 1024 whose 256 x 256 tiles fill every SM
     // pair.  The WQ_GEMM_WIDE knob pins the choice (tests and tuning).
-    if (use_wide(a)) return launch_gemm_wide(a, st);
+    if (a.chain != nullptr || use_wide(a)) return launch_gemm_wide(a, st);
     return a.w8 ? launch_gemm_t<true>(a, st) : launch_gemm_t<false>(a, st);
 }
 

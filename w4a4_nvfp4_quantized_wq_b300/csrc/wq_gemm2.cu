@@ -34,6 +34,8 @@
 #include <cstdlib>
 
 #include "ptx.cuh"
+#include "quant_block.cuh"
+#include "quant_math.cuh"
 #include "wq_internal.h"
 
 #ifdef WQ_TRACE
@@ -80,6 +82,8 @@ struct WParams {
     const float* bias;
     const float* colscale;
     int* err;
+    int chain;               // 1: quantise the tile for the next layer instead of storing y
+    ChainArgs ch;
 };
 
 __host__ __device__ constexpr uint32_t stage_bytes(bool w8) { return w8 ? kStage8 : kStage4; }
@@ -93,6 +97,91 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// ---------------------------------------------------------------- chain epilogue
+// One row's 64-column block held as two 32-value halves (x: columns 0..31, y: 32..63), in place.
+__device__ __forceinline__ float& cv(uint32_t (&x)[32], uint32_t (&y)[32], int i) {
+    return *reinterpret_cast<float*>(i < 32 ? &x[i] : &y[i - 32]);
+}
+
+// The next layer's input transform of one 64-block (FoldQuantVLA Key Contribution 2 / QuantWAMs
+// Eq. (1)): smoothing before or after the Walsh-Hadamard butterflies at strides 1..32 (the pages'
+// order, one fp32 add or subtract each), then the exact 1/8.  inv_pairs: the block's 64 inv_s in
+// pair order (per 32-channel half, channels k and k + 16 side by side).
+__device__ __forceinline__ void chain_transform(uint32_t (&x)[32], uint32_t (&y)[32], const float* inv_pairs,
+                                                int rotate) {
+    const bool after = (rotate & 3) == 3;
+    auto smooth = [&]() {
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const float2 sv = __ldg(reinterpret_cast<const float2*>(inv_pairs + 32 * hf + 2 * k));
+                cv(x, y, 32 * hf + k) = __fmul_rn(cv(x, y, 32 * hf + k), sv.x);
+                cv(x, y, 32 * hf + k + 16) = __fmul_rn(cv(x, y, 32 * hf + k + 16), sv.y);
+            }
+    };
+    if (inv_pairs != nullptr && !after) smooth();
+    if (rotate & 1) {
+#pragma unroll
+        for (int h = 1; h < 64; h <<= 1)
+#pragma unroll
+            for (int i = 0; i < 64; ++i)
+                if ((i & h) == 0) {
+                    const float a = cv(x, y, i), b = cv(x, y, i + h);
+                    cv(x, y, i) = __fadd_rn(a, b);
+                    cv(x, y, i + h) = __fsub_rn(a, b);
+                }
+#pragma unroll
+        for (int i = 0; i < 64; ++i) cv(x, y, i) = __fmul_rn(cv(x, y, i), 0.125f);
+        if (inv_pairs != nullptr && after) smooth();
+    }
+}
+
+// Kept channels of the block to x_O (fp16) and +0 in the values; NVFP4 codes and e4m3 scales of
+// the block with the fixed g (the same rounding steps as the activation quantiser), stored in the
+// layouts the next layer's GEMM reads.
+__device__ __forceinline__ void chain_emit(uint32_t (&x)[32], uint32_t (&y)[32], const ChainArgs& c, int m,
+                                           bool row_ok, int kb, int K) {
+    if (c.n_out) {
+        const uint32_t m0 = __ldg(c.omega_blk + 4 * kb), m1 = __ldg(c.omega_blk + 4 * kb + 1);
+        uint32_t idx = __ldg(c.omega_blk + 4 * kb + 2);
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+            const uint32_t bit = i < 32 ? (m0 >> i) & 1u : (m1 >> (i - 32)) & 1u;
+            if (bit) {
+                if (row_ok) c.xo[static_cast<size_t>(m) * c.xo_ld + idx] = __half_as_ushort(__float2half_rn(cv(x, y, i)));
+                cv(x, y, i) = 0.0f;
+                ++idx;
+            }
+        }
+    }
+    const float g = c.g, rg = __frcp_rn(c.g);
+    uint32_t words[8], sc4 = 0;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        float vals[16];
+        float bm = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            vals[i] = cv(x, y, 16 * b + i);
+            bm = fmaxf(bm, fabsf(vals[i]));
+        }
+        const uint32_t sc = scale_code<false>(bm, g, rg);
+        const float d = __fmul_rn(dec_e4m3(sc), g);
+        const float r = __frcp_rn(d);
+        words[2 * b] = d != 0.0f ? e2m1_codes8_r<false>(vals, d, r) : 0u;
+        words[2 * b + 1] = d != 0.0f ? e2m1_codes8_r<false>(vals + 8, d, r) : 0u;
+        sc4 |= sc << (8 * b);
+    }
+    if (row_ok) {
+        uint4* dst = reinterpret_cast<uint4*>(c.codes + static_cast<size_t>(m) * (K / 2) + kb * 32);
+        dst[0] = make_uint4(words[0], words[1], words[2], words[3]);
+        dst[1] = make_uint4(words[4], words[5], words[6], words[7]);
+        const size_t off = (static_cast<size_t>(m / 128) * (K / 64) + kb) * kSfAtom + (m % 32) * 16 + ((m % 128) / 32) * 4;
+        *reinterpret_cast<uint32_t*>(c.sf + off) = sc4;
+    }
 }
 
 template <bool kW8>
@@ -150,7 +239,7 @@ wide_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
-        tma_prefetch_desc(&tmY);
+        if (!p.chain) tma_prefetch_desc(&tmY);
     }
     if (warp == 1) {
         tmem_alloc_pair(smem_u32(tmem_holder), 512);
@@ -435,6 +524,36 @@ wide_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             }
             if (lane == 0) WT_ADD(11, te3);
             WT_T0(te4);
+            if (!kW8 && p.chain) {
+                // the next layer's NVFP4 input from this row's 128 columns (two 64-blocks), from
+                // the bf16 value the output would have stored
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    a0[i] = __float_as_uint(__bfloat162float(__float2bfloat16_rn(__uint_as_float(a0[i]))));
+                    a1[i] = __float_as_uint(__bfloat162float(__float2bfloat16_rn(__uint_as_float(a1[i]))));
+                    a2[i] = __float_as_uint(__bfloat162float(__float2bfloat16_rn(__uint_as_float(a2[i]))));
+                    a3[i] = __float_as_uint(__bfloat162float(__float2bfloat16_rn(__uint_as_float(a3[i]))));
+                }
+                const bool row_ok = row < M;
+                const int c0 = nb * 256 + 128 * hh;
+                if (c0 < N) {
+                    const int kb = c0 / 64;
+                    chain_transform(a0, a1, p.ch.inv_s ? p.ch.inv_s + 64 * kb : nullptr, p.ch.rotate);
+                    chain_emit(a0, a1, p.ch, row, row_ok, kb, N);
+                }
+                if (c0 + 64 < N) {
+                    const int kb = c0 / 64 + 1;
+                    chain_transform(a2, a3, p.ch.inv_s ? p.ch.inv_s + 64 * kb : nullptr, p.ch.rotate);
+                    chain_emit(a2, a3, p.ch, row, row_ok, kb, N);
+                }
+                if (row_ok && nb == 0 && hh == 0) {
+                    p.ch.g_out[row] = p.ch.g;
+                    for (int cc = p.ch.n_out; cc < p.ch.xo_ld; ++cc) p.ch.xo[static_cast<size_t>(row) * p.ch.xo_ld + cc] = 0;
+                }
+                if (lane == 0) WT_ADD(12, te4);
+                if (lane == 0) WT_ADD(9, te1);
+                continue;
+            }
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const uint32_t* acc = j == 0 ? a0 : (j == 1 ? a1 : (j == 2 ? a2 : a3));
@@ -495,6 +614,11 @@ cudaError_t launch_gemm_wide(const GemmArgs& a, cudaStream_t st) {
     p.off_bar = p.off_y + kYBytes;
     p.sfa = a.sfa; p.sfb = a.sfb; p.gA = a.gA; p.gW = a.gW; p.bias = a.bias; p.colscale = a.colscale;
     p.err = a.err;
+    if (a.chain != nullptr) {
+        if (w8 || (a.N % 64) != 0) return cudaErrorInvalidValue;
+        p.chain = 1;
+        p.ch = *a.chain;
+    }
     const uint32_t total = p.off_bar + 8u * (4 * S + 6) + 16u + 1024u;
     static bool attr_set[2] = {false, false};
     if (!attr_set[w8]) {

@@ -81,6 +81,21 @@ cudaError_t launch_quantize_act(const QuantArgs& a, cudaStream_t stream);
 // True when M rows take the persistent stream schedule (else the cluster schedule).
 bool quant_stream_schedule(int M, int num_sms);
 
+// The epilogue quantises the tile's bf16 output for the next layer instead of storing it
+// (wq_linear_forward_chain): the next layer's smoothing, block-64 FWHT along this layer's N, kept
+// channels and NVFP4 coding with its fixed tensor scale.
+struct ChainArgs {
+    const float* inv_s;             // next layer's inv_s in pair order [N] or null
+    int rotate;                     // bit 0: FWHT; bit 1: smooth after the rotation
+    const uint32_t* omega_blk;      // next layer's kept-channel table [N/64][4] or null
+    int n_out, xo_ld;               // kept channels and the x_O row stride
+    uint16_t* xo;                   // fp16 [M, xo_ld]
+    uint8_t* codes;                 // [M, N/2]
+    uint8_t* sf;                    // MMA layout, ceil(M/128) x N/64 atoms
+    float* g_out;                   // [M], every entry the fixed g
+    float g;                        // the next layer's fixed tensor scale
+};
+
 struct GemmArgs {
     int M, N, K, r, n_out;
     const CUtensorMap* tmA;   // activation codes [M, K/2] u8, box 128x128, swizzle 128B
@@ -101,6 +116,7 @@ struct GemmArgs {
     int force_split;          // 0: choose; otherwise CTAs per tile (power of two <= 16)
     bool w8 = false;          // 8-bit layer: A/W are int8 codes stored as bf16 [., K]
     const float* colscale = nullptr;  // 8-bit layer: per-output-column scale [N]
+    const ChainArgs* chain = nullptr; // non-null: quantise the output for the next layer (pair schedule)
 };
 
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream);

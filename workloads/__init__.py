@@ -172,19 +172,32 @@ def lowrank_factors(W: np.ndarray, s: np.ndarray, r: int):
     return L1, L2
 
 
-def pooled_energy_topk(x: np.ndarray, s: np.ndarray, k_out: int, rotate: bool) -> np.ndarray:
+def _block_hadamard(a: np.ndarray, axis: int) -> np.ndarray:
+    """Dense block-64 Sylvester transform (1/8 normalised) along `axis`, fp64 (calibration only)."""
+    from scipy.linalg import hadamard
+    H = hadamard(64).astype(np.float64) / 8.0
+    a = np.moveaxis(np.asarray(a, np.float64), axis, -1)
+    sh = a.shape
+    out = (a.reshape(*sh[:-1], sh[-1] // 64, 64) @ H).reshape(sh)
+    return np.moveaxis(out, -1, axis)
+
+
+def pooled_energy_topk(x: np.ndarray, s: np.ndarray, k_out: int, rotate: bool,
+                       smooth_after: bool = False) -> np.ndarray:
     """Top-K channels of z(c) = mean_t xt[t,c]^2 on the transformed input (dense H)."""
     if k_out == 0:
         return np.zeros(0, dtype=np.int32)
-    from scipy.linalg import hadamard
     M, K = x.shape
-    H = hadamard(64).astype(np.float64) / 8.0
     z = np.zeros(K, dtype=np.float64)
     step = 2048
     for m0 in range(0, M, step):
-        xs = x[m0:m0 + step].astype(np.float64) / s.astype(np.float64)[None, :]
-        if rotate:
-            xs = (xs.reshape(xs.shape[0], K // 64, 64) @ H).reshape(xs.shape[0], K)
+        xs = x[m0:m0 + step].astype(np.float64)
+        if smooth_after and rotate:
+            xs = _block_hadamard(xs, 1) / s.astype(np.float64)[None, :]
+        else:
+            xs = xs / s.astype(np.float64)[None, :]
+            if rotate:
+                xs = _block_hadamard(xs, 1)
         z += (xs * xs).sum(axis=0)
     z /= M
     order = sorted(range(K), key=lambda c: (-z[c], c))[:k_out]
@@ -204,6 +217,7 @@ class LayerInputs:
     L2: Optional[np.ndarray]      # fp32 [r, N]
     omega: np.ndarray             # int32 [n_omega]
     rotate: bool = True
+    smooth_after: bool = False    # rotation first, then smoothing (QuantWAMs Eq. (1))
 
     @property
     def x_f32(self) -> np.ndarray:
@@ -217,9 +231,12 @@ class LayerInputs:
 def make_layer_inputs(workload: str, layer: int = 0, M: Optional[int] = None,
                       K: Optional[int] = None, N: Optional[int] = None,
                       rank: Optional[int] = None, n_omega: Optional[int] = None,
-                      smooth: Optional[bool] = None, rotate: Optional[bool] = None) -> LayerInputs:
+                      smooth: Optional[bool] = None, rotate: Optional[bool] = None,
+                      smooth_after: bool = False) -> LayerInputs:
     """Draw one layer of a workload.  Shape/feature overrides give smaller parity cases
-    with the same distributions (the seed stream is unchanged)."""
+    with the same distributions (the seed stream is unchanged).  smooth_after: the
+    calibration products are taken in the rotate-then-smooth basis (s from the rotated
+    activations and weights, the low-rank factors of S H W, Omega of x H S^-1)."""
     wl = WORKLOADS[workload]
     spec = wl.layers[layer]
     M = wl.M if M is None else M
@@ -234,11 +251,19 @@ def make_layer_inputs(workload: str, layer: int = 0, M: Optional[int] = None,
     xb = bf16_from_bits(x_bits)
     W = _draw_w(wl, K, N, layer)
     b = _draw_b(wl, N, layer)
-    s = smoothing_factors(xb, W) if do_smooth else None
-    s_eff = s if s is not None else np.ones(K, dtype=np.float32)
-    L1, L2 = lowrank_factors(W, s_eff, r) if (spec.mode == "w4a4" and r > 0) else (None, None)
-    omega = pooled_energy_topk(xb, s_eff, n_om, do_rot) if spec.mode == "w4a4" else np.zeros(0, np.int32)
-    return LayerInputs(wl, dataclasses.replace(spec, K=K, N=N), M, x_bits, W, b, s, L1, L2, omega, do_rot)
+    after = bool(smooth_after) and do_rot
+    if after:
+        xr = _block_hadamard(xb, 1).astype(np.float32)          # x H
+        Wr = _block_hadamard(W, 0).astype(np.float32)           # H W (H symmetric)
+        s = smoothing_factors(xr, Wr) if do_smooth else None
+        s_eff = s if s is not None else np.ones(K, dtype=np.float32)
+        L1, L2 = lowrank_factors(Wr, s_eff, r) if (spec.mode == "w4a4" and r > 0) else (None, None)
+    else:
+        s = smoothing_factors(xb, W) if do_smooth else None
+        s_eff = s if s is not None else np.ones(K, dtype=np.float32)
+        L1, L2 = lowrank_factors(W, s_eff, r) if (spec.mode == "w4a4" and r > 0) else (None, None)
+    omega = pooled_energy_topk(xb, s_eff, n_om, do_rot, after) if spec.mode == "w4a4" else np.zeros(0, np.int32)
+    return LayerInputs(wl, dataclasses.replace(spec, K=K, N=N), M, x_bits, W, b, s, L1, L2, omega, do_rot, after)
 
 
 def make_conv_inputs(T: Optional[int] = None, H: Optional[int] = None, W: Optional[int] = None,
