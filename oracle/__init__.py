@@ -76,6 +76,14 @@ def lib() -> ctypes.CDLL:
             L.orc_linear_forward_w8a8.restype = i32
             L.orc_set_smooth_after.argtypes = [i32]
             L.orc_set_smooth_after.restype = None
+            L.orc_e4m3s_encode.argtypes = [f32]; L.orc_e4m3s_encode.restype = ctypes.c_uint8
+            L.orc_e4m3s_decode.argtypes = [ctypes.c_uint8]; L.orc_e4m3s_decode.restype = ctypes.c_double
+            L.orc_quantize_act_fp8.argtypes = [P, i64, i64, P, i32, P, P, i32]
+            L.orc_quantize_act_fp8.restype = i32
+            L.orc_quantize_weights_fp8.argtypes = [P, i64, i64, P, P]
+            L.orc_quantize_weights_fp8.restype = i32
+            L.orc_linear_forward_fp8.argtypes = [P, P, i64, P, P, i64, i64, P, P, i32]
+            L.orc_linear_forward_fp8.restype = i32
             _lib = L
     return _lib
 
@@ -378,6 +386,54 @@ def reference_forward_w8a8(layer, n_threads: int = 0, rows=None):
     wq8 = prepare_weights_int8(layer.W, layer.s, layer.rotate, n_threads)
     aq = quantize_act_int8(x_bits, layer.s, layer.rotate, n_threads)
     return linear_forward_w8a8(aq, wq8, layer.bias, n_threads), aq, wq8
+
+
+# ------------------------------------------------------------------ W8A8 in FP8
+@dataclass
+class Fp8Quant:
+    q: np.ndarray            # uint8 e4m3 codes [rows, K]
+    scale: np.ndarray        # fp32 [rows]
+
+
+def quantize_act_fp8(x_bits, s, rotate, n_threads: int = 0) -> Fp8Quant:
+    """Per-token e4m3 of the transformed activations (QuantWAMs sec. 4.2: FP8 W8A8 for the
+    upgraded layers), scale = amax / 448."""
+    x_bits = _c(x_bits, np.uint16)
+    M, K = x_bits.shape
+    inv_s = inv_smoothing(s)
+    q = np.zeros((M, K), np.uint8)
+    a = np.zeros(M, np.float32)
+    rc = lib().orc_quantize_act_fp8(_p(x_bits), M, K, _p(inv_s), int(rotate), _p(q), _p(a), int(n_threads))
+    if rc:
+        raise ValueError(f"orc_quantize_act_fp8 failed: {rc}")
+    return Fp8Quant(q, a)
+
+
+def prepare_weights_fp8(W, s, rotate, n_threads: int = 0) -> Fp8Quant:
+    """Fold smoothing + rotation into W (Proposition 1), then per-output-channel e4m3."""
+    wq = prepare_weights(W, s, None, None, None, rotate, n_threads)
+    K, N = wq.Rp.shape
+    q = np.zeros((N, K), np.uint8)
+    w = np.zeros(N, np.float32)
+    lib().orc_quantize_weights_fp8(_p(np.ascontiguousarray(wq.Rp)), K, N, _p(q), _p(w))
+    return Fp8Quant(q, w)
+
+
+def linear_forward_fp8(aq: Fp8Quant, wq8: Fp8Quant, bias, n_threads: int = 0) -> np.ndarray:
+    M, K = aq.q.shape
+    N = wq8.q.shape[0]
+    y = np.zeros((M, N), np.float64)
+    bias = _c(bias, np.float32)
+    lib().orc_linear_forward_fp8(_p(aq.q), _p(aq.scale), M, _p(wq8.q), _p(wq8.scale), N, K, _p(bias), _p(y),
+                                 int(n_threads))
+    return y
+
+
+def reference_forward_fp8(layer, n_threads: int = 0, rows=None):
+    x_bits = layer.x_bits if rows is None else layer.x_bits[rows]
+    wq8 = prepare_weights_fp8(layer.W, layer.s, layer.rotate, n_threads)
+    aq = quantize_act_fp8(x_bits, layer.s, layer.rotate, n_threads)
+    return linear_forward_fp8(aq, wq8, layer.bias, n_threads), aq, wq8
 
 
 # ------------------------------------------------------------------ Conv3d (VAE)

@@ -627,6 +627,109 @@ int orc_linear_forward_w8a8(const int8_t *qa, const float *a, long M, const int8
     return 0;
 }
 
+/* ------------------------------------------------------------------ W8A8 (FP8) */
+/* Upgraded layers in FP8 W8A8 (QuantWAMs sec. 4.2 "Backend": "upgraded layers use FP8 W8A8
+ * kernels").  Reading: e4m3 values (4 exponent bits, bias 7, 3 mantissa bits, finite maximum
+ * 448, sign bit 7) with one fp32 scale per token and per output column, scale = amax / 448,
+ * q = e4m3_rne_satfinite(RN(v / scale)) -- the quotient one IEEE fp32 division, then one
+ * rounding to e4m3; a zero scale gives zero codes.  Same transformed basis as the other
+ * layers.  The product of two e4m3 values is exact in fp64, so the fp64 sum is exact up to
+ * the fp64 accumulation. */
+
+/* Signed e4m3 code of v (sign bit 7 | the unsigned code of |v|). */
+uint8_t orc_e4m3s_encode(float v)
+{
+    uint8_t sign = signbit(v) ? 0x80 : 0;
+    return (uint8_t)(sign | orc_e4m3_encode(fabsf(v)));
+}
+
+double orc_e4m3s_decode(uint8_t c)
+{
+    double m = orc_e4m3_decode((uint8_t)(c & 0x7F));
+    return (c & 0x80) ? -m : m;
+}
+
+float orc_fp8_scale(float amax) { return amax / 448.0f; }
+
+static uint8_t fp8_code(float v, float scale)
+{
+    if (scale == 0.0f) return 0;
+    return orc_e4m3s_encode(v / scale);
+}
+
+/* x bf16 [M, K] -> q e4m3 [M, K], a fp32 [M] (smoothing and rotation as for W4A4). */
+int orc_quantize_act_fp8(const uint16_t *x_bf16, long M, long K, const float *inv_s, int rotate,
+                         uint8_t *q, float *a, int n_threads)
+{
+    if (K % 16 || (rotate && K % 64)) return -1;
+#ifdef _OPENMP
+    if (n_threads > 0) omp_set_num_threads(n_threads);
+#else
+    (void)n_threads;
+#endif
+    int rc = 0;
+#pragma omp parallel
+    {
+        float *xt = (float *)malloc(sizeof(float) * (size_t)K);
+        if (!xt) {
+#pragma omp atomic write
+            rc = -4;
+        } else {
+#pragma omp for schedule(static)
+            for (long m = 0; m < M; ++m) {
+                orc_act_transform_row(x_bf16 + m * K, K, inv_s, rotate, xt);
+                float amax = 0.0f;
+                for (long k = 0; k < K; ++k) {
+                    float v = fabsf(xt[k]);
+                    if (v > amax) amax = v;
+                }
+                float s = orc_fp8_scale(amax);
+                a[m] = s;
+                for (long k = 0; k < K; ++k) q[m * K + k] = fp8_code(xt[k], s);
+            }
+            free(xt);
+        }
+    }
+    return rc;
+}
+
+/* Folded weight Rp fp32 [K, N] -> q e4m3 [N, K] (K-major), w fp32 [N]. */
+int orc_quantize_weights_fp8(const float *Rp, long K, long N, uint8_t *q, float *w)
+{
+    for (long n = 0; n < N; ++n) {
+        float amax = 0.0f;
+        for (long k = 0; k < K; ++k) {
+            float v = fabsf(Rp[k * N + n]);
+            if (v > amax) amax = v;
+        }
+        float s = orc_fp8_scale(amax);
+        w[n] = s;
+        for (long k = 0; k < K; ++k) q[n * K + k] = fp8_code(Rp[k * N + n], s);
+    }
+    return 0;
+}
+
+/* y[m][n] = (sum_k dec(qa[m][k]) dec(qw[n][k])) * a[m] * w[n] + b[n], fp64. */
+int orc_linear_forward_fp8(const uint8_t *qa, const float *a, long M, const uint8_t *qw, const float *w, long N,
+                           long K, const float *bias, double *y, int n_threads)
+{
+#ifdef _OPENMP
+    if (n_threads > 0) omp_set_num_threads(n_threads);
+#else
+    (void)n_threads;
+#endif
+#pragma omp parallel for schedule(static)
+    for (long m = 0; m < M; ++m)
+        for (long n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (long k = 0; k < K; ++k) acc += orc_e4m3s_decode(qa[m * K + k]) * orc_e4m3s_decode(qw[n * K + k]);
+            double v = acc * (double)a[m] * (double)w[n];
+            if (bias) v += (double)bias[n];
+            y[m * N + n] = v;
+        }
+    return 0;
+}
+
 /* ------------------------------------------------------------------ Conv3d */
 /* NVFP4 execution of the video VAE's 3x3x3 convolutions (LatentQuant, Abstract).  Plainest
  * reading: the input tensor is quantised once, per voxel along channels (16-channel blocks)
