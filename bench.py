@@ -45,6 +45,8 @@ WORKLOAD_TEXT = {
                 "M=31200 voxels, K=10368, N=384, NVFP4 with a per-tensor activation scale",
     "backbone": "language backbone prefill M=768: QKV 2048->6144 and gate/up 2048->32768 in W4A4, "
                 "o_proj 2048->2048 and down 16384->2048 in W8A8 (int8 codes held as bf16)",
+    "backbone_fp8": "language backbone prefill M=768: QKV 2048->6144 and gate/up 2048->32768 in W4A4, "
+                    "o_proj 2048->2048 and down 16384->2048 in FP8 W8A8 (e4m3 codes, kind::f8f6f4)",
 }
 
 
@@ -63,7 +65,8 @@ def parse_args():
     a = ap.parse_args()
     # defaults keep the timed region to seconds (a video-DiT step is ~1 ms, an expert step ~30 us)
     d_steps, d_warm, d_iters = {"video_dit": (200, 10, 30), "vae_conv": (200, 10, 50), "backbone": (500, 20, 100),
-                                "expert": (2000, 50, 200), "tiny": (2000, 50, 200)}[a.workload]
+                                "backbone_fp8": (500, 20, 100), "expert": (2000, 50, 200),
+                                "tiny": (2000, 50, 200)}[a.workload]
     a.steps = d_steps if a.steps is None else a.steps
     a.warmup = d_warm if a.warmup is None else a.warmup
     a.kernel_iters = d_iters if a.kernel_iters is None else a.kernel_iters
@@ -96,7 +99,7 @@ def job_throughput(units_per_rank_step: float, steps: int, ws: int, job_ms: floa
 
 def layers_of(name):
     import workloads as wl
-    w = wl.WORKLOADS[name]
+    w = wl.WORKLOADS[base_workload(name)]
     return w, list(range(len(w.layers)))
 
 
@@ -286,26 +289,44 @@ def profiled_traffic(kernel: str, workload: str):
     return None
 
 
+def base_workload(name):
+    """The workload whose inputs a bench workload uses (backbone_fp8 runs the backbone's 8-bit
+    layers in FP8)."""
+    return "backbone" if name == "backbone_fp8" else name
+
+
+def eight_bit_mode(wq, name):
+    return wq.WQ_MODE_W8A8_FP8 if name == "backbone_fp8" else wq.WQ_MODE_W8A8
+
+
 # ------------------------------------------------------------------ oracle (CPU) timing
 def oracle_layer_data(name):
     import workloads as wl
     w, idx = layers_of(name)
-    return [wl.make_layer_inputs(name, layer=i) for i in idx]
+    return [wl.make_layer_inputs(base_workload(name), layer=i) for i in idx]
 
 
-def time_oracle(layers, budget_s: float, n_threads: int, min_passes=1):
+def oracle_eight_bit(fp8):
+    """The oracle's 8-bit layer functions: (prepare, quantise, forward), int8 or e4m3."""
+    import oracle
+    if fp8:
+        return oracle.prepare_weights_fp8, oracle.quantize_act_fp8, oracle.linear_forward_fp8
+    return oracle.prepare_weights_int8, oracle.quantize_act_int8, oracle.linear_forward_w8a8
+
+
+def time_oracle(layers, budget_s: float, n_threads: int, min_passes=1, fp8=False):
     """Time the oracle's per-token work (quantiser, low-rank, forward) on row samples;
     returns (tokens/s, rows per pass, passes, seconds)."""
     import oracle
-    prepared = [(L, oracle.prepare_weights_int8(L.W, L.s, L.rotate, n_threads) if L.spec.mode == "w8a8" else
+    prep8, quant8, fwd8 = oracle_eight_bit(fp8)
+    prepared = [(L, prep8(L.W, L.s, L.rotate, n_threads) if L.spec.mode == "w8a8" else
                  oracle.prepare_weights(L.W, L.s, L.L1, L.L2, L.omega, L.rotate, n_threads)) for L in layers]
 
     def one(rows):
         for L, wqo in prepared:
             xb = L.x_bits[rows]
             if L.spec.mode == "w8a8":
-                oracle.linear_forward_w8a8(oracle.quantize_act_int8(xb, L.s, L.rotate, n_threads), wqo, L.bias,
-                                           n_threads)
+                fwd8(quant8(xb, L.s, L.rotate, n_threads), wqo, L.bias, n_threads)
                 continue
             aq = oracle.quantize_act(xb, L.s, L.rotate, L.omega, n_threads=n_threads)
             U = oracle.lowrank_act(xb, wqo.P) if wqo.P.shape[1] else None
@@ -339,7 +360,8 @@ def run_reference(args):
     n_threads = os.cpu_count() or 1
     layers = oracle_layer_data(args.workload)
     import oracle as orc
-    prepared = [(L, orc.prepare_weights_int8(L.W, L.s, L.rotate, n_threads) if L.spec.mode == "w8a8" else
+    prep8, quant8, fwd8 = oracle_eight_bit(args.workload == "backbone_fp8")
+    prepared = [(L, prep8(L.W, L.s, L.rotate, n_threads) if L.spec.mode == "w8a8" else
                  orc.prepare_weights(L.W, L.s, L.L1, L.L2, L.omega, L.rotate, n_threads)) for L in layers]
     M = layers[0].M
     # size each step's row sample so that warmup + steps fit in about a minute
@@ -350,7 +372,7 @@ def run_reference(args):
         for L, wqo in prepared:
             xb = L.x_bits[rows]
             if L.spec.mode == "w8a8":
-                orc.linear_forward_w8a8(orc.quantize_act_int8(xb, L.s, L.rotate, n_threads), wqo, L.bias, n_threads)
+                fwd8(quant8(xb, L.s, L.rotate, n_threads), wqo, L.bias, n_threads)
                 continue
             aq = orc.quantize_act(xb, L.s, L.rotate, L.omega, n_threads=n_threads)
             U = orc.lowrank_act(xb, wqo.P) if wqo.P.shape[1] else None
@@ -399,13 +421,14 @@ def run_wq(args):
     wlw, idx = layers_of(args.workload)
     if args.only_layer:
         idx = [i for i in idx if wlw.layers[i].name == args.only_layer]
-    layers = [wl.make_layer_inputs(args.workload, layer=i) for i in idx]
+    layers = [wl.make_layer_inputs(base_workload(args.workload), layer=i) for i in idx]
     M = wlw.M
     stream = torch.cuda.Stream(device=dev)
     H = []
     for L in layers:
         if L.spec.mode == "w8a8":
-            w = wq.wq_prepare_weights(L.spec.K, L.spec.N, L.W, L.bias, L.s, rotate=L.rotate, mode=wq.WQ_MODE_W8A8)
+            w = wq.wq_prepare_weights(L.spec.K, L.spec.N, L.W, L.bias, L.s, rotate=L.rotate,
+                                      mode=eight_bit_mode(wq, args.workload))
         else:
             w = wq.wq_prepare_weights(L.spec.K, L.spec.N, L.W, L.bias, L.s, L.L1, L.L2,
                                       L.omega if L.omega.size else None, rotate=L.rotate)
@@ -580,7 +603,8 @@ def run_wq(args):
     if rank == 0 and not args.no_cpu_baseline and ws == 1:
         n_threads = os.cpu_count() or 1
         try:
-            tps, rows, passes, el = time_oracle(layers, args.cpu_baseline_seconds, n_threads)
+            tps, rows, passes, el = time_oracle(layers, args.cpu_baseline_seconds, n_threads,
+                                                fp8=args.workload == "backbone_fp8")
             cpu = {"value": tps, "unit": "tokens/s", "cores": n_threads, "kind": "oracle",
                    "sample": f"{rows} of {M} rows x {passes} passes over all {len(layers)} layers "
                              f"({el:.1f} s, weights prepared beforehand)"}

@@ -66,7 +66,7 @@ typedef enum wq_status {
     WQ_ERR_TIMEOUT = -5        /* a kernel gave up waiting on one of its barriers         */
 } wq_status;
 
-enum { WQ_MODE_W4A4 = 0, WQ_MODE_W8A8 = 1 };
+enum { WQ_MODE_W4A4 = 0, WQ_MODE_W8A8 = 1, WQ_MODE_W8A8_FP8 = 2 };
 enum { WQ_SCALE_LAYOUT_ROWMAJOR = 0, WQ_SCALE_LAYOUT_MMA = 1 };
 /* Granularity of the activations' fp32 tensor scale g (4-bit layers):
  *   ROW     one g per row, from that row's amax at run time (FoldQuantVLA, Key Contribution 2:
@@ -88,7 +88,10 @@ enum { WQ_ORDER_SMOOTH_ROTATE = 0, WQ_ORDER_ROTATE_SMOOTH = 1 };
  * attention-output and FFN down projections kept at W8A8) in the same smoothed + rotated basis:
  * per-row activation scale a = amax / 127, per-output-column weight scale w = amax / 127,
  * q = round-half-even(v / scale) clamped to [-127, 127]; y = a[m] w[n] (sum_k qa qw) + b.
- * rank and n_outliers must be 0 in this mode. */
+ * mode = WQ_MODE_W8A8_FP8 is the same 8-bit path in e4m3 (QuantWAMs sec. 4.2 "Backend": the
+ * saliency-upgraded layers run FP8 W8A8 kernels): scales amax / 448, q = e4m3_rn_satfinite(v /
+ * scale) with the quotient one IEEE fp32 division; one byte per value in HBM and tcgen05
+ * kind::f8f6f4 MMAs.  rank and n_outliers must be 0 in both 8-bit modes. */
 typedef struct wq_config {
     int K;            /* input features (reduction dimension)                              */
     int N;            /* output features                                                   */
@@ -265,9 +268,10 @@ WQ_API wq_status wq_linear_forward_chain(wq_weights_t h, wq_weights_t next, cons
                                          size_t workspace_bytes, void *stream);
 
 /*
- * The selective 8-bit projection (handle prepared with mode WQ_MODE_W8A8): the 8-bit variant of
- * the fused quantiser, then the tcgen05 GEMM on the int8 codes (held as exact bf16 integers,
- * kind::f16, fp32 accumulation) with the epilogue y = a[m] w[n] acc + b.
+ * The selective 8-bit projection (handle prepared with mode WQ_MODE_W8A8 or WQ_MODE_W8A8_FP8): the
+ * 8-bit variant of the fused quantiser, then the tcgen05 GEMM -- on the int8 codes held as exact
+ * bf16 integers (kind::f16), or on e4m3 bytes (kind::f8f6f4) -- with fp32 accumulation and the
+ * epilogue y = a[m] w[n] acc + b.
  *   x, y, workspace  as for wq_linear_forward (workspace: wq_workspace_bytes(h, M)).
  */
 WQ_API wq_status wq_linear_forward_w8a8(wq_weights_t h, const void *x, int M, void *y,
@@ -275,12 +279,14 @@ WQ_API wq_status wq_linear_forward_w8a8(wq_weights_t h, const void *x, int M, vo
 
 /*
  * The 8-bit quantiser alone (W8A8 handles), device outputs:
- *   codes  bf16 [M, K] holding the integers q in [-127, 127];  scale fp32 [M] (a = amax / 127).
+ *   codes  WQ_MODE_W8A8: bf16 [M, K] holding the integers q in [-127, 127] (scale a = amax / 127);
+ *          WQ_MODE_W8A8_FP8: e4m3 bytes [M, K] (scale a = amax / 448).   scale fp32 [M].
  */
 WQ_API wq_status wq_quantize_activations_w8a8(wq_weights_t h, const void *x, int M, void *codes,
                                               float *scale, void *stream);
 
-/* W8A8 weights back to host (synchronous): q int8 [N, K] (K-major), w fp32 [N]. */
+/* 8-bit weights back to host (synchronous): q [N, K] bytes (K-major; int8 values, or e4m3 codes for
+ * WQ_MODE_W8A8_FP8), w fp32 [N]. */
 WQ_API wq_status wq_export_weights_w8a8(wq_weights_t h, int8_t *q, float *w);
 
 /*

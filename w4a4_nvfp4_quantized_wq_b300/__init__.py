@@ -18,7 +18,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libwq.so")
 
 WQ_OK, WQ_ERR_INVALID, WQ_ERR_UNSUPPORTED, WQ_ERR_CUDA, WQ_ERR_OOM, WQ_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
-WQ_MODE_W4A4, WQ_MODE_W8A8 = 0, 1
+WQ_MODE_W4A4, WQ_MODE_W8A8, WQ_MODE_W8A8_FP8 = 0, 1, 2
 WQ_SCALE_LAYOUT_ROWMAJOR, WQ_SCALE_LAYOUT_MMA = 0, 1
 WQ_PATH_TWO_KERNEL, WQ_PATH_FUSED = 0, 1
 WQ_GEMM_SINGLE, WQ_GEMM_SPLITK, WQ_GEMM_WIDE = 0, 1, 2
@@ -422,10 +422,12 @@ def wq_linear_forward_w8a8(w: Weights, x, y=None, workspace=None, stream=None):
 
 
 def wq_quantize_activations_w8a8(w: Weights, x, stream=None):
-    """8-bit quantiser alone: (codes bf16 [M, K] holding integers, scale fp32 [M]) on the device."""
+    """8-bit quantiser alone: (codes, scale fp32 [M]) on the device; codes are bf16 [M, K] holding
+    integers (WQ_MODE_W8A8) or e4m3 bytes uint8 [M, K] (WQ_MODE_W8A8_FP8)."""
     import torch
     M, K = x.shape
-    codes = torch.empty((M, K), dtype=torch.bfloat16, device=x.device)
+    fp8 = w.cfg.mode == WQ_MODE_W8A8_FP8
+    codes = torch.empty((M, K), dtype=torch.uint8 if fp8 else torch.bfloat16, device=x.device)
     scale = torch.empty(M, dtype=torch.float32, device=x.device)
     _check(lib().wq_quantize_activations_w8a8(ctypes.c_void_p(w.handle), ctypes.c_void_p(x.data_ptr()), M,
                                               ctypes.c_void_p(codes.data_ptr()), ctypes.c_void_p(scale.data_ptr()),
@@ -434,7 +436,8 @@ def wq_quantize_activations_w8a8(w: Weights, x, stream=None):
 
 
 def wq_export_weights_w8a8(w: Weights):
-    q = np.zeros((w.N, w.K), np.int8)
+    """(q [N, K], w [N]): int8 values, or e4m3 codes as uint8 for WQ_MODE_W8A8_FP8."""
+    q = np.zeros((w.N, w.K), np.uint8 if w.cfg.mode == WQ_MODE_W8A8_FP8 else np.int8)
     sc = np.zeros(w.N, np.float32)
     _check(lib().wq_export_weights_w8a8(ctypes.c_void_p(w.handle), q.ctypes.data_as(ctypes.c_void_p),
                                         sc.ctypes.data_as(ctypes.c_void_p)))

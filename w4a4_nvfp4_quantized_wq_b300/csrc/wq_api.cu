@@ -251,9 +251,11 @@ wq_status check_config(const wq_config* c) {
     if (!c) return fail(WQ_ERR_INVALID, "cfg is NULL");
     if (c->K <= 0 || c->N <= 0 || c->rank < 0 || c->n_outliers < 0)
         return fail(WQ_ERR_INVALID, "negative or zero size in cfg");
-    if (c->mode != WQ_MODE_W4A4 && c->mode != WQ_MODE_W8A8) return fail(WQ_ERR_INVALID, "unknown mode");
-    if (c->mode == WQ_MODE_W8A8 && (c->rank != 0 || c->n_outliers != 0))
-        return fail(WQ_ERR_UNSUPPORTED, "WQ_MODE_W8A8 takes rank 0 and no outlier channels");
+    if (c->mode != WQ_MODE_W4A4 && c->mode != WQ_MODE_W8A8 && c->mode != WQ_MODE_W8A8_FP8)
+        return fail(WQ_ERR_INVALID, "unknown mode");
+    const bool eight = c->mode != WQ_MODE_W4A4;
+    if (eight && (c->rank != 0 || c->n_outliers != 0))
+        return fail(WQ_ERR_UNSUPPORTED, "the 8-bit modes take rank 0 and no outlier channels");
     if (c->rotate != 0 && c->rotate != 1) return fail(WQ_ERR_INVALID, "rotate must be 0 or 1");
     if (c->K % 64 || c->K > 16384) return fail(WQ_ERR_UNSUPPORTED, "K must be a multiple of 64 and <= 16384");
     if (c->N % 16) return fail(WQ_ERR_UNSUPPORTED, "N must be a multiple of 16");
@@ -261,14 +263,14 @@ wq_status check_config(const wq_config* c) {
     if (c->n_outliers > 64 || c->n_outliers > c->K) return fail(WQ_ERR_UNSUPPORTED, "n_outliers must be <= 64 and <= K");
     if (c->act_scale != WQ_ACT_SCALE_ROW && c->act_scale != WQ_ACT_SCALE_TENSOR && c->act_scale != WQ_ACT_SCALE_STATIC)
         return fail(WQ_ERR_INVALID, "unknown act_scale");
-    if (c->mode == WQ_MODE_W8A8 && c->act_scale != WQ_ACT_SCALE_ROW)
-        return fail(WQ_ERR_UNSUPPORTED, "WQ_MODE_W8A8 takes WQ_ACT_SCALE_ROW");
+    if (eight && c->act_scale != WQ_ACT_SCALE_ROW)
+        return fail(WQ_ERR_UNSUPPORTED, "the 8-bit modes take WQ_ACT_SCALE_ROW");
     if (c->act_scale == WQ_ACT_SCALE_STATIC && !(c->act_gscale > 0.0f && std::isfinite(c->act_gscale)))
         return fail(WQ_ERR_INVALID, "WQ_ACT_SCALE_STATIC needs a finite act_gscale > 0");
     if (c->transform_order != WQ_ORDER_SMOOTH_ROTATE && c->transform_order != WQ_ORDER_ROTATE_SMOOTH)
         return fail(WQ_ERR_INVALID, "unknown transform_order");
-    if (c->mode == WQ_MODE_W8A8 && c->transform_order != WQ_ORDER_SMOOTH_ROTATE)
-        return fail(WQ_ERR_UNSUPPORTED, "WQ_MODE_W8A8 takes WQ_ORDER_SMOOTH_ROTATE");
+    if (eight && c->transform_order != WQ_ORDER_SMOOTH_ROTATE)
+        return fail(WQ_ERR_UNSUPPORTED, "the 8-bit modes take WQ_ORDER_SMOOTH_ROTATE");
     return WQ_OK;
 }
 
@@ -432,16 +434,27 @@ WQ_API wq_status wq_prepare_weights(const wq_config* cfg, const float* W, const 
         }
     }
 
-    if (cfg->mode == WQ_MODE_W8A8) {
-        // ---- symmetric int8 per output column (kept as exact bf16 integers, K-major)
-        std::vector<uint16_t> q8(static_cast<size_t>(N) * K);
+    if (cfg->mode == WQ_MODE_W8A8 || cfg->mode == WQ_MODE_W8A8_FP8) {
+        // ---- symmetric 8-bit per output column, K-major: int8 values kept as exact bf16 integers,
+        // or e4m3 bytes (scale amax / 448, code e4m3_rn_satfinite(RN(v / scale)))
+        const bool f8 = cfg->mode == WQ_MODE_W8A8_FP8;
+        std::vector<uint16_t> q8(f8 ? 0 : static_cast<size_t>(N) * K);
+        std::vector<uint8_t> e8(f8 ? static_cast<size_t>(N) * K : 0);
         std::vector<float> wsc(N);
         parallel_for(static_cast<size_t>(N), [&](size_t n) {
             float am = 0.0f;
             for (int k = 0; k < K; ++k) am = std::max(am, std::fabs(Rp[static_cast<size_t>(k) * N + n]));
-            const float sc = am / 127.0f;
+            const float sc = am / (f8 ? 448.0f : 127.0f);
             wsc[n] = sc;
             for (int k = 0; k < K; ++k) {
+                if (f8) {
+                    uint8_t c = 0;
+                    if (sc != 0.0f)
+                        c = static_cast<uint8_t>(__nv_cvt_float_to_fp8(Rp[static_cast<size_t>(k) * N + n] / sc,
+                                                                       __NV_SATFINITE, __NV_E4M3));
+                    e8[n * K + k] = c;
+                    continue;
+                }
                 float r = 0.0f;
                 if (sc != 0.0f) r = std::nearbyint(Rp[static_cast<size_t>(k) * N + n] / sc);
                 r = std::min(127.0f, std::max(-127.0f, r));
@@ -458,7 +471,11 @@ WQ_API wq_status wq_prepare_weights(const wq_config* cfg, const float* W, const 
         cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
         std::vector<float> bias_f(N, 0.0f);
         if (bias) std::copy(bias, bias + N, bias_f.begin());
-        if ((st = upload(&h->d_codes, q8.data(), q8.size() * 2, cs)) != WQ_OK) return bail(st);
+        if (f8) {
+            if ((st = upload(&h->d_codes, e8.data(), e8.size(), cs)) != WQ_OK) return bail(st);
+        } else if ((st = upload(&h->d_codes, q8.data(), q8.size() * 2, cs)) != WQ_OK) {
+            return bail(st);
+        }
         if ((st = upload(&h->d_colscale, wsc.data(), N * 4, cs)) != WQ_OK) return bail(st);
         if (bias && (st = upload(&h->d_bias, bias_f.data(), N * 4, cs)) != WQ_OK) return bail(st);
         if (s && (st = upload(&h->d_inv_s, inv_s_pairs.data(), K * 4, cs)) != WQ_OK) return bail(st);
@@ -466,9 +483,11 @@ WQ_API wq_status wq_prepare_weights(const wq_config* cfg, const float* W, const 
         if (cudaMemsetAsync(h->d_err, 0, sizeof(int), cs) != cudaSuccess) return bail(fail(WQ_ERR_CUDA, "memset"));
         if (cudaStreamSynchronize(cs) != cudaSuccess) return bail(fail(WQ_ERR_CUDA, "upload synchronise failed"));
         const char* why = "";
-        if (!wq::encode_tmap_2d(&h->tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h->d_codes, K, N, 2ull * K, 64, 128,
-                                CU_TENSOR_MAP_SWIZZLE_128B, &why))
-            return bail(fail(WQ_ERR_CUDA, why));
+        const bool okm = f8 ? wq::encode_tmap_2d(&h->tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, h->d_codes, K, N, K, 128, 128,
+                                                 CU_TENSOR_MAP_SWIZZLE_128B, &why)
+                            : wq::encode_tmap_2d(&h->tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h->d_codes, K, N, 2ull * K,
+                                                 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, &why);
+        if (!okm) return bail(fail(WQ_ERR_CUDA, why));
         *out = h;
         return WQ_OK;
     }
@@ -553,13 +572,17 @@ WQ_API wq_status wq_prepare_weights(const wq_config* cfg, const float* W, const 
     return WQ_OK;
 }
 
-static size_t w8_workspace_bytes(int M, int K) {
-    return align_up(static_cast<size_t>(M) * K * 2, 1024) + align_up(static_cast<size_t>(M) * 4, 1024);
+// 8-bit codes [M, K] (bf16-held int8: 2 bytes, e4m3: 1 byte) and the row scales
+static size_t w8_code_bytes(wq_weights_t h, int M) {
+    return static_cast<size_t>(M) * h->cfg.K * (h->cfg.mode == WQ_MODE_W8A8_FP8 ? 1 : 2);
+}
+static size_t w8_workspace_bytes(wq_weights_t h, int M) {
+    return align_up(w8_code_bytes(h, M), 1024) + align_up(static_cast<size_t>(M) * 4, 1024);
 }
 
 WQ_API size_t wq_workspace_bytes(wq_weights_t h, int M) {
     if (!h || M < 0) return 0;
-    if (h->cfg.mode == WQ_MODE_W8A8) return w8_workspace_bytes(M, h->cfg.K);
+    if (h->cfg.mode != WQ_MODE_W4A4) return w8_workspace_bytes(h, M);
     return wq::carve_workspace(nullptr, M, h->cfg.K, h->r_pad, h->no_pad).bytes;
 }
 
@@ -654,7 +677,8 @@ static wq_status run_quant(wq_weights_t h, const void* x, int M, int layout, uin
     qa.sf_layout = layout;
     qa.g = g;
     qa.num_sms = h->num_sms;
-    qa.int8 = h->cfg.mode == WQ_MODE_W8A8;
+    qa.int8 = h->cfg.mode != WQ_MODE_W4A4;
+    qa.fp8 = h->cfg.mode == WQ_MODE_W8A8_FP8;
     const cudaError_t e = wq::launch_quantize_act(qa, st);
     if (e != cudaSuccess) return cuda_fail(e, "activation quantiser launch");
     return WQ_OK;
@@ -686,11 +710,13 @@ static wq_status run_gemm(wq_weights_t h, const uint8_t* codes, const uint8_t* s
     std::lock_guard<std::mutex> lk(h->mu);
     if (h->key_codes != codes || h->key_u != u || h->key_xo != xo || h->key_y != y || h->key_M != M) {
         const char* why = "";
-        const bool w8 = h->cfg.mode == WQ_MODE_W8A8;
+        const bool w8 = h->cfg.mode == WQ_MODE_W8A8, f8 = h->cfg.mode == WQ_MODE_W8A8_FP8;
         bool ok = (w8 ? wq::encode_tmap_2d(&h->tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, codes, K, M, 2ull * K, 64, 128,
                                            CU_TENSOR_MAP_SWIZZLE_128B, &why)
-                      : wq::encode_tmap_2d(&h->tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, K / 2, M, K / 2, 128, 128,
-                                           CU_TENSOR_MAP_SWIZZLE_128B, &why)) &&
+                      : f8 ? wq::encode_tmap_2d(&h->tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, K, M, K, 128, 128,
+                                                CU_TENSOR_MAP_SWIZZLE_128B, &why)
+                           : wq::encode_tmap_2d(&h->tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, K / 2, M, K / 2, 128, 128,
+                                                CU_TENSOR_MAP_SWIZZLE_128B, &why)) &&
                   wq::encode_tmap_2d(&h->tmY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, y, N, M, 2ull * N, 64, 32,
                                      CU_TENSOR_MAP_SWIZZLE_128B, &why);
         if (ok && r)
@@ -717,7 +743,8 @@ static wq_status run_gemm(wq_weights_t h, const uint8_t* codes, const uint8_t* s
     ga.sfa = sf; ga.sfb = h->d_sf; ga.gA = g; ga.gW = h->gW; ga.bias = h->d_bias;
     ga.err = h->d_err; ga.num_sms = h->num_sms;
     ga.y = y;
-    ga.w8 = h->cfg.mode == WQ_MODE_W8A8;
+    ga.w8 = h->cfg.mode != WQ_MODE_W4A4;
+    ga.fp8 = h->cfg.mode == WQ_MODE_W8A8_FP8;
     ga.colscale = h->d_colscale;
     ga.force_split = wq::tune(wq::kTuneGemmSplit);     // 0: choose (tests and tuning pin it)
     ga.chain = chain;
@@ -748,7 +775,8 @@ WQ_API int wq_gemm_schedule(wq_weights_t h, int M) {
     if (M < 0) return fail(WQ_ERR_INVALID, "M < 0");
     wq::GemmArgs ga{};
     ga.M = M > 0 ? M : 1; ga.N = h->cfg.N; ga.K = h->cfg.K; ga.r = h->r_pad; ga.n_out = h->no_pad;
-    ga.w8 = h->cfg.mode == WQ_MODE_W8A8;
+    ga.w8 = h->cfg.mode != WQ_MODE_W4A4;
+    ga.fp8 = h->cfg.mode == WQ_MODE_W8A8_FP8;
     ga.num_sms = h->num_sms;
     ga.force_split = wq::tune(wq::kTuneGemmSplit);
     const int s = wq::gemm_schedule(ga);
@@ -852,7 +880,7 @@ WQ_API wq_status wq_linear_forward_quantized(wq_weights_t h, const uint8_t* code
     if (!h) return fail(WQ_ERR_INVALID, "NULL handle");
     if (M < 0) return fail(WQ_ERR_INVALID, "M < 0");
     if (M == 0) return WQ_OK;
-    const bool w8 = h->cfg.mode == WQ_MODE_W8A8;
+    const bool w8 = h->cfg.mode != WQ_MODE_W4A4;
     if (!codes || (!scales_mma && !w8) || !gscale || !y) return fail(WQ_ERR_INVALID, "NULL buffer");
     if (h->cfg.rank > 0 && !u) return fail(WQ_ERR_INVALID, "u is required when rank > 0");
     if (h->cfg.n_outliers > 0 && !x_omega) return fail(WQ_ERR_INVALID, "x_omega is required when n_outliers > 0");
@@ -867,7 +895,7 @@ WQ_API wq_status wq_linear_forward_quantized(wq_weights_t h, const uint8_t* code
 WQ_API wq_status wq_linear_forward_w8a8(wq_weights_t h, const void* x, int M, void* y, void* workspace,
                                         size_t workspace_bytes, void* stream) {
     if (!h) return fail(WQ_ERR_INVALID, "NULL handle");
-    if (h->cfg.mode != WQ_MODE_W8A8) return fail(WQ_ERR_INVALID, "handle was not prepared with WQ_MODE_W8A8");
+    if (h->cfg.mode == WQ_MODE_W4A4) return fail(WQ_ERR_INVALID, "handle was not prepared with an 8-bit mode");
     if (M < 0) return fail(WQ_ERR_INVALID, "M < 0");
     if (M == 0) return WQ_OK;
     if (!x || !y || !workspace) return fail(WQ_ERR_INVALID, "NULL buffer");
@@ -875,10 +903,9 @@ WQ_API wq_status wq_linear_forward_w8a8(wq_weights_t h, const void* x, int M, vo
         return fail(WQ_ERR_INVALID, "x and y must be 16-byte aligned");
     if (reinterpret_cast<uintptr_t>(workspace) & 255) return fail(WQ_ERR_INVALID, "workspace must be 256-byte aligned");
     if (const wq_status d = check_device(h)) return d;
-    const int K = h->cfg.K;
-    if (workspace_bytes < w8_workspace_bytes(M, K)) return fail(WQ_ERR_INVALID, "workspace too small");
+    if (workspace_bytes < w8_workspace_bytes(h, M)) return fail(WQ_ERR_INVALID, "workspace too small");
     uint8_t* codes = static_cast<uint8_t*>(workspace);
-    float* a = reinterpret_cast<float*>(codes + align_up(static_cast<size_t>(M) * K * 2, 1024));
+    float* a = reinterpret_cast<float*>(codes + align_up(w8_code_bytes(h, M), 1024));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     wq_status s = run_quant(h, x, M, WQ_SCALE_LAYOUT_ROWMAJOR, codes, nullptr, a, nullptr, nullptr, nullptr, st);
     if (s != WQ_OK) return s;
@@ -888,7 +915,7 @@ WQ_API wq_status wq_linear_forward_w8a8(wq_weights_t h, const void* x, int M, vo
 WQ_API wq_status wq_quantize_activations_w8a8(wq_weights_t h, const void* x, int M, void* codes, float* scale,
                                               void* stream) {
     if (!h) return fail(WQ_ERR_INVALID, "NULL handle");
-    if (h->cfg.mode != WQ_MODE_W8A8) return fail(WQ_ERR_INVALID, "handle was not prepared with WQ_MODE_W8A8");
+    if (h->cfg.mode == WQ_MODE_W4A4) return fail(WQ_ERR_INVALID, "handle was not prepared with an 8-bit mode");
     if (M < 0) return fail(WQ_ERR_INVALID, "M < 0");
     if (M == 0) return WQ_OK;
     if (!x || !codes || !scale) return fail(WQ_ERR_INVALID, "NULL buffer");
@@ -901,9 +928,11 @@ WQ_API wq_status wq_quantize_activations_w8a8(wq_weights_t h, const void* x, int
 
 WQ_API wq_status wq_export_weights_w8a8(wq_weights_t h, int8_t* q, float* w) {
     if (!h) return fail(WQ_ERR_INVALID, "NULL handle");
-    if (h->cfg.mode != WQ_MODE_W8A8) return fail(WQ_ERR_INVALID, "handle was not prepared with WQ_MODE_W8A8");
+    if (h->cfg.mode == WQ_MODE_W4A4) return fail(WQ_ERR_INVALID, "handle was not prepared with an 8-bit mode");
     const int K = h->cfg.K, N = h->cfg.N;
-    if (q) {
+    if (q && h->cfg.mode == WQ_MODE_W8A8_FP8) {
+        WQ_CUDA(cudaMemcpy(q, h->d_codes, static_cast<size_t>(N) * K, cudaMemcpyDeviceToHost), "export");
+    } else if (q) {
         std::vector<uint16_t> b(static_cast<size_t>(N) * K);
         WQ_CUDA(cudaMemcpy(b.data(), h->d_codes, b.size() * 2, cudaMemcpyDeviceToHost), "export");
         for (size_t i = 0; i < b.size(); ++i)
@@ -1022,7 +1051,7 @@ WQ_API wq_status wq_linear_forward_host(wq_weights_t h, const void* x_host, int 
     void* dy = base + wsb + align_up(xb, 1024);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     WQ_CUDA(cudaMemcpyAsync(dx, x_host, xb, cudaMemcpyHostToDevice, st), "x upload");
-    const wq_status s = h->cfg.mode == WQ_MODE_W8A8 ? wq_linear_forward_w8a8(h, dx, M, dy, workspace, wsb, stream)
+    const wq_status s = h->cfg.mode != WQ_MODE_W4A4 ? wq_linear_forward_w8a8(h, dx, M, dy, workspace, wsb, stream)
                                                     : wq_linear_forward(h, dx, M, dy, workspace, wsb, stream);
     if (s != WQ_OK) return s;
     WQ_CUDA(cudaMemcpyAsync(y_host, dy, yb, cudaMemcpyDeviceToHost, st), "y download");

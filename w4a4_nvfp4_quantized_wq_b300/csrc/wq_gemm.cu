@@ -95,6 +95,7 @@ struct KParams {
     const float* bias;
     const float* colscale;           // per-output-column scale (8-bit layers) or null
     int* err;
+    int fp8;                         // 8-bit layer with e4m3 values (kind::f8f6f4, 128 K per stage)
 };
 
 __host__ __device__ constexpr uint32_t stage_bytes(bool w8) { return w8 ? 2 * kTileBytes : kStageBytes; }
@@ -165,9 +166,9 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     const int n_tiles = (N + 127) / 128;
     const int tiles = ((M + 127) / 128) * n_tiles;
     constexpr uint32_t kSB = stage_bytes(kW8);
-    constexpr int kStageX = kW8 ? 64 : 128;           // TMA x extent of a stage (elements)
+    const int kStageX = (kW8 && !p.fp8) ? 64 : 128;   // TMA x extent of a stage (elements)
     const int num_kb = p.K / 64;
-    const int num_kt = kW8 ? num_kb : (num_kb + 3) / 4;
+    const int num_kt = kW8 ? (p.fp8 ? (num_kb + 1) / 2 : num_kb) : (num_kb + 3) / 4;
     const bool split = p.split > 1;
     const uint32_t rank = split ? cluster_ctarank() : 0u;
     const int tile_first = split ? static_cast<int>(blockIdx.x) / p.split : static_cast<int>(blockIdx.x);
@@ -304,6 +305,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             const uint32_t idesc_fp4 = (1u << 7) | (1u << 10) | mn;          // e2m1 x e2m1, ue4m3 scales
             const uint32_t idesc_bf16 = (1u << 4) | (1u << 7) | (1u << 10) | mn;  // bf16 x bf16 -> f32
             const uint32_t idesc_f16 = (1u << 4) | mn;                         // f16 x f16 -> f32
+            const uint32_t idesc_f8 = (1u << 4) | mn;                          // e4m3 x e4m3 -> f32
             int stage = 0;
             uint32_t ph = 0, sph = 0;
             int tl = 0;
@@ -332,7 +334,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     // (TMA-filled stages need no tcgen05 fence: the mbarrier completion orders them)
                     if (!mbar_wait(bar_full + 8u * stage, ph, abort_flag, p.err, 5)) { ok = false; break; }
                     if (tl == 0 && kt == kt_lo) WQ_TRACE_AT(4);
-                    const int nkb = kW8 ? 4 : min(4, num_kb - kt * 4);
+                    const int nkb = kW8 ? (p.fp8 ? min(4, (p.K - kt * 128) / 32) : 4) : min(4, num_kb - kt * 4);
                     const uint32_t sA = base + static_cast<uint32_t>(stage) * kSB;
                     const uint32_t sf_t = tmem + p.sf_col + 32u * stage;
                     if (kt == kt_lo) copy_scales(stage, kt);
@@ -340,7 +342,9 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     const uint64_t bd = smem_desc(sA + kTileBytes, 16, 1024, 2);
                     for (int kb = 0; kb < nkb; ++kb) {
                         const uint32_t accum = (kt != kt_lo || kb != 0) ? 1u : 0u;
-                        if (kW8)
+                        if (kW8 && p.fp8)
+                            mma_f8(d_acc, ad + 2u * kb, bd + 2u * kb, idesc_f8, accum);
+                        else if (kW8)
                             mma_f16(d_acc, ad + 2u * kb, bd + 2u * kb, idesc_bf16, accum);
                         else
                             mma_nvf4(d_acc, ad + 2u * kb, bd + 2u * kb, idesc_fp4, sf_t + 4u * kb,
@@ -646,7 +650,7 @@ Plan gemm_plan(const GemmArgs& a) {
 template <bool kW8>
 int gemm_split(const GemmArgs& a, const Plan& pl) {
     const int tiles = ((a.M + 127) / 128) * ((a.N + 127) / 128);
-    const int num_kt = kW8 ? a.K / 64 : (a.K / 64 + 3) / 4;
+    const int num_kt = kW8 ? (a.fp8 ? (a.K / 64 + 1) / 2 : a.K / 64) : (a.K / 64 + 3) / 4;
     return a.force_split > 0 ? a.force_split : choose_split<kW8>(tiles, num_kt, a.num_sms, pl.total);
 }
 
@@ -657,7 +661,7 @@ cudaError_t launch_gemm_t(const GemmArgs& a, cudaStream_t st) {
     const cudaError_t ea = gemm_attributes<kW8>();
     if (ea != cudaSuccess) return ea;
     const int tiles = ((a.M + 127) / 128) * ((a.N + 127) / 128);
-    const int num_kt = kW8 ? a.K / 64 : (a.K / 64 + 3) / 4;
+    const int num_kt = kW8 ? (a.fp8 ? (a.K / 64 + 1) / 2 : a.K / 64) : (a.K / 64 + 3) / 4;
     const int split = gemm_split<kW8>(a, pl);
     if (split > num_kt || split > 16 || (split & (split - 1))) return cudaErrorInvalidValue;
     // split-K push form: the receive slots (per rows x split senders x 512 B) go in ring stages
@@ -681,6 +685,7 @@ cudaError_t launch_gemm_t(const GemmArgs& a, cudaStream_t st) {
     kp.off_bar = pl.off_bar; kp.sf_col = pl.sf_col;
     kp.sfa = a.sfa; kp.sfb = a.sfb; kp.gA = a.gA; kp.gW = a.gW; kp.bias = a.bias; kp.colscale = a.colscale;
     kp.err = a.err;
+    kp.fp8 = a.fp8 ? 1 : 0;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(split > 1 ? tiles * split : (tiles < a.num_sms ? tiles : a.num_sms)));
     cfg.blockDim = dim3(kThreads);

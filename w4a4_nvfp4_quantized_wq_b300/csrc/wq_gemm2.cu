@@ -84,6 +84,7 @@ struct WParams {
     int* err;
     int chain;               // 1: quantise the tile for the next layer instead of storing y
     ChainArgs ch;
+    int fp8;                 // 8-bit layer with e4m3 values (kind::f8f6f4, 128 K per stage)
 };
 
 __host__ __device__ constexpr uint32_t stage_bytes(bool w8) { return w8 ? kStage8 : kStage4; }
@@ -274,10 +275,11 @@ wide_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     const uint32_t sA = base + s * SB, fb = bar_full + 8u * s;
                     if (kt < num_kt) {
                         if (kW8) {
+                            const int x0 = kt * (p.fp8 ? 128 : 64);     // 128-byte rows either way
                             mbar_arrive_expect_tx(fb, 2 * kHalf);
-                            tma_load_2d(sA + kHalf, &tmB, kt * 64, nrow, fb);
+                            tma_load_2d(sA + kHalf, &tmB, x0, nrow, fb);
                             if (!dep) { griddep_wait(); dep = true; }
-                            tma_load_2d(sA, &tmA, kt * 64, mrow, fb);
+                            tma_load_2d(sA, &tmA, x0, mrow, fb);
                         } else {
                             const int kb0 = kt * 4, nkb = min(4, p.num_kb - kb0);
                             mbar_arrive_expect_tx(fb, 2 * kHalf + 3u * nkb * kSfAtom);
@@ -360,6 +362,7 @@ wide_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             const uint32_t idesc_fp4 = (1u << 7) | (1u << 10) | mn;
             const uint32_t idesc_bf16 = (1u << 4) | (1u << 7) | (1u << 10) | mn;
             const uint32_t idesc_f16 = (1u << 4) | mn;
+            const uint32_t idesc_f8 = (1u << 4) | mn;                        // e4m3 x e4m3 -> f32
             uint32_t q = 0;
             int tl = 0;
             bool ok = true;
@@ -384,7 +387,11 @@ wide_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     // (TMA-filled stages need no tcgen05 fence: the mbarrier completion orders them)
                     const uint32_t sA = base + s * SB;
                     const uint64_t ad = smem_desc(sA, 16, 1024, 2), bd = smem_desc(sA + kHalf, 16, 1024, 2);
-                    if (kW8) {
+                    if (kW8 && p.fp8) {
+                        const int nmma = min(4, (p.K - kt * 128) / 32);
+                        for (int kb = 0; kb < nmma; ++kb)
+                            mma_f8_pair(tmem, ad + 2u * kb, bd + 2u * kb, idesc_f8, (kt | kb) != 0 ? 1u : 0u);
+                    } else if (kW8) {
 #pragma unroll
                         for (int kb = 0; kb < 4; ++kb)
                             mma_f16_pair(tmem, ad + 2u * kb, bd + 2u * kb, idesc_bf16, (kt | kb) != 0 ? 1u : 0u);
@@ -607,7 +614,8 @@ cudaError_t launch_gemm_wide(const GemmArgs& a, cudaStream_t st) {
     WParams p{};
     p.M = a.M; p.N = a.N; p.K = a.K; p.r = a.r; p.n_out = a.n_out; p.stages = S;
     p.num_kb = a.K / 64;
-    p.num_kt = w8 ? a.K / 64 : (p.num_kb + 3) / 4;
+    p.num_kt = w8 ? (a.fp8 ? (p.num_kb + 1) / 2 : a.K / 64) : (p.num_kb + 3) / 4;
+    p.fp8 = a.fp8 ? 1 : 0;
     p.nrb_a = (a.M + 127) / 128;
     p.nrb_b = (a.N + 127) / 128;
     p.off_y = static_cast<uint32_t>(S) * SB;

@@ -69,6 +69,7 @@ struct QuantArgs {
     float* g;                       // [M]
     int num_sms;                    // used to spread small batches over more CTAs
     bool int8 = false;              // 8-bit layer: codes are int8 values stored as bf16 [M, K]
+    bool fp8 = false;               // with int8: e4m3 bytes [M, K] instead, scale amax / 448
     // Activation tensor scale: WQ_ACT_SCALE_ROW (one per row, from the row), WQ_ACT_SCALE_TENSOR
     // (one for all M rows: a first launch takes the maximum, a second quantises) or
     // WQ_ACT_SCALE_STATIC (the calibrated `static_g`, one pass).  Every mode writes g[m] per row.
@@ -114,7 +115,8 @@ struct GemmArgs {
     int num_sms;
     void* y;                  // bf16 [M, N] (written directly by the split-K reduction)
     int force_split;          // 0: choose; otherwise CTAs per tile (power of two <= 16)
-    bool w8 = false;          // 8-bit layer: A/W are int8 codes stored as bf16 [., K]
+    bool w8 = false;          // 8-bit layer: A/W are int8 codes stored as bf16 [., K] (or e4m3, fp8)
+    bool fp8 = false;         // 8-bit layer with e4m3 bytes [., K] (kind::f8f6f4)
     const float* colscale = nullptr;  // 8-bit layer: per-output-column scale [N]
     const ChainArgs* chain = nullptr; // non-null: quantise the output for the next layer (pair schedule)
 };

@@ -109,6 +109,7 @@ struct QParams {
     int phase;
     float static_g;
     unsigned int* amax_bits;
+    int fp8;            // 8-bit layer in e4m3 (scale amax / 448, bytes [M, K]) instead of int8
 };
 
 // Zero the x_O columns beyond the kept channels for the rows of one tile (they meet zero weight
@@ -181,6 +182,50 @@ __device__ __forceinline__ void emit_int8(const f2 (&P)[16], float gsc, float ra
             pkw[e] = *reinterpret_cast<const uint32_t*>(&h);
         }
         if (row_ok) dst[j] = make_uint4(pkw[0], pkw[1], pkw[2], pkw[3]);
+    }
+}
+
+// e4m3 codes of this lane's half row of block kb (QuantWAMs sec. 4.2: FP8 W8A8 for the upgraded
+// layers): q = e4m3_rn_satfinite(RN(v / a)) with ra = RN(1 / a); the quotient's conversion is
+// bracketed as for the e2m1 codes (both ends of t (1 -+ 2^-21), t = RN(v ra), converting to the same
+// code prove it; otherwise the exact division).  Bytes in natural channel order.
+__device__ __forceinline__ uint32_t e4m3_pair_q(float a0, float a1, float sc, float ra) {
+    const float t0 = __fmul_rn(a0, ra), t1 = __fmul_rn(a1, ra);
+    uint16_t lo, hi;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(__fmul_rn(t1, 0.99999952316284180f)),
+        "f"(__fmul_rn(t0, 0.99999952316284180f)));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(__fmul_rn(t1, 1.00000047683715820f)),
+        "f"(__fmul_rn(t0, 1.00000047683715820f)));
+    if (lo == hi && ra < 3.0e38f) return lo;
+    uint16_t ex;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(ex) : "f"(__fdiv_rn(a1, sc)), "f"(__fdiv_rn(a0, sc)));
+    return ex;
+}
+__device__ __forceinline__ void emit_fp8(const f2 (&P)[16], float gsc, float ra, int row, bool row_ok, int kb,
+                                         int half, const QParams& p) {
+    // byte c of the half at position c: channels 0..15 are the pairs' first lanes, 16..31 the second
+    uint32_t bytes[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        // word q holds channels 4q .. 4q+3 of the half: 0..15 from the pairs' lows, 16..31 from highs
+        const int c0 = 4 * q;
+        float v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int c = c0 + e;
+            v[e] = c < 16 ? lo2(P[c]) : hi2(P[c - 16]);
+        }
+        uint32_t word = 0u;
+        if (gsc != 0.0f) {
+            const uint32_t p01 = e4m3_pair_q(v[0], v[1], gsc, ra), p23 = e4m3_pair_q(v[2], v[3], gsc, ra);
+            word = (p01 & 0xFFFFu) | (p23 << 16);
+        }
+        bytes[q] = word;
+    }
+    if (row_ok) {
+        uint4* dst = reinterpret_cast<uint4*>(p.codes + static_cast<size_t>(row) * p.K + kb * 64 + 32 * half);
+        dst[0] = make_uint4(bytes[0], bytes[1], bytes[2], bytes[3]);
+        dst[1] = make_uint4(bytes[4], bytes[5], bytes[6], bytes[7]);
     }
 }
 
@@ -375,7 +420,7 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmX, const QParams p) {
             }
         }
     }
-    const float gsc = __fdiv_rn(amax, kInt8 ? 127.0f : 2688.0f);
+    const float gsc = __fdiv_rn(amax, kInt8 ? (p.fp8 ? 448.0f : 127.0f) : 2688.0f);
     const float rg_inv = __frcp_rn(gsc);
     if (rank == 0 && warp == 0 && half == 0 && row_ok) p.g[row] = gsc;
     if (threadIdx.x == 0) WQ_QTRACE_AT(4);
@@ -392,7 +437,8 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmX, const QParams p) {
             P[2 * j + 1] = pk2(t.z, t.w);
         }
         if constexpr (kInt8) {
-            emit_int8<true>(P, gsc, rg_inv, row, row_ok, kb_lo + i, half, p);
+            if (p.fp8) emit_fp8(P, gsc, rg_inv, row, row_ok, kb_lo + i, half, p);
+            else emit_int8<true>(P, gsc, rg_inv, row, row_ok, kb_lo + i, half, p);
         } else {
             const float2 bm = ld_shared_v2f(slot + kMaxOff + static_cast<uint32_t>(r) * 16u + 8u * half);
             emit_nvfp4<true>(P, bm.x, bm.y, gsc, rg_inv, row, row_ok, kb_lo + i, half, p);
@@ -587,7 +633,7 @@ quantize_stream_kernel(const __grid_constant__ CUtensorMap tmX, const QParams p)
             zero_xo_pad(p, tile, threadIdx.x, kConsumerWarps * 32);
             named_bar_sync(1, kConsumerWarps * 32);        // maxima and partials are free again
             if (p.phase == 0) {
-                gsc = __fdiv_rn(amax, kInt8 ? 127.0f : 2688.0f);
+                gsc = __fdiv_rn(amax, kInt8 ? (p.fp8 ? 448.0f : 127.0f) : 2688.0f);
                 rg_inv = __frcp_rn(gsc);
             }
             cta_amax = fmaxf(cta_amax, amax);
@@ -613,7 +659,8 @@ quantize_stream_kernel(const __grid_constant__ CUtensorMap tmX, const QParams p)
                 const uint32_t m0 = p.n_out ? s_omega[4 * kb] : 0u, m1 = p.n_out ? s_omega[4 * kb + 1] : 0u;
                 if ((half ? m1 : m0) != 0u) apply_keep(P, half ? m1 : m0);
                 if constexpr (kInt8) {
-                    emit_int8<false>(P, gsc, rg_inv, row, row_ok, kb, half, p);
+                    if (p.fp8) emit_fp8(P, gsc, rg_inv, row, row_ok, kb, half, p);
+                    else emit_int8<false>(P, gsc, rg_inv, row, row_ok, kb, half, p);
                 } else {
                     float ma, mb;
                     absmax_pairs(P, ma, mb);
@@ -741,6 +788,7 @@ cudaError_t launch_quantize_act(const QuantArgs& a, cudaStream_t st) {
     qp.phase = a.act_scale == WQ_ACT_SCALE_STATIC ? 3 : 0;
     qp.static_g = a.static_g;
     qp.amax_bits = a.amax_bits;
+    qp.fp8 = a.fp8 ? 1 : 0;
     qp.pfrag = a.pfrag; qp.u = a.u; qp.codes = a.codes; qp.sf = a.sf; qp.sf_layout = a.sf_layout; qp.g = a.g;
     qp.err = a.err;
     if (a.int8)
