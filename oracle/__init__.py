@@ -76,6 +76,8 @@ def lib() -> ctypes.CDLL:
             L.orc_linear_forward_w8a8.restype = i32
             L.orc_set_smooth_after.argtypes = [i32]
             L.orc_set_smooth_after.restype = None
+            L.orc_pooled_energy.argtypes = [P, i64, i64, P, i32, P]; L.orc_pooled_energy.restype = i32
+            L.orc_topk_channels.argtypes = [P, i64, i32, P]; L.orc_topk_channels.restype = i32
             L.orc_e4m3s_encode.argtypes = [f32]; L.orc_e4m3s_encode.restype = ctypes.c_uint8
             L.orc_e4m3s_decode.argtypes = [ctypes.c_uint8]; L.orc_e4m3s_decode.restype = ctypes.c_double
             L.orc_quantize_act_fp8.argtypes = [P, i64, i64, P, i32, P, P, i32]
@@ -386,6 +388,31 @@ def reference_forward_w8a8(layer, n_threads: int = 0, rows=None):
     wq8 = prepare_weights_int8(layer.W, layer.s, layer.rotate, n_threads)
     aq = quantize_act_int8(x_bits, layer.s, layer.rotate, n_threads)
     return linear_forward_w8a8(aq, wq8, layer.bias, n_threads), aq, wq8
+
+
+# ------------------------------------------------------------------ outlier calibration
+def pooled_energy(x_bits, s, rotate: bool, smooth_after: bool = False) -> np.ndarray:
+    """z(c) = mean_t xt[t, c]^2 of the quantiser's transform (QuantWAMs sec. 3.1 Eq. (1)-(3),
+    one context)."""
+    x_bits = _c(x_bits, np.uint16)
+    M, K = x_bits.shape
+    inv_s = inv_smoothing(s)
+    z = np.zeros(K, np.float64)
+    with transform_order(smooth_after):
+        rc = lib().orc_pooled_energy(_p(x_bits), M, K, _p(inv_s), int(rotate), _p(z))
+    if rc:
+        raise ValueError(f"orc_pooled_energy failed: {rc}")
+    return z
+
+
+def topk_channels(z: np.ndarray, n: int) -> np.ndarray:
+    """The n channels of largest z, ties to the lower index, ascending (QuantWAMs Eq. (3) Top-K)."""
+    z = _c(z, np.float64)
+    om = np.zeros(n, np.int32)
+    rc = lib().orc_topk_channels(_p(z), z.size, int(n), _p(om))
+    if rc:
+        raise ValueError(f"orc_topk_channels failed: {rc}")
+    return om
 
 
 # ------------------------------------------------------------------ W8A8 in FP8

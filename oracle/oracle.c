@@ -730,6 +730,46 @@ int orc_linear_forward_fp8(const uint8_t *qa, const float *a, long M, const uint
     return 0;
 }
 
+/* ------------------------------------------------------------------ outlier calibration */
+/* QuantWAMs sec. 3.1 Eq. (1)-(3): the pooled squared energy of each channel of the transformed
+ * activation, z(c) = mean_t xt[t, c]^2 (one context, pi = 1), and the Top-K channels by z, which
+ * stay in 16-bit.  xt is the quantiser's own transform of each row (fp32, the same steps and
+ * order as orc_act_transform_row); each square and the sum over rows are taken in fp64, rows in
+ * ascending order.  Ties in z go to the lower channel index; the selected set is returned in
+ * ascending channel order. */
+int orc_pooled_energy(const uint16_t *x_bf16, long M, long K, const float *inv_s, int rotate, double *z)
+{
+    float *xt = (float *)malloc(sizeof(float) * (size_t)K);
+    if (!xt) return -4;
+    for (long k = 0; k < K; ++k) z[k] = 0.0;
+    for (long m = 0; m < M; ++m) {
+        orc_act_transform_row(x_bf16 + m * K, K, inv_s, rotate, xt);
+        for (long k = 0; k < K; ++k) z[k] += (double)xt[k] * (double)xt[k];
+    }
+    for (long k = 0; k < K; ++k) z[k] = M > 0 ? z[k] / (double)M : 0.0;
+    free(xt);
+    return 0;
+}
+
+/* The n channels with the largest z (ties: lower index first), ascending. */
+int orc_topk_channels(const double *z, long K, int n, int32_t *omega)
+{
+    if (n < 0 || n > K) return -1;
+    char *taken = (char *)calloc((size_t)K, 1);
+    if (!taken) return -4;
+    for (int j = 0; j < n; ++j) {
+        long best = -1;
+        for (long k = 0; k < K; ++k)
+            if (!taken[k] && (best < 0 || z[k] > z[best])) best = k;   /* strict: the lower index wins ties */
+        taken[best] = 1;
+    }
+    int j = 0;
+    for (long k = 0; k < K; ++k)
+        if (taken[k]) omega[j++] = (int32_t)k;
+    free(taken);
+    return 0;
+}
+
 /* ------------------------------------------------------------------ Conv3d */
 /* NVFP4 execution of the video VAE's 3x3x3 convolutions (LatentQuant, Abstract).  Plainest
  * reading: the input tensor is quantised once, per voxel along channels (16-channel blocks)

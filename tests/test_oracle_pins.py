@@ -683,3 +683,42 @@ def test_fp8_w8a8_plain_case_reduces_to_matmul_and_beats_w4a4():
     e8 = np.linalg.norm(y8 - ref) / np.linalg.norm(ref)
     e4 = np.linalg.norm(y4 - ref) / np.linalg.norm(ref)
     assert e8 < 0.05 and e8 < e4, (e8, e4)
+
+
+# ------------------------------------------------------------------ outlier calibration
+@pytest.mark.parametrize("after", [False, True])
+def test_pooled_energy_against_dense_transform(after):
+    """z(c) = mean_t xt[t,c]^2 (QuantWAMs sec. 3.1 Eq. (1)-(3), one context): on integer rows with
+    power-of-two smoothing the fp32 transform is exact, so z equals numpy's fp64 mean of the dense
+    Sylvester product squared (up to fp64 summation); random rows within 1e-6 of it."""
+    rng = np.random.default_rng(81)
+    M, K = 37, 192
+    x = rng.integers(-300, 300, (M, K)).astype(np.float32)
+    bits = wlmod.bf16_bits(x)
+    s = (2.0 ** rng.integers(-2, 3, K)).astype(np.float32)
+    H = hadamard(64).astype(np.float64) / 8.0
+    xf = wlmod.bf16_from_bits(bits).astype(np.float64)
+    inv = 1.0 / s.astype(np.float64)
+    if after:
+        xt = (xf.reshape(M, 3, 64) @ H).reshape(M, K) * inv
+    else:
+        xt = ((xf * inv).reshape(M, 3, 64) @ H).reshape(M, K)
+    want = (xt * xt).mean(axis=0)
+    got = oracle.pooled_energy(bits, s, True, after)
+    np.testing.assert_allclose(got, want, rtol=1e-14)
+    L = wlmod.make_layer_inputs("video_dit", M=64, K=256, N=16, rank=0, n_omega=0)
+    sm = L.s
+    xs = wlmod.bf16_from_bits(L.x_bits).astype(np.float64) / sm.astype(np.float64)
+    xt = (xs.reshape(64, 4, 64) @ H).reshape(64, 256)
+    np.testing.assert_allclose(oracle.pooled_energy(L.x_bits, sm, True), (xt * xt).mean(axis=0), rtol=1e-6)
+
+
+def test_topk_channels_ties_and_order():
+    z = np.array([1.0, 5.0, 3.0, 5.0, 0.5, 3.0, 7.0, 5.0])
+    assert oracle.topk_channels(z, 3).tolist() == [1, 3, 6]         # 7, then the two lowest 5s
+    assert oracle.topk_channels(z, 5).tolist() == [1, 2, 3, 6, 7]
+    assert oracle.topk_channels(z, 0).tolist() == []
+    rng = np.random.default_rng(82)
+    z = rng.standard_normal(1000) ** 2
+    want = np.sort(np.lexsort((np.arange(1000), -z))[:41])
+    assert np.array_equal(oracle.topk_channels(z, 41), want)
