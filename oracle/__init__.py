@@ -80,12 +80,14 @@ def lib() -> ctypes.CDLL:
             L.orc_topk_channels.argtypes = [P, i64, i32, P]; L.orc_topk_channels.restype = i32
             L.orc_e4m3s_encode.argtypes = [f32]; L.orc_e4m3s_encode.restype = ctypes.c_uint8
             L.orc_e4m3s_decode.argtypes = [ctypes.c_uint8]; L.orc_e4m3s_decode.restype = ctypes.c_double
-            L.orc_quantize_act_fp8.argtypes = [P, i64, i64, P, i32, P, P, i32]
+            L.orc_quantize_act_fp8.argtypes = [P, i64, i64, P, i32, P, i32, P, P, P, i32]
             L.orc_quantize_act_fp8.restype = i32
             L.orc_quantize_weights_fp8.argtypes = [P, i64, i64, P, P]
             L.orc_quantize_weights_fp8.restype = i32
             L.orc_linear_forward_fp8.argtypes = [P, P, i64, P, P, i64, i64, P, P, i32]
             L.orc_linear_forward_fp8.restype = i32
+            L.orc_linear_forward_w4a8.argtypes = [P, P, i64, P, P, f32, i64, i64, P, P, i32, P, P, i32, P, P, i32]
+            L.orc_linear_forward_w4a8.restype = i32
             _lib = L
     return _lib
 
@@ -420,20 +422,25 @@ def topk_channels(z: np.ndarray, n: int) -> np.ndarray:
 class Fp8Quant:
     q: np.ndarray            # uint8 e4m3 codes [rows, K]
     scale: np.ndarray        # fp32 [rows]
+    x_omega: Optional[np.ndarray] = None   # fp16 bits [rows, n_omega] (kept channels)
 
 
-def quantize_act_fp8(x_bits, s, rotate, n_threads: int = 0) -> Fp8Quant:
+def quantize_act_fp8(x_bits, s, rotate, n_threads: int = 0, omega=None) -> Fp8Quant:
     """Per-token e4m3 of the transformed activations (QuantWAMs sec. 4.2: FP8 W8A8 for the
-    upgraded layers), scale = amax / 448."""
+    upgraded layers; A8 at the protected steps), scale = amax / 448; kept channels (omega) go to
+    fp16 and are zeroed first."""
     x_bits = _c(x_bits, np.uint16)
     M, K = x_bits.shape
     inv_s = inv_smoothing(s)
+    omega = np.zeros(0, np.int32) if omega is None else _c(omega, np.int32)
+    xo = np.zeros((M, omega.size), np.uint16)
     q = np.zeros((M, K), np.uint8)
     a = np.zeros(M, np.float32)
-    rc = lib().orc_quantize_act_fp8(_p(x_bits), M, K, _p(inv_s), int(rotate), _p(q), _p(a), int(n_threads))
+    rc = lib().orc_quantize_act_fp8(_p(x_bits), M, K, _p(inv_s), int(rotate), _p(omega), int(omega.size), _p(xo),
+                                    _p(q), _p(a), int(n_threads))
     if rc:
         raise ValueError(f"orc_quantize_act_fp8 failed: {rc}")
-    return Fp8Quant(q, a)
+    return Fp8Quant(q, a, xo)
 
 
 def prepare_weights_fp8(W, s, rotate, n_threads: int = 0) -> Fp8Quant:
@@ -461,6 +468,29 @@ def reference_forward_fp8(layer, n_threads: int = 0, rows=None):
     wq8 = prepare_weights_fp8(layer.W, layer.s, layer.rotate, n_threads)
     aq = quantize_act_fp8(x_bits, layer.s, layer.rotate, n_threads)
     return linear_forward_fp8(aq, wq8, layer.bias, n_threads), aq, wq8
+
+
+def reference_forward_w4a8(layer, n_threads: int = 0, rows=None):
+    """A W4 layer at an A8-protected step (QuantWAMs sec. 4.2, sec. 5): its NVFP4 weights, low-rank
+    branch and kept channels, its activations in e4m3 per token.  Returns (y fp64, Fp8Quant,
+    WeightQuant, U)."""
+    x_bits = layer.x_bits if rows is None else layer.x_bits[rows]
+    with transform_order(getattr(layer, "smooth_after", False)):
+        wq = prepare_weights(layer.W, layer.s, layer.L1, layer.L2, layer.omega, layer.rotate, n_threads)
+        aq = quantize_act_fp8(x_bits, layer.s, layer.rotate, n_threads, omega=layer.omega)
+    U = lowrank_act(x_bits, wq.P) if wq.P.shape[1] else np.zeros((x_bits.shape[0], 0), np.uint16)
+    M, K = aq.q.shape
+    N = wq.codes.shape[0]
+    r = wq.P.shape[1]
+    no = wq.W_omega.shape[0]
+    y = np.zeros((M, N), np.float64)
+    bias = _c(layer.bias, np.float32)
+    rc = lib().orc_linear_forward_w4a8(_p(aq.q), _p(aq.scale), M, _p(wq.codes), _p(wq.scales), np.float32(wq.gW), N,
+                                       K, _p(_c(U, np.uint16)), _p(wq.Q), r, _p(aq.x_omega), _p(wq.W_omega), no,
+                                       _p(bias), _p(y), int(n_threads))
+    if rc:
+        raise ValueError(f"orc_linear_forward_w4a8 failed: {rc}")
+    return y, aq, wq, U
 
 
 # ------------------------------------------------------------------ Conv3d (VAE)

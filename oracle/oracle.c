@@ -657,8 +657,11 @@ static uint8_t fp8_code(float v, float scale)
     return orc_e4m3s_encode(v / scale);
 }
 
-/* x bf16 [M, K] -> q e4m3 [M, K], a fp32 [M] (smoothing and rotation as for W4A4). */
+/* x bf16 [M, K] -> q e4m3 [M, K], a fp32 [M] (smoothing and rotation as for W4A4).  The
+ * channels in omega (n_omega of them, nullable when 0) go to x_omega fp16 [M, n_omega] and are
+ * zeroed before the row maximum, as in the 4-bit quantiser. */
 int orc_quantize_act_fp8(const uint16_t *x_bf16, long M, long K, const float *inv_s, int rotate,
+                         const int32_t *omega, int n_omega, uint16_t *x_omega,
                          uint8_t *q, float *a, int n_threads)
 {
     if (K % 16 || (rotate && K % 64)) return -1;
@@ -678,6 +681,10 @@ int orc_quantize_act_fp8(const uint16_t *x_bf16, long M, long K, const float *in
 #pragma omp for schedule(static)
             for (long m = 0; m < M; ++m) {
                 orc_act_transform_row(x_bf16 + m * K, K, inv_s, rotate, xt);
+                for (int j = 0; j < n_omega; ++j) {
+                    x_omega[m * n_omega + j] = orc_f16_from_f32(xt[omega[j]]);
+                    xt[omega[j]] = 0.0f;
+                }
                 float amax = 0.0f;
                 for (long k = 0; k < K; ++k) {
                     float v = fabsf(xt[k]);
@@ -727,6 +734,45 @@ int orc_linear_forward_fp8(const uint8_t *qa, const float *a, long M, const uint
             if (bias) v += (double)bias[n];
             y[m * N + n] = v;
         }
+    return 0;
+}
+
+/* ------------------------------------------------------------------ W4A8 */
+/* A8-protected steps (QuantWAMs sec. 4.2 and sec. 5: one of ten Fast-WAM action steps, two of twenty
+ * and six of fifty LingBot-VA steps run their activations at 8 bits).  Reading: the 4-bit layer keeps
+ * its NVFP4 weights, low-rank branch and fp16 kept channels; its activations are quantised to e4m3
+ * per token (orc_quantize_act_fp8, with the kept-channel split).  fp64:
+ *   y[m][n] = a[m] gW sum_k dec8(qa[m][k]) deqW[n][k] + sum_j U Q + sum_c x_O W_O + b. */
+int orc_linear_forward_w4a8(const uint8_t *qa, const float *a, long M, const uint8_t *codesW,
+                            const uint8_t *scalesW, float gW, long N, long K, const uint16_t *U, const uint16_t *Q,
+                            int r, const uint16_t *x_omega, const uint16_t *W_omega, int n_omega,
+                            const float *bias, double *y, int n_threads)
+{
+    double *deqW = (double *)malloc(sizeof(double) * (size_t)N * (size_t)K);
+    if (!deqW) return -4;
+#ifdef _OPENMP
+    if (n_threads > 0) omp_set_num_threads(n_threads);
+#else
+    (void)n_threads;
+#endif
+#pragma omp parallel for schedule(static)
+    for (long n = 0; n < N; ++n)
+        for (long k = 0; k < K; ++k)
+            deqW[n * K + k] = nvfp4_elem(codesW + n * (K / 2), scalesW + n * (K / 16), k);
+#pragma omp parallel for schedule(static)
+    for (long m = 0; m < M; ++m)
+        for (long n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (long k = 0; k < K; ++k) acc += orc_e4m3s_decode(qa[m * K + k]) * deqW[n * K + k];
+            double v = acc * (double)a[m] * (double)gW;
+            for (int j = 0; j < r; ++j)
+                v += (double)orc_f32_from_bf16(U[m * r + j]) * (double)orc_f32_from_bf16(Q[(long)j * N + n]);
+            for (int c = 0; c < n_omega; ++c)
+                v += (double)orc_f32_from_f16(x_omega[m * n_omega + c]) * (double)orc_f32_from_f16(W_omega[(long)c * N + n]);
+            if (bias) v += (double)bias[n];
+            y[m * N + n] = v;
+        }
+    free(deqW);
     return 0;
 }
 

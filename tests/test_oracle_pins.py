@@ -722,3 +722,26 @@ def test_topk_channels_ties_and_order():
     z = rng.standard_normal(1000) ** 2
     want = np.sort(np.lexsort((np.arange(1000), -z))[:41])
     assert np.array_equal(oracle.topk_channels(z, 41), want)
+
+
+# ------------------------------------------------------------------ W4A8 (A8-protected steps)
+def test_w4a8_reduces_to_dequantised_matmul_and_sits_between_w4a4_and_fp8():
+    """s = 1, no rotation, no branches: the W4A8 forward equals (dec(qa) a)(deq(W) gW)^T + b from
+    numpy with torch decoding the e4m3 codes; with branches and transforms its error lies below the
+    W4A4 error (8-bit activations) on the same 4-bit weights; kept channels leave the e4m3 codes at 0."""
+    L = wlmod.make_layer_inputs("expert", M=9, K=256, N=48, rank=0, n_omega=0, smooth=False, rotate=False)
+    y, aq, wq, _ = oracle.reference_forward_w4a8(L)
+    dec = torch.from_numpy(aq.q).view(torch.float8_e4m3fn).double().numpy()
+    B = _dequant(wq.codes, wq.scales, 256) * np.float64(wq.gW)
+    ref = (dec * aq.scale[:, None].astype(np.float64)) @ B.T + L.bias
+    np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+    L = wlmod.make_layer_inputs("video_dit", M=48, K=512, N=128, rank=16, n_omega=16)
+    y8, a8, *_ = oracle.reference_forward_w4a8(L)
+    y4, *_ = oracle.reference_forward(L)
+    ref = L.x_f32.astype(np.float64) @ L.W.astype(np.float64) + L.bias
+    e8 = np.linalg.norm(y8 - ref) / np.linalg.norm(ref)
+    e4 = np.linalg.norm(y4 - ref) / np.linalg.norm(ref)
+    assert e8 < e4, (e8, e4)
+    assert not a8.q[:, L.omega].any()
+    aq4 = oracle.quantize_act(L.x_bits, L.s, True, L.omega)
+    assert np.array_equal(a8.x_omega, aq4.x_omega)            # the same fp16 kept channels
