@@ -66,7 +66,7 @@ typedef enum wq_status {
     WQ_ERR_TIMEOUT = -5        /* a kernel gave up waiting on one of its barriers         */
 } wq_status;
 
-enum { WQ_MODE_W4A4 = 0, WQ_MODE_W8A8 = 1, WQ_MODE_W8A8_FP8 = 2 };
+enum { WQ_MODE_W4A4 = 0, WQ_MODE_W8A8 = 1, WQ_MODE_W8A8_FP8 = 2, WQ_MODE_W4A8 = 3 };
 enum { WQ_SCALE_LAYOUT_ROWMAJOR = 0, WQ_SCALE_LAYOUT_MMA = 1 };
 /* Granularity of the activations' fp32 tensor scale g (4-bit layers):
  *   ROW     one g per row, from that row's amax at run time (FoldQuantVLA, Key Contribution 2:
@@ -91,7 +91,16 @@ enum { WQ_ORDER_SMOOTH_ROTATE = 0, WQ_ORDER_ROTATE_SMOOTH = 1 };
  * mode = WQ_MODE_W8A8_FP8 is the same 8-bit path in e4m3 (QuantWAMs sec. 4.2 "Backend": the
  * saliency-upgraded layers run FP8 W8A8 kernels): scales amax / 448, q = e4m3_rn_satfinite(v /
  * scale) with the quotient one IEEE fp32 division; one byte per value in HBM and tcgen05
- * kind::f8f6f4 MMAs.  rank and n_outliers must be 0 in both 8-bit modes. */
+ * kind::f8f6f4 MMAs.  rank and n_outliers must be 0 in both 8-bit modes.
+ * mode = WQ_MODE_W4A8 is a 4-bit layer at an A8-protected step (QuantWAMs sec. 4.2 and sec. 5: one
+ * of ten Fast-WAM action-denoising steps, 2/20 and 6/50 LingBot-VA steps keep 8-bit activations):
+ * the same folded NVFP4 weights, low-rank branch and fp16 kept channels as WQ_MODE_W4A4 (same
+ * options, rank and n_outliers allowed, act_scale WQ_ACT_SCALE_ROW), activations in e4m3 per token
+ * (scale amax / 448 after the kept-channel split).  The tensor cores take both operands in bf16,
+ * which holds every e4m3 value and every NVFP4 value dec(code) dec(scale) exactly (no tensor kind
+ * multiplies e4m3 by e2m1 under NVFP4's e4m3-per-16 weight scales), so the handle stores the
+ * weight values expanded to bf16 [N, K] next to the NVFP4 codes, and wq_linear_forward writes the
+ * activation values as bf16 [M, K] (wq_workspace_bytes covers them). */
 typedef struct wq_config {
     int K;            /* input features (reduction dimension)                              */
     int N;            /* output features                                                   */
@@ -211,7 +220,9 @@ WQ_API wq_status wq_linear_forward_host(wq_weights_t h, const void *x_host, int 
 /*
  * Run only the activation quantiser (for parity checks and for callers that keep the
  * quantised activations).  All outputs are device pointers:
- *   codes   uint8 [M, K/2]; element 2i of a row in the low nibble of byte i.
+ *   codes   uint8 [M, K/2]; element 2i of a row in the low nibble of byte i.  WQ_MODE_W4A8 handles:
+ *           the e4m3 activation values as bf16 [M, K] instead (scales unused, may be NULL; gscale
+ *           the per-row scale amax / 448).
  *   scales  e4m3 bytes: WQ_SCALE_LAYOUT_ROWMAJOR -> [M, K/16];
  *           WQ_SCALE_LAYOUT_MMA -> ceil(M/128) x (K/64) atoms of 512 bytes, atom (mb, kb)
  *           at offset (mb * K/64 + kb) * 512, row r of the 128-row block and 16-block j of
@@ -376,6 +387,26 @@ WQ_API wq_status wq_selftest_wait_timeout(int *site, double *waited_ms, int *rel
  */
 WQ_API wq_status wq_mma_peak(int kind, int n, int pair, int copies, int copy_shape, int iters, int feeder,
                              int zero_data, int accs, double *tflops, double *ns_per_mma, double *sm_mhz);
+
+/*
+ * On-device outlier calibration (QuantWAMs sec. 3.1, Eq. (1)-(3), one context): the pooled squared
+ * energy of each channel of the transformed activation, z(c) = mean_t xt[t, c]^2, where xt is the
+ * activation quantiser's transform of each row (the smoothing 1/s before or after the block-64
+ * Walsh-Hadamard rotation, per transform_order; fp32 steps, fp64 squares and sums), and the Top-K
+ * channels by z -- the Omega that wq_prepare_weights takes for the fp16 exception path.
+ *   x        device bf16 [M, K] calibration activations (M >= 1; K % 64 == 0, K <= 16384).
+ *   s        device fp32 [K] smoothing factors (> 0) or NULL for s = 1.
+ *   rotate   1: block-64 FWHT; 0: none.   transform_order: WQ_ORDER_*.
+ *   n_top    0 <= n_top <= K channels to select.
+ *   z        device fp64 [K], out.   omega  device int32 [n_top], out: ascending channel indices,
+ *            the n_top largest z (ties go to the lower index).
+ *   workspace  device, wq_calibration_workspace_bytes(M, K) bytes, 256-byte aligned.
+ * Four kernels on `stream`.  Returns WQ_ERR_INVALID / WQ_ERR_UNSUPPORTED on bad arguments.
+ */
+WQ_API size_t wq_calibration_workspace_bytes(int M, int K);
+WQ_API wq_status wq_calibrate_outliers(const void *x, int M, int K, const float *s, int rotate, int transform_order,
+                                       int n_top, double *z, int32_t *omega, void *workspace,
+                                       size_t workspace_bytes, void *stream);
 
 /* Release the handle and its device memory (synchronises the device first).  NULL is a no-op. */
 WQ_API void wq_free_weights(wq_weights_t h);

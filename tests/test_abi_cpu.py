@@ -46,7 +46,8 @@ def _cfg(K=256, N=128, r=0, no=0, rot=1, mode=0, act=0, g=0.0, order=0):
     (dict(K=64, no=64, r=0), None),                      # accepted shape (checked below to succeed)
     (dict(mode=1, r=16), wq.WQ_ERR_UNSUPPORTED),
     (dict(mode=1, act=1), wq.WQ_ERR_UNSUPPORTED),
-    (dict(mode=3), wq.WQ_ERR_INVALID),
+    (dict(mode=4), wq.WQ_ERR_INVALID),
+    (dict(mode=3, act=1), wq.WQ_ERR_UNSUPPORTED),
     (dict(mode=2, r=16), wq.WQ_ERR_UNSUPPORTED),
     (dict(mode=2, order=1), wq.WQ_ERR_UNSUPPORTED),
     (dict(rot=2), wq.WQ_ERR_INVALID),

@@ -496,3 +496,35 @@ def test_side_strides_and_tuning_roundtrip():
     wq.wq_set_tuning("WQ_GEMM_WIDE", old)
     with pytest.raises(wq.WqError):
         wq.wq_set_tuning("WQ_NO_SUCH_KNOB", 1)
+
+
+# ------------------------------------------------------------------ W4A8 (A8-protected steps)
+W4A8_CASES = ["expert_small", "dit_r32_o64_ragged_n", "top2pct_o41_r24", "multi_tile_kstage_tail",
+              "rot_smooth_r32_o16", "min_k64_n16_m1"]
+
+
+@pytest.mark.parametrize("case", W4A8_CASES)
+@pytest.mark.parametrize("wide", ["0", "1"])
+def test_w4a8_protected_step(case, wide, tuning):
+    """QuantWAMs sec. 4.2 / sec. 5: a 4-bit layer at an A8-protected step.  e4m3 activation codes
+    (read back as their bf16 values), row scales and fp16 kept channels bit-exact against the
+    oracle; NVFP4 weight codes and scales bit-exact; y within tolerance on both GEMM schedules."""
+    tuning("WQ_GEMM_WIDE", wide)
+    L = layer(case)
+    w = prep(L, mode=wq.WQ_MODE_W4A8)
+    ex = wq.wq_export_weights(w)
+    o = ow(L)
+    assert np.array_equal(ex["codes"], o.codes) and np.array_equal(ex["scales"], o.scales)
+    x = x_dev(L.x_bits)
+    codes, _, g, xo, u = wq.wq_quantize_activations(w, x)
+    y = wq.wq_linear_forward(w, x)
+    torch.cuda.synchronize()
+    wq.wq_check_device_error(w)
+    y_ref, aq, _, _ = oracle.reference_forward_w4a8(L)
+    dec = torch.from_numpy(aq.q).view(torch.float8_e4m3fn).float().to(torch.bfloat16)
+    assert torch.equal(codes.cpu().view(torch.int16), dec.view(torch.int16))
+    assert np.array_equal(g.cpu().numpy(), aq.scale)
+    if L.omega.size:
+        got, pad = side_out(xo, L.omega.size)
+        assert np.array_equal(got, aq.x_omega) and not pad.any()
+    assert_y_close(L, y, y_ref)

@@ -18,7 +18,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libwq.so")
 
 WQ_OK, WQ_ERR_INVALID, WQ_ERR_UNSUPPORTED, WQ_ERR_CUDA, WQ_ERR_OOM, WQ_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
-WQ_MODE_W4A4, WQ_MODE_W8A8, WQ_MODE_W8A8_FP8 = 0, 1, 2
+WQ_MODE_W4A4, WQ_MODE_W8A8, WQ_MODE_W8A8_FP8, WQ_MODE_W4A8 = 0, 1, 2, 3
 WQ_SCALE_LAYOUT_ROWMAJOR, WQ_SCALE_LAYOUT_MMA = 0, 1
 WQ_PATH_TWO_KERNEL, WQ_PATH_FUSED = 0, 1
 WQ_GEMM_SINGLE, WQ_GEMM_SPLITK, WQ_GEMM_WIDE = 0, 1, 2
@@ -34,7 +34,7 @@ EXPORTED = ["wq_prepare_weights", "wq_get_config", "wq_workspace_bytes", "wq_lin
             "wq_export_weights", "wq_check_device_error", "wq_free_weights", "wq_last_error",
             "wq_forward_path", "wq_selftest_wait_timeout", "wq_gemm_schedule",
             "wq_quant_schedule", "wq_side_strides", "wq_set_tuning", "wq_get_tuning", "wq_mma_peak",
-            "wq_linear_forward_chain"]
+            "wq_linear_forward_chain", "wq_calibration_workspace_bytes", "wq_calibrate_outliers"]
 
 
 class WqError(RuntimeError):
@@ -116,6 +116,10 @@ def lib() -> ctypes.CDLL:
         D = ctypes.POINTER(ctypes.c_double)
         L.wq_mma_peak.argtypes = [I, I, I, I, I, I, I, I, I, D, D, D]
         L.wq_mma_peak.restype = I
+        L.wq_calibration_workspace_bytes.argtypes = [I, I]
+        L.wq_calibration_workspace_bytes.restype = S
+        L.wq_calibrate_outliers.argtypes = [P, I, I, P, I, I, I, P, P, P, S, P]
+        L.wq_calibrate_outliers.restype = I
         L.wq_free_weights.argtypes = [P]
         L.wq_free_weights.restype = None
         L.wq_last_error.argtypes = []
@@ -267,7 +271,10 @@ def wq_quantize_activations(w: Weights, x, scale_layout: int = WQ_SCALE_LAYOUT_R
     import torch
     M, K = x.shape
     dev = x.device
-    codes = torch.empty((M, K // 2), dtype=torch.uint8, device=dev)
+    if w.cfg.mode == WQ_MODE_W4A8:
+        codes = torch.empty((M, K), dtype=torch.bfloat16, device=dev)      # e4m3 values held as bf16
+    else:
+        codes = torch.empty((M, K // 2), dtype=torch.uint8, device=dev)
     if scale_layout == WQ_SCALE_LAYOUT_MMA:
         scales = torch.zeros(((M + 127) // 128) * (K // 64) * 512, dtype=torch.uint8, device=dev)
     else:
@@ -384,6 +391,25 @@ def wq_mma_peak(kind: str = "fp4", n: int = 256, pair: bool = False, copies: int
     _check(lib().wq_mma_peak(MMA_KIND[kind], n, int(bool(pair)), copies, copy_shape, iters, feeder,
                              int(bool(zero_data)), accs, ctypes.byref(t), ctypes.byref(ns), ctypes.byref(mhz)))
     return t.value, ns.value, mhz.value
+
+
+def wq_calibrate_outliers(x, s=None, rotate: bool = True, transform_order: int = WQ_ORDER_SMOOTH_ROTATE,
+                          n_top: int = 0, stream=None):
+    """Pooled channel energy z(c) of the transformed calibration activations x (device bf16
+    [M, K]) and its Top-K channels: returns device tensors (z fp64 [K], omega int32 [n_top])."""
+    import torch
+    M, K = x.shape
+    dev = x.device
+    z = torch.empty(K, dtype=torch.float64, device=dev)
+    om = torch.empty(max(n_top, 1), dtype=torch.int32, device=dev)
+    s_t = None
+    if s is not None:
+        s_t = torch.as_tensor(np.asarray(s, np.float32)).to(dev)
+    ws = _alloc_workspace(int(lib().wq_calibration_workspace_bytes(M, K)), dev)
+    ptr = lambda t: ctypes.c_void_p(t.data_ptr() if t is not None else None)
+    _check(lib().wq_calibrate_outliers(ptr(x), M, K, ptr(s_t), int(bool(rotate)), int(transform_order), int(n_top),
+                                       ptr(z), ptr(om), ptr(ws), ws.numel(), ctypes.c_void_p(_stream_ptr(stream))))
+    return z, om[:n_top]
 
 
 def wq_check_device_error(w: Weights, stream=None):

@@ -221,6 +221,7 @@ struct wq_weights {
     uint16_t* d_WOt = nullptr;     // [N, n_out] fp16
     int* d_err = nullptr;
     float* d_colscale = nullptr;   // W8A8: per-output-column weight scale [N]
+    uint16_t* d_wexp = nullptr;    // W4A8: the NVFP4 weight values (code x block scale) as exact bf16 [N, K]
     int r_pad = 0;                 // stored rank: side_width(rank) (U, P, Q^T columns)
     int no_pad = 0;                // stored outlier width: side_width(n_outliers) (x_O, W_O^T columns)
     unsigned int* d_amax = nullptr;// WQ_ACT_SCALE_TENSOR: running batch maximum of wq_quantize_activations
@@ -251,9 +252,11 @@ wq_status check_config(const wq_config* c) {
     if (!c) return fail(WQ_ERR_INVALID, "cfg is NULL");
     if (c->K <= 0 || c->N <= 0 || c->rank < 0 || c->n_outliers < 0)
         return fail(WQ_ERR_INVALID, "negative or zero size in cfg");
-    if (c->mode != WQ_MODE_W4A4 && c->mode != WQ_MODE_W8A8 && c->mode != WQ_MODE_W8A8_FP8)
+    if (c->mode != WQ_MODE_W4A4 && c->mode != WQ_MODE_W8A8 && c->mode != WQ_MODE_W8A8_FP8 && c->mode != WQ_MODE_W4A8)
         return fail(WQ_ERR_INVALID, "unknown mode");
-    const bool eight = c->mode != WQ_MODE_W4A4;
+    const bool eight = c->mode == WQ_MODE_W8A8 || c->mode == WQ_MODE_W8A8_FP8;
+    if (c->mode == WQ_MODE_W4A8 && c->act_scale != WQ_ACT_SCALE_ROW)
+        return fail(WQ_ERR_UNSUPPORTED, "WQ_MODE_W4A8 takes WQ_ACT_SCALE_ROW");
     if (eight && (c->rank != 0 || c->n_outliers != 0))
         return fail(WQ_ERR_UNSUPPORTED, "the 8-bit modes take rank 0 and no outlier channels");
     if (c->rotate != 0 && c->rotate != 1) return fail(WQ_ERR_INVALID, "rotate must be 0 or 1");
@@ -287,6 +290,7 @@ void free_device(wq_weights* h) {
     cudaFree(h->d_err);
     cudaFree(h->d_colscale);
     cudaFree(h->d_amax);
+    cudaFree(h->d_wexp);
 }
 
 template <typename T>
@@ -568,6 +572,28 @@ WQ_API wq_status wq_prepare_weights(const wq_config* cfg, const float* W, const 
     if (no && !wq::encode_tmap_2d(&h->tmWO, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, h->d_WOt, nop, N, 2 * nop, nop, 128,
                                   swizzle_for_row_bytes(2 * nop), &why))
         return bail(fail(WQ_ERR_CUDA, why));
+    if (cfg->mode == WQ_MODE_W4A8) {
+        // A8 steps multiply the NVFP4 weights on the 16-bit tensor path: each value dec(code) dec(scale)
+        // has at most 6 significant bits and lies in [2^-10, 2688], so bf16 holds it exactly (gW stays
+        // in the epilogue)
+        std::vector<uint16_t> wexp(static_cast<size_t>(N) * K);
+        parallel_for(static_cast<size_t>(N), [&](size_t n) {
+            for (int k = 0; k < K; ++k) {
+                const uint32_t byte = codes[n * (K / 2) + k / 2];
+                const uint32_t c = (k & 1) ? (byte >> 4) : (byte & 15u);
+                const float mag[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
+                const size_t off = ((n / wq::kBlockM) * (K / 64) + k / 64) * wq::kSfAtom + (n % 32) * 16 +
+                                   ((n % wq::kBlockM) / 32) * 4 + (k % 64) / 16;
+                const float v = ((c & 8u) ? -mag[c & 7u] : mag[c & 7u]) * e4m3_value(sf_mma[off]);
+                wexp[n * K + k] = bf16_bits(v);
+            }
+        });
+        if ((st = upload(&h->d_wexp, wexp.data(), wexp.size() * 2, cs)) != WQ_OK) return bail(st);
+        if (cudaStreamSynchronize(cs) != cudaSuccess) return bail(fail(WQ_ERR_CUDA, "upload synchronise failed"));
+        if (!wq::encode_tmap_2d(&h->tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h->d_wexp, K, N, 2ull * K, 64, 128,
+                                CU_TENSOR_MAP_SWIZZLE_128B, &why))
+            return bail(fail(WQ_ERR_CUDA, why));
+    }
     *out = h;
     return WQ_OK;
 }
@@ -580,8 +606,15 @@ static size_t w8_workspace_bytes(wq_weights_t h, int M) {
     return align_up(w8_code_bytes(h, M), 1024) + align_up(static_cast<size_t>(M) * 4, 1024);
 }
 
+// W4A8: the e4m3 activation values as bf16 [M, K] in place of the fp4 codes (4 x their bytes: the
+// fp4-code region of a 4K-wide carve), the row scales, U, x_O and the batch-maximum word
+static wq::ActWorkspace carve_w4a8(void* base, int M, int K, int r, int no) {
+    return wq::carve_workspace(base, M, 4 * K, r, no);
+}
+
 WQ_API size_t wq_workspace_bytes(wq_weights_t h, int M) {
     if (!h || M < 0) return 0;
+    if (h->cfg.mode == WQ_MODE_W4A8) return carve_w4a8(nullptr, M, h->cfg.K, h->r_pad, h->no_pad).bytes;
     if (h->cfg.mode != WQ_MODE_W4A4) return w8_workspace_bytes(h, M);
     return wq::carve_workspace(nullptr, M, h->cfg.K, h->r_pad, h->no_pad).bytes;
 }
@@ -678,7 +711,8 @@ static wq_status run_quant(wq_weights_t h, const void* x, int M, int layout, uin
     qa.g = g;
     qa.num_sms = h->num_sms;
     qa.int8 = h->cfg.mode != WQ_MODE_W4A4;
-    qa.fp8 = h->cfg.mode == WQ_MODE_W8A8_FP8;
+    qa.fp8 = h->cfg.mode == WQ_MODE_W8A8_FP8 || h->cfg.mode == WQ_MODE_W4A8;
+    qa.fp8_bf16 = h->cfg.mode == WQ_MODE_W4A8;
     const cudaError_t e = wq::launch_quantize_act(qa, st);
     if (e != cudaSuccess) return cuda_fail(e, "activation quantiser launch");
     return WQ_OK;
@@ -689,8 +723,9 @@ WQ_API wq_status wq_quantize_activations(wq_weights_t h, const void* x, int M, i
     if (!h) return fail(WQ_ERR_INVALID, "NULL handle");
     if (M < 0) return fail(WQ_ERR_INVALID, "M < 0");
     if (M == 0) return WQ_OK;
-    if (!x || !codes || !scales || !gscale) return fail(WQ_ERR_INVALID, "NULL buffer");
-    if (h->cfg.mode != WQ_MODE_W4A4) return fail(WQ_ERR_INVALID, "W8A8 handle: use wq_quantize_activations_w8a8");
+    if (!x || !codes || (!scales && h->cfg.mode == WQ_MODE_W4A4) || !gscale) return fail(WQ_ERR_INVALID, "NULL buffer");
+    if (h->cfg.mode != WQ_MODE_W4A4 && h->cfg.mode != WQ_MODE_W4A8)
+        return fail(WQ_ERR_INVALID, "W8A8 handle: use wq_quantize_activations_w8a8");
     if (h->cfg.n_outliers > 0 && !x_omega)
         return fail(WQ_ERR_INVALID, "x_omega is required when n_outliers > 0 (the kept channels are zeroed)");
     if (scale_layout != WQ_SCALE_LAYOUT_ROWMAJOR && scale_layout != WQ_SCALE_LAYOUT_MMA)
@@ -710,7 +745,7 @@ static wq_status run_gemm(wq_weights_t h, const uint8_t* codes, const uint8_t* s
     std::lock_guard<std::mutex> lk(h->mu);
     if (h->key_codes != codes || h->key_u != u || h->key_xo != xo || h->key_y != y || h->key_M != M) {
         const char* why = "";
-        const bool w8 = h->cfg.mode == WQ_MODE_W8A8, f8 = h->cfg.mode == WQ_MODE_W8A8_FP8;
+        const bool w8 = h->cfg.mode == WQ_MODE_W8A8 || h->cfg.mode == WQ_MODE_W4A8, f8 = h->cfg.mode == WQ_MODE_W8A8_FP8;
         bool ok = (w8 ? wq::encode_tmap_2d(&h->tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, codes, K, M, 2ull * K, 64, 128,
                                            CU_TENSOR_MAP_SWIZZLE_128B, &why)
                       : f8 ? wq::encode_tmap_2d(&h->tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, K, M, K, 128, 128,
@@ -800,9 +835,20 @@ WQ_API wq_status wq_linear_forward(wq_weights_t h, const void* x, int M, void* y
     if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15)
         return fail(WQ_ERR_INVALID, "x and y must be 16-byte aligned");
     if (reinterpret_cast<uintptr_t>(workspace) & 255) return fail(WQ_ERR_INVALID, "workspace must be 256-byte aligned");
-    if (h->cfg.mode != WQ_MODE_W4A4) return fail(WQ_ERR_INVALID, "W8A8 handle: use wq_linear_forward_w8a8");
+    if (h->cfg.mode != WQ_MODE_W4A4 && h->cfg.mode != WQ_MODE_W4A8)
+        return fail(WQ_ERR_INVALID, "W8A8 handle: use wq_linear_forward_w8a8");
     if (const wq_status d = check_device(h)) return d;
     const int K = h->cfg.K, r = h->r_pad, no = h->no_pad;
+    if (h->cfg.mode == WQ_MODE_W4A8) {
+        // an A8-protected step: e4m3 activations (as exact bf16) times the bf16-held NVFP4 weights
+        const wq::ActWorkspace w8 = carve_w4a8(workspace, M, K, r, no);
+        if (workspace_bytes < w8.bytes) return fail(WQ_ERR_INVALID, "workspace too small");
+        cudaStream_t st8 = static_cast<cudaStream_t>(stream);
+        wq_status s8 = run_quant(h, x, M, WQ_SCALE_LAYOUT_ROWMAJOR, w8.codes, nullptr, w8.g, no ? w8.xo : nullptr,
+                                 r ? w8.u : nullptr, w8.amax, st8);
+        if (s8 != WQ_OK) return s8;
+        return run_gemm(h, w8.codes, nullptr, w8.g, w8.u, w8.xo, M, y, st8);
+    }
     const wq::ActWorkspace ws = wq::carve_workspace(workspace, M, K, r, no);
     if (workspace_bytes < ws.bytes) return fail(WQ_ERR_INVALID, "workspace too small");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -895,7 +941,8 @@ WQ_API wq_status wq_linear_forward_quantized(wq_weights_t h, const uint8_t* code
 WQ_API wq_status wq_linear_forward_w8a8(wq_weights_t h, const void* x, int M, void* y, void* workspace,
                                         size_t workspace_bytes, void* stream) {
     if (!h) return fail(WQ_ERR_INVALID, "NULL handle");
-    if (h->cfg.mode == WQ_MODE_W4A4) return fail(WQ_ERR_INVALID, "handle was not prepared with an 8-bit mode");
+    if (h->cfg.mode != WQ_MODE_W8A8 && h->cfg.mode != WQ_MODE_W8A8_FP8)
+        return fail(WQ_ERR_INVALID, "handle was not prepared with an 8-bit weight mode");
     if (M < 0) return fail(WQ_ERR_INVALID, "M < 0");
     if (M == 0) return WQ_OK;
     if (!x || !y || !workspace) return fail(WQ_ERR_INVALID, "NULL buffer");
@@ -915,7 +962,8 @@ WQ_API wq_status wq_linear_forward_w8a8(wq_weights_t h, const void* x, int M, vo
 WQ_API wq_status wq_quantize_activations_w8a8(wq_weights_t h, const void* x, int M, void* codes, float* scale,
                                               void* stream) {
     if (!h) return fail(WQ_ERR_INVALID, "NULL handle");
-    if (h->cfg.mode == WQ_MODE_W4A4) return fail(WQ_ERR_INVALID, "handle was not prepared with an 8-bit mode");
+    if (h->cfg.mode != WQ_MODE_W8A8 && h->cfg.mode != WQ_MODE_W8A8_FP8)
+        return fail(WQ_ERR_INVALID, "handle was not prepared with an 8-bit weight mode");
     if (M < 0) return fail(WQ_ERR_INVALID, "M < 0");
     if (M == 0) return WQ_OK;
     if (!x || !codes || !scale) return fail(WQ_ERR_INVALID, "NULL buffer");
@@ -928,7 +976,8 @@ WQ_API wq_status wq_quantize_activations_w8a8(wq_weights_t h, const void* x, int
 
 WQ_API wq_status wq_export_weights_w8a8(wq_weights_t h, int8_t* q, float* w) {
     if (!h) return fail(WQ_ERR_INVALID, "NULL handle");
-    if (h->cfg.mode == WQ_MODE_W4A4) return fail(WQ_ERR_INVALID, "handle was not prepared with an 8-bit mode");
+    if (h->cfg.mode != WQ_MODE_W8A8 && h->cfg.mode != WQ_MODE_W8A8_FP8)
+        return fail(WQ_ERR_INVALID, "handle was not prepared with an 8-bit weight mode");
     const int K = h->cfg.K, N = h->cfg.N;
     if (q && h->cfg.mode == WQ_MODE_W8A8_FP8) {
         WQ_CUDA(cudaMemcpy(q, h->d_codes, static_cast<size_t>(N) * K, cudaMemcpyDeviceToHost), "export");
@@ -1051,8 +1100,9 @@ WQ_API wq_status wq_linear_forward_host(wq_weights_t h, const void* x_host, int 
     void* dy = base + wsb + align_up(xb, 1024);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     WQ_CUDA(cudaMemcpyAsync(dx, x_host, xb, cudaMemcpyHostToDevice, st), "x upload");
-    const wq_status s = h->cfg.mode != WQ_MODE_W4A4 ? wq_linear_forward_w8a8(h, dx, M, dy, workspace, wsb, stream)
-                                                    : wq_linear_forward(h, dx, M, dy, workspace, wsb, stream);
+    const bool eight = h->cfg.mode == WQ_MODE_W8A8 || h->cfg.mode == WQ_MODE_W8A8_FP8;
+    const wq_status s = eight ? wq_linear_forward_w8a8(h, dx, M, dy, workspace, wsb, stream)
+                              : wq_linear_forward(h, dx, M, dy, workspace, wsb, stream);
     if (s != WQ_OK) return s;
     WQ_CUDA(cudaMemcpyAsync(y_host, dy, yb, cudaMemcpyDeviceToHost, st), "y download");
     return WQ_OK;
@@ -1061,7 +1111,8 @@ WQ_API wq_status wq_linear_forward_host(wq_weights_t h, const void* x_host, int 
 WQ_API wq_status wq_export_weights(wq_weights_t h, uint8_t* codes, uint8_t* scales, float* gW, uint16_t* P,
                                    uint16_t* Q, uint16_t* W_omega) {
     if (!h) return fail(WQ_ERR_INVALID, "NULL handle");
-    if (h->cfg.mode != WQ_MODE_W4A4) return fail(WQ_ERR_INVALID, "W8A8 handle: use wq_export_weights_w8a8");
+    if (h->cfg.mode != WQ_MODE_W4A4 && h->cfg.mode != WQ_MODE_W4A8)
+        return fail(WQ_ERR_INVALID, "W8A8 handle: use wq_export_weights_w8a8");
     const int K = h->cfg.K, N = h->cfg.N, r = h->cfg.rank, no = h->cfg.n_outliers;
     const int rp = h->r_pad, nop = h->no_pad;
     if (codes) WQ_CUDA(cudaMemcpy(codes, h->d_codes, static_cast<size_t>(N) * K / 2, cudaMemcpyDeviceToHost), "export");

@@ -110,6 +110,7 @@ struct QParams {
     float static_g;
     unsigned int* amax_bits;
     int fp8;            // 8-bit layer in e4m3 (scale amax / 448, bytes [M, K]) instead of int8
+    int fp8_bf16;       // with fp8: the e4m3 values written as exact bf16 [M, K] (A8 steps of a W4 layer)
 };
 
 // Zero the x_O columns beyond the kept channels for the rows of one tile (they meet zero weight
@@ -222,11 +223,30 @@ __device__ __forceinline__ void emit_fp8(const f2 (&P)[16], float gsc, float ra,
         }
         bytes[q] = word;
     }
-    if (row_ok) {
-        uint4* dst = reinterpret_cast<uint4*>(p.codes + static_cast<size_t>(row) * p.K + kb * 64 + 32 * half);
-        dst[0] = make_uint4(bytes[0], bytes[1], bytes[2], bytes[3]);
-        dst[1] = make_uint4(bytes[4], bytes[5], bytes[6], bytes[7]);
+    if (!row_ok) return;
+    if (p.fp8_bf16) {
+        // the values of the codes, exact in bf16 (3 mantissa bits, exponents 2^-9 .. 2^8)
+        uint32_t vals[16];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+#pragma unroll
+            for (int hw = 0; hw < 2; ++hw) {
+                const uint16_t pair = static_cast<uint16_t>(bytes[q] >> (16 * hw));
+                uint32_t h2;
+                asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(pair));
+                const __half2 hv = *reinterpret_cast<const __half2*>(&h2);
+                const __nv_bfloat162 bv = __floats2bfloat162_rn(__low2float(hv), __high2float(hv));
+                vals[2 * q + hw] = *reinterpret_cast<const uint32_t*>(&bv);
+            }
+        }
+        uint4* dst = reinterpret_cast<uint4*>(p.codes + (static_cast<size_t>(row) * p.K + kb * 64 + 32 * half) * 2);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) dst[j] = make_uint4(vals[4 * j], vals[4 * j + 1], vals[4 * j + 2], vals[4 * j + 3]);
+        return;
     }
+    uint4* dst = reinterpret_cast<uint4*>(p.codes + static_cast<size_t>(row) * p.K + kb * 64 + 32 * half);
+    dst[0] = make_uint4(bytes[0], bytes[1], bytes[2], bytes[3]);
+    dst[1] = make_uint4(bytes[4], bytes[5], bytes[6], bytes[7]);
 }
 
 // ==================================================================== cluster schedule
@@ -789,11 +809,20 @@ cudaError_t launch_quantize_act(const QuantArgs& a, cudaStream_t st) {
     qp.static_g = a.static_g;
     qp.amax_bits = a.amax_bits;
     qp.fp8 = a.fp8 ? 1 : 0;
+    qp.fp8_bf16 = a.fp8_bf16 ? 1 : 0;
     qp.pfrag = a.pfrag; qp.u = a.u; qp.codes = a.codes; qp.sf = a.sf; qp.sf_layout = a.sf_layout; qp.g = a.g;
     qp.err = a.err;
-    if (a.int8)
-        return a.r == 0 && a.n_out == 0 && qp.phase == 0 ? launch_r<0, true>(*a.tmX, qp, stream, a.num_sms, st)
-                                                         : cudaErrorInvalidValue;
+    if (a.int8) {
+        // 8-bit activations; the low-rank and kept-channel side outputs only for W4 layers at A8 steps
+        if (qp.phase != 0 || ((a.r != 0 || a.n_out != 0) && !(a.fp8 && a.fp8_bf16))) return cudaErrorInvalidValue;
+        switch (a.r) {
+            case 0: return launch_r<0, true>(*a.tmX, qp, stream, a.num_sms, st);
+            case 16: return launch_r<16, true>(*a.tmX, qp, stream, a.num_sms, st);
+            case 32: return launch_r<32, true>(*a.tmX, qp, stream, a.num_sms, st);
+            case 64: return launch_r<64, true>(*a.tmX, qp, stream, a.num_sms, st);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     auto launch = [&](const QParams& q) -> cudaError_t {
         switch (a.r) {
             case 0: return launch_r<0, false>(*a.tmX, q, stream, a.num_sms, st);
