@@ -77,6 +77,10 @@ def lib() -> ctypes.CDLL:
             L.orc_set_smooth_after.argtypes = [i32]
             L.orc_set_smooth_after.restype = None
             L.orc_pooled_energy.argtypes = [P, i64, i64, P, i32, P]; L.orc_pooled_energy.restype = i32
+            L.orc_projection_basis.argtypes = [P, i64, i32, i32, P]; L.orc_projection_basis.restype = i32
+            L.orc_project_complement.argtypes = [P, i64, i64, P, P, i32]; L.orc_project_complement.restype = None
+            L.orc_quantize_act_projected.argtypes = [P, i64, i64, P, i32, P, i32, P, P, i32, P, P, P, P, P]
+            L.orc_quantize_act_projected.restype = i32
             L.orc_topk_channels.argtypes = [P, i64, i32, P]; L.orc_topk_channels.restype = i32
             L.orc_e4m3s_encode.argtypes = [f32]; L.orc_e4m3s_encode.restype = ctypes.c_uint8
             L.orc_e4m3s_decode.argtypes = [ctypes.c_uint8]; L.orc_e4m3s_decode.restype = ctypes.c_double
@@ -390,6 +394,52 @@ def reference_forward_w8a8(layer, n_threads: int = 0, rows=None):
     wq8 = prepare_weights_int8(layer.W, layer.s, layer.rotate, n_threads)
     aq = quantize_act_int8(x_bits, layer.s, layer.rotate, n_threads)
     return linear_forward_w8a8(aq, wq8, layer.bias, n_threads), aq, wq8
+
+
+# ------------------------------------------------------------------ projected complement (Q-WAM ASP)
+def projection_basis(L1: np.ndarray, rotate: bool) -> np.ndarray:
+    """Vt = bf16(S_r^-2 L1^T H) [r, K]: the action subspace in the rotated basis, scaled so that
+    u Vt (u = x P, the branch's down-projection) is the activation's component in it."""
+    L1 = _c(L1, np.float32)
+    K, r = L1.shape
+    Vt = np.zeros((r, K), np.uint16)
+    rc = lib().orc_projection_basis(_p(L1), K, r, int(rotate), _p(Vt))
+    if rc:
+        raise ValueError(f"orc_projection_basis failed: {rc}")
+    return Vt
+
+
+def quantize_act_projected(x_bits, s, rotate, omega, U, Vt, keep_xt: bool = False) -> ActQuant:
+    """Q-WAM abstract: the activation quantiser on the complement of the protected subspace."""
+    x_bits = _c(x_bits, np.uint16)
+    M, K = x_bits.shape
+    inv_s = inv_smoothing(s)
+    omega = np.zeros(0, np.int32) if omega is None else _c(omega, np.int32)
+    no = int(omega.size)
+    U = _c(U, np.uint16)
+    Vt = _c(Vt, np.uint16)
+    r = Vt.shape[0]
+    codes = np.zeros((M, K // 2), np.uint8)
+    scales = np.zeros((M, K // 16), np.uint8)
+    g = np.zeros(M, np.float32)
+    xo = np.zeros((M, no), np.uint16)
+    xt = np.zeros((M, K), np.float32) if keep_xt else None
+    rc = lib().orc_quantize_act_projected(_p(x_bits), M, K, _p(inv_s), int(rotate), _p(omega), no, _p(U), _p(Vt), r,
+                                          _p(codes), _p(scales), _p(g), _p(xo), _p(xt))
+    if rc:
+        raise ValueError(f"orc_quantize_act_projected failed: {rc}")
+    return ActQuant(codes, scales, g, xo, xt)
+
+
+def reference_forward_projected(layer, n_threads: int = 0, rows=None):
+    """Full oracle pass of the projected-complement variant: (y fp64, ActQuant, WeightQuant, U, Vt)."""
+    x_bits = layer.x_bits if rows is None else layer.x_bits[rows]
+    wq = prepare_weights(layer.W, layer.s, layer.L1, layer.L2, layer.omega, layer.rotate, n_threads)
+    U = lowrank_act(x_bits, wq.P)
+    Vt = projection_basis(layer.L1, layer.rotate)
+    aq = quantize_act_projected(x_bits, layer.s, layer.rotate, layer.omega, U, Vt)
+    y = linear_forward(aq, wq, U, layer.bias, n_threads=n_threads)
+    return y, aq, wq, U, Vt
 
 
 # ------------------------------------------------------------------ outlier calibration

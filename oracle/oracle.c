@@ -737,6 +737,81 @@ int orc_linear_forward_fp8(const uint8_t *qa, const float *a, long M, const uint
     return 0;
 }
 
+/* ------------------------------------------------------------------ projected complement */
+/* Q-WAM abstract (Action-Subspace Protection): a 16-bit low-rank branch protects the action
+ * subspace and the complementary weights AND activations are quantised.  Reading: with the branch
+ * factors L1 L2 = U_r S_r V_r^T (top-r SVD of the smoothed weight), the activation's complement is
+ * x_c = xs - (xs U_r) U_r^T, in the rotated basis xt_c = xt - u Vt with u = the branch's bf16
+ * down-projection x P (P = diag(1/s) L1, so xs U_r = u S_r^-1) and
+ *   Vt[j][k] = bf16( (H L1[:, j])[k] / ||L1[:, j]||^2 )      (S_r^-2 L1^T H, fp64, one rounding).
+ * Each element: acc = xt[k]; acc = fma(-u[j], Vt[j][k], acc) for j = 0 .. r-1 in that order (fp32).
+ * The weight complement R = (I - U_r U_r^T) W_s already gives xc R = xs R, so the folding identity
+ * holds unchanged; only the quantiser's input changes (then the kept-channel split and NVFP4). */
+
+/* Vt [r, K] bf16 bits from L1 [K, r] (fp32), rotate as in the fold. */
+int orc_projection_basis(const float *L1, long K, int r, int rotate, uint16_t *Vt)
+{
+    double *col = (double *)malloc(sizeof(double) * (size_t)K);
+    if (!col) return -4;
+    for (int j = 0; j < r; ++j) {
+        double nrm = 0.0;
+        for (long k = 0; k < K; ++k) {
+            col[k] = (double)L1[k * r + j];
+            nrm += col[k] * col[k];
+        }
+        if (rotate)
+            for (long b = 0; b < K / 64; ++b) orc_fwht64_f64(col + 64 * b, 1);
+        for (long k = 0; k < K; ++k) Vt[(long)j * K + k] = orc_bf16_from_f64(nrm > 0.0 ? col[k] / nrm : 0.0);
+    }
+    free(col);
+    return 0;
+}
+
+/* xt_c = xt - u Vt for M rows: xt fp32 [M, K] in place, u bf16 [M, r], Vt bf16 [r, K]. */
+void orc_project_complement(float *xt, long M, long K, const uint16_t *u, const uint16_t *Vt, int r)
+{
+#pragma omp parallel for schedule(static)
+    for (long m = 0; m < M; ++m)
+        for (long k = 0; k < K; ++k) {
+            float acc = xt[m * K + k];
+            for (int j = 0; j < r; ++j)
+                acc = fmaf(-orc_f32_from_bf16(u[m * r + j]), orc_f32_from_bf16(Vt[(long)j * K + k]), acc);
+            xt[m * K + k] = acc;
+        }
+}
+
+/* The activation quantiser on the projected complement: transform, subtract u Vt, kept-channel
+ * split, per-row NVFP4 (as orc_quantize_act with per_tensor = 0). */
+int orc_quantize_act_projected(const uint16_t *x_bf16, long M, long K, const float *inv_s, int rotate,
+                               const int32_t *omega, int n_omega, const uint16_t *u, const uint16_t *Vt, int r,
+                               uint8_t *codes, uint8_t *scales, float *g, uint16_t *x_omega, float *xt_out)
+{
+    if (K % 16 || (rotate && K % 64)) return -1;
+    float *xt = (float *)malloc(sizeof(float) * (size_t)M * (size_t)K);
+    if (!xt) return -4;
+    for (long m = 0; m < M; ++m) orc_act_transform_row(x_bf16 + m * K, K, inv_s, rotate, xt + m * K);
+    orc_project_complement(xt, M, K, u, Vt, r);
+#pragma omp parallel for schedule(static)
+    for (long m = 0; m < M; ++m) {
+        float *row = xt + m * K;
+        for (int j = 0; j < n_omega; ++j) {
+            x_omega[m * n_omega + j] = orc_f16_from_f32(row[omega[j]]);
+            row[omega[j]] = 0.0f;
+        }
+        float amax = 0.0f;
+        for (long k = 0; k < K; ++k) {
+            float a = fabsf(row[k]);
+            if (a > amax) amax = a;
+        }
+        float gm = orc_nvfp4_tensor_scale(amax);
+        g[m] = gm;
+        orc_nvfp4_quantize(row, K, gm, codes + m * (K / 2), scales + m * (K / 16));
+    }
+    if (xt_out) memcpy(xt_out, xt, sizeof(float) * (size_t)M * (size_t)K);
+    free(xt);
+    return 0;
+}
+
 /* ------------------------------------------------------------------ W4A8 */
 /* A8-protected steps (QuantWAMs sec. 4.2 and sec. 5: one of ten Fast-WAM action steps, two of twenty
  * and six of fifty LingBot-VA steps run their activations at 8 bits).  Reading: the 4-bit layer keeps

@@ -745,3 +745,72 @@ def test_w4a8_reduces_to_dequantised_matmul_and_sits_between_w4a4_and_fp8():
     assert not a8.q[:, L.omega].any()
     aq4 = oracle.quantize_act(L.x_bits, L.s, True, L.omega)
     assert np.array_equal(a8.x_omega, aq4.x_omega)            # the same fp16 kept channels
+
+
+# ------------------------------------------------------------------ Q-WAM projected complement
+def test_projected_complement_is_orthogonal_and_keeps_the_fold():
+    """Q-WAM abstract (the complementary activations are quantised): xt_c = xt - u Vt is (up to the
+    bf16 roundings of u and Vt) orthogonal to the protected subspace, and with quantisation off the
+    three branches still compute x W + b (x_c R = x_s R for the complement R)."""
+    L = wlmod.make_layer_inputs("video_dit", M=24, K=256, N=64, rank=16, n_omega=0)
+    wq = oracle.prepare_weights(L.W, L.s, L.L1, L.L2, None, True)
+    U = oracle.lowrank_act(L.x_bits, wq.P)
+    Vt = oracle.projection_basis(L.L1, True)
+    aq = oracle.quantize_act_projected(L.x_bits, L.s, True, None, U, Vt, keep_xt=True)
+    H = hadamard(64).astype(np.float64) / 8.0
+    Ur = L.L1.astype(np.float64) / np.linalg.norm(L.L1.astype(np.float64), axis=0)[None, :]
+    HUr = (H @ Ur.reshape(4, 64, 16)).reshape(256, 16)          # the subspace in the rotated basis
+    xt = oracle.quantize_act(L.x_bits, L.s, True, keep_xt=True).xt.astype(np.float64)
+    before = np.abs(xt @ HUr).max()
+    after = np.abs(aq.xt.astype(np.float64) @ HUr).max()
+    assert after < 1e-2 * before, (before, after)
+    # the fold: xt_c R' + u Q + b = x W + b without quantisation
+    y = aq.xt.astype(np.float64) @ wq.Rp.astype(np.float64) + \
+        wlmod.bf16_from_bits(U).astype(np.float64) @ wlmod.bf16_from_bits(wq.Q).astype(np.float64) + L.bias
+    ref = L.x_f32.astype(np.float64) @ L.W.astype(np.float64) + L.bias
+    assert np.max(np.abs(y - ref)) / np.max(np.abs(ref)) < 2e-2
+    ynp = xt @ wq.Rp.astype(np.float64) + wlmod.bf16_from_bits(U).astype(np.float64) @ \
+        wlmod.bf16_from_bits(wq.Q).astype(np.float64) + L.bias
+    assert np.max(np.abs(y - ynp)) / np.max(np.abs(ref)) < 2e-2
+
+
+def test_projection_basis_and_fma_sequence_against_numpy():
+    """Vt = bf16(S^-2 L1^T H) from dense fp64 matrices (single rounding); the subtraction is the fp32
+    fma sequence j = 0 .. r-1, restated with numpy's fp32 arithmetic via the exact fp64 product."""
+    rng = np.random.default_rng(91)
+    K, r = 128, 8
+    L1 = rng.standard_normal((K, r)).astype(np.float32)
+    Vt = oracle.projection_basis(L1, True)
+    H = hadamard(64).astype(np.float64) / 8.0
+    l1 = L1.astype(np.float64)
+    want = ((H @ l1.reshape(2, 64, r)).reshape(K, r) / (l1 * l1).sum(axis=0)[None, :]).T
+    assert np.array_equal(Vt, np.array([[_exact_bf16_bits(float(v)) for v in row] for row in want], np.uint16))
+    M = 5
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    u = wlmod.bf16_bits(rng.standard_normal((M, r)).astype(np.float32))
+    xt = x.copy()
+    oracle.lib().orc_project_complement(xt.ctypes.data_as(ctypes.c_void_p), M, K, u.ctypes.data_as(ctypes.c_void_p),
+                                        Vt.ctypes.data_as(ctypes.c_void_p), r)
+    uf = wlmod.bf16_from_bits(u).astype(np.float64)
+    vf = wlmod.bf16_from_bits(Vt).astype(np.float64)
+    acc = x.copy()
+    for j in range(r):      # fma: the exact product and sum rounded once to fp32
+        acc = (acc.astype(np.float64) - uf[:, j:j + 1] * vf[j][None, :]).astype(np.float32)
+    assert np.array_equal(xt, acc)
+
+
+def test_projected_complement_lowers_error_when_the_subspace_carries_the_outliers():
+    """When the activations' large components lie in the protected subspace, quantising the
+    complement instead of the whole activation lowers the W4A4 error (Q-WAM's premise)."""
+    L = wlmod.make_layer_inputs("video_dit", M=64, K=512, N=128, rank=16, n_omega=0)
+    rng = np.random.default_rng(92)
+    s = L.s.astype(np.float64)
+    Ur = L.L1.astype(np.float64) / np.linalg.norm(L.L1.astype(np.float64), axis=0)[None, :]
+    x = L.x_f32.astype(np.float64) + 20.0 * (rng.standard_normal((64, 16)) @ Ur.T) * s[None, :]
+    L.x_bits = wlmod.bf16_bits(x.astype(np.float32))
+    y_p, *_ = oracle.reference_forward_projected(L)
+    y_n, *_ = oracle.reference_forward(L)
+    ref = L.x_f32.astype(np.float64) @ L.W.astype(np.float64) + L.bias
+    e_p = np.linalg.norm(y_p - ref) / np.linalg.norm(ref)
+    e_n = np.linalg.norm(y_n - ref) / np.linalg.norm(ref)
+    assert e_p < e_n, (e_p, e_n)
