@@ -100,7 +100,17 @@ enum { WQ_ORDER_SMOOTH_ROTATE = 0, WQ_ORDER_ROTATE_SMOOTH = 1 };
  * which holds every e4m3 value and every NVFP4 value dec(code) dec(scale) exactly (no tensor kind
  * multiplies e4m3 by e2m1 under NVFP4's e4m3-per-16 weight scales), so the handle stores the
  * weight values expanded to bf16 [N, K] next to the NVFP4 codes, and wq_linear_forward writes the
- * activation values as bf16 [M, K] (wq_workspace_bytes covers them). */
+ * activation values as bf16 [M, K] (wq_workspace_bytes covers them).
+ * project = 1 (Q-WAM abstract, Action-Subspace Protection: the 16-bit low-rank branch protects the
+ * action subspace and the complementary weights AND activations are quantised): with the branch's
+ * bf16 down-projection u = x P, the activation quantiser works on
+ *     xt_c = xt - u Vt,   Vt[j][k] = bf16((H L1[:, j])[k] / ||L1[:, j]||^2)   (fp64, one rounding),
+ * the complement of the span of L1 (the top-r left singular directions of diag(s) W) in the rotated
+ * basis, one fp32 fma per rank term in the order j = 0 .. rank-1, before the kept-channel split.
+ * The weights are unchanged: the complement R = W_s - L1 L2 already annihilates nothing of x's
+ * complement and y = xt_c R' + u Q + x_O W_O + b equals the full activation's result up to the
+ * quantisation.  Needs rank > 0, WQ_MODE_W4A4, WQ_ACT_SCALE_ROW and WQ_ORDER_SMOOTH_ROTATE; the
+ * quantiser then takes two launches (U, then both passes over the projected values). */
 typedef struct wq_config {
     int K;            /* input features (reduction dimension)                              */
     int N;            /* output features                                                   */
@@ -111,6 +121,8 @@ typedef struct wq_config {
     int act_scale;    /* WQ_ACT_SCALE_* (4-bit layers; W8A8 takes WQ_ACT_SCALE_ROW)        */
     float act_gscale; /* WQ_ACT_SCALE_STATIC: the calibrated g (> 0, finite); else ignored */
     int transform_order; /* WQ_ORDER_*: where the smoothing sits relative to the rotation  */
+    int project;      /* 1: quantise the activation's complement of the protected subspace  */
+                      /* (Q-WAM Action-Subspace Protection, below); 0: the full activation */
 } wq_config;
 
 /*

@@ -33,8 +33,8 @@ def test_library_exports_every_declared_symbol():
         assert hasattr(L, name), name
 
 
-def _cfg(K=256, N=128, r=0, no=0, rot=1, mode=0, act=0, g=0.0, order=0):
-    return wq.wq_config(K, N, r, no, rot, mode, act, g, order)
+def _cfg(K=256, N=128, r=0, no=0, rot=1, mode=0, act=0, g=0.0, order=0, proj=0):
+    return wq.wq_config(K, N, r, no, rot, mode, act, g, order, proj)
 
 
 @pytest.mark.parametrize("cfg,status", [
@@ -57,6 +57,11 @@ def _cfg(K=256, N=128, r=0, no=0, rot=1, mode=0, act=0, g=0.0, order=0):
     (dict(act=2, g=float("inf")), wq.WQ_ERR_INVALID),
     (dict(order=2), wq.WQ_ERR_INVALID),
     (dict(mode=1, order=1), wq.WQ_ERR_UNSUPPORTED),
+    (dict(proj=2, r=16), wq.WQ_ERR_INVALID),
+    (dict(proj=1), wq.WQ_ERR_UNSUPPORTED),                # no branch to project on
+    (dict(proj=1, r=16, act=1), wq.WQ_ERR_UNSUPPORTED),
+    (dict(proj=1, r=16, order=1), wq.WQ_ERR_UNSUPPORTED),
+    (dict(proj=1, r=16, mode=3), wq.WQ_ERR_UNSUPPORTED),
 ])
 def test_prepare_rejects_bad_config(cfg, status):
     if status is None:

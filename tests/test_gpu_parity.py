@@ -528,3 +528,71 @@ def test_w4a8_protected_step(case, wide, tuning):
         got, pad = side_out(xo, L.omega.size)
         assert np.array_equal(got, aq.x_omega) and not pad.any()
     assert_y_close(L, y, y_ref)
+
+
+# ------------------------------------------------------------------ Q-WAM projected complement
+PROJ_CASES = ["tiny_full", "expert_small", "ragged_m130", "dit_r32_o64_ragged_n", "no_rotate_o16",
+              "no_smooth_r64", "multi_tile_kstage_tail", "top2pct_o41_r24", "o5_r8", "o64_r40_no_rotate"]
+
+
+def check_projected(L, w, x, rows=None, min_exact=0.9):
+    """The projected-complement quantiser and forward against the oracle.  The projection takes
+    u = bf16(x P) as an input; the GPU sums x P in fp32 and the oracle in fp64, so a row's u can
+    differ by the bound of u_close.  On every row whose u is identical (at least min_exact of
+    them) the codes, scales, g and x_Omega are bit-exact and y is within the y tolerance."""
+    codes, scales, g, xo, u = wq.wq_quantize_activations(w, x, wq.WQ_SCALE_LAYOUT_ROWMAJOR)
+    y = wq.wq_linear_forward(w, x)
+    torch.cuda.synchronize()
+    wq.wq_check_device_error(w)
+    y_ref, aq, o, U, _ = oracle.reference_forward_projected(L, rows=rows)
+    sel = slice(None) if rows is None else torch.from_numpy(rows)
+    xb = L.x_bits if rows is None else L.x_bits[rows]
+    ug, pad = side_out(u[sel], L.rank)
+    assert u_close(ug, U, xb, o.P).all() and not pad.any()
+    same = (ug == U).all(axis=1)
+    assert same.mean() >= min_exact, f"only {same.sum()} of {same.size} rows with identical u"
+    idx = np.nonzero(same)[0]
+    assert np.array_equal(g[sel].cpu().numpy()[idx], aq.g[idx])
+    assert np.array_equal(scales[sel].cpu().numpy()[idx], aq.scales[idx])
+    assert np.array_equal(codes[sel].cpu().numpy()[idx], aq.codes[idx])
+    if L.omega.size:
+        got, xpad = side_out(xo[sel], L.omega.size)
+        assert np.array_equal(got[idx], aq.x_omega[idx]) and not xpad.any()
+    r_idx = idx if rows is None else rows[idx]
+    assert_y_close(L, y[torch.from_numpy(r_idx).cuda()], y_ref[idx], r_idx)
+
+
+@pytest.mark.parametrize("case", PROJ_CASES)
+def test_projected_complement(case):
+    """Q-WAM abstract (Action-Subspace Protection): the activations' complement of the low-rank
+    branch's subspace is what the quantiser sees.  Weights unchanged (bit-exact against the
+    oracle's fold); the quantiser on the stream schedule (two launches)."""
+    L = layer(case)
+    w = prep(L, project=True)
+    assert wq.wq_quant_schedule(w, L.M) == wq.WQ_QUANT_STREAM
+    assert wq.wq_forward_path(w, L.M) == wq.WQ_PATH_TWO_KERNEL
+    ex = wq.wq_export_weights(w)
+    o = ow(L)
+    assert np.array_equal(ex["codes"], o.codes) and np.array_equal(ex["scales"], o.scales)
+    check_projected(L, w, x_dev(L.x_bits))
+
+
+def test_projected_complement_changes_the_codes():
+    """The projection is applied: the projected handle's codes differ from the plain handle's on
+    the same input."""
+    L = layer("dit_r32_o64_ragged_n")
+    x = x_dev(L.x_bits)
+    c0, *_ = wq.wq_quantize_activations(prep(L), x, wq.WQ_SCALE_LAYOUT_ROWMAJOR)
+    c1, *_ = wq.wq_quantize_activations(prep(L, project=True), x, wq.WQ_SCALE_LAYOUT_ROWMAJOR)
+    torch.cuda.synchronize()
+    assert not torch.equal(c0, c1)
+
+
+@pytest.mark.parametrize("wl_name", ["video_dit", "expert"])
+def test_projected_complement_full_size(wl_name):
+    """The full-size projection (video_dit's attention qkv input, the expert's up projection):
+    one row of every 128-row tile plus the first and last rows."""
+    L = wl.make_layer_inputs(wl_name, layer=0)
+    w = prep(L, project=True)
+    rows = _tile_rows(L.M, 31)
+    check_projected(L, w, x_dev(L.x_bits), rows=rows, min_exact=0.85)

@@ -46,7 +46,8 @@ class WqError(RuntimeError):
 class wq_config(ctypes.Structure):
     _fields_ = [("K", ctypes.c_int), ("N", ctypes.c_int), ("rank", ctypes.c_int),
                 ("n_outliers", ctypes.c_int), ("rotate", ctypes.c_int), ("mode", ctypes.c_int),
-                ("act_scale", ctypes.c_int), ("act_gscale", ctypes.c_float), ("transform_order", ctypes.c_int)]
+                ("act_scale", ctypes.c_int), ("act_gscale", ctypes.c_float), ("transform_order", ctypes.c_int),
+                ("project", ctypes.c_int)]
 
 
 _lib = None
@@ -174,12 +175,13 @@ class Weights:
 def wq_prepare_weights(K: int, N: int, W, bias=None, s=None, L1=None, L2=None, omega=None,
                        rotate: bool = True, mode: int = WQ_MODE_W4A4, stream=None,
                        act_scale: int = WQ_ACT_SCALE_ROW, act_gscale: float = 0.0,
-                       transform_order: int = WQ_ORDER_SMOOTH_ROTATE) -> Weights:
-    """Fold and quantise one projection (host inputs, numpy or CPU tensors)."""
+                       transform_order: int = WQ_ORDER_SMOOTH_ROTATE, project: bool = False) -> Weights:
+    """Fold and quantise one projection (host inputs, numpy or CPU tensors).  project: quantise
+    the activations' complement of the low-rank branch's subspace (Q-WAM ASP)."""
     rank = 0 if L1 is None else int(np.shape(L1)[1])
     n_out = 0 if omega is None else int(np.size(omega))
     cfg = wq_config(K, N, rank, n_out, int(bool(rotate)), mode, int(act_scale), float(act_gscale),
-                    int(transform_order))
+                    int(transform_order), int(bool(project)))
     keep = []
     ptrs = []
     for a, dt in ((W, np.float32), (bias, np.float32), (s, np.float32), (L1, np.float32),

@@ -222,6 +222,7 @@ struct wq_weights {
     int* d_err = nullptr;
     float* d_colscale = nullptr;   // W8A8: per-output-column weight scale [N]
     uint16_t* d_wexp = nullptr;    // W4A8: the NVFP4 weight values (code x block scale) as exact bf16 [N, K]
+    uint16_t* d_Vt = nullptr;      // projected complement: bf16 [rank, K], the protected subspace's basis
     int r_pad = 0;                 // stored rank: side_width(rank) (U, P, Q^T columns)
     int no_pad = 0;                // stored outlier width: side_width(n_outliers) (x_O, W_O^T columns)
     unsigned int* d_amax = nullptr;// WQ_ACT_SCALE_TENSOR: running batch maximum of wq_quantize_activations
@@ -274,6 +275,11 @@ wq_status check_config(const wq_config* c) {
         return fail(WQ_ERR_INVALID, "unknown transform_order");
     if (eight && c->transform_order != WQ_ORDER_SMOOTH_ROTATE)
         return fail(WQ_ERR_UNSUPPORTED, "the 8-bit modes take WQ_ORDER_SMOOTH_ROTATE");
+    if (c->project != 0 && c->project != 1) return fail(WQ_ERR_INVALID, "project must be 0 or 1");
+    if (c->project && (c->rank == 0 || c->mode != WQ_MODE_W4A4 || c->act_scale != WQ_ACT_SCALE_ROW ||
+                       c->transform_order != WQ_ORDER_SMOOTH_ROTATE))
+        return fail(WQ_ERR_UNSUPPORTED,
+                    "project takes rank > 0, WQ_MODE_W4A4, WQ_ACT_SCALE_ROW and WQ_ORDER_SMOOTH_ROTATE");
     return WQ_OK;
 }
 
@@ -291,6 +297,7 @@ void free_device(wq_weights* h) {
     cudaFree(h->d_colscale);
     cudaFree(h->d_amax);
     cudaFree(h->d_wexp);
+    cudaFree(h->d_Vt);
 }
 
 template <typename T>
@@ -594,6 +601,24 @@ WQ_API wq_status wq_prepare_weights(const wq_config* cfg, const float* W, const 
                                 CU_TENSOR_MAP_SWIZZLE_128B, &why))
             return bail(fail(WQ_ERR_CUDA, why));
     }
+    if (cfg->project) {
+        // Vt[j] = FWHT_64(L1[:, j]) / ||L1[:, j]||^2, fp64, one rounding to bf16
+        std::vector<uint16_t> Vt(static_cast<size_t>(r) * K);
+        std::vector<double> col(K);
+        for (int j = 0; j < r; ++j) {
+            double nrm = 0.0;
+            for (int k = 0; k < K; ++k) {
+                col[k] = static_cast<double>(L1[static_cast<size_t>(k) * r + j]);
+                nrm += col[k] * col[k];
+            }
+            if (cfg->rotate)
+                for (int b = 0; b < K / 64; ++b) fwht64_f64(col.data() + 64 * b, 1);
+            for (int k = 0; k < K; ++k)
+                Vt[static_cast<size_t>(j) * K + k] = bf16_bits_from_f64(nrm > 0.0 ? col[k] / nrm : 0.0);
+        }
+        if ((st = upload(&h->d_Vt, Vt.data(), Vt.size() * 2, cs)) != WQ_OK) return bail(st);
+        if (cudaStreamSynchronize(cs) != cudaSuccess) return bail(fail(WQ_ERR_CUDA, "upload synchronise failed"));
+    }
     *out = h;
     return WQ_OK;
 }
@@ -713,6 +738,11 @@ static wq_status run_quant(wq_weights_t h, const void* x, int M, int layout, uin
     qa.int8 = h->cfg.mode != WQ_MODE_W4A4;
     qa.fp8 = h->cfg.mode == WQ_MODE_W8A8_FP8 || h->cfg.mode == WQ_MODE_W4A8;
     qa.fp8_bf16 = h->cfg.mode == WQ_MODE_W4A8;
+    if (h->cfg.project) {
+        if (!u) return fail(WQ_ERR_INVALID, "project: the U buffer is required (u = x P feeds the projection)");
+        qa.vt = h->d_Vt;
+        qa.r_real = h->cfg.rank;
+    }
     const cudaError_t e = wq::launch_quantize_act(qa, st);
     if (e != cudaSuccess) return cuda_fail(e, "activation quantiser launch");
     return WQ_OK;
@@ -791,7 +821,7 @@ static wq_status run_gemm(wq_weights_t h, const uint8_t* codes, const uint8_t* s
 
 namespace {
 bool use_fused(wq_weights_t h, int M, int& nb, int& cs) {
-    return h->cfg.mode == WQ_MODE_W4A4 && h->cfg.act_scale == WQ_ACT_SCALE_ROW &&
+    return h->cfg.mode == WQ_MODE_W4A4 && h->cfg.act_scale == WQ_ACT_SCALE_ROW && !h->cfg.project &&
            h->cfg.transform_order == WQ_ORDER_SMOOTH_ROTATE && wq::tune(wq::kTuneFused) == 1 &&
            wq::fused_plan(M, h->cfg.K, h->cfg.N, h->r_pad, h->no_pad, nb, cs);
 }
@@ -801,7 +831,7 @@ WQ_API int wq_quant_schedule(wq_weights_t h, int M) {
     if (!h) return fail(WQ_ERR_INVALID, "NULL handle");
     if (M < 0) return fail(WQ_ERR_INVALID, "M < 0");
     // batch-wide tensor scales take the stream kernel (its two-launch and one-pass forms)
-    if (h->cfg.act_scale != WQ_ACT_SCALE_ROW) return WQ_QUANT_STREAM;
+    if (h->cfg.act_scale != WQ_ACT_SCALE_ROW || h->cfg.project) return WQ_QUANT_STREAM;
     return wq::quant_stream_schedule(M, h->num_sms) ? WQ_QUANT_STREAM : WQ_QUANT_CLUSTER;
 }
 
@@ -1009,7 +1039,7 @@ WQ_API wq_status wq_prepare_conv3d(const float* w, int C_in, int C_out, int kt, 
         for (int c = 0; c < C_in; ++c)
             for (int t = 0; t < 27; ++t)
                 Wm[(static_cast<size_t>(t) * C_in + c) * N + n] = w[(static_cast<size_t>(n) * C_in + c) * 27 + t];
-    wq_config cfg{K, N, 0, 0, 0, WQ_MODE_W4A4, WQ_ACT_SCALE_ROW, 0.0f, WQ_ORDER_SMOOTH_ROTATE};
+    wq_config cfg{K, N, 0, 0, 0, WQ_MODE_W4A4, WQ_ACT_SCALE_ROW, 0.0f, WQ_ORDER_SMOOTH_ROTATE, 0};
     wq_weights_t h = nullptr;
     const wq_status st = wq_prepare_weights(&cfg, Wm.data(), nullptr, nullptr, nullptr, nullptr, nullptr, stream, &h);
     if (st != WQ_OK) return st;

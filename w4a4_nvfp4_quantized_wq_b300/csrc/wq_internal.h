@@ -71,6 +71,8 @@ struct QuantArgs {
     bool int8 = false;              // 8-bit layer: codes are int8 values stored as bf16 [M, K]
     bool fp8 = false;               // with int8: e4m3 bytes [M, K] instead, scale amax / 448
     bool fp8_bf16 = false;          // with fp8: the e4m3 values as exact bf16 [M, K] (W4A8)
+    const uint16_t* vt = nullptr;   // Q-WAM projected complement: bf16 [r_real, K] (null: off)
+    int r_real = 0;                 // the configured rank (the projection's loop length)
     // Activation tensor scale: WQ_ACT_SCALE_ROW (one per row, from the row), WQ_ACT_SCALE_TENSOR
     // (one for all M rows: a first launch takes the maximum, a second quantises) or
     // WQ_ACT_SCALE_STATIC (the calibrated `static_g`, one pass).  Every mode writes g[m] per row.

@@ -111,6 +111,10 @@ struct QParams {
     unsigned int* amax_bits;
     int fp8;            // 8-bit layer in e4m3 (scale amax / 448, bytes [M, K]) instead of int8
     int fp8_bf16;       // with fp8: the e4m3 values written as exact bf16 [M, K] (A8 steps of a W4 layer)
+    // Q-WAM projected complement (phase 6): xt -= u Vt right after each block's transform, u the
+    // bf16 U rows written by a first launch (phase 1), Vt bf16 [r_real, K]
+    const uint16_t* vt;
+    int r_real;
 };
 
 // Zero the x_O columns beyond the kept channels for the rows of one tile (they meet zero weight
@@ -247,6 +251,31 @@ __device__ __forceinline__ void emit_fp8(const f2 (&P)[16], float gsc, float ra,
     uint4* dst = reinterpret_cast<uint4*>(p.codes + static_cast<size_t>(row) * p.K + kb * 64 + 32 * half);
     dst[0] = make_uint4(bytes[0], bytes[1], bytes[2], bytes[3]);
     dst[1] = make_uint4(bytes[4], bytes[5], bytes[6], bytes[7]);
+}
+
+// xt -= u Vt for this lane's half row of block kb, one fp32 fma per rank term in the order
+// j = 0 .. r-1 (the pairs' two lanes are separate IEEE fmas), u from the row's stored bf16 U.
+template <int R>
+__device__ __forceinline__ void project_block(f2 (&P)[16], const QParams& p, int row, bool row_ok, int kb, int half) {
+    if constexpr (R > 0) {
+        const uint16_t* urow = p.u + static_cast<size_t>(row) * R;
+        const uint16_t* vb = p.vt + kb * 64 + 32 * half;
+        for (int j = 0; j < p.r_real; ++j) {
+            const float uj = row_ok ? __uint_as_float(static_cast<uint32_t>(urow[j]) << 16) : 0.0f;
+            const f2 nu = pk2(-uj, -uj);
+            const uint4* v4 = reinterpret_cast<const uint4*>(vb + static_cast<size_t>(j) * p.K);
+            const uint4 q0 = __ldg(v4), q1 = __ldg(v4 + 1), q2 = __ldg(v4 + 2), q3 = __ldg(v4 + 3);
+            const uint32_t w[16] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w,
+                                    q2.x, q2.y, q2.z, q2.w, q3.x, q3.y, q3.z, q3.w};
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const uint32_t a = w[k / 2], b = w[8 + k / 2];
+                const float vlo = __uint_as_float((k & 1) ? (a & 0xFFFF0000u) : (a << 16));   // channel k
+                const float vhi = __uint_as_float((k & 1) ? (b & 0xFFFF0000u) : (b << 16));   // channel k + 16
+                P[k] = fma2(nu, pk2(vlo, vhi), P[k]);
+            }
+        }
+    }
 }
 
 // ==================================================================== cluster schedule
@@ -533,7 +562,7 @@ quantize_stream_kernel(const __grid_constant__ CUtensorMap tmX, const QParams p)
             if (p.n_out) bulk_load(base + lay.off_omega, p.omega_blk, 16u * nblk, bar_const);
             uint32_t q = 0;
             bool ok = true;
-            const int passes = p.phase == 0 ? 2 : 1;
+            const int passes = (p.phase == 0 || p.phase == 6) ? 2 : 1;
             for (int tile = blockIdx.x; ok && tile < p.row_tiles; tile += gridDim.x)
                 for (int pass = 0; ok && pass < passes; ++pass)
                     for (int kb = 0; kb < nblk; ++kb, ++q) {
@@ -561,9 +590,11 @@ quantize_stream_kernel(const __grid_constant__ CUtensorMap tmX, const QParams p)
     const uint32_t upart = base + lay.off_upart + static_cast<uint32_t>(warp * NT) * 512u;
     bool ok = __all_sync(kFullMask, mbar_wait(bar_const, 0, abort_flag, p.err, 24));
     const bool first_pass = p.phase != 2;     // smoothing, FWHT, U, x_O, maxima
-    const bool second_pass = p.phase == 0 || p.phase == 2;
+    const bool second_pass = p.phase == 0 || p.phase == 2 || p.phase == 6;
+    const bool project = p.phase == 6;        // U comes from the previous launch
     // phase 2: the batch maximum was folded in by the previous grid; phase 3: the calibrated g
     float g_fixed = p.static_g;
+    if (p.phase == 6) griddep_wait();          // U rows written by the previous grid
     if (p.phase == 2) {
         griddep_wait();
         g_fixed = __fdiv_rn(__uint_as_float(*reinterpret_cast<volatile unsigned int*>(p.amax_bits)), 2688.0f);
@@ -595,7 +626,10 @@ quantize_stream_kernel(const __grid_constant__ CUtensorMap tmX, const QParams p)
                 f2 P[16];
                 load_transform(box, r, half, p.inv_s ? s_invs + 256u * s : 0u, p.rotate, P);
                 QPH(1);
-                if constexpr (R > 0) u_step<NT>(box, lane, kb, p.pfrag, upart, kb == warp);
+                if constexpr (R > 0) {
+                    if (project) project_block<R>(P, p, row, row_ok, kb, half);
+                    else u_step<NT>(box, lane, kb, p.pfrag, upart, kb == warp);
+                }
                 QPH(2);
                 const uint32_t m0 = p.n_out ? s_omega[4 * kb] : 0u, m1 = p.n_out ? s_omega[4 * kb + 1] : 0u;
                 if ((m0 | m1) != 0u) {
@@ -640,7 +674,7 @@ quantize_stream_kernel(const __grid_constant__ CUtensorMap tmX, const QParams p)
             amax = 0.0f;
             for (int w = 0; w < active; ++w) amax = fmaxf(amax, s_amax[w * kRows + r]);
             if constexpr (R > 0) {
-                for (int idx = threadIdx.x; idx < NT * 128; idx += kConsumerWarps * 32) {
+                for (int idx = threadIdx.x; idx < (project ? 0 : NT * 128); idx += kConsumerWarps * 32) {
                     float sum = 0.0f;
                     for (int w = 0; w < active; ++w)
                         sum = __fadd_rn(sum, ld_shared_f32(base + lay.off_upart + static_cast<uint32_t>(w * NT) * 512u + 4u * idx));
@@ -652,7 +686,7 @@ quantize_stream_kernel(const __grid_constant__ CUtensorMap tmX, const QParams p)
             }
             zero_xo_pad(p, tile, threadIdx.x, kConsumerWarps * 32);
             named_bar_sync(1, kConsumerWarps * 32);        // maxima and partials are free again
-            if (p.phase == 0) {
+            if (p.phase == 0 || p.phase == 6) {
                 gsc = __fdiv_rn(amax, kInt8 ? (p.fp8 ? 448.0f : 127.0f) : 2688.0f);
                 rg_inv = __frcp_rn(gsc);
             }
@@ -675,6 +709,7 @@ quantize_stream_kernel(const __grid_constant__ CUtensorMap tmX, const QParams p)
                 load_transform(base + s * kBoxBytes, r, half, p.inv_s ? s_invs + 256u * s : 0u, p.rotate, P);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_empty + 8u * s);
+                if (project) project_block<R>(P, p, row, row_ok, kb, half);
                 QPH(6);
                 const uint32_t m0 = p.n_out ? s_omega[4 * kb] : 0u, m1 = p.n_out ? s_omega[4 * kb + 1] : 0u;
                 if ((half ? m1 : m0) != 0u) apply_keep(P, half ? m1 : m0);
@@ -691,7 +726,7 @@ quantize_stream_kernel(const __grid_constant__ CUtensorMap tmX, const QParams p)
         }
         QPH(7);
     }
-    if (p.phase == 1 && warp == 0) {
+    if (p.phase == 1 && p.amax_bits != nullptr && warp == 0) {
         // lanes 0..15 hold the maxima of the CTA's rows r; one atomic per CTA (non-negative
         // floats order like their bit patterns)
 #pragma unroll
@@ -792,7 +827,7 @@ cudaError_t launch_quantize_act(const QuantArgs& a, cudaStream_t st) {
     const int row_tiles = (a.M + kRows - 1) / kRows;
     // batch-wide tensor scales run on the stream kernel: the maximum and the codes as two
     // launches (TENSOR) or the codes in one pass (STATIC)
-    const bool stream = a.act_scale != WQ_ACT_SCALE_ROW || quant_stream_schedule(a.M, a.num_sms);
+    const bool stream = a.act_scale != WQ_ACT_SCALE_ROW || a.vt != nullptr || quant_stream_schedule(a.M, a.num_sms);
     // the WQ_QUANT_SPLIT knob pins the CTAs per row tile of the cluster schedule (tuning and tests)
     {
         const int v = tune(kTuneQuantSplit);
@@ -810,6 +845,8 @@ cudaError_t launch_quantize_act(const QuantArgs& a, cudaStream_t st) {
     qp.amax_bits = a.amax_bits;
     qp.fp8 = a.fp8 ? 1 : 0;
     qp.fp8_bf16 = a.fp8_bf16 ? 1 : 0;
+    qp.vt = a.vt;
+    qp.r_real = a.r_real;
     qp.pfrag = a.pfrag; qp.u = a.u; qp.codes = a.codes; qp.sf = a.sf; qp.sf_layout = a.sf_layout; qp.g = a.g;
     qp.err = a.err;
     if (a.int8) {
@@ -832,6 +869,19 @@ cudaError_t launch_quantize_act(const QuantArgs& a, cudaStream_t st) {
             default: return cudaErrorInvalidValue;
         }
     };
+    if (a.vt != nullptr) {
+        // Q-WAM projected complement: U first (phase 1 without the maximum), then both passes on
+        // the projected values
+        if (a.r == 0 || a.u == nullptr || a.act_scale != WQ_ACT_SCALE_ROW) return cudaErrorInvalidValue;
+        QParams q1 = qp;
+        q1.phase = 1;
+        q1.amax_bits = nullptr;
+        const cudaError_t e = launch(q1);
+        if (e != cudaSuccess) return e;
+        QParams q2 = qp;
+        q2.phase = 6;
+        return launch(q2);
+    }
     if (a.act_scale == WQ_ACT_SCALE_TENSOR) {
         if (!a.amax_bits) return cudaErrorInvalidValue;
         QParams q1 = qp;
