@@ -534,8 +534,8 @@ def run_wq(args):
                 byts = quant8_algorithmic_bytes(M, spec.K, L.s is not None) if w8 else \
                     quant_algorithmic_bytes(M, spec.K, L.rank, L.omega.size, L.s is not None)
                 flops = 0.0
-                kern = ("quantize_stream_kernel" if wq.wq_quant_schedule(w, M) == wq.WQ_QUANT_STREAM
-                        else "quantize_kernel")
+                kern = {wq.WQ_QUANT_STREAM: "quantize_stream_kernel", wq.WQ_QUANT_RESIDENT: "quantize_resident_kernel"
+                        }.get(wq.wq_quant_schedule(w, M), "quantize_kernel")
             rl = kernel_roofline(flops, byts, ms, peaks)
             per_kernel.append(dict(name=f"{kname}[{spec.name}]", kernel=kern, ms=ms, bytes=byts, flops=flops,
                                    spread_us=[1e3 * min(times), 1e3 * max(times)], **rl))

@@ -187,6 +187,9 @@ WQ_API int wq_forward_path(wq_weights_t h, int M);
 
 #define WQ_QUANT_CLUSTER 0  /* a 16-row tile per cluster, K spread over its CTAs (few rows) */
 #define WQ_QUANT_STREAM 1   /* persistent CTAs streaming row tiles (at least 2 x SMs of them) */
+#define WQ_QUANT_RESIDENT 2 /* persistent CTAs keeping each row tile's transformed values in
+                               registers: 4-bit layers, per-row scales, K <= 1536 (the default
+                               for many rows there) */
 /*
  * Which activation-quantiser schedule M rows take (host query).  Returns a WQ_QUANT_* value,
  * or WQ_ERR_INVALID for a NULL handle or M < 0.
@@ -209,7 +212,9 @@ WQ_API int wq_gemm_schedule(wq_weights_t h, int M);
  * read once at the library's first use, and afterwards changes only through this call.
  *   "WQ_FUSED" 0/1; "WQ_GEMM_SPLIT" 0 (auto) or 1..16; "WQ_GEMM_WIDE" -1 (auto), 0, 1;
  *   "WQ_GEMM_PUSH" -1 (auto) or 0 (pull form); "WQ_GEMM_STAGES" 0 (auto) or a ring depth;
- *   "WQ_QUANT_SCHEDULE" -1 (auto), 0 (cluster), 1 (stream); "WQ_QUANT_SPLIT" 0 (auto) or 1..16;
+ *   "WQ_QUANT_SCHEDULE" -1 (auto), 0 (cluster), 1 (stream), 2 (register-resident where it applies,
+ *   else stream);
+ *   "WQ_QUANT_SPLIT" 0 (auto) or 1..16;
  *   "WQ_QUANT_CTAS_PER_SM" 0 (auto) or a count.
  * Process-wide; takes effect for launches issued after it returns.  Returns WQ_ERR_INVALID for an
  * unknown name.  wq_get_tuning returns the current value (or WQ_ERR_INVALID's value for an unknown name).

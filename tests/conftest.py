@@ -28,7 +28,7 @@ def tuning():
 
     def set_knob(name, value):
         if isinstance(value, str):
-            value = {"stream": 1, "cluster": 0}.get(value, None) if not value.lstrip("-").isdigit() else int(value)
+            value = {"stream": 1, "cluster": 0, "resident": 2}.get(value, None) if not value.lstrip("-").isdigit() else int(value)
         wq.wq_set_tuning(name, int(value))
         touched.append(name)
 

@@ -6,7 +6,9 @@ Bar (written here, derived in the design notes):
   * U = bf16(x P): within one bf16 ulp plus the fp32 summation bound K 2^-24 sum|x P|
     (fp32 vs fp64 accumulation before one rounding);
   * y: |y_gpu - y_oracle| <= 1e-3 (|y| + ||x_row|| ||w_col|| / sqrt(K)) + 2^-8 |y|
-    (fp32 accumulation vs fp64, plus the bf16 rounding of the output).
+    (fp32 accumulation vs fp64, plus the bf16 rounding of the output), plus, where the oracle's U
+    is at hand, U's bound above carried through Q (sum_j dU_j |Q_jn|): a U element within one
+    bf16 ulp of the oracle's moves y by that much.
 """
 import numpy as np
 import pytest
@@ -57,9 +59,26 @@ def y_tolerance(L, y_ref, rows=None):
     return 1e-3 * (np.abs(y_ref) + xn * wn / np.sqrt(L.spec.K)) + 2.0 ** -8 * np.abs(y_ref)
 
 
-def assert_y_close(L, y_gpu, y_ref, rows=None):
+def u_term(L, ref, rows=None):
+    """The part of y's bound that U's own bound (u_close: one bf16 ulp plus the fp32 summation
+    bound, fp32 on the device vs fp64 in the oracle) contributes through Q: sum_j dU[m, j] |Q[j, n]|."""
+    _, _, o, U = ref
+    if U is None or not L.rank:
+        return 0.0
+    xb = L.x_bits if rows is None else L.x_bits[rows]
+    b = np.abs(wl.bf16_from_bits(U).astype(np.float64))
+    absdot = np.abs(wl.bf16_from_bits(xb).astype(np.float64)) @ np.abs(wl.bf16_from_bits(o.P).astype(np.float64))
+    dU = np.maximum(b * 2.0 ** -7, 2.0 ** -133) + L.spec.K * 2.0 ** -24 * absdot
+    return dU @ np.abs(wl.bf16_from_bits(o.Q).astype(np.float64))
+
+
+def assert_y_close(L, y_gpu, y_ref, rows=None, ref=None):
+    """y within y_tolerance; with the oracle's full result `ref` (reference_forward's tuple) the
+    bound also carries U's bound through Q."""
     y = y_gpu.float().cpu().numpy().astype(np.float64)
     tol = y_tolerance(L, y_ref, rows)
+    if ref is not None:
+        tol = tol + u_term(L, ref, rows)
     err = np.abs(y - y_ref)
     bad = err > tol
     assert not bad.any(), (f"{bad.sum()} of {bad.size} outside tolerance; worst excess "
@@ -177,11 +196,12 @@ def test_activation_quant_split(case, split, tuning):
 
 
 @pytest.mark.parametrize("case", list(CASES))
-@pytest.mark.parametrize("schedule", ["stream", "cluster"])
+@pytest.mark.parametrize("schedule", ["stream", "cluster", "resident"])
 def test_activation_quant_schedules(case, schedule, tuning):
-    """Both quantiser schedules on every case: persistent CTAs that stream each row tile's
-    blocks twice (the second pass recomputes the transform) and clusters that keep the
-    transformed blocks resident."""
+    """Every quantiser schedule on every case: persistent CTAs that stream each row tile's
+    blocks twice (the second pass recomputes the transform), clusters that keep the transformed
+    blocks resident in shared memory, and persistent CTAs (clusters for a wide K) that keep each
+    row tile's transformed values in registers."""
     tuning("WQ_QUANT_SCHEDULE", schedule)
     L = layer(case)
     w = prep(L)
@@ -202,8 +222,9 @@ def test_forward_parity(case):
     w = prep(L)
     y = wq.wq_linear_forward(w, x_dev(L.x_bits))
     wq.wq_check_device_error(w)
-    y_ref, *_ = oracle.reference_forward(L)
-    assert_y_close(L, y, y_ref)
+    ref = oracle.reference_forward(L)
+    y_ref = ref[0]
+    assert_y_close(L, y, y_ref, ref=ref)
 
 
 @pytest.mark.parametrize("case", list(CASES))
@@ -221,8 +242,9 @@ def test_forward_parity_fused_and_two_kernel_paths(case, fused, tuning):
     assert wq.wq_forward_path(w, L.M) == expected
     y = wq.wq_linear_forward(w, x_dev(L.x_bits))
     wq.wq_check_device_error(w)
-    y_ref, *_ = oracle.reference_forward(L)
-    assert_y_close(L, y, y_ref)
+    ref = oracle.reference_forward(L)
+    y_ref = ref[0]
+    assert_y_close(L, y, y_ref, ref=ref)
 
 
 @pytest.mark.parametrize("case", list(CASES))
@@ -239,8 +261,9 @@ def test_forward_parity_gemm_schedules(case, wide, tuning):
     assert (sched == wq.WQ_GEMM_WIDE) == (wide == "1")
     y = wq.wq_linear_forward(w, x_dev(L.x_bits))
     wq.wq_check_device_error(w)
-    y_ref, *_ = oracle.reference_forward(L)
-    assert_y_close(L, y, y_ref)
+    ref = oracle.reference_forward(L)
+    y_ref = ref[0]
+    assert_y_close(L, y, y_ref, ref=ref)
 
 
 @pytest.mark.parametrize("case,split", [("expert_small", 1), ("expert_small", 2), ("expert_small", 4),
@@ -259,8 +282,9 @@ def test_forward_parity_split_k(case, split, push, tuning):
     w = prep(L)
     y = wq.wq_linear_forward(w, x_dev(L.x_bits))
     wq.wq_check_device_error(w)
-    y_ref, *_ = oracle.reference_forward(L)
-    assert_y_close(L, y, y_ref)
+    ref = oracle.reference_forward(L)
+    y_ref = ref[0]
+    assert_y_close(L, y, y_ref, ref=ref)
 
 
 def test_forward_is_deterministic_and_host_path_matches():
@@ -293,8 +317,9 @@ def test_zero_rows_and_empty_batch():
     _, _, g, _, _ = wq.wq_quantize_activations(w, x_dev(bits))
     torch.cuda.synchronize()
     assert g[3].item() == 0.0 and g[17].item() == 0.0
-    y_ref, *_ = oracle.reference_forward(L)
-    assert_y_close(L, y, y_ref)
+    ref = oracle.reference_forward(L)
+    y_ref = ref[0]
+    assert_y_close(L, y, y_ref, ref=ref)
     empty = torch.empty((0, 256), dtype=torch.bfloat16, device="cuda")
     y0 = wq.wq_linear_forward(w, empty)
     assert y0.shape == (0, 128)
@@ -401,8 +426,9 @@ def test_expert_batch1_full_size(layer_idx):
     w = prep(L)
     y = wq.wq_linear_forward(w, x_dev(L.x_bits))
     wq.wq_check_device_error(w)
-    y_ref, *_ = oracle.reference_forward(L)
-    assert_y_close(L, y, y_ref)
+    ref = oracle.reference_forward(L)
+    y_ref = ref[0]
+    assert_y_close(L, y, y_ref, ref=ref)
 
 
 @pytest.mark.parametrize("wl_name,layer_idx", [("video_dit", 0), ("video_dit", 1), ("video_dit", 2),
@@ -426,8 +452,9 @@ def test_full_size_every_row_and_tile(wl_name, layer_idx):
         got, pad = side_out(xo, L.omega.size)
         assert np.array_equal(got, aq.x_omega) and not pad.any()
     rows = _tile_rows(L.M, 100 + layer_idx)
-    y_ref, *_ = oracle.reference_forward(L, rows=rows)
-    assert_y_close(L, y[torch.from_numpy(rows).cuda()], y_ref, rows)
+    ref = oracle.reference_forward(L, rows=rows)
+    y_ref = ref[0]
+    assert_y_close(L, y[torch.from_numpy(rows).cuda()], y_ref, rows, ref=ref)
 
 
 @pytest.mark.parametrize("wide", ["1", "0"])
@@ -441,8 +468,9 @@ def test_full_size_long_k_both_gemm_schedules(wide, tuning):
     y = wq.wq_linear_forward(w, x_dev(L.x_bits))
     wq.wq_check_device_error(w)
     rows = _tile_rows(L.M, 300)
-    y_ref, *_ = oracle.reference_forward(L, rows=rows)
-    assert_y_close(L, y[torch.from_numpy(rows).cuda()], y_ref, rows)
+    ref = oracle.reference_forward(L, rows=rows)
+    y_ref = ref[0]
+    assert_y_close(L, y[torch.from_numpy(rows).cuda()], y_ref, rows, ref=ref)
 
 
 # ------------------------------------------------------------------ batch-wide tensor scales
@@ -596,3 +624,40 @@ def test_projected_complement_full_size(wl_name):
     w = prep(L, project=True)
     rows = _tile_rows(L.M, 31)
     check_projected(L, w, x_dev(L.x_bits), rows=rows, min_exact=0.85)
+
+
+# ------------------------------------------------------------------ register-resident quantiser
+@pytest.mark.parametrize("K,rank,n_omega", [(64, 16, 3), (192, 16, 5), (1088, 32, 64), (1536, 64, 16), (1536, 0, 0)])
+def test_resident_quant_shapes(K, rank, n_omega, tuning):
+    """The register-resident quantiser on its K range: one block, a pair and a lone block, 17 blocks
+    (nine warps, the last with a lone block), twelve pairs with rank 64 (P read from L2) and twelve
+    pairs without the branch; 72 rows (a ragged last tile).  Codes, scales, g and x_Omega
+    bit-exact; U within its bound."""
+    tuning("WQ_QUANT_SCHEDULE", "resident")
+    L = wl.make_layer_inputs("video_dit", M=72, K=K, N=128, rank=rank, n_omega=n_omega)
+    w = prep(L)
+    assert wq.wq_quant_schedule(w, L.M) == wq.WQ_QUANT_RESIDENT
+    x = x_dev(L.x_bits)
+    codes, scales, g, xo, u = wq.wq_quantize_activations(w, x, wq.WQ_SCALE_LAYOUT_ROWMAJOR)
+    torch.cuda.synchronize()
+    wq.wq_check_device_error(w)
+    aq = oq(L)
+    assert np.array_equal(g.cpu().numpy(), aq.g)
+    assert np.array_equal(scales.cpu().numpy(), aq.scales)
+    assert np.array_equal(codes.cpu().numpy(), aq.codes)
+    check_side(L, xo, u, aq)
+
+
+@pytest.mark.parametrize("case", list(CASES))
+def test_forward_parity_resident_quantiser(case, tuning):
+    """The whole forward with the register-resident quantiser feeding the GEMM (a case whose K is
+    wider than 1536 takes the stream schedule)."""
+    tuning("WQ_QUANT_SCHEDULE", "resident")
+    tuning("WQ_FUSED", "0")
+    L = layer(case)
+    w = prep(L)
+    y = wq.wq_linear_forward(w, x_dev(L.x_bits))
+    wq.wq_check_device_error(w)
+    ref = oracle.reference_forward(L)
+    y_ref = ref[0]
+    assert_y_close(L, y, y_ref, ref=ref)

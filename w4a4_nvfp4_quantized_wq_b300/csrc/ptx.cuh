@@ -91,6 +91,44 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
         }
     }
 }
+// Waits that sleep in the barrier (up to WQ_SLEEP_NS per try) instead of spinning, for kernels whose
+// waiting warps share the SM's issue slots with working ones.  kCluster: acquire at cluster scope
+// (arrivals by other CTAs of the cluster).
+#ifndef WQ_SLEEP_NS
+#define WQ_SLEEP_NS 20000u
+#endif
+template <bool kCluster>
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    if constexpr (kCluster)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok) : "r"(bar), "r"(parity), "r"(WQ_SLEEP_NS) : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok) : "r"(bar), "r"(parity), "r"(WQ_SLEEP_NS) : "memory");
+    return ok != 0;
+}
+template <bool kCluster>
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err,
+                                                int code) {
+    if (mbar_try_wait_sleep<kCluster>(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait_sleep<kCluster>(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > WQ_WAIT_NS) {
+            *abort_flag = 1;
+            if (err) atomicCAS(err, 0, code);
+            return false;
+        }
+    }
+}
 __device__ __forceinline__ void fence_proxy_async_all() { asm volatile("fence.proxy.async;" ::: "memory"); }
 
 // ------------------------------------------------------------------ TMA / bulk copies

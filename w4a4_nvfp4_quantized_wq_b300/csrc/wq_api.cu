@@ -140,8 +140,8 @@ void init_knobs() {
         for (int k = 0; k < kTuneCount; ++k) {
             int v = kKnobs[k].dflt;
             if (const char* e = std::getenv(kKnobs[k].name)) {
-                if (k == kTuneQuantSchedule && (e[0] == 's' || e[0] == 'c'))
-                    v = e[0] == 's' ? 1 : 0;
+                if (k == kTuneQuantSchedule && (e[0] == 's' || e[0] == 'c' || e[0] == 'r'))
+                    v = e[0] == 's' ? 1 : (e[0] == 'r' ? 2 : 0);
                 else if (e[0] != '\0')
                     v = std::atoi(e);
             }
@@ -214,6 +214,7 @@ struct wq_weights {
     uint8_t* d_sf = nullptr;       // MMA layout, ceil(N/128) * K/64 atoms
     float* d_bias = nullptr;       // [N]
     float* d_inv_s = nullptr;      // [K], quantiser pair order (see pair_order)
+    float* d_inv_s_rr = nullptr;   // [K], per 64-block the pairs (k, k + 32) (register-resident quantiser)
     uint32_t* d_omega_blk = nullptr;// [K/64][4]: Omega bit mask (2 words), index of its first channel, 0
     uint16_t* d_P = nullptr;       // [K, r] bf16
     uint32_t* d_Pfrag = nullptr;   // P in mma.sync m16n8k16 B-fragment order
@@ -288,6 +289,7 @@ void free_device(wq_weights* h) {
     cudaFree(h->d_sf);
     cudaFree(h->d_bias);
     cudaFree(h->d_inv_s);
+    cudaFree(h->d_inv_s_rr);
     cudaFree(h->d_omega_blk);
     cudaFree(h->d_P);
     cudaFree(h->d_Pfrag);
@@ -555,6 +557,9 @@ WQ_API wq_status wq_prepare_weights(const wq_config* cfg, const float* W, const 
     if ((st = upload(&h->d_sf, sf_mma.data(), sf_mma.size(), cs)) != WQ_OK) return bail(st);
     if (bias && (st = upload(&h->d_bias, bias_f.data(), N * 4, cs)) != WQ_OK) return bail(st);
     if (s && (st = upload(&h->d_inv_s, inv_s_pairs.data(), K * 4, cs)) != WQ_OK) return bail(st);
+    std::vector<float> inv_s_rr(s ? K : 0);
+    for (int k = 0; k < (s ? K : 0); ++k) inv_s_rr[k] = inv_s[(k / 64) * 64 + (k % 64) / 2 + 32 * (k % 2)];
+    if (s && (st = upload(&h->d_inv_s_rr, inv_s_rr.data(), K * 4, cs)) != WQ_OK) return bail(st);
     if (no && (st = upload(&h->d_omega_blk, omega_blk.data(), omega_blk.size() * 4, cs)) != WQ_OK) return bail(st);
     if (r && (st = upload(&h->d_P, P.data(), P.size() * 2, cs)) != WQ_OK) return bail(st);
     if (r && (st = upload(&h->d_Pfrag, Pfrag.data(), Pfrag.size() * 4, cs)) != WQ_OK) return bail(st);
@@ -722,6 +727,7 @@ static wq_status run_quant(wq_weights_t h, const void* x, int M, int layout, uin
     qa.M = M;
     qa.K = h->cfg.K;
     qa.inv_s = h->d_inv_s;
+    qa.inv_s_rr = h->d_inv_s_rr;
     qa.rotate = h->cfg.rotate | (h->cfg.rotate && h->cfg.transform_order == WQ_ORDER_ROTATE_SMOOTH ? 2 : 0);
     qa.omega_blk = h->d_omega_blk;
     qa.n_out = xo ? h->cfg.n_outliers : 0;
@@ -832,7 +838,15 @@ WQ_API int wq_quant_schedule(wq_weights_t h, int M) {
     if (M < 0) return fail(WQ_ERR_INVALID, "M < 0");
     // batch-wide tensor scales take the stream kernel (its two-launch and one-pass forms)
     if (h->cfg.act_scale != WQ_ACT_SCALE_ROW || h->cfg.project) return WQ_QUANT_STREAM;
-    return wq::quant_stream_schedule(M, h->num_sms) ? WQ_QUANT_STREAM : WQ_QUANT_CLUSTER;
+    if (!wq::quant_stream_schedule(M, h->num_sms)) return WQ_QUANT_CLUSTER;
+    wq::QuantArgs qa{};
+    qa.K = h->cfg.K;
+    qa.r = h->r_pad;
+    qa.int8 = h->cfg.mode != WQ_MODE_W4A4;
+    qa.inv_s = h->d_inv_s;
+    qa.inv_s_rr = h->d_inv_s_rr;
+    return wq::tune(wq::kTuneQuantSchedule) != 1 && wq::quant_resident_eligible(qa) ? WQ_QUANT_RESIDENT
+                                                                                    : WQ_QUANT_STREAM;
 }
 
 WQ_API int wq_gemm_schedule(wq_weights_t h, int M) {

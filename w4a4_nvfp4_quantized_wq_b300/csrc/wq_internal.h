@@ -55,6 +55,7 @@ struct QuantArgs {
     int* err;                       // device error flag
     int M, K;
     const float* inv_s;             // [K] or null; per 32-channel half, pairs (s_k, s_k+16), k = 0..15
+    const float* inv_s_rr = nullptr;// the same [K] with per 64-block the pairs (s_k, s_k+32), k = 0..31
     int rotate;
     const uint32_t* omega_blk;      // [K/64][4]: kept-channel mask (lo, hi), x_O index of the first, 0
     int n_out;                      // kept channels (0: none)
@@ -82,8 +83,12 @@ struct QuantArgs {
 };
 
 cudaError_t launch_quantize_act(const QuantArgs& a, cudaStream_t stream);
-// True when M rows take the persistent stream schedule (else the cluster schedule).
+// True when M rows take a persistent schedule (stream or register-resident; else the cluster
+// schedule).
 bool quant_stream_schedule(int M, int num_sms);
+// The register-resident schedule (wq_quant_rr.cu): 4-bit layers, per-row scales, K <= 1536.
+bool quant_resident_eligible(const QuantArgs& a);
+cudaError_t launch_quantize_resident(const QuantArgs& a, cudaStream_t stream);
 
 // The epilogue quantises the tile's bf16 output for the next layer instead of storing it
 // (wq_linear_forward_chain): the next layer's smoothing, block-64 FWHT along this layer's N, kept

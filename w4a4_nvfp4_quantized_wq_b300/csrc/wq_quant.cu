@@ -815,9 +815,10 @@ cudaError_t launch_r(const CUtensorMap& tm, const QParams& qp, bool stream, int 
 bool quant_stream_schedule(int M, int num_sms) {
     // many row tiles: the persistent stream schedule; few: spread K over clusters
     bool stream = (M + kRows - 1) / kRows >= 2 * num_sms;
-    // the WQ_QUANT_SCHEDULE knob pins the schedule (tuning and tests)
+    // the WQ_QUANT_SCHEDULE knob pins the schedule (tuning and tests): 0 cluster, 1 stream,
+    // 2 register-resident (where it applies; else stream)
     const int fm = tune(kTuneQuantSchedule);
-    if (fm >= 0) stream = fm == 1;
+    if (fm >= 0) stream = fm >= 1;
     return stream;
 }
 
@@ -835,6 +836,9 @@ cudaError_t launch_quantize_act(const QuantArgs& a, cudaStream_t st) {
         if (v >= 1 && v <= 16 && v <= nblk && (nblk + v - 1) / v <= kMaxBlocks) ch = Choice{v, (nblk + v - 1) / v};
     }
     if (ch.max_nb > kMaxBlocks) return cudaErrorInvalidValue;
+    // many rows of a 4-bit layer with per-row scales and K <= 1536: the register-resident schedule
+    // (knob value 1 pins the two-pass stream schedule instead)
+    if (stream && tune(kTuneQuantSchedule) != 1 && quant_resident_eligible(a)) return launch_quantize_resident(a, st);
     QParams qp{};
     qp.M = a.M; qp.K = a.K; qp.nblk = a.K / 64; qp.csplit = ch.csplit; qp.max_nb = ch.max_nb;
     qp.row_tiles = row_tiles;
