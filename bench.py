@@ -554,6 +554,11 @@ def run_wq(args):
                       "form": "tcgen05.mma.cta_group::2 kind::mxf4nvf4 M256 N256 K64, no scale copies"}
     except Exception as exc:  # reported, not hidden
         microbench = {"error": repr(exc)}
+    if "tflops" in microbench:
+        # each contraction's rate against the tensor pipe's measured FP4 issue rate as well
+        gemms = [k for k in per_kernel if k["flops"]]
+        microbench["frac_by_kernel"] = {k["name"]: k["flops"] / (k["ms"] / 1e3) / 1e12 / microbench["tflops"]
+                                        for k in gemms}
     roofline = {"kernel": f"{dom['name']} {dom['kernel']}", "bound": dom["bound"], "achieved": ach, "peak": peak,
                 "unit": unit, "frac": ach / peak,
                 "traffic": profiled_traffic(dom["kernel"], args.workload),

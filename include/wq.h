@@ -107,9 +107,9 @@ enum { WQ_ORDER_SMOOTH_ROTATE = 0, WQ_ORDER_ROTATE_SMOOTH = 1 };
  *     xt_c = xt - u Vt,   Vt[j][k] = bf16((H L1[:, j])[k] / ||L1[:, j]||^2)   (fp64, one rounding),
  * the complement of the span of L1 (the top-r left singular directions of diag(s) W) in the rotated
  * basis, one fp32 fma per rank term in the order j = 0 .. rank-1, before the kept-channel split.
- * The weights are unchanged: the complement R = W_s - L1 L2 already annihilates nothing of x's
- * complement and y = xt_c R' + u Q + x_O W_O + b equals the full activation's result up to the
- * quantisation.  Needs rank > 0, WQ_MODE_W4A4, WQ_ACT_SCALE_ROW and WQ_ORDER_SMOOTH_ROTATE; the
+ * The weights are unchanged: the complement R = W_s - L1 L2 has no component on the protected
+ * directions (U_r^T R = 0 for L1 = U_r S_r), so xt_c R' = xt R' and y = xt_c R' + u Q + x_O W_O + b
+ * equals the full activation's result up to the quantisation.  Needs rank > 0, WQ_MODE_W4A4, WQ_ACT_SCALE_ROW and WQ_ORDER_SMOOTH_ROTATE; the
  * quantiser then takes two launches (U, then both passes over the projected values). */
 typedef struct wq_config {
     int K;            /* input features (reduction dimension)                              */

@@ -661,3 +661,53 @@ def test_forward_parity_resident_quantiser(case, tuning):
     ref = oracle.reference_forward(L)
     y_ref = ref[0]
     assert_y_close(L, y, y_ref, ref=ref)
+
+
+# ------------------------------------------------------------------ exhaustive value sweep
+def _sweep_rows():
+    """Rows of K = 1024 whose first 16-block is [2688, 0, ...] (so g = amax / 2688 = 1) and whose
+    other 63 blocks each hold a maximum 6 dec(c) (so the block's e4m3 scale is exactly code c)
+    and 15 values from every finite bf16 value v with |v| <= 6 dec(c), for every scale code
+    c = 1 .. 126: each value meets each scale it can sit under."""
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    finite = bits[(bits & 0x7F80) != 0x7F80]
+    vals = wl.bf16_from_bits(finite).astype(np.float64)
+    e = np.arange(1, 127)
+    dec = np.where((e >> 3) == 0, (e & 7) * 2.0 ** -9, (1 + (e & 7) / 8) * 2.0 ** ((e >> 3) - 7))
+    blocks = []
+    for c, d in zip(e, dec):
+        bm = 6.0 * d
+        sel = finite[np.abs(vals) <= bm]
+        pad = (-sel.size) % 15
+        sel = np.concatenate([sel, np.zeros(pad, np.uint16)]).reshape(-1, 15)
+        head = np.full((sel.shape[0], 1), wl.bf16_bits(np.array([bm], np.float32))[0], np.uint16)
+        blocks.append(np.concatenate([head, sel], axis=1))
+    blocks = np.concatenate(blocks)                        # [n, 16]
+    nb = 63
+    blocks = np.concatenate([blocks, np.zeros(((-len(blocks)) % nb, 16), np.uint16)])
+    rows = blocks.reshape(-1, nb * 16)
+    first = np.zeros((rows.shape[0], 16), np.uint16)
+    first[:, 0] = wl.bf16_bits(np.array([2688.0], np.float32))[0]
+    return np.ascontiguousarray(np.concatenate([first, rows], axis=1))
+
+
+@pytest.mark.parametrize("schedule", ["stream", "cluster", "resident"])
+def test_every_bf16_value_under_every_scale(schedule, tuning):
+    """Every finite bf16 value quantised under every e4m3 block scale it can sit under (g = 1, no
+    smoothing, no rotation, no branches), through wq_quantize_activations on each schedule:
+    codes, scales and g bit-exact against the oracle."""
+    tuning("WQ_QUANT_SCHEDULE", schedule)
+    x_bits = _sweep_rows()
+    M, K = x_bits.shape
+    W = np.random.default_rng(11).standard_normal((K, 16)).astype(np.float32) * 0.02
+    w = wq.wq_prepare_weights(K, 16, W, rotate=False)
+    want = {"stream": wq.WQ_QUANT_STREAM, "cluster": wq.WQ_QUANT_CLUSTER, "resident": wq.WQ_QUANT_RESIDENT}[schedule]
+    assert wq.wq_quant_schedule(w, M) == want
+    codes, scales, g, _, _ = wq.wq_quantize_activations(w, x_dev(x_bits), wq.WQ_SCALE_LAYOUT_ROWMAJOR)
+    torch.cuda.synchronize()
+    wq.wq_check_device_error(w)
+    aq = oracle.quantize_act(x_bits, None, False, None)
+    assert np.all(aq.g == 1.0)
+    assert np.array_equal(g.cpu().numpy(), aq.g)
+    assert np.array_equal(scales.cpu().numpy(), aq.scales)
+    assert np.array_equal(codes.cpu().numpy(), aq.codes)

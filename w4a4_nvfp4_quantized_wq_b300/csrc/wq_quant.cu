@@ -1,4 +1,5 @@
-// wq_quant.cu -- fused activation transform + NVFP4 quantiser (x is read from HBM once).
+// wq_quant.cu -- fused activation transform + NVFP4 quantiser: the cluster and stream schedules
+// (the register-resident schedule for K <= 1536 is in wq_quant_rr.cu).
 //
 // Per activation row (FoldQuantVLA, Key Contribution 2: channel scaling, block Hadamard
 // via the FWHT with beta = 64, dynamic per-token quantisation; QuantWAMs sec. 3.1 Eq. (1):
