@@ -226,10 +226,14 @@ WQ_API int wq_get_tuning(const char *name);
 WQ_API size_t wq_host_workspace_bytes(wq_weights_t h, int M);
 
 /*
- * End-to-end variant over HOST buffers: copies x (host bf16 [M, K], preferably pinned)
- * to the device, runs wq_linear_forward, copies y back to host bf16 [M, N].  Both copies
- * and the kernels are enqueued on `stream`; y is valid after the stream synchronises.
- * workspace: device, at least wq_host_workspace_bytes(h, M) bytes.
+ * End-to-end variant over HOST buffers: copies x (host bf16 [M, K], pinned for the copies to
+ * overlap) to the device, runs wq_linear_forward, copies y back to host bf16 [M, N].  From
+ * M = 4096 rows the batch goes in up to eight row chunks whose uploads and downloads run on two
+ * copy streams of the handle, overlapping each other and the kernels; the uploads start after the
+ * work queued on `stream` before the call, and `stream` resumes only after the last download, so
+ * y is valid once `stream` synchronises (as for a single chunk, which uses `stream` alone).
+ * workspace: device, at least wq_host_workspace_bytes(h, M) bytes.  Calls that share a handle are
+ * serialised on the host while they enqueue.
  */
 WQ_API wq_status wq_linear_forward_host(wq_weights_t h, const void *x_host, int M, void *y_host,
                                         void *workspace, size_t workspace_bytes, void *stream);

@@ -306,6 +306,31 @@ def test_forward_is_deterministic_and_host_path_matches():
     assert torch.equal(y1.cpu(), yh)
 
 
+@pytest.mark.parametrize("M", [4100, 16384])
+def test_host_path_row_chunks(M):
+    """From 4096 rows the host-buffer path runs in row chunks with the uploads and downloads on the
+    handle's copy streams; on a side stream that alone is synchronised, y equals the device path
+    run on the same chunks, bit for bit, and the oracle on sampled rows within tolerance."""
+    L = wl.make_layer_inputs("video_dit", M=M, K=512, N=272, rank=32, n_omega=16)
+    w = prep(L)
+    x = x_dev(L.x_bits)
+    nch = max(1, min(8, M // 2048))
+    per = -(-(-(-M // nch)) // 256) * 256
+    y_dev = torch.cat([wq.wq_linear_forward(w, x[r0:r0 + per]) for r0 in range(0, M, per)])
+    xh = x.cpu().pin_memory()
+    yh = torch.zeros((M, L.spec.N), dtype=torch.bfloat16).pin_memory()
+    ws = torch.empty(wq.wq_host_workspace_bytes(w, M), dtype=torch.uint8, device="cuda")
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    wq.wq_linear_forward_host(w, xh, yh, ws, side)
+    side.synchronize()
+    wq.wq_check_device_error(w)
+    assert torch.equal(y_dev.cpu(), yh)
+    rows = _sampled_rows(M, 24, 7)
+    ref = oracle.reference_forward(L, rows=rows)
+    assert_y_close(L, yh[torch.from_numpy(rows)], ref[0], rows, ref=ref)
+
+
 def test_zero_rows_and_empty_batch():
     L = wl.make_layer_inputs("expert", M=40, K=256, N=128, rank=16)
     bits = L.x_bits.copy()

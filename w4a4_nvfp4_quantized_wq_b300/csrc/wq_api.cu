@@ -242,6 +242,10 @@ struct wq_weights {
     const void* key_x = nullptr;
     int key_xM = -1;
     CUtensorMap tmX{};
+    // host-buffer path: a copy stream each way and the events that order the row chunks
+    std::mutex mu_host;
+    cudaStream_t copy_in = nullptr, copy_out = nullptr;
+    std::vector<cudaEvent_t> host_events;
 };
 
 namespace wq {
@@ -300,6 +304,9 @@ void free_device(wq_weights* h) {
     cudaFree(h->d_amax);
     cudaFree(h->d_wexp);
     cudaFree(h->d_Vt);
+    if (h->copy_in) cudaStreamDestroy(h->copy_in);
+    if (h->copy_out) cudaStreamDestroy(h->copy_out);
+    for (cudaEvent_t e : h->host_events) cudaEventDestroy(e);
 }
 
 template <typename T>
@@ -1138,17 +1145,61 @@ WQ_API wq_status wq_linear_forward_host(wq_weights_t h, const void* x_host, int 
     if (workspace_bytes < wq_host_workspace_bytes(h, M)) return fail(WQ_ERR_INVALID, "workspace too small");
     if (const wq_status d = check_device(h)) return d;
     const size_t wsb = wq_workspace_bytes(h, M);
-    const size_t xb = static_cast<size_t>(M) * h->cfg.K * 2, yb = static_cast<size_t>(M) * h->cfg.N * 2;
+    const int K = h->cfg.K, N = h->cfg.N;
+    const size_t xb = static_cast<size_t>(M) * K * 2;
     uint8_t* base = static_cast<uint8_t*>(workspace);
-    void* dx = base + wsb;
-    void* dy = base + wsb + align_up(xb, 1024);
+    uint8_t* dx = base + wsb;
+    uint8_t* dy = base + wsb + align_up(xb, 1024);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    WQ_CUDA(cudaMemcpyAsync(dx, x_host, xb, cudaMemcpyHostToDevice, st), "x upload");
     const bool eight = h->cfg.mode == WQ_MODE_W8A8 || h->cfg.mode == WQ_MODE_W8A8_FP8;
-    const wq_status s = eight ? wq_linear_forward_w8a8(h, dx, M, dy, workspace, wsb, stream)
-                              : wq_linear_forward(h, dx, M, dy, workspace, wsb, stream);
-    if (s != WQ_OK) return s;
-    WQ_CUDA(cudaMemcpyAsync(y_host, dy, yb, cudaMemcpyDeviceToHost, st), "y download");
+    auto forward = [&](const void* xd, int rows, void* yd) {
+        const size_t w = wq_workspace_bytes(h, rows);
+        return eight ? wq_linear_forward_w8a8(h, xd, rows, yd, workspace, w, stream)
+                     : wq_linear_forward(h, xd, rows, yd, workspace, w, stream);
+    };
+    // Row chunks of at least 2048 rows (at most 8): chunk c's upload (copy_in), forward (`stream`)
+    // and download (copy_out) are ordered by events, so the copies of different chunks overlap
+    // each other and the kernels, in both directions at once.  The uploads start after the work
+    // queued on `stream` before this call, and `stream` resumes only after the last download.
+    const int nch = std::max(1, std::min(8, M / 2048));
+    if (nch == 1) {
+        WQ_CUDA(cudaMemcpyAsync(dx, x_host, xb, cudaMemcpyHostToDevice, st), "x upload");
+        const wq_status s = forward(dx, M, dy);
+        if (s != WQ_OK) return s;
+        WQ_CUDA(cudaMemcpyAsync(y_host, dy, static_cast<size_t>(M) * N * 2, cudaMemcpyDeviceToHost, st), "y download");
+        return WQ_OK;
+    }
+    const int rows_per = static_cast<int>(align_up(static_cast<size_t>((M + nch - 1) / nch), 256));
+    std::lock_guard<std::mutex> lk(h->mu_host);
+    if (!h->copy_in) WQ_CUDA(cudaStreamCreateWithFlags(&h->copy_in, cudaStreamNonBlocking), "copy stream");
+    if (!h->copy_out) WQ_CUDA(cudaStreamCreateWithFlags(&h->copy_out, cudaStreamNonBlocking), "copy stream");
+    while (h->host_events.size() < 2u * 8u + 2u) {
+        cudaEvent_t e;
+        WQ_CUDA(cudaEventCreateWithFlags(&e, cudaEventDisableTiming), "event");
+        h->host_events.push_back(e);
+    }
+    cudaEvent_t* ev = h->host_events.data();            // [0] start, [1] end, [2 + 2c] in, [3 + 2c] out
+    WQ_CUDA(cudaEventRecord(ev[0], st), "event");
+    WQ_CUDA(cudaStreamWaitEvent(h->copy_in, ev[0], 0), "event wait");
+    WQ_CUDA(cudaStreamWaitEvent(h->copy_out, ev[0], 0), "event wait");
+    const uint8_t* xh = static_cast<const uint8_t*>(x_host);
+    uint8_t* yh = static_cast<uint8_t*>(y_host);
+    for (int c = 0, r0 = 0; r0 < M; ++c, r0 += rows_per) {
+        const int rows = std::min(rows_per, M - r0);
+        const size_t xo = static_cast<size_t>(r0) * K * 2, yo = static_cast<size_t>(r0) * N * 2;
+        WQ_CUDA(cudaMemcpyAsync(dx + xo, xh + xo, static_cast<size_t>(rows) * K * 2, cudaMemcpyHostToDevice, h->copy_in),
+                "x upload");
+        WQ_CUDA(cudaEventRecord(ev[2 + 2 * c], h->copy_in), "event");
+        WQ_CUDA(cudaStreamWaitEvent(st, ev[2 + 2 * c], 0), "event wait");
+        const wq_status s = forward(dx + xo, rows, dy + yo);
+        if (s != WQ_OK) return s;
+        WQ_CUDA(cudaEventRecord(ev[3 + 2 * c], st), "event");
+        WQ_CUDA(cudaStreamWaitEvent(h->copy_out, ev[3 + 2 * c], 0), "event wait");
+        WQ_CUDA(cudaMemcpyAsync(yh + yo, dy + yo, static_cast<size_t>(rows) * N * 2, cudaMemcpyDeviceToHost, h->copy_out),
+                "y download");
+    }
+    WQ_CUDA(cudaEventRecord(ev[1], h->copy_out), "event");
+    WQ_CUDA(cudaStreamWaitEvent(st, ev[1], 0), "event wait");
     return WQ_OK;
 }
 
