@@ -275,17 +275,33 @@ __device__ __forceinline__ void nvfp4_half_codes(const f2 (&P)[16], float bma, f
     const float da = __fmul_rn(dec_e4m3(sa), gsc), db = __fmul_rn(dec_e4m3(sb), gsc);
     const float ra = __frcp_rn(da), rb = __frcp_rn(db);
     w[0] = w[1] = w[2] = w[3] = 0u;
-    if (ra < 3.0e38f && rb < 3.0e38f) {
-        // both blocks have a non-zero, non-tiny scale: packed path
+    uint32_t bad = (ra < 3.0e38f && rb < 3.0e38f) ? 0u : 1u;
+    if (!bad) {
+        // both blocks have a non-zero, non-tiny scale: every code from the bracket of e2m1_codes8_r,
+        // two blocks per packed multiply; a straddled bracket anywhere sends the half to the exact
+        // quotients below (one branch per half instead of one per pair)
         const f2 rr = pk2(ra, rb);
+        const f2 mlo = pk2(0.99999952316284180f, 0.99999952316284180f);
+        const f2 mhi = pk2(1.00000047683715820f, 1.00000047683715820f);
 #pragma unroll
-        for (int k = 0; k < 16; k += 2) {
-            uint32_t ca, cb;
-            codes_2x2<kOut>(P[k], P[k + 1], rr, da, db, ca, cb);
-            w[k / 8] |= ca << (8 * ((k / 2) % 4));
-            w[2 + k / 8] |= cb << (8 * ((k / 2) % 4));
+        for (int j = 0; j < 2; ++j) {
+            uint32_t lb[4], hb[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int k = 8 * j + 2 * e;
+                const f2 q0 = mul2(P[k], rr), q1 = mul2(P[k + 1], rr);
+                const f2 l0 = mul2(q0, mlo), l1 = mul2(q1, mlo), h0 = mul2(q0, mhi), h1 = mul2(q1, mhi);
+                const uint32_t alo = cvt_e2m1x2(lo2(l0), lo2(l1)), ahi = cvt_e2m1x2(lo2(h0), lo2(h1));
+                const uint32_t blo = cvt_e2m1x2(hi2(l0), hi2(l1)), bhi = cvt_e2m1x2(hi2(h0), hi2(h1));
+                bad |= (alo ^ ahi) | (blo ^ bhi);
+                lb[e] = alo;
+                hb[e] = blo;
+            }
+            w[j] = __byte_perm(__byte_perm(lb[0], lb[1], 0x0040), __byte_perm(lb[2], lb[3], 0x0040), 0x5410);
+            w[2 + j] = __byte_perm(__byte_perm(hb[0], hb[1], 0x0040), __byte_perm(hb[2], hb[3], 0x0040), 0x5410);
         }
-    } else {
+    }
+    if (bad) {
         float va[16], vb[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
