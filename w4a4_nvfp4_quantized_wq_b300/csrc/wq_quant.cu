@@ -80,7 +80,7 @@ constexpr int kMaxBlocks = 16;                          // blocks of one CTA (cl
 #define WQ_QUANT_RING 16
 #endif
 #ifndef WQ_QUANT_MINB
-#define WQ_QUANT_MINB 3
+#define WQ_QUANT_MINB 2
 #endif
 constexpr int kRing = WQ_QUANT_RING;                    // ring slots (stream schedule)
 constexpr unsigned kFullMask = 0xFFFFFFFFu;
@@ -783,9 +783,9 @@ cudaError_t launch_r(const CUtensorMap& tm, const QParams& qp, bool stream, int 
         if (e != cudaSuccess) return e;
         if (per_sm < 1) return cudaErrorInvalidConfiguration;
         // Every resident CTA is used even when the row tiles in flight outgrow the L2 and part of
-        // the second pass comes from DRAM: the kernel is latency-bound with DRAM well below its
-        // peak, so more warps per SM pay more than the extra reads cost (K = 8960: 383 us at two
-        // CTAs per SM, 339 us at three).
+        // the second pass comes from DRAM: the kernel is bound by its instructions with DRAM well
+        // below its peak.  Two CTAs per SM of up to 112 registers (no spills at rank 0 or 16)
+        // measured 323 us at K = 8960 against 332 us for three CTAs capped at 72 registers.
         // the WQ_QUANT_CTAS_PER_SM knob overrides the residency (tuning)
         const int v = tune(kTuneQuantCtasPerSm);
         if (v >= 1 && v <= per_sm + 8) per_sm = v;
