@@ -179,6 +179,21 @@ bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* bas
     return true;
 }
 
+bool encode_scale_tmap(CUtensorMap* map, const void* base, int rows, int K, int box_row_blocks, const char** why) {
+    EncodeTiledFn fn = get_encode_fn();
+    if (!fn) { *why = "cuTensorMapEncodeTiled unavailable"; return false; }
+    const uint64_t nkb = static_cast<uint64_t>(K / 64);
+    const cuuint64_t dims[3] = {kSfAtom / 4, nkb, static_cast<cuuint64_t>((rows + kBlockM - 1) / kBlockM)};
+    const cuuint64_t strides[2] = {kSfAtom, nkb * kSfAtom};
+    const cuuint32_t box[3] = {kSfAtom / 4, 4, static_cast<cuuint32_t>(box_row_blocks)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) { *why = "cuTensorMapEncodeTiled failed (scales)"; return false; }
+    return true;
+}
+
 ActWorkspace carve_workspace(void* base, int M, int K, int r, int n_out) {
     ActWorkspace w;
     const size_t m_pad = align_up(static_cast<size_t>(M), kBlockM);
@@ -230,14 +245,16 @@ struct wq_weights {
     int conv_cin = 0;              // Conv3d handles: input channels (K = 27 conv_cin)
     CUtensorMap tmBconv{};         // weight codes with 64-byte boxes (Conv3d, fused small-batch path)
     CUtensorMap tmB{}, tmQ{}, tmWO{};
+    CUtensorMap tmSFB{};           // weight scales in 4-K-block x 2-row-block boxes (CTA-pair GEMM)
     // activation / output tensor maps, re-encoded when the buffers change
     std::mutex mu;
     const void* key_codes = nullptr;
     const void* key_u = nullptr;
     const void* key_xo = nullptr;
     const void* key_y = nullptr;
+    const void* key_sf = nullptr;
     int key_M = -1;
-    CUtensorMap tmA{}, tmU{}, tmXO{}, tmY{};
+    CUtensorMap tmA{}, tmU{}, tmXO{}, tmY{}, tmSFA{};
     std::mutex mu_x;
     const void* key_x = nullptr;
     int key_xM = -1;
@@ -582,6 +599,7 @@ WQ_API wq_status wq_prepare_weights(const wq_config* cfg, const float* W, const 
     const char* why = "";
     if (!wq::encode_tmap_2d(&h->tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, h->d_codes, K / 2, N, K / 2, 128, 128,
                             CU_TENSOR_MAP_SWIZZLE_128B, &why) ||
+        !wq::encode_scale_tmap(&h->tmSFB, h->d_sf, N, K, 2, &why) ||
         !wq::encode_tmap_2d(&h->tmBconv, CU_TENSOR_MAP_DATA_TYPE_UINT8, h->d_codes, K / 2, N, K / 2, 64, 128,
                             CU_TENSOR_MAP_SWIZZLE_64B, &why))
         return bail(fail(WQ_ERR_CUDA, why));
@@ -786,7 +804,8 @@ static wq_status run_gemm(wq_weights_t h, const uint8_t* codes, const uint8_t* s
                           const wq::ChainArgs* chain = nullptr) {
     const int K = h->cfg.K, N = h->cfg.N, r = h->r_pad, no = h->no_pad, no_real = h->cfg.n_outliers;
     std::lock_guard<std::mutex> lk(h->mu);
-    if (h->key_codes != codes || h->key_u != u || h->key_xo != xo || h->key_y != y || h->key_M != M) {
+    if (h->key_codes != codes || h->key_u != u || h->key_xo != xo || h->key_y != y || h->key_sf != sf ||
+        h->key_M != M) {
         const char* why = "";
         const bool w8 = h->cfg.mode == WQ_MODE_W8A8 || h->cfg.mode == WQ_MODE_W4A8, f8 = h->cfg.mode == WQ_MODE_W8A8_FP8;
         bool ok = (w8 ? wq::encode_tmap_2d(&h->tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, codes, K, M, 2ull * K, 64, 128,
@@ -797,6 +816,7 @@ static wq_status run_gemm(wq_weights_t h, const uint8_t* codes, const uint8_t* s
                                                 CU_TENSOR_MAP_SWIZZLE_128B, &why)) &&
                   wq::encode_tmap_2d(&h->tmY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, y, N, M, 2ull * N, 64, 32,
                                      CU_TENSOR_MAP_SWIZZLE_128B, &why);
+        if (ok && !w8 && !f8) ok = wq::encode_scale_tmap(&h->tmSFA, sf, M, K, 1, &why);
         if (ok && r)
             ok = wq::encode_tmap_2d(&h->tmU, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, u, r, M, 2 * r, r, 128,
                                     swizzle_for_row_bytes(2 * r), &why);
@@ -812,12 +832,14 @@ static wq_status run_gemm(wq_weights_t h, const uint8_t* codes, const uint8_t* s
         h->key_u = u;
         h->key_xo = xo;
         h->key_y = y;
+        h->key_sf = sf;
         h->key_M = M;
     }
     wq::GemmArgs ga{};
     ga.M = M; ga.N = N; ga.K = K; ga.r = r; ga.n_out = no;
     ga.tmA = &h->tmA; ga.tmB = &h->tmB; ga.tmU = &h->tmU; ga.tmQ = &h->tmQ;
     ga.tmXO = &h->tmXO; ga.tmWO = &h->tmWO; ga.tmY = &h->tmY;
+    ga.tmSFA = &h->tmSFA; ga.tmSFB = &h->tmSFB;
     ga.sfa = sf; ga.sfb = h->d_sf; ga.gA = g; ga.gW = h->gW; ga.bias = h->d_bias;
     ga.err = h->d_err; ga.num_sms = h->num_sms;
     ga.y = y;

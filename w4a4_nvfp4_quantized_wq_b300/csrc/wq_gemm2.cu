@@ -9,15 +9,17 @@
 //             scale atoms and all 256 rows' B scale atoms (each CTA's TMEM needs the whole
 //             tile's B scales), into an S-stage ring; after the K stages of a tile, the side
 //             operands (U with this CTA's Q^T rows; x_O with its W_O^T rows) as extra stages.
+//             Both CTAs' copies complete rank 0's barriers directly (cta_group::2 TMA): one
+//             barrier per stage for the scale atoms, issued first, and one for the operand
+//             tiles, so the scales can go to TMEM while the tiles are still landing.
 //   warp 1    rank 0: TMEM (collective over the pair) and the single MMA-issuing thread: the
-//             pair MMAs of a stage once its scales are in TMEM; their completion frees the
-//             stage in both CTAs (multicast commit).  rank 1: relays "stage full" of its own
-//             ring to rank 0's barrier, since an mbarrier can only be waited on in its own CTA.
-//   warp 10   rank 0: the scale feeder.  Once both CTAs' halves of a stage have landed it
-//             issues the stage's tcgen05.cp.cta_group::2 copies of the scale atoms (each CTA
-//             copies its own shared memory into its own TMEM) and commits them to the stage's
-//             "scales ready" barrier.  A tcgen05.cp issued by the MMA thread itself stalls its
-//             MMA stream (~60-90 ns per copy on B300); from another warp it costs the MMAs nothing.
+//             pair MMAs of a stage once its tiles have landed and its scales are in TMEM; their
+//             completion frees the stage in both CTAs (multicast commit).
+//   warp 10   rank 0: the scale feeder.  Once both CTAs' scale atoms of a stage have landed it
+//             issues the stage's tcgen05.cp.cta_group::2 copies (each CTA copies its own shared
+//             memory into its own TMEM) and commits them to the stage's "scales ready" barrier.
+//             A tcgen05.cp issued by the MMA thread itself stalls its MMA stream (~60-90 ns per
+//             copy on B300); from another warp it costs the MMAs nothing.
 //   warps 2-9 epilogue: two warps per TMEM lane quadrant, 128 columns each.  The 256-column
 //             accumulator fills TMEM's first half (the other half holds five stages of scale
 //             factors), so it is single-buffered: the epilogue drains it into registers and
@@ -60,6 +62,7 @@ constexpr int kScaleWarp = 10;
 constexpr uint32_t kHalf = 128 * 128;                   // 128 rows x 128 bytes
 constexpr uint32_t kSfaOff = 2 * kHalf;                 // 4 A atoms (this CTA's rows)
 constexpr uint32_t kSfbOff = kSfaOff + 4 * kSfAtom;     // 4 atoms of B rows 0..127, then 4 of 128..255
+constexpr uint32_t kSfStage = 12 * kSfAtom;             // one CTA's scale boxes of a stage (fixed: 4 K blocks)
 constexpr uint32_t kStage4 = kSfbOff + 8 * kSfAtom;     // 38 KiB, a multiple of 1 KiB
 constexpr uint32_t kStage8 = 2 * kHalf;
 constexpr uint32_t kSideB = 16384;                      // offset of the B-side operand in a side stage
@@ -73,10 +76,7 @@ constexpr int kMaxStages = 5;                           // 256 + 5 x 48 <= 512 T
 struct WParams {
     int M, N, K, r, n_out, stages;
     int num_kb, num_kt;
-    int nrb_a, nrb_b;        // 128-row atom blocks of the activation / weight scales
     uint32_t off_y, off_bar;
-    const uint8_t* sfa;
-    const uint8_t* sfb;
     const float* gA;
     float gW;
     const float* bias;
@@ -190,7 +190,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 wide_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmQ,
                  const __grid_constant__ CUtensorMap tmXO, const __grid_constant__ CUtensorMap tmWO,
-                 const __grid_constant__ CUtensorMap tmY, const WParams p) {
+                 const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmSFA,
+                 const __grid_constant__ CUtensorMap tmSFB, const WParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -201,8 +202,8 @@ wide_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     const uint32_t rank = cluster_ctarank();
     const int S = p.stages;
     const uint32_t bar_full = base + p.off_bar;
-    const uint32_t bar_pfull = bar_full + 8u * S;        // rank 0: the peer's stage is full
-    const uint32_t bar_empty = bar_pfull + 8u * S;
+    const uint32_t bar_scf = bar_full + 8u * S;          // rank 0: both CTAs' scale atoms of the stage landed
+    const uint32_t bar_empty = bar_scf + 8u * S;
     const uint32_t bar_tfull = bar_empty + 8u * S;
     const uint32_t bar_tempty = bar_tfull + 8u;          // rank 0: both epilogues drained the accumulator
     const uint32_t bar_sfull = bar_tempty + 8u;
@@ -224,7 +225,7 @@ wide_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(bar_full + 8u * s, 1);
-            mbar_init(bar_pfull + 8u * s, 1);
+            mbar_init(bar_scf + 8u * s, 1);
             mbar_init(bar_empty + 8u * s, 1);
         }
         mbar_init(bar_tfull, 1);
@@ -240,6 +241,10 @@ wide_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        if (!kW8) {
+            tma_prefetch_desc(&tmSFA);
+            tma_prefetch_desc(&tmSFB);
+        }
         if (!p.chain) tma_prefetch_desc(&tmY);
     }
     if (warp == 1) {
@@ -256,13 +261,15 @@ wide_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer (each CTA)
         if (lane == 0) {
+            // rank 0's barriers as cluster addresses: both CTAs' copies complete them, and rank 0
+            // alone arms them with the pair's byte counts
+            const uint32_t full0 = mapa_shared(bar_full, 0), scf0 = mapa_shared(bar_scf, 0);
+            const bool lead = rank == 0;
             uint32_t q = 0;
             bool ok = true, dep = false;
             for (int tile = pair; ok && tile < tiles; tile += npairs) {
                 const int mb = tile / nnt, nb = tile % nnt;
                 const int mrow = mb * 256 + static_cast<int>(rank) * 128, nrow = nb * 256 + static_cast<int>(rank) * 128;
-                const int ra = min(mb * 2 + static_cast<int>(rank), p.nrb_a - 1);
-                const int rb0 = min(nb * 2, p.nrb_b - 1), rb1 = min(nb * 2 + 1, p.nrb_b - 1);
                 for (int kt = 0; kt < num_kt + side_stages; ++kt, ++q) {
                     const uint32_t s = q % static_cast<uint32_t>(S);
                     WT_T0(tw0);
@@ -272,42 +279,44 @@ wide_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                         break;
                     }
                     WT_ADD(0, tw0);
-                    const uint32_t sA = base + s * SB, fb = bar_full + 8u * s;
+                    const uint32_t sA = base + s * SB, fb = full0 + 8u * s, sb = scf0 + 8u * s;
                     if (kt < num_kt) {
                         if (kW8) {
                             const int x0 = kt * (p.fp8 ? 128 : 64);     // 128-byte rows either way
-                            mbar_arrive_expect_tx(fb, 2 * kHalf);
-                            tma_load_2d(sA + kHalf, &tmB, x0, nrow, fb);
+                            if (lead) mbar_arrive_expect_tx(bar_full + 8u * s, 4 * kHalf);
+                            tma_load_2d_pair(sA + kHalf, &tmB, x0, nrow, fb);
                             if (!dep) { griddep_wait(); dep = true; }
-                            tma_load_2d(sA, &tmA, x0, mrow, fb);
+                            tma_load_2d_pair(sA, &tmA, x0, mrow, fb);
                         } else {
-                            const int kb0 = kt * 4, nkb = min(4, p.num_kb - kb0);
-                            mbar_arrive_expect_tx(fb, 2 * kHalf + 3u * nkb * kSfAtom);
-                            tma_load_2d(sA + kHalf, &tmB, kt * 128, nrow, fb);
-                            bulk_load(sA + kSfbOff, p.sfb + (static_cast<size_t>(rb0) * p.num_kb + kb0) * kSfAtom,
-                                      nkb * kSfAtom, fb);
-                            bulk_load(sA + kSfbOff + 4 * kSfAtom, p.sfb + (static_cast<size_t>(rb1) * p.num_kb + kb0) * kSfAtom,
-                                      nkb * kSfAtom, fb);
+                            // scale boxes first (4 K blocks each; blocks past K and rows past M or N
+                            // read as zeros), the weight side before the wait on the previous grid
+                            const int kb0 = kt * 4;
+                            if (lead) {
+                                mbar_arrive_expect_tx(bar_scf + 8u * s, 2 * kSfStage);
+                                mbar_arrive_expect_tx(bar_full + 8u * s, 4 * kHalf);
+                            }
+                            tma_load_3d_pair(sA + kSfbOff, &tmSFB, 0, kb0, 2 * nb, sb);
+                            tma_load_2d_pair(sA + kHalf, &tmB, kt * 128, nrow, fb);
                             if (!dep) { griddep_wait(); dep = true; }
-                            tma_load_2d(sA, &tmA, kt * 128, mrow, fb);
-                            bulk_load(sA + kSfaOff, p.sfa + (static_cast<size_t>(ra) * p.num_kb + kb0) * kSfAtom,
-                                      nkb * kSfAtom, fb);
+                            tma_load_3d_pair(sA + kSfaOff, &tmSFA, 0, kb0, 2 * mb + static_cast<int>(rank), sb);
+                            tma_load_2d_pair(sA, &tmA, kt * 128, mrow, fb);
                         }
-                    } else if (kt == num_kt && p.r > 0) {
-                        mbar_arrive_expect_tx(fb, 512u * p.r);
-                        tma_load_2d(sA, &tmU, 0, mrow, fb);
-                        tma_load_2d(sA + kSideB, &tmQ, 0, nrow, fb);
                     } else {
-                        mbar_arrive_expect_tx(fb, 512u * p.n_out);
-                        tma_load_2d(sA, &tmXO, 0, mrow, fb);
-                        tma_load_2d(sA + kSideB, &tmWO, 0, nrow, fb);
+                        const bool lowrank = kt == num_kt && p.r > 0;
+                        if (lead) {
+                            mbar_arrive_expect_tx(bar_full + 8u * s, 1024u * static_cast<uint32_t>(lowrank ? p.r : p.n_out));
+                            if (!kW8) mbar_arrive(bar_scf + 8u * s);      // no scales: the phase still turns
+                        }
+                        tma_load_2d_pair(sA, lowrank ? &tmU : &tmXO, 0, mrow, fb);
+                        tma_load_2d_pair(sA + kSideB, lowrank ? &tmQ : &tmWO, 0, nrow, fb);
                     }
                 }
             }
-            // never leave with copies still landing in shared memory
+            // never leave with copies still landing in shared memory: a stage is released (in both
+            // CTAs) only after the MMAs that read it, which waited for its bytes
             const uint32_t first = q > static_cast<uint32_t>(S) ? q - S : 0u;
             for (uint32_t t = first; t < q; ++t)
-                mbar_wait(bar_full + 8u * (t % S), (t / S) & 1u, abort_flag, p.err, 32);
+                mbar_wait(bar_empty + 8u * (t % S), (t / S) & 1u, abort_flag, p.err, 32);
         }
     } else if (warp == kScaleWarp) {
         // ------------------------------------------------------------ rank 0: scale feeder
@@ -320,9 +329,8 @@ wide_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 for (int kt = 0; kt < num_kt + side_stages; ++kt, ++q) {
                     const uint32_t s = q % static_cast<uint32_t>(S), ph = (q / S) & 1u;
                     // the stage's MMAs of S uses ago completed before the producer refilled it,
-                    // so the stage's TMEM slot is free once its data has landed
-                    if (!mbar_wait(bar_full + 8u * s, ph, abort_flag, p.err, 43) ||
-                        !mbar_wait(bar_pfull + 8u * s, ph, abort_flag, p.err, 44)) { ok = false; break; }
+                    // so the stage's TMEM slot is free once its scale atoms have landed
+                    if (!mbar_wait(bar_scf + 8u * s, ph, abort_flag, p.err, 43)) { ok = false; break; }
                     if (kt < num_kt) {
                         const uint32_t sA = base + s * SB;
                         const int nkb = min(4, p.num_kb - kt * 4);
@@ -343,20 +351,7 @@ wide_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             mbar_wait(bar_sfinal, 0, abort_flag, p.err, 46);
         }
     } else if (warp == 1) {
-        if (lane == 0 && rank != 0) {
-            // ------------------------------------------------------------ rank 1: relay
-            const uint32_t pfull0 = mapa_shared(bar_pfull, 0);
-            uint32_t q = 0;
-            bool ok = true;
-            for (int tile = pair; ok && tile < tiles; tile += npairs)
-                for (int kt = 0; kt < num_kt + side_stages; ++kt, ++q) {
-                    const uint32_t s = q % static_cast<uint32_t>(S);
-                    WT_T0(tw0);
-                    if (!mbar_wait(bar_full + 8u * s, (q / S) & 1u, abort_flag, p.err, 33)) { ok = false; break; }
-                    WT_ADD(1, tw0);
-                    mbar_arrive_cluster(pfull0 + 8u * s);
-                }
-        } else if (lane == 0) {
+        if (lane == 0 && rank == 0) {
             // ------------------------------------------------------------ rank 0: MMA issuer
             const uint32_t mn = ((256u >> 3) << 17) | ((256u >> 4) << 24);   // M = 256 (pair), N = 256
             const uint32_t idesc_fp4 = (1u << 7) | (1u << 10) | mn;
@@ -381,9 +376,6 @@ wide_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     WT_T0(tw1);
                     if (!mbar_wait(bar_full + 8u * s, ph, abort_flag, p.err, 35)) { ok = false; break; }
                     WT_ADD(3, tw1);
-                    WT_T0(tw2);
-                    if (!mbar_wait(bar_pfull + 8u * s, ph, abort_flag, p.err, 36)) { ok = false; break; }
-                    WT_ADD(4, tw2);
                     // (TMA-filled stages need no tcgen05 fence: the mbarrier completion orders them)
                     const uint32_t sA = base + s * SB;
                     const uint64_t ad = smem_desc(sA, 16, 1024, 2), bd = smem_desc(sA + kHalf, 16, 1024, 2);
@@ -420,8 +412,7 @@ wide_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     uint32_t acc = 0;
                     for (int st = 0; st < side_stages; ++st, ++q) {
                         const uint32_t s = q % static_cast<uint32_t>(S), ph = (q / S) & 1u;
-                        if (!mbar_wait(bar_full + 8u * s, ph, abort_flag, p.err, 38) ||
-                            !mbar_wait(bar_pfull + 8u * s, ph, abort_flag, p.err, 39)) { ok = false; break; }
+                        if (!mbar_wait(bar_full + 8u * s, ph, abort_flag, p.err, 38)) { ok = false; break; }
                         const uint32_t sA = base + s * SB;
                         const bool lowrank = st == 0 && p.r > 0;
                         const uint32_t rb = 2u * static_cast<uint32_t>(lowrank ? p.r : p.n_out);
@@ -616,11 +607,10 @@ cudaError_t launch_gemm_wide(const GemmArgs& a, cudaStream_t st) {
     p.num_kb = a.K / 64;
     p.num_kt = w8 ? (a.fp8 ? (p.num_kb + 1) / 2 : a.K / 64) : (p.num_kb + 3) / 4;
     p.fp8 = a.fp8 ? 1 : 0;
-    p.nrb_a = (a.M + 127) / 128;
-    p.nrb_b = (a.N + 127) / 128;
     p.off_y = static_cast<uint32_t>(S) * SB;
     p.off_bar = p.off_y + kYBytes;
-    p.sfa = a.sfa; p.sfb = a.sfb; p.gA = a.gA; p.gW = a.gW; p.bias = a.bias; p.colscale = a.colscale;
+    if (!w8 && (a.tmSFA == nullptr || a.tmSFB == nullptr)) return cudaErrorInvalidValue;
+    p.gA = a.gA; p.gW = a.gW; p.bias = a.bias; p.colscale = a.colscale;
     p.err = a.err;
     if (a.chain != nullptr) {
         if (w8 || (a.N % 64) != 0) return cudaErrorInvalidValue;
@@ -653,10 +643,14 @@ cudaError_t launch_gemm_wide(const GemmArgs& a, cudaStream_t st) {
     at[1].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 2;
+    // the 8-bit layers carry no scale boxes: any map fills the unused parameters
+    const CUtensorMap& sfa = w8 ? *a.tmA : *a.tmSFA;
+    const CUtensorMap& sfb = w8 ? *a.tmB : *a.tmSFB;
     if (w8)
         return cudaLaunchKernelEx(&cfg, wide_gemm_kernel<true>, *a.tmA, *a.tmB, *a.tmU, *a.tmQ, *a.tmXO, *a.tmWO,
-                                  *a.tmY, p);
-    return cudaLaunchKernelEx(&cfg, wide_gemm_kernel<false>, *a.tmA, *a.tmB, *a.tmU, *a.tmQ, *a.tmXO, *a.tmWO, *a.tmY, p);
+                                  *a.tmY, sfa, sfb, p);
+    return cudaLaunchKernelEx(&cfg, wide_gemm_kernel<false>, *a.tmA, *a.tmB, *a.tmU, *a.tmQ, *a.tmXO, *a.tmWO, *a.tmY,
+                              sfa, sfb, p);
 }
 
 }  // namespace wq

@@ -114,6 +114,10 @@ struct GemmArgs {
     const CUtensorMap* tmXO;  // x_O    [M, n_out] fp16, box n_out x 128
     const CUtensorMap* tmWO;  // W_O^T  [N, n_out] fp16, box n_out x 128
     const CUtensorMap* tmY;   // y      [M, N]     bf16, box 64 x 32, swizzle 128B
+    // the scales as [128-row blocks][K/64 blocks][128 u32] (one 512-byte atom per row block and
+    // K block), boxes of 4 K blocks x 1 (activations) or 2 (weights) row blocks; CTA-pair schedule
+    const CUtensorMap* tmSFA = nullptr;
+    const CUtensorMap* tmSFB = nullptr;
     const uint8_t* sfa;       // activation scales, MMA layout
     const uint8_t* sfb;       // weight scales, MMA layout
     const float* gA;          // [M]
@@ -188,5 +192,8 @@ int handle_device(wq_weights_t h);
 bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
                     uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
                     CUtensorMapSwizzle swizzle, const char** why);
+// The MMA-layout scales of `rows` rows and K columns as a 3-D map: [row blocks][K/64][128 u32],
+// boxes of 4 K blocks x box_row_blocks row blocks (out-of-range atoms read as zeros).
+bool encode_scale_tmap(CUtensorMap* map, const void* base, int rows, int K, int box_row_blocks, const char** why);
 
 }  // namespace wq
