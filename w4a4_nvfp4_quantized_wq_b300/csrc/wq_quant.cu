@@ -314,8 +314,10 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmX, const QParams p) {
     const uint32_t bar_full = base + lay.off_bar;
     const uint32_t bar_const = bar_full + 8u * static_cast<uint32_t>(p.max_nb);
     const uint32_t s_invs = base + lay.off_invs;
-    const uint32_t* s_omega = reinterpret_cast<const uint32_t*>(base_ptr + lay.off_omega);
-    float* s_amax = reinterpret_cast<float*>(base_ptr + lay.off_amax);
+    // shared-space accesses only (ld/st.shared): a generic access can wait behind the thread's
+    // outstanding global stores
+    const uint32_t s_omega = base + lay.off_omega;
+    const uint32_t s_amax = base + lay.off_amax;
     float* s_rmax = reinterpret_cast<float*>(base_ptr + lay.off_rmax);
     float* s_u = reinterpret_cast<float*>(base_ptr + lay.off_u);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + lay.off_abort);
@@ -394,20 +396,36 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmX, const QParams p) {
 #pragma unroll
         for (int j = 0; j < 8; ++j)
             st_shared_v4f(rowb + 16u * j, lo2(P[2 * j]), hi2(P[2 * j]), lo2(P[2 * j + 1]), hi2(P[2 * j + 1]));
-        const uint32_t m0 = p.n_out ? s_omega[4 * i] : 0u, m1 = p.n_out ? s_omega[4 * i + 1] : 0u;
+        const uint32_t m0 = p.n_out ? ld_shared_u32(s_omega + 16u * i) : 0u;
+        const uint32_t m1 = p.n_out ? ld_shared_u32(s_omega + 16u * i + 4u) : 0u;
         const uint32_t mine = half ? m1 : m0;
-        if (mine != 0u) {
-            // kept channels: fp16 value out and +0 in the slot (channel e of the half is float
-            // 2 (e % 16) + e / 16 of the stored row-half), +0 in the registers
-            uint32_t idx = s_omega[4 * i + 2] + (half ? static_cast<uint32_t>(__popc(m0)) : 0u);
-            uint16_t* xrow = p.xo + static_cast<size_t>(row) * p.xo_ld;
-            for (uint32_t m = mine; m != 0u; m &= m - 1u, ++idx) {
-                const uint32_t e = static_cast<uint32_t>(__ffs(m) - 1);
-                const uint32_t a = rowb + 4u * (2u * (e & 15u) + (e >> 4));
-                if (row_ok) xrow[idx] = __half_as_ushort(__float2half_rn(ld_shared_f32(a)));
-                st_shared_f32(a, 0.0f);
+        if ((m0 | m1) != 0u) {
+            // kept channels out by the whole warp from the stored rows (channel e of a row half is
+            // float 2 (e % 16) + e / 16 of it): lane l takes channel l of each half for the 16
+            // rows, fp16 value out and +0 in the slot; +0 in the registers
+            __syncwarp();
+            const uint32_t below = (1u << lane) - 1u;
+            const bool k0 = (m0 >> lane) & 1u, k1 = (m1 >> lane) & 1u;
+            const uint32_t first = ld_shared_u32(s_omega + 16u * i + 8u);
+            const uint32_t i0 = first + static_cast<uint32_t>(__popc(m0 & below));
+            const uint32_t i1 = first + static_cast<uint32_t>(__popc(m0) + __popc(m1 & below));
+            const uint32_t ce = slot + kF32Off + 4u * (2u * (static_cast<uint32_t>(lane) & 15u) + (static_cast<uint32_t>(lane) >> 4));
+            if (k0 || k1) {
+#pragma unroll 4
+                for (int rr = 0; rr < kRows; ++rr) {
+                    const int rw = tile * kRows + rr;
+                    const uint32_t a0 = ce + static_cast<uint32_t>(rr) * kRowBytes, a1 = a0 + 128u;
+                    const float v0 = k0 ? ld_shared_f32(a0) : 0.0f, v1 = k1 ? ld_shared_f32(a1) : 0.0f;
+                    if (k0) st_shared_f32(a0, 0.0f);
+                    if (k1) st_shared_f32(a1, 0.0f);
+                    if (rw < p.M) {
+                        uint16_t* xr = p.xo + static_cast<size_t>(rw) * p.xo_ld;
+                        if (k0) xr[i0] = __half_as_ushort(__float2half_rn(v0));
+                        if (k1) xr[i1] = __half_as_ushort(__float2half_rn(v1));
+                    }
+                }
             }
-            apply_keep(P, mine);
+            if (mine != 0u) apply_keep(P, mine);
         }
         float ma, mb;
         absmax_pairs(P, ma, mb);
@@ -420,10 +438,10 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmX, const QParams p) {
     if (threadIdx.x == 0) WQ_QTRACE_AT(3);
     if (rank == 0) zero_xo_pad(p, tile, threadIdx.x, kConsumerWarps * 32);
     amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 16));
-    if (half == 0) s_amax[warp * kRows + r] = amax;
+    if (half == 0) st_shared_f32(s_amax + 4u * static_cast<uint32_t>(warp * kRows + r), amax);
     named_bar_sync(1, kConsumerWarps * 32);
     amax = 0.0f;
-    for (int w = 0; w < active; ++w) amax = fmaxf(amax, s_amax[w * kRows + r]);
+    for (int w = 0; w < active; ++w) amax = fmaxf(amax, ld_shared_f32(s_amax + 4u * static_cast<uint32_t>(w * kRows + r)));
     if constexpr (R > 0) {
         for (int idx = threadIdx.x; idx < NT * 128; idx += kConsumerWarps * 32) {
             float sum = 0.0f;
@@ -431,7 +449,7 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmX, const QParams p) {
             int rr, cc;
             frag_pos(idx, rr, cc);
             if (clustered) {
-                s_u[rr * R + cc] = sum;
+                st_shared_f32(smem_u32(s_u + rr * R + cc), sum);
             } else {
                 const int rg = tile * kRows + rr;
                 if (rg < p.M) p.u[static_cast<size_t>(rg) * R + cc] = __bfloat16_as_ushort(__float2bfloat16_rn(sum));
@@ -439,7 +457,7 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmX, const QParams p) {
         }
     }
     if (clustered) {
-        if (warp == 0 && half == 0) s_rmax[r] = amax;
+        if (warp == 0 && half == 0) st_shared_f32(smem_u32(s_rmax + r), amax);
         cluster_arrive();
         cluster_wait();
         // all peers' values are requested before any is used, so the remote reads overlap
@@ -533,8 +551,10 @@ quantize_stream_kernel(const __grid_constant__ CUtensorMap tmX, const QParams p)
     const uint32_t bar_empty = bar_full + 8u * kRing;
     const uint32_t bar_const = bar_empty + 8u * kRing;
     const uint32_t s_invs = base + lay.off_invs;
-    const uint32_t* s_omega = reinterpret_cast<const uint32_t*>(base_ptr + lay.off_omega);
-    float* s_amax = reinterpret_cast<float*>(base_ptr + lay.off_amax);
+    // shared-space accesses only (ld/st.shared): a generic access can wait behind the thread's
+    // outstanding global stores
+    const uint32_t s_omega = base + lay.off_omega;
+    const uint32_t s_amax = base + lay.off_amax;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + lay.off_abort);
     const int nblk = p.nblk;
 
@@ -607,7 +627,6 @@ quantize_stream_kernel(const __grid_constant__ CUtensorMap tmX, const QParams p)
     for (int tile = blockIdx.x; tile < p.row_tiles; tile += gridDim.x) {
         const int row = tile * kRows + r;
         const bool row_ok = row < p.M;
-        uint16_t* xrow = p.xo + static_cast<size_t>(row) * p.xo_ld;
         float gsc = g_fixed;
         float rg_inv = __frcp_rn(g_fixed);
         if (first_pass) {
@@ -632,10 +651,13 @@ quantize_stream_kernel(const __grid_constant__ CUtensorMap tmX, const QParams p)
                     else u_step<NT>(box, lane, kb, p.pfrag, upart, kb == warp);
                 }
                 QPH(2);
-                const uint32_t m0 = p.n_out ? s_omega[4 * kb] : 0u, m1 = p.n_out ? s_omega[4 * kb + 1] : 0u;
+                const uint32_t m0 = p.n_out ? ld_shared_u32(s_omega + 16u * kb) : 0u;
+                const uint32_t m1 = p.n_out ? ld_shared_u32(s_omega + 16u * kb + 4u) : 0u;
                 if ((m0 | m1) != 0u) {
-                    // kept channels: fp16 values out through a copy in the consumed box (lane l
-                    // writes its 32 channels as fp16 pairs at l * 64 B), +0 in the registers
+                    // kept channels: fp16 values through a copy in the consumed box (lane l writes its
+                    // 32 channels as fp16 pairs at l * 64 B), then out by the whole warp: lane l takes
+                    // channel l of each half for the 16 rows, so a block with many kept channels
+                    // costs a few row sweeps and a row's stores are contiguous; +0 in the registers
                     __syncwarp();                  // every lane is done reading the box
                     const uint32_t sc = box + static_cast<uint32_t>(lane) * 64u;
 #pragma unroll
@@ -649,15 +671,31 @@ quantize_stream_kernel(const __grid_constant__ CUtensorMap tmX, const QParams p)
                         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(sc + 16u * j), "r"(hw[0]), "r"(hw[1]),
                                      "r"(hw[2]), "r"(hw[3]) : "memory");
                     }
-                    const uint32_t mine = half ? m1 : m0;
-                    uint32_t idx = s_omega[4 * kb + 2] + (half ? static_cast<uint32_t>(__popc(m0)) : 0u);
-                    for (uint32_t m = mine; m != 0u; m &= m - 1u, ++idx) {
-                        const uint32_t e = static_cast<uint32_t>(__ffs(m) - 1);
-                        uint16_t hv;
-                        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(hv) : "r"(sc + 4u * (e & 15u) + 2u * (e >> 4)) : "memory");
-                        if (row_ok) xrow[idx] = hv;
+                    __syncwarp();
+                    const uint32_t below = (1u << lane) - 1u;
+                    const bool k0 = (m0 >> lane) & 1u, k1 = (m1 >> lane) & 1u;
+                    const uint32_t first = ld_shared_u32(s_omega + 16u * kb + 8u);
+                    const uint32_t i0 = first + static_cast<uint32_t>(__popc(m0 & below));
+                    const uint32_t i1 = first + static_cast<uint32_t>(__popc(m0) + __popc(m1 & below));
+                    // channel e of a row half sits at 4 (e % 16) + 2 (e / 16) of that lane's copy
+                    const uint32_t ce = 4u * (static_cast<uint32_t>(lane) & 15u) + 2u * (static_cast<uint32_t>(lane) >> 4);
+                    if (k0 || k1) {
+#pragma unroll 4
+                        for (int rr = 0; rr < kRows; ++rr) {
+                            const int rw = tile * kRows + rr;
+                            uint16_t h0 = 0, h1 = 0;
+                            if (k0) asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h0) : "r"(box + static_cast<uint32_t>(rr) * 64u + ce) : "memory");
+                            if (k1) asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h1) : "r"(box + static_cast<uint32_t>(rr + 16) * 64u + ce) : "memory");
+                            if (rw < p.M) {
+                                uint16_t* xr = p.xo + static_cast<size_t>(rw) * p.xo_ld;
+                                if (k0) xr[i0] = h0;
+                                if (k1) xr[i1] = h1;
+                            }
+                        }
                     }
+                    const uint32_t mine = half ? m1 : m0;
                     if (mine != 0u) apply_keep(P, mine);
+                    fence_proxy_async_smem();      // the copy precedes the producer's next TMA into the slot
                 }
                 float ma, mb;
                 absmax_pairs(P, ma, mb);
@@ -670,10 +708,11 @@ quantize_stream_kernel(const __grid_constant__ CUtensorMap tmX, const QParams p)
             QPH(3);
             // ---- row amax and U over the warps, in warp order
             amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 16));
-            if (half == 0) s_amax[warp * kRows + r] = amax;
+            if (half == 0) st_shared_f32(s_amax + 4u * static_cast<uint32_t>(warp * kRows + r), amax);
             named_bar_sync(1, kConsumerWarps * 32);
             amax = 0.0f;
-            for (int w = 0; w < active; ++w) amax = fmaxf(amax, s_amax[w * kRows + r]);
+            for (int w = 0; w < active; ++w)
+                amax = fmaxf(amax, ld_shared_f32(s_amax + 4u * static_cast<uint32_t>(w * kRows + r)));
             if constexpr (R > 0) {
                 for (int idx = threadIdx.x; idx < (project ? 0 : NT * 128); idx += kConsumerWarps * 32) {
                     float sum = 0.0f;
@@ -712,8 +751,8 @@ quantize_stream_kernel(const __grid_constant__ CUtensorMap tmX, const QParams p)
                 if (lane == 0) mbar_arrive(bar_empty + 8u * s);
                 if (project) project_block<R>(P, p, row, row_ok, kb, half);
                 QPH(6);
-                const uint32_t m0 = p.n_out ? s_omega[4 * kb] : 0u, m1 = p.n_out ? s_omega[4 * kb + 1] : 0u;
-                if ((half ? m1 : m0) != 0u) apply_keep(P, half ? m1 : m0);
+                const uint32_t mk = p.n_out ? ld_shared_u32(s_omega + 16u * kb + 4u * static_cast<uint32_t>(half)) : 0u;
+                if (mk != 0u) apply_keep(P, mk);
                 if constexpr (kInt8) {
                     if (p.fp8) emit_fp8(P, gsc, rg_inv, row, row_ok, kb, half, p);
                     else emit_int8<false>(P, gsc, rg_inv, row, row_ok, kb, half, p);

@@ -36,6 +36,24 @@
 #include "quant_math.cuh"
 #include "wq_internal.h"
 
+#ifdef WQ_TRACE
+// Per-phase cycle counters for kernel development builds only (never defined in the product build).
+__device__ unsigned long long g_wq_rtrace[16];
+extern "C" WQ_API int wq_rtrace_read(void* host, size_t bytes) {
+    return static_cast<int>(cudaMemcpyFromSymbol(host, g_wq_rtrace, bytes));
+}
+#define RT_DECL unsigned long long rt_acc[8] = {0, 0, 0, 0, 0, 0, 0, 0}; long long rt_t = clock64(), rt_n = 0
+#define RT(i) do { const long long t_ = clock64(); rt_acc[i] += static_cast<unsigned long long>(t_ - rt_t); rt_t = t_; } while (0)
+#define RT_TILE() (++rt_n)
+#define RT_FLUSH() do { if (lane == 0) { for (int i_ = 0; i_ < 8; ++i_) atomicAdd(&g_wq_rtrace[i_], rt_acc[i_]); \
+                                           atomicAdd(&g_wq_rtrace[8], static_cast<unsigned long long>(rt_n)); } } while (0)
+#else
+#define RT_DECL
+#define RT(i) ((void)0)
+#define RT_TILE() ((void)0)
+#define RT_FLUSH() ((void)0)
+#endif
+
 namespace wq {
 namespace {
 
@@ -254,7 +272,7 @@ __global__ void __maxnreg__(144) quantize_resident_kernel(const __grid_constant_
     const RLayout lay = make_rlayout(p.W, R, p.p_smem != 0);
     const uint32_t bar_full = base + lay.off_bar;
     const uint32_t bar_const = bar_full + 8u * static_cast<uint32_t>(p.W);
-    const uint32_t* s_omega = reinterpret_cast<const uint32_t*>(base_ptr + lay.off_omega);
+    const uint32_t s_omega = base + lay.off_omega;     // shared-space accesses only (ld/st.shared)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + lay.off_abort);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int nb = p.nblk;                                   // the CTA owns every block
@@ -303,23 +321,27 @@ __global__ void __maxnreg__(144) quantize_resident_kernel(const __grid_constant_
     }
     bool ok = __all_sync(kRMask, mbar_wait_sleep<false>(bar_const, 0, abort_flag, p.err, 44));
     int issued = static_cast<int>(blockIdx.x) < p.row_tiles ? 0 : -1;  // iteration of the last load issued
-    const uint32_t m0 = (p.n_out && blk_ok) ? s_omega[4 * kb] : 0u;
-    const uint32_t m1 = (p.n_out && blk_ok) ? s_omega[4 * kb + 1] : 0u;
-    const uint32_t xo_first = (p.n_out && blk_ok) ? s_omega[4 * kb + 2] : 0u;
+    const uint32_t m0 = (p.n_out && blk_ok) ? ld_shared_u32(s_omega + 16u * kb) : 0u;
+    const uint32_t m1 = (p.n_out && blk_ok) ? ld_shared_u32(s_omega + 16u * kb + 4u) : 0u;
 
     int it = 0;
+    RT_DECL;
     for (int tile = blockIdx.x; tile < p.row_tiles; tile += gridDim.x, ++it) {
+        RT(7);
+        RT_TILE();
         const int row = tile * kRTile + r;
         const bool row_ok = row < p.M;
         const uint32_t par = static_cast<uint32_t>(it) & 1u;
         const uint32_t upart_t = base + lay.off_upart + par * upart_stride;     // this tile's partials
-        float* s_amax = reinterpret_cast<float*>(base_ptr + lay.off_amax) + par * (kRTile * p.W);
+        const uint32_t s_amax = base + lay.off_amax + par * static_cast<uint32_t>(4 * kRTile * p.W);
         f2 V[32];
         float bm[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         // ---- pass 1
         if (ok) ok = __all_sync(kRMask, mbar_wait_sleep<false>(bar_full + 8u * warp, par, abort_flag, p.err, 45));
+        RT(0);
         if (ok) {
             if constexpr (R > 0) u_pair<NT>(slot, lane, nblocks, p, kb0, pf_s, upart_t + static_cast<uint32_t>(warp * NT) * 512u);
+            RT(1);
             if (blk_ok) {
                 load_row64(box, r, V);
                 if (invs != 0u && !after) smooth64(V, invs);
@@ -328,8 +350,9 @@ __global__ void __maxnreg__(144) quantize_resident_kernel(const __grid_constant_
                     if (invs != 0u && after) smooth64(V, invs);
                 }
                 if ((m0 | m1) != 0u) {
-                    // kept channels: the row's fp16 values through its own (consumed) row of the
-                    // box, pair k at 4 k, then out by channel index; +0 in the registers
+                    // kept channels: the row's fp16 values into its own (consumed) row of the box,
+                    // pair k in 16-byte chunk k / 4 swizzled by the row (chunk ^ r % 8), for the
+                    // warp's copy-out below; +0 in the registers
                     const uint32_t rb = box + static_cast<uint32_t>(r) * 128u;
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
@@ -339,23 +362,11 @@ __global__ void __maxnreg__(144) quantize_resident_kernel(const __grid_constant_
                             const __half2 h2 = __floats2half2_rn(lo2(V[4 * j + t]), hi2(V[4 * j + t]));
                             hw[t] = *reinterpret_cast<const uint32_t*>(&h2);
                         }
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(rb + 16u * j), "r"(hw[0]),
-                                     "r"(hw[1]), "r"(hw[2]), "r"(hw[3]) : "memory");
-                    }
-                    uint16_t* xrow = p.xo + static_cast<size_t>(row) * p.xo_ld;
-                    uint32_t idx = xo_first;
-                    for (uint32_t m = m0; m != 0u; m &= m - 1u, ++idx) {
-                        uint16_t hv;
-                        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(hv) : "r"(rb + 4u * static_cast<uint32_t>(__ffs(m) - 1)) : "memory");
-                        if (row_ok) xrow[idx] = hv;
-                    }
-                    for (uint32_t m = m1; m != 0u; m &= m - 1u, ++idx) {
-                        uint16_t hv;
-                        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(hv) : "r"(rb + 4u * static_cast<uint32_t>(__ffs(m) - 1) + 2u) : "memory");
-                        if (row_ok) xrow[idx] = hv;
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                                     :: "r"(rb + 16u * (static_cast<uint32_t>(j) ^ (static_cast<uint32_t>(r) & 7u))),
+                                        "r"(hw[0]), "r"(hw[1]), "r"(hw[2]), "r"(hw[3]) : "memory");
                     }
                     keep64(V, m0, m1);
-                    fence_proxy_async_smem();   // these writes precede the next tile's TMA into the slot
                 }
 #pragma unroll
                 for (int k = 0; k < 16; ++k) {
@@ -365,6 +376,40 @@ __global__ void __maxnreg__(144) quantize_resident_kernel(const __grid_constant_
                     bm[3] = fmaxf(bm[3], fabsf(hi2(V[16 + k])));
                 }
             }
+            if (p.n_out) {
+                // the kept channels of the pair's blocks out to x_O by the whole warp: lane l takes
+                // channels l and l + 32 of a block (the pair at 4 l of each row) for its 16 rows,
+                // so a block with many kept channels costs its warp a few row sweeps and the
+                // stores of a row are contiguous
+                __syncwarp();
+                bool wrote = false;
+                for (int bb = 0; bb < nblocks; ++bb) {
+                    const uint32_t om = s_omega + 16u * static_cast<uint32_t>(kb0 + bb);
+                    const uint32_t mb0 = ld_shared_u32(om), mb1 = ld_shared_u32(om + 4u);
+                    if ((mb0 | mb1) == 0u) continue;
+                    wrote = true;
+                    const uint32_t below = (1u << lane) - 1u;
+                    const bool k0 = (mb0 >> lane) & 1u, k1 = (mb1 >> lane) & 1u;
+                    const uint32_t i0 = ld_shared_u32(om + 8u) + static_cast<uint32_t>(__popc(mb0 & below));
+                    const uint32_t i1 = ld_shared_u32(om + 8u) + static_cast<uint32_t>(__popc(mb0) + __popc(mb1 & below));
+                    const uint32_t bx = slot + static_cast<uint32_t>(bb) * kRBox + 4u * (static_cast<uint32_t>(lane) & 3u);
+                    if (k0 || k1) {
+#pragma unroll 4
+                        for (int rr = 0; rr < kRTile; ++rr) {
+                            const int rw = tile * kRTile + rr;
+                            const uint32_t a = bx + static_cast<uint32_t>(rr) * 128u +
+                                               16u * ((static_cast<uint32_t>(lane) >> 2) ^ (static_cast<uint32_t>(rr) & 7u));
+                            const uint32_t hv = ld_shared_u32(a);
+                            if (rw < p.M) {
+                                uint16_t* xr = p.xo + static_cast<size_t>(rw) * p.xo_ld;
+                                if (k0) xr[i0] = static_cast<uint16_t>(hv & 0xFFFFu);
+                                if (k1) xr[i1] = static_cast<uint16_t>(hv >> 16);
+                            }
+                        }
+                    }
+                }
+                if (wrote) fence_proxy_async_smem();   // the scratch precedes the next tile's TMA into the slot
+            }
             __syncwarp();                 // the slot is read: the next tile's boxes may land in it
             if (lane == 0 && tile + static_cast<int>(gridDim.x) < p.row_tiles) load_tile(tile + gridDim.x);
             if (tile + static_cast<int>(gridDim.x) < p.row_tiles) issued = it + 1;
@@ -372,10 +417,21 @@ __global__ void __maxnreg__(144) quantize_resident_kernel(const __grid_constant_
         // ---- exchange: the row maximum and U over the warps (warp order)
         float amax = fmaxf(fmaxf(bm[0], bm[1]), fmaxf(bm[2], bm[3]));
         amax = fmaxf(amax, __shfl_xor_sync(kRMask, amax, 16));
-        if (b == 0) s_amax[warp * kRTile + r] = amax;
+        if (b == 0) st_shared_f32(s_amax + 4u * static_cast<uint32_t>(warp * kRTile + r), amax);
+        RT(2);
         named_bar_sync(1, nthr);
+        RT(3);
         amax = 0.0f;
-        for (int w = 0; w < p.W; ++w) amax = fmaxf(amax, s_amax[w * kRTile + r]);
+        {
+            // every warp's maximum of the row requested before any is used
+            float wm[kMaxPairs];
+#pragma unroll
+            for (int w = 0; w < kMaxPairs; ++w)
+                wm[w] = w < p.W ? ld_shared_f32(s_amax + 4u * static_cast<uint32_t>(w * kRTile + r)) : 0.0f;
+#pragma unroll
+            for (int w = 0; w < kMaxPairs; ++w) amax = fmaxf(amax, wm[w]);
+        }
+        RT(6);
         if constexpr (R > 0) {
             // groups of four U sums (row rr, columns cc0 .. cc0 + 3), spread over the warps
             for (int gi = (threadIdx.x % 32) * p.W + warp; gi < 4 * R; gi += nthr) {
@@ -399,8 +455,10 @@ __global__ void __maxnreg__(144) quantize_resident_kernel(const __grid_constant_
                 }
             }
         }
+        RT(4);
         const float gsc = __fdiv_rn(amax, 2688.0f);
         const float rg_inv = __frcp_rn(gsc);
+        RT(7);
         if (warp == 0 && b == 0 && row_ok) p.g[row] = gsc;
         if (p.n_out && p.xo_ld > p.n_out) {
             // x_O's columns beyond the kept channels are zero
@@ -428,7 +486,9 @@ __global__ void __maxnreg__(144) quantize_resident_kernel(const __grid_constant_
                 *reinterpret_cast<uint32_t*>(p.sf + off) = scales;
             }
         }
+        RT(5);
     }
+    RT_FLUSH();
     // every copy this warp issued has landed before the CTA can finish
     if (issued >= 0) mbar_wait_sleep<false>(bar_full + 8u * warp, static_cast<uint32_t>(issued) & 1u, abort_flag, p.err, 47);
 }
