@@ -433,25 +433,24 @@ __global__ void __maxnreg__(144) quantize_resident_kernel(const __grid_constant_
         }
         RT(6);
         if constexpr (R > 0) {
-            // groups of four U sums (row rr, columns cc0 .. cc0 + 3), spread over the warps
-            for (int gi = (threadIdx.x % 32) * p.W + warp; gi < 4 * R; gi += nthr) {
-                const int rr = gi / (R / 4), cc0 = 4 * (gi % (R / 4));
-                const uint32_t i0 = 4u * ((static_cast<uint32_t>(cc0 / 8) * 32u + static_cast<uint32_t>((rr % 8) * 4 + (cc0 % 8) / 2)) * 4u +
-                                          static_cast<uint32_t>((rr / 8) * 2));
-                float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
-                for (int w = 0; w < p.W; ++w) {
-                    const uint32_t a = upart_t + static_cast<uint32_t>(w * NT) * 512u + i0;
-                    const float2 v01 = ld_shared_v2f(a), v23 = ld_shared_v2f(a + 16u);
-                    s0 = __fadd_rn(s0, v01.x);
-                    s1 = __fadd_rn(s1, v01.y);
-                    s2 = __fadd_rn(s2, v23.x);
-                    s3 = __fadd_rn(s3, v23.y);
-                }
+            // pairs of U sums (row rr, columns cc and cc + 1) over the CTA's threads, each summed
+            // over the warps' partials in warp order
+            for (int pi = static_cast<int>(threadIdx.x); pi < NT * 64; pi += nthr) {
+                const uint32_t off = 8u * static_cast<uint32_t>(pi);
+                float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+                for (int w = 0; w < kMaxPairs; ++w)
+                    if (w < p.W) {
+                        const float2 v = ld_shared_v2f(upart_t + static_cast<uint32_t>(w * NT) * 512u + off);
+                        s0 = __fadd_rn(s0, v.x);
+                        s1 = __fadd_rn(s1, v.y);
+                    }
+                int rr, cc;
+                frag_pos(2 * pi, rr, cc);
                 const int rg = tile * kRTile + rr;
                 if (rg < p.M) {
-                    const __nv_bfloat162 lo = __floats2bfloat162_rn(s0, s1), hi = __floats2bfloat162_rn(s2, s3);
-                    *reinterpret_cast<uint2*>(p.u + static_cast<size_t>(rg) * R + cc0) =
-                        make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+                    const __nv_bfloat162 h = __floats2bfloat162_rn(s0, s1);
+                    *reinterpret_cast<uint32_t*>(p.u + static_cast<size_t>(rg) * R + cc) = *reinterpret_cast<const uint32_t*>(&h);
                 }
             }
         }
