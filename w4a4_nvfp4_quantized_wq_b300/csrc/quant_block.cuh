@@ -231,40 +231,69 @@ __device__ __forceinline__ void u_frags(uint32_t box, int lane, uint32_t (&a)[4]
     }
     __syncwarp();                          // the box is read before a partial may land on it
 }
-__device__ __forceinline__ void u_tile(const uint32_t (&a)[4][4], uint4 q0, uint4 q1, uint32_t ua, bool first) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    mma_bf16_16816(acc, a[0][0], a[0][1], a[0][2], a[0][3], q0.x, q0.y);
-    mma_bf16_16816(acc, a[1][0], a[1][1], a[1][2], a[1][3], q0.z, q0.w);
-    mma_bf16_16816(acc, a[2][0], a[2][1], a[2][2], a[2][3], q1.x, q1.y);
-    mma_bf16_16816(acc, a[3][0], a[3][1], a[3][2], a[3][3], q1.z, q1.w);
+// Up to four n-tiles of one block at once: the tensor-core chains of different n-tiles are
+// independent, so they are issued interleaved (k-step outer, n-tile inner) in one basic block;
+// each chain still runs its four k-steps in order from zero.  Then the warp's partial of each
+// n-tile is written (first block) or read, added to and written back.
+template <int NG>
+__device__ __forceinline__ void u_group(const uint32_t (&a)[4][4], const uint4 (&q)[NG][2], uint32_t ua0, bool first) {
+    float t[NG][4];
+#pragma unroll
+    for (int g = 0; g < NG; ++g) t[g][0] = t[g][1] = t[g][2] = t[g][3] = 0.0f;
+#pragma unroll
+    for (int f = 0; f < 4; ++f)
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+            const uint4& qq = q[g][f >> 1];
+            mma_bf16_16816(t[g], a[f][0], a[f][1], a[f][2], a[f][3], (f & 1) ? qq.z : qq.x, (f & 1) ? qq.w : qq.y);
+        }
     if (first) {
-        st_shared_v4f(ua, acc[0], acc[1], acc[2], acc[3]);
+#pragma unroll
+        for (int g = 0; g < NG; ++g) st_shared_v4f(ua0 + static_cast<uint32_t>(g) * 512u, t[g][0], t[g][1], t[g][2], t[g][3]);
     } else {
-        const float4 o = ld_shared_v4f(ua);
-        st_shared_v4f(ua, __fadd_rn(o.x, acc[0]), __fadd_rn(o.y, acc[1]), __fadd_rn(o.z, acc[2]), __fadd_rn(o.w, acc[3]));
+        float4 o[NG];
+#pragma unroll
+        for (int g = 0; g < NG; ++g) o[g] = ld_shared_v4f(ua0 + static_cast<uint32_t>(g) * 512u);
+#pragma unroll
+        for (int g = 0; g < NG; ++g)
+            st_shared_v4f(ua0 + static_cast<uint32_t>(g) * 512u, __fadd_rn(o[g].x, t[g][0]), __fadd_rn(o[g].y, t[g][1]),
+                          __fadd_rn(o[g].z, t[g][2]), __fadd_rn(o[g].w, t[g][3]));
     }
 }
 // P fragments from global memory (block kb of the whole table).
 template <int NT>
 __device__ __forceinline__ void u_step(uint32_t box, int lane, int kb, const uint32_t* pfrag, uint32_t upart, bool first) {
+    constexpr int NG = NT < 4 ? NT : 4;
     uint32_t a[4][4];
     u_frags(box, lane, a);
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        const uint4* pb = reinterpret_cast<const uint4*>(pfrag + (static_cast<size_t>(kb * NT + nt) * 32 + lane) * 8);
-        u_tile(a, __ldg(pb), __ldg(pb + 1), upart + (static_cast<uint32_t>(nt) * 32u + lane) * 16u, first);
+    for (int n0 = 0; n0 < NT; n0 += NG) {
+        uint4 q[NG][2];
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+            const uint4* pb = reinterpret_cast<const uint4*>(pfrag + (static_cast<size_t>(kb * NT + n0 + g) * 32 + lane) * 8);
+            q[g][0] = __ldg(pb);
+            q[g][1] = __ldg(pb + 1);
+        }
+        u_group<NG>(a, q, upart + (static_cast<uint32_t>(n0) * 32u + lane) * 16u, first);
     }
 }
 // P fragments of one block staged in shared memory at `pf` (NT x 32 lanes x 32 bytes).
 template <int NT>
 __device__ __forceinline__ void u_step_smem(uint32_t box, int lane, uint32_t pf, uint32_t upart, bool first) {
+    constexpr int NG = NT < 4 ? NT : 4;
     uint32_t a[4][4];
     u_frags(box, lane, a);
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        const uint32_t pb = pf + (static_cast<uint32_t>(nt) * 32u + lane) * 32u;
-        const uint4 q0 = ld_shared_v4(pb), q1 = ld_shared_v4(pb + 16u);
-        u_tile(a, q0, q1, upart + (static_cast<uint32_t>(nt) * 32u + lane) * 16u, first);
+    for (int n0 = 0; n0 < NT; n0 += NG) {
+        uint4 q[NG][2];
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+            const uint32_t pb = pf + (static_cast<uint32_t>(n0 + g) * 32u + lane) * 32u;
+            q[g][0] = ld_shared_v4(pb);
+            q[g][1] = ld_shared_v4(pb + 16u);
+        }
+        u_group<NG>(a, q, upart + (static_cast<uint32_t>(n0) * 32u + lane) * 16u, first);
     }
 }
 

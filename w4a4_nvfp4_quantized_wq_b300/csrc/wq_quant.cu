@@ -643,14 +643,16 @@ quantize_stream_kernel(const __grid_constant__ CUtensorMap tmX, const QParams p)
                 }
                 QPH(0);
                 const uint32_t box = base + s * kBoxBytes;
+                // the block's share of U first (it reads the raw box), so the transformed values
+                // are not live across the tensor-core step
+                if constexpr (R > 0)
+                    if (!project) u_step<NT>(box, lane, kb, p.pfrag, upart, kb == warp);
+                QPH(2);
                 f2 P[16];
                 load_transform(box, r, half, p.inv_s ? s_invs + 256u * s : 0u, p.rotate, P);
-                QPH(1);
-                if constexpr (R > 0) {
+                if constexpr (R > 0)
                     if (project) project_block<R>(P, p, row, row_ok, kb, half);
-                    else u_step<NT>(box, lane, kb, p.pfrag, upart, kb == warp);
-                }
-                QPH(2);
+                QPH(1);
                 const uint32_t m0 = p.n_out ? ld_shared_u32(s_omega + 16u * kb) : 0u;
                 const uint32_t m1 = p.n_out ? ld_shared_u32(s_omega + 16u * kb + 4u) : 0u;
                 if ((m0 | m1) != 0u) {

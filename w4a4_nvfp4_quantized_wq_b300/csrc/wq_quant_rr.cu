@@ -115,28 +115,46 @@ __device__ __forceinline__ void u_pair(uint32_t slot, int lane, int nblocks, con
         if (bb < nblocks) {
             uint32_t a[4][4];
             u_frags(slot + static_cast<uint32_t>(bb) * kRBox, lane, a);
+            // n-tiles in groups of up to four: the group's P fragments, then its tensor-core
+            // chains issued interleaved (independent chains; each runs its four k-steps in order
+            // from zero, so the accumulation depth is 64 as in the other schedules), then one
+            // fp32 add per partial
+            constexpr int NG = NT < 4 ? NT : (NT > 4 ? 2 : 4);   // rank 64: pairs, for registers
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                uint4 q0, q1;
+            for (int n0 = 0; n0 < NT; n0 += NG) {
+                uint4 q[NG][2];
                 if (p.p_smem) {
-                    const uint32_t pb = pf_s + ((static_cast<uint32_t>(bb * NT + nt)) * 32u + static_cast<uint32_t>(lane)) * 32u;
-                    q0 = ld_shared_v4(pb);
-                    q1 = ld_shared_v4(pb + 16u);
-                } else {
-                    const uint4* pb = reinterpret_cast<const uint4*>(
-                        p.pfrag + (static_cast<size_t>((kb0 + bb) * NT + nt) * 32 + lane) * 8);
-                    q0 = __ldg(pb);
-                    q1 = __ldg(pb + 1);
-                }
-                // the block's 64 products from zero on the tensor cores, then one fp32 add: the
-                // tensor-core accumulation depth is 64 as in the other schedules
-                float t[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                mma_bf16_16816(t, a[0][0], a[0][1], a[0][2], a[0][3], q0.x, q0.y);
-                mma_bf16_16816(t, a[1][0], a[1][1], a[1][2], a[1][3], q0.z, q0.w);
-                mma_bf16_16816(t, a[2][0], a[2][1], a[2][2], a[2][3], q1.x, q1.y);
-                mma_bf16_16816(t, a[3][0], a[3][1], a[3][2], a[3][3], q1.z, q1.w);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) acc[nt][e] = __fadd_rn(acc[nt][e], t[e]);
+                    for (int g = 0; g < NG; ++g) {
+                        const uint32_t pb =
+                            pf_s + ((static_cast<uint32_t>(bb * NT + n0 + g)) * 32u + static_cast<uint32_t>(lane)) * 32u;
+                        q[g][0] = ld_shared_v4(pb);
+                        q[g][1] = ld_shared_v4(pb + 16u);
+                    }
+                } else {
+#pragma unroll
+                    for (int g = 0; g < NG; ++g) {
+                        const uint4* pb = reinterpret_cast<const uint4*>(
+                            p.pfrag + (static_cast<size_t>((kb0 + bb) * NT + n0 + g) * 32 + lane) * 8);
+                        q[g][0] = __ldg(pb);
+                        q[g][1] = __ldg(pb + 1);
+                    }
+                }
+                float t[NG][4];
+#pragma unroll
+                for (int g = 0; g < NG; ++g) t[g][0] = t[g][1] = t[g][2] = t[g][3] = 0.0f;
+#pragma unroll
+                for (int f = 0; f < 4; ++f)
+#pragma unroll
+                    for (int g = 0; g < NG; ++g) {
+                        const uint4& qq = q[g][f >> 1];
+                        mma_bf16_16816(t[g], a[f][0], a[f][1], a[f][2], a[f][3], (f & 1) ? qq.z : qq.x,
+                                       (f & 1) ? qq.w : qq.y);
+                    }
+#pragma unroll
+                for (int g = 0; g < NG; ++g)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) acc[n0 + g][e] = __fadd_rn(acc[n0 + g][e], t[g][e]);
             }
         }
     }
