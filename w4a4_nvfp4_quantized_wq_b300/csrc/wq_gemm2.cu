@@ -470,14 +470,22 @@ wide_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             if (lane == 0) mbar_arrive_cluster(tempty0);
             if (lane == 0) WT_ADD(10, te1);
             if (has_side) {
+                // alpha acc while the side MMAs run (the same RN(alpha acc) the combine below adds to)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    a0[i] = __float_as_uint(__fmul_rn(alpha, __uint_as_float(a0[i])));
+                    a1[i] = __float_as_uint(__fmul_rn(alpha, __uint_as_float(a1[i])));
+                    a2[i] = __float_as_uint(__fmul_rn(alpha, __uint_as_float(a2[i])));
+                    a3[i] = __float_as_uint(__fmul_rn(alpha, __uint_as_float(a3[i])));
+                }
                 WT_T0(te2);
                 if (!mbar_wait(bar_sfull, static_cast<uint32_t>(tl) & 1u, abort_flag, p.err, 42)) break;
                 if (lane == 0) WT_ADD(8, te2);
                 tc_fence_after();
             }
-            // before the accumulator goes back only the side results are folded in (v = alpha acc +
-            // side, chunk by chunk as they are read); column scales, bias and the bf16 stores follow
-            // after the release and overlap the next tile's main loop
+            // before the accumulator goes back only the side results are folded in (v = RN(alpha acc)
+            // + side, chunk by chunk as they are read); column scales, bias and the bf16 stores
+            // follow after the release and overlap the next tile's main loop
             WT_T0(te3);
             if (has_side) {
 #pragma unroll
@@ -488,7 +496,7 @@ wide_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
-                        acc[i] = __float_as_uint(__fadd_rn(__fmul_rn(alpha, __uint_as_float(acc[i])), __uint_as_float(sd[i])));
+                        acc[i] = __float_as_uint(__fadd_rn(__uint_as_float(acc[i]), __uint_as_float(sd[i])));
                 }
                 tc_fence_before();
                 __syncwarp();
