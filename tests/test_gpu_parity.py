@@ -673,6 +673,37 @@ def test_resident_quant_shapes(K, rank, n_omega, tuning):
     check_side(L, xo, u, aq)
 
 
+# Kept channels in the patterns the copy-out has to get right: half a block's channels (all in
+# the lower 32), a block with one channel at each end of both halves, the two blocks of one pair
+# both with kept channels (a warp of the resident schedule, a cluster CTA's neighbouring warps),
+# and most of the last block; 64 in all, sorted.
+KEPT_PATTERN = np.array(sorted(list(range(128, 160)) + [192 + 31, 192 + 32, 192 + 63] + [256, 256 + 33] +
+                               [320 + 5, 320 + 40, 320 + 62] + list(range(1472, 1496))), dtype=np.int32)
+
+
+@pytest.mark.parametrize("schedule", ["cluster", "stream", "resident"])
+def test_kept_channel_patterns(schedule, tuning):
+    """x_Omega, codes, scales and g bit-exact and U within its bound for a hand-placed Omega
+    (KEPT_PATTERN) on every quantiser schedule; 200 rows (a ragged last tile)."""
+    import dataclasses
+    tuning("WQ_QUANT_SCHEDULE", schedule)
+    L = wl.make_layer_inputs("video_dit", M=200, K=1536, N=128, rank=32, n_omega=64)
+    L = dataclasses.replace(L, omega=KEPT_PATTERN.copy())
+    assert KEPT_PATTERN.size == 64 and np.all(np.diff(KEPT_PATTERN) > 0)
+    w = prep(L)
+    want = {"cluster": wq.WQ_QUANT_CLUSTER, "stream": wq.WQ_QUANT_STREAM, "resident": wq.WQ_QUANT_RESIDENT}[schedule]
+    assert wq.wq_quant_schedule(w, L.M) == want
+    x = x_dev(L.x_bits)
+    codes, scales, g, xo, u = wq.wq_quantize_activations(w, x, wq.WQ_SCALE_LAYOUT_ROWMAJOR)
+    torch.cuda.synchronize()
+    wq.wq_check_device_error(w)
+    aq = oq(L)
+    assert np.array_equal(g.cpu().numpy(), aq.g)
+    assert np.array_equal(scales.cpu().numpy(), aq.scales)
+    assert np.array_equal(codes.cpu().numpy(), aq.codes)
+    check_side(L, xo, u, aq)
+
+
 @pytest.mark.parametrize("case", list(CASES))
 def test_forward_parity_resident_quantiser(case, tuning):
     """The whole forward with the register-resident quantiser feeding the GEMM (a case whose K is
