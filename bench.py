@@ -529,7 +529,8 @@ def run_wq(args):
                 byts = gemm8_algorithmic_bytes(M, spec.K, spec.N, L.bias is not None) if w8 else \
                     gemm_algorithmic_bytes(M, spec.K, spec.N, L.rank, L.omega.size, L.bias is not None)
                 flops = 2.0 * M * spec.K * spec.N
-                kern = ("wide_gemm_kernel" if wq.wq_gemm_schedule(w, M) == wq.WQ_GEMM_WIDE else "nvfp4_gemm_kernel")
+                kern = {wq.WQ_GEMM_WIDE: "wide_gemm_kernel", wq.WQ_GEMM_WIDE_DB: "wide_db_gemm_kernel"}.get(
+                    wq.wq_gemm_schedule(w, M), "nvfp4_gemm_kernel")
             else:
                 byts = quant8_algorithmic_bytes(M, spec.K, L.s is not None) if w8 else \
                     quant_algorithmic_bytes(M, spec.K, L.rank, L.omega.size, L.s is not None)

@@ -198,7 +198,9 @@ WQ_API int wq_quant_schedule(wq_weights_t h, int M);
 
 #define WQ_GEMM_SINGLE 0   /* 128 x 128 tiles, one persistent CTA per SM */
 #define WQ_GEMM_SPLITK 1   /* 128 x 128 tiles, K split over a thread-block cluster (few tiles) */
-#define WQ_GEMM_WIDE 2     /* 256 x 256 tiles on CTA pairs (4-bit layers with K >= 4096) */
+#define WQ_GEMM_WIDE 2     /* 256 x 256 tiles on CTA pairs, one accumulator (4-bit layers, many tiles) */
+#define WQ_GEMM_WIDE_DB 3  /* 256 x 192 tiles on CTA pairs, two accumulators (4-bit layers, many tiles,
+                              K <= 4096): the epilogue of one tile overlaps the next tile's MMAs */
 /*
  * Which GEMM schedule the two-kernel path (and wq_linear_forward_quantized) uses for M rows
  * under the current environment (host query; it may ask the CUDA runtime how many clusters
@@ -215,7 +217,8 @@ WQ_API int wq_gemm_schedule(wq_weights_t h, int M);
  *   "WQ_QUANT_SCHEDULE" -1 (auto), 0 (cluster), 1 (stream), 2 (register-resident where it applies,
  *   else stream);
  *   "WQ_QUANT_SPLIT" 0 (auto) or 1..16;
- *   "WQ_QUANT_CTAS_PER_SM" 0 (auto) or a count.
+ *   "WQ_QUANT_CTAS_PER_SM" 0 (auto) or a count;
+ *   "WQ_GEMM_DB" -1 (auto), 0, 1: the two-accumulator form of the pair schedule off / on.
  * Process-wide; takes effect for launches issued after it returns.  Returns WQ_ERR_INVALID for an
  * unknown name.  wq_get_tuning returns the current value (or WQ_ERR_INVALID's value for an unknown name).
  */

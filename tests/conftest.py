@@ -16,7 +16,7 @@ def pytest_configure(config):
 
 _KNOB_DEFAULTS = {"WQ_FUSED": 0, "WQ_GEMM_SPLIT": 0, "WQ_GEMM_WIDE": -1, "WQ_GEMM_PUSH": -1,
                   "WQ_GEMM_STAGES": 0, "WQ_QUANT_SCHEDULE": -1, "WQ_QUANT_SPLIT": 0,
-                  "WQ_QUANT_CTAS_PER_SM": 0}
+                  "WQ_QUANT_CTAS_PER_SM": 0, "WQ_GEMM_DB": -1}
 
 
 @pytest.fixture

@@ -123,6 +123,7 @@ def test_path_constants_match_the_header():
     txt = open(os.path.join(ROOT, "include", "wq.h")).read()
     defs = dict(re.findall(r"#define\s+(WQ_\w+)\s+(-?\d+)", txt))
     for name in ("WQ_PATH_TWO_KERNEL", "WQ_PATH_FUSED", "WQ_GEMM_SINGLE", "WQ_GEMM_SPLITK", "WQ_GEMM_WIDE",
+                 "WQ_GEMM_WIDE_DB",
                  "WQ_QUANT_CLUSTER", "WQ_QUANT_STREAM", "WQ_QUANT_RESIDENT"):
         assert int(defs[name]) == getattr(wq, name), name
 

@@ -248,17 +248,21 @@ def test_forward_parity_fused_and_two_kernel_paths(case, fused, tuning):
 
 
 @pytest.mark.parametrize("case", list(CASES))
-@pytest.mark.parametrize("wide", ["1", "0"])
+@pytest.mark.parametrize("wide", ["db", "1", "0"])
 def test_forward_parity_gemm_schedules(case, wide, tuning):
-    """Both GEMM schedules on every case: 256 x 256 tiles on CTA pairs (tcgen05 cta_group::2,
-    single-buffered accumulator, side branch computed into the drained accumulator) and
-    128 x 128 tiles on single CTAs; partial tiles in M and N included."""
-    tuning("WQ_GEMM_WIDE", wide)
+    """Every GEMM schedule on every case: 256 x 192 tiles on CTA pairs with two accumulators
+    ("db": the side branch of one tile computed while the next tile's main loop runs), 256 x 256
+    tiles on CTA pairs (tcgen05 cta_group::2, single-buffered accumulator, side branch computed
+    into the drained accumulator) and 128 x 128 tiles on single CTAs; partial tiles in M and N
+    included."""
+    tuning("WQ_GEMM_WIDE", "0" if wide == "0" else "1")
+    tuning("WQ_GEMM_DB", "1" if wide == "db" else "0")
     tuning("WQ_FUSED", "0")              # small batches too run the GEMM under test
     L = layer(case)
     w = prep(L)
     sched = wq.wq_gemm_schedule(w, L.M)
-    assert (sched == wq.WQ_GEMM_WIDE) == (wide == "1")
+    assert sched == {"db": wq.WQ_GEMM_WIDE_DB, "1": wq.WQ_GEMM_WIDE}.get(wide, sched)
+    assert (sched in (wq.WQ_GEMM_WIDE, wq.WQ_GEMM_WIDE_DB)) == (wide != "0")
     y = wq.wq_linear_forward(w, x_dev(L.x_bits))
     wq.wq_check_device_error(w)
     ref = oracle.reference_forward(L)
@@ -489,7 +493,7 @@ def test_full_size_long_k_both_gemm_schedules(wide, tuning):
     tuning("WQ_GEMM_WIDE", wide)
     L = wl.make_layer_inputs("video_dit", layer=3)
     w = prep(L)
-    assert (wq.wq_gemm_schedule(w, L.M) == wq.WQ_GEMM_WIDE) == (wide == "1")
+    assert (wq.wq_gemm_schedule(w, L.M) == wq.WQ_GEMM_WIDE) == (wide == "1")   # K = 8960: one accumulator
     y = wq.wq_linear_forward(w, x_dev(L.x_bits))
     wq.wq_check_device_error(w)
     rows = _tile_rows(L.M, 300)

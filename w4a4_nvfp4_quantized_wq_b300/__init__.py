@@ -21,7 +21,7 @@ WQ_OK, WQ_ERR_INVALID, WQ_ERR_UNSUPPORTED, WQ_ERR_CUDA, WQ_ERR_OOM, WQ_ERR_TIMEO
 WQ_MODE_W4A4, WQ_MODE_W8A8, WQ_MODE_W8A8_FP8, WQ_MODE_W4A8 = 0, 1, 2, 3
 WQ_SCALE_LAYOUT_ROWMAJOR, WQ_SCALE_LAYOUT_MMA = 0, 1
 WQ_PATH_TWO_KERNEL, WQ_PATH_FUSED = 0, 1
-WQ_GEMM_SINGLE, WQ_GEMM_SPLITK, WQ_GEMM_WIDE = 0, 1, 2
+WQ_GEMM_SINGLE, WQ_GEMM_SPLITK, WQ_GEMM_WIDE, WQ_GEMM_WIDE_DB = 0, 1, 2, 3
 WQ_QUANT_CLUSTER, WQ_QUANT_STREAM, WQ_QUANT_RESIDENT = 0, 1, 2
 WQ_ACT_SCALE_ROW, WQ_ACT_SCALE_TENSOR, WQ_ACT_SCALE_STATIC = 0, 1, 2
 WQ_ORDER_SMOOTH_ROTATE, WQ_ORDER_ROTATE_SMOOTH = 0, 1
@@ -359,7 +359,7 @@ def wq_forward_path(w: Weights, M: int) -> int:
 
 
 def wq_gemm_schedule(w: Weights, M: int) -> int:
-    """WQ_GEMM_SINGLE, WQ_GEMM_SPLITK or WQ_GEMM_WIDE: the GEMM schedule for M rows."""
+    """WQ_GEMM_SINGLE, WQ_GEMM_SPLITK, WQ_GEMM_WIDE or WQ_GEMM_WIDE_DB: the GEMM schedule for M rows."""
     r = lib().wq_gemm_schedule(ctypes.c_void_p(w.handle), M)
     if r < 0:
         _check(r)

@@ -128,6 +128,7 @@ struct KnobDef {
 constexpr KnobDef kKnobs[kTuneCount] = {
     {"WQ_FUSED", 0},          {"WQ_GEMM_SPLIT", 0},     {"WQ_GEMM_WIDE", -1},        {"WQ_GEMM_PUSH", -1},
     {"WQ_GEMM_STAGES", 0},    {"WQ_QUANT_SCHEDULE", -1}, {"WQ_QUANT_SPLIT", 0},      {"WQ_QUANT_CTAS_PER_SM", 0},
+    {"WQ_GEMM_DB", -1},
 };
 std::once_flag g_knob_once;
 }  // namespace
@@ -180,10 +181,15 @@ bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* bas
 }
 
 bool encode_scale_tmap(CUtensorMap* map, const void* base, int rows, int K, int box_row_blocks, const char** why) {
+    return encode_scale_tmap_blocks(map, base, (rows + kBlockM - 1) / kBlockM, K, box_row_blocks, why);
+}
+
+bool encode_scale_tmap_blocks(CUtensorMap* map, const void* base, int row_blocks, int K, int box_row_blocks,
+                              const char** why) {
     EncodeTiledFn fn = get_encode_fn();
     if (!fn) { *why = "cuTensorMapEncodeTiled unavailable"; return false; }
     const uint64_t nkb = static_cast<uint64_t>(K / 64);
-    const cuuint64_t dims[3] = {kSfAtom / 4, nkb, static_cast<cuuint64_t>((rows + kBlockM - 1) / kBlockM)};
+    const cuuint64_t dims[3] = {kSfAtom / 4, nkb, static_cast<cuuint64_t>(row_blocks)};
     const cuuint64_t strides[2] = {kSfAtom, nkb * kSfAtom};
     const cuuint32_t box[3] = {kSfAtom / 4, 4, static_cast<cuuint32_t>(box_row_blocks)};
     const cuuint32_t estr[3] = {1, 1, 1};
@@ -246,6 +252,10 @@ struct wq_weights {
     CUtensorMap tmBconv{};         // weight codes with 64-byte boxes (Conv3d, fused small-batch path)
     CUtensorMap tmB{}, tmQ{}, tmWO{};
     CUtensorMap tmSFB{};           // weight scales in 4-K-block x 2-row-block boxes (CTA-pair GEMM)
+    // two-accumulator pair GEMM (256 x 192 tiles): 96-row boxes of the weight codes, Q^T and W_O^T,
+    // and the weight scales in 192-row tile layout (two atoms per tile and K block)
+    uint8_t* d_sf192 = nullptr;
+    CUtensorMap tmB96{}, tmQ96{}, tmWO96{}, tmSFB192{};
     // activation / output tensor maps, re-encoded when the buffers change
     std::mutex mu;
     const void* key_codes = nullptr;
@@ -254,7 +264,7 @@ struct wq_weights {
     const void* key_y = nullptr;
     const void* key_sf = nullptr;
     int key_M = -1;
-    CUtensorMap tmA{}, tmU{}, tmXO{}, tmY{}, tmSFA{};
+    CUtensorMap tmA{}, tmU{}, tmXO{}, tmY{}, tmSFA{}, tmY32{};
     std::mutex mu_x;
     const void* key_x = nullptr;
     int key_xM = -1;
@@ -308,6 +318,7 @@ wq_status check_config(const wq_config* c) {
 void free_device(wq_weights* h) {
     cudaFree(h->d_codes);
     cudaFree(h->d_sf);
+    cudaFree(h->d_sf192);
     cudaFree(h->d_bias);
     cudaFree(h->d_inv_s);
     cudaFree(h->d_inv_s_rr);
@@ -579,6 +590,20 @@ WQ_API wq_status wq_prepare_weights(const wq_config* cfg, const float* W, const 
     if (bias) std::copy(bias, bias + N, bias_f.begin());
     if ((st = upload(&h->d_codes, codes.data(), codes.size(), cs)) != WQ_OK) return bail(st);
     if ((st = upload(&h->d_sf, sf_mma.data(), sf_mma.size(), cs)) != WQ_OK) return bail(st);
+    // the same scales in 192-row tile layout: tile t's rows 0..127 in atom block 2 t, rows 128..191
+    // in the first half of atom block 2 t + 1 (the rest zero)
+    const size_t nt192 = (static_cast<size_t>(N) + 191) / 192, nkb = static_cast<size_t>(K / 64);
+    std::vector<uint8_t> sf192(nt192 * 2 * nkb * wq::kSfAtom, 0);
+    for (size_t n = 0; n < static_cast<size_t>(N); ++n) {
+        const size_t t = n / 192, m = (n % 192) % 128, z = 2 * t + (n % 192) / 128;
+        for (size_t kb = 0; kb < nkb; ++kb)
+            for (size_t j = 0; j < 4; ++j) {
+                const size_t src = ((n / wq::kBlockM) * nkb + kb) * wq::kSfAtom + (n % 32) * 16 + ((n % wq::kBlockM) / 32) * 4 + j;
+                const size_t dst = (z * nkb + kb) * wq::kSfAtom + (m % 32) * 16 + (m / 32) * 4 + j;
+                sf192[dst] = sf_mma[src];
+            }
+    }
+    if ((st = upload(&h->d_sf192, sf192.data(), sf192.size(), cs)) != WQ_OK) return bail(st);
     if (bias && (st = upload(&h->d_bias, bias_f.data(), N * 4, cs)) != WQ_OK) return bail(st);
     if (s && (st = upload(&h->d_inv_s, inv_s_pairs.data(), K * 4, cs)) != WQ_OK) return bail(st);
     std::vector<float> inv_s_rr(s ? K : 0);
@@ -600,14 +625,21 @@ WQ_API wq_status wq_prepare_weights(const wq_config* cfg, const float* W, const 
     if (!wq::encode_tmap_2d(&h->tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, h->d_codes, K / 2, N, K / 2, 128, 128,
                             CU_TENSOR_MAP_SWIZZLE_128B, &why) ||
         !wq::encode_scale_tmap(&h->tmSFB, h->d_sf, N, K, 2, &why) ||
+        !wq::encode_tmap_2d(&h->tmB96, CU_TENSOR_MAP_DATA_TYPE_UINT8, h->d_codes, K / 2, N, K / 2, 128, 96,
+                            CU_TENSOR_MAP_SWIZZLE_128B, &why) ||
+        !wq::encode_scale_tmap_blocks(&h->tmSFB192, h->d_sf192, static_cast<int>(2 * nt192), K, 2, &why) ||
         !wq::encode_tmap_2d(&h->tmBconv, CU_TENSOR_MAP_DATA_TYPE_UINT8, h->d_codes, K / 2, N, K / 2, 64, 128,
                             CU_TENSOR_MAP_SWIZZLE_64B, &why))
         return bail(fail(WQ_ERR_CUDA, why));
-    if (r && !wq::encode_tmap_2d(&h->tmQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h->d_Qt, rp, N, 2 * rp, rp, 128,
-                                 swizzle_for_row_bytes(2 * rp), &why))
+    if (r && (!wq::encode_tmap_2d(&h->tmQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h->d_Qt, rp, N, 2 * rp, rp, 128,
+                                  swizzle_for_row_bytes(2 * rp), &why) ||
+              !wq::encode_tmap_2d(&h->tmQ96, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h->d_Qt, rp, N, 2 * rp, rp, 96,
+                                  swizzle_for_row_bytes(2 * rp), &why)))
         return bail(fail(WQ_ERR_CUDA, why));
-    if (no && !wq::encode_tmap_2d(&h->tmWO, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, h->d_WOt, nop, N, 2 * nop, nop, 128,
-                                  swizzle_for_row_bytes(2 * nop), &why))
+    if (no && (!wq::encode_tmap_2d(&h->tmWO, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, h->d_WOt, nop, N, 2 * nop, nop, 128,
+                                   swizzle_for_row_bytes(2 * nop), &why) ||
+               !wq::encode_tmap_2d(&h->tmWO96, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, h->d_WOt, nop, N, 2 * nop, nop, 96,
+                                   swizzle_for_row_bytes(2 * nop), &why)))
         return bail(fail(WQ_ERR_CUDA, why));
     if (cfg->mode == WQ_MODE_W4A8) {
         // A8 steps multiply the NVFP4 weights on the 16-bit tensor path: each value dec(code) dec(scale)
@@ -816,7 +848,10 @@ static wq_status run_gemm(wq_weights_t h, const uint8_t* codes, const uint8_t* s
                                                 CU_TENSOR_MAP_SWIZZLE_128B, &why)) &&
                   wq::encode_tmap_2d(&h->tmY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, y, N, M, 2ull * N, 64, 32,
                                      CU_TENSOR_MAP_SWIZZLE_128B, &why);
-        if (ok && !w8 && !f8) ok = wq::encode_scale_tmap(&h->tmSFA, sf, M, K, 1, &why);
+        if (ok && !w8 && !f8)
+            ok = wq::encode_scale_tmap(&h->tmSFA, sf, M, K, 1, &why) &&
+                 wq::encode_tmap_2d(&h->tmY32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, y, N, M, 2ull * N, 32, 32,
+                                    CU_TENSOR_MAP_SWIZZLE_NONE, &why);
         if (ok && r)
             ok = wq::encode_tmap_2d(&h->tmU, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, u, r, M, 2 * r, r, 128,
                                     swizzle_for_row_bytes(2 * r), &why);
@@ -840,6 +875,8 @@ static wq_status run_gemm(wq_weights_t h, const uint8_t* codes, const uint8_t* s
     ga.tmA = &h->tmA; ga.tmB = &h->tmB; ga.tmU = &h->tmU; ga.tmQ = &h->tmQ;
     ga.tmXO = &h->tmXO; ga.tmWO = &h->tmWO; ga.tmY = &h->tmY;
     ga.tmSFA = &h->tmSFA; ga.tmSFB = &h->tmSFB;
+    ga.tmB96 = &h->tmB96; ga.tmQ96 = &h->tmQ96; ga.tmWO96 = &h->tmWO96; ga.tmSFB192 = &h->tmSFB192;
+    ga.tmY32 = &h->tmY32;
     ga.sfa = sf; ga.sfb = h->d_sf; ga.gA = g; ga.gW = h->gW; ga.bias = h->d_bias;
     ga.err = h->d_err; ga.num_sms = h->num_sms;
     ga.y = y;

@@ -719,8 +719,21 @@ bool use_wide(const GemmArgs& a) {
     return wide;
 }
 
+// Within the pair schedule, the two-accumulator form (256 x 192 tiles): 4-bit layers without a
+// fused next-layer quantiser, with K <= 4096 (where the per-tile drain and side branch of the
+// single-buffered 256-column form are a large part of a tile) and at least 16 row tiles.
+// Measured on B300: M = 16384, K = 1536: 131 -> 107 us (N = 4608), 240 -> 197 us (N = 8960),
+// 55 -> 43 us (N = 1536); K = 8960 equal (172 us); M = 768, K = 2048, N = 32768 4% slower.
+// The WQ_GEMM_DB knob pins it.
+bool use_wide_db(const GemmArgs& a) {
+    if (a.w8 || a.chain != nullptr) return false;
+    const int f = tune(kTuneGemmDb);
+    if (f >= 0) return f == 1;
+    return a.K <= 4096 && a.M >= 4096;
+}
+
 int gemm_schedule(const GemmArgs& a) {
-    if (use_wide(a)) return 2;
+    if (use_wide(a)) return use_wide_db(a) ? 3 : 2;
     if (a.w8) {
         if (gemm_attributes<true>() != cudaSuccess) return -1;
         return gemm_split<true>(a, gemm_plan<true>(a)) > 1 ? 1 : 0;
@@ -738,7 +751,10 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
     // their own, so its MMA stream runs at the instruction rate; the accumulator is
     // single-buffered, so each tile pays the drain and the side branch before the next main
     // loop.  It is chosen for 4-bit layers with K >= 1024 whose 256 x 256 tiles fill every SM
-    // pair.  The WQ_GEMM_WIDE knob pins the choice (tests and tuning).
+    // pair.  The WQ_GEMM_WIDE knob pins the choice (tests and tuning).  Within the pair schedule the
+    // two-accumulator form (256 x 192 tiles, wq_gemm3.cu) takes the layers with K <= 4096: it
+    // costs a quarter of each MMA's columns but no MMA waits for an epilogue.
+    if (a.chain == nullptr && use_wide(a) && use_wide_db(a)) return launch_gemm_wide_db(a, st);
     if (a.chain != nullptr || use_wide(a)) return launch_gemm_wide(a, st);
     return a.w8 ? launch_gemm_t<true>(a, st) : launch_gemm_t<false>(a, st);
 }

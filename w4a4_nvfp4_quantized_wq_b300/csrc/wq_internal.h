@@ -44,6 +44,7 @@ enum TuneKnob {
     kTuneQuantSchedule,    // WQ_QUANT_SCHEDULE: 1 = stream, 0 = cluster (or "stream" / "cluster")
     kTuneQuantSplit,       // WQ_QUANT_SPLIT: CTAs per row tile of the cluster quantiser (0 = auto)
     kTuneQuantCtasPerSm,   // WQ_QUANT_CTAS_PER_SM: resident stream-quantiser CTAs per SM (0 = auto)
+    kTuneGemmDb,           // WQ_GEMM_DB: 1 / 0 pins the two-accumulator form of the pair GEMM on / off
     kTuneCount
 };
 int tune(TuneKnob k);
@@ -118,6 +119,14 @@ struct GemmArgs {
     // K block), boxes of 4 K blocks x 1 (activations) or 2 (weights) row blocks; CTA-pair schedule
     const CUtensorMap* tmSFA = nullptr;
     const CUtensorMap* tmSFB = nullptr;
+    // the two-accumulator pair schedule (256 x 192 tiles): this CTA's 96 rows of the weight codes,
+    // Q^T and W_O^T; the weight scales in 192-row tile layout (two atoms per tile and K block,
+    // rows 128..191 in the second); y in 32 x 32 boxes without swizzle
+    const CUtensorMap* tmB96 = nullptr;
+    const CUtensorMap* tmQ96 = nullptr;
+    const CUtensorMap* tmWO96 = nullptr;
+    const CUtensorMap* tmSFB192 = nullptr;
+    const CUtensorMap* tmY32 = nullptr;
     const uint8_t* sfa;       // activation scales, MMA layout
     const uint8_t* sfb;       // weight scales, MMA layout
     const float* gA;          // [M]
@@ -140,6 +149,9 @@ int gemm_schedule(const GemmArgs& a);
 // CTA-pair schedule (256 x 256 tiles) for batches with many output tiles (wq_gemm2.cu).
 cudaError_t launch_gemm_wide(const GemmArgs& a, cudaStream_t stream);
 int wide_gemm_tiles(int M, int N);
+// Two-accumulator CTA-pair schedule (256 x 192 tiles, wq_gemm3.cu): 4-bit layers, no chain.
+cudaError_t launch_gemm_wide_db(const GemmArgs& a, cudaStream_t stream);
+int wide_db_tiles(int M, int N);
 
 // The whole W4A4 forward of a small batch in one kernel (wq_fused.cu).
 struct FusedArgs {
@@ -195,5 +207,8 @@ bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* bas
 // The MMA-layout scales of `rows` rows and K columns as a 3-D map: [row blocks][K/64][128 u32],
 // boxes of 4 K blocks x box_row_blocks row blocks (out-of-range atoms read as zeros).
 bool encode_scale_tmap(CUtensorMap* map, const void* base, int rows, int K, int box_row_blocks, const char** why);
+// The same over an explicit number of 128-row atom blocks (the weights' 192-row tile layout).
+bool encode_scale_tmap_blocks(CUtensorMap* map, const void* base, int row_blocks, int K, int box_row_blocks,
+                              const char** why);
 
 }  // namespace wq
