@@ -140,6 +140,11 @@ def test_tuning_knobs_through_the_abi():
     finally:
         del os.environ["WQ_QUANT_SPLIT"]
     assert L.wq_set_tuning(b"WQ_QUANT_SPLIT", old) == wq.WQ_OK
+    old_db = L.wq_get_tuning(b"WQ_GEMM_DB")
+    if "WQ_GEMM_DB" not in os.environ:
+        assert old_db == -1                          # automatic unless the environment pins it
+    assert L.wq_set_tuning(b"WQ_GEMM_DB", 0) == wq.WQ_OK and L.wq_get_tuning(b"WQ_GEMM_DB") == 0
+    assert L.wq_set_tuning(b"WQ_GEMM_DB", old_db) == wq.WQ_OK
     assert L.wq_set_tuning(b"WQ_NOT_A_KNOB", 1) == wq.WQ_ERR_INVALID
     assert "unknown" in wq.wq_last_error()
     assert L.wq_get_tuning(b"WQ_NOT_A_KNOB") == wq.WQ_ERR_INVALID
